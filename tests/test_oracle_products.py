@@ -1,0 +1,179 @@
+"""Pins for the oracle's fixed-order GEMV, the MoE gather and the fp64 GEMM."""
+import numpy as np
+import pytest
+
+import oracle
+import synthetic as S
+from conftest import expand, golden
+
+
+def _bf16(vals):
+    return S.f32_to_bf16_bits(np.asarray(vals, dtype=np.float32))
+
+
+@pytest.mark.parametrize("case", golden("gemv_order.json")["cases"], ids=lambda c: c["name"])
+def test_gemv_golden_order(case):
+    K = case["K"]
+    N = case.get("N", 1)
+    w = np.zeros((N, K), np.uint16)
+    w[0] = _bf16(expand(case["w"], K))
+    x = _bf16([case["x"]] * K)
+    if "slices" in case:
+        assert oracle.gemv_slices(N, K) == case["slices"]
+    y32, _ = oracle.gemv(w, x, rows=[0])
+    assert y32[0] == np.float32(case["y"])
+
+
+def test_gemv_plans_golden():
+    for p in golden("gemv_order.json")["plans"]:
+        assert oracle.gemv_slices(p["N"], p["K"]) == p["S"], p
+
+
+def _tree32(a):
+    """The five butterfly steps written out as lane 0's expression tree."""
+    f = np.float32
+    def b16(u):
+        return f(a[u] + a[u ^ 16])
+    def b8(u):
+        return f(b16(u) + b16(u ^ 8))
+    def b4(u):
+        return f(b8(u) + b8(u ^ 4))
+    def b2(u):
+        return f(b4(u) + b4(u ^ 2))
+    return f(b2(0) + b2(1))
+
+
+@pytest.mark.parametrize("N,K", [(1, 1), (1, 15), (1, 16), (1, 17), (1, 100), (1, 511), (1, 512),
+                                 (1, 513), (1, 1000), (1, 2600), (1, 5000), (3000, 2600)])
+def test_gemv_brute_force_tree(N, K):
+    # bf16 * bf16 is exact in float32, so fmaf == float32(product) + acc rounded once.
+    g = np.random.default_rng(K)
+    w = _bf16(g.standard_normal(K) * 0.05).reshape(1, K)
+    x = _bf16(g.standard_normal(K))
+    wf, xf = S.bf16_bits_to_f32(w[0]), S.bf16_bits_to_f32(x)
+    J = -(-K // 512)
+    # plan: smallest power of two >= ceil(2432/N), capped at 8 and at J
+    want = -(-2432 // N)
+    Sl = 1
+    while Sl < want and Sl * 2 <= 8 and Sl * 2 <= J:
+        Sl *= 2
+    assert oracle.gemv_slices(N, K) == Sl
+    parts = []
+    for s in range(Sl):
+        lanes = np.zeros(32, np.float32)
+        for j in range(s * J // Sl, (s + 1) * J // Sl):
+            for u in range(32):
+                for k in range(512 * j + 16 * u, min(K, 512 * j + 16 * u + 16)):
+                    lanes[u] = np.float32(lanes[u] + np.float32(wf[k] * xf[k]))
+        parts.append(_tree32(lanes))
+    y = parts[0]
+    for p_ in parts[1:]:
+        y = np.float32(y + p_)
+    assert np.float32(oracle.gemv_one(w[0], N, x)) == y
+
+
+def test_gemv_one_hot_gives_column():
+    g = np.random.default_rng(3)
+    N, K = 40, 1300
+    w = _bf16(g.standard_normal((N, K)) * 0.02)
+    for j in (0, 17, 511, 512, 1299):
+        x = np.zeros(K, np.uint16)
+        x[j] = 0x3F80   # 1.0
+        y32, y16 = oracle.gemv(w, x)
+        assert np.array_equal(y32, S.bf16_bits_to_f32(w[:, j]))
+        assert np.array_equal(y16.view(np.int16) & 0x7FFF, w[:, j].view(np.int16) & 0x7FFF)
+
+
+def test_gemv_integer_data_is_exact():
+    g = np.random.default_rng(4)
+    N, K = 33, 3000
+    wi = g.integers(-8, 9, size=(N, K))
+    xi = g.integers(-8, 9, size=K)
+    y32, _ = oracle.gemv(_bf16(wi), _bf16(xi))
+    assert np.array_equal(y32.astype(np.int64), wi @ xi)
+
+
+def test_gemv_bf16_output_rounding():
+    # nearest-even rounding of the float32 result to bf16
+    assert oracle.f32_to_bf16(1.0) == 0x3F80
+    assert oracle.f32_to_bf16(float(np.float32(1.0 + 2.0 ** -8))) == 0x3F80          # tie -> even
+    assert oracle.f32_to_bf16(float(np.float32(1.0 + 3 * 2.0 ** -8))) == 0x3F82      # tie -> even (up)
+    assert oracle.f32_to_bf16(float(np.float32(1.0 + 2.0 ** -8 + 2.0 ** -20))) == 0x3F81
+    assert oracle.f32_to_bf16(float("inf")) == 0x7F80
+    assert oracle.f32_to_bf16(float("nan")) == 0x7FC0
+    assert oracle.f32_to_bf16(float(np.ldexp(2.0 - 2.0 ** -7, 127))) == 0x7F7F        # largest bf16
+    assert oracle.f32_to_bf16(float(np.ldexp(2.0 - 2.0 ** -8, 127))) == 0x7F80        # tie -> even = inf
+
+
+def test_gemv_rows_subset_matches_full_and_single():
+    w = S.weights(300, 2100, (61, 0, 0, 0), outliers=True)
+    x = S.activations(2100, (61, 999, 0))
+    full, _ = oracle.gemv(w, x)
+    rows = [0, 7, 150, 299]
+    sub, _ = oracle.gemv(w, x, rows=rows)
+    assert np.array_equal(full[rows], sub)
+    assert all(np.float32(oracle.gemv_one(w[r], 300, x)) == full[r] for r in rows)
+
+
+# ---------------------------------------------------------------------------
+# MoE expert gather
+# ---------------------------------------------------------------------------
+def test_moe_matches_per_expert_gemv_and_token_split():
+    E, Ne, K, T, topk = 16, 24, 700, 5, 4
+    W = S.weights(E * Ne, K, (71, 0, 0, 0))
+    X = S.activations(K, (71, 999, 0), count=T)
+    ids, p = S.routing(T, E, topk, (71, 777, 0, 0))
+    y, out32, out16 = oracle.moe_gemv(W, E, ids, p, X)
+    for t in range(T):
+        for j in range(topk):
+            e = ids[t, j]
+            ref, _ = oracle.gemv(W[e * Ne:(e + 1) * Ne], X[t])
+            assert np.array_equal(y[t, j], ref)
+        y1, o1, _ = oracle.moe_gemv(W, E, ids[t:t + 1], p[t:t + 1], X[t:t + 1])
+        assert np.array_equal(y1[0], y[t])
+        assert np.array_equal(o1[0], out32[t])
+
+
+def test_moe_combine_closed_forms():
+    E, Ne, K, T, topk = 8, 10, 64, 2, 3
+    W = S.weights(E * Ne, K, (72, 0, 0, 0))
+    X = S.activations(K, (72, 999, 0), count=T)
+    ids = np.array([[1, 4, 6], [0, 2, 7]], np.int32)
+    p_onehot = np.array([[1, 0, 0], [0, 0, 1]], np.float32)
+    y, out, _ = oracle.moe_gemv(W, E, ids, p_onehot, X)
+    assert np.array_equal(out[0], y[0, 0])
+    assert np.array_equal(out[1], y[1, 2])
+    p_half = np.array([[0.5, 0.25, 0.25], [0.5, 0.5, 0]], np.float32)
+    y, out, _ = oracle.moe_gemv(W, E, ids, p_half, X)
+    # ((0.5 a + 0.25 b) + 0.25 c), each step rounded once; scaling by 2^-k is exact
+    f = np.float32
+    a, b, c = y[0, 0], y[0, 1], y[0, 2]
+    assert np.array_equal(out[0], f(f(f(0.5) * a + f(0.25) * b) + f(0.25) * c))
+
+
+def test_moe_rejects_bad_ids():
+    W = S.weights(4 * 8, 32, (73, 0, 0, 0))
+    X = S.activations(32, (73, 999, 0), count=1)
+    with pytest.raises(ValueError):
+        oracle.moe_gemv(W, 4, np.array([[0, 4]], np.int32), None, X)
+
+
+# ---------------------------------------------------------------------------
+# prompt GEMM in fp64
+# ---------------------------------------------------------------------------
+def test_gemm_f64_matches_library_matmul():
+    X = S.activations(300, (81, 999, 0), count=7)
+    W = S.weights(50, 300, (81, 0, 0, 0), outliers=True)
+    Y = oracle.gemm_f64(X, W)
+    ref = S.bf16_bits_to_f32(X).astype(np.float64) @ S.bf16_bits_to_f32(W).astype(np.float64).T
+    assert np.allclose(Y, ref, rtol=1e-12, atol=1e-15)
+    cols = [3, 49, 0]
+    assert np.array_equal(oracle.gemm_f64(X, W, cols=cols), Y[:, cols])
+
+
+def test_gemm_f64_integer_exact():
+    g = np.random.default_rng(5)
+    Xi = g.integers(-20, 21, size=(5, 129))
+    Wi = g.integers(-20, 21, size=(9, 129))
+    Y = oracle.gemm_f64(_bf16(Xi), _bf16(Wi))
+    assert np.array_equal(Y, (Xi @ Wi.T).astype(np.float64))
