@@ -1,0 +1,330 @@
+"""decode_gemv_tensor_gb300 -- thin Python binding of libdgt (C ABI in include/dgt.h).
+
+Lossless BF16 exponent-rank weight compression decoded inside the matrix
+product, for one GB300 (sm_103a).  Every step runs in libdgt: the host packer
+and container in C++, the transcode, rebuild and product kernels in CUDA.
+This module only marshals arguments: numpy arrays for host data, torch tensors
+for device memory and streams.  It fails loudly when libdgt.so is missing.
+
+Names follow the C ABI: pack, unpack, write, read, upload, load_r4,
+r4_to_bf16, gemv, gemv_bf16, gemv_slices, read_status.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+import numpy as np
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libdgt.so")
+
+DGT_OK = 0
+STATUS = {0: "ok", -1: "invalid argument", -2: "unsupported shape", -3: "corrupt packed data",
+          -4: "CUDA error", -5: "device wait timed out", -6: "out of host memory", -7: "I/O error",
+          -8: "unsupported device or configuration"}
+
+
+class DgtError(RuntimeError):
+    def __init__(self, code, where):
+        super().__init__(f"{where}: {STATUS.get(code, 'unknown')} ({code})")
+        self.code = code
+
+
+class PackedView(C.Structure):
+    _fields_ = [
+        ("rows", C.c_uint64), ("cols", C.c_uint64), ("format", C.c_int32), ("rice_k", C.c_int32),
+        ("n_table", C.c_int32), ("reserved", C.c_int32), ("table", C.c_uint8 * 256),
+        ("n_esc15", C.c_uint64), ("sm", C.c_void_p), ("words", C.c_void_p), ("n_words", C.c_uint64),
+        ("blkq", C.c_void_p), ("n_blocks", C.c_uint64), ("grp", C.c_void_p), ("n_groups", C.c_uint64),
+        ("payload", C.c_void_p), ("payload_bytes", C.c_uint64), ("tw", C.c_void_p), ("tesc", C.c_void_p),
+        ("n_tiles", C.c_uint64), ("esc1", C.c_void_p), ("n_esc1", C.c_uint64), ("grp1", C.c_void_p),
+        ("n_groups1", C.c_uint64),
+    ]
+
+
+class R4Struct(C.Structure):
+    _fields_ = [
+        ("rows", C.c_uint64), ("cols", C.c_uint64), ("n_table", C.c_int32), ("reserved", C.c_int32),
+        ("table", C.c_uint8 * 256), ("n_esc", C.c_uint64), ("sm", C.c_void_p), ("nib", C.c_void_p),
+        ("esc", C.c_void_p), ("seg", C.c_void_p),
+    ]
+
+
+_lib = None
+
+
+def lib():
+    """The loaded libdgt (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"libdgt.so is not built ({LIB_PATH}); run "
+                              "`python -c 'import __graft_entry__ as g; g.build()'`")
+        L = C.CDLL(LIB_PATH)
+        vp, u64, i32 = C.c_void_p, C.c_uint64, C.c_int
+        sig = {
+            "dgt_status_string": (C.c_char_p, [i32]),
+            "dgt_version": (i32, []),
+            "dgt_pack": (i32, [vp, u64, u64, i32, i32, C.POINTER(vp)]),
+            "dgt_packed_free": (None, [vp]),
+            "dgt_packed_get_view": (i32, [vp, C.POINTER(PackedView)]),
+            "dgt_packed_bits_per_weight": (C.c_double, [vp]),
+            "dgt_unpack": (i32, [C.POINTER(PackedView), vp, i32]),
+            "dgt_write": (i32, [C.c_char_p, C.POINTER(vp), C.POINTER(C.c_char_p), i32]),
+            "dgt_read": (i32, [C.c_char_p, C.POINTER(C.POINTER(vp)), C.POINTER(C.POINTER(C.c_char_p)),
+                               C.POINTER(i32)]),
+            "dgt_read_free": (None, [C.POINTER(vp), C.POINTER(C.c_char_p), i32]),
+            "dgt_r4_nseg": (u64, [u64]),
+            "dgt_r4_sizes": (i32, [u64, u64, u64, C.POINTER(u64), C.POINTER(u64), C.POINTER(u64)]),
+            "dgt_r4_init_from_view": (i32, [C.POINTER(PackedView), vp, vp, vp, C.POINTER(R4Struct)]),
+            "dgt_load_r4": (i32, [C.POINTER(PackedView), C.POINTER(R4Struct), vp, vp]),
+            "dgt_r4_to_bf16": (i32, [C.POINTER(R4Struct), vp, vp, vp]),
+            "dgt_read_status": (i32, [vp, vp, C.POINTER(C.c_int32)]),
+            "dgt_gemv_slices": (i32, [u64, u64]),
+            "dgt_gemv": (i32, [C.POINTER(R4Struct), vp, vp, vp, vp]),
+            "dgt_gemv_bf16": (i32, [vp, u64, u64, vp, vp, vp, vp]),
+        }
+        for name, (res, args) in sig.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+def _check(rc, where):
+    if rc != DGT_OK:
+        raise DgtError(rc, where)
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream=None):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return C.c_void_p(s.cuda_stream)
+
+
+# ---------------------------------------------------------------------------
+# host: pack / unpack / container
+# ---------------------------------------------------------------------------
+class Packed:
+    """A library-owned packed tensor (host).  Arrays are numpy views into it."""
+
+    _ARRAYS2 = [("sm", "sm", np.uint8, "n"), ("words", "words", np.uint32, "n_words"),
+                ("blkq", "blkq", np.uint8, "n_blocks"), ("grp", "grp", np.uint32, "n_groups*2")]
+    _ARRAYS1 = [("sm", "sm", np.uint8, "n"), ("payload", "payload", np.uint8, "payload_bytes"),
+                ("tw", "tw", np.uint8, "n_tiles"), ("tesc", "tesc", np.uint8, "n_tiles"),
+                ("esc1", "esc1", np.uint8, "n_esc1"), ("grp1", "grp1", np.uint32, "n_groups1*3")]
+
+    def __init__(self, handle):
+        self._h = C.c_void_p(handle)
+        self.view = PackedView()
+        _check(lib().dgt_packed_get_view(self._h, C.byref(self.view)), "dgt_packed_get_view")
+
+    def __del__(self):
+        if getattr(self, "_h", None) and _lib is not None:
+            _lib.dgt_packed_free(self._h)
+            self._h = None
+
+    @property
+    def rows(self):
+        return self.view.rows
+
+    @property
+    def cols(self):
+        return self.view.cols
+
+    @property
+    def format(self):
+        return self.view.format
+
+    @property
+    def table(self):
+        return np.frombuffer(bytes(self.view.table), np.uint8)
+
+    def _count(self, spec):
+        v = self.view
+        if spec == "n":
+            return v.rows * v.cols
+        if "*" in spec:
+            f, m = spec.split("*")
+            return getattr(v, f) * int(m)
+        return getattr(v, spec)
+
+    def arrays(self):
+        """name -> numpy view (host memory owned by this object)."""
+        out = {}
+        for name, field, dt, spec in (self._ARRAYS2 if self.format == 2 else self._ARRAYS1):
+            cnt = int(self._count(spec))
+            p = getattr(self.view, field)
+            if cnt == 0 or not p:
+                out[name] = np.zeros(0, dt)
+            else:
+                buf = (C.c_uint8 * (cnt * np.dtype(dt).itemsize)).from_address(p)
+                out[name] = np.frombuffer(buf, dt, count=cnt)
+        return out
+
+    def bits_per_weight(self):
+        return float(lib().dgt_packed_bits_per_weight(self._h))
+
+
+def pack(w, format: int = 2, nthreads: int = 0) -> Packed:
+    """dgt_pack: a bf16 matrix given as uint16 bit patterns [rows, cols]."""
+    w = np.ascontiguousarray(w, dtype=np.uint16)
+    rows, cols = w.shape if w.ndim == 2 else (1, w.size)
+    h = C.c_void_p()
+    _check(lib().dgt_pack(w.ctypes.data if w.size else None, rows, cols, format, nthreads, C.byref(h)),
+           "dgt_pack")
+    return Packed(h.value)
+
+
+def unpack(p: Packed, nthreads: int = 0) -> np.ndarray:
+    """dgt_unpack on the host: the original bf16 bit patterns [rows, cols]."""
+    out = np.empty((p.rows, p.cols), np.uint16)
+    _check(lib().dgt_unpack(C.byref(p.view), out.ctypes.data if out.size else None, nthreads),
+           "dgt_unpack")
+    return out
+
+
+def write(path: str, tensors: dict) -> None:
+    """dgt_write: a safetensors container of packed tensors."""
+    names = list(tensors)
+    hs = (C.c_void_p * len(names))(*[tensors[n]._h.value for n in names])
+    ns = (C.c_char_p * len(names))(*[n.encode() for n in names])
+    _check(lib().dgt_write(path.encode(), hs, ns, len(names)), "dgt_write")
+
+
+def read(path: str) -> dict:
+    """dgt_read: name -> Packed."""
+    L = lib()
+    ts = C.POINTER(C.c_void_p)()
+    ns = C.POINTER(C.c_char_p)()
+    cnt = C.c_int()
+    _check(L.dgt_read(path.encode(), C.byref(ts), C.byref(ns), C.byref(cnt)), "dgt_read")
+    out = {}
+    for i in range(cnt.value):
+        out[ns[i].decode()] = Packed(ts[i])
+        ts[i] = None          # ownership moves to the Packed object
+    L.dgt_read_free(ts, ns, cnt.value)
+    return out
+
+
+def gemv_slices(rows: int, cols: int) -> int:
+    return int(lib().dgt_gemv_slices(rows, cols))
+
+
+def r4_nseg(cols: int) -> int:
+    return int(lib().dgt_r4_nseg(cols))
+
+
+# ---------------------------------------------------------------------------
+# device
+# ---------------------------------------------------------------------------
+class DevicePacked:
+    """The arrays of a packed tensor copied to device memory (torch uint8
+    tensors), and the view with their device addresses."""
+
+    def __init__(self, p: Packed, device="cuda", stream=None, pinned=False):
+        import torch
+        self.host = p
+        self.tensors = {}
+        for name, arr in p.arrays().items():
+            t = torch.from_numpy(arr.view(np.uint8).copy() if arr.size else np.zeros(16, np.uint8))
+            if pinned:
+                t = t.pin_memory()
+            self.tensors[name] = t.to(device, non_blocking=pinned)
+        self.view = PackedView.from_buffer_copy(p.view)
+        for name, t in self.tensors.items():
+            setattr(self.view, name if name != "words" else "words", t.data_ptr())
+        self.rows, self.cols = p.rows, p.cols
+
+
+def upload(p: Packed, device="cuda") -> DevicePacked:
+    return DevicePacked(p, device)
+
+
+class R4:
+    """R4 runtime tensor: torch device buffers (nib, esc, seg; sm aliases the
+    packed upload) and the dgt_r4 descriptor."""
+
+    def __init__(self, dev: DevicePacked):
+        import torch
+        v = dev.view
+        nb, eb, sb = C.c_uint64(), C.c_uint64(), C.c_uint64()
+        _check(lib().dgt_r4_sizes(v.rows, v.cols, v.n_esc15, C.byref(nb), C.byref(eb), C.byref(sb)),
+               "dgt_r4_sizes")
+        d = dev.tensors["sm"].device
+        self.nib = torch.empty(max(nb.value, 16), dtype=torch.uint8, device=d)
+        self.esc = torch.empty(max(eb.value, 16), dtype=torch.uint8, device=d)
+        self.seg = torch.empty(max(sb.value // 4, 4), dtype=torch.int32, device=d)
+        self.sm = dev.tensors["sm"]
+        self.dev = dev
+        self.s = R4Struct()
+        _check(lib().dgt_r4_init_from_view(C.byref(v), _ptr(self.nib), _ptr(self.esc), _ptr(self.seg),
+                                           C.byref(self.s)), "dgt_r4_init_from_view")
+        self.rows, self.cols = v.rows, v.cols
+        self.n_esc = v.n_esc15
+
+
+def load_r4(dev: DevicePacked, status=None, stream=None) -> R4:
+    """dgt_load_r4: transcode the uploaded format-1/2 tensor into R4 on the GPU."""
+    r4 = R4(dev)
+    _check(lib().dgt_load_r4(C.byref(dev.view), C.byref(r4.s), _ptr(status), _stream(stream)), "dgt_load_r4")
+    return r4
+
+
+def load_r4_into(dev: DevicePacked, r4: R4, status=None, stream=None) -> R4:
+    """dgt_load_r4 into existing R4 buffers (no allocation)."""
+    _check(lib().dgt_load_r4(C.byref(dev.view), C.byref(r4.s), _ptr(status), _stream(stream)), "dgt_load_r4")
+    return r4
+
+
+def share_sm(dst: DevicePacked, src: DevicePacked) -> None:
+    """Let dst use src's device copy of the sign/mantissa bytes (same tensor)."""
+    dst.tensors["sm"] = src.tensors["sm"]
+    dst.view.sm = src.tensors["sm"].data_ptr()
+
+
+def r4_to_bf16(r4: R4, out=None, status=None, stream=None):
+    """dgt_r4_to_bf16: rebuild the bf16 matrix on the GPU (torch.bfloat16 [rows, cols])."""
+    import torch
+    if out is None:
+        out = torch.empty((r4.rows, r4.cols), dtype=torch.bfloat16, device=r4.sm.device)
+    _check(lib().dgt_r4_to_bf16(C.byref(r4.s), _ptr(out), _ptr(status), _stream(stream)), "dgt_r4_to_bf16")
+    return out
+
+
+def read_status(status, stream=None) -> int:
+    v = C.c_int32()
+    _check(lib().dgt_read_status(_ptr(status), _stream(stream), C.byref(v)), "dgt_read_status")
+    return v.value
+
+
+def gemv(W: R4, x, y=None, y32=None, stream=None):
+    """dgt_gemv: y = W x with W in R4; x bf16 [cols] on the device.
+    Returns (y bf16 [rows], y32 float32 [rows])."""
+    import torch
+    dev = W.sm.device
+    if y is None:
+        y = torch.empty(W.rows, dtype=torch.bfloat16, device=dev)
+    if y32 is None:
+        y32 = torch.empty(W.rows, dtype=torch.float32, device=dev)
+    _check(lib().dgt_gemv(C.byref(W.s), _ptr(x), _ptr(y), _ptr(y32), _stream(stream)), "dgt_gemv")
+    return y, y32
+
+
+def gemv_bf16(W, x, y=None, y32=None, stream=None):
+    """dgt_gemv_bf16: the same product and order with bf16 weights [rows, cols]."""
+    import torch
+    rows, cols = W.shape
+    if y is None:
+        y = torch.empty(rows, dtype=torch.bfloat16, device=W.device)
+    if y32 is None:
+        y32 = torch.empty(rows, dtype=torch.float32, device=W.device)
+    _check(lib().dgt_gemv_bf16(_ptr(W), rows, cols, _ptr(x), _ptr(y), _ptr(y32), _stream(stream)),
+           "dgt_gemv_bf16")
+    return y, y32

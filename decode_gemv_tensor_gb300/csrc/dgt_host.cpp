@@ -1,0 +1,468 @@
+// dgt_host.cpp -- host side of libdgt: the packer (formats 1 and 2), host
+// unpack, the safetensors container, status strings and the GEMV plan.
+//
+// Method: Binade project README -- title paragraphs (sign+mantissa byte,
+// exponent frequency rank, Rice codes), "How it works" (one table per tensor,
+// the two file formats, R4 at load) and "Use" (pack / unpack).  The per-block
+// 8-bit index follows the "Best measured configuration" section of the
+// "Lossless BF16 weight compression" README (BLOCK=64, 8-bit lengths).
+//
+// Everything here is multithreaded over independent groups / tiles with
+// std::thread; results do not depend on the thread count.
+#include <algorithm>
+#include <atomic>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+#include <string>
+#include <thread>
+#include <vector>
+
+#include "../../include/dgt.h"
+#include "dgt_internal.h"
+#include "dgt_packed.h"
+
+namespace {
+
+int resolve_threads(int nthreads) {
+    if (nthreads > 0) return nthreads;
+    unsigned h = std::thread::hardware_concurrency();
+    return h ? (int)h : 1;
+}
+
+// Run fn(begin, end) over [0, count) split into contiguous pieces.
+template <class F>
+void parallel_for(int nthreads, uint64_t count, F fn) {
+    if (count == 0) return;
+    uint64_t nt = std::min<uint64_t>((uint64_t)nthreads, count);
+    if (nt <= 1 || count < 4) {
+        fn((uint64_t)0, count);
+        return;
+    }
+    std::vector<std::thread> th;
+    th.reserve(nt);
+    for (uint64_t t = 0; t < nt; t++) {
+        uint64_t b = count * t / nt, e = count * (t + 1) / nt;
+        th.emplace_back([=] { fn(b, e); });
+    }
+    for (auto &x : th) x.join();
+}
+
+// LSB-first bit writer into a word range that starts zeroed.
+struct BitWriter {
+    uint32_t *w;
+    uint64_t acc = 0;
+    int fill = 0;
+    explicit BitWriter(uint32_t *dst) : w(dst) {}
+    void put(uint64_t bits, int len) {  // len <= 32
+        acc |= bits << fill;
+        fill += len;
+        if (fill >= 32) {
+            *w++ = (uint32_t)acc;
+            acc >>= 32;
+            fill -= 32;
+        }
+    }
+    void zeros(int len) {
+        while (len > 32) { put(0, 32); len -= 32; }
+        put(0, len);
+    }
+    void flush() {
+        if (fill > 0) { *w++ = (uint32_t)acc; acc = 0; fill = 0; }
+    }
+};
+
+struct BitReader {
+    const uint32_t *w;
+    uint64_t pos, limit;
+    bool bad = false;
+    int bit() {
+        if (pos >= limit) { bad = true; return 1; }
+        int b = (int)((w[pos >> 5] >> (pos & 31)) & 1u);
+        pos++;
+        return b;
+    }
+    uint32_t bits(int len) {
+        uint32_t v = 0;
+        for (int i = 0; i < len; i++) v |= (uint32_t)bit() << i;
+        return v;
+    }
+};
+
+inline uint8_t sm_of(uint16_t b) { return (uint8_t)(((b >> 8) & 0x80) | (b & 0x7F)); }
+inline uint8_t exp_of(uint16_t b) { return (uint8_t)((b >> 7) & 0xFF); }
+inline uint16_t bf16_of(uint8_t sm, uint8_t e) {
+    return (uint16_t)(((uint16_t)(sm & 0x80) << 8) | ((uint16_t)e << 7) | (sm & 0x7F));
+}
+
+int pack_format2(dgt_packed *p, const std::vector<uint8_t> &rk, int nt) {
+    const uint64_t n = p->v.rows * p->v.cols;
+    const uint64_t nblk = (n + DGT_BLOCK - 1) / DGT_BLOCK;
+    const uint64_t ngrp = (nblk + DGT_GROUP - 1) / DGT_GROUP;
+    // per group: bits for each k, and the number of ranks >= 15
+    std::vector<uint64_t> gbits(ngrp * 8);
+    std::vector<uint32_t> gesc(ngrp);
+    parallel_for(nt, ngrp, [&](uint64_t g0, uint64_t g1) {
+        for (uint64_t g = g0; g < g1; g++) {
+            uint64_t bits[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+            uint32_t e15 = 0;
+            uint64_t b_end = std::min(nblk, (g + 1) * DGT_GROUP);
+            for (uint64_t b = g * DGT_GROUP; b < b_end; b++) {
+                uint64_t i0 = b * DGT_BLOCK, cnt = std::min<uint64_t>(DGT_BLOCK, n - i0);
+                uint32_t q[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+                for (uint64_t i = 0; i < cnt; i++) {
+                    uint32_t r = rk[i0 + i];
+                    e15 += r >= 15;
+                    for (int k = 0; k < 8; k++) q[k] += r >> k;
+                }
+                for (int k = 0; k < 8; k++)
+                    bits[k] += q[k] <= 254 ? cnt * (uint64_t)(k + 1) + q[k] : 8 * cnt;
+            }
+            for (int k = 0; k < 8; k++) gbits[g * 8 + k] = bits[k];
+            gesc[g] = e15;
+        }
+    });
+    int best_k = 0;
+    uint64_t best_words = UINT64_MAX;
+    for (int k = 0; k < 8; k++) {
+        uint64_t words = 0;
+        for (uint64_t g = 0; g < ngrp; g++) words += (gbits[g * 8 + k] + 31) / 32;
+        if (words < best_words) { best_words = words; best_k = k; }
+    }
+    if (ngrp == 0) best_words = 0;
+    if (best_words >= (1ull << 32)) return DGT_ERR_SHAPE;
+    const int k = best_k;
+    p->v.rice_k = k;
+    p->words.assign(best_words, 0u);
+    p->blkq.assign(nblk, 0);
+    p->grp.assign(ngrp * 2, 0u);
+    uint64_t off = 0, esc = 0;
+    for (uint64_t g = 0; g < ngrp; g++) {
+        p->grp[2 * g] = (uint32_t)off;
+        p->grp[2 * g + 1] = (uint32_t)esc;
+        off += (gbits[g * 8 + k] + 31) / 32;
+        esc += gesc[g];
+    }
+    parallel_for(nt, ngrp, [&](uint64_t g0, uint64_t g1) {
+        for (uint64_t g = g0; g < g1; g++) {
+            BitWriter bw(p->words.data() + p->grp[2 * g]);
+            uint64_t b_end = std::min(nblk, (g + 1) * DGT_GROUP);
+            for (uint64_t b = g * DGT_GROUP; b < b_end; b++) {
+                uint64_t i0 = b * DGT_BLOCK, cnt = std::min<uint64_t>(DGT_BLOCK, n - i0);
+                uint32_t q = 0;
+                for (uint64_t i = 0; i < cnt; i++) q += (uint32_t)rk[i0 + i] >> k;
+                if (q <= 254) {
+                    p->blkq[b] = (uint8_t)q;
+                    for (uint64_t i = 0; i < cnt; i++) {
+                        uint32_t r = rk[i0 + i];
+                        uint32_t quo = r >> k;
+                        bw.zeros((int)quo);
+                        bw.put(1u | ((uint64_t)(r & ((1u << k) - 1u)) << 1), k + 1);
+                    }
+                } else {
+                    p->blkq[b] = 255;
+                    for (uint64_t i = 0; i < cnt; i++) bw.put(rk[i0 + i], 8);
+                }
+            }
+            bw.flush();
+        }
+    });
+    return DGT_OK;
+}
+
+inline int tile_width(const uint8_t *r, uint64_t cnt) {
+    uint32_t hist[256];
+    std::memset(hist, 0, sizeof(hist));
+    bool nz = false;
+    for (uint64_t i = 0; i < cnt; i++) { hist[r[i]]++; nz |= r[i] != 0; }
+    if (!nz) return 0;
+    // ranks >= t for every threshold t, from the histogram
+    uint32_t ge[257];
+    ge[256] = 0;
+    for (int t = 255; t >= 0; t--) ge[t] = ge[t + 1] + hist[t];
+    int best = 1;
+    uint64_t best_cost = UINT64_MAX;
+    for (int w = 1; w <= 8; w++) {
+        uint64_t cost = (uint64_t)DGT_TILE * w + 8ull * ge[(1 << w) - 1];
+        if (cost < best_cost) { best_cost = cost; best = w; }
+    }
+    return best;
+}
+
+int pack_format1(dgt_packed *p, const std::vector<uint8_t> &rk, int nt) {
+    const uint64_t n = p->v.rows * p->v.cols;
+    const uint64_t ntile = (n + DGT_TILE - 1) / DGT_TILE;
+    const uint64_t ngrp = (ntile + DGT_GROUP - 1) / DGT_GROUP;
+    p->tw.assign(ntile, 0);
+    p->tesc.assign(ntile, 0);
+    std::vector<uint8_t> te15(ntile);
+    parallel_for(nt, ntile, [&](uint64_t t0, uint64_t t1) {
+        for (uint64_t t = t0; t < t1; t++) {
+            uint64_t i0 = t * DGT_TILE, cnt = std::min<uint64_t>(DGT_TILE, n - i0);
+            int w = tile_width(&rk[i0], cnt);
+            uint32_t top = w ? (1u << w) - 1u : 0u;
+            uint32_t e = 0, e15 = 0;
+            for (uint64_t i = 0; i < cnt; i++) {
+                e += w && rk[i0 + i] >= top;
+                e15 += rk[i0 + i] >= 15;
+            }
+            p->tw[t] = (uint8_t)w;
+            p->tesc[t] = (uint8_t)e;
+            te15[t] = (uint8_t)e15;
+        }
+    });
+    std::vector<uint64_t> poff(ntile + 1), eoff(ntile + 1);
+    uint64_t e15 = 0;
+    p->grp1.assign(ngrp * 3, 0u);
+    poff[0] = eoff[0] = 0;
+    for (uint64_t t = 0; t < ntile; t++) {
+        if (t % DGT_GROUP == 0) {
+            uint64_t g = t / DGT_GROUP;
+            if (poff[t] / 16 >= (1ull << 32) || eoff[t] >= (1ull << 32)) return DGT_ERR_SHAPE;
+            p->grp1[3 * g] = (uint32_t)(poff[t] / 16);
+            p->grp1[3 * g + 1] = (uint32_t)eoff[t];
+            p->grp1[3 * g + 2] = (uint32_t)e15;
+        }
+        poff[t + 1] = poff[t] + 16ull * p->tw[t];
+        eoff[t + 1] = eoff[t] + p->tesc[t];
+        e15 += te15[t];
+    }
+    p->payload.assign(poff[ntile], 0);
+    p->esc1.assign(eoff[ntile], 0);
+    parallel_for(nt, ntile, [&](uint64_t t0, uint64_t t1) {
+        for (uint64_t t = t0; t < t1; t++) {
+            int w = p->tw[t];
+            if (!w) continue;
+            uint64_t i0 = t * DGT_TILE, cnt = std::min<uint64_t>(DGT_TILE, n - i0);
+            uint32_t top = (1u << w) - 1u;
+            uint8_t *dst = p->payload.data() + poff[t];
+            uint8_t *ed = p->esc1.data() + eoff[t];
+            uint64_t acc = 0;
+            int fill = 0;
+            for (uint64_t i = 0; i < DGT_TILE; i++) {
+                uint32_t r = i < cnt ? rk[i0 + i] : 0u;
+                uint32_t c = r < top ? r : top;
+                if (i < cnt && c == top) *ed++ = (uint8_t)r;
+                acc |= (uint64_t)c << fill;
+                fill += w;
+                while (fill >= 8) { *dst++ = (uint8_t)acc; acc >>= 8; fill -= 8; }
+            }
+        }
+    });
+    return DGT_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *dgt_status_string(int status) {
+    switch (status) {
+        case DGT_OK: return "ok";
+        case DGT_ERR_ARG: return "invalid argument";
+        case DGT_ERR_SHAPE: return "unsupported shape";
+        case DGT_ERR_CORRUPT: return "corrupt packed data";
+        case DGT_ERR_CUDA: return "CUDA error";
+        case DGT_ERR_TIMEOUT: return "device wait timed out";
+        case DGT_ERR_OOM: return "out of host memory";
+        case DGT_ERR_IO: return "I/O error";
+        case DGT_ERR_UNSUPPORTED: return "unsupported device or configuration";
+        default: return "unknown status";
+    }
+}
+
+int dgt_version(void) { return 100; }
+
+int dgt_pack(const uint16_t *bf16, uint64_t rows, uint64_t cols, int format, int nthreads,
+             dgt_packed **out) {
+    if (!out || (format != 1 && format != 2)) return DGT_ERR_ARG;
+    *out = nullptr;
+    const uint64_t n = rows * cols;
+    if ((rows && n / rows != cols) || n >= (1ull << 40)) return DGT_ERR_SHAPE;
+    if (n && !bf16) return DGT_ERR_ARG;
+    const int nt = resolve_threads(nthreads);
+    dgt_packed *p = new (std::nothrow) dgt_packed();
+    if (!p) return DGT_ERR_OOM;
+    try {
+        std::memset(&p->v, 0, sizeof(p->v));
+        p->v.rows = rows;
+        p->v.cols = cols;
+        p->v.format = format;
+        // exponent histogram
+        const uint64_t chunks = std::min<uint64_t>((uint64_t)nt * 4, std::max<uint64_t>(1, n / 65536));
+        std::vector<uint64_t> part(chunks * 256, 0);
+        parallel_for(nt, chunks, [&](uint64_t c0, uint64_t c1) {
+            for (uint64_t c = c0; c < c1; c++) {
+                uint64_t *h = &part[c * 256];
+                for (uint64_t i = n * c / chunks; i < n * (c + 1) / chunks; i++) h[exp_of(bf16[i])]++;
+            }
+        });
+        uint64_t counts[256] = {0};
+        for (uint64_t c = 0; c < chunks; c++)
+            for (int e = 0; e < 256; e++) counts[e] += part[c * 256 + e];
+        // rank table: count descending, exponent ascending
+        int order[256], T = 0;
+        for (int e = 0; e < 256; e++)
+            if (counts[e]) order[T++] = e;
+        std::stable_sort(order, order + T, [&](int a, int b) { return counts[a] > counts[b]; });
+        uint8_t rank_of[256];
+        std::memset(rank_of, 0, sizeof(rank_of));
+        for (int r = 0; r < T; r++) {
+            p->v.table[r] = (uint8_t)order[r];
+            rank_of[order[r]] = (uint8_t)r;
+        }
+        p->v.n_table = T;
+        uint64_t e15 = 0;
+        for (int r = 15; r < T; r++) e15 += counts[order[r]];
+        p->v.n_esc15 = e15;
+        // sign/mantissa bytes and ranks
+        p->sm.resize(n);
+        std::vector<uint8_t> rk(n);
+        parallel_for(nt, (n + 4095) / 4096, [&](uint64_t b0, uint64_t b1) {
+            for (uint64_t i = b0 * 4096; i < std::min(n, b1 * 4096); i++) {
+                uint16_t b = bf16[i];
+                p->sm[i] = sm_of(b);
+                rk[i] = rank_of[exp_of(b)];
+            }
+        });
+        int rc = format == 2 ? pack_format2(p, rk, nt) : pack_format1(p, rk, nt);
+        if (rc != DGT_OK) {
+            delete p;
+            return rc;
+        }
+        p->refresh();
+    } catch (const std::bad_alloc &) {
+        delete p;
+        return DGT_ERR_OOM;
+    }
+    *out = p;
+    return DGT_OK;
+}
+
+void dgt_packed_free(dgt_packed *p) { delete p; }
+
+int dgt_packed_get_view(const dgt_packed *p, dgt_packed_view *view) {
+    if (!p || !view) return DGT_ERR_ARG;
+    *view = p->v;
+    return DGT_OK;
+}
+
+double dgt_packed_bits_per_weight(const dgt_packed *p) {
+    if (!p) return 0.0;
+    const uint64_t n = p->v.rows * p->v.cols;
+    if (!n) return 0.0;
+    uint64_t b = p->sm.size() + (uint64_t)p->v.n_table;
+    if (p->v.format == 2)
+        b += p->words.size() * 4 + p->blkq.size() + p->grp.size() * 4;
+    else
+        b += p->payload.size() + p->tw.size() + p->tesc.size() + p->esc1.size() + p->grp1.size() * 4;
+    return (double)b * 8.0 / (double)n;
+}
+
+int dgt_unpack(const dgt_packed_view *v, uint16_t *out, int nthreads) {
+    if (!v || (v->format != 1 && v->format != 2)) return DGT_ERR_ARG;
+    const uint64_t n = v->rows * v->cols;
+    if (n && (!out || !v->sm)) return DGT_ERR_ARG;
+    const int nt = resolve_threads(nthreads);
+    std::atomic<int> bad(0);
+    if (v->format == 2) {
+        const uint64_t nblk = (n + DGT_BLOCK - 1) / DGT_BLOCK;
+        const uint64_t ngrp = (nblk + DGT_GROUP - 1) / DGT_GROUP;
+        if (v->n_blocks != nblk || v->n_groups != ngrp || v->rice_k < 0 || v->rice_k > 7)
+            return DGT_ERR_CORRUPT;
+        const int k = v->rice_k;
+        parallel_for(nt, ngrp, [&](uint64_t g0, uint64_t g1) {
+            for (uint64_t g = g0; g < g1 && !bad.load(std::memory_order_relaxed); g++) {
+                BitReader br{v->words, (uint64_t)v->grp[2 * g] * 32, v->n_words * 32};
+                uint64_t b_end = std::min(nblk, (g + 1) * DGT_GROUP);
+                for (uint64_t b = g * DGT_GROUP; b < b_end; b++) {
+                    uint64_t i0 = b * DGT_BLOCK, cnt = std::min<uint64_t>(DGT_BLOCK, n - i0);
+                    uint8_t q = v->blkq[b];
+                    if (q != 255) {
+                        uint64_t start = br.pos;
+                        uint32_t qs = 0;
+                        for (uint64_t i = 0; i < cnt; i++) {
+                            uint32_t quo = 0;
+                            while (!br.bit() && quo <= 255) quo++;
+                            uint32_t r = (quo << k) | br.bits(k);
+                            if (r > 255) br.bad = true;
+                            qs += quo;
+                            out[i0 + i] = bf16_of(v->sm[i0 + i], v->table[r & 255]);
+                        }
+                        if (qs != q || br.pos - start != cnt * (uint64_t)(k + 1) + q) br.bad = true;
+                    } else {
+                        for (uint64_t i = 0; i < cnt; i++)
+                            out[i0 + i] = bf16_of(v->sm[i0 + i], v->table[br.bits(8)]);
+                    }
+                    if (br.bad) { bad.store(1); break; }
+                }
+            }
+        });
+    } else {
+        const uint64_t ntile = (n + DGT_TILE - 1) / DGT_TILE;
+        const uint64_t ngrp = (ntile + DGT_GROUP - 1) / DGT_GROUP;
+        if (v->n_tiles != ntile || v->n_groups1 != ngrp) return DGT_ERR_CORRUPT;
+        parallel_for(nt, ngrp, [&](uint64_t g0, uint64_t g1) {
+            for (uint64_t g = g0; g < g1 && !bad.load(std::memory_order_relaxed); g++) {
+                uint64_t off = (uint64_t)v->grp1[3 * g] * 16, e = v->grp1[3 * g + 1];
+                uint64_t t_end = std::min(ntile, (g + 1) * DGT_GROUP);
+                for (uint64_t t = g * DGT_GROUP; t < t_end; t++) {
+                    int w = v->tw[t];
+                    uint64_t i0 = t * DGT_TILE, cnt = std::min<uint64_t>(DGT_TILE, n - i0);
+                    if (w > 8 || off + 16ull * w > v->payload_bytes) { bad.store(1); break; }
+                    uint32_t top = w ? (1u << w) - 1u : 0u, seen = 0;
+                    for (uint64_t i = 0; i < cnt; i++) {
+                        uint32_t c = 0;
+                        for (int b = 0; b < w; b++) {
+                            uint64_t bit = off * 8 + i * (uint64_t)w + b;
+                            c |= (uint32_t)((v->payload[bit >> 3] >> (bit & 7)) & 1u) << b;
+                        }
+                        uint32_t r = c;
+                        if (w && c == top) {
+                            if (e >= v->n_esc1) { bad.store(1); break; }
+                            r = v->esc1[e++];
+                            seen++;
+                        }
+                        out[i0 + i] = bf16_of(v->sm[i0 + i], v->table[r]);
+                    }
+                    if (seen != v->tesc[t]) { bad.store(1); break; }
+                    off += 16ull * w;
+                }
+            }
+        });
+    }
+    return bad.load() ? DGT_ERR_CORRUPT : DGT_OK;
+}
+
+uint64_t dgt_r4_nseg(uint64_t cols) { return (cols + DGT_SEG - 1) / DGT_SEG; }
+
+int dgt_r4_sizes(uint64_t rows, uint64_t cols, uint64_t n_esc, uint64_t *nib_bytes,
+                 uint64_t *esc_bytes, uint64_t *seg_bytes) {
+    uint64_t n = rows * cols;
+    if (rows && n / rows != cols) return DGT_ERR_SHAPE;
+    if (nib_bytes) *nib_bytes = (n + 1) / 2;
+    if (esc_bytes) *esc_bytes = n_esc;
+    if (seg_bytes) *seg_bytes = (rows * dgt_r4_nseg(cols) + 1) * 4;
+    return DGT_OK;
+}
+
+int dgt_r4_init_from_view(const dgt_packed_view *v, uint8_t *d_nib, uint8_t *d_esc,
+                          uint32_t *d_seg, dgt_r4 *r4) {
+    if (!v || !r4) return DGT_ERR_ARG;
+    std::memset(r4, 0, sizeof(*r4));
+    r4->rows = v->rows;
+    r4->cols = v->cols;
+    r4->n_table = v->n_table;
+    std::memcpy(r4->table, v->table, 256);
+    r4->n_esc = v->n_esc15;
+    r4->sm = v->sm;
+    r4->nib = d_nib;
+    r4->esc = d_esc;
+    r4->seg = d_seg;
+    return DGT_OK;
+}
+
+int dgt_gemv_slices(uint64_t rows, uint64_t cols) { return dgt_plan_slices(rows, cols); }
+
+}  // extern "C"

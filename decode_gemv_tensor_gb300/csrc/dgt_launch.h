@@ -1,0 +1,53 @@
+// dgt_launch.h -- host-side launch helpers shared by libdgt's CUDA sources.
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/dgt.h"
+
+namespace dgt {
+
+struct DeviceInfo {
+    int device;
+    int sms;
+    int cc_major, cc_minor;
+};
+
+// The current device's SM count and compute capability, cached per device.
+static inline int device_info(DeviceInfo *out) {
+    static DeviceInfo cache[64];
+    static bool have[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return DGT_ERR_CUDA;
+    if (dev < 64 && have[dev]) {
+        *out = cache[dev];
+        return DGT_OK;
+    }
+    DeviceInfo d;
+    d.device = dev;
+    if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+        return DGT_ERR_CUDA;
+    if (dev < 64) {
+        cache[dev] = d;
+        have[dev] = true;
+    }
+    *out = d;
+    return DGT_OK;
+}
+
+// Allow `smem` bytes of dynamic shared memory and report resident CTAs per SM.
+static inline int prepare_kernel(const void *fn, size_t smem, int threads, int *blocks_per_sm) {
+    if (smem > 48 * 1024 &&
+        cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        return DGT_ERR_CUDA;
+    int b = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, fn, threads, smem) != cudaSuccess) return DGT_ERR_CUDA;
+    *blocks_per_sm = b > 0 ? b : 1;
+    return DGT_OK;
+}
+
+static inline bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+}  // namespace dgt

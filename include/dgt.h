@@ -1,0 +1,263 @@
+/*
+ * dgt.h -- C ABI of libdgt: lossless BF16 exponent-rank weight compression,
+ * decoded inside the matrix product, for one NVIDIA GB300 (sm_103a).
+ *
+ * The method (Binade project README, title paragraphs and "How it works"):
+ * each BF16 weight keeps its sign and 7-bit mantissa as one raw byte; its 8-bit
+ * exponent is replaced by its frequency rank in a per-tensor table.  On disk
+ * the ranks are Rice coded (format 2) or stored at a fixed width per
+ * 128-weight tile with escapes (format 1).  At load a GPU kernel turns either
+ * format into R4 -- one 4-bit rank per weight plus rare escapes -- which the
+ * matrix-vector, expert-gather and prompt GEMM kernels decode in registers
+ * while they compute.  Every product adds in one fixed, documented order, so
+ * the R4 kernels and the BF16-weight kernels of this library give
+ * bit-identical results.
+ *
+ * Conventions for every entry point:
+ *  - Return value: DGT_OK (0) or a negative DGT_ERR_* code; nothing throws
+ *    across the ABI.  dgt_status_string() names a code.
+ *  - "device" pointers are CUDA device addresses on the current device; the
+ *    caller owns and allocates every device buffer (the library allocates no
+ *    device memory).  "host" pointers are ordinary process memory.
+ *  - stream is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *    Device entry points only enqueue work; they return after the launch.
+ *    Errors detected by a kernel (corrupt stream, bounded wait ran out) are
+ *    written to the caller's device status word (int32, may be NULL) and are
+ *    read with dgt_read_status() once the stream has reached that point.
+ *  - Matrices are row-major [rows, cols] = [N, K] (out x in, like a
+ *    PyTorch Linear weight); the element count n = rows * cols.
+ *  - BF16 values travel as uint16_t bit patterns.
+ */
+#ifndef DGT_H
+#define DGT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ------------------------------------------------------------------------ */
+/* Status codes                                                             */
+/* ------------------------------------------------------------------------ */
+#define DGT_OK 0
+#define DGT_ERR_ARG (-1)         /* null pointer, bad enum, misaligned buffer */
+#define DGT_ERR_SHAPE (-2)       /* sizes outside the supported range          */
+#define DGT_ERR_CORRUPT (-3)     /* packed data disagrees with its own index    */
+#define DGT_ERR_CUDA (-4)        /* a CUDA runtime call or launch failed        */
+#define DGT_ERR_TIMEOUT (-5)     /* a bounded device wait ran out               */
+#define DGT_ERR_OOM (-6)         /* host allocation failed                      */
+#define DGT_ERR_IO (-7)          /* file open / read / write failed             */
+#define DGT_ERR_UNSUPPORTED (-8) /* no kernel for this device or configuration  */
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char *dgt_status_string(int status);
+
+/* ABI version of this header (major * 100 + minor). */
+int dgt_version(void);
+
+/* ------------------------------------------------------------------------ */
+/* Layout constants                                                         */
+/* ------------------------------------------------------------------------ */
+#define DGT_BLOCK 64   /* format 2: ranks per Rice block, one index byte each */
+#define DGT_GROUP 32   /* format 2: blocks per group; format 1: tiles per group */
+#define DGT_TILE 128   /* format 1: ranks per fixed-width tile                */
+#define DGT_SEG 512    /* R4: row-relative escape-index segment (columns)     */
+
+/* ------------------------------------------------------------------------ */
+/* Packed tensor (host object, library-owned)                               */
+/* ------------------------------------------------------------------------ */
+typedef struct dgt_packed dgt_packed;
+
+/*
+ * A read-only view of one packed tensor's arrays.  dgt_packed_get_view() fills
+ * it with HOST pointers into a dgt_packed.  To load on the GPU the caller
+ * copies each array to device memory and passes a copy of the view whose
+ * pointers are the DEVICE addresses of those copies (every array must start
+ * on a 16-byte boundary).
+ *
+ * Format 2 (Binade README, "Two file formats"; block index after the
+ * "Best measured configuration" of the "Lossless BF16 weight compression"
+ * README): ranks are cut into blocks of 64 and groups of 32 blocks.  A block
+ * whose quotient sum Q = sum(r >> k) is <= 254 is Rice coded -- per rank
+ * (r >> k) zero bits, a one bit, then the k low bits of r, least significant
+ * first -- and its index byte blkq is Q (length count*(k+1)+Q bits); a block
+ * with Q >= 255 holds 8-bit raw ranks and index byte 255.  Stream bit j is
+ * bit (j % 32) of little-endian word j / 32.  Each group starts on a word;
+ * grp holds two words per group: {first word, ranks >= 15 before the group}.
+ *
+ * Format 1 (same section, "fixed width per 128-weight tile with escapes"):
+ * per tile a width w in 0..8 (tw); 128 codes of w bits, least significant bit
+ * first, 16*w bytes (payload); code 2^w - 1 is an escape whose rank follows in
+ * esc1 (tile order); tesc counts a tile's escapes; grp1 holds three words per
+ * 32 tiles: {payload offset / 16, esc1 entries before, ranks >= 15 before}.
+ */
+typedef struct dgt_packed_view {
+    uint64_t rows, cols;      /* N, K                                        */
+    int32_t format;           /* 1 or 2                                      */
+    int32_t rice_k;           /* format 2: Rice parameter 0..7               */
+    int32_t n_table;          /* T: distinct exponents (0..256)              */
+    int32_t reserved;
+    uint8_t table[256];       /* rank -> exponent, entries >= T are 0        */
+    uint64_t n_esc15;         /* ranks >= 15 (R4 escapes)                    */
+    const uint8_t *sm;        /* n bytes: sign << 7 | mantissa               */
+    const uint32_t *words;    /* format 2: Rice stream, n_words words        */
+    uint64_t n_words;
+    const uint8_t *blkq;      /* format 2: ceil(n/64) index bytes            */
+    uint64_t n_blocks;
+    const uint32_t *grp;      /* format 2: 2 words per group                 */
+    uint64_t n_groups;
+    const uint8_t *payload;   /* format 1: tile codes                        */
+    uint64_t payload_bytes;
+    const uint8_t *tw;        /* format 1: width per tile                    */
+    const uint8_t *tesc;      /* format 1: escapes per tile                  */
+    uint64_t n_tiles;
+    const uint8_t *esc1;      /* format 1: raw escaped ranks                 */
+    uint64_t n_esc1;
+    const uint32_t *grp1;     /* format 1: 3 words per 32 tiles              */
+    uint64_t n_groups1;
+} dgt_packed_view;
+
+/*
+ * Pack a BF16 matrix (Binade README: "binade pack"; title paragraph and
+ * "How it works").  bf16: host, rows*cols values.  format: 1 or 2.
+ * nthreads: host threads to use (<= 0: all hardware threads).  On success
+ * *out owns a new object; free it with dgt_packed_free().  The rank table
+ * sorts exponents by count (descending), ties by exponent (ascending); format
+ * 2 takes the k in 0..7 with the fewest stream words, ties to the smaller k;
+ * format 1 takes per tile the w minimising 128*w + 8*escapes, ties to the
+ * smaller w, and w = 0 iff the tile is all rank 0.
+ * Errors: DGT_ERR_ARG (null, bad format), DGT_ERR_SHAPE (n >= 2^40 or a group
+ * index overflowing 32 bits), DGT_ERR_OOM.
+ */
+int dgt_pack(const uint16_t *bf16, uint64_t rows, uint64_t cols, int format, int nthreads,
+             dgt_packed **out);
+
+/* Free a packed object (NULL is ignored). */
+void dgt_packed_free(dgt_packed *p);
+
+/* Fill *view with host pointers into p (valid until p is freed). */
+int dgt_packed_get_view(const dgt_packed *p, dgt_packed_view *view);
+
+/* Bits per weight of every stored array (sm, table, stream, index). */
+double dgt_packed_bits_per_weight(const dgt_packed *p);
+
+/*
+ * Host unpack (Binade README, "Use": "binade unpack ... rebuilds the original
+ * BF16 checkpoint, bit for bit").  view: host pointers.  out_bf16: host,
+ * rows*cols values, caller-owned.  Errors: DGT_ERR_ARG, DGT_ERR_CORRUPT (a
+ * block or tile disagrees with its index byte; out is then unspecified).
+ */
+int dgt_unpack(const dgt_packed_view *view, uint16_t *out_bf16, int nthreads);
+
+/*
+ * File container (model cards: "the packed bytes are stored as uint8
+ * tensors"): a safetensors file -- u64 little-endian header length, a JSON
+ * header, then the data -- with, per tensor name X, arrays "X.sm", "X.rice",
+ * "X.blkq", "X.grp" (format 2) or "X.f1", "X.tw", "X.tesc", "X.esc1",
+ * "X.grp1" (format 1), and the metadata entry "X" = "format=..;rows=..;...".
+ * dgt_write: tensors/names are host arrays of count entries.
+ * dgt_read: *tensors and *names are library-allocated arrays of *count
+ * entries; release them with dgt_read_free().
+ * Errors: DGT_ERR_ARG, DGT_ERR_IO, DGT_ERR_CORRUPT (malformed header or
+ * arrays whose sizes disagree with the metadata), DGT_ERR_OOM.
+ */
+int dgt_write(const char *path, const dgt_packed *const *tensors, const char *const *names,
+              int count);
+int dgt_read(const char *path, dgt_packed ***tensors, char ***names, int *count);
+void dgt_read_free(dgt_packed **tensors, char **names, int count);
+
+/* ------------------------------------------------------------------------ */
+/* R4 runtime layout (device, caller-owned)                                 */
+/* ------------------------------------------------------------------------ */
+/*
+ * Binade README, "Runtime layout": every rank in 4 bits, with rare escapes.
+ * nib: ceil(n/2) bytes, element i in byte i/2, low nibble when i is even,
+ *      value min(rank, 15).
+ * esc: n_esc bytes, the rank of every element whose nibble is 15, flat order.
+ * seg: rows*nseg + 1 words, nseg = ceil(cols/512); seg[r*nseg + j] counts the
+ *      escapes at flat positions < r*cols + 512*j; the last word is n_esc.
+ * sm:  n bytes, sign << 7 | mantissa (the packed array itself, not a copy).
+ * All four device arrays must start on 16-byte boundaries.
+ */
+typedef struct dgt_r4 {
+    uint64_t rows, cols;
+    int32_t n_table;
+    int32_t reserved;
+    uint8_t table[256];
+    uint64_t n_esc;
+    const uint8_t *sm;
+    uint8_t *nib;
+    uint8_t *esc;
+    uint32_t *seg;
+} dgt_r4;
+
+/* nseg = ceil(cols / 512). */
+uint64_t dgt_r4_nseg(uint64_t cols);
+
+/* Byte sizes of the R4 arrays for a rows x cols tensor with n_esc escapes. */
+int dgt_r4_sizes(uint64_t rows, uint64_t cols, uint64_t n_esc, uint64_t *nib_bytes,
+                 uint64_t *esc_bytes, uint64_t *seg_bytes);
+
+/*
+ * Load transcode (Binade README, "Runtime layout": "At load a GPU kernel
+ * turns either format into R4").  dev: a view with DEVICE pointers of a
+ * format 1 or 2 tensor.  r4: rows, cols, n_table, table, n_esc and sm must
+ * be set by the caller (dgt_r4_init_from_view does it); nib, esc and seg are
+ * written.  d_status: device int32 set to 0 then to a DGT_ERR_* code if a
+ * kernel finds the stream corrupt.  Asynchronous on stream.
+ * Errors (immediate): DGT_ERR_ARG, DGT_ERR_SHAPE, DGT_ERR_CUDA.
+ */
+int dgt_load_r4(const dgt_packed_view *dev, dgt_r4 *r4, int32_t *d_status, void *stream);
+
+/* Fill rows, cols, table, n_table, n_esc from a view and set the four array
+   pointers (sm is taken from the view). */
+int dgt_r4_init_from_view(const dgt_packed_view *view, uint8_t *d_nib, uint8_t *d_esc,
+                          uint32_t *d_seg, dgt_r4 *r4);
+
+/*
+ * R4 -> BF16 rebuild (Binade README, "NVIDIA GPUs" and "Exactness": the
+ * runtime "rebuilds the BF16 weight" where no fused kernel applies).
+ * d_out: device, rows*cols uint16, 16-byte aligned.  Asynchronous.
+ */
+int dgt_r4_to_bf16(const dgt_r4 *r4, uint16_t *d_out, int32_t *d_status, void *stream);
+
+/* Copy the device status word to the host after the stream reaches it. */
+int dgt_read_status(const int32_t *d_status, void *stream, int32_t *status);
+
+/* ------------------------------------------------------------------------ */
+/* Batch-1 products                                                         */
+/* ------------------------------------------------------------------------ */
+/*
+ * Summation order shared by dgt_gemv and dgt_gemv_bf16 (Binade README,
+ * "Exactness": the kernels add in one order, so outputs are bit-identical):
+ * rounds of 512 columns; in round j lane u (0..31) owns columns
+ * [512j + 16u, 512j + 16u + 16) (clipped at K); each lane starts at +0 and
+ * applies fmaf(w, x, acc) over its columns in increasing order, round after
+ * round; five butterfly steps acc_u += acc_(u xor d), d = 16, 8, 4, 2, 1; the
+ * slice result is lane 0's value.  With S slices, slice s owns rounds
+ * [floor(s*J/S), floor((s+1)*J/S)), J = ceil(K/512), and
+ * y = ((P_0 + P_1) + ...) + P_(S-1).  y_bf16 is y rounded to nearest-even
+ * (NaN -> 0x7FC0).  dgt_gemv_slices() is the plan S(N, K): the smallest power
+ * of two >= ceil(2432/N), capped at 8 and at the largest power of two <= J.
+ */
+int dgt_gemv_slices(uint64_t rows, uint64_t cols);
+
+/*
+ * y = W x with W in R4 (Binade README, "Results": "Matvec kernel"; "How it
+ * works": "its matvec streams at full bandwidth").  d_x: device, cols bf16.
+ * d_y: device, rows bf16 (may be NULL).  d_y32: device, rows float (may be
+ * NULL).  Asynchronous.  Errors: DGT_ERR_ARG, DGT_ERR_SHAPE (cols >= 2^31),
+ * DGT_ERR_CUDA.
+ */
+int dgt_gemv(const dgt_r4 *W, const uint16_t *d_x, uint16_t *d_y, float *d_y32, void *stream);
+
+/* The same product and order with plain BF16 weights d_W [rows, cols]. */
+int dgt_gemv_bf16(const uint16_t *d_W, uint64_t rows, uint64_t cols, const uint16_t *d_x,
+                  uint16_t *d_y, float *d_y32, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DGT_H */

@@ -1,0 +1,127 @@
+"""GPU parity for the batch-1 products: the R4 GEMV and the BF16 GEMV against
+the oracle's fixed order, bit for bit (float32 and bf16 outputs), on ragged
+shapes, every slice plan, both kernel paths, and the pages' model shapes."""
+import numpy as np
+import pytest
+
+import oracle
+import synthetic as S
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def dgt():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import decode_gemv_tensor_gb300 as d
+    d.lib()
+    return d
+
+
+def _dev_bf16(a):
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda().view(torch.bfloat16)
+
+
+def _host(t):
+    return t.view(torch.int16).cpu().numpy().view(np.uint16) if t.dtype == torch.bfloat16 else t.cpu().numpy()
+
+
+def _run_both(dgt, w, x, fmt=2):
+    r4 = dgt.load_r4(dgt.upload(dgt.pack(w, fmt)))
+    xd = _dev_bf16(x)
+    y16, y32 = dgt.gemv(r4, xd)
+    b16, b32 = dgt.gemv_bf16(_dev_bf16(w), xd)
+    return _host(y16), _host(y32), _host(b16), _host(b32)
+
+
+def _eq32(a, b):
+    return np.array_equal(a.view(np.uint32), b.view(np.uint32))
+
+
+SHAPES = [(1, 16), (1, 512), (5, 512), (3, 1000), (1, 4096), (8, 2048), (40, 1300), (100, 1024),
+          (300, 2112), (704, 2816), (2816, 704), (1024, 3072), (2048, 3840), (17, 16000), (2, 60000),
+          (9, 8), (4, 0)]
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: f"{s[0]}x{s[1]}")
+def test_gemv_matches_oracle(dgt, shape):
+    N, K = shape
+    w = S.weights(N, K, (201, N, K), outliers=True)
+    x = S.activations(K, (201, 999, K)) if K else np.zeros(0, np.uint16)
+    r32, r16 = oracle.gemv(w, x)
+    y16, y32, b16, b32 = _run_both(dgt, w, x)
+    assert _eq32(y32, r32) and np.array_equal(y16, r16), "R4 GEMV"
+    assert _eq32(b32, r32) and np.array_equal(b16, r16), "BF16 GEMV"
+
+
+def test_gemv_every_slice_plan(dgt):
+    seen = set()
+    for N, K in [(4096, 1024), (1200, 2048), (700, 4096), (200, 4096), (30, 8192)]:
+        seen.add(dgt.gemv_slices(N, K))
+        w = S.weights(N, K, (202, N, K), outliers=True)
+        x = S.activations(K, (202, 999, K))
+        r32, r16 = oracle.gemv(w, x)
+        y16, y32, b16, b32 = _run_both(dgt, w, x, fmt=1)
+        assert _eq32(y32, r32) and _eq32(b32, r32)
+    assert seen == {1, 2, 4, 8}
+
+
+def test_gemv_order_sensitive_rows(dgt):
+    # rows that change value under any reordering of the sum
+    K = 2048
+    N = 64
+    g = np.random.default_rng(5)
+    w = np.zeros((N, K), np.float32)
+    for r in range(N):
+        pos = g.choice(K, size=40, replace=False)
+        w[r, pos[:20]] = 2.0 ** 24 * np.where(g.random(20) < 0.5, 1, -1)
+        w[r, pos[20:]] = 1.0
+    wb = S.f32_to_bf16_bits(w)
+    x = S.f32_to_bf16_bits(np.ones(K, np.float32))
+    r32, _ = oracle.gemv(wb, x)
+    _, y32, _, b32 = _run_both(dgt, wb, x)
+    assert _eq32(y32, r32) and _eq32(b32, r32)
+
+
+def test_gemv_generic_path_equals_fast_path(dgt):
+    N, K = 257, 4096
+    w = S.weights(N, K, (203, 0, 0, 0), outliers=True)
+    x = S.activations(K, (203, 999, 0))
+    r4 = dgt.load_r4(dgt.upload(dgt.pack(w, 2)))
+    xd = _dev_bf16(x)
+    y16, y32 = dgt.gemv(r4, xd)
+    # x starting 2 bytes past a 16-byte boundary forces the any-shape kernel
+    buf = torch.empty(K + 8, dtype=torch.bfloat16, device="cuda")
+    buf[1:1 + K].copy_(xd)
+    g16, g32 = dgt.gemv(r4, buf[1:1 + K])
+    wd = _dev_bf16(w)
+    h16, h32 = dgt.gemv_bf16(wd, buf[1:1 + K])
+    assert torch.equal(y32.view(torch.int32), g32.view(torch.int32))
+    assert torch.equal(y32.view(torch.int32), h32.view(torch.int32))
+    assert torch.equal(y16.view(torch.int16), g16.view(torch.int16))
+
+
+def test_gemv_bulk_4096x16384_full(dgt):
+    w = S.weights(4096, 16384, (2, 0, 0, 0), outliers=True)
+    x = S.activations(16384, (2, 999, 0))
+    r32, r16 = oracle.gemv(w, x)
+    y16, y32, b16, b32 = _run_both(dgt, w, x)
+    assert _eq32(y32, r32) and np.array_equal(y16, r16)
+    assert _eq32(b32, r32) and np.array_equal(b16, r16)
+
+
+@pytest.mark.parametrize("model", [S.DENSE_3B, S.DENSE_12B], ids=lambda m: m["name"])
+def test_gemv_model_projections_sampled(dgt, model):
+    # one layer's projections at full size: R4 == BF16 on every row, oracle on sampled rows
+    g = np.random.default_rng(9)
+    for pi, (name, N, K) in enumerate(model["proj"]):
+        w = S.weights(N, K, (3, 0, pi, 0))
+        x = S.activations(K, (3, 999, pi))
+        y16, y32, b16, b32 = _run_both(dgt, w, x)
+        assert _eq32(y32, b32) and np.array_equal(y16, b16), name
+        rows = np.unique(np.concatenate([[0, N - 1], g.choice(N, 62, replace=False)]))
+        r32, r16 = oracle.gemv(w, x, rows=rows)
+        assert _eq32(y32[rows], r32) and np.array_equal(y16[rows], r16), name
