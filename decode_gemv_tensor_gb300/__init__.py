@@ -82,8 +82,8 @@ def lib():
             "dgt_r4_to_bf16": (i32, [C.POINTER(R4Struct), vp, vp, vp]),
             "dgt_read_status": (i32, [vp, vp, C.POINTER(C.c_int32)]),
             "dgt_gemv_slices": (i32, [u64, u64]),
-            "dgt_gemv": (i32, [C.POINTER(R4Struct), vp, vp, vp, vp]),
-            "dgt_gemv_bf16": (i32, [vp, u64, u64, vp, vp, vp, vp]),
+            "dgt_gemv": (i32, [C.POINTER(R4Struct), vp, vp, vp, vp, vp]),
+            "dgt_gemv_bf16": (i32, [vp, u64, u64, vp, vp, vp, vp, vp]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -304,7 +304,7 @@ def read_status(status, stream=None) -> int:
     return v.value
 
 
-def gemv(W: R4, x, y=None, y32=None, stream=None):
+def gemv(W: R4, x, y=None, y32=None, status=None, stream=None):
     """dgt_gemv: y = W x with W in R4; x bf16 [cols] on the device.
     Returns (y bf16 [rows], y32 float32 [rows])."""
     import torch
@@ -313,11 +313,11 @@ def gemv(W: R4, x, y=None, y32=None, stream=None):
         y = torch.empty(W.rows, dtype=torch.bfloat16, device=dev)
     if y32 is None:
         y32 = torch.empty(W.rows, dtype=torch.float32, device=dev)
-    _check(lib().dgt_gemv(C.byref(W.s), _ptr(x), _ptr(y), _ptr(y32), _stream(stream)), "dgt_gemv")
+    _check(lib().dgt_gemv(C.byref(W.s), _ptr(x), _ptr(y), _ptr(y32), _ptr(status), _stream(stream)), "dgt_gemv")
     return y, y32
 
 
-def gemv_bf16(W, x, y=None, y32=None, stream=None):
+def gemv_bf16(W, x, y=None, y32=None, status=None, stream=None):
     """dgt_gemv_bf16: the same product and order with bf16 weights [rows, cols]."""
     import torch
     rows, cols = W.shape
@@ -325,6 +325,6 @@ def gemv_bf16(W, x, y=None, y32=None, stream=None):
         y = torch.empty(rows, dtype=torch.bfloat16, device=W.device)
     if y32 is None:
         y32 = torch.empty(rows, dtype=torch.float32, device=W.device)
-    _check(lib().dgt_gemv_bf16(_ptr(W), rows, cols, _ptr(x), _ptr(y), _ptr(y32), _stream(stream)),
+    _check(lib().dgt_gemv_bf16(_ptr(W), rows, cols, _ptr(x), _ptr(y), _ptr(y32), _ptr(status), _stream(stream)),
            "dgt_gemv_bf16")
     return y, y32

@@ -12,14 +12,20 @@
 // d = 16, 8, 4, 2, 1; with S slices (dgt_plan_slices) slice s owns rounds
 // [sJ/S, (s+1)J/S) and the slice results are added left to right.
 //
-// GB300 design: 8 warps per CTA, (8/S) rows x S slices per CTA iteration, a
-// persistent grid sized by occupancy.  x is converted once per CTA into
-// shared memory as float32 in a [round][quad][lane] float4 layout, so each
-// lane's four LDS.128 per round are conflict-free.  R4 weights stream with one
-// 16-byte load of sign/mantissa bytes and one 8-byte load of nibbles per lane
-// and round (L1 no-allocate), four rounds in flight; the exponent comes from
-// register byte-permutes.  Escapes are found per round from the row-segment
-// index (a warp-uniform count, so rounds without escapes pay one shuffle).
+// GB300 design: a persistent grid of one 16-warp CTA per SM.  CTA b owns a
+// contiguous, even share of the rows and walks its (row, slice) units warp by
+// warp, so no SM waits on a second wave.  x is copied once per CTA into shared
+// memory as bf16 pairs in a [round][half][lane] uint4 layout (two
+// conflict-free LDS.128 per lane and round), and the products use the
+// mixed-precision fma.rn.f32.bf16, which takes the bf16 halves directly.
+// R4 weights stream with one 16-byte load of
+// sign/mantissa bytes and one 8-byte load of nibbles per lane and round
+// (L1 no-allocate), double-buffered so that eight rounds are in flight per
+// lane; the exponent comes from register byte-permutes.  Escapes are known
+// per round from the row-segment index: a ballot gives a warp-uniform mask of
+// rounds with escapes, which go to one out-of-line function (one escape is
+// patched from a prefetched exponent, more are staged through shared
+// memory); rounds without escapes pay one test and stay in a small loop.
 #include <cuda_runtime.h>
 
 #include "../../include/dgt.h"
@@ -29,9 +35,9 @@
 
 namespace dgt {
 
-constexpr int GW = 8;       // warps per CTA
-constexpr int UNROLL = 4;   // rounds in flight per lane
-constexpr uint32_t MAX_FAST_ROUNDS = 104;  // x in shared memory: 104 * 2 KB
+constexpr int GW = 8;        // warps per CTA of the any-shape kernel
+constexpr int CHUNK = 128;   // (row, slice) units per CTA chunk
+constexpr uint32_t MAX_FAST_ROUNDS = 160;  // x staged in shared memory, 1 KB per round
 
 struct GemvArgs {
     const uint8_t *sm;
@@ -44,157 +50,497 @@ struct GemvArgs {
     float *y32;
     uint64_t rows, cols, nseg, n_esc;
     uint32_t J;
+    int S;
     R4Lut L;
     uint8_t table[256];
     int32_t *status;
 };
 
-// acc = fmaf(w_i, x_i, acc) over the chunk's 16 weights in column order.
-__device__ __forceinline__ float fma_chunk(const uint32_t p[8], const float4 *xs, uint32_t j, uint32_t lane,
-                                           float acc) {
+// Two fused multiply-adds in column order, the bf16 operands taken straight
+// from the low and high halves of w and x: acc = fma(w.lo, x.lo, acc), then
+// acc = fma(w.hi, x.hi, acc).  Each is one fp32 FMA with a single rounding.
+__device__ __forceinline__ float fma2_bf16(uint32_t w, uint32_t x, float acc) {
+    asm("{\n\t.reg .b16 a0, a1, b0, b1;\n\t"
+        "mov.b32 {a0, a1}, %1;\n\t"
+        "mov.b32 {b0, b1}, %2;\n\t"
+        "fma.rn.f32.bf16 %0, a0, b0, %0;\n\t"
+        "fma.rn.f32.bf16 %0, a1, b1, %0;\n\t}"
+        : "+f"(acc)
+        : "r"(w), "r"(x));
+    return acc;
+}
+
+// Lane chunk of 16 weights (eight bf16 pairs) against x staged as bf16 pairs:
+// round j, lane u -> two uint4 at [(2j + h) * 32 + u].
+__device__ __forceinline__ float fma_chunk16(const uint32_t p[8], const uint4 *xs, uint32_t j, uint32_t lane,
+                                             float acc) {
+    const uint4 xa = xs[(2 * j) * 32 + lane];
+    const uint4 xb = xs[(2 * j + 1) * 32 + lane];
+    acc = fma2_bf16(p[0], xa.x, acc);
+    acc = fma2_bf16(p[1], xa.y, acc);
+    acc = fma2_bf16(p[2], xa.z, acc);
+    acc = fma2_bf16(p[3], xa.w, acc);
+    acc = fma2_bf16(p[4], xb.x, acc);
+    acc = fma2_bf16(p[5], xb.y, acc);
+    acc = fma2_bf16(p[6], xb.z, acc);
+    acc = fma2_bf16(p[7], xb.w, acc);
+    return acc;
+}
+
+template <bool R4, int U>
+struct Batch {
+    uint4 s[U];   // R4: sign/mantissa bytes; BF16: first 8 weights
+    uint2 n[U];   // R4: nibbles
+    uint4 v[U];   // BF16: last 8 weights
+};
+
+template <bool R4, int U>
+__device__ __forceinline__ void load_batch(Batch<R4, U> &B, const uint8_t *smp, const uint8_t *nbp,
+                                           const uint16_t *wp, uint32_t jb, uint32_t j1, uint32_t Jm1,
+                                           bool last_ok) {
 #pragma unroll
-    for (int q = 0; q < 4; q++) {
-        const float4 xv = xs[(j * 4 + q) * 32 + lane];
-        acc = fmaf(bf16lo(p[2 * q]), xv.x, acc);
-        acc = fmaf(bf16hi(p[2 * q]), xv.y, acc);
-        acc = fmaf(bf16lo(p[2 * q + 1]), xv.z, acc);
-        acc = fmaf(bf16hi(p[2 * q + 1]), xv.w, acc);
+    for (int t = 0; t < U; t++) {
+        const uint32_t j = jb + t;
+        if (j < j1 && (j != Jm1 || last_ok)) {
+            if (R4) {
+                B.s[t] = ldg_stream16(smp + (size_t)j * 512);
+                B.n[t] = ldg_stream8(nbp + (size_t)j * 256);
+            } else {
+                ldg_stream32(wp + (size_t)j * 512, B.s[t], B.v[t]);
+            }
+        }
+    }
+}
+
+// Escape information of up to 32 rounds [jbase, jbase + 32) of one row:
+// lane t holds round jbase + t.
+struct SegInfo {
+    uint32_t cnt, base, fexp, emask;
+};
+
+__device__ __forceinline__ SegInfo load_seginfo(const GemvArgs &a, const uint8_t *table_s, uint64_t row,
+                                                uint32_t jbase, uint32_t j1, uint32_t lane) {
+    SegInfo g;
+    g.cnt = g.base = g.fexp = 0;
+    const uint32_t j = jbase + lane;
+    if (j < j1) {
+        const uint32_t *sp = a.seg + row * a.nseg + j;
+        g.base = sp[0];
+        g.cnt = sp[1] - g.base;
+        if (g.cnt && g.base < a.n_esc) g.fexp = table_s[a.esc[g.base]];
+    }
+    g.emask = __ballot_sync(DGT_FULL, g.cnt != 0);
+    return g;
+}
+
+// A round of an R4 row that holds escapes: decode, patch, multiply-add.
+// Kept out of line so that the common path stays small in the instruction
+// cache.  Called by all 32 lanes; c = escapes in the round, b = the first
+// escape's index, e = its exponent.
+__device__ __noinline__ float round_with_escapes(const uint8_t *esc, uint64_t n_esc, R4Lut L, uint2 n,
+                                                 uint4 s, const uint4 *xs,
+                                                 uint8_t *escb, const uint8_t *table_s, uint32_t j,
+                                                 uint32_t lane, bool act, uint32_t c, uint32_t b, uint32_t e,
+                                                 float acc) {
+    uint32_t p[8];
+    r4_dec16(n, s, L, p);
+    const uint32_t m0 = act ? nib15_mask(n.x) : 0u;
+    const uint32_t m1 = act ? nib15_mask(n.y) : 0u;
+    if (c == 1) {
+        if (m0 | m1) {
+            const uint32_t pos = m0 ? (__ffs(m0) - 1) >> 2 : 8 + ((__ffs(m1) - 1) >> 2);
+#pragma unroll
+            for (int i = 0; i < 8; i++) {
+                if ((pos >> 1) == (uint32_t)i) {
+                    const uint32_t sh = (pos & 1) * 16;
+                    p[i] = (p[i] & ~(0x7F80u << sh)) | (e << (7 + sh));
+                }
+            }
+        }
+    } else {
+        const uint32_t cc = c > DGT_SEG ? DGT_SEG : c;
+        for (uint32_t i = lane; i < cc; i += 32) escb[i] = (uint64_t)b + i < n_esc ? esc[b + i] : 0;
+        __syncwarp();
+        patch_escapes(p, m0, m1, cc, escb, table_s);
+        __syncwarp();
+    }
+    if (act) acc = fma_chunk16(p, xs, j, lane, acc);
+    return acc;
+}
+
+// Decode a 16-weight lane chunk of a round that holds escapes (out of line:
+// keeps the common path small).  Called by all 32 lanes; c = escapes in the
+// round, b = index of the first, e = its exponent.
+struct Pairs8 {
+    uint32_t v[8];
+};
+
+__device__ __noinline__ Pairs8 decode_with_escapes_impl(const uint8_t *esc, uint64_t n_esc, R4Lut L, uint2 n,
+                                                      uint4 s, uint8_t *escb, const uint8_t *table_s,
+                                                      uint32_t lane, bool act, uint32_t c, uint32_t b,
+                                                      uint32_t e) {
+    Pairs8 out;
+    uint32_t *p = out.v;
+    r4_dec16(n, s, L, p);
+    const uint32_t m0 = act ? nib15_mask(n.x) : 0u;
+    const uint32_t m1 = act ? nib15_mask(n.y) : 0u;
+    if (c == 1) {
+        if (m0 | m1) {
+            const uint32_t pos = m0 ? (__ffs(m0) - 1) >> 2 : 8 + ((__ffs(m1) - 1) >> 2);
+#pragma unroll
+            for (int i = 0; i < 8; i++) {
+                if ((pos >> 1) == (uint32_t)i) {
+                    const uint32_t sh = (pos & 1) * 16;
+                    p[i] = (p[i] & ~(0x7F80u << sh)) | (e << (7 + sh));
+                }
+            }
+        }
+    } else {
+        const uint32_t cc = c > DGT_SEG ? DGT_SEG : c;
+        for (uint32_t i = lane; i < cc; i += 32) escb[i] = (uint64_t)b + i < n_esc ? esc[b + i] : 0;
+        __syncwarp();
+        patch_escapes(p, m0, m1, cc, escb, table_s);
+        __syncwarp();
+    }
+    return out;
+}
+
+__device__ __forceinline__ void decode_with_escapes(const uint8_t *esc, uint64_t n_esc, const R4Lut &L, uint2 n,
+                                                    uint4 s, uint8_t *escb, const uint8_t *table_s,
+                                                    uint32_t lane, bool act, uint32_t c, uint32_t b, uint32_t e,
+                                                    uint32_t p[8]) {
+    const Pairs8 r = decode_with_escapes_impl(esc, n_esc, L, n, s, escb, table_s, lane, act, c, b, e);
+#pragma unroll
+    for (int i = 0; i < 8; i++) p[i] = r.v[i];
+}
+
+template <bool R4, int U>
+__device__ __forceinline__ float compute_batch(const GemvArgs &a, const Batch<R4, U> &B, const uint4 *xs,
+                                               uint8_t *escb, const uint8_t *table_s, const SegInfo &g,
+                                               uint32_t jb, uint32_t jbase, uint32_t j1, uint32_t Jm1,
+                                               bool last_ok, uint32_t lane, float acc) {
+#pragma unroll
+    for (int t = 0; t < U; t++) {
+        const uint32_t j = jb + t;
+        if (j >= j1) break;
+        const bool act = j != Jm1 || last_ok;
+        uint32_t p[8];
+        if (R4) {
+            const uint32_t bit = j - jbase;
+            if ((g.emask >> bit) & 1u) {
+                const uint32_t c = __shfl_sync(DGT_FULL, g.cnt, bit);
+                const uint32_t b = __shfl_sync(DGT_FULL, g.base, bit);
+                const uint32_t e = __shfl_sync(DGT_FULL, g.fexp, bit);
+                acc = round_with_escapes(a.esc, a.n_esc, a.L, B.n[t], B.s[t], xs, escb, table_s, j, lane, act, c, b,
+                                         e, acc);
+                continue;
+            }
+            r4_dec16(B.n[t], B.s[t], a.L, p);
+        } else {
+            p[0] = B.s[t].x; p[1] = B.s[t].y; p[2] = B.s[t].z; p[3] = B.s[t].w;
+            p[4] = B.v[t].x; p[5] = B.v[t].y; p[6] = B.v[t].z; p[7] = B.v[t].w;
+        }
+        if (act) acc = fma_chunk16(p, xs, j, lane, acc);
     }
     return acc;
+}
+
+// One (row, slice) unit: the lane's fmaf chain over rounds [j0, j1).
+template <bool R4, int U>
+__device__ __forceinline__ float unit_dot(const GemvArgs &a, const uint4 *xs, uint8_t *escb, const uint8_t *table_s,
+                                          uint64_t row, uint32_t j0, uint32_t j1, uint32_t lane, bool last_ok) {
+    const uint64_t rb = row * a.cols + 16 * lane;
+    const uint8_t *smp = R4 ? a.sm + rb : nullptr;
+    const uint8_t *nbp = R4 ? a.nib + rb / 2 : nullptr;
+    const uint16_t *wp = R4 ? nullptr : a.W + rb;
+    const uint32_t Jm1 = a.J - 1;
+    SegInfo g = {0, 0, 0, 0};
+    uint32_t jbase = j0;
+    if (R4) g = load_seginfo(a, table_s, row, jbase, j1, lane);
+    float acc = 0.0f;
+    Batch<R4, U> A, B;
+    load_batch<R4, U>(A, smp, nbp, wp, j0, j1, Jm1, last_ok);
+    for (uint32_t jb = j0; jb < j1; jb += 2 * U) {
+        if (R4 && jb - jbase >= 32) {
+            jbase = jb;
+            g = load_seginfo(a, table_s, row, jbase, j1, lane);
+        }
+        load_batch<R4, U>(B, smp, nbp, wp, jb + U, j1, Jm1, last_ok);
+        acc = compute_batch<R4, U>(a, A, xs, escb, table_s, g, jb, jbase, j1, Jm1, last_ok, lane, acc);
+        load_batch<R4, U>(A, smp, nbp, wp, jb + 2 * U, j1, Jm1, last_ok);
+        acc = compute_batch<R4, U>(a, B, xs, escb, table_s, g, jb + U, jbase, j1, Jm1, last_ok, lane, acc);
+    }
+    return acc;
+}
+
+// Streaming kernel: one CTA of 16 warps per SM; CTA b owns rows
+// [b*N/G, (b+1)*N/G) and walks their (row, slice) units in chunks of 128,
+// warp w taking units w, w+16, ...; slice partials meet in shared memory and
+// are added left to right.
+template <bool R4, int PW, int U>
+__global__ void __launch_bounds__(PW * 32, 1) k_gemv(GemvArgs a) {
+    extern __shared__ uint4 xs[];
+    __shared__ uint8_t table_s[256];
+    __shared__ uint8_t escb[PW][DGT_SEG];
+    __shared__ float part[CHUNK];
+    const uint32_t tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
+    const uint32_t K = (uint32_t)a.cols;
+    for (uint32_t i = tid; i < K / 8; i += PW * 32) {
+        const uint32_t k = 8 * i, j = k >> 9, u = (k >> 4) & 31, h = (k >> 3) & 1;
+        xs[(2 * j + h) * 32 + u] = *reinterpret_cast<const uint4 *>(a.x + k);
+    }
+    if (R4 && tid < 256) table_s[tid] = a.table[tid];
+    __syncthreads();
+    const int S = a.S;
+    const uint64_t G = gridDim.x;
+    const uint64_t r0 = (uint64_t)blockIdx.x * a.rows / G, r1 = (uint64_t)(blockIdx.x + 1) * a.rows / G;
+    const uint64_t units = (r1 - r0) * S;
+    const bool last_ok = 16 * lane < K - 512 * (a.J - 1);
+    for (uint64_t c0 = 0; c0 < units; c0 += CHUNK) {
+        const uint32_t cu = (uint32_t)min((uint64_t)CHUNK, units - c0);
+        for (uint32_t u = w; u < cu; u += PW) {
+            const uint64_t uu = c0 + u;
+            const uint64_t row = r0 + uu / S;
+            const uint32_t s = (uint32_t)(uu % S);
+            const uint32_t j0 = (uint32_t)((uint64_t)s * a.J / S), j1 = (uint32_t)((uint64_t)(s + 1) * a.J / S);
+            float acc = unit_dot<R4, U>(a, xs, escb[w], table_s, row, j0, j1, lane, last_ok);
+#pragma unroll
+            for (int d = 16; d >= 1; d >>= 1) acc += __shfl_xor_sync(DGT_FULL, acc, d);
+            if (lane == 0) part[u] = acc;
+        }
+        __syncthreads();
+        for (uint32_t t = tid; t < cu / S; t += PW * 32) {
+            float y = part[t * S];
+            for (int s = 1; s < S; s++) y = y + part[t * S + s];
+            const uint64_t row = r0 + c0 / S + t;
+            if (a.y32) a.y32[row] = y;
+            if (a.y) a.y[row] = f32_to_bf16_rne(y);
+        }
+        __syncthreads();
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Bulk-copy streaming kernel (the default when cols % 32 == 0).  One CTA per
+// SM: 16 consumer warps and one producer warp.  CTA b owns rows
+// [b*N/G, (b+1)*N/G); consumer warp w takes the (row, slice) units w, w+16, ...
+// Each consumer warp owns a ring of NS shared-memory stages; lane w of the
+// producer warp keeps that ring full with 1-D bulk copies (cp.async.bulk),
+// each stage a piece of up to C rounds of one unit, its arrival counted on a
+// "full" mbarrier; the consumer releases a stage through an "empty" mbarrier.
+// So consumers only wait, decode from shared memory and multiply-add.  Every
+// wait is bounded: one that runs out sets the status word, and the warps stop
+// their work and let the copies in flight land before the CTA exits.
+// ---------------------------------------------------------------------------
+constexpr int TNW = 16;    // consumer warps
+constexpr uint32_t TNS = 3;
+constexpr uint32_t TCHUNK = 1024;  // (row, slice) units per combine chunk
+
+template <bool R4>
+struct TmaCfg;
+template <>
+struct TmaCfg<true> {
+    static constexpr uint32_t C = 4;               // rounds per piece
+    static constexpr uint32_t STAGE = 4 * 768;     // sm bytes then nibbles
+};
+template <>
+struct TmaCfg<false> {
+    static constexpr uint32_t C = 2;
+    static constexpr uint32_t STAGE = 2 * 1024;
+};
+
+struct UnitRange {
+    uint64_t row;
+    uint32_t j0, j1;
+};
+
+__device__ __forceinline__ UnitRange unit_range(uint64_t uu, uint64_t r0, uint32_t log2S, uint32_t J) {
+    UnitRange u;
+    u.row = r0 + (uu >> log2S);
+    const uint32_t s = (uint32_t)uu & ((1u << log2S) - 1u);
+    u.j0 = (s * J) >> log2S;
+    u.j1 = ((s + 1) * J) >> log2S;
+    return u;
 }
 
 template <bool R4>
-__device__ __forceinline__ float row_fast(const GemvArgs &a, const float4 *xs, uint8_t *escb,
-                                          const uint8_t *table_s, uint64_t row, uint32_t j0, uint32_t j1,
-                                          uint32_t lane) {
-    const uint64_t rbase = row * a.cols;
-    float acc = 0.0f;
-    uint32_t segb = 0, segc = 0, jbat = j0;
+__device__ __forceinline__ void issue_piece(const GemvArgs &a, uint64_t row, uint32_t j, uint32_t j1,
+                                            uint32_t stage, uint32_t bar) {
+    const uint32_t n = min(TmaCfg<R4>::C, j1 - j);
+    const uint64_t k0 = (uint64_t)j * 512;
+    const uint32_t cols = (uint32_t)(min((uint64_t)(j + n) * 512, a.cols) - k0);
+    const uint64_t f = row * a.cols + k0;
     if (R4) {
-        const uint32_t *segr = a.seg + row * a.nseg;
-        const uint32_t jj = j0 + lane;
-        if (jj < a.nseg) {
-            segb = segr[jj];
-            segc = segr[jj + 1] - segb;
-        }
+        mbar_arrive_expect_tx(bar, cols + cols / 2);
+        bulk_g2s(stage, a.sm + f, cols, bar);
+        bulk_g2s(stage + TmaCfg<R4>::C * 512, a.nib + f / 2, cols / 2, bar);
+    } else {
+        mbar_arrive_expect_tx(bar, cols * 2);
+        bulk_g2s(stage, a.W + f, cols * 2, bar);
     }
-    for (uint32_t jb = j0; jb < j1; jb += UNROLL) {
-        if (R4 && jb - jbat == 32) {
-            jbat = jb;
-            const uint32_t *segr = a.seg + row * a.nseg;
-            const uint32_t jj = jb + lane;
-            segb = segc = 0;
-            if (jj < a.nseg) {
-                segb = segr[jj];
-                segc = segr[jj + 1] - segb;
-            }
-        }
-        uint4 sv[UNROLL], wv2[UNROLL];
-        uint2 nv[UNROLL];
-        uint32_t cnt[UNROLL], sb[UNROLL], ev[UNROLL];
-#pragma unroll
-        for (int t = 0; t < UNROLL; t++) {
-            const uint32_t j = jb + t;
-            const uint64_t k0 = (uint64_t)j * 512 + 16 * lane;
-            const bool act = j < j1 && k0 < a.cols;
-            sv[t] = make_uint4(0, 0, 0, 0);
-            wv2[t] = make_uint4(0, 0, 0, 0);
-            nv[t] = make_uint2(0, 0);
-            cnt[t] = 0;
-            sb[t] = 0;
-            ev[t] = 0;
-            if (R4) {
-                if (act) {
-                    sv[t] = ldg_stream16(a.sm + rbase + k0);
-                    nv[t] = ldg_stream8(a.nib + (rbase + k0) / 2);
-                }
-                const uint32_t c = __shfl_sync(DGT_FULL, segc, (j - jbat) & 31);
-                const uint32_t b = __shfl_sync(DGT_FULL, segb, (j - jbat) & 31);
-                if (j < j1 && c) {
-                    cnt[t] = c;
-                    sb[t] = b;
-                    if (lane < c && (uint64_t)b + lane < a.n_esc) ev[t] = a.esc[b + lane];
-                }
-            } else if (act) {
-                const uint4 *src = reinterpret_cast<const uint4 *>(a.W + rbase + k0);
-                sv[t] = ldg_stream16(src);
-                wv2[t] = ldg_stream16(src + 1);
-            }
-        }
-#pragma unroll
-        for (int t = 0; t < UNROLL; t++) {
-            const uint32_t j = jb + t;
-            if (j >= j1) break;
-            const bool act = (uint64_t)j * 512 + 16 * lane < a.cols;
-            uint32_t p[8];
-            if (R4) {
-                r4_dec16(nv[t], sv[t], a.L, p);
-                if (cnt[t]) {
-                    const uint32_t c = cnt[t];
-                    if (lane < c) escb[lane] = (uint8_t)ev[t];
-                    for (uint32_t i = lane + 32; i < c && i < DGT_SEG; i += 32)
-                        escb[i] = (uint64_t)sb[t] + i < a.n_esc ? a.esc[sb[t] + i] : 0;
-                    __syncwarp();
-                    const uint32_t m0 = act ? nib15_mask(nv[t].x) : 0u;
-                    const uint32_t m1 = act ? nib15_mask(nv[t].y) : 0u;
-                    if ((!patch_escapes(p, m0, m1, c > DGT_SEG ? DGT_SEG : c, escb, table_s) ||
-                         c > DGT_SEG) && lane == 0)
-                        set_status(a.status, DGT_ERR_CORRUPT);
-                    __syncwarp();
-                }
-            } else {
-                p[0] = sv[t].x; p[1] = sv[t].y; p[2] = sv[t].z; p[3] = sv[t].w;
-                p[4] = wv2[t].x; p[5] = wv2[t].y; p[6] = wv2[t].z; p[7] = wv2[t].w;
-            }
-            if (act) acc = fma_chunk(p, xs, j, lane, acc);
-        }
-    }
-    return acc;
 }
 
-template <bool R4, int S>
-__global__ void __launch_bounds__(GW * 32) k_gemv(GemvArgs a) {
-    extern __shared__ float4 xs[];
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+template <bool R4>
+__global__ void __launch_bounds__((TNW + 1) * 32, 1) k_gemv_tma(GemvArgs a) {
+    constexpr uint32_t C = TmaCfg<R4>::C, STAGE = TmaCfg<R4>::STAGE;
+    extern __shared__ __align__(128) uint8_t dsm[];
+    __shared__ __align__(8) uint64_t full[TNW][TNS];
+    __shared__ __align__(8) uint64_t empty[TNW][TNS];
     __shared__ uint8_t table_s[256];
-    __shared__ uint8_t escb[GW][DGT_SEG];
-    __shared__ float part[GW];
+    __shared__ uint8_t escb[R4 ? TNW : 1][R4 ? DGT_SEG : 1];
+    __shared__ float part[TCHUNK];
+    __shared__ int abort_flag;
     const uint32_t tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
-    const uint32_t K = (uint32_t)a.cols;
-    for (uint32_t i = tid; i < K / 8; i += GW * 32) {
-        const uint4 v = *reinterpret_cast<const uint4 *>(a.x + 8 * i);
-        const uint32_t k = 8 * i, j = k >> 9, u = (k >> 4) & 31, q = (k >> 2) & 3;
-        xs[(j * 4 + q) * 32 + u] = make_float4(bf16lo(v.x), bf16hi(v.x), bf16lo(v.y), bf16hi(v.y));
-        xs[(j * 4 + q + 1) * 32 + u] = make_float4(bf16lo(v.z), bf16hi(v.z), bf16lo(v.w), bf16hi(v.w));
+    uint4 *xs = reinterpret_cast<uint4 *>(dsm + (size_t)TNW * TNS * STAGE);
+    const uint64_t G = gridDim.x;
+    const uint64_t r0 = (uint64_t)blockIdx.x * a.rows / G, r1 = (uint64_t)(blockIdx.x + 1) * a.rows / G;
+    const uint32_t log2S = __ffs(a.S) - 1;
+    const uint64_t units = (r1 - r0) << log2S;
+    const uint64_t nchunks = (units + TCHUNK - 1) / TCHUNK;
+    const uint32_t J = a.J;
+
+    if (tid < TNW * TNS) {
+        mbar_init(smem_u32(&full[0][0]) + 8 * tid, 1);
+        mbar_init(smem_u32(&empty[0][0]) + 8 * tid, 1);
     }
-    if (R4) table_s[tid] = a.table[tid];
+    if (tid == 0) abort_flag = 0;
+    fence_mbarrier_init();
     __syncthreads();
-    constexpr uint32_t RPB = GW / S;
-    const uint32_t rl = w / S, s = w % S;
-    const uint32_t j0 = (uint32_t)((uint64_t)s * a.J / S), j1 = (uint32_t)((uint64_t)(s + 1) * a.J / S);
-    const uint64_t groups = (a.rows + RPB - 1) / RPB;
-    for (uint64_t gi = blockIdx.x; gi < groups; gi += gridDim.x) {
-        const uint64_t row = gi * RPB + rl;
-        float acc = 0.0f;
-        if (row < a.rows) acc = row_fast<R4>(a, xs, escb[w], table_s, row, j0, j1, lane);
-#pragma unroll
-        for (int d = 16; d >= 1; d >>= 1) acc += __shfl_xor_sync(DGT_FULL, acc, d);
-        if (S == 1) {
-            if (lane == 0 && row < a.rows) {
-                if (a.y32) a.y32[row] = acc;
-                if (a.y) a.y[row] = f32_to_bf16_rne(acc);
+
+    if (w == TNW) {
+        // ---- producer warp: lane l keeps consumer warp l's ring full, chunk by chunk
+        const uint32_t ring_a = smem_u32(dsm + (size_t)(lane % TNW) * TNS * STAGE);
+        const uint32_t full_a = smem_u32(&full[lane % TNW][0]), empty_a = smem_u32(&empty[lane % TNW][0]);
+        uint32_t st = 0, uses = 0;
+        for (uint64_t ch = 0; ch < nchunks; ch++) {
+            const uint64_t c0 = ch * TCHUNK, cend = min(c0 + TCHUNK, units);
+            if (lane < TNW) {
+                for (uint64_t uu = c0 + lane; uu < cend; uu += TNW) {
+                    const UnitRange u = unit_range(uu, r0, log2S, J);
+                    for (uint32_t j = u.j0; j < u.j1; j += C) {
+                        if (*(volatile int *)&abort_flag) break;
+                        if (uses >= TNS && !mbar_wait(empty_a + 8 * st, ((uses / TNS) - 1) & 1u)) {
+                            set_status(a.status, DGT_ERR_TIMEOUT);
+                            atomicExch(&abort_flag, 1);
+                            break;
+                        }
+                        issue_piece<R4>(a, u.row, j, u.j1, ring_a + st * STAGE, full_a + 8 * st);
+                        uses++;
+                        st = st + 1 == TNS ? 0 : st + 1;
+                    }
+                }
             }
-        } else {
-            if (lane == 0) part[w] = acc;
+            __syncwarp();
             __syncthreads();
-            if (s == 0 && lane == 0 && row < a.rows) {
-                float y = part[w];
-#pragma unroll
-                for (int t = 1; t < S; t++) y = y + part[w + t];
-                if (a.y32) a.y32[row] = y;
-                if (a.y) a.y[row] = f32_to_bf16_rne(y);
-            }
             __syncthreads();
         }
+        // every copy this lane issued has landed before the CTA may exit
+        if (lane < TNW) {
+            for (uint32_t q = uses > TNS ? uses - TNS : 0; q < uses; q++)
+                mbar_wait(full_a + 8 * (q % TNS), (q / TNS) & 1u);
+        }
+        return;
+    }
+
+    // ---- consumer warps
+    const uint32_t K = (uint32_t)a.cols;
+    for (uint32_t i = tid; i < J * 64; i += TNW * 32) {
+        const uint32_t k = 8 * i, j = k >> 9, u = (k >> 4) & 31, h = (k >> 3) & 1;
+        xs[(2 * j + h) * 32 + u] = k < K ? *reinterpret_cast<const uint4 *>(a.x + k) : make_uint4(0, 0, 0, 0);
+    }
+    if (R4 && tid < 256) table_s[tid] = a.table[tid];
+    asm volatile("bar.sync 1, %0;" ::"r"(TNW * 32) : "memory");
+    const R4Lut L = a.L;
+    const uint8_t *ring = dsm + (size_t)w * TNS * STAGE;
+    const uint32_t full_a = smem_u32(&full[w][0]), empty_a = smem_u32(&empty[w][0]);
+    const uint32_t Jm1 = J - 1;
+    const bool act = 16 * lane < K - 512 * Jm1;
+    const bool cut = (K & 511) != 0;
+    uint32_t st = 0, phases = 0;
+    bool ok = true;
+    for (uint64_t ch = 0; ch < nchunks; ch++) {
+        const uint64_t c0 = ch * TCHUNK, cend = min(c0 + TCHUNK, units);
+        for (uint64_t uu = c0 + w; uu < cend; uu += TNW) {
+            const UnitRange u = unit_range(uu, r0, log2S, J);
+            SegInfo g = {0, 0, 0, 0};
+            uint32_t jbase = u.j0;
+            if (R4) g = load_seginfo(a, table_s, u.row, jbase, u.j1, lane);
+            float acc = 0.0f;
+            for (uint32_t jp = u.j0; jp < u.j1; jp += C) {
+                if (ok && *(volatile int *)&abort_flag) ok = false;
+                if (ok && !mbar_wait(full_a + 8 * st, (phases >> st) & 1u)) {
+                    ok = false;
+                    if (lane == 0) {
+                        set_status(a.status, DGT_ERR_TIMEOUT);
+                        atomicExch(&abort_flag, 1);
+                    }
+                }
+                ok = __all_sync(DGT_FULL, ok);
+                phases ^= 1u << st;
+                const uint32_t n = min(C, u.j1 - jp);
+                if (R4 && jp - jbase >= 32) {
+                    jbase = jp;
+                    g = load_seginfo(a, table_s, u.row, jbase, u.j1, lane);
+                }
+                const uint32_t pm = R4 ? g.emask >> (jp - jbase) : 0u;
+                const uint32_t rp = (cut && Jm1 - jp < n) ? Jm1 - jp : 0xFFFFFFFFu;
+                const uint8_t *stg = ring + st * STAGE;
+                if (ok) {
+#pragma unroll
+                    for (uint32_t r = 0; r < C; r++) {
+                        if (r >= n) break;
+                        const uint32_t j = jp + r;
+                        uint32_t p[8];
+                        if (R4) {
+                            const uint4 sv = *reinterpret_cast<const uint4 *>(stg + r * 512 + 16 * lane);
+                            const uint2 nv = *reinterpret_cast<const uint2 *>(stg + C * 512 + r * 256 + 8 * lane);
+                            if ((pm >> r) & 1u) {
+                                const uint32_t bit = j - jbase;
+                                const uint32_t c = __shfl_sync(DGT_FULL, g.cnt, bit);
+                                const uint32_t b = __shfl_sync(DGT_FULL, g.base, bit);
+                                const uint32_t e = __shfl_sync(DGT_FULL, g.fexp, bit);
+                                decode_with_escapes(a.esc, a.n_esc, L, nv, sv, escb[R4 ? w : 0], table_s, lane,
+                                                    r != rp || act, c, b, e, p);
+                            } else {
+                                r4_dec16(nv, sv, L, p);
+                            }
+                        } else {
+                            const uint4 lo = *reinterpret_cast<const uint4 *>(stg + r * 1024 + 32 * lane);
+                            const uint4 hi = *reinterpret_cast<const uint4 *>(stg + r * 1024 + 32 * lane + 16);
+                            p[0] = lo.x; p[1] = lo.y; p[2] = lo.z; p[3] = lo.w;
+                            p[4] = hi.x; p[5] = hi.y; p[6] = hi.z; p[7] = hi.w;
+                        }
+                        if (r == rp) {
+                            // the row's last round, cut by K: lanes past K add +0 (x there is 0 too)
+                            const uint32_t m = act ? 0xFFFFFFFFu : 0u;
+#pragma unroll
+                            for (int i = 0; i < 8; i++) p[i] &= m;
+                        }
+                        acc = fma_chunk16(p, xs, j, lane, acc);
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(empty_a + 8 * st);
+                st = st + 1 == TNS ? 0 : st + 1;
+            }
+#pragma unroll
+            for (int d = 16; d >= 1; d >>= 1) acc += __shfl_xor_sync(DGT_FULL, acc, d);
+            if (lane == 0) part[uu - c0] = acc;
+        }
+        __syncthreads();
+        const uint32_t S = 1u << log2S;
+        for (uint32_t t = tid; t < (cend - c0) / S; t += TNW * 32) {
+            float y = part[t * S];
+            for (uint32_t s = 1; s < S; s++) y = y + part[t * S + s];
+            const uint64_t row = r0 + c0 / S + t;
+            if (a.y32) a.y32[row] = y;
+            if (a.y) a.y[row] = f32_to_bf16_rne(y);
+        }
+        __syncthreads();
     }
 }
 
@@ -261,39 +607,45 @@ __global__ void __launch_bounds__(GW * 32) k_gemv_any(GemvArgs a, int S) {
 }
 
 template <bool R4>
-int launch_gemv(GemvArgs &a, bool fast, cudaStream_t st) {
+int launch_gemv(GemvArgs &a, int path, cudaStream_t st) {
     DeviceInfo di;
     if (device_info(&di) != DGT_OK) return DGT_ERR_CUDA;
-    const int S = dgt_plan_slices(a.rows, a.cols);
-    const uint64_t groups = (a.rows + (GW / S) - 1) / (GW / S);
+    a.S = dgt_plan_slices(a.rows, a.cols);
     int bps = 0;
-    if (!fast) {
+    if (path == 2) {
+        const size_t smem = (size_t)TNW * TNS * TmaCfg<R4>::STAGE + (size_t)a.J * 1024;
+        if (prepare_kernel((const void *)k_gemv_tma<R4>, smem, (TNW + 1) * 32, &bps) != DGT_OK) return DGT_ERR_CUDA;
+        const unsigned grid = (unsigned)min((uint64_t)di.sms, a.rows);
+        k_gemv_tma<R4><<<grid, (TNW + 1) * 32, smem, st>>>(a);
+    } else if (path == 1) {
+        const size_t smem = (size_t)a.J * 1024;
+        if (prepare_kernel((const void *)k_gemv<R4, 16, 4>, smem, 16 * 32, &bps) != DGT_OK) return DGT_ERR_CUDA;
+        const unsigned grid = (unsigned)min((uint64_t)di.sms, a.rows);
+        k_gemv<R4, 16, 4><<<grid, 16 * 32, smem, st>>>(a);
+    } else {
+        const uint64_t groups = (a.rows + (GW / a.S) - 1) / (GW / a.S);
         if (prepare_kernel((const void *)k_gemv_any<R4>, 0, GW * 32, &bps) != DGT_OK) return DGT_ERR_CUDA;
         const uint64_t grid = min((uint64_t)di.sms * bps, groups);
-        k_gemv_any<R4><<<(unsigned)grid, GW * 32, 0, st>>>(a, S);
-    } else {
-        const size_t smem = (size_t)a.J * 2048;
-        const void *fn = S == 1   ? (const void *)k_gemv<R4, 1>
-                         : S == 2 ? (const void *)k_gemv<R4, 2>
-                         : S == 4 ? (const void *)k_gemv<R4, 4>
-                                  : (const void *)k_gemv<R4, 8>;
-        if (prepare_kernel(fn, smem, GW * 32, &bps) != DGT_OK) return DGT_ERR_CUDA;
-        const unsigned grid = (unsigned)min((uint64_t)di.sms * bps, groups);
-        switch (S) {
-            case 1: k_gemv<R4, 1><<<grid, GW * 32, smem, st>>>(a); break;
-            case 2: k_gemv<R4, 2><<<grid, GW * 32, smem, st>>>(a); break;
-            case 4: k_gemv<R4, 4><<<grid, GW * 32, smem, st>>>(a); break;
-            default: k_gemv<R4, 8><<<grid, GW * 32, smem, st>>>(a); break;
-        }
+        k_gemv_any<R4><<<(unsigned)grid, GW * 32, 0, st>>>(a, a.S);
     }
     return cudaPeekAtLastError() == cudaSuccess ? DGT_OK : DGT_ERR_CUDA;
+}
+
+// 2: bulk-copy kernel, 1: register-streaming kernel, 0: any-shape kernel.
+template <bool R4>
+int choose_path(uint64_t K, uint32_t J, bool aligned) {
+    if (K == 0 || K % 16 != 0 || !aligned) return 0;
+    const size_t tma_smem = (size_t)TNW * TNS * TmaCfg<R4>::STAGE + (size_t)J * 1024;
+    if (K % 32 == 0 && tma_smem <= 200 * 1024) return 2;
+    return J <= MAX_FAST_ROUNDS ? 1 : 0;
 }
 
 }  // namespace dgt
 
 using namespace dgt;
 
-extern "C" int dgt_gemv(const dgt_r4 *W, const uint16_t *d_x, uint16_t *d_y, float *d_y32, void *stream) {
+extern "C" int dgt_gemv(const dgt_r4 *W, const uint16_t *d_x, uint16_t *d_y, float *d_y32, int32_t *d_status,
+                        void *stream) {
     if (!W) return DGT_ERR_ARG;
     const uint64_t N = W->rows, K = W->cols;
     if (K >= (1ull << 31) || (N && (N * K) / N != K)) return DGT_ERR_SHAPE;
@@ -315,14 +667,13 @@ extern "C" int dgt_gemv(const dgt_r4 *W, const uint16_t *d_x, uint16_t *d_y, flo
     a.J = (uint32_t)((K + 511) / 512);
     a.L = make_r4lut(W->table, W->n_table);
     for (int i = 0; i < 256; i++) a.table[i] = W->table[i];
-    a.status = nullptr;
-    const bool fast = K > 0 && K % 16 == 0 && a.J <= MAX_FAST_ROUNDS && aligned16(W->sm) &&
-                      aligned16(W->nib) && aligned16(d_x);
-    return launch_gemv<true>(a, fast, (cudaStream_t)stream);
+    a.status = d_status;
+    const int path = choose_path<true>(K, a.J, aligned16(W->sm) && aligned16(W->nib) && aligned16(d_x));
+    return launch_gemv<true>(a, path, (cudaStream_t)stream);
 }
 
 extern "C" int dgt_gemv_bf16(const uint16_t *d_W, uint64_t rows, uint64_t cols, const uint16_t *d_x,
-                             uint16_t *d_y, float *d_y32, void *stream) {
+                             uint16_t *d_y, float *d_y32, int32_t *d_status, void *stream) {
     const uint64_t N = rows, K = cols;
     if (K >= (1ull << 31) || (N && (N * K) / N != K)) return DGT_ERR_SHAPE;
     if (N == 0) return DGT_OK;
@@ -330,12 +681,13 @@ extern "C" int dgt_gemv_bf16(const uint16_t *d_W, uint64_t rows, uint64_t cols, 
     if (K && (!d_x || !d_W)) return DGT_ERR_ARG;
     GemvArgs a = {};
     a.W = d_W;
+    a.status = d_status;
     a.x = d_x;
     a.y = d_y;
     a.y32 = d_y32;
     a.rows = N;
     a.cols = K;
     a.J = (uint32_t)((K + 511) / 512);
-    const bool fast = K > 0 && K % 16 == 0 && a.J <= MAX_FAST_ROUNDS && aligned16(d_W) && aligned16(d_x);
-    return launch_gemv<false>(a, fast, (cudaStream_t)stream);
+    const int path = choose_path<false>(K, a.J, aligned16(d_W) && aligned16(d_x));
+    return launch_gemv<false>(a, path, (cudaStream_t)stream);
 }

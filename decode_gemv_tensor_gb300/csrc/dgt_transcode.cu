@@ -394,11 +394,11 @@ __global__ void __launch_bounds__(TW * 32) k_f1_to_r4(F1Args a) {
                             bad = true;
                         }
                         ei++;
-                        if (r >= 15) {
-                            if (ec < LIST) S.list[w][lane][ec] = (uint16_t)((s << 8) | r);
-                            ec++;
-                            if (s < 64) em0 |= 1ull << s; else em1 |= 1ull << (s - 64);
-                        }
+                    }
+                    if (r >= 15 && s < cnt) {
+                        if (ec < LIST) S.list[w][lane][ec] = (uint16_t)((s << 8) | r);
+                        ec++;
+                        if (s < 64) em0 |= 1ull << s; else em1 |= 1ull << (s - 64);
                     }
                     if (s >= cnt) r = 0;
                     word |= (r < 15 ? r : 15u) << (4 * i);
@@ -432,11 +432,13 @@ __global__ void __launch_bounds__(TW * 32) k_f1_to_r4(F1Args a) {
                 for (uint32_t s = 0; s < cnt; s++) {
                     uint64_t v = load_bits64(S.pay[w], toff + (s / 8) * wd);
                     uint32_t c = (uint32_t)(v >> ((s % 8) * wd)) & top;
-                    if (c == top && ej < ge1) {
-                        uint32_t r = e1staged ? S.e1[w][ej] : a.esc1[e10 + ej];
+                    uint32_t r = c;
+                    if (c == top) {
+                        r = 0;
+                        if (ej < ge1) r = e1staged ? S.e1[w][ej] : a.esc1[e10 + ej];
                         ej++;
-                        if (r >= 15) a.esc[dst++] = (uint8_t)r;
                     }
+                    if (r >= 15) a.esc[dst++] = (uint8_t)r;
                 }
             }
         }

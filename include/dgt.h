@@ -240,7 +240,7 @@ int dgt_read_status(const int32_t *d_status, void *stream, int32_t *status);
  * [floor(s*J/S), floor((s+1)*J/S)), J = ceil(K/512), and
  * y = ((P_0 + P_1) + ...) + P_(S-1).  y_bf16 is y rounded to nearest-even
  * (NaN -> 0x7FC0).  dgt_gemv_slices() is the plan S(N, K): the smallest power
- * of two >= ceil(2432/N), capped at 8 and at the largest power of two <= J.
+ * of two >= ceil(16384/N), capped at 8 and at the largest power of two <= J.
  */
 int dgt_gemv_slices(uint64_t rows, uint64_t cols);
 
@@ -248,14 +248,18 @@ int dgt_gemv_slices(uint64_t rows, uint64_t cols);
  * y = W x with W in R4 (Binade README, "Results": "Matvec kernel"; "How it
  * works": "its matvec streams at full bandwidth").  d_x: device, cols bf16.
  * d_y: device, rows bf16 (may be NULL).  d_y32: device, rows float (may be
- * NULL).  Asynchronous.  Errors: DGT_ERR_ARG, DGT_ERR_SHAPE (cols >= 2^31),
- * DGT_ERR_CUDA.
+ * NULL; not both).  d_status: device int32 or NULL; a kernel whose bounded
+ * wait for its streamed data runs out writes DGT_ERR_TIMEOUT there (the
+ * word is never cleared by this call).  W must come from dgt_load_r4 (its
+ * escape index is trusted).  Asynchronous.  Errors: DGT_ERR_ARG,
+ * DGT_ERR_SHAPE (cols >= 2^31), DGT_ERR_CUDA.
  */
-int dgt_gemv(const dgt_r4 *W, const uint16_t *d_x, uint16_t *d_y, float *d_y32, void *stream);
+int dgt_gemv(const dgt_r4 *W, const uint16_t *d_x, uint16_t *d_y, float *d_y32, int32_t *d_status,
+             void *stream);
 
 /* The same product and order with plain BF16 weights d_W [rows, cols]. */
 int dgt_gemv_bf16(const uint16_t *d_W, uint64_t rows, uint64_t cols, const uint16_t *d_x,
-                  uint16_t *d_y, float *d_y32, void *stream);
+                  uint16_t *d_y, float *d_y32, int32_t *d_status, void *stream);
 
 #ifdef __cplusplus
 }
