@@ -84,6 +84,11 @@ def lib():
             "dgt_gemv_slices": (i32, [u64, u64]),
             "dgt_gemv": (i32, [C.POINTER(R4Struct), vp, vp, vp, vp, vp]),
             "dgt_gemv_bf16": (i32, [vp, u64, u64, vp, vp, vp, vp, vp]),
+            "dgt_moe_workspace_bytes": (C.c_size_t, [C.c_uint32, u64, u64, C.c_uint32, C.c_uint32]),
+            "dgt_moe_gemv": (i32, [C.POINTER(R4Struct), C.c_uint32, vp, vp, C.c_uint32, C.c_uint32, vp, vp, vp,
+                                   vp, vp, C.c_size_t, vp, vp]),
+            "dgt_moe_gemv_bf16": (i32, [vp, u64, u64, C.c_uint32, vp, vp, C.c_uint32, C.c_uint32, vp, vp, vp,
+                                        vp, vp, C.c_size_t, vp, vp]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -328,3 +333,53 @@ def gemv_bf16(W, x, y=None, y32=None, status=None, stream=None):
     _check(lib().dgt_gemv_bf16(_ptr(W), rows, cols, _ptr(x), _ptr(y), _ptr(y32), _ptr(status), _stream(stream)),
            "dgt_gemv_bf16")
     return y, y32
+
+
+def moe_workspace_bytes(n_experts: int, expert_rows: int, cols: int, tokens: int, topk: int) -> int:
+    return int(lib().dgt_moe_workspace_bytes(n_experts, expert_rows, cols, tokens, topk))
+
+
+def _moe_outputs(tokens, topk, ne, dev, want_y, want_out, y32, out, out32):
+    import torch
+    if want_y and y32 is None:
+        y32 = torch.empty((tokens, topk, ne), dtype=torch.float32, device=dev)
+    if want_out and out is None:
+        out = torch.empty((tokens, ne), dtype=torch.bfloat16, device=dev)
+    if want_out and out32 is None:
+        out32 = torch.empty((tokens, ne), dtype=torch.float32, device=dev)
+    return y32, out, out32
+
+
+def moe_gemv(W: R4, n_experts: int, ids, p, x, ws=None, y32=None, out=None, out32=None, status=None,
+             stream=None, want_y=True):
+    """dgt_moe_gemv: expert gather with stacked R4 experts.  ids int32 [T, topk],
+    p float32 [T, topk] or None, x bf16 [T, K].  Returns (y32, out, out32)."""
+    import torch
+    tokens, topk = ids.shape
+    ne = W.rows // n_experts
+    dev = W.sm.device
+    y32, out, out32 = _moe_outputs(tokens, topk, ne, dev, want_y, p is not None, y32, out, out32)
+    nb = moe_workspace_bytes(n_experts, ne, W.cols, tokens, topk)
+    if ws is None:
+        ws = torch.empty(max(nb, 256), dtype=torch.uint8, device=dev)
+    _check(lib().dgt_moe_gemv(C.byref(W.s), n_experts, _ptr(ids), _ptr(p), tokens, topk, _ptr(x), _ptr(y32),
+                              _ptr(out), _ptr(out32), _ptr(ws), ws.numel(), _ptr(status), _stream(stream)),
+           "dgt_moe_gemv")
+    return y32, out, out32
+
+
+def moe_gemv_bf16(W, n_experts: int, ids, p, x, ws=None, y32=None, out=None, out32=None, status=None,
+                  stream=None, want_y=True):
+    """dgt_moe_gemv_bf16: the same gather with stacked bf16 experts W [E*Ne, K]."""
+    import torch
+    tokens, topk = ids.shape
+    rows, cols = W.shape
+    ne = rows // n_experts
+    y32, out, out32 = _moe_outputs(tokens, topk, ne, W.device, want_y, p is not None, y32, out, out32)
+    nb = moe_workspace_bytes(n_experts, ne, cols, tokens, topk)
+    if ws is None:
+        ws = torch.empty(max(nb, 256), dtype=torch.uint8, device=W.device)
+    _check(lib().dgt_moe_gemv_bf16(_ptr(W), rows, cols, n_experts, _ptr(ids), _ptr(p), tokens, topk, _ptr(x),
+                                   _ptr(y32), _ptr(out), _ptr(out32), _ptr(ws), ws.numel(), _ptr(status),
+                                   _stream(stream)), "dgt_moe_gemv_bf16")
+    return y32, out, out32

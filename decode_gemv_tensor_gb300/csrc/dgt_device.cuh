@@ -157,6 +157,37 @@ __device__ __forceinline__ void ldg_stream32(const void *p, uint4 &lo, uint4 &hi
         : "l"(p));
 }
 
+// Two fused multiply-adds in column order, the bf16 operands taken straight
+// from the low and high halves of w and x: acc = fma(w.lo, x.lo, acc), then
+// acc = fma(w.hi, x.hi, acc).  Each is one fp32 FMA with a single rounding.
+__device__ __forceinline__ float fma2_bf16(uint32_t w, uint32_t x, float acc) {
+    asm("{\n\t.reg .b16 a0, a1, b0, b1;\n\t"
+        "mov.b32 {a0, a1}, %1;\n\t"
+        "mov.b32 {b0, b1}, %2;\n\t"
+        "fma.rn.f32.bf16 %0, a0, b0, %0;\n\t"
+        "fma.rn.f32.bf16 %0, a1, b1, %0;\n\t}"
+        : "+f"(acc)
+        : "r"(w), "r"(x));
+    return acc;
+}
+
+// Lane chunk of 16 weights (eight bf16 pairs) against x staged as bf16 pairs:
+// round j, lane u -> two uint4 at [(2j + h) * 32 + u].
+__device__ __forceinline__ float fma_chunk16(const uint32_t p[8], const uint4 *xs, uint32_t j, uint32_t lane,
+                                             float acc) {
+    const uint4 xa = xs[(2 * j) * 32 + lane];
+    const uint4 xb = xs[(2 * j + 1) * 32 + lane];
+    acc = fma2_bf16(p[0], xa.x, acc);
+    acc = fma2_bf16(p[1], xa.y, acc);
+    acc = fma2_bf16(p[2], xa.z, acc);
+    acc = fma2_bf16(p[3], xa.w, acc);
+    acc = fma2_bf16(p[4], xb.x, acc);
+    acc = fma2_bf16(p[5], xb.y, acc);
+    acc = fma2_bf16(p[6], xb.z, acc);
+    acc = fma2_bf16(p[7], xb.w, acc);
+    return acc;
+}
+
 // ---- mbarrier and bulk-copy (TMA, 1-D) helpers --------------------------------
 __device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
 

@@ -261,6 +261,40 @@ int dgt_gemv(const dgt_r4 *W, const uint16_t *d_x, uint16_t *d_y, float *d_y32, 
 int dgt_gemv_bf16(const uint16_t *d_W, uint64_t rows, uint64_t cols, const uint16_t *d_x,
                   uint16_t *d_y, float *d_y32, int32_t *d_status, void *stream);
 
+/* ------------------------------------------------------------------------ */
+/* Mixture-of-experts expert gather                                         */
+/* ------------------------------------------------------------------------ */
+/*
+ * Binade README, "How it works" (Exactness: "the matvec, the MoE expert
+ * gather and the GEMM" follow one order) and "Limitations" ("every expert
+ * product").  W stacks the experts of one projection as one R4 tensor
+ * [n_experts * Ne, K] (one rank table).  For token t < tokens and slot
+ * j < topk, y[t, j, :] = W[ids[t, j]] x_t in the order of dgt_gemv with the
+ * plan S(Ne, K); with routing weights p (may be NULL),
+ * out[t, :] = fmaf(p[t, topk-1], y[t, topk-1, :], ... fmaf(p[t, 0], y[t, 0, :], +0)).
+ * d_ids: device int32 [tokens, topk], each in [0, n_experts) (others set
+ * DGT_ERR_ARG in the status word and leave their outputs undefined).
+ * d_p: device float [tokens, topk] or NULL.  d_x: device bf16 [tokens, K].
+ * d_y32: device float [tokens, topk, Ne] or NULL.  d_out / d_out32: device
+ * bf16 / float [tokens, Ne] or NULL (written only when d_p is given).
+ * d_ws: device workspace of dgt_moe_workspace_bytes() bytes, 256-byte
+ * aligned, caller-owned, contents need not be initialised.  d_status: device
+ * int32, set to 0 then to an error code.  Limits: K % 16 == 0, topk <= 255,
+ * tokens * topk <= 65536, tokens * ceil(K/512) KB of x <= 160 KB,
+ * n_experts <= 4096.  Asynchronous.
+ */
+size_t dgt_moe_workspace_bytes(uint32_t n_experts, uint64_t expert_rows, uint64_t cols, uint32_t tokens,
+                               uint32_t topk);
+int dgt_moe_gemv(const dgt_r4 *W, uint32_t n_experts, const int32_t *d_ids, const float *d_p, uint32_t tokens,
+                 uint32_t topk, const uint16_t *d_x, float *d_y32, uint16_t *d_out, float *d_out32, void *d_ws,
+                 size_t ws_bytes, int32_t *d_status, void *stream);
+
+/* The same gather and order with plain BF16 stacked weights d_W [rows, cols]. */
+int dgt_moe_gemv_bf16(const uint16_t *d_W, uint64_t rows, uint64_t cols, uint32_t n_experts,
+                      const int32_t *d_ids, const float *d_p, uint32_t tokens, uint32_t topk,
+                      const uint16_t *d_x, float *d_y32, uint16_t *d_out, float *d_out32, void *d_ws,
+                      size_t ws_bytes, int32_t *d_status, void *stream);
+
 #ifdef __cplusplus
 }
 #endif
