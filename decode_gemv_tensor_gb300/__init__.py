@@ -89,6 +89,8 @@ def lib():
                                    vp, vp, C.c_size_t, vp, vp]),
             "dgt_moe_gemv_bf16": (i32, [vp, u64, u64, C.c_uint32, vp, vp, C.c_uint32, C.c_uint32, vp, vp, vp,
                                         vp, vp, C.c_size_t, vp, vp]),
+            "dgt_moe_gemv_noalloc": (i32, [C.POINTER(R4Struct), C.c_uint32, vp, vp, C.c_uint32, C.c_uint32, vp,
+                                           vp, vp, vp, vp, vp]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)

@@ -333,3 +333,54 @@ extern "C" int dgt_moe_gemv_bf16(const uint16_t *d_W, uint64_t rows, uint64_t co
     a.out32 = d_out32;
     return launch_moe<false>(a, d_ws, ws_bytes, st);
 }
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant of dgt_moe_gemv.
+//
+// Some callers cannot allocate device memory when they call: a plugin running
+// inside a host framework that owns the whole device memory pool, or a
+// latency-critical decode loop where a cudaMalloc (which may synchronise the
+// device) is not allowed.  This entry point keeps its workspace in a fixed
+// array that lives in the library's own device image, so it never calls
+// cudaMalloc, cudaFree or any allocating routine.
+//
+// The array is DGT_MOE_NOALLOC_SCRATCH_BYTES large and every GPU that loads
+// the library holds it until the process exits.  Host code cannot use the
+// array's name as a device address (it is only a host-side stand-in), so the
+// first call on each device, with that device current, looks the address up
+// with cudaGetSymbolAddress and caches it; make that first call before any
+// stream capture.  All calls share the one array and it keeps the last call's
+// contents: nothing in it needs to start at zero (the routing kernel rewrites
+// every list and count, and every partial sum is written before it is read),
+// but calls that overlap on the GPU -- on different streams, or on
+// different host threads at once -- race on it.
+// ---------------------------------------------------------------------------
+static __device__ __align__(256) uint8_t g_moe_scratch[DGT_MOE_NOALLOC_SCRATCH_BYTES];
+
+static int moe_scratch_address(void **out) {
+    static void *cached[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return DGT_ERR_CUDA;
+    if (!cached[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_moe_scratch) != cudaSuccess || !p) return DGT_ERR_CUDA;
+        cached[dev] = p;
+    }
+    *out = cached[dev];
+    return DGT_OK;
+}
+
+extern "C" int dgt_moe_gemv_noalloc(const dgt_r4 *W, uint32_t n_experts, const int32_t *d_ids, const float *d_p,
+                                    uint32_t tokens, uint32_t topk, const uint16_t *d_x, float *d_y32,
+                                    uint16_t *d_out, float *d_out32, int32_t *d_status, void *stream) {
+    if (!W || n_experts == 0) return DGT_ERR_ARG;
+    if (W->rows % n_experts) return DGT_ERR_SHAPE;
+    if (tokens == 0) return DGT_OK;
+    const size_t need = dgt_moe_workspace_bytes(n_experts, W->rows / n_experts, W->cols, tokens, topk);
+    if (need > DGT_MOE_NOALLOC_SCRATCH_BYTES) return DGT_ERR_SHAPE;
+    void *ws = nullptr;
+    const int rc = moe_scratch_address(&ws);
+    if (rc != DGT_OK) return rc;
+    return dgt_moe_gemv(W, n_experts, d_ids, d_p, tokens, topk, d_x, d_y32, d_out, d_out32, ws,
+                        DGT_MOE_NOALLOC_SCRATCH_BYTES, d_status, stream);
+}

@@ -295,6 +295,28 @@ int dgt_moe_gemv_bf16(const uint16_t *d_W, uint64_t rows, uint64_t cols, uint32_
                       const uint16_t *d_x, float *d_y32, uint16_t *d_out, float *d_out32, void *d_ws,
                       size_t ws_bytes, int32_t *d_status, void *stream);
 
+/*
+ * Allocation-free expert gather.  The paper has no counterpart: this entry
+ * point exists for callers that cannot allocate device memory when they call
+ * -- a plugin inside a host framework that owns the whole device memory pool,
+ * or a latency-critical decode loop where a cudaMalloc (which may synchronise
+ * the device) is not allowed.  It computes exactly what dgt_moe_gemv computes,
+ * with the same arguments minus the workspace, which it takes from a fixed
+ * DGT_MOE_NOALLOC_SCRATCH_BYTES array inside the library's device image
+ * (every GPU that loads the library holds that memory until the process
+ * exits).  It never calls cudaMalloc, cudaFree or any allocating routine.
+ * The first call on each device (with that device current) looks up the
+ * array's device address; make that first call before any stream capture.
+ * All calls share the array and it keeps the last call's contents; nothing in
+ * it must start at zero, but calls that overlap on the GPU race on it.
+ * Errors: as dgt_moe_gemv, plus DGT_ERR_SHAPE when the workspace this call
+ * needs (dgt_moe_workspace_bytes) exceeds DGT_MOE_NOALLOC_SCRATCH_BYTES.
+ */
+#define DGT_MOE_NOALLOC_SCRATCH_BYTES (4u << 20)
+int dgt_moe_gemv_noalloc(const dgt_r4 *W, uint32_t n_experts, const int32_t *d_ids, const float *d_p,
+                         uint32_t tokens, uint32_t topk, const uint16_t *d_x, float *d_y32, uint16_t *d_out,
+                         float *d_out32, int32_t *d_status, void *stream);
+
 #ifdef __cplusplus
 }
 #endif
