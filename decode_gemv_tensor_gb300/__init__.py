@@ -51,6 +51,10 @@ class R4Struct(C.Structure):
     ]
 
 
+class GemmPlan(C.Structure):
+    _fields_ = [("m_tile", C.c_int32), ("split_k", C.c_int32), ("reserved0", C.c_int32), ("reserved1", C.c_int32)]
+
+
 _lib = None
 
 
@@ -84,6 +88,10 @@ def lib():
             "dgt_gemv_slices": (i32, [u64, u64]),
             "dgt_gemv": (i32, [C.POINTER(R4Struct), vp, vp, vp, vp, vp]),
             "dgt_gemv_bf16": (i32, [vp, u64, u64, vp, vp, vp, vp, vp]),
+            "dgt_gemm_default_plan": (i32, [u64, u64, u64, C.POINTER(GemmPlan)]),
+            "dgt_gemm_workspace_bytes": (C.c_size_t, [u64, u64, C.POINTER(GemmPlan)]),
+            "dgt_gemm": (i32, [C.POINTER(R4Struct), vp, u64, vp, vp, C.POINTER(GemmPlan), vp, C.c_size_t, vp, vp]),
+            "dgt_gemm_bf16": (i32, [vp, u64, u64, vp, u64, vp, vp, C.POINTER(GemmPlan), vp, C.c_size_t, vp, vp]),
             "dgt_moe_workspace_bytes": (C.c_size_t, [C.c_uint32, u64, u64, C.c_uint32, C.c_uint32]),
             "dgt_moe_gemv": (i32, [C.POINTER(R4Struct), C.c_uint32, vp, vp, C.c_uint32, C.c_uint32, vp, vp, vp,
                                    vp, vp, C.c_size_t, vp, vp]),
@@ -385,3 +393,48 @@ def moe_gemv_bf16(W, n_experts: int, ids, p, x, ws=None, y32=None, out=None, out
                                    _ptr(y32), _ptr(out), _ptr(out32), _ptr(ws), ws.numel(), _ptr(status),
                                    _stream(stream)), "dgt_moe_gemv_bf16")
     return y32, out, out32
+
+
+def gemm_plan(M: int, N: int, K: int, m_tile=None, split_k=None) -> GemmPlan:
+    """dgt_gemm_default_plan, optionally overridden."""
+    p = GemmPlan()
+    _check(lib().dgt_gemm_default_plan(M, N, K, C.byref(p)), "dgt_gemm_default_plan")
+    if m_tile is not None:
+        p.m_tile = m_tile
+    if split_k is not None:
+        p.split_k = split_k
+    return p
+
+
+def _gemm_out(M, N, dev, Y32, Y, plan, ws):
+    import torch
+    if Y32 is None:
+        Y32 = torch.empty((M, N), dtype=torch.float32, device=dev)
+    if Y is None:
+        Y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    nb = int(lib().dgt_gemm_workspace_bytes(M, N, C.byref(plan)))
+    if ws is None and nb:
+        ws = torch.empty(nb, dtype=torch.uint8, device=dev)
+    return Y32, Y, ws
+
+
+def gemm(W: R4, X, plan=None, Y32=None, Y=None, ws=None, status=None, stream=None):
+    """dgt_gemm: Y = X W^T on tcgen05 with W in R4; X bf16 [M, K].  Returns (Y32, Y)."""
+    M, K = X.shape
+    N = W.rows
+    plan = plan or gemm_plan(M, N, K)
+    Y32, Y, ws = _gemm_out(M, N, W.sm.device, Y32, Y, plan, ws)
+    _check(lib().dgt_gemm(C.byref(W.s), _ptr(X), M, _ptr(Y32), _ptr(Y), C.byref(plan), _ptr(ws),
+                          0 if ws is None else ws.numel(), _ptr(status), _stream(stream)), "dgt_gemm")
+    return Y32, Y
+
+
+def gemm_bf16(W, X, plan=None, Y32=None, Y=None, ws=None, status=None, stream=None):
+    """dgt_gemm_bf16: the same product, tiles, split and order with bf16 weights W [N, K]."""
+    M, K = X.shape
+    N = W.shape[0]
+    plan = plan or gemm_plan(M, N, K)
+    Y32, Y, ws = _gemm_out(M, N, W.device, Y32, Y, plan, ws)
+    _check(lib().dgt_gemm_bf16(_ptr(W), N, K, _ptr(X), M, _ptr(Y32), _ptr(Y), C.byref(plan), _ptr(ws),
+                               0 if ws is None else ws.numel(), _ptr(status), _stream(stream)), "dgt_gemm_bf16")
+    return Y32, Y

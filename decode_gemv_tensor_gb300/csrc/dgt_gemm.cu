@@ -1,0 +1,487 @@
+// dgt_gemm.cu -- prompt products Y = X W^T on the 5th-generation tensor cores
+// (tcgen05, accumulators in tensor memory), with W in R4 decoded in the
+// producer (or plain BF16 for the twin).
+//
+// Binade README, "Results" (prompt matmuls at 16 to 2048 rows), "NVIDIA GPUs"
+// (each output is a sequence of tensor-core MMA steps along K; split-K
+// partitions follow a fixed rule) and "How it works" (Exactness: the GEMM
+// mirrors the BF16 kernel step for step).  The R4 GEMM and the BF16 GEMM of
+// this file issue the same MMA instructions on byte-identical shared-memory
+// tiles with the same split and the same reduction order, so their outputs
+// are bit-identical; against exact arithmetic the fp32 result is checked
+// normwise.
+//
+// Design (cta_group::1, one CTA of 8 warps per tile):
+//  - Swap-AB: the 128-row W tile is operand A (M = 128), the X tile is operand
+//    B (N = mt in 16..256), the fp32 accumulator D = W x X^T lives in tensor
+//    memory: lane = W row, column = X row.
+//  - Operands are K-major SWIZZLE_128B tiles of 64 bf16 along K.  X (and W
+//    for the twin) arrive by 2-D TMA.  For R4, 2-D TMA stages the raw
+//    sign/mantissa and nibble tiles and warps 4..7 (one thread per W row)
+//    decode them into the same swizzled layout the TMA would write, with a
+//    running per-row escape index.
+//  - Warp 0 lane 0 issues TMA, warp 1 lane 0 issues tcgen05.mma (four K=16
+//    steps per 64-wide stage) and commits each stage back to the producer;
+//    warps 4..7 read the accumulator with tcgen05.ld and write Y (or the
+//    split-K partial).  A second kernel adds the split partials in slice
+//    order.
+//  - Every mbarrier wait is bounded; on a timeout the CTA raises an abort
+//    flag, records DGT_ERR_TIMEOUT, lets its copies land and frees its tensor
+//    memory before returning.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include "../../include/dgt.h"
+#include "dgt_device.cuh"
+#include "dgt_launch.h"
+
+namespace dgt {
+
+constexpr uint32_t GT_N = 128;      // W rows per tile (MMA M)
+constexpr uint32_t GT_K = 64;       // bf16 columns per stage (one 128-byte swizzle row)
+constexpr uint32_t GT_MAXP = 8;     // pipeline stages, upper bound
+constexpr uint32_t GT_SMEM_LIMIT = 200 * 1024;
+
+struct GemmArgs {
+    const uint8_t *nib, *esc;
+    const uint32_t *seg;
+    uint64_t n_esc, nseg;
+    uint64_t M, N, K;
+    uint32_t mt, kb_total, split, stages;
+    float *y32;
+    uint16_t *y;
+    float *partial;
+    int32_t *status;
+    R4Lut L;
+    uint8_t table[256];
+};
+
+// ---- tcgen05 / TMA wrappers -------------------------------------------------
+__device__ __forceinline__ void tmem_alloc(uint32_t slot_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_smem), "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.u32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint32_t mbar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(mbar)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t r[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, uint32_t mbar, int32_t x,
+                                            int32_t y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], "
+        "[%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(mbar), "r"(x), "r"(y)
+        : "memory");
+}
+
+// Shared-memory matrix descriptor: K-major, SWIZZLE_128B, 8-row core groups
+// 1024 bytes apart (stride byte offset), leading byte offset unused (16),
+// descriptor version 1 for tcgen05.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFF);
+    d |= (uint64_t)(16 >> 4) << 16;
+    d |= (uint64_t)(1024 >> 4) << 32;
+    d |= 1ull << 46;
+    d |= 2ull << 61;
+    return d;
+}
+
+// Instruction descriptor for kind::f16: D fp32, A and B bf16, both K-major,
+// N = n columns, M = 128.
+__host__ __device__ constexpr uint32_t idesc_bf16(uint32_t n) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((n >> 3) << 17) | ((128u >> 4) << 24);
+}
+
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int *abort_flag) {
+    for (uint32_t i = 0; i < MBAR_SPIN_LIMIT; i++) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 63) == 63 && *abort_flag) return false;
+    }
+    return false;
+}
+
+__host__ __device__ inline uint32_t gemm_stage_bytes(bool r4, uint32_t mt) {
+    return GT_N * 128 + mt * 128 + (r4 ? GT_N * 64 + GT_N * 32 : 0);
+}
+
+// Decode one W row's 64 weights of a stage from the raw tiles into its
+// swizzled bf16 row; escapes come from the running index eidx.
+__device__ __forceinline__ void decode_row64(const GemmArgs &a, const uint8_t *raw_sm, const uint8_t *raw_nib,
+                                             uint8_t *arow, uint32_t t, uint64_t &eidx, const uint8_t *table_s,
+                                             bool &bad) {
+#pragma unroll
+    for (uint32_t q = 0; q < 4; q++) {
+        const uint4 sv = *reinterpret_cast<const uint4 *>(raw_sm + q * 16);
+        const uint2 nv = *reinterpret_cast<const uint2 *>(raw_nib + q * 8);
+        uint32_t p[8];
+        r4_dec16(nv, sv, a.L, p);
+        const uint32_t m0 = nib15_mask(nv.x), m1 = nib15_mask(nv.y);
+        if (m0 | m1) {
+#pragma unroll
+            for (int i = 0; i < 16; i++) {
+                const uint32_t m = i < 8 ? m0 : m1;
+                if ((m >> (4 * (i & 7))) & 1u) {
+                    uint32_t e = 0;
+                    if (eidx < a.n_esc) e = table_s[a.esc[eidx]];
+                    else bad = true;
+                    eidx++;
+                    const uint32_t sh = 16 * (i & 1);
+                    p[i >> 1] = (p[i >> 1] & ~(0x7F80u << sh)) | (e << (7 + sh));
+                }
+            }
+        }
+        // 16-byte chunks 2q and 2q+1 of the row, at their swizzled positions
+        const uint32_t c0 = (2 * q) ^ (t & 7), c1 = (2 * q + 1) ^ (t & 7);
+        *reinterpret_cast<uint4 *>(arow + c0 * 16) = make_uint4(p[0], p[1], p[2], p[3]);
+        *reinterpret_cast<uint4 *>(arow + c1 * 16) = make_uint4(p[4], p[5], p[6], p[7]);
+    }
+}
+
+template <bool R4>
+__global__ void __launch_bounds__(256, 1)
+    k_gemm(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
+           const __grid_constant__ CUtensorMap tm_nib, GemmArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t bar_full[GT_MAXP], bar_raw[GT_MAXP], bar_w[GT_MAXP], bar_empty[GT_MAXP];
+    __shared__ __align__(8) uint64_t bar_done;
+    __shared__ uint32_t tmem_slot;
+    __shared__ uint8_t table_s[256];
+    __shared__ int abort_flag;
+    uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    const uint32_t tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t mt = a.mt, P = a.stages;
+    const uint32_t SB = gemm_stage_bytes(R4, mt);
+    const uint32_t n0 = blockIdx.x * GT_N, m0 = blockIdx.y * mt, sl = blockIdx.z;
+    const uint32_t kb0 = (uint32_t)((uint64_t)sl * a.kb_total / a.split);
+    const uint32_t kb1 = (uint32_t)((uint64_t)(sl + 1) * a.kb_total / a.split);
+    const uint32_t nkb = kb1 - kb0;
+    const uint32_t ncols = mt <= 32 ? 32 : (mt <= 64 ? 64 : (mt <= 128 ? 128 : 256));
+    auto A = [&](uint32_t s) { return base + (size_t)s * SB; };
+    auto B = [&](uint32_t s) { return base + (size_t)s * SB + GT_N * 128; };
+    auto RS = [&](uint32_t s) { return base + (size_t)s * SB + GT_N * 128 + mt * 128; };
+    auto RN = [&](uint32_t s) { return base + (size_t)s * SB + GT_N * 128 + mt * 128 + GT_N * 64; };
+
+    if (tid == 0) {
+        for (uint32_t i = 0; i < P; i++) {
+            mbar_init(smem_u32(&bar_full[i]), 1);
+            mbar_init(smem_u32(&bar_raw[i]), 1);
+            mbar_init(smem_u32(&bar_w[i]), 4);
+            mbar_init(smem_u32(&bar_empty[i]), 1);
+        }
+        mbar_init(smem_u32(&bar_done), 1);
+        abort_flag = 0;
+        fence_mbarrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&tmem_slot), ncols);
+        tmem_relinquish();
+    }
+    table_s[tid] = a.table[tid];
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t taddr = tmem_slot;
+    volatile int *abortp = &abort_flag;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---- TMA producer
+            uint32_t issued = 0;
+            for (uint32_t i = 0; i < nkb; i++) {
+                const uint32_t s = i % P, use = i / P;
+                if (use > 0 && !wait_or_abort(smem_u32(&bar_empty[s]), (use - 1) & 1u, abortp)) {
+                    set_status(a.status, DGT_ERR_TIMEOUT);
+                    *abortp = 1;
+                    break;
+                }
+                const int32_t k = (int32_t)((kb0 + i) * GT_K);
+                mbar_arrive_expect_tx(smem_u32(&bar_full[s]), mt * 128 + (R4 ? 0 : GT_N * 128));
+                tma_load_2d(smem_u32(B(s)), &tm_x, smem_u32(&bar_full[s]), k, (int32_t)m0);
+                if (!R4) {
+                    tma_load_2d(smem_u32(A(s)), &tm_w, smem_u32(&bar_full[s]), k, (int32_t)n0);
+                } else {
+                    mbar_arrive_expect_tx(smem_u32(&bar_raw[s]), GT_N * 64 + GT_N * 32);
+                    tma_load_2d(smem_u32(RS(s)), &tm_w, smem_u32(&bar_raw[s]), k, (int32_t)n0);
+                    tma_load_2d(smem_u32(RN(s)), &tm_nib, smem_u32(&bar_raw[s]), k / 2, (int32_t)n0);
+                }
+                issued++;
+            }
+            // let every copy issued land before the CTA can exit
+            for (uint32_t i = issued > P ? issued - P : 0; i < issued; i++) {
+                const uint32_t s = i % P, par = (i / P) & 1u;
+                wait_or_abort(smem_u32(&bar_full[s]), par, abortp) || mbar_wait(smem_u32(&bar_full[s]), par);
+                if (R4) wait_or_abort(smem_u32(&bar_raw[s]), par, abortp) || mbar_wait(smem_u32(&bar_raw[s]), par);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---- MMA issuer
+            const uint32_t idesc = idesc_bf16(mt);
+            for (uint32_t i = 0; i < nkb; i++) {
+                const uint32_t s = i % P, par = (i / P) & 1u;
+                if (!wait_or_abort(smem_u32(&bar_full[s]), par, abortp) ||
+                    (R4 && !wait_or_abort(smem_u32(&bar_w[s]), par, abortp))) {
+                    set_status(a.status, DGT_ERR_TIMEOUT);
+                    *abortp = 1;
+                    break;
+                }
+                tc_fence_after();
+                const uint64_t ad = sw128_desc(smem_u32(A(s))), bd = sw128_desc(smem_u32(B(s)));
+#pragma unroll
+                for (uint32_t kk = 0; kk < GT_K / 16; kk++)
+                    mma_bf16(taddr, ad + 2 * kk, bd + 2 * kk, idesc, (i > 0 || kk > 0) ? 1u : 0u);
+                mma_commit(smem_u32(&bar_empty[s]));
+            }
+            mma_commit(smem_u32(&bar_done));
+        }
+    } else if (warp >= 4) {
+        const uint32_t t = tid - 128;  // W row within the tile, and TMEM lane
+        if (R4) {
+            // ---- decoders: thread t owns W row n0 + t
+            const uint64_t row = n0 + t;
+            const uint64_t kstart = (uint64_t)kb0 * GT_K;
+            const uint64_t j = kstart / DGT_SEG;
+            uint64_t eidx = a.seg[row * a.nseg + j];
+            for (uint64_t k = j * DGT_SEG; k < kstart; k += 2) {
+                const uint8_t b = a.nib[(row * a.K + k) / 2];
+                eidx += ((b & 15) == 15) + ((b >> 4) == 15);
+            }
+            bool bad = false;
+            for (uint32_t i = 0; i < nkb; i++) {
+                const uint32_t s = i % P, par = (i / P) & 1u;
+                if (!wait_or_abort(smem_u32(&bar_raw[s]), par, abortp)) {
+                    if (lane == 0) set_status(a.status, DGT_ERR_TIMEOUT);
+                    *abortp = 1;
+                    break;
+                }
+                decode_row64(a, RS(s) + t * 64, RN(s) + t * 32, A(s) + t * 128, t, eidx, table_s, bad);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&bar_w[s]));
+            }
+            if (bad) set_status(a.status, DGT_ERR_CORRUPT);
+        }
+        // ---- epilogue: thread t holds accumulator row t (W row n0 + t)
+        const bool ok = wait_or_abort(smem_u32(&bar_done), 0, abortp) || mbar_wait(smem_u32(&bar_done), 0);
+        tc_fence_after();
+        if (ok && !*abortp) {
+            const uint32_t lane_base = ((warp - 4) * 32) << 16;
+            const uint64_t n = n0 + t;
+            for (uint32_t c = 0; c < mt; c += 16) {
+                uint32_t r[16];
+                tmem_ld16(taddr + lane_base + c, r);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 16; i++) {
+                    const uint64_t m = (uint64_t)m0 + c + i;
+                    if (m < a.M) {
+                        const float v = __uint_as_float(r[i]);
+                        if (a.split == 1) {
+                            if (a.y32) a.y32[m * a.N + n] = v;
+                            if (a.y) a.y[m * a.N + n] = f32_to_bf16_rne(v);
+                        } else {
+                            a.partial[((uint64_t)sl * a.M + m) * a.N + n] = v;
+                        }
+                    }
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(taddr, ncols);
+}
+
+__global__ void __launch_bounds__(256) k_gemm_reduce(GemmArgs a) {
+    const uint64_t total = a.M * a.N;
+    for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (uint64_t)gridDim.x * blockDim.x) {
+        float y = a.partial[i];
+        for (uint32_t s = 1; s < a.split; s++) y = y + a.partial[(uint64_t)s * total + i];
+        if (a.y32) a.y32[i] = y;
+        if (a.y) a.y[i] = f32_to_bf16_rne(y);
+    }
+}
+
+// ---- host side ---------------------------------------------------------------
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+static bool make_map(CUtensorMap *m, CUtensorMapDataType dt, const void *ptr, uint64_t inner, uint64_t outer,
+                     uint64_t stride_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {stride_bytes};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t es[2] = {1, 1};
+    return fn(m, dt, 2, const_cast<void *>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+static uint32_t gemm_stages(bool r4, uint32_t mt) {
+    uint32_t p = GT_SMEM_LIMIT / gemm_stage_bytes(r4, mt);
+    return p > GT_MAXP ? GT_MAXP : p;
+}
+
+template <bool R4>
+static int launch_gemm(GemmArgs &a, const void *w_or_sm, const uint16_t *d_X, void *d_ws, size_t ws_bytes,
+                       cudaStream_t st) {
+    CUtensorMap tm_x, tm_w, tm_nib;
+    if (!make_map(&tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d_X, a.K, a.M, a.K * 2, GT_K, a.mt,
+                  CU_TENSOR_MAP_SWIZZLE_128B))
+        return DGT_ERR_CUDA;
+    if (R4) {
+        if (!make_map(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, w_or_sm, a.K, a.N, a.K, GT_K, GT_N,
+                      CU_TENSOR_MAP_SWIZZLE_NONE) ||
+            !make_map(&tm_nib, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.nib, a.K / 2, a.N, a.K / 2, GT_K / 2, GT_N,
+                      CU_TENSOR_MAP_SWIZZLE_NONE))
+            return DGT_ERR_CUDA;
+    } else {
+        if (!make_map(&tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, w_or_sm, a.K, a.N, a.K * 2, GT_K, GT_N,
+                      CU_TENSOR_MAP_SWIZZLE_128B))
+            return DGT_ERR_CUDA;
+        tm_nib = tm_w;
+    }
+    if (a.split > 1) {
+        const size_t need = (size_t)a.split * a.M * a.N * 4;
+        if (!d_ws || ws_bytes < need || !aligned16(d_ws)) return DGT_ERR_ARG;
+        a.partial = static_cast<float *>(d_ws);
+    }
+    const size_t smem = (size_t)a.stages * gemm_stage_bytes(R4, a.mt) + 1024;
+    int bps = 0;
+    if (prepare_kernel((const void *)k_gemm<R4>, smem, 256, &bps) != DGT_OK) return DGT_ERR_CUDA;
+    dim3 grid((unsigned)(a.N / GT_N), (unsigned)((a.M + a.mt - 1) / a.mt), a.split);
+    k_gemm<R4><<<grid, 256, smem, st>>>(tm_x, tm_w, tm_nib, a);
+    if (a.split > 1) {
+        DeviceInfo di;
+        if (device_info(&di) != DGT_OK) return DGT_ERR_CUDA;
+        const uint64_t total = a.M * a.N;
+        uint64_t g = (total + 255) / 256;
+        if (g > (uint64_t)di.sms * 8) g = (uint64_t)di.sms * 8;
+        k_gemm_reduce<<<(unsigned)g, 256, 0, st>>>(a);
+    }
+    return cudaPeekAtLastError() == cudaSuccess ? DGT_OK : DGT_ERR_CUDA;
+}
+
+static int fill_common(GemmArgs &a, uint64_t M, uint64_t N, uint64_t K, const dgt_gemm_plan *plan, float *d_Y32,
+                       uint16_t *d_Y, int32_t *d_status, cudaStream_t st) {
+    if (M == 0 || N == 0 || K == 0) return DGT_ERR_SHAPE;
+    if (N % GT_N || K % GT_K || M >= (1ull << 31) || N >= (1ull << 31) || K >= (1ull << 31)) return DGT_ERR_SHAPE;
+    if (!d_Y32 && !d_Y) return DGT_ERR_ARG;
+    dgt_gemm_plan p;
+    if (plan) p = *plan;
+    else dgt_gemm_default_plan(M, N, K, &p);
+    if (p.m_tile < 16 || p.m_tile > 256 || p.m_tile % 16 || p.split_k < 1 || (uint64_t)p.split_k > K / GT_K)
+        return DGT_ERR_ARG;
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.mt = (uint32_t)p.m_tile;
+    a.kb_total = (uint32_t)(K / GT_K);
+    a.split = (uint32_t)p.split_k;
+    a.y32 = d_Y32;
+    a.y = d_Y;
+    a.status = d_status;
+    if (d_status && cudaMemsetAsync(d_status, 0, 4, st) != cudaSuccess) return DGT_ERR_CUDA;
+    return DGT_OK;
+}
+
+}  // namespace dgt
+
+using namespace dgt;
+
+extern "C" int dgt_gemm_default_plan(uint64_t M, uint64_t N, uint64_t K, dgt_gemm_plan *plan) {
+    if (!plan || M == 0 || N == 0 || K == 0) return DGT_ERR_ARG;
+    uint32_t mt = M <= 256 ? (uint32_t)((M + 15) / 16 * 16) : 256u;
+    const uint64_t tiles = ((N + GT_N - 1) / GT_N) * ((M + mt - 1) / mt);
+    uint64_t split = (152 + tiles - 1) / tiles;
+    const uint64_t kb = K / GT_K;
+    if (split > kb / 4) split = kb / 4;
+    if (split > 16) split = 16;
+    if (split < 1) split = 1;
+    plan->m_tile = (int32_t)mt;
+    plan->split_k = (int32_t)split;
+    plan->reserved0 = 0;
+    plan->reserved1 = 0;
+    return DGT_OK;
+}
+
+extern "C" size_t dgt_gemm_workspace_bytes(uint64_t M, uint64_t N, const dgt_gemm_plan *plan) {
+    if (!plan || plan->split_k <= 1) return 0;
+    return (size_t)plan->split_k * M * N * 4;
+}
+
+extern "C" int dgt_gemm(const dgt_r4 *W, const uint16_t *d_X, uint64_t M, float *d_Y32, uint16_t *d_Y,
+                        const dgt_gemm_plan *plan, void *d_ws, size_t ws_bytes, int32_t *d_status, void *stream) {
+    if (!W || !d_X) return DGT_ERR_ARG;
+    cudaStream_t st = (cudaStream_t)stream;
+    GemmArgs a = {};
+    int rc = fill_common(a, M, W->rows, W->cols, plan, d_Y32, d_Y, d_status, st);
+    if (rc != DGT_OK) return rc;
+    if (!W->sm || !W->nib || !W->seg || (W->n_esc && !W->esc) || !aligned16(W->sm) || !aligned16(W->nib) ||
+        !aligned16(d_X))
+        return DGT_ERR_ARG;
+    a.nib = W->nib;
+    a.esc = W->esc;
+    a.seg = W->seg;
+    a.n_esc = W->n_esc;
+    a.nseg = dgt_r4_nseg(W->cols);
+    a.L = make_r4lut(W->table, W->n_table);
+    for (int i = 0; i < 256; i++) a.table[i] = W->table[i];
+    a.stages = gemm_stages(true, a.mt);
+    return launch_gemm<true>(a, W->sm, d_X, d_ws, ws_bytes, st);
+}
+
+extern "C" int dgt_gemm_bf16(const uint16_t *d_W, uint64_t N, uint64_t K, const uint16_t *d_X, uint64_t M,
+                             float *d_Y32, uint16_t *d_Y, const dgt_gemm_plan *plan, void *d_ws, size_t ws_bytes,
+                             int32_t *d_status, void *stream) {
+    if (!d_W || !d_X) return DGT_ERR_ARG;
+    cudaStream_t st = (cudaStream_t)stream;
+    GemmArgs a = {};
+    int rc = fill_common(a, M, N, K, plan, d_Y32, d_Y, d_status, st);
+    if (rc != DGT_OK) return rc;
+    if (!aligned16(d_W) || !aligned16(d_X)) return DGT_ERR_ARG;
+    a.stages = gemm_stages(true, a.mt);   // same pipeline depth as the R4 GEMM
+    return launch_gemm<false>(a, d_W, d_X, d_ws, ws_bytes, st);
+}

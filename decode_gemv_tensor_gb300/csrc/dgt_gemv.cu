@@ -349,10 +349,6 @@ __device__ __forceinline__ void issue_piece(const GemvArgs &a, uint64_t row, uin
     }
 }
 
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
 template <bool R4>
 __global__ void __launch_bounds__((TNW + 1) * 32, 1) k_gemv_tma(GemvArgs a) {
     constexpr uint32_t C = TmaCfg<R4>::C, STAGE = TmaCfg<R4>::STAGE;

@@ -295,6 +295,41 @@ int dgt_moe_gemv_bf16(const uint16_t *d_W, uint64_t rows, uint64_t cols, uint32_
                       const uint16_t *d_x, float *d_y32, uint16_t *d_out, float *d_out32, void *d_ws,
                       size_t ws_bytes, int32_t *d_status, void *stream);
 
+/* ------------------------------------------------------------------------ */
+/* Prompt GEMM on tcgen05                                                   */
+/* ------------------------------------------------------------------------ */
+/*
+ * Y[M, N] = X[M, K] W[N, K]^T on the tensor cores (Binade README, "Results":
+ * prompt matmuls at 16..2048 rows; "NVIDIA GPUs": each output is a sequence
+ * of tensor-core MMA steps along K and split-K partitions follow a fixed
+ * rule; "How it works", Exactness).  The plan fixes the arithmetic: the X
+ * tile height m_tile (16..256, multiple of 16; each W tile is 128 rows) and
+ * the number of K slices split_k (added left to right after the MMAs).  The
+ * R4 GEMM and the BF16 GEMM with the same plan issue the same MMA sequence on
+ * byte-identical tiles, so their outputs are bit-identical.
+ * dgt_gemm_default_plan: m_tile = round_up(M, 16) up to 256; split_k = enough
+ * slices for 152 tiles, at most K/256 and 16.
+ * d_X: device bf16 [M, K].  d_Y32 / d_Y: device float / bf16 [M, N] (either
+ * may be NULL).  d_ws: device workspace of dgt_gemm_workspace_bytes() bytes
+ * (split partials; NULL when split_k == 1).  Limits: N % 128 == 0,
+ * K % 64 == 0, 16-byte aligned arrays.  Asynchronous; d_status receives
+ * DGT_ERR_TIMEOUT if a bounded wait runs out, DGT_ERR_CORRUPT if an escape
+ * index runs past the escape list.
+ */
+typedef struct dgt_gemm_plan {
+    int32_t m_tile;
+    int32_t split_k;
+    int32_t reserved0, reserved1;
+} dgt_gemm_plan;
+
+int dgt_gemm_default_plan(uint64_t M, uint64_t N, uint64_t K, dgt_gemm_plan *plan);
+size_t dgt_gemm_workspace_bytes(uint64_t M, uint64_t N, const dgt_gemm_plan *plan);
+int dgt_gemm(const dgt_r4 *W, const uint16_t *d_X, uint64_t M, float *d_Y32, uint16_t *d_Y,
+             const dgt_gemm_plan *plan, void *d_ws, size_t ws_bytes, int32_t *d_status, void *stream);
+int dgt_gemm_bf16(const uint16_t *d_W, uint64_t N, uint64_t K, const uint16_t *d_X, uint64_t M, float *d_Y32,
+                  uint16_t *d_Y, const dgt_gemm_plan *plan, void *d_ws, size_t ws_bytes, int32_t *d_status,
+                  void *stream);
+
 /*
  * Allocation-free expert gather.  The paper has no counterpart: this entry
  * point exists for callers that cannot allocate device memory when they call
