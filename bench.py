@@ -3,10 +3,15 @@
 
 Workload "bulk-4096x16384": a batch of 4 distinct 4096 x 16384 BF16 tensors
 (64M weights each, N(0, 0.02) with 0.1% outliers at 100x), packed on the host
-in both file formats, resident in HBM when timing starts.  One step runs every
-device row of the path over the whole batch:
-  Rice -> R4 (format 2 load transcode), format 1 -> R4, R4 -> BF16 rebuild,
-  R4 GEMV and the BF16 GEMV twin (x = N(0, 1) bf16, one per tensor).
+in both file formats, resident in HBM when timing starts, plus one MoE
+projection of 128 stacked experts (704 x 2816, random init).  One step runs
+every device row of the path:
+  per bulk tensor: Rice -> R4 (format 2 load transcode), format 1 -> R4,
+  R4 -> BF16 rebuild, R4 GEMV and the BF16 GEMV twin (x = N(0, 1) bf16), and
+  the R4 and BF16 tcgen05 GEMMs at 16 prompt rows;
+  the MoE expert gather (R4 and BF16 twin) at 1 and 16 tokens, top-8.
+The GEMM at 128 and 2048 rows is tensor-bound and is reported separately
+("gemm_tensor", TFLOP/s against the measured bf16 peak).
 Between a kernel's reuses of one tensor's data the other tensors and kernels
 move far more than the 129 MB L2, so no explicit flush is needed.
 
@@ -41,9 +46,13 @@ METRIC = "R4-fused GEMV HBM GB/s (frac of ~8 TB/s); Rice→R4 decode Gsym/s"
 UNIT = "GB/s"
 ROWS, COLS, BATCH = 4096, 16384, 4
 FALLBACK_HBM = 6800.0
-KERNELS = ["rice_to_r4", "f1_to_r4", "r4_to_bf16", "gemv_r4", "gemv_bf16"]
+GEMM_M = 16
+KERNELS = ["rice_to_r4", "f1_to_r4", "r4_to_bf16", "gemv_r4", "gemv_bf16", "moe_r4", "moe_bf16", "gemm_r4",
+           "gemm_bf16"]
 KERNEL_SRC = {"rice_to_r4": "dgt_transcode.cu", "f1_to_r4": "dgt_transcode.cu",
-              "r4_to_bf16": "dgt_transcode.cu", "gemv_r4": "dgt_gemv.cu", "gemv_bf16": "dgt_gemv.cu"}
+              "r4_to_bf16": "dgt_transcode.cu", "gemv_r4": "dgt_gemv.cu", "gemv_bf16": "dgt_gemv.cu",
+              "moe_r4": "dgt_moe.cu", "moe_bf16": "dgt_moe.cu", "gemm_r4": "dgt_gemm.cu",
+              "gemm_bf16": "dgt_gemm.cu"}
 
 
 def hbm_peak():
@@ -227,57 +236,104 @@ def run_ours(args, rank, world, dist):
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
     dgt.lib()
+    stream = torch.cuda.current_stream(dev)
+
+    def bf16_dev(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
 
     # ---- setup (untimed): pack on the host, upload, allocate outputs
     items = []
     for b in range(BATCH):
         w = S.weights(ROWS, COLS, (2, rank, b, 0), outliers=True)
         x = S.activations(COLS, (2, 999, rank * BATCH + b))
+        xm = S.activations(COLS, (2, 998, rank * BATCH + b), count=GEMM_M).reshape(GEMM_M, COLS)
         p2, p1 = dgt.pack(w, 2), dgt.pack(w, 1)
         d2, d1 = dgt.upload(p2, dev), dgt.upload(p1, dev)
         dgt.share_sm(d1, d2)
         it = dict(p2=p2, p1=p1, d2=d2, d1=d1, w=w)
         it["r4a"], it["r4b"] = dgt.R4(d2), dgt.R4(d1)
         it["wbf"] = torch.empty((ROWS, COLS), dtype=torch.bfloat16, device=dev)
-        it["x"] = torch.from_numpy(x.view(np.int16)).to(dev).view(torch.bfloat16)
-        it["y16"] = torch.empty(ROWS, dtype=torch.bfloat16, device=dev)
-        it["y32"] = torch.empty(ROWS, dtype=torch.float32, device=dev)
-        it["b16"] = torch.empty(ROWS, dtype=torch.bfloat16, device=dev)
-        it["b32"] = torch.empty(ROWS, dtype=torch.float32, device=dev)
-        it["bytes"] = algo_bytes(p2.arrays(), p1.arrays(), w.size, p2.view.n_esc15, ROWS, COLS)
+        it["x"], it["xm"] = bf16_dev(x), bf16_dev(xm)
+        for nm, shape, dt in (("y16", ROWS, torch.bfloat16), ("y32", ROWS, torch.float32),
+                              ("b16", ROWS, torch.bfloat16), ("b32", ROWS, torch.float32),
+                              ("g16", (GEMM_M, ROWS), torch.bfloat16), ("g32", (GEMM_M, ROWS), torch.float32),
+                              ("h16", (GEMM_M, ROWS), torch.bfloat16), ("h32", (GEMM_M, ROWS), torch.float32)):
+            it[nm] = torch.empty(shape, dtype=dt, device=dev)
+        it["plan"] = dgt.gemm_plan(GEMM_M, ROWS, COLS)
+        it["gws"] = torch.empty(max(16, it["plan"].split_k * GEMM_M * ROWS * 4), dtype=torch.uint8, device=dev)
+        base = algo_bytes(p2.arrays(), p1.arrays(), w.size, p2.view.n_esc15, ROWS, COLS)
+        r4_w = w.size + (w.size + 1) // 2 + p2.view.n_esc15 + (ROWS * ((COLS + 511) // 512) + 1) * 4
+        base["gemm_r4"] = r4_w + GEMM_M * COLS * 2 + GEMM_M * ROWS * 6
+        base["gemm_bf16"] = 2 * w.size + GEMM_M * COLS * 2 + GEMM_M * ROWS * 6
+        it["bytes"] = base
         items.append(it)
         del w
-    stream = torch.cuda.current_stream(dev)
+    # one MoE projection: 128 stacked experts (gate, 704 x 2816), top-8, at 1 and 16 tokens
+    E, TOPK = S.MOE["experts"], S.MOE["topk"]
+    _, NE, KE = S.MOE["expert_proj"][0]
+    wm = S.weights(E * NE, KE, (5, rank, 0, 0))
+    pm = dgt.pack(wm, 2)
+    moe = dict(dp=dgt.upload(pm, dev))
+    moe["r4"] = dgt.load_r4(moe["dp"])
+    moe["wbf"] = bf16_dev(wm)
+    moe_runs = []
+    for T in (1, 16):
+        ids, pr = S.routing(T, E, TOPK, (5, 777, rank, T))
+        xs = S.activations(KE, (5, 999, T), count=T).reshape(T, KE)
+        r = dict(T=T, ids=torch.from_numpy(ids).to(dev), p=torch.from_numpy(pr).to(dev), x=bf16_dev(xs))
+        r["ws"] = torch.empty(dgt.moe_workspace_bytes(E, NE, KE, T, TOPK), dtype=torch.uint8, device=dev)
+        for nm, shape in (("y", (T, TOPK, NE)), ("o32", (T, NE)), ("yb", (T, TOPK, NE)), ("o32b", (T, NE))):
+            r[nm] = torch.empty(shape, dtype=torch.float32, device=dev)
+        r["o16"] = torch.empty((T, NE), dtype=torch.bfloat16, device=dev)
+        r["o16b"] = torch.empty((T, NE), dtype=torch.bfloat16, device=dev)
+        distinct = len(np.unique(ids))
+        io = T * KE * 2 + T * TOPK * NE * 4 + T * NE * 6
+        r["bytes_r4"] = distinct * NE * KE * 1.5 + io
+        r["bytes_bf16"] = distinct * NE * KE * 2 + io
+        moe_runs.append(r)
+    del wm
 
     def step(ev=None):
-        def rec(k, i, which):
-            if ev is not None:
-                e = torch.cuda.Event(enable_timing=True)
-                e.record(stream)
-                ev[k][which].append(e)
+        def timed(k, fn):
+            if ev is None:
+                fn()
+                return
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            ev[k].append((e0, e1))
         for it in items:
-            rec("rice_to_r4", 0, 0)
-            dgt.load_r4_into(it["d2"], it["r4a"], stream=stream)
-            rec("rice_to_r4", 0, 1)
+            timed("rice_to_r4", lambda: dgt.load_r4_into(it["d2"], it["r4a"], stream=stream))
         for it in items:
-            rec("f1_to_r4", 0, 0)
-            dgt.load_r4_into(it["d1"], it["r4b"], stream=stream)
-            rec("f1_to_r4", 0, 1)
+            timed("f1_to_r4", lambda: dgt.load_r4_into(it["d1"], it["r4b"], stream=stream))
         for it in items:
-            rec("r4_to_bf16", 0, 0)
-            dgt.r4_to_bf16(it["r4a"], out=it["wbf"], stream=stream)
-            rec("r4_to_bf16", 0, 1)
+            timed("r4_to_bf16", lambda: dgt.r4_to_bf16(it["r4a"], out=it["wbf"], stream=stream))
         for it in items:
-            rec("gemv_r4", 0, 0)
-            dgt.gemv(it["r4a"], it["x"], it["y16"], it["y32"], stream=stream)
-            rec("gemv_r4", 0, 1)
+            timed("gemv_r4", lambda: dgt.gemv(it["r4a"], it["x"], it["y16"], it["y32"], stream=stream))
         for it in items:
-            rec("gemv_bf16", 0, 0)
-            dgt.gemv_bf16(it["wbf"], it["x"], it["b16"], it["b32"], stream=stream)
-            rec("gemv_bf16", 0, 1)
+            timed("gemv_bf16", lambda: dgt.gemv_bf16(it["wbf"], it["x"], it["b16"], it["b32"], stream=stream))
+        for r in moe_runs:
+            timed("moe_r4", lambda: dgt.moe_gemv(moe["r4"], E, r["ids"], r["p"], r["x"], ws=r["ws"], y32=r["y"],
+                                                 out=r["o16"], out32=r["o32"], stream=stream))
+        for r in moe_runs:
+            timed("moe_bf16", lambda: dgt.moe_gemv_bf16(moe["wbf"], E, r["ids"], r["p"], r["x"], ws=r["ws"],
+                                                        y32=r["yb"], out=r["o16b"], out32=r["o32b"], stream=stream))
+        for it in items:
+            timed("gemm_r4", lambda: dgt.gemm(it["r4a"], it["xm"], plan=it["plan"], Y32=it["g32"], Y=it["g16"],
+                                              ws=it["gws"], stream=stream))
+        for it in items:
+            timed("gemm_bf16", lambda: dgt.gemm_bf16(it["wbf"], it["xm"], plan=it["plan"], Y32=it["h32"],
+                                                     Y=it["h16"], ws=it["gws"], stream=stream))
 
-    launches_per_step = 5 * BATCH
-    step_bytes = sum(sum(it["bytes"].values()) for it in items)
+    split_launches = sum(2 if it["plan"].split_k > 1 else 1 for it in items)
+    launches_per_step = 5 * BATCH + 2 * 3 * len(moe_runs) + 2 * split_launches
+    moe_bytes = {"moe_r4": sum(r["bytes_r4"] for r in moe_runs), "moe_bf16": sum(r["bytes_bf16"] for r in moe_runs)}
+    op_bytes = {k: sum(it["bytes"][k] for it in items) for k in KERNELS if not k.startswith("moe")}
+    op_bytes.update(moe_bytes)
+    op_count = {k: (len(moe_runs) if k.startswith("moe") else BATCH) for k in KERNELS}
+    step_bytes = sum(op_bytes.values())
 
     # ---- correctness gate on the timed configuration (untimed)
     step()
@@ -285,6 +341,9 @@ def run_ours(args, rank, world, dist):
     for it in items:
         assert torch.equal(it["r4a"].nib, it["r4b"].nib) and torch.equal(it["r4a"].seg, it["r4b"].seg)
         assert torch.equal(it["y32"].view(torch.int32), it["b32"].view(torch.int32)), "R4 != BF16 GEMV"
+        assert torch.equal(it["g32"].view(torch.int32), it["h32"].view(torch.int32)), "R4 != BF16 GEMM"
+    for r in moe_runs:
+        assert torch.equal(r["y"].view(torch.int32), r["yb"].view(torch.int32)), "R4 != BF16 MoE"
     wb0 = items[0]["wbf"].view(torch.int16).cpu().numpy().view(np.uint16)
     assert np.array_equal(wb0, items[0]["w"]), "R4 -> BF16 mismatch"
     for it in items:
@@ -300,7 +359,7 @@ def run_ours(args, rank, world, dist):
     barrier()
     clocks = Clocks(dev.index)
     clocks.start()
-    ev = {k: ([], []) for k in KERNELS}
+    ev = {k: [] for k in KERNELS}
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     barrier()
@@ -320,69 +379,70 @@ def run_ours(args, rank, world, dist):
     peak, peak_kind = hbm_peak()
     kern = {}
     for k in KERNELS:
-        durs = [a.elapsed_time(b) for a, b in zip(*ev[k])]
+        durs = [a.elapsed_time(b) for a, b in ev[k]]
         avg_ms = sum(durs) / len(durs)
-        b = sum(it["bytes"][k] for it in items) / BATCH
-        e = {"launches": len(durs), "ms_avg": avg_ms, "share": sum(durs) / ms, "gb_s": b / (avg_ms / 1e3) / 1e9}
+        b = op_bytes[k] / op_count[k]
+        e = {"calls": len(durs), "ms_avg": avg_ms, "share": sum(durs) / ms, "gb_s": b / (avg_ms / 1e3) / 1e9}
         e["frac"] = e["gb_s"] / peak
         if k in ("rice_to_r4", "f1_to_r4", "r4_to_bf16"):
             e["gsym_s"] = ROWS * COLS / (avg_ms / 1e3) / 1e9
         kern[k] = e
     dom = max(KERNELS, key=lambda k: kern[k]["share"])
-    db = sum(it["bytes"][dom] for it in items) / BATCH
     roof = {"kernel": dom, "bound": "hbm", "achieved": kern[dom]["gb_s"], "peak": peak, "unit": "GB/s",
             "frac": kern[dom]["gb_s"] / peak, "peak_kind": peak_kind,
-            "algorithmic_bytes_per_launch": db, "traffic": ncu_traffic(dom)}
+            "algorithmic_bytes_per_launch": op_bytes[dom] / op_count[dom], "traffic": ncu_traffic(dom)}
+
+    # ---- prompt GEMM at 128 and 2048 rows (tensor-bound), outside the timed step
+    extras = gemm_extras(dgt, torch, dev) if rank == 0 else None
 
     # ---- end to end through the C ABI from pinned host buffers
     e2e = None
-    if rank == 0 or world > 1:
-        host = []
-        h2d = d2h = 0
-        for it in items:
-            hs = {}
-            for tag in ("d2", "d1"):
-                for name, t in it[tag].tensors.items():
-                    if tag == "d1" and name == "sm":
-                        continue
-                    h = torch.empty_like(t, device="cpu").pin_memory()
-                    h.copy_(t)
-                    hs[(tag, name)] = (h, t)
-                    h2d += t.numel() * t.element_size()
-            hx = it["x"].cpu().pin_memory()
-            hs[("x", "x")] = (hx, it["x"])
-            h2d += it["x"].numel() * 2
-            outs = []
-            for name in ("y16", "y32", "b16", "b32"):
-                t = it[name]
-                outs.append((torch.empty_like(t, device="cpu").pin_memory(), t))
-                d2h += t.numel() * t.element_size()
-            host.append((hs, outs))
+    host = []
+    h2d = d2h = 0
+    pinned_in, pinned_out = [], []
+    for it in items:
+        for tag in ("d2", "d1"):
+            for name, t in it[tag].tensors.items():
+                if tag == "d1" and name == "sm":
+                    continue
+                pinned_in.append((torch.empty_like(t, device="cpu").pin_memory().copy_(t), t))
+        for nm in ("x", "xm"):
+            pinned_in.append((it[nm].cpu().pin_memory(), it[nm]))
+        for nm in ("y16", "y32", "b16", "b32", "g16", "g32", "h16", "h32"):
+            pinned_out.append((torch.empty_like(it[nm], device="cpu").pin_memory(), it[nm]))
+    for name, t in moe["dp"].tensors.items():
+        pinned_in.append((torch.empty_like(t, device="cpu").pin_memory().copy_(t), t))
+    for r in moe_runs:
+        for nm in ("ids", "p", "x"):
+            pinned_in.append((r[nm].cpu().pin_memory(), r[nm]))
+        for nm in ("y", "o32", "o16", "yb", "o32b", "o16b"):
+            pinned_out.append((torch.empty_like(r[nm], device="cpu").pin_memory(), r[nm]))
+    h2d = sum(t.numel() * t.element_size() for _, t in pinned_in)
+    d2h = sum(t.numel() * t.element_size() for _, t in pinned_out)
 
-        def e2e_step():
-            for (hs, _), it in zip(host, items):
-                for h, t in hs.values():
-                    t.copy_(h, non_blocking=True)
-            step()
-            for (_, outs) in host:
-                for h, t in outs:
-                    h.copy_(t, non_blocking=True)
-            stream.synchronize()
+    def e2e_step():
+        for h, t in pinned_in:
+            t.copy_(h, non_blocking=True)
+        dgt.load_r4_into(moe["dp"], moe["r4"], stream=stream)
+        step()
+        for h, t in pinned_out:
+            h.copy_(t, non_blocking=True)
+        stream.synchronize()
 
-        for _ in range(max(1, args.warmup)):
-            e2e_step()
-        barrier()
-        s0 = time.perf_counter()
-        for _ in range(args.steps):
-            e2e_step()
-        barrier()
-        es = time.perf_counter() - s0
-        if dist is not None:
-            tt = torch.tensor([es], device=dev)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            es = float(tt.item())
-        e2e = {"value": step_bytes * world * args.steps / es / 1e9, "unit": UNIT,
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": es / args.steps * 1e3}
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    barrier()
+    s0 = time.perf_counter()
+    for _ in range(args.steps):
+        e2e_step()
+    barrier()
+    es = time.perf_counter() - s0
+    if dist is not None:
+        tt = torch.tensor([es], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        es = float(tt.item())
+    e2e = {"value": step_bytes * world * args.steps / es / 1e9, "unit": UNIT, "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": d2h, "ms_per_step": es / args.steps * 1e3}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -394,20 +454,124 @@ def run_ours(args, rank, world, dist):
                 "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
                 "config": {"workload": "bulk-4096x16384", "rows": ROWS, "cols": COLS, "batch": BATCH,
                            "weights": "N(0,0.02) bf16 + 0.1% outliers x100, seeded",
-                           "step": "rice->R4, f1->R4, R4->bf16, R4 GEMV, bf16 GEMV over the batch",
+                           "step": "per bulk tensor: rice->R4, f1->R4, R4->bf16, R4 GEMV, bf16 GEMV, R4 and bf16 "
+                                   "GEMM at 16 rows; one 128-expert MoE projection (704 x 2816, top-8) gathered "
+                                   "at 1 and 16 tokens, R4 and bf16",
                            "l2": "inputs larger than L2 between reuses (no flush)"},
                 "headline": {"gemv_r4_gb_s": kern["gemv_r4"]["gb_s"], "gemv_r4_frac": kern["gemv_r4"]["frac"],
                              "rice_to_r4_gsym_s": kern["rice_to_r4"]["gsym_s"],
                              "rice_to_r4_frac": kern["rice_to_r4"]["frac"],
                              "r4_vs_bf16_gemv_speedup": kern["gemv_bf16"]["ms_avg"] / kern["gemv_r4"]["ms_avg"]},
-                "kernels": kern, "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+                "kernels": kern, "roofline": roof, "gemm_tensor": extras, "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": launches_per_step * args.steps, "clocks": clk,
                 "gpu": torch.cuda.get_device_name(dev)}
         print(json.dumps(line), flush=True)
 
 
+def gemm_extras(dgt, torch, dev):
+    """R4 and bf16 GEMM at 128 and 2048 rows on the 12B q-projection shape
+    (4096 x 3840), CUDA events, median of 10, three weight copies rotated."""
+    N, K = 4096, 3840
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            tpk, tkind = float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        tpk, tkind = 1900.0, "fallback"
+    ws = [S.weights(N, K, (4, 0, 0, c)) for c in range(3)]
+    r4s = [dgt.load_r4(dgt.upload(dgt.pack(w, 2), dev)) for w in ws]
+    wbs = [torch.from_numpy(w.view(np.int16)).to(dev).view(torch.bfloat16) for w in ws]
+    out = {}
+    st = torch.cuda.current_stream(dev)
+    for M in (128, 2048):
+        X = torch.from_numpy(S.activations(K, (4, 999, M), count=M).reshape(M, K).view(np.int16)).to(dev)
+        X = X.view(torch.bfloat16)
+        plan = dgt.gemm_plan(M, N, K)
+        y32 = torch.empty((M, N), device=dev)
+        y16 = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        gws = torch.empty(max(16, plan.split_k * M * N * 4), dtype=torch.uint8, device=dev)
+        res = {}
+        for name, fn in (("r4", lambda i: dgt.gemm(r4s[i % 3], X, plan=plan, Y32=y32, Y=y16, ws=gws, stream=st)),
+                         ("bf16", lambda i: dgt.gemm_bf16(wbs[i % 3], X, plan=plan, Y32=y32, Y=y16, ws=gws,
+                                                          stream=st))):
+            for i in range(3):
+                fn(i)
+            evs = []
+            for i in range(10):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(st)
+                fn(i)
+                e1.record(st)
+                evs.append((e0, e1))
+            torch.cuda.synchronize()
+            t = sorted(a.elapsed_time(b) for a, b in evs)[5]
+            tf = 2.0 * M * N * K / (t / 1e3) / 1e12
+            res[name] = {"ms": t, "tflops": tf, "frac": tf / tpk}
+        out[f"M{M}"] = {"shape": [M, N, K], "plan": [plan.m_tile, plan.split_k], "bound": "tensor",
+                        "peak_tflops": tpk, "peak_kind": tkind, **res}
+    return out
+
+
+def run_case(args):
+    """One named kernel, a few launches on one bulk-sized input, for profilers:
+    python bench.py --case gemv_r4 --reps 3 (see profiles/ for the commands)."""
+    import torch
+
+    import decode_gemv_tensor_gb300 as dgt
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+
+    def bf(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    c = args.case
+    if c.startswith("moe"):
+        E, TOPK = S.MOE["experts"], S.MOE["topk"]
+        _, NE, KE = S.MOE["expert_proj"][0]
+        w = S.weights(E * NE, KE, (5, 0, 0, 0))
+        T = 16
+        ids, p = S.routing(T, E, TOPK, (5, 777, 0, T))
+        x = bf(S.activations(KE, (5, 999, T), count=T).reshape(T, KE))
+        idd, pd = torch.from_numpy(ids).to(dev), torch.from_numpy(p).to(dev)
+        r4 = dgt.load_r4(dgt.upload(dgt.pack(w, 2), dev))
+        wb = bf(w)
+        for _ in range(args.reps):
+            if c == "moe_r4":
+                dgt.moe_gemv(r4, E, idd, pd, x)
+            else:
+                dgt.moe_gemv_bf16(wb, E, idd, pd, x)
+    else:
+        rows, cols = (4096, 3840) if c == "gemm2048" else (ROWS, COLS)
+        w = S.weights(rows, cols, (2, 0, 0, 0), outliers=True)
+        fmt = 1 if c == "f1_to_r4" else 2
+        d = dgt.upload(dgt.pack(w, fmt), dev)
+        r4 = dgt.load_r4(d)
+        wb = dgt.r4_to_bf16(r4)
+        x = bf(S.activations(cols, (2, 999, 0)))
+        M = 2048 if c == "gemm2048" else GEMM_M
+        xm = bf(S.activations(cols, (2, 998, 0), count=M).reshape(M, cols))
+        for _ in range(args.reps):
+            if c in ("rice_to_r4", "f1_to_r4"):
+                dgt.load_r4_into(d, r4)
+            elif c == "r4_to_bf16":
+                dgt.r4_to_bf16(r4, out=wb)
+            elif c == "gemv_r4":
+                dgt.gemv(r4, x)
+            elif c == "gemv_bf16":
+                dgt.gemv_bf16(wb, x)
+            elif c in ("gemm_r4", "gemm2048"):
+                dgt.gemm(r4, xm)
+            elif c == "gemm_bf16":
+                dgt.gemm_bf16(wb, xm)
+            else:
+                raise SystemExit(f"unknown case {c}")
+    torch.cuda.synchronize()
+    print(f"case {c}: {args.reps} launches ok")
+
+
 def main():
     ap = argparse.ArgumentParser()
+    ap.add_argument("--case", default=None, help="run one kernel on one input (profiling)")
+    ap.add_argument("--reps", type=int, default=3)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
@@ -415,6 +579,9 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
+    if args.case:
+        run_case(args)
+        return
     args.warmup = max(args.warmup, 3) if args.impl == "ours" else args.warmup
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
