@@ -134,41 +134,51 @@ __host__ __device__ inline uint32_t gemm_stage_bytes(bool r4, uint32_t mt) {
     return GT_N * 128 + mt * 128 + (r4 ? GT_N * 64 + GT_N * 32 : 0);
 }
 
-// Decode one W row's 64 weights of a stage from the raw tiles into its
-// swizzled bf16 row; escapes come from the running index eidx.
-__device__ __forceinline__ void decode_row64(const GemmArgs &a, const uint8_t *raw_sm, const uint8_t *raw_nib,
-                                             uint8_t *arow, uint32_t t, uint64_t &eidx, const uint8_t *table_s,
-                                             bool &bad) {
+// Decoder thread (row t, chunk q): the 16 weights [16q, 16q + 16) of W row t
+// of a stage, from the raw tiles into the row's swizzled bf16 chunks 2q and
+// 2q+1.  The four chunk threads of a row are lanes 4j..4j+3 of one warp; they
+// place their escapes by a prefix sum over the four and advance the row's
+// running escape index eidx by the row's total.
+__device__ __forceinline__ void decode_chunk16(const GemmArgs &a, const uint8_t *raw_sm, const uint8_t *raw_nib,
+                                               uint8_t *arow, uint32_t t, uint32_t q, uint64_t &eidx,
+                                               const uint8_t *table_s, bool &bad) {
+    const uint4 sv = *reinterpret_cast<const uint4 *>(raw_sm + q * 16);
+    const uint2 nv = *reinterpret_cast<const uint2 *>(raw_nib + q * 8);
+    uint32_t p[8];
+    r4_dec16(nv, sv, a.L, p);
+    const uint32_t m0 = nib15_mask(nv.x), m1 = nib15_mask(nv.y);
+    const uint32_t c = __popc(m0) + __popc(m1);
+    uint32_t incl = c;
+    uint32_t y = __shfl_up_sync(DGT_FULL, incl, 1, 4);
+    if (q >= 1) incl += y;
+    y = __shfl_up_sync(DGT_FULL, incl, 2, 4);
+    if (q >= 2) incl += y;
+    const uint32_t total = __shfl_sync(DGT_FULL, incl, 3, 4);
+    if (c) {
+        uint64_t e = eidx + incl - c;
 #pragma unroll
-    for (uint32_t q = 0; q < 4; q++) {
-        const uint4 sv = *reinterpret_cast<const uint4 *>(raw_sm + q * 16);
-        const uint2 nv = *reinterpret_cast<const uint2 *>(raw_nib + q * 8);
-        uint32_t p[8];
-        r4_dec16(nv, sv, a.L, p);
-        const uint32_t m0 = nib15_mask(nv.x), m1 = nib15_mask(nv.y);
-        if (m0 | m1) {
-#pragma unroll
-            for (int i = 0; i < 16; i++) {
-                const uint32_t m = i < 8 ? m0 : m1;
-                if ((m >> (4 * (i & 7))) & 1u) {
-                    uint32_t e = 0;
-                    if (eidx < a.n_esc) e = table_s[a.esc[eidx]];
-                    else bad = true;
-                    eidx++;
-                    const uint32_t sh = 16 * (i & 1);
-                    p[i >> 1] = (p[i >> 1] & ~(0x7F80u << sh)) | (e << (7 + sh));
-                }
+        for (int i = 0; i < 16; i++) {
+            const uint32_t m = i < 8 ? m0 : m1;
+            if ((m >> (4 * (i & 7))) & 1u) {
+                uint32_t ex = 0;
+                if (e < a.n_esc) ex = table_s[a.esc[e]];
+                else bad = true;
+                e++;
+                const uint32_t sh = 16 * (i & 1);
+                p[i >> 1] = (p[i >> 1] & ~(0x7F80u << sh)) | (ex << (7 + sh));
             }
         }
-        // 16-byte chunks 2q and 2q+1 of the row, at their swizzled positions
-        const uint32_t c0 = (2 * q) ^ (t & 7), c1 = (2 * q + 1) ^ (t & 7);
-        *reinterpret_cast<uint4 *>(arow + c0 * 16) = make_uint4(p[0], p[1], p[2], p[3]);
-        *reinterpret_cast<uint4 *>(arow + c1 * 16) = make_uint4(p[4], p[5], p[6], p[7]);
     }
+    eidx += total;
+    const uint32_t c0 = (2 * q) ^ (t & 7), c1 = (2 * q + 1) ^ (t & 7);
+    *reinterpret_cast<uint4 *>(arow + c0 * 16) = make_uint4(p[0], p[1], p[2], p[3]);
+    *reinterpret_cast<uint4 *>(arow + c1 * 16) = make_uint4(p[4], p[5], p[6], p[7]);
 }
 
+constexpr uint32_t GT_THREADS = 640;   // 4 control/epilogue warps + 16 decoder warps
+
 template <bool R4>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(GT_THREADS, 1)
     k_gemm(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
            const __grid_constant__ CUtensorMap tm_nib, GemmArgs a) {
     extern __shared__ uint8_t smem_raw[];
@@ -195,7 +205,7 @@ __global__ void __launch_bounds__(256, 1)
         for (uint32_t i = 0; i < P; i++) {
             mbar_init(smem_u32(&bar_full[i]), 1);
             mbar_init(smem_u32(&bar_raw[i]), 1);
-            mbar_init(smem_u32(&bar_w[i]), 4);
+            mbar_init(smem_u32(&bar_w[i]), 16);
             mbar_init(smem_u32(&bar_empty[i]), 1);
         }
         mbar_init(smem_u32(&bar_done), 1);
@@ -206,7 +216,7 @@ __global__ void __launch_bounds__(256, 1)
         tmem_alloc(smem_u32(&tmem_slot), ncols);
         tmem_relinquish();
     }
-    table_s[tid] = a.table[tid];
+    if (tid < 256) table_s[tid] = a.table[tid];
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -265,16 +275,28 @@ __global__ void __launch_bounds__(256, 1)
             mma_commit(smem_u32(&bar_done));
         }
     } else if (warp >= 4) {
-        const uint32_t t = tid - 128;  // W row within the tile, and TMEM lane
         if (R4) {
-            // ---- decoders: thread t owns W row n0 + t
+            // ---- decoders: thread (t, q) owns chunk q of W row n0 + t
+            const uint32_t d = tid - 128, t = d >> 2, q = d & 3;
             const uint64_t row = n0 + t;
             const uint64_t kstart = (uint64_t)kb0 * GT_K;
             const uint64_t j = kstart / DGT_SEG;
             uint64_t eidx = a.seg[row * a.nseg + j];
-            for (uint64_t k = j * DGT_SEG; k < kstart; k += 2) {
-                const uint8_t b = a.nib[(row * a.K + k) / 2];
-                eidx += ((b & 15) == 15) + ((b >> 4) == 15);
+            {
+                // escapes of this row's segment before kstart: at most 448 nibbles,
+                // read as up to 14 independent 16-byte loads
+                const uint4 *np = reinterpret_cast<const uint4 *>(a.nib + (row * a.K + j * DGT_SEG) / 2);
+                const uint32_t nv = (uint32_t)((kstart - j * DGT_SEG) / 32);
+                uint32_t cnt = 0;
+#pragma unroll
+                for (uint32_t v = 0; v < DGT_SEG / 32 - 2; v++) {
+                    if (v < nv) {
+                        const uint4 qv = np[v];
+                        cnt += __popc(nib15_mask(qv.x)) + __popc(nib15_mask(qv.y)) + __popc(nib15_mask(qv.z)) +
+                               __popc(nib15_mask(qv.w));
+                    }
+                }
+                eidx += cnt;
             }
             bool bad = false;
             for (uint32_t i = 0; i < nkb; i++) {
@@ -284,13 +306,17 @@ __global__ void __launch_bounds__(256, 1)
                     *abortp = 1;
                     break;
                 }
-                decode_row64(a, RS(s) + t * 64, RN(s) + t * 32, A(s) + t * 128, t, eidx, table_s, bad);
+                decode_chunk16(a, RS(s) + t * 64, RN(s) + t * 32, A(s) + t * 128, t, q, eidx, table_s, bad);
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&bar_w[s]));
             }
             if (bad) set_status(a.status, DGT_ERR_CORRUPT);
         }
+        if (warp >= 8) {
+            // decoder-only warps are done
+        } else {
+        const uint32_t t = tid - 128;  // accumulator row, TMEM lane
         // ---- epilogue: thread t holds accumulator row t (W row n0 + t)
         const bool ok = wait_or_abort(smem_u32(&bar_done), 0, abortp) || mbar_wait(smem_u32(&bar_done), 0);
         tc_fence_after();
@@ -315,6 +341,7 @@ __global__ void __launch_bounds__(256, 1)
                     }
                 }
             }
+        }
         }
     }
     tc_fence_before();
@@ -390,9 +417,9 @@ static int launch_gemm(GemmArgs &a, const void *w_or_sm, const uint16_t *d_X, vo
     }
     const size_t smem = (size_t)a.stages * gemm_stage_bytes(R4, a.mt) + 1024;
     int bps = 0;
-    if (prepare_kernel((const void *)k_gemm<R4>, smem, 256, &bps) != DGT_OK) return DGT_ERR_CUDA;
+    if (prepare_kernel((const void *)k_gemm<R4>, smem, GT_THREADS, &bps) != DGT_OK) return DGT_ERR_CUDA;
     dim3 grid((unsigned)(a.N / GT_N), (unsigned)((a.M + a.mt - 1) / a.mt), a.split);
-    k_gemm<R4><<<grid, 256, smem, st>>>(tm_x, tm_w, tm_nib, a);
+    k_gemm<R4><<<grid, GT_THREADS, smem, st>>>(tm_x, tm_w, tm_nib, a);
     if (a.split > 1) {
         DeviceInfo di;
         if (device_info(&di) != DGT_OK) return DGT_ERR_CUDA;
@@ -435,7 +462,7 @@ extern "C" int dgt_gemm_default_plan(uint64_t M, uint64_t N, uint64_t K, dgt_gem
     if (!plan || M == 0 || N == 0 || K == 0) return DGT_ERR_ARG;
     uint32_t mt = M <= 256 ? (uint32_t)((M + 15) / 16 * 16) : 256u;
     const uint64_t tiles = ((N + GT_N - 1) / GT_N) * ((M + mt - 1) / mt);
-    uint64_t split = (152 + tiles - 1) / tiles;
+    uint64_t split = tiles >= 152 ? 1 : 152 / tiles;   // one CTA per SM, one wave
     const uint64_t kb = K / GT_K;
     if (split > kb / 4) split = kb / 4;
     if (split > 16) split = 16;

@@ -13,11 +13,11 @@
 //  1. k_moe_route (one CTA): counts the pairs per expert, lists the experts
 //     in use, and places every pair (t, j) in its expert's list in (t, j)
 //     order -- deterministic, no atomics in the placement.
-//  2. k_moe: one warp per (expert in use, row, slice) unit streams that row
-//     slice of the expert once, decodes each 16-weight lane chunk once and
-//     runs one fmaf chain per routed token (up to 16 per pass) against x
-//     staged in shared memory; the butterfly-reduced slice results go to the
-//     workspace.
+//  2. k_moe: a warp takes two rows of an expert in use at a time and streams
+//     each row once (up to 8 rounds of loads in flight), decodes each 16-weight
+//     lane chunk once and runs one fmaf chain per routed token (up to 4 per
+//     pass) against x staged in shared memory; at each slice end the chains
+//     are butterfly-reduced into the workspace.
 //  3. k_moe_combine: adds each pair's slices left to right (y) and applies
 //     the routing weights in slot order (out).
 #include <cuda_runtime.h>
@@ -30,7 +30,7 @@
 namespace dgt {
 
 constexpr int MW = 8;               // warps per CTA
-constexpr uint32_t MOE_TPASS = 16;  // tokens per pass over a row slice
+constexpr uint32_t MOE_TPASS = 4;   // tokens per pass over a row
 constexpr uint32_t MOE_MAX_EXPERTS = 4096;
 constexpr uint32_t MOE_MAX_PAIRS = 1u << 16;
 constexpr uint32_t MOE_XS_LIMIT = 160 * 1024;  // x of every token in shared memory
@@ -113,8 +113,36 @@ __global__ void __launch_bounds__(1024) k_moe_route(MoeArgs a) {
     (void)nact;
 }
 
+// One round of one expert row for one lane: eight bf16 pairs (escapes patched).
 template <bool R4>
-__global__ void __launch_bounds__(MW * 32) k_moe(MoeArgs a) {
+__device__ __forceinline__ void moe_round(const MoeArgs &a, uint4 sv, uint2 nv, uint4 hv, uint32_t c, uint32_t b,
+                                          bool act, uint8_t *escb, const uint8_t *table_s, uint32_t p[8]) {
+    if (R4) {
+        r4_dec16(nv, sv, a.L, p);
+        if (c) {
+            const uint32_t lane = lane_id();
+            const uint32_t cc = c > DGT_SEG ? DGT_SEG : c;
+            for (uint32_t i = lane; i < cc; i += 32) escb[i] = (uint64_t)b + i < a.n_esc ? a.esc[b + i] : 0;
+            __syncwarp();
+            const uint32_t m0 = act ? nib15_mask(nv.x) : 0u, m1 = act ? nib15_mask(nv.y) : 0u;
+            if (!patch_escapes(p, m0, m1, cc, escb, table_s) && lane == 0) set_status(a.status, DGT_ERR_CORRUPT);
+            __syncwarp();
+        }
+    } else {
+        p[0] = sv.x; p[1] = sv.y; p[2] = sv.z; p[3] = sv.w;
+        p[4] = hv.x; p[5] = hv.y; p[6] = hv.z; p[7] = hv.w;
+    }
+}
+
+// A warp takes MOE_RG consecutive rows of one expert in use; for each row it
+// issues the loads of up to 8 rounds at once, then walks the rounds slice by
+// slice, running one fmaf chain per routed token; at the end of each slice
+// the chains are butterfly-reduced and stored as that slice's partials.
+constexpr uint32_t MOE_RG = 2;
+constexpr uint32_t MOE_RB = 4;   // rounds loaded at once
+
+template <bool R4>
+__global__ void __launch_bounds__(MW * 32, 2) k_moe(MoeArgs a) {
     extern __shared__ uint4 xs[];  // [token][round][half][lane]
     __shared__ uint8_t table_s[256];
     __shared__ uint8_t escb[MW][DGT_SEG];
@@ -131,78 +159,85 @@ __global__ void __launch_bounds__(MW * 32) k_moe(MoeArgs a) {
     const uint32_t P = a.tokens * a.topk;
     const uint32_t nact = a.active[P];
     const uint32_t S = a.S, log2S = __ffs(S) - 1;
-    const uint64_t per_expert = a.ne << log2S;
-    const uint64_t units = (uint64_t)nact * per_expert;
+    const uint64_t groups = (a.ne + MOE_RG - 1) / MOE_RG;
+    const uint64_t units = (uint64_t)nact * groups;
     const uint32_t Jm1 = J - 1;
     const bool last_ok = 16 * lane < K - 512 * Jm1;
     for (uint64_t uu = (uint64_t)blockIdx.x * MW + w; uu < units; uu += (uint64_t)gridDim.x * MW) {
-        const uint32_t ai = (uint32_t)(uu / per_expert);
-        const uint64_t rs = uu - (uint64_t)ai * per_expert;
-        const uint64_t r = rs >> log2S;
-        const uint32_t s = (uint32_t)rs & (S - 1);
+        const uint32_t ai = (uint32_t)(uu / groups);
+        const uint64_t g = uu - (uint64_t)ai * groups;
         const uint32_t e = a.active[ai];
         const uint32_t l0 = a.eoff[e], nt = a.eoff[e + 1] - l0;
-        const uint64_t grow = (uint64_t)e * a.ne + r;
-        const uint32_t j0 = (s * J) >> log2S, j1 = ((s + 1) * J) >> log2S;
         for (uint32_t tg = 0; tg < nt; tg += MOE_TPASS) {
             const uint32_t ntg = min(MOE_TPASS, nt - tg);
             const uint32_t ent = lane < ntg ? a.elist[l0 + tg + lane] : 0u;
-            float acc[MOE_TPASS];
             uint32_t tk[MOE_TPASS];
 #pragma unroll
-            for (int i = 0; i < (int)MOE_TPASS; i++) {
-                acc[i] = 0.0f;
-                tk[i] = (__shfl_sync(DGT_FULL, ent, i) >> 8) % a.tokens;
-            }
-            for (uint32_t j = j0; j < j1; j++) {
-                const bool act = j != Jm1 || last_ok;
-                const uint64_t f = grow * a.cols + (uint64_t)j * 512 + 16 * lane;
-                uint32_t p[8];
-                if (R4) {
-                    uint4 sv = make_uint4(0, 0, 0, 0);
-                    uint2 nv = make_uint2(0, 0);
-                    if (act) {
-                        sv = ldg_stream16(a.sm + f);
-                        nv = ldg_stream8(a.nib + f / 2);
-                    }
-                    r4_dec16(nv, sv, a.L, p);
-                    const uint32_t *sp = a.seg + grow * a.nseg + j;
-                    const uint32_t b = sp[0], c = sp[1] - b;
-                    if (c) {
-                        const uint32_t cc = c > DGT_SEG ? DGT_SEG : c;
-                        for (uint32_t i = lane; i < cc; i += 32)
-                            escb[w][i] = (uint64_t)b + i < a.n_esc ? a.esc[b + i] : 0;
-                        __syncwarp();
-                        const uint32_t m0 = act ? nib15_mask(nv.x) : 0u, m1 = act ? nib15_mask(nv.y) : 0u;
-                        if (!patch_escapes(p, m0, m1, cc, escb[w], table_s) && lane == 0)
-                            set_status(a.status, DGT_ERR_CORRUPT);
-                        __syncwarp();
-                    }
-                } else {
-                    uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
-                    if (act) {
-                        lo = ldg_stream16(a.W + f);
-                        hi = ldg_stream16(a.W + f + 8);
-                    }
-                    p[0] = lo.x; p[1] = lo.y; p[2] = lo.z; p[3] = lo.w;
-                    p[4] = hi.x; p[5] = hi.y; p[6] = hi.z; p[7] = hi.w;
-                }
-                if (act) {
+            for (int i = 0; i < (int)MOE_TPASS; i++) tk[i] = (__shfl_sync(DGT_FULL, ent, i) >> 8) % a.tokens;
+            for (uint64_t r = g * MOE_RG; r < a.ne && r < (g + 1) * MOE_RG; r++) {
+                const uint64_t grow = (uint64_t)e * a.ne + r;
+                float acc[MOE_TPASS];
 #pragma unroll
-                    for (int i = 0; i < (int)MOE_TPASS; i++) {
-                        if ((uint32_t)i < ntg) acc[i] = fma_chunk16(p, xs + (size_t)tk[i] * J * 64, j, lane, acc[i]);
+                for (int i = 0; i < (int)MOE_TPASS; i++) acc[i] = 0.0f;
+                uint32_t s = 0, send = J >> log2S;  // current slice and its end round
+                for (uint32_t jb = 0; jb < J; jb += MOE_RB) {
+                    uint4 sv[MOE_RB], hv[MOE_RB];
+                    uint2 nv[MOE_RB];
+                    uint32_t sgb = 0, sgc = 0;
+                    if (R4 && lane <= MOE_RB && jb + lane <= J) {
+                        const uint32_t *sp = a.seg + grow * a.nseg + jb + lane;
+                        sgb = sp[0];
+                        sgc = jb + lane < J ? sp[1] - sgb : 0u;
                     }
-                }
-            }
 #pragma unroll
-            for (int i = 0; i < (int)MOE_TPASS; i++) {
-                if ((uint32_t)i < ntg) {
-                    float v = acc[i];
+                    for (uint32_t t = 0; t < MOE_RB; t++) {
+                        const uint32_t j = jb + t;
+                        const bool act = j < J && (j != Jm1 || last_ok);
+                        const uint64_t f = grow * a.cols + (uint64_t)j * 512 + 16 * lane;
+                        sv[t] = hv[t] = make_uint4(0, 0, 0, 0);
+                        nv[t] = make_uint2(0, 0);
+                        if (act) {
+                            if (R4) {
+                                sv[t] = ldg_stream16(a.sm + f);
+                                nv[t] = ldg_stream8(a.nib + f / 2);
+                            } else {
+                                sv[t] = ldg_stream16(a.W + f);
+                                hv[t] = ldg_stream16(a.W + f + 8);
+                            }
+                        }
+                    }
 #pragma unroll
-                    for (int d = 16; d >= 1; d >>= 1) v += __shfl_xor_sync(DGT_FULL, v, d);
-                    const uint32_t en = __shfl_sync(DGT_FULL, ent, i);
-                    const uint32_t q = (en >> 8) * a.topk + (en & 0xFF);
-                    if (lane == 0) a.partial[((uint64_t)q * a.ne + r) * S + s] = v;
+                    for (uint32_t t = 0; t < MOE_RB; t++) {
+                        const uint32_t j = jb + t;
+                        if (j >= J) break;
+                        const bool act = j != Jm1 || last_ok;
+                        const uint32_t c = R4 ? __shfl_sync(DGT_FULL, sgc, t) : 0u;
+                        const uint32_t b = R4 ? __shfl_sync(DGT_FULL, sgb, t) : 0u;
+                        uint32_t p[8];
+                        moe_round<R4>(a, sv[t], nv[t], hv[t], c, b, act, escb[w], table_s, p);
+                        if (act) {
+#pragma unroll
+                            for (int i = 0; i < (int)MOE_TPASS; i++)
+                                if ((uint32_t)i < ntg) acc[i] = fma_chunk16(p, xs + (size_t)tk[i] * J * 64, j, lane, acc[i]);
+                        }
+                        if (j + 1 == send) {
+                            // end of slice s: reduce and store, start the next slice from +0
+#pragma unroll
+                            for (int i = 0; i < (int)MOE_TPASS; i++) {
+                                if ((uint32_t)i < ntg) {
+                                    float v = acc[i];
+#pragma unroll
+                                    for (int d = 16; d >= 1; d >>= 1) v += __shfl_xor_sync(DGT_FULL, v, d);
+                                    const uint32_t en = __shfl_sync(DGT_FULL, ent, i);
+                                    const uint64_t q = (uint64_t)(en >> 8) * a.topk + (en & 0xFF);
+                                    if (lane == 0) a.partial[(q * a.ne + r) * S + s] = v;
+                                    acc[i] = 0.0f;
+                                }
+                            }
+                            s++;
+                            send = ((s + 1) * J) >> log2S;
+                        }
+                    }
                 }
             }
         }
@@ -247,7 +282,7 @@ int launch_moe(MoeArgs &a, void *d_ws, size_t ws_bytes, cudaStream_t st) {
     int bps = 0;
     if (prepare_kernel((const void *)k_moe<R4>, smem, MW * 32, &bps) != DGT_OK) return DGT_ERR_CUDA;
     const uint64_t pairs = (uint64_t)a.tokens * a.topk;
-    const uint64_t max_units = (pairs < a.n_experts ? pairs : (uint64_t)a.n_experts) * a.ne * a.S;
+    const uint64_t max_units = (pairs < a.n_experts ? pairs : (uint64_t)a.n_experts) * ((a.ne + 1) / 2);
     uint64_t grid = (max_units + MW - 1) / MW;
     if (grid > (uint64_t)di.sms * bps) grid = (uint64_t)di.sms * bps;
     if (grid < 1) grid = 1;

@@ -307,8 +307,9 @@ int dgt_moe_gemv_bf16(const uint16_t *d_W, uint64_t rows, uint64_t cols, uint32_
  * the number of K slices split_k (added left to right after the MMAs).  The
  * R4 GEMM and the BF16 GEMM with the same plan issue the same MMA sequence on
  * byte-identical tiles, so their outputs are bit-identical.
- * dgt_gemm_default_plan: m_tile = round_up(M, 16) up to 256; split_k = enough
- * slices for 152 tiles, at most K/256 and 16.
+ * dgt_gemm_default_plan: m_tile = round_up(M, 16) up to 256; split_k =
+ * floor(152 / tiles) (one wave of one CTA per SM; 1 when tiles >= 152), at
+ * most K/256 and 16.
  * d_X: device bf16 [M, K].  d_Y32 / d_Y: device float / bf16 [M, N] (either
  * may be NULL).  d_ws: device workspace of dgt_gemm_workspace_bytes() bytes
  * (split partials; NULL when split_k == 1).  Limits: N % 128 == 0,
