@@ -8,11 +8,10 @@
 // warp prefix sum, output staged in shared memory and written coalesced),
 // re-designed for sm_103a:
 //  - one warp per group of 32 blocks (format 2) or 32 tiles (format 1), one
-//    lane per block/tile; a persistent grid of 256-thread CTAs;
-//  - format 2: each lane decodes its Rice block with a 4096-entry shared
-//    table indexed by the next 12 stream bits, which yields up to six ranks,
-//    their bit count and their nibbles in one lookup; long codes and ranks
-//    >= 15 take a short window decode;
+//    lane per block/tile; a persistent grid;
+//  - format 2: each lane decodes its Rice block two codes at a time through a
+//    12-bit window table in shared memory, so a full block is exactly 32
+//    table steps; windows the table does not finish take an out-of-line step;
 //  - escapes (ranks >= 15) are collected per lane, placed by a warp prefix sum
 //    from the group's escape base, and the row-segment escape index (seg) is
 //    written for every segment that starts inside the group;
@@ -26,10 +25,6 @@
 
 namespace dgt {
 
-constexpr int TW = 8;           // warps per CTA
-constexpr int K1_CAP = 384;     // staged stream words per group (else read from global)
-constexpr int K2_E1CAP = 256;   // staged format-1 escapes per group
-constexpr int LIST = 4;         // per-lane escape list (format 1), overflow re-walks
 
 // ---------------------------------------------------------------------------
 // segment starts inside a unit [B0, B0 + cnt): seg index and offset
@@ -59,6 +54,19 @@ __device__ __forceinline__ void next_seg_start(SegWalk &s, uint64_t cols) {
 
 // ---------------------------------------------------------------------------
 // format 2 (Rice) -> R4
+//
+// One warp per group, one lane per 64-rank block.  A full Rice block is
+// decoded in exactly 32 steps of two codes each: the next 12 stream bits index
+// a table whose entry holds both codes' ranks as one output byte and the bits
+// they use, so a step is a few integer instructions, its output byte lands at
+// a fixed place and no lane waits on another.  The table is replicated REP
+// times, copy c in the banks = c (mod REP), so that only the lanes sharing a
+// copy can conflict.  An entry also carries the rank of one escape
+// (rank >= 15) when both codes fit; windows the table cannot finish (codes
+// longer than the window, two escapes) take an out-of-line step that decodes
+// the two codes one by one.  The next group's stream is copied to shared
+// memory (cp.async) while this one decodes.  Partial and raw blocks, and
+// groups too long to stage, take a per-code path.
 // ---------------------------------------------------------------------------
 struct F2Args {
     const uint32_t *words;
@@ -74,30 +82,55 @@ struct F2Args {
     int32_t *status;
 };
 
-struct K1Smem {
-    uint32_t lut[4096];
-    uint32_t buf[TW][K1_CAP + 2];
-    uint32_t outw[TW][256];
-    uint8_t escr[TW][2048];
+#ifndef DGT_RICE_REP
+#define DGT_RICE_REP 8
+#endif
+constexpr int RW = 32;          // warps per CTA
+constexpr int RWIN = 12;        // table window bits
+constexpr int REP = DGT_RICE_REP;  // table copies (lane l uses copy l mod REP)
+constexpr int RCAP = 192;       // staged stream words per group (about 170 at 2.7 bits/rank)
+constexpr int RPAD = 16;        // zero words after the staged stream
+constexpr int RBUF = RCAP + RPAD;
+constexpr int RLIST = 16;       // escapes kept per lane; more re-walk the block
+constexpr uint32_t RARE = 1u << 26;
+
+// Per-lane escape record of the block being decoded.
+struct LaneEsc {
+    unsigned long long emask;   // bit s: rank s of the block is an escape
+    uint32_t ec;                // escapes seen
+    uint32_t bad;
+    uint32_t end;               // bit position after the block
+    uint32_t cur;               // which stream buffer holds the group
+    uint8_t list[RLIST];        // escape ranks, in order
 };
 
-// Table entry for a 12-bit window v (bit 0 = next stream bit): the complete
-// codes at its start, up to six, each of rank < 15.
-// bits 0..2: count, 3..6: bits used, 7..30: ranks as nibbles.
-__device__ __forceinline__ uint32_t rice_lut_entry(uint32_t v, int k) {
-    uint32_t pos = 0, ns = 0, ranks = 0;
-    while (ns < 6) {
+struct RiceSmem {
+    uint32_t lut[(1 << RWIN) * REP];
+    uint32_t buf[2][RW][RBUF];
+    LaneEsc le[RW][32];
+    int k;
+};
+
+// Table entry for window v (bit 0 = next stream bit).  Both codes fit:
+// bits 0..4 and 27..31 = their bit count, 8..15 = output byte (min(rank,15)
+// nibbles); with one escape also bit 24/25 (first/second code), 16..23 = its
+// rank, and RARE.  Otherwise RARE alone.
+__device__ __forceinline__ uint32_t rice_pair_entry(uint32_t v, int k) {
+    uint32_t pos = 0, byte = 0, escf = 0, escr = 0;
+    for (int s = 0; s < 2; s++) {
         uint32_t q = 0;
-        while (pos + q < 12 && !((v >> (pos + q)) & 1u)) q++;
-        if (pos + q >= 12 || pos + q + 1 + (uint32_t)k > 12) break;
-        uint32_t rem = (v >> (pos + q + 1)) & ((1u << k) - 1u);
-        uint32_t r = (q << k) | rem;
-        if (r >= 15) break;
-        ranks |= r << (4 * ns);
-        ns++;
+        while (pos + q < RWIN && !((v >> (pos + q)) & 1u)) q++;
+        if (pos + q + 1 + (uint32_t)k > RWIN) return RARE;
+        const uint32_t r = (q << k) | ((v >> (pos + q + 1)) & ((1u << k) - 1u));
+        if (r >= 15) {
+            if (escf) return RARE;
+            escf = 1u << (24 + s);
+            escr = r;
+        }
+        byte |= min(r, 15u) << (4 * s);
         pos += q + 1 + k;
     }
-    return ns | (pos << 3) | (ranks << 7);
+    return pos | (byte << 8) | (escr << 16) | escf | (escf ? RARE : 0u) | (pos << 27);
 }
 
 template <class Src>
@@ -107,205 +140,316 @@ struct WordReader {
     __device__ __forceinline__ uint32_t operator()(uint32_t i) const { return i < nw ? src[i] : 0u; }
 };
 
-// Decode one block of cnt ranks starting at bit pos.  Nibble words go to
-// out[0..], escape ranks to escr[position]; returns the escape count and the
-// escape position mask; *end gets the bit position after the block.
+// One code at bit pos (Rice parameter k, or 8 raw bits when raw): returns its
+// rank and advances pos.  Unary runs longer than 255 or ranks above 255 set
+// bad.
 template <class Rd>
-__device__ __forceinline__ uint32_t rice_block(const Rd &rd, uint32_t pos, uint32_t cnt, uint32_t q,
-                                               int k, const uint32_t *lut, uint32_t *out,
-                                               uint8_t *escr, uint64_t &emask, uint32_t *end,
-                                               bool &bad) {
-    uint32_t wi = pos >> 5;
-    uint32_t lo = rd(wi), hi = rd(wi + 1);
-    uint64_t acc = 0;
-    uint32_t fill = 0, wo = 0, sym = 0, ec = 0;
-    const uint32_t kmask = (1u << k) - 1u;
-    emask = 0;
-    while (sym < cnt) {
-        uint32_t win = __funnelshift_r(lo, hi, pos & 31);
-        uint32_t add, nbits, nsym;
-        if (q != 255) {
-            uint32_t e = lut[win & 0xFFFu];
-            nsym = e & 7u;
-            if (nsym) {
-                add = e >> 7;
-                nbits = (e >> 3) & 15u;
-                if (sym + nsym > cnt) {
-                    // last lookup of the block: take only the codes that belong to it
-                    uint32_t m = cnt - sym, t = win;
-                    nbits = 0;
-                    for (uint32_t i = 0; i < m; i++) {
-                        uint32_t z = __ffs(t) - 1;
-                        nbits += z + 1 + k;
-                        t >>= z + 1 + k;
-                    }
-                    add &= (1u << (4 * m)) - 1u;
-                    nsym = m;
-                }
-            } else {
-                // one code that the table does not finish: a long code or rank >= 15
-                uint32_t z;
-                uint32_t r;
-                if (win != 0 && (z = __ffs(win) - 1) + 1 + k <= 32) {
-                    r = (z << k) | ((win >> (z + 1)) & kmask);
-                    nbits = z + 1 + k;
-                } else {
-                    // more than 32 bits: walk word by word (bounded by 255 zeros)
-                    uint32_t p = pos, zz = 0;
-                    for (;;) {
-                        uint32_t wv = rd(p >> 5) >> (p & 31);
-                        uint32_t avail = 32 - (p & 31);
-                        if (wv) {
-                            uint32_t f = __ffs(wv) - 1;
-                            zz += f;
-                            p += f;
-                            break;
-                        }
-                        zz += avail;
-                        p += avail;
-                        if (zz > 255) break;
-                    }
-                    p += 1;
-                    uint32_t rem = __funnelshift_r(rd(p >> 5), rd((p >> 5) + 1), p & 31) & kmask;
-                    r = (zz << k) | rem;
-                    nbits = p + k - pos;
-                    if (zz > 255) bad = true;
-                }
-                if (r > 255) { bad = true; r = 255; }
-                if (r >= 15) {
-                    escr[sym] = (uint8_t)r;
-                    emask |= 1ull << sym;
-                    ec++;
-                    r = 15;
-                }
-                add = r;
-                nsym = 1;
-            }
-        } else {
-            uint32_t r = win & 0xFFu;
-            if (r >= 15) {
-                escr[sym] = (uint8_t)r;
-                emask |= 1ull << sym;
-                ec++;
-                r = 15;
-            }
-            add = r;
-            nbits = 8;
-            nsym = 1;
-        }
-        acc |= (uint64_t)add << fill;
-        fill += 4 * nsym;
-        sym += nsym;
-        pos += nbits;
-        if (fill >= 32) {
-            out[wo++] = (uint32_t)acc;
-            acc >>= 32;
-            fill -= 32;
-        }
-        uint32_t nwi = pos >> 5;
-        if (nwi != wi) {
-            if (nwi == wi + 1) {
-                lo = hi;
-                hi = rd(nwi + 1);
-            } else {
-                lo = rd(nwi);
-                hi = rd(nwi + 1);
-            }
-            wi = nwi;
-        }
+__device__ __forceinline__ uint32_t rice_code(const Rd &rd, uint32_t &pos, int k, bool raw, bool &bad) {
+    const uint32_t wi = pos >> 5;
+    const uint32_t win = __funnelshift_r(rd(wi), rd(wi + 1), pos);
+    if (raw) {
+        pos += 8;
+        return win & 0xFFu;
     }
-    if (fill) out[wo] = (uint32_t)acc;
-    *end = pos;
-    return ec;
+    const uint32_t kmask = (1u << k) - 1u;
+    uint32_t r;
+    uint32_t z;
+    if (win != 0 && (z = __ffs(win) - 1) + 1 + (uint32_t)k <= 32) {
+        r = (z << k) | (k ? (win >> (z + 1)) & kmask : 0u);
+        pos += z + 1 + k;
+    } else {
+        // the unary part runs past this window: walk word by word
+        uint32_t p = pos, zz = 0;
+        for (;;) {
+            const uint32_t wv = rd(p >> 5) >> (p & 31);
+            const uint32_t avail = 32 - (p & 31);
+            if (wv) {
+                const uint32_t f = __ffs(wv) - 1;
+                zz += f;
+                p += f;
+                break;
+            }
+            zz += avail;
+            p += avail;
+            if (zz > 255) break;
+        }
+        p += 1;
+        const uint32_t rem = __funnelshift_r(rd(p >> 5), rd((p >> 5) + 1), p) & kmask;
+        r = (zz << k) | rem;
+        pos = p + k;
+        if (zz > 255) bad = true;
+    }
+    if (r > 255) {
+        bad = true;
+        r = 255;
+    }
+    return r;
 }
 
-__global__ void __launch_bounds__(TW * 32) k_rice_to_r4(F2Args a) {
+__device__ __forceinline__ void note_escape(LaneEsc *le, uint32_t r, uint32_t s) {
+    const uint32_t c = le->ec;
+    if (c < RLIST) le->list[c] = (uint8_t)r;
+    le->ec = c + 1;
+    le->emask |= 1ull << s;
+}
+
+struct RareOut {
+    uint32_t e, pos, win;
+};
+
+// Out-of-line part of step j: record the table entry's escape, or decode the
+// two codes at pos one by one (returning an entry with the output byte and a
+// zero bit count, pos after the codes, clamped to the block end, and the
+// window there).  The lane's state is read from shared memory so that the
+// call passes four words.
+__device__ __noinline__ RareOut rice_rare(uint32_t e, uint32_t pos, uint32_t win, uint32_t j) {
     extern __shared__ uint4 smem_raw[];
-    K1Smem &S = *reinterpret_cast<K1Smem *>(smem_raw);
-    for (uint32_t v = threadIdx.x; v < 4096; v += blockDim.x) S.lut[v] = rice_lut_entry(v, a.k);
+    RiceSmem &S = *reinterpret_cast<RiceSmem *>(smem_raw);
+    const uint32_t w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    LaneEsc *le = &S.le[w][lane];
+    RareOut o;
+    if (e & (3u << 24)) {
+        note_escape(le, (e >> 16) & 0xFFu, 2 * j + ((e >> 25) & 1u));
+        o.e = e;
+        o.pos = pos;
+        o.win = win;
+        return o;
+    }
+    const uint32_t *buf = S.buf[le->cur][w];
+    const int k = S.k;
+    const uint32_t end = le->end;
+    WordReader<const uint32_t *> rd{buf, RBUF};
+    bool bad = false;
+    const uint32_t r0 = rice_code(rd, pos, k, false, bad);
+    const uint32_t r1 = rice_code(rd, pos, k, false, bad);
+    if (pos > end) {
+        bad = true;
+        pos = end;
+    }
+    if (r0 >= 15) note_escape(le, r0, 2 * j);
+    if (r1 >= 15) note_escape(le, r1, 2 * j + 1);
+    if (bad) le->bad = 1;
+    o.e = (min(r0, 15u) | (min(r1, 15u) << 4)) << 8;
+    o.pos = pos;
+    o.win = __funnelshift_r(buf[pos >> 5], buf[(pos >> 5) + 1], pos);
+    return o;
+}
+
+// Step j of a full block: returns the table entry (output byte at bits 8..15).
+template <bool REFILL>
+__device__ __forceinline__ uint32_t rice_step(const uint32_t *lutc, const uint32_t *buf, uint32_t &pos,
+                                              uint32_t &win, uint32_t prev, uint32_t j) {
+    if (REFILL) {
+        const uint32_t wi = pos >> 5;
+        win = __funnelshift_r(buf[wi], buf[wi + 1], pos);
+    } else {
+        win = __funnelshift_r(win, 0u, prev);
+    }
+    uint32_t e = lutc[(win & ((1u << RWIN) - 1u)) * REP];
+    if (e & RARE) {
+        const RareOut o = rice_rare(e, pos, win, j);
+        e = o.e;
+        pos = o.pos;
+        win = o.win;
+    }
+    pos += e >> 27;
+    return e;
+}
+
+// Per-code path for one block: nibbles go straight to nib (bytes), escapes to
+// the lane's record.  Returns the bit position after the block.
+template <class Rd>
+__device__ __noinline__ uint32_t rice_block_slow(Rd rd, uint32_t pos, uint32_t cnt, bool raw, int k,
+                                                 uint8_t *nib, LaneEsc *le) {
+    bool bad = false;
+    uint32_t byte = 0;
+    for (uint32_t s = 0; s < cnt; s++) {
+        const uint32_t r = rice_code(rd, pos, k, raw, bad);
+        if (r >= 15) note_escape(le, r, s);
+        byte |= min(r, 15u) << (4 * (s & 1));
+        if ((s & 1) || s + 1 == cnt) {
+            nib[s >> 1] = (uint8_t)byte;
+            byte = 0;
+        }
+    }
+    if (bad) le->bad = 1;
+    return pos;
+}
+
+// Escapes of one block written straight to esc (more than RLIST of them).
+template <class Rd>
+__device__ __noinline__ void rice_block_escapes(Rd rd, uint32_t pos, uint32_t cnt, bool raw, int k, uint8_t *dst) {
+    bool bad = false;
+    for (uint32_t s = 0; s < cnt; s++) {
+        const uint32_t r = rice_code(rd, pos, k, raw, bad);
+        if (r >= 15) *dst++ = (uint8_t)r;
+    }
+}
+
+__device__ __forceinline__ void cp_async4(uint32_t *dst, const uint32_t *src, uint32_t bytes) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+
+// Copy group g's stream words (up to RBUF; zeros after its end) into dst.
+__device__ __forceinline__ void rice_stage(const F2Args &a, uint64_t g, uint32_t *dst, uint32_t lane) {
+    if (g < a.ngrp) {
+        const uint64_t w0 = a.grp[2 * g];
+        const uint64_t w1 = g + 1 < a.ngrp ? (uint64_t)a.grp[2 * g + 2] : a.n_words;
+        const uint64_t nw = (w1 > w0 && w1 <= a.n_words && w0 < a.n_words) ? w1 - w0 : 0;
+        for (uint32_t i = lane; i < RBUF; i += 32) {
+            const bool in = i < nw;
+            cp_async4(dst + i, in ? a.words + w0 + i : a.words, in ? 4u : 0u);
+        }
+    }
+    cp_async_commit();
+}
+
+__global__ void __launch_bounds__(RW * 32, 1) k_rice_to_r4(F2Args a) {
+    extern __shared__ uint4 smem_raw[];
+    RiceSmem &S = *reinterpret_cast<RiceSmem *>(smem_raw);
+    static_assert(REP % 4 == 0, "table rows are written as uint4");
+    for (uint32_t v = threadIdx.x; v < (1u << RWIN); v += blockDim.x) {
+        const uint32_t e = rice_pair_entry(v, a.k);
+#pragma unroll
+        for (int c = 0; c < REP / 4; c++) reinterpret_cast<uint4 *>(S.lut)[v * (REP / 4) + c] = make_uint4(e, e, e, e);
+    }
+    if (threadIdx.x == 0) S.k = a.k;
     if (blockIdx.x == 0 && threadIdx.x == 0) a.seg[a.seg_last] = (uint32_t)a.n_esc;
     __syncthreads();
     const uint32_t w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint64_t nbytes = (a.n + 1) / 2;
-    for (uint64_t g = (uint64_t)blockIdx.x * TW + w; g < a.ngrp; g += (uint64_t)gridDim.x * TW) {
+    const uint32_t *lutc = S.lut + (lane & (REP - 1));
+    LaneEsc *le = &S.le[w][lane];
+    const int k = a.k;
+    // row / column of the group's first rank, stepped with the grid stride
+    const uint64_t g0 = (uint64_t)blockIdx.x * RW + w, G = (uint64_t)gridDim.x * RW;
+    const uint64_t GS = (uint64_t)DGT_GROUP * DGT_BLOCK;
+    uint64_t r0 = (g0 * GS) / a.cols, c0 = (g0 * GS) % a.cols;
+    const uint64_t step_r = (G * GS) / a.cols, step_c = (G * GS) % a.cols;
+    rice_stage(a, g0, S.buf[0][w], lane);
+    uint32_t cur = 0;
+    for (uint64_t g = g0; g < a.ngrp; g += G, cur ^= 1) {
+        uint32_t *buf = S.buf[cur][w];
+        rice_stage(a, g + G, S.buf[cur ^ 1][w], lane);
         const uint64_t blk = g * DGT_GROUP + lane;
         const uint64_t B0 = blk * DGT_BLOCK;
         const uint32_t cnt = blk < a.nblk ? (uint32_t)min((uint64_t)DGT_BLOCK, a.n - B0) : 0u;
         const uint32_t q = cnt ? a.blkq[blk] : 0u;
-        const uint32_t len = cnt == 0 ? 0u : (q != 255 ? cnt * (uint32_t)(a.k + 1) + q : 8u * cnt);
+        const uint32_t len = cnt == 0 ? 0u : (q != 255 ? cnt * (uint32_t)(k + 1) + q : 8u * cnt);
         uint32_t gbits;
         const uint32_t off = warp_excl_scan(len, &gbits);
         const uint32_t nw = (gbits + 31) / 32;
         const uint64_t gw0 = a.grp[2 * g], gbase = a.grp[2 * g + 1];
         const uint64_t next_w = g + 1 < a.ngrp ? (uint64_t)a.grp[2 * g + 2] : a.n_words;
         const uint64_t next_e = g + 1 < a.ngrp ? (uint64_t)a.grp[2 * g + 3] : a.n_esc;
+        // this lane's block: row and column of its first rank
+        uint64_t br = r0, bc = c0 + (uint64_t)DGT_BLOCK * lane;
+        if (bc >= a.cols) {
+            if (a.cols >= GS) {
+                bc -= a.cols;
+                br++;
+            } else {
+                br += bc / a.cols;
+                bc %= a.cols;
+            }
+        }
+        c0 += step_c;
+        r0 += step_r;
+        if (c0 >= a.cols) {
+            c0 -= a.cols;
+            r0++;
+        }
+        cp_async_wait1();
+        __syncwarp();
         if (gw0 + nw != next_w || next_w > a.n_words) {
             if (lane == 0) set_status(a.status, DGT_ERR_CORRUPT);
+            __syncwarp();
             continue;
         }
-        const bool staged = nw <= K1_CAP;
-        if (staged) {
-            for (uint32_t i = lane; i < nw + 2; i += 32) S.buf[w][i] = i < nw ? a.words[gw0 + i] : 0u;
-            __syncwarp();
-        }
-        uint64_t emask = 0;
-        uint32_t ec = 0, end = off;
+        const bool staged = nw <= RCAP;
+        const uint32_t end = off + len;
+        le->emask = 0;
+        le->ec = 0;
+        le->bad = 0;
+        le->end = end;
+        le->cur = cur;
         bool bad = false;
-        if (cnt) {
-            if (staged) {
-                WordReader<const uint32_t *> rd{S.buf[w], nw + 2};
-                ec = rice_block(rd, off, cnt, q, a.k, S.lut, &S.outw[w][8 * lane], &S.escr[w][64 * lane],
-                                emask, &end, bad);
-            } else {
-                WordReader<const uint32_t *> rd{a.words + gw0, nw};
-                ec = rice_block(rd, off, cnt, q, a.k, S.lut, &S.outw[w][8 * lane], &S.escr[w][64 * lane],
-                                emask, &end, bad);
+        if (staged && cnt == DGT_BLOCK && q != 255) {
+            uint32_t pos = off, win = 0, out[8];
+#pragma unroll
+            for (int it = 0; it < 8; it++) {
+                const uint32_t e0 = rice_step<true>(lutc, buf, pos, win, 0u, 4 * it + 0);
+                const uint32_t e1 = rice_step<false>(lutc, buf, pos, win, e0, 4 * it + 1);
+                const uint32_t e2 = rice_step<true>(lutc, buf, pos, win, 0u, 4 * it + 2);
+                const uint32_t e3 = rice_step<false>(lutc, buf, pos, win, e2, 4 * it + 3);
+                out[it] = __byte_perm(__byte_perm(e0, e1, 0x51u), __byte_perm(e2, e3, 0x51u), 0x5410u);
             }
-            if (end != off + len) bad = true;
+            if (pos != end) bad = true;
+            uint4 *dst = reinterpret_cast<uint4 *>(a.nib + B0 / 2);
+            dst[0] = make_uint4(out[0], out[1], out[2], out[3]);
+            dst[1] = make_uint4(out[4], out[5], out[6], out[7]);
+        } else if (cnt) {
+            uint32_t p;
+            if (staged)
+                p = rice_block_slow(WordReader<const uint32_t *>{buf, RBUF}, off, cnt, q == 255, k,
+                                    a.nib + B0 / 2, le);
+            else
+                p = rice_block_slow(WordReader<const uint32_t *>{a.words + gw0, nw}, off, cnt, q == 255, k,
+                                    a.nib + B0 / 2, le);
+            if (p != end) bad = true;
         }
-        __syncwarp();
-        // nibbles of the group, coalesced
-        const uint64_t b0 = g * 1024;
-        const uint32_t gbytes = (uint32_t)min((uint64_t)1024, nbytes - b0);
-        const uint8_t *ob = reinterpret_cast<const uint8_t *>(S.outw[w]);
-        if (gbytes == 1024) {
-            uint4 *dst = reinterpret_cast<uint4 *>(a.nib + b0);
-            const uint4 *src = reinterpret_cast<const uint4 *>(S.outw[w]);
-            dst[lane] = src[lane];
-            dst[lane + 32] = src[lane + 32];
-        } else {
-            for (uint32_t i = lane; i < gbytes; i += 32) a.nib[b0 + i] = ob[i];
-        }
-        // escapes and segment index
+        const uint32_t ec = le->ec;
+        const uint64_t emask = le->emask;
+        if (le->bad) bad = true;
+        // escapes, placed by a warp prefix sum from the group's escape base
         uint32_t etot;
         const uint32_t eb = warp_excl_scan(ec, &etot);
         if (gbase + etot != next_e || next_e > a.n_esc) bad = true;
         if (ec && !bad) {
-            uint64_t m = emask;
-            uint64_t dst = gbase + eb;
-            while (m) {
-                uint32_t i = __ffsll((long long)m) - 1;
-                m &= m - 1;
-                a.esc[dst++] = S.escr[w][64 * lane + i];
+            uint8_t *dst = a.esc + gbase + eb;
+            if (ec <= RLIST) {
+                for (uint32_t i = 0; i < ec; i++) dst[i] = le->list[i];
+            } else if (staged) {
+                rice_block_escapes(WordReader<const uint32_t *>{buf, RBUF}, off, cnt, q == 255, k, dst);
+            } else {
+                rice_block_escapes(WordReader<const uint32_t *>{a.words + gw0, nw}, off, cnt, q == 255, k, dst);
             }
         }
-        const uint64_t r0 = __shfl_sync(DGT_FULL, lane == 0 ? (g * 2048) / a.cols : 0ull, 0);
+        // row-segment escape index for every segment that starts in this block
         if (cnt && !bad) {
-            SegWalk s = first_seg_start(B0, r0, a.cols);
-            for (uint64_t f = s.r * a.cols + s.c; f < B0 + cnt; f = s.r * a.cols + s.c) {
-                uint32_t o = (uint32_t)(f - B0);
-                uint64_t before = o ? (emask & ((~0ull) >> (64 - o))) : 0ull;
-                a.seg[s.r * a.nseg + s.c / DGT_SEG] = (uint32_t)(gbase + eb + __popcll(before));
-                next_seg_start(s, a.cols);
+            uint32_t done = 0;
+            uint64_t rr = br, cc = bc;
+            while (done < cnt) {
+                for (uint64_t s = (cc + DGT_SEG - 1) / DGT_SEG * DGT_SEG; s < a.cols && s - cc < cnt - done;
+                     s += DGT_SEG) {
+                    const uint32_t o = done + (uint32_t)(s - cc);
+                    const uint64_t before = o ? (emask & ((~0ull) >> (64 - o))) : 0ull;
+                    a.seg[rr * a.nseg + s / DGT_SEG] = (uint32_t)(gbase + eb + __popcll(before));
+                }
+                done += (uint32_t)min(a.cols - cc, (uint64_t)(cnt - done));
+                rr++;
+                cc = 0;
             }
         }
         if (bad) set_status(a.status, DGT_ERR_CORRUPT);
         __syncwarp();
     }
+    asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
 // ---------------------------------------------------------------------------
 // format 1 -> R4
+//
+// One warp per group of 32 tiles, one lane per 128-rank tile.  A full tile of
+// width w <= 4 is read with w 16-byte loads into registers.  Each run of eight
+// w-bit codes becomes eight nibbles by three shift-and-add steps (the codes
+// keep their order), and the codes equal to the escape code 2^w - 1 are found
+// with one add and one mask.  The nibble words go to shared memory; each lane
+// then patches its escaped nibbles from the group's escape bytes, in order,
+// and records the ranks >= 15.  The group's nibbles leave with coalesced
+// 16-byte stores.  Widths 5..8 and a short last tile take a per-code path.
 // ---------------------------------------------------------------------------
 struct F1Args {
     const uint8_t *payload;
@@ -323,135 +467,282 @@ struct F1Args {
     int32_t *status;
 };
 
-struct K2Smem {
-    uint32_t pay[TW][1024 + 4];   // 32 tiles x up to 128 bytes, + guard
-    uint32_t outw[TW][512];       // 4096 nibbles
-    uint8_t e1[TW][K2_E1CAP];
-    uint16_t list[TW][32][LIST];
+constexpr int FW = 8;           // warps per CTA
+constexpr int F1_E1CAP = 512;   // staged format-1 escape bytes per group
+constexpr int F1_LIST = 16;     // ranks >= 15 kept per tile; more re-walk the tile
+constexpr int F1_OSTR = 17;     // words per tile row of the staged output (16 + pad)
+
+struct F1Smem {
+    uint32_t out[FW][32 * F1_OSTR];
+    uint8_t e1[FW][F1_E1CAP];
+    uint16_t list[FW][32][F1_LIST];
 };
 
-__device__ __forceinline__ uint64_t load_bits64(const uint32_t *sw, uint32_t byteoff) {
-    uint32_t wi = byteoff >> 2, sh = (byteoff & 3) * 8;
-    uint32_t w0 = sw[wi], w1 = sw[wi + 1], w2 = sw[wi + 2];
-    uint32_t lo = __funnelshift_r(w0, w1, sh), hi = __funnelshift_r(w1, w2, sh);
-    return (uint64_t)lo | ((uint64_t)hi << 32);
+// Eight w-bit codes (bits 0..8w-1 of x, first code lowest) -> eight nibbles.
+template <int W>
+__device__ __forceinline__ uint32_t f1_widen(uint32_t x) {
+    if constexpr (W >= 4) {
+        return x;
+    } else {
+    constexpr uint32_t fm = (1u << W) - 1u;
+    constexpr uint32_t ma = ((1u << (4 * W)) - 1u) << (4 * W);
+    constexpr uint32_t mb = (((1u << (2 * W)) - 1u) << (2 * W)) * 0x00010001u;
+    constexpr uint32_t mc = (fm << W) * 0x01010101u;
+    x &= (1u << (8 * W)) - 1u;
+    x += (x & ma) * ((1u << (16 - 4 * W)) - 1u);  // codes 4..7 up to bit 16
+    x += (x & mb) * ((1u << (8 - 2 * W)) - 1u);   // codes 2,3 / 6,7 up to bit 8 of their half
+    x += (x & mc) * ((1u << (4 - W)) - 1u);       // odd codes up to bit 4 of their byte
+    return x;
+    }
 }
 
-__global__ void __launch_bounds__(TW * 32) k_f1_to_r4(F1Args a) {
+// One marker bit inside every nibble that holds the escape code 2^w - 1.
+template <int W>
+__device__ __forceinline__ uint32_t f1_marks(uint32_t y) {
+    if constexpr (W >= 4)
+        return nib15_mask(y);
+    else
+        return (y + 0x11111111u) & (0x11111111u << W);
+}
+
+struct F1Lane {
+    uint32_t ei;      // next format-1 escape of the group for this tile
+    uint32_t rc;      // ranks >= 15 recorded
+    bool bad;
+};
+
+__device__ __forceinline__ void f1_record(uint16_t *list, F1Lane &L, uint32_t s, uint32_t r) {
+    if (L.rc < F1_LIST) list[L.rc] = (uint16_t)((s << 8) | r);
+    L.rc++;
+}
+
+// Full tile of width W (1..4): nibble words to orow, escapes patched in order.
+template <int W>
+__device__ __forceinline__ void f1_tile(const uint8_t *tp, uint32_t *orow, const uint8_t *e1, uint32_t ge1,
+                                        uint16_t *list, F1Lane &L) {
+    uint32_t pw[4 * W];
+#pragma unroll
+    for (int i = 0; i < W; i++) {
+        const uint4 v = ldg_stream16(tp + 16 * i);
+        pw[4 * i] = v.x;
+        pw[4 * i + 1] = v.y;
+        pw[4 * i + 2] = v.z;
+        pw[4 * i + 3] = v.w;
+    }
+    uint32_t clo = 0, chi = 0;  // escape count of word p in nibble p (words 0..7 / 8..15)
+#pragma unroll
+    for (int p = 0; p < 16; p++) {
+        const int b = 8 * W * p, wi = b >> 5, sh = b & 31;
+        uint32_t x;
+        if (sh + 8 * W <= 32)
+            x = pw[wi] >> sh;
+        else
+            x = __funnelshift_r(pw[wi], pw[wi + 1], sh);
+        const uint32_t y = f1_widen<W>(x);
+        const uint32_t c = __popc(f1_marks<W>(y));
+        if (p < 8)
+            clo += c << (4 * p);
+        else
+            chi += c << (4 * (p - 8));
+        orow[p] = y;
+    }
+    // patch the escaped nibbles: the tile's escapes take the group's bytes in order
+#pragma unroll
+    for (int h = 0; h < 2; h++) {
+        uint32_t m = h ? chi : clo;
+        while (m) {
+            const uint32_t z = __ffs(m) - 1;
+            m &= ~(0xFu << (z & ~3u));
+            const uint32_t p = (z >> 2) + 8 * h;
+            uint32_t y = orow[p];
+            uint32_t t = f1_marks<W>(y);
+            while (t) {
+                const uint32_t i = (__ffs(t) - 1) >> 2;
+                t &= t - 1;
+                uint32_t r = 0;
+                if (L.ei < ge1) r = e1[L.ei];
+                else L.bad = true;
+                L.ei++;
+                if constexpr (W < 4) y ^= ((min(r, 15u) ^ ((1u << W) - 1u)) << (4 * i));
+                if (r >= 15) f1_record(list, L, 8 * p + i, r);
+            }
+            orow[p] = y;
+        }
+    }
+}
+
+// Any width 0..8 and length: code by code from global memory.
+__device__ __noinline__ F1Lane f1_tile_any(const uint8_t *tp, uint32_t wd, uint32_t cnt, uint32_t *orow,
+                                           const uint8_t *e1, uint32_t ge1, uint16_t *list, F1Lane L,
+                                           uint8_t *direct) {
+    const uint32_t top = wd ? (1u << wd) - 1u : 0u;
+    const uint32_t tbytes = 16 * wd;
+    uint32_t word = 0;
+    for (uint32_t s = 0; s < DGT_TILE; s++) {
+        uint32_t r = 0;
+        if (s < cnt && wd) {
+            const uint32_t bit = s * wd, by = bit >> 3;
+            const uint32_t v = tp[by] | ((by + 1 < tbytes ? (uint32_t)tp[by + 1] : 0u) << 8);
+            const uint32_t c = (v >> (bit & 7)) & top;
+            r = c;
+            if (c == top) {
+                r = 0;
+                if (L.ei < ge1) r = e1[L.ei];
+                else L.bad = true;
+                L.ei++;
+            }
+        }
+        if (r >= 15) {
+            if (direct) *direct++ = (uint8_t)r;
+            else f1_record(list, L, s, r);
+        }
+        word |= min(r, 15u) << (4 * (s & 7));
+        if ((s & 7) == 7) {
+            if (!direct) orow[s >> 3] = word;
+            word = 0;
+        }
+    }
+    return L;
+}
+
+// Escape bytes of the group: staged copy, or global memory.
+struct E1Src {
+    const uint8_t *p;
+};
+
+__global__ void __launch_bounds__(FW * 32) k_f1_to_r4(F1Args a) {
     extern __shared__ uint4 smem_raw[];
-    K2Smem &S = *reinterpret_cast<K2Smem *>(smem_raw);
+    F1Smem &S = *reinterpret_cast<F1Smem *>(smem_raw);
     if (blockIdx.x == 0 && threadIdx.x == 0) a.seg[a.seg_last] = (uint32_t)a.n_esc;
     const uint32_t w = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint64_t nbytes = (a.n + 1) / 2;
-    for (uint64_t g = (uint64_t)blockIdx.x * TW + w; g < a.ngrp; g += (uint64_t)gridDim.x * TW) {
+    uint32_t *orow = &S.out[w][lane * F1_OSTR];
+    uint16_t *list = S.list[w][lane];
+    const uint64_t g0 = (uint64_t)blockIdx.x * FW + w, G = (uint64_t)gridDim.x * FW;
+    const uint64_t GS = (uint64_t)DGT_GROUP * DGT_TILE;
+    uint64_t r0 = (g0 * GS) / a.cols, c0 = (g0 * GS) % a.cols;
+    const uint64_t step_r = (G * GS) / a.cols, step_c = (G * GS) % a.cols;
+    for (uint64_t g = g0; g < a.ngrp; g += G) {
         const uint64_t t = g * DGT_GROUP + lane;
         const uint64_t B0 = t * DGT_TILE;
         const uint32_t cnt = t < a.ntile ? (uint32_t)min((uint64_t)DGT_TILE, a.n - B0) : 0u;
         const uint32_t wd = cnt ? a.tw[t] : 0u;
         const uint32_t te = cnt ? a.tesc[t] : 0u;
-        uint32_t gpay, ge1;
-        const uint32_t toff = warp_excl_scan(16 * wd, &gpay);
-        const uint32_t e1off = warp_excl_scan(te, &ge1);
+        uint32_t gsum;
+        const uint32_t pre = warp_excl_scan((16 * min(wd, 9u)) | (te << 16), &gsum);
+        const uint32_t toff = pre & 0xFFFFu, e1off = pre >> 16;
+        const uint32_t gpay = gsum & 0xFFFFu, ge1 = gsum >> 16;
         const uint64_t p0 = (uint64_t)a.grp1[3 * g] * 16, e10 = a.grp1[3 * g + 1], gbase = a.grp1[3 * g + 2];
         const uint64_t next_p = g + 1 < a.ngrp ? (uint64_t)a.grp1[3 * g + 3] * 16 : a.payload_bytes;
         const uint64_t next_e1 = g + 1 < a.ngrp ? (uint64_t)a.grp1[3 * g + 4] : a.n_esc1;
         const uint64_t next_e = g + 1 < a.ngrp ? (uint64_t)a.grp1[3 * g + 5] : a.n_esc;
-        bool gbad = __any_sync(DGT_FULL, wd > 8) || p0 + gpay != next_p || next_p > a.payload_bytes ||
-                    e10 + ge1 != next_e1 || next_e1 > a.n_esc1;
+        uint64_t br = r0, bc = c0 + (uint64_t)DGT_TILE * lane;
+        if (bc >= a.cols) {
+            if (a.cols >= GS) {
+                bc -= a.cols;
+                br++;
+            } else {
+                br += bc / a.cols;
+                bc %= a.cols;
+            }
+        }
+        c0 += step_c;
+        r0 += step_r;
+        if (c0 >= a.cols) {
+            c0 -= a.cols;
+            r0++;
+        }
+        const bool gbad = __any_sync(DGT_FULL, wd > 8) || p0 + gpay != next_p || next_p > a.payload_bytes ||
+                          e10 + ge1 != next_e1 || next_e1 > a.n_esc1;
         if (gbad) {
             if (lane == 0) set_status(a.status, DGT_ERR_CORRUPT);
             continue;
         }
-        // stage the group's payload (16-byte units) and its format-1 escapes
-        {
-            const uint4 *src = reinterpret_cast<const uint4 *>(a.payload + p0);
-            uint4 *dst = reinterpret_cast<uint4 *>(S.pay[w]);
-            for (uint32_t i = lane; i < gpay / 16; i += 32) dst[i] = src[i];
-            if (lane < 4) S.pay[w][gpay / 4 + lane] = 0u;
-            if (ge1 <= K2_E1CAP)
-                for (uint32_t i = lane; i < ge1; i += 32) S.e1[w][i] = a.esc1[e10 + i];
-        }
+        const bool e1staged = ge1 <= F1_E1CAP;
+        if (e1staged)
+            for (uint32_t i = lane; i < ge1; i += 32) S.e1[w][i] = a.esc1[e10 + i];
         __syncwarp();
-        const bool e1staged = ge1 <= K2_E1CAP;
-        const uint32_t top = wd ? (1u << wd) - 1u : 0u;
-        uint32_t ei = e1off, ec = 0;
-        uint64_t em0 = 0, em1 = 0;
-        bool bad = false;
-        if (cnt) {
-            for (uint32_t p = 0; p < 16; p++) {
-                uint64_t v = wd ? load_bits64(S.pay[w], toff + p * wd) : 0ull;
-                uint32_t word = 0;
-#pragma unroll
-                for (uint32_t i = 0; i < 8; i++) {
-                    uint32_t c = (uint32_t)(v >> (i * wd)) & top;
-                    uint32_t r = c;
-                    uint32_t s = p * 8 + i;
-                    if (wd && c == top && s < cnt) {
-                        if (ei < ge1) {
-                            r = e1staged ? S.e1[w][ei] : a.esc1[e10 + ei];
-                        } else {
-                            r = 0;
-                            bad = true;
-                        }
-                        ei++;
-                    }
-                    if (r >= 15 && s < cnt) {
-                        if (ec < LIST) S.list[w][lane][ec] = (uint16_t)((s << 8) | r);
-                        ec++;
-                        if (s < 64) em0 |= 1ull << s; else em1 |= 1ull << (s - 64);
-                    }
-                    if (s >= cnt) r = 0;
-                    word |= (r < 15 ? r : 15u) << (4 * i);
-                }
-                S.outw[w][16 * lane + p] = word;
+        const uint8_t *e1 = (e1staged ? S.e1[w] : a.esc1 + e10);
+        F1Lane L{e1off, 0u, false};
+        const uint8_t *tp = a.payload + p0 + toff;
+        if (cnt == DGT_TILE && wd >= 1 && wd <= 4) {
+            switch (wd) {
+                case 1: f1_tile<1>(tp, orow, e1, ge1, list, L); break;
+                case 2: f1_tile<2>(tp, orow, e1, ge1, list, L); break;
+                case 3: f1_tile<3>(tp, orow, e1, ge1, list, L); break;
+                default: f1_tile<4>(tp, orow, e1, ge1, list, L); break;
             }
-            if (ei - e1off != te) bad = true;
+        } else if (cnt == DGT_TILE && wd == 0) {
+#pragma unroll
+            for (int p = 0; p < 16; p++) orow[p] = 0;
+        } else if (cnt) {
+            L = f1_tile_any(tp, wd, cnt, orow, e1, ge1, list, L, nullptr);
         }
+        bool bad = L.bad || (L.ei - e1off != te);
         __syncwarp();
-        const uint64_t b0 = g * 2048;
-        const uint32_t gbytes = (uint32_t)min((uint64_t)2048, nbytes - b0);
-        if (gbytes == 2048) {
+        // the group's nibbles, coalesced
+        const uint64_t b0 = g * (DGT_GROUP * DGT_TILE / 2);
+        const uint32_t gbytes = (uint32_t)min((uint64_t)(DGT_GROUP * DGT_TILE / 2), nbytes - b0);
+        const uint32_t *og = S.out[w];
+        if (gbytes == DGT_GROUP * DGT_TILE / 2) {
             uint4 *dst = reinterpret_cast<uint4 *>(a.nib + b0);
-            const uint4 *src = reinterpret_cast<const uint4 *>(S.outw[w]);
 #pragma unroll
-            for (int i = 0; i < 4; i++) dst[lane + 32 * i] = src[lane + 32 * i];
+            for (int m = 0; m < 4; m++) {
+                const uint32_t v = lane + 32 * m, row = v >> 2, c = 4 * (v & 3);
+                const uint32_t *src = og + row * F1_OSTR + c;
+                dst[v] = make_uint4(src[0], src[1], src[2], src[3]);
+            }
         } else {
-            const uint8_t *ob = reinterpret_cast<const uint8_t *>(S.outw[w]);
-            for (uint32_t i = lane; i < gbytes; i += 32) a.nib[b0 + i] = ob[i];
-        }
-        uint32_t etot;
-        const uint32_t eb = warp_excl_scan(ec, &etot);
-        if (gbase + etot != next_e || next_e > a.n_esc) bad = true;
-        if (ec && !bad) {
-            uint64_t dst = gbase + eb;
-            if (ec <= LIST) {
-                for (uint32_t i = 0; i < ec; i++) a.esc[dst + i] = (uint8_t)(S.list[w][lane][i] & 0xFF);
-            } else {
-                // more escapes than the list holds: walk the tile's codes again
-                uint32_t ej = e1off;
-                for (uint32_t s = 0; s < cnt; s++) {
-                    uint64_t v = load_bits64(S.pay[w], toff + (s / 8) * wd);
-                    uint32_t c = (uint32_t)(v >> ((s % 8) * wd)) & top;
-                    uint32_t r = c;
-                    if (c == top) {
-                        r = 0;
-                        if (ej < ge1) r = e1staged ? S.e1[w][ej] : a.esc1[e10 + ej];
-                        ej++;
-                    }
-                    if (r >= 15) a.esc[dst++] = (uint8_t)r;
-                }
+            const uint8_t *ob = reinterpret_cast<const uint8_t *>(og);
+            for (uint32_t i = lane; i < gbytes; i += 32) {
+                const uint32_t row = i >> 6, o = i & 63;
+                a.nib[b0 + i] = ob[row * F1_OSTR * 4 + o];
             }
         }
-        const uint64_t r0 = __shfl_sync(DGT_FULL, lane == 0 ? (g * 4096) / a.cols : 0ull, 0);
+        // ranks >= 15, placed by a warp prefix sum from the group's escape base
+        const uint32_t rc = L.rc;
+        uint32_t etot;
+        const uint32_t eb = warp_excl_scan(rc, &etot);
+        if (gbase + etot != next_e || next_e > a.n_esc) bad = true;
+        if (rc && !bad) {
+            uint8_t *dst = a.esc + gbase + eb;
+            if (rc <= F1_LIST) {
+                for (uint32_t i = 0; i < rc; i++) dst[i] = (uint8_t)(list[i] & 0xFF);
+            } else {
+                f1_tile_any(tp, wd, cnt, orow, e1, ge1, list, F1Lane{e1off, 0u, false}, dst);
+            }
+        }
+        // row-segment escape index for every segment that starts in this tile
         if (cnt && !bad) {
-            SegWalk s = first_seg_start(B0, r0, a.cols);
-            for (uint64_t f = s.r * a.cols + s.c; f < B0 + cnt; f = s.r * a.cols + s.c) {
-                uint32_t o = (uint32_t)(f - B0);
-                uint32_t before;
-                if (o <= 64) before = o ? __popcll(em0 & ((~0ull) >> (64 - o))) : 0u;
-                else before = __popcll(em0) + __popcll(em1 & ((~0ull) >> (128 - o)));
-                a.seg[s.r * a.nseg + s.c / DGT_SEG] = (uint32_t)(gbase + eb + before);
-                next_seg_start(s, a.cols);
+            uint32_t done = 0;
+            uint64_t rr = br, cc = bc;
+            while (done < cnt) {
+                for (uint64_t s = (cc + DGT_SEG - 1) / DGT_SEG * DGT_SEG; s < a.cols && s - cc < cnt - done;
+                     s += DGT_SEG) {
+                    const uint32_t o = done + (uint32_t)(s - cc);
+                    uint32_t before = 0;
+                    if (o) {
+                        if (rc <= F1_LIST) {
+                            for (uint32_t i = 0; i < rc; i++) before += (uint32_t)((list[i] >> 8) < o);
+                        } else {
+                            // count again from the codes (more than F1_LIST of them)
+                            uint32_t ej = e1off;
+                            const uint32_t top = (1u << wd) - 1u;
+                            for (uint32_t s2 = 0; s2 < o; s2++) {
+                                const uint32_t bit = s2 * wd, by = bit >> 3;
+                                const uint32_t v = tp[by] | ((by + 1 < 16 * wd ? (uint32_t)tp[by + 1] : 0u) << 8);
+                                const uint32_t c = (v >> (bit & 7)) & top;
+                                uint32_t r = c;
+                                if (c == top) r = ej < ge1 ? e1[ej++] : 0u;
+                                before += r >= 15;
+                            }
+                        }
+                    }
+                    a.seg[rr * a.nseg + s / DGT_SEG] = (uint32_t)(gbase + eb + before);
+                }
+                done += (uint32_t)min(a.cols - cc, (uint64_t)(cnt - done));
+                rr++;
+                cc = 0;
             }
         }
         if (bad) set_status(a.status, DGT_ERR_CORRUPT);
@@ -593,11 +884,11 @@ extern "C" int dgt_load_r4(const dgt_packed_view *dev, dgt_r4 *r4, int32_t *d_st
         a.n_esc = dev->n_esc15;
         a.seg_last = seg_last;
         a.status = d_status;
-        const size_t smem = sizeof(K1Smem);
+        const size_t smem = sizeof(RiceSmem);
         int bps = 0;
-        if (prepare_kernel((const void *)k_rice_to_r4, smem, TW * 32, &bps) != DGT_OK) return DGT_ERR_CUDA;
-        uint64_t grid = min((uint64_t)di.sms * bps, (a.ngrp + TW - 1) / TW);
-        k_rice_to_r4<<<(unsigned)grid, TW * 32, smem, st>>>(a);
+        if (prepare_kernel((const void *)k_rice_to_r4, smem, RW * 32, &bps) != DGT_OK) return DGT_ERR_CUDA;
+        uint64_t grid = min((uint64_t)di.sms * bps, (a.ngrp + RW - 1) / RW);
+        k_rice_to_r4<<<(unsigned)grid, RW * 32, smem, st>>>(a);
     } else {
         if (!dev->tw || !dev->tesc || !dev->grp1 || (dev->payload_bytes && !dev->payload) ||
             (dev->n_esc1 && !dev->esc1) || (dev->payload && !aligned16(dev->payload)))
@@ -622,11 +913,11 @@ extern "C" int dgt_load_r4(const dgt_packed_view *dev, dgt_r4 *r4, int32_t *d_st
         a.n_esc = dev->n_esc15;
         a.seg_last = seg_last;
         a.status = d_status;
-        const size_t smem = sizeof(K2Smem);
+        const size_t smem = sizeof(F1Smem);
         int bps = 0;
-        if (prepare_kernel((const void *)k_f1_to_r4, smem, TW * 32, &bps) != DGT_OK) return DGT_ERR_CUDA;
-        uint64_t grid = min((uint64_t)di.sms * bps, (a.ngrp + TW - 1) / TW);
-        k_f1_to_r4<<<(unsigned)grid, TW * 32, smem, st>>>(a);
+        if (prepare_kernel((const void *)k_f1_to_r4, smem, FW * 32, &bps) != DGT_OK) return DGT_ERR_CUDA;
+        uint64_t grid = min((uint64_t)di.sms * bps, (a.ngrp + FW - 1) / FW);
+        k_f1_to_r4<<<(unsigned)grid, FW * 32, smem, st>>>(a);
     }
     return cudaPeekAtLastError() == cudaSuccess ? DGT_OK : DGT_ERR_CUDA;
 }
