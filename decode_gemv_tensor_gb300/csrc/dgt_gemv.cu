@@ -84,19 +84,20 @@ __device__ __forceinline__ void load_batch(Batch<R4, U> &B, const uint8_t *smp, 
 // Escape information of up to 32 rounds [jbase, jbase + 32) of one row:
 // lane t holds round jbase + t.
 struct SegInfo {
-    uint32_t cnt, base, fexp, emask;
+    uint32_t cnt, base, fexp, fexp1, emask;
 };
 
 __device__ __forceinline__ SegInfo load_seginfo(const GemvArgs &a, const uint8_t *table_s, uint64_t row,
                                                 uint32_t jbase, uint32_t j1, uint32_t lane) {
     SegInfo g;
-    g.cnt = g.base = g.fexp = 0;
+    g.cnt = g.base = g.fexp = g.fexp1 = 0;
     const uint32_t j = jbase + lane;
     if (j < j1) {
         const uint32_t *sp = a.seg + row * a.nseg + j;
         g.base = sp[0];
         g.cnt = sp[1] - g.base;
         if (g.cnt && g.base < a.n_esc) g.fexp = table_s[a.esc[g.base]];
+        if (g.cnt >= 2 && (uint64_t)g.base + 1 < a.n_esc) g.fexp1 = table_s[a.esc[g.base + 1]];
     }
     g.emask = __ballot_sync(DGT_FULL, g.cnt != 0);
     return g;
@@ -223,7 +224,7 @@ __device__ __forceinline__ float unit_dot(const GemvArgs &a, const uint4 *xs, ui
     const uint8_t *nbp = R4 ? a.nib + rb / 2 : nullptr;
     const uint16_t *wp = R4 ? nullptr : a.W + rb;
     const uint32_t Jm1 = a.J - 1;
-    SegInfo g = {0, 0, 0, 0};
+    SegInfo g = {0, 0, 0, 0, 0};
     uint32_t jbase = j0;
     if (R4) g = load_seginfo(a, table_s, row, jbase, j1, lane);
     float acc = 0.0f;
@@ -290,19 +291,27 @@ __global__ void __launch_bounds__(PW * 32, 1) k_gemv(GemvArgs a) {
 }
 
 // ---------------------------------------------------------------------------
-// Bulk-copy streaming kernel (the default when cols % 32 == 0).  One CTA per
-// SM: 16 consumer warps and one producer warp.  CTA b owns rows
-// [b*N/G, (b+1)*N/G); consumer warp w takes the (row, slice) units w, w+16, ...
-// Each consumer warp owns a ring of NS shared-memory stages; lane w of the
-// producer warp keeps that ring full with 1-D bulk copies (cp.async.bulk),
-// each stage a piece of up to C rounds of one unit, its arrival counted on a
-// "full" mbarrier; the consumer releases a stage through an "empty" mbarrier.
-// So consumers only wait, decode from shared memory and multiply-add.  Every
-// wait is bounded: one that runs out sets the status word, and the warps stop
-// their work and let the copies in flight land before the CTA exits.
+// Bulk-copy streaming kernel (the default when cols % 32 == 0).  One CTA of
+// 16 warps per SM; CTA b owns rows [b*N/G, (b+1)*N/G) and warp w takes the
+// (row, slice) units w, w+16, ...  Each warp owns a ring of NS shared-memory
+// stages and keeps it full itself: after it has read a stage, lane 0 issues
+// the 1-D bulk copies (cp.async.bulk) of the piece NS ahead into it, the
+// arrival counted on the stage's mbarrier.  No warp waits on another warp's
+// progress.  A full piece is C rounds, decoded from shared memory without
+// per-round tests except the warp-uniform escape bit.  An R4 round whose
+// segment holds one escape decodes with the rank-15 entry of the exponent
+// table replaced by that escape's exponent (only the escaped weight has
+// nibble 15); two escapes in different lanes do the same per lane; other
+// cases go out of line.  The row-segment escape counts of the next unit and
+// the exponents of their first two escapes are fetched while the current unit
+// runs.  Every wait is bounded: one that runs out sets the status word, and
+// the warp stops, lets its copies in flight land and exits.
 // ---------------------------------------------------------------------------
-constexpr int TNW = 16;    // consumer warps
-constexpr uint32_t TNS = 3;
+#ifndef DGT_GEMV_INTERLEAVE
+#define DGT_GEMV_INTERLEAVE 0
+#endif
+constexpr int TNW = 16;    // warps per CTA
+constexpr uint32_t TNS_MAX = 5;
 constexpr uint32_t TCHUNK = 1024;  // (row, slice) units per combine chunk
 
 template <bool R4>
@@ -310,11 +319,13 @@ struct TmaCfg;
 template <>
 struct TmaCfg<true> {
     static constexpr uint32_t C = 4;               // rounds per piece
+    static constexpr uint32_t NS = 3;              // stages per warp
     static constexpr uint32_t STAGE = 4 * 768;     // sm bytes then nibbles
 };
 template <>
 struct TmaCfg<false> {
     static constexpr uint32_t C = 2;
+    static constexpr uint32_t NS = 5;
     static constexpr uint32_t STAGE = 2 * 1024;
 };
 
@@ -323,9 +334,9 @@ struct UnitRange {
     uint32_t j0, j1;
 };
 
-__device__ __forceinline__ UnitRange unit_range(uint64_t uu, uint64_t r0, uint32_t log2S, uint32_t J) {
+__device__ __forceinline__ UnitRange unit_range(uint64_t uu, uint64_t r0, uint64_t rs, uint32_t log2S, uint32_t J) {
     UnitRange u;
-    u.row = r0 + (uu >> log2S);
+    u.row = r0 + (uu >> log2S) * rs;
     const uint32_t s = (uint32_t)uu & ((1u << log2S) - 1u);
     u.j0 = (s * J) >> log2S;
     u.j1 = ((s + 1) * J) >> log2S;
@@ -333,12 +344,13 @@ __device__ __forceinline__ UnitRange unit_range(uint64_t uu, uint64_t r0, uint32
 }
 
 template <bool R4>
-__device__ __forceinline__ void issue_piece(const GemvArgs &a, uint64_t row, uint32_t j, uint32_t j1,
+__device__ __forceinline__ void issue_piece(const GemvArgs &a, uint64_t rowf, uint32_t j, uint32_t j1,
                                             uint32_t stage, uint32_t bar) {
     const uint32_t n = min(TmaCfg<R4>::C, j1 - j);
-    const uint64_t k0 = (uint64_t)j * 512;
-    const uint32_t cols = (uint32_t)(min((uint64_t)(j + n) * 512, a.cols) - k0);
-    const uint64_t f = row * a.cols + k0;
+    const uint32_t k0 = j * 512;
+    const uint32_t cols = min((j + n) * 512, (uint32_t)a.cols) - k0;
+    const uint64_t f = rowf + k0;
+    fence_proxy_async_smem();
     if (R4) {
         mbar_arrive_expect_tx(bar, cols + cols / 2);
         bulk_g2s(stage, a.sm + f, cols, bar);
@@ -349,12 +361,129 @@ __device__ __forceinline__ void issue_piece(const GemvArgs &a, uint64_t row, uin
     }
 }
 
+// The next piece a warp copies: unit uu (of this CTA), rounds [j, j1) of
+// the row whose first weight is at flat index rowf.
+struct PieceCursor {
+    uint64_t uu, rowf;
+    uint32_t j, j1;
+};
+
+__device__ __forceinline__ void cursor_set(PieceCursor &c, uint64_t uu, uint64_t units, uint64_t r0, uint64_t rs,
+                                           uint32_t log2S, uint32_t J, uint64_t K) {
+    c.uu = uu;
+    if (uu < units) {
+        const UnitRange u = unit_range(uu, r0, rs, log2S, J);
+        c.rowf = u.row * K;
+        c.j = u.j0;
+        c.j1 = u.j1;
+    }
+}
+
+// Escape counts of the next unit's first 32 rounds (lane t: round j0 + t) and
+// the ranks of their first two escapes, loaded ahead of use.
+struct SegPre {
+    uint32_t cnt, base, e0, e1;
+};
+
+__device__ __forceinline__ void seg_issue(const GemvArgs &a, uint64_t row, uint32_t jb, uint32_t j1,
+                                          uint32_t lane, SegPre &p) {
+    p.cnt = p.base = 0;
+    const uint32_t j = jb + lane;
+    if (j < j1) {
+        const uint32_t *sp = a.seg + row * a.nseg + j;
+        p.base = sp[0];
+        p.cnt = sp[1] - p.base;
+    }
+}
+
+__device__ __forceinline__ void seg_issue_esc(const GemvArgs &a, SegPre &p) {
+    p.e0 = (p.cnt >= 1 && p.base < a.n_esc) ? a.esc[p.base] : 0u;
+    p.e1 = (p.cnt >= 2 && (uint64_t)p.base + 1 < a.n_esc) ? a.esc[p.base + 1] : 0u;
+}
+
+__device__ __forceinline__ SegInfo seg_finish(const SegPre &p, const uint8_t *table_s) {
+    SegInfo g;
+    g.cnt = p.cnt;
+    g.base = p.base;
+    g.fexp = table_s[p.e0];
+    g.fexp1 = table_s[p.e1];
+    g.emask = __ballot_sync(DGT_FULL, p.cnt != 0);
+    return g;
+}
+
+// A copy of v the compiler cannot trace back to its source.
+__device__ __forceinline__ uint32_t opaque(uint32_t v) {
+    uint32_t r;
+    asm volatile("mov.b32 %0, %1;" : "=r"(r) : "r"(v));
+    return r;
+}
+
+// The exponent table with the rank-15 entry replaced by exponent e.
+__device__ __forceinline__ R4Lut lut15(const R4Lut &L, uint32_t e) {
+    R4Lut o = L;
+    o.h3 = prmt(L.h3, e >> 1, 0x4210u);
+    o.l1 = (L.l1 & 0x7FFFFFFFu) | ((e & 1u) << 31);
+    return o;
+}
+
+// Per round of a seg window (lane t: round jbase + t): the two table words
+// of the round's decode (rank 15 -> the exponent of its first escape when it
+// has one) and a mask of rounds with two or more escapes.
+struct RoundLut {
+    uint32_t h3, l1, multi;
+};
+
+__device__ __forceinline__ RoundLut round_luts(const SegInfo &g, const R4Lut &L) {
+    RoundLut o;
+    const R4Lut m = lut15(L, g.fexp);
+    o.h3 = g.cnt ? m.h3 : L.h3;
+    o.l1 = g.cnt ? m.l1 : L.l1;
+    o.multi = __ballot_sync(DGT_FULL, g.cnt >= 2);
+    return o;
+}
+
+// A round whose segment holds two or more escapes, when every lane holds at
+// most one of them: the exponent of this lane's escape (its place among the
+// round's escaped lanes; the first two come prefetched).  Returns false when
+// a lane holds more than one, or the counts disagree.
+__device__ __forceinline__ bool multi_exponent(const GemvArgs &a, const SegInfo &g, uint32_t bit, uint2 nv,
+                                               const uint8_t *table_s, uint32_t lane, uint32_t &e) {
+    const uint32_t c = __shfl_sync(DGT_FULL, g.cnt, bit);
+    const uint32_t e0 = __shfl_sync(DGT_FULL, g.fexp, bit);
+    const uint32_t e1 = __shfl_sync(DGT_FULL, g.fexp1, bit);
+    const uint32_t b = __shfl_sync(DGT_FULL, g.base, bit);
+    const uint32_t k = __popc(nib15_mask(nv.x)) + __popc(nib15_mask(nv.y));
+    const uint32_t bal = __ballot_sync(DGT_FULL, k != 0);
+    if (__any_sync(DGT_FULL, k > 1) || (uint32_t)__popc(bal) != c) return false;
+    const uint32_t q = __popc(bal & ((1u << lane) - 1u));
+    e = q == 0 ? e0 : e1;
+    if (k && q >= 2) e = (uint64_t)b + q < a.n_esc ? table_s[a.esc[b + q]] : 0u;
+    return true;
+}
+
+// Any R4 round with escapes, in line: decode, then patch every escaped weight
+// from the segment's escape ranks (staged in shared memory).
+__device__ __forceinline__ void r4_round_general(const GemvArgs &a, const R4Lut &L, uint2 nv, uint4 sv,
+                                                 const SegInfo &g, uint32_t bit, uint8_t *escb,
+                                                 const uint8_t *table_s, uint32_t lane, bool act, uint32_t p[8]) {
+    const uint32_t c = __shfl_sync(DGT_FULL, g.cnt, bit);
+    const uint32_t b = __shfl_sync(DGT_FULL, g.base, bit);
+    r4_dec16(nv, sv, L, p);
+    const uint32_t m0 = act ? nib15_mask(nv.x) : 0u;
+    const uint32_t m1 = act ? nib15_mask(nv.y) : 0u;
+    const uint32_t cc = c > DGT_SEG ? DGT_SEG : c;
+    for (uint32_t i = lane; i < cc; i += 32) escb[i] = (uint64_t)b + i < a.n_esc ? a.esc[b + i] : 0;
+    __syncwarp();
+    patch_escapes(p, m0, m1, cc, escb, table_s);
+    __syncwarp();
+}
+
 template <bool R4>
 __global__ void __launch_bounds__((TNW + 1) * 32, 1) k_gemv_tma(GemvArgs a) {
-    constexpr uint32_t C = TmaCfg<R4>::C, STAGE = TmaCfg<R4>::STAGE;
+    constexpr uint32_t C = TmaCfg<R4>::C, TNS = TmaCfg<R4>::NS, STAGE = TmaCfg<R4>::STAGE;
     extern __shared__ __align__(128) uint8_t dsm[];
-    __shared__ __align__(8) uint64_t full[TNW][TNS];
-    __shared__ __align__(8) uint64_t empty[TNW][TNS];
+    __shared__ __align__(8) uint64_t full[TNW][TNS_MAX];
+    __shared__ __align__(8) uint64_t empty[TNW][TNS_MAX];
     __shared__ uint8_t table_s[256];
     __shared__ uint8_t escb[R4 ? TNW : 1][R4 ? DGT_SEG : 1];
     __shared__ float part[TCHUNK];
@@ -362,13 +491,21 @@ __global__ void __launch_bounds__((TNW + 1) * 32, 1) k_gemv_tma(GemvArgs a) {
     const uint32_t tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
     uint4 *xs = reinterpret_cast<uint4 *>(dsm + (size_t)TNW * TNS * STAGE);
     const uint64_t G = gridDim.x;
-    const uint64_t r0 = (uint64_t)blockIdx.x * a.rows / G, r1 = (uint64_t)(blockIdx.x + 1) * a.rows / G;
+#if DGT_GEMV_INTERLEAVE
+    // CTA b owns rows b, b + G, b + 2G, ...: the whole grid sweeps one window
+    const uint64_t r0 = blockIdx.x, rs = G;
+    const uint64_t nrows = a.rows > r0 ? (a.rows - r0 + G - 1) / G : 0;
+#else
+    const uint64_t r0 = (uint64_t)blockIdx.x * a.rows / G, rs = 1;
+    const uint64_t nrows = (uint64_t)(blockIdx.x + 1) * a.rows / G - r0;
+#endif
     const uint32_t log2S = __ffs(a.S) - 1;
-    const uint64_t units = (r1 - r0) << log2S;
+    const uint64_t units = nrows << log2S;
     const uint64_t nchunks = (units + TCHUNK - 1) / TCHUNK;
     const uint32_t J = a.J;
+    const uint32_t K = (uint32_t)a.cols;
 
-    if (tid < TNW * TNS) {
+    if (tid < TNW * TNS_MAX) {
         mbar_init(smem_u32(&full[0][0]) + 8 * tid, 1);
         mbar_init(smem_u32(&empty[0][0]) + 8 * tid, 1);
     }
@@ -377,72 +514,94 @@ __global__ void __launch_bounds__((TNW + 1) * 32, 1) k_gemv_tma(GemvArgs a) {
     __syncthreads();
 
     if (w == TNW) {
-        // ---- producer warp: lane l keeps consumer warp l's ring full, chunk by chunk
-        const uint32_t ring_a = smem_u32(dsm + (size_t)(lane % TNW) * TNS * STAGE);
-        const uint32_t full_a = smem_u32(&full[lane % TNW][0]), empty_a = smem_u32(&empty[lane % TNW][0]);
-        uint32_t st = 0, uses = 0;
-        for (uint64_t ch = 0; ch < nchunks; ch++) {
-            const uint64_t c0 = ch * TCHUNK, cend = min(c0 + TCHUNK, units);
-            if (lane < TNW) {
-                for (uint64_t uu = c0 + lane; uu < cend; uu += TNW) {
-                    const UnitRange u = unit_range(uu, r0, log2S, J);
-                    for (uint32_t j = u.j0; j < u.j1; j += C) {
-                        if (*(volatile int *)&abort_flag) break;
-                        if (uses >= TNS && !mbar_wait(empty_a + 8 * st, ((uses / TNS) - 1) & 1u)) {
-                            set_status(a.status, DGT_ERR_TIMEOUT);
-                            atomicExch(&abort_flag, 1);
-                            break;
-                        }
-                        issue_piece<R4>(a, u.row, j, u.j1, ring_a + st * STAGE, full_a + 8 * st);
-                        uses++;
-                        st = st + 1 == TNS ? 0 : st + 1;
-                    }
+        // ---- producer warp: lane c keeps consumer warp c's ring full.  It
+        // polls the ring's "empty" barriers without blocking, so no consumer
+        // waits for another.
+        if (lane < TNW) {
+            const uint32_t ring_a = smem_u32(dsm + (size_t)lane * TNS * STAGE);
+            const uint32_t full_a = smem_u32(&full[lane][0]), empty_a = smem_u32(&empty[lane][0]);
+            PieceCursor cur;
+            cursor_set(cur, lane, units, r0, rs, log2S, J, a.cols);
+            uint32_t q = 0, idle = 0;
+            while (cur.uu < units && !*(volatile int *)&abort_flag) {
+                const uint32_t st = q % TNS;
+                if (q < TNS || mbar_test_wait(empty_a + 8 * st, ((q / TNS) - 1) & 1u)) {
+                    issue_piece<R4>(a, cur.rowf, cur.j, cur.j1, ring_a + st * STAGE, full_a + 8 * st);
+                    q++;
+                    idle = 0;
+                    cur.j += C;
+                    if (cur.j >= cur.j1) cursor_set(cur, cur.uu + TNW, units, r0, rs, log2S, J, a.cols);
+                } else if (++idle >= MBAR_SPIN_LIMIT) {
+                    set_status(a.status, DGT_ERR_TIMEOUT);
+                    atomicExch(&abort_flag, 1);
+                    break;
                 }
             }
-            __syncwarp();
-            __syncthreads();
-            __syncthreads();
-        }
-        // every copy this lane issued has landed before the CTA may exit
-        if (lane < TNW) {
-            for (uint32_t q = uses > TNS ? uses - TNS : 0; q < uses; q++)
-                mbar_wait(full_a + 8 * (q % TNS), (q / TNS) & 1u);
         }
         return;
     }
 
     // ---- consumer warps
-    const uint32_t K = (uint32_t)a.cols;
     for (uint32_t i = tid; i < J * 64; i += TNW * 32) {
         const uint32_t k = 8 * i, j = k >> 9, u = (k >> 4) & 31, h = (k >> 3) & 1;
         xs[(2 * j + h) * 32 + u] = k < K ? *reinterpret_cast<const uint4 *>(a.x + k) : make_uint4(0, 0, 0, 0);
     }
     if (R4 && tid < 256) table_s[tid] = a.table[tid];
     asm volatile("bar.sync 1, %0;" ::"r"(TNW * 32) : "memory");
-    const R4Lut L = a.L;
+
+    // the exponent table, held in registers (opaque copies: never re-read from
+    // the parameter space inside the loop)
+    R4Lut L;
+    L.h0 = opaque(a.L.h0);
+    L.h1 = opaque(a.L.h1);
+    L.h2 = opaque(a.L.h2);
+    L.h3 = opaque(a.L.h3);
+    L.l0 = opaque(a.L.l0);
+    L.l1 = opaque(a.L.l1);
     const uint8_t *ring = dsm + (size_t)w * TNS * STAGE;
     const uint32_t full_a = smem_u32(&full[w][0]), empty_a = smem_u32(&empty[w][0]);
     const uint32_t Jm1 = J - 1;
     const bool act = 16 * lane < K - 512 * Jm1;
     const bool cut = (K & 511) != 0;
-    uint32_t st = 0, phases = 0;
+    uint32_t st = 0, phases = 0, waited = 0;
     bool ok = true;
+    SegPre pre = {0, 0, 0, 0};
+    if (R4 && (uint64_t)w < units) {
+        const UnitRange u = unit_range(w, r0, rs, log2S, J);
+        seg_issue(a, u.row, u.j0, u.j1, lane, pre);
+        seg_issue_esc(a, pre);
+    }
     for (uint64_t ch = 0; ch < nchunks; ch++) {
         const uint64_t c0 = ch * TCHUNK, cend = min(c0 + TCHUNK, units);
         for (uint64_t uu = c0 + w; uu < cend; uu += TNW) {
-            const UnitRange u = unit_range(uu, r0, log2S, J);
-            SegInfo g = {0, 0, 0, 0};
+            const UnitRange u = unit_range(uu, r0, rs, log2S, J);
+            SegInfo g = {0, 0, 0, 0, 0};
+            RoundLut rl = {0, 0, 0};
             uint32_t jbase = u.j0;
-            if (R4) g = load_seginfo(a, table_s, u.row, jbase, u.j1, lane);
+            SegPre nxt = {0, 0, 0, 0};
+            bool nxt_esc = false;
+            const bool has_next = uu + TNW < units;
+            if (R4) {
+                g = seg_finish(pre, table_s);
+                rl = round_luts(g, L);
+                if (has_next) {
+                    const UnitRange un = unit_range(uu + TNW, r0, rs, log2S, J);
+                    seg_issue(a, un.row, un.j0, un.j1, lane, nxt);
+                }
+            }
             float acc = 0.0f;
             for (uint32_t jp = u.j0; jp < u.j1; jp += C) {
-                if (ok && *(volatile int *)&abort_flag) ok = false;
-                if (ok && !mbar_wait(full_a + 8 * st, (phases >> st) & 1u)) {
-                    ok = false;
-                    if (lane == 0) {
-                        set_status(a.status, DGT_ERR_TIMEOUT);
-                        atomicExch(&abort_flag, 1);
+                if (ok) {
+                    if (mbar_wait(full_a + 8 * st, (phases >> st) & 1u)) {
+                        waited++;
+                    } else {
+                        ok = false;
+                        if (lane == 0) {
+                            set_status(a.status, DGT_ERR_TIMEOUT);
+                            atomicExch(&abort_flag, 1);
+                        }
                     }
+                    if (*(volatile int *)&abort_flag) ok = false;
                 }
                 ok = __all_sync(DGT_FULL, ok);
                 phases ^= 1u << st;
@@ -450,28 +609,74 @@ __global__ void __launch_bounds__((TNW + 1) * 32, 1) k_gemv_tma(GemvArgs a) {
                 if (R4 && jp - jbase >= 32) {
                     jbase = jp;
                     g = load_seginfo(a, table_s, u.row, jbase, u.j1, lane);
+                    rl = round_luts(g, L);
                 }
-                const uint32_t pm = R4 ? g.emask >> (jp - jbase) : 0u;
+                const uint32_t b0 = jp - jbase;
                 const uint32_t rp = (cut && Jm1 - jp < n) ? Jm1 - jp : 0xFFFFFFFFu;
+                const uint32_t pm = R4 ? (rl.multi >> b0) & ((1u << n) - 1u) : 0u;
                 const uint8_t *stg = ring + st * STAGE;
-                if (ok) {
+                bool slow = n != C || rp != 0xFFFFFFFFu;
+                // rounds with two or more escapes: per-lane rank-15 entries, worked
+                // out before the multiply-adds; anything else takes the slow loop
+                uint32_t mh3[C], ml1[C];
+#pragma unroll
+                for (uint32_t r = 0; r < C; r++) mh3[r] = ml1[r] = 0;
+                if (R4 && ok && pm && !slow) {
 #pragma unroll
                     for (uint32_t r = 0; r < C; r++) {
-                        if (r >= n) break;
+                        if ((pm >> r) & 1u) {
+                            const uint2 nv = *reinterpret_cast<const uint2 *>(stg + C * 512 + r * 256 + 8 * lane);
+                            uint32_t e;
+                            if (multi_exponent(a, g, b0 + r, nv, table_s, lane, e)) {
+                                const R4Lut t = lut15(L, e);
+                                mh3[r] = t.h3;
+                                ml1[r] = t.l1;
+                            } else {
+                                slow = true;
+                            }
+                        }
+                    }
+                }
+                if (ok && !slow) {
+#pragma unroll
+                    for (uint32_t r = 0; r < C; r++) {
                         const uint32_t j = jp + r;
                         uint32_t p[8];
                         if (R4) {
                             const uint4 sv = *reinterpret_cast<const uint4 *>(stg + r * 512 + 16 * lane);
                             const uint2 nv = *reinterpret_cast<const uint2 *>(stg + C * 512 + r * 256 + 8 * lane);
+                            R4Lut Lr = L;
+                            const uint32_t h3 = __shfl_sync(DGT_FULL, rl.h3, b0 + r);
+                            const uint32_t l1 = __shfl_sync(DGT_FULL, rl.l1, b0 + r);
+                            Lr.h3 = ((pm >> r) & 1u) ? mh3[r] : h3;
+                            Lr.l1 = ((pm >> r) & 1u) ? ml1[r] : l1;
+                            r4_dec16(nv, sv, Lr, p);
+                        } else {
+                            const uint4 lo = *reinterpret_cast<const uint4 *>(stg + r * 1024 + 32 * lane);
+                            const uint4 hi = *reinterpret_cast<const uint4 *>(stg + r * 1024 + 32 * lane + 16);
+                            p[0] = lo.x; p[1] = lo.y; p[2] = lo.z; p[3] = lo.w;
+                            p[4] = hi.x; p[5] = hi.y; p[6] = hi.z; p[7] = hi.w;
+                        }
+                        acc = fma_chunk16(p, xs, j, lane, acc);
+                    }
+                } else if (ok) {
+                    // partial or cut piece, or a round whose escapes need the general patch
+                    for (uint32_t r = 0; r < n; r++) {
+                        const uint32_t j = jp + r;
+                        const bool ract = r != rp || act;
+                        uint32_t p[8];
+                        if (R4) {
+                            const uint4 sv = *reinterpret_cast<const uint4 *>(stg + r * 512 + 16 * lane);
+                            const uint2 nv = *reinterpret_cast<const uint2 *>(stg + C * 512 + r * 256 + 8 * lane);
+                            const uint32_t h3 = __shfl_sync(DGT_FULL, rl.h3, b0 + r);
+                            const uint32_t l1 = __shfl_sync(DGT_FULL, rl.l1, b0 + r);
                             if ((pm >> r) & 1u) {
-                                const uint32_t bit = j - jbase;
-                                const uint32_t c = __shfl_sync(DGT_FULL, g.cnt, bit);
-                                const uint32_t b = __shfl_sync(DGT_FULL, g.base, bit);
-                                const uint32_t e = __shfl_sync(DGT_FULL, g.fexp, bit);
-                                decode_with_escapes(a.esc, a.n_esc, L, nv, sv, escb[R4 ? w : 0], table_s, lane,
-                                                    r != rp || act, c, b, e, p);
+                                r4_round_general(a, L, nv, sv, g, b0 + r, escb[R4 ? w : 0], table_s, lane, ract, p);
                             } else {
-                                r4_dec16(nv, sv, L, p);
+                                R4Lut Lr = L;
+                                Lr.h3 = h3;
+                                Lr.l1 = l1;
+                                r4_dec16(nv, sv, Lr, p);
                             }
                         } else {
                             const uint4 lo = *reinterpret_cast<const uint4 *>(stg + r * 1024 + 32 * lane);
@@ -489,24 +694,34 @@ __global__ void __launch_bounds__((TNW + 1) * 32, 1) k_gemv_tma(GemvArgs a) {
                     }
                 }
                 __syncwarp();
-                if (lane == 0) mbar_arrive(empty_a + 8 * st);
+                // a stage is released only after a good wait: after a timeout the
+                // producer stops, and the copies in flight are waited for below
+                if (ok && lane == 0) mbar_arrive(empty_a + 8 * st);
                 st = st + 1 == TNS ? 0 : st + 1;
+                if (R4 && has_next && !nxt_esc) {
+                    seg_issue_esc(a, nxt);
+                    nxt_esc = true;
+                }
             }
+            if (R4) pre = nxt;
 #pragma unroll
             for (int d = 16; d >= 1; d >>= 1) acc += __shfl_xor_sync(DGT_FULL, acc, d);
             if (lane == 0) part[uu - c0] = acc;
         }
-        __syncthreads();
+        asm volatile("bar.sync 1, %0;" ::"r"(TNW * 32) : "memory");
         const uint32_t S = 1u << log2S;
         for (uint32_t t = tid; t < (cend - c0) / S; t += TNW * 32) {
             float y = part[t * S];
             for (uint32_t s = 1; s < S; s++) y = y + part[t * S + s];
-            const uint64_t row = r0 + c0 / S + t;
+            const uint64_t row = r0 + (c0 / S + t) * rs;
             if (a.y32) a.y32[row] = y;
             if (a.y) a.y[row] = f32_to_bf16_rne(y);
         }
-        __syncthreads();
+        asm volatile("bar.sync 1, %0;" ::"r"(TNW * 32) : "memory");
     }
+    // after a timeout: copies that may still be in flight land before exit
+    if (!ok)
+        for (uint32_t q = waited; q < waited + TNS; q++) mbar_wait(full_a + 8 * (q % TNS), (q / TNS) & 1u);
 }
 
 // Any shape / alignment: one warp per (row, slice), element loads, x read
@@ -578,7 +793,7 @@ int launch_gemv(GemvArgs &a, int path, cudaStream_t st) {
     a.S = dgt_plan_slices(a.rows, a.cols);
     int bps = 0;
     if (path == 2) {
-        const size_t smem = (size_t)TNW * TNS * TmaCfg<R4>::STAGE + (size_t)a.J * 1024;
+        const size_t smem = (size_t)TNW * TmaCfg<R4>::NS * TmaCfg<R4>::STAGE + (size_t)a.J * 1024;
         if (prepare_kernel((const void *)k_gemv_tma<R4>, smem, (TNW + 1) * 32, &bps) != DGT_OK) return DGT_ERR_CUDA;
         const unsigned grid = (unsigned)min((uint64_t)di.sms, a.rows);
         k_gemv_tma<R4><<<grid, (TNW + 1) * 32, smem, st>>>(a);
@@ -600,7 +815,7 @@ int launch_gemv(GemvArgs &a, int path, cudaStream_t st) {
 template <bool R4>
 int choose_path(uint64_t K, uint32_t J, bool aligned) {
     if (K == 0 || K % 16 != 0 || !aligned) return 0;
-    const size_t tma_smem = (size_t)TNW * TNS * TmaCfg<R4>::STAGE + (size_t)J * 1024;
+    const size_t tma_smem = (size_t)TNW * TmaCfg<R4>::NS * TmaCfg<R4>::STAGE + (size_t)J * 1024;
     if (K % 32 == 0 && tma_smem <= 200 * 1024) return 2;
     return J <= MAX_FAST_ROUNDS ? 1 : 0;
 }
