@@ -13,11 +13,12 @@
 //  1. k_moe_route (one CTA): counts the pairs per expert, lists the experts
 //     in use, and places every pair (t, j) in its expert's list in (t, j)
 //     order -- deterministic, no atomics in the placement.
-//  2. k_moe: a warp takes two rows of an expert in use at a time and streams
-//     each row once (up to 8 rounds of loads in flight), decodes each 16-weight
-//     lane chunk once and runs one fmaf chain per routed token (up to 4 per
-//     pass) against x staged in shared memory; at each slice end the chains
-//     are butterfly-reduced into the workspace.
+//  2. k_moe: the rows of the experts in use are split over one CTA per SM by
+//     cost (row passes and token chains); a producer warp streams each consumer warp's rows into shared
+//     memory with bulk copies, and the consumer decodes each 16-weight lane
+//     chunk once and runs one fmaf chain per routed token (up to 4 per pass
+//     over the row), x read through L1; at each slice end the chains are
+//     butterfly-reduced into the workspace.
 //  3. k_moe_combine: adds each pair's slices left to right (y) and applies
 //     the routing weights in slot order (out).
 #include <cuda_runtime.h>
@@ -26,14 +27,12 @@
 #include "dgt_device.cuh"
 #include "dgt_internal.h"
 #include "dgt_launch.h"
+#include "dgt_r4esc.cuh"
 
 namespace dgt {
 
-constexpr int MW = 8;               // warps per CTA
-constexpr uint32_t MOE_TPASS = 4;   // tokens per pass over a row
 constexpr uint32_t MOE_MAX_EXPERTS = 4096;
 constexpr uint32_t MOE_MAX_PAIRS = 1u << 16;
-constexpr uint32_t MOE_XS_LIMIT = 160 * 1024;  // x of every token in shared memory
 
 struct MoeArgs {
     const uint8_t *sm, *nib, *esc;
@@ -47,20 +46,27 @@ struct MoeArgs {
     float *out32;
     uint64_t cols, nseg, n_esc, ne;
     uint32_t n_experts, tokens, topk, J, S;
+    int bulk;          // rows stream through bulk copies (else direct loads)
+    uint32_t xs_slots; // tokens whose x fits in shared memory
     R4Lut L;
     uint8_t table[256];
     // workspace
     uint32_t *eoff;    // n_experts + 1
     uint32_t *elist;   // pairs: t << 8 | j
     uint32_t *active;  // experts in use, then the count at active[pairs]
+    uint32_t *rbound;  // CTA b takes active rows [rbound[b], rbound[b + 1])
+    uint32_t grid;     // CTAs of the gather kernel
     float *partial;    // pairs * ne * S
     int32_t *status;
 };
 
 static inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
+constexpr uint32_t MOE_MAX_CTAS = 1024;
+constexpr uint32_t MAXT = 4;     // tokens per pass over a row (more stream the row again)
+
 struct WsLayout {
-    size_t eoff, elist, active, partial, total;
+    size_t eoff, elist, active, rbound, partial, total;
 };
 
 static inline WsLayout moe_ws_layout(uint32_t n_experts, uint64_t ne, uint64_t cols, uint32_t tokens,
@@ -71,18 +77,62 @@ static inline WsLayout moe_ws_layout(uint32_t n_experts, uint64_t ne, uint64_t c
     l.eoff = 0;
     l.elist = align256(l.eoff + 4ull * (n_experts + 1));
     l.active = align256(l.elist + 4ull * pairs);
-    l.partial = align256(l.active + 4ull * (pairs + 1));
+    l.rbound = align256(l.active + 4ull * (pairs + 1));
+    l.partial = align256(l.rbound + 4ull * (MOE_MAX_CTAS + 1));
     l.total = align256(l.partial + 4ull * pairs * ne * (uint64_t)S);
     return l;
 }
 
-__global__ void __launch_bounds__(1024) k_moe_route(MoeArgs a) {
-    __shared__ uint32_t cnt[MOE_MAX_EXPERTS];
-    __shared__ uint32_t nact;
-    const uint32_t P = a.tokens * a.topk;
-    for (uint32_t e = threadIdx.x; e < a.n_experts; e += blockDim.x) cnt[e] = 0;
+// Exclusive prefix sum over a 1024-thread block of one 64-bit value per
+// thread; *total gets the block sum.
+__device__ __forceinline__ uint64_t block_excl_scan64(uint64_t v, uint64_t *sw, uint64_t *total) {
+    const uint32_t lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    uint64_t x = v;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const uint64_t y = __shfl_up_sync(DGT_FULL, x, d);
+        if (lane >= (uint32_t)d) x += y;
+    }
+    if (lane == 31) sw[w] = x;
     __syncthreads();
-    for (uint32_t q = threadIdx.x; q < P; q += blockDim.x) {
+    if (w == 0) {
+        uint64_t t = sw[lane];
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const uint64_t y = __shfl_up_sync(DGT_FULL, t, d);
+            if (lane >= (uint32_t)d) t += y;
+        }
+        sw[lane] = t;
+    }
+    __syncthreads();
+    const uint64_t before = (w ? sw[w - 1] : 0ull) + x - v;
+    *total = sw[31];
+    __syncthreads();
+    return before;
+}
+
+// Cost of one row of an expert with nt routed pairs: its passes over the row
+// (each a stream of the row, weighted as ROW_COST token chains) and its chains.
+constexpr uint64_t ROW_COST = 2;
+__device__ __forceinline__ uint64_t moe_row_cost(uint32_t nt) {
+    return ((nt + MAXT - 1) / MAXT) * ROW_COST + nt;
+}
+
+// One CTA: count the pairs per expert, list the experts in use, place every
+// pair (t, j) in its expert's list in (t, j) order (deterministic, no
+// atomics in the placement), and split the rows of the experts in use over
+// the gather kernel's CTAs by cost (passes and token chains), so that a CTA
+// whose rows belong to an expert with many tokens gets fewer rows.
+__global__ void __launch_bounds__(1024) k_moe_route(MoeArgs a) {
+    // cnt (per expert) and, once every thread has read it, the cost prefix
+    // (per active expert) share one array
+    __shared__ uint64_t cost[MOE_MAX_EXPERTS + 1];
+    __shared__ uint64_t sw[32];
+    uint32_t *cnt = reinterpret_cast<uint32_t *>(cost);
+    const uint32_t P = a.tokens * a.topk, tid = threadIdx.x;
+    for (uint32_t e = tid; e < a.n_experts; e += blockDim.x) cnt[e] = 0;
+    __syncthreads();
+    for (uint32_t q = tid; q < P; q += blockDim.x) {
         const int32_t e = a.ids[q];
         if (e < 0 || (uint32_t)e >= a.n_experts) {
             set_status(a.status, DGT_ERR_ARG);
@@ -91,160 +141,570 @@ __global__ void __launch_bounds__(1024) k_moe_route(MoeArgs a) {
         atomicAdd(&cnt[e], 1u);
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
-        uint32_t o = 0, na = 0;
-        for (uint32_t e = 0; e < a.n_experts; e++) {
-            a.eoff[e] = o;
-            if (cnt[e]) a.active[na++] = e;
-            o += cnt[e];
+    // eoff (pairs before each expert) and the active list, four experts per thread
+    constexpr uint32_t PER = MOE_MAX_EXPERTS / 1024;
+    uint32_t c4[PER], f4[PER];
+    uint64_t cs = 0, fs = 0;
+#pragma unroll
+    for (uint32_t i = 0; i < PER; i++) {
+        const uint32_t e = tid * PER + i;
+        c4[i] = e < a.n_experts ? cnt[e] : 0u;
+        f4[i] = c4[i] != 0;
+        cs += c4[i];
+        fs += f4[i];
+    }
+    uint64_t ptot, atot;
+    uint64_t o = block_excl_scan64(cs, sw, &ptot);
+    uint64_t na = block_excl_scan64(fs, sw, &atot);
+    const uint32_t nact = (uint32_t)atot;
+#pragma unroll
+    for (uint32_t i = 0; i < PER; i++) {
+        const uint32_t e = tid * PER + i;
+        if (e < a.n_experts) {
+            a.eoff[e] = (uint32_t)o;
+            if (c4[i]) {
+                a.active[na] = e;
+                cost[na] = a.ne * moe_row_cost(c4[i]);
+            }
         }
-        a.eoff[a.n_experts] = o;
-        a.active[P] = na;
-        nact = na;
+        o += c4[i];
+        na += f4[i];
+    }
+    if (tid == 0) {
+        a.eoff[a.n_experts] = (uint32_t)ptot;
+        a.active[P] = nact;
     }
     __syncthreads();
-    for (uint32_t q = threadIdx.x; q < P; q += blockDim.x) {
+    // cost prefix over the active experts (in active[] order)
+    uint64_t cv[PER], csum = 0;
+#pragma unroll
+    for (uint32_t i = 0; i < PER; i++) {
+        const uint32_t k = tid * PER + i;
+        cv[i] = k < nact ? cost[k] : 0ull;
+        csum += cv[i];
+    }
+    uint64_t ctot;
+    uint64_t cb = block_excl_scan64(csum, sw, &ctot);
+#pragma unroll
+    for (uint32_t i = 0; i < PER; i++) {
+        const uint32_t k = tid * PER + i;
+        if (k < nact) cost[k] = cb;
+        cb += cv[i];
+    }
+    if (tid == 0) cost[nact] = ctot;
+    __syncthreads();
+    // CTA b starts at the row where the cost b * ctot / grid falls
+    for (uint32_t b = tid; b <= a.grid; b += blockDim.x) {
+        uint64_t row = (uint64_t)nact * a.ne;
+        if (b < a.grid && nact) {
+            const uint64_t c = ctot * b / a.grid;
+            uint32_t lo = 0, hi = nact - 1;   // largest k with cost[k] <= c
+            while (lo < hi) {
+                const uint32_t mid = (lo + hi + 1) / 2;
+                if (cost[mid] <= c) lo = mid;
+                else hi = mid - 1;
+            }
+            const uint64_t rc = (cost[lo + 1] - cost[lo]) / a.ne;
+            uint64_t r = rc ? (c - cost[lo]) / rc : 0;
+            if (r > a.ne) r = a.ne;
+            row = (uint64_t)lo * a.ne + r;
+        }
+        a.rbound[b] = (uint32_t)row;
+    }
+    // placement
+    for (uint32_t q = tid; q < P; q += blockDim.x) {
         const int32_t e = a.ids[q];
         if (e < 0 || (uint32_t)e >= a.n_experts) continue;
         uint32_t before = 0;
         for (uint32_t q2 = 0; q2 < q; q2++) before += a.ids[q2] == e;
         a.elist[a.eoff[e] + before] = ((q / a.topk) << 8) | (q % a.topk);
     }
-    (void)nact;
 }
 
-// One round of one expert row for one lane: eight bf16 pairs (escapes patched).
+// ---------------------------------------------------------------------------
+// Expert rows streamed through shared memory.  The rows of the experts in use
+// (active[] order, expert by expert) are split over one CTA per SM by cost;
+// consumer warp w of a CTA takes its rows w, w + MNW, ...  A producer warp
+// keeps each consumer's ring of stages full with 1-D bulk copies of pieces of
+// MC rounds (polling the rings' "empty" barriers without blocking).  For each
+// row a warp decodes every 16-weight lane chunk once and runs one fmaf chain
+// per routed token (up to MAXT per pass over the row; more tokens stream the
+// row again), x read through L1.  At every slice end the chains are
+// butterfly-reduced into the workspace.
+// ---------------------------------------------------------------------------
+constexpr int MNW = 15;          // consumer warps (+ the producer: 4 warps per scheduler)
+constexpr uint32_t MC = 4;       // rounds per piece
+constexpr uint32_t MNS_MAX = 3;  // stages per consumer (R4: 3, BF16: 2)
+constexpr uint32_t XS_BYTES = 64 * 1024;   // x of the CTA's tokens staged in shared memory
+constexpr uint32_t XS_TOKENS = 1024;       // token bitmap / slot map size
+
 template <bool R4>
-__device__ __forceinline__ void moe_round(const MoeArgs &a, uint4 sv, uint2 nv, uint4 hv, uint32_t c, uint32_t b,
-                                          bool act, uint8_t *escb, const uint8_t *table_s, uint32_t p[8]) {
-    if (R4) {
-        r4_dec16(nv, sv, a.L, p);
-        if (c) {
-            const uint32_t lane = lane_id();
-            const uint32_t cc = c > DGT_SEG ? DGT_SEG : c;
-            for (uint32_t i = lane; i < cc; i += 32) escb[i] = (uint64_t)b + i < a.n_esc ? a.esc[b + i] : 0;
-            __syncwarp();
-            const uint32_t m0 = act ? nib15_mask(nv.x) : 0u, m1 = act ? nib15_mask(nv.y) : 0u;
-            if (!patch_escapes(p, m0, m1, cc, escb, table_s) && lane == 0) set_status(a.status, DGT_ERR_CORRUPT);
-            __syncwarp();
-        }
+struct MoeStage {
+    static constexpr uint32_t BYTES = R4 ? MC * 768 : MC * 1024;
+    static constexpr uint32_t NS = R4 ? 3 : 2;
+};
+
+// Row gi of the active rows: the expert's flat row and its routed pairs.
+struct MoeRow {
+    uint64_t grow;     // row of the stacked weight tensor
+    uint32_t r;        // row inside the expert
+    uint32_t l0, nt;   // the expert's pairs: elist[l0 .. l0 + nt)
+    uint32_t li;       // the expert's place in the CTA's expert table (or XT_MAX)
+};
+
+// The experts a CTA's rows belong to (consecutive in active[] order), with
+// their first routed pairs, staged in shared memory once per CTA.
+constexpr uint32_t XT_MAX = 64;    // experts per CTA table
+constexpr uint32_t XT_ENT = 16;    // pairs kept per expert
+struct MoeTable {
+    uint64_t ai0;                  // first expert (index into active[])
+    uint32_t n;                    // experts in the table
+    uint32_t e[XT_MAX], l0[XT_MAX], nt[XT_MAX];
+    uint32_t ent[XT_MAX][XT_ENT];
+};
+
+// Place of an active row: expert ai (index into active[]) and row r in it,
+// stepped without division.
+struct RowPos {
+    uint64_t ai;
+    uint32_t r;
+};
+
+__device__ __forceinline__ RowPos row_pos(const MoeArgs &a, uint64_t gi) {
+    RowPos p;
+    p.ai = gi / a.ne;
+    p.r = (uint32_t)(gi - p.ai * a.ne);
+    return p;
+}
+
+__device__ __forceinline__ void row_step(const MoeArgs &a, RowPos &p, uint32_t d) {
+    p.r += d;
+    while (p.r >= a.ne) {
+        p.r -= (uint32_t)a.ne;
+        p.ai++;
+    }
+}
+
+__device__ __forceinline__ MoeRow moe_row(const MoeArgs &a, const MoeTable &T, RowPos pos) {
+    MoeRow m;
+    const uint64_t ai = pos.ai;
+    m.r = pos.r;
+    const uint64_t li = ai - T.ai0;
+    uint32_t e;
+    if (li < T.n) {
+        m.li = (uint32_t)li;
+        e = T.e[li];
+        m.l0 = T.l0[li];
+        m.nt = T.nt[li];
     } else {
-        p[0] = sv.x; p[1] = sv.y; p[2] = sv.z; p[3] = sv.w;
-        p[4] = hv.x; p[5] = hv.y; p[6] = hv.z; p[7] = hv.w;
+        const uint32_t P = a.tokens * a.topk;
+        m.li = XT_MAX;
+        e = a.active[ai] % a.n_experts;
+        m.l0 = min(a.eoff[e], P);
+        m.nt = min(max(a.eoff[e + 1], m.l0), P) - m.l0;
+    }
+    m.grow = (uint64_t)e * a.ne + m.r;
+    return m;
+}
+
+// Pair k of a row's expert (t << 8 | slot).
+__device__ __forceinline__ uint32_t moe_pair(const MoeArgs &a, const MoeTable &T, const MoeRow &m, uint32_t k) {
+    return (m.li < XT_MAX && k < XT_ENT) ? T.ent[m.li][k] : a.elist[m.l0 + k];
+}
+
+// The next piece a producer lane copies.
+struct MoeCursor {
+    uint64_t i;        // CTA-local row index (warp w: w, w + MNW, ...)
+    RowPos pos;
+    uint64_t grow;
+    uint32_t pass, npass, j;
+};
+
+__device__ __forceinline__ void moe_cursor_load(const MoeArgs &a, const MoeTable &T, MoeCursor &c, uint64_t nrows) {
+    c.pass = 0;
+    c.j = 0;
+    if (c.i < nrows) {
+        const MoeRow m = moe_row(a, T, c.pos);
+        c.grow = m.grow;
+        c.npass = (m.nt + MAXT - 1) / MAXT;
     }
 }
 
-// A warp takes MOE_RG consecutive rows of one expert in use; for each row it
-// issues the loads of up to 8 rounds at once, then walks the rounds slice by
-// slice, running one fmaf chain per routed token; at the end of each slice
-// the chains are butterfly-reduced and stored as that slice's partials.
-constexpr uint32_t MOE_RG = 2;
-constexpr uint32_t MOE_RB = 4;   // rounds loaded at once
+template <bool R4>
+__device__ __forceinline__ void moe_issue(const MoeArgs &a, uint64_t grow, uint32_t j, uint32_t stage, uint32_t bar) {
+    const uint32_t n = min(MC, a.J - j);
+    const uint32_t k0 = j * 512;
+    const uint32_t cols = min((j + n) * 512, (uint32_t)a.cols) - k0;
+    const uint64_t f = grow * a.cols + k0;
+    fence_proxy_async_smem();
+    if (R4) {
+        mbar_arrive_expect_tx(bar, cols + cols / 2);
+        bulk_g2s(stage, a.sm + f, cols, bar);
+        bulk_g2s(stage + MC * 512, a.nib + f / 2, cols / 2, bar);
+    } else {
+        mbar_arrive_expect_tx(bar, cols * 2);
+        bulk_g2s(stage, a.W + f, cols * 2, bar);
+    }
+}
+
+// x of token t for lane chunk (round j, lane): two uint4 of bf16 pairs; zero
+// past K.
+__device__ __forceinline__ void moe_x(const MoeArgs &a, uint32_t t, uint32_t j, uint32_t lane, bool act, uint4 &xa,
+                                      uint4 &xb) {
+    if (act) {
+        const uint4 *xp = reinterpret_cast<const uint4 *>(a.x + (size_t)t * a.cols + 512 * j + 16 * lane);
+        xa = __ldg(xp);
+        xb = __ldg(xp + 1);
+    } else {
+        xa = xb = make_uint4(0, 0, 0, 0);
+    }
+}
+
+__device__ __forceinline__ float fma_chunk16_x(const uint32_t p[8], uint4 xa, uint4 xb, float acc) {
+    acc = fma2_bf16(p[0], xa.x, acc);
+    acc = fma2_bf16(p[1], xa.y, acc);
+    acc = fma2_bf16(p[2], xa.z, acc);
+    acc = fma2_bf16(p[3], xa.w, acc);
+    acc = fma2_bf16(p[4], xb.x, acc);
+    acc = fma2_bf16(p[5], xb.y, acc);
+    acc = fma2_bf16(p[6], xb.z, acc);
+    acc = fma2_bf16(p[7], xb.w, acc);
+    return acc;
+}
+
+// A consumer warp's ring state.
+struct MoeRing {
+    const uint8_t *ring;
+    uint32_t full_a, empty_a;
+    uint32_t st, phases, waited;
+    bool ok;
+    int *abort;        // tells the producer to stop after a timeout
+};
+
+// One pass over one row for NT token chains (the first ntp of them are real;
+// the others repeat token 0 and store nothing): pieces from the ring, each
+// 16-weight lane chunk decoded once, one fmaf chain per token, slice partials
+// butterfly-reduced into the workspace.
+template <bool R4, int NT>
+__device__ __forceinline__ void moe_row_pass(const MoeArgs &a, MoeRing &rg, const MoeRow &m, uint32_t ent,
+                                             uint32_t ntp, const R4Lut &L, SegInfo &g, RoundLut &rl,
+                                             const uint8_t *table_s, uint8_t *escb, uint32_t lane, bool act_last,
+                                             uint32_t S, uint32_t log2S, const uint16_t *xslot, const uint16_t *xsm) {
+    constexpr uint32_t STAGE = MoeStage<R4>::BYTES;
+    const uint32_t J = a.J, Jm1 = J - 1;
+    const uint4 *xr[NT];
+    uint32_t en[NT];
+#pragma unroll
+    for (int t = 0; t < NT; t++) {
+        en[t] = __shfl_sync(DGT_FULL, ent, (uint32_t)t < ntp ? t : 0);
+        const uint32_t tk = (en[t] >> 8) % a.tokens;
+        const uint32_t slot = (xslot && tk < XS_TOKENS) ? xslot[tk] : 0xFFFFu;
+        xr[t] = (slot != 0xFFFFu ? reinterpret_cast<const uint4 *>(xsm + (size_t)slot * a.cols)
+                                 : reinterpret_cast<const uint4 *>(a.x + (size_t)tk * a.cols)) + 2 * lane;
+    }
+    float acc[NT];
+#pragma unroll
+    for (int t = 0; t < NT; t++) acc[t] = 0.0f;
+    uint32_t s = 0, send = J >> log2S, jbase = 0;
+    for (uint32_t jp = 0; jp < J; jp += MC) {
+        if (rg.ok && a.bulk) {
+            if (mbar_wait(rg.full_a + 8 * rg.st, (rg.phases >> rg.st) & 1u)) {
+                rg.waited++;
+            } else {
+                rg.ok = false;
+                if (lane == 0) {
+                    set_status(a.status, DGT_ERR_TIMEOUT);
+                    atomicExch(rg.abort, 1);
+                }
+            }
+            if (*(volatile int *)rg.abort) rg.ok = false;
+        }
+        rg.ok = __all_sync(DGT_FULL, rg.ok);
+        rg.phases ^= 1u << rg.st;
+        const uint32_t n = min(MC, J - jp);
+        if (R4 && jp - jbase >= 32) {
+            jbase = jp;
+            g = load_seginfo(a, table_s, m.grow, jbase, J, lane);
+            rl = round_luts(g, L);
+        }
+        const uint8_t *stg = rg.ring + rg.st * STAGE;
+        const uint4 *xp[NT];
+#pragma unroll
+        for (int t = 0; t < NT; t++) xp[t] = xr[t] + 64 * jp;
+#pragma unroll
+        for (uint32_t r = 0; r < MC; r++) {
+            if (r >= n) break;
+            const uint32_t j = jp + r;
+            const bool act = j != Jm1 || act_last;
+            uint32_t p[8];
+            if (R4) {
+                uint4 sv;
+                uint2 nv;
+                if (a.bulk) {
+                    sv = *reinterpret_cast<const uint4 *>(stg + r * 512 + 16 * lane);
+                    nv = *reinterpret_cast<const uint2 *>(stg + MC * 512 + r * 256 + 8 * lane);
+                } else {
+                    // rows whose nibbles are not 16-byte aligned: direct loads
+                    const uint64_t f = m.grow * a.cols + 512 * j + 16 * lane;
+                    sv = act ? ldg_stream16(a.sm + f) : make_uint4(0, 0, 0, 0);
+                    nv = act ? ldg_stream8(a.nib + f / 2) : make_uint2(0, 0);
+                }
+                const uint32_t bit = j - jbase;
+                R4Lut Lr = L;
+                Lr.h3 = __shfl_sync(DGT_FULL, rl.h3, bit);
+                Lr.l1 = __shfl_sync(DGT_FULL, rl.l1, bit);
+                if ((rl.multi >> bit) & 1u) {
+                    uint32_t e;
+                    const uint2 nva = act ? nv : make_uint2(0, 0);
+                    if (multi_exponent(a, g, bit, nva, table_s, lane, e)) {
+                        r4_dec16(nv, sv, lut15(L, e), p);
+                    } else {
+                        r4_round_general(a, L, nv, sv, g, bit, escb, table_s, lane, act, p);
+                    }
+                } else {
+                    r4_dec16(nv, sv, Lr, p);
+                }
+            } else {
+                const uint4 lo = *reinterpret_cast<const uint4 *>(stg + r * 1024 + 32 * lane);
+                const uint4 hi = *reinterpret_cast<const uint4 *>(stg + r * 1024 + 32 * lane + 16);
+                p[0] = lo.x; p[1] = lo.y; p[2] = lo.z; p[3] = lo.w;
+                p[4] = hi.x; p[5] = hi.y; p[6] = hi.z; p[7] = hi.w;
+            }
+            if (act) {
+#pragma unroll
+                for (int t = 0; t < NT; t++) {
+                    const uint4 xa = xp[t][64 * r], xb = xp[t][64 * r + 1];
+                    acc[t] = fma_chunk16_x(p, xa, xb, acc[t]);
+                }
+            }
+            if (j + 1 == send) {
+                // end of slice s: reduce and store; the next slice starts from +0
+#pragma unroll
+                for (int t = 0; t < NT; t++) {
+                    float v = acc[t];
+#pragma unroll
+                    for (int d = 16; d >= 1; d >>= 1) v += __shfl_xor_sync(DGT_FULL, v, d);
+                    const uint64_t q = (uint64_t)(en[t] >> 8) * a.topk + (en[t] & 0xFF);
+                    if (lane == 0 && rg.ok && (uint32_t)t < ntp) a.partial[(q * a.ne + m.r) * S + s] = v;
+                    acc[t] = 0.0f;
+                }
+                s++;
+                send = ((s + 1) * J) >> log2S;
+            }
+        }
+        __syncwarp();
+        if (a.bulk) {
+            if (rg.ok && lane == 0) mbar_arrive(rg.empty_a + 8 * rg.st);
+            rg.st = rg.st + 1 == MoeStage<R4>::NS ? 0 : rg.st + 1;
+        }
+    }
+}
 
 template <bool R4>
-__global__ void __launch_bounds__(MW * 32, 2) k_moe(MoeArgs a) {
-    extern __shared__ uint4 xs[];  // [token][round][half][lane]
+__global__ void __launch_bounds__((MNW + 1) * 32, 1) k_moe(MoeArgs a) {
+    constexpr uint32_t STAGE = MoeStage<R4>::BYTES, MNS = MoeStage<R4>::NS;
+    extern __shared__ __align__(128) uint8_t dsm[];
+    __shared__ __align__(8) uint64_t full[MNW][MNS_MAX];
+    __shared__ __align__(8) uint64_t empty[MNW][MNS_MAX];
+    __shared__ uint32_t tok_bits[XS_TOKENS / 32];
+    __shared__ uint16_t xslot[XS_TOKENS];
     __shared__ uint8_t table_s[256];
-    __shared__ uint8_t escb[MW][DGT_SEG];
+    __shared__ uint8_t escb[R4 ? MNW : 1][R4 ? DGT_SEG : 1];
+    __shared__ int abort_flag;
+    __shared__ MoeTable T;
     const uint32_t tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
-    const uint32_t K = (uint32_t)a.cols, J = a.J;
-    for (uint32_t i = tid; i < a.tokens * J * 64; i += MW * 32) {
-        const uint32_t t = i / (J * 64), r = i - t * J * 64;
-        const uint32_t k = 8 * r, j = k >> 9, u = (k >> 4) & 31, h = (k >> 3) & 1;
-        xs[(((size_t)t * J + j) * 2 + h) * 32 + u] =
-            k < K ? *reinterpret_cast<const uint4 *>(a.x + (size_t)t * K + k) : make_uint4(0, 0, 0, 0);
-    }
-    if (R4) table_s[tid] = a.table[tid];
-    __syncthreads();
     const uint32_t P = a.tokens * a.topk;
-    const uint32_t nact = a.active[P];
-    const uint32_t S = a.S, log2S = __ffs(S) - 1;
-    const uint64_t groups = (a.ne + MOE_RG - 1) / MOE_RG;
-    const uint64_t units = (uint64_t)nact * groups;
-    const uint32_t Jm1 = J - 1;
-    const bool last_ok = 16 * lane < K - 512 * Jm1;
-    for (uint64_t uu = (uint64_t)blockIdx.x * MW + w; uu < units; uu += (uint64_t)gridDim.x * MW) {
-        const uint32_t ai = (uint32_t)(uu / groups);
-        const uint64_t g = uu - (uint64_t)ai * groups;
-        const uint32_t e = a.active[ai];
-        const uint32_t l0 = a.eoff[e], nt = a.eoff[e + 1] - l0;
-        for (uint32_t tg = 0; tg < nt; tg += MOE_TPASS) {
-            const uint32_t ntg = min(MOE_TPASS, nt - tg);
-            const uint32_t ent = lane < ntg ? a.elist[l0 + tg + lane] : 0u;
-            uint32_t tk[MOE_TPASS];
-#pragma unroll
-            for (int i = 0; i < (int)MOE_TPASS; i++) tk[i] = (__shfl_sync(DGT_FULL, ent, i) >> 8) % a.tokens;
-            for (uint64_t r = g * MOE_RG; r < a.ne && r < (g + 1) * MOE_RG; r++) {
-                const uint64_t grow = (uint64_t)e * a.ne + r;
-                float acc[MOE_TPASS];
-#pragma unroll
-                for (int i = 0; i < (int)MOE_TPASS; i++) acc[i] = 0.0f;
-                uint32_t s = 0, send = J >> log2S;  // current slice and its end round
-                for (uint32_t jb = 0; jb < J; jb += MOE_RB) {
-                    uint4 sv[MOE_RB], hv[MOE_RB];
-                    uint2 nv[MOE_RB];
-                    uint32_t sgb = 0, sgc = 0;
-                    if (R4 && lane <= MOE_RB && jb + lane <= J) {
-                        const uint32_t *sp = a.seg + grow * a.nseg + jb + lane;
-                        sgb = sp[0];
-                        sgc = jb + lane < J ? sp[1] - sgb : 0u;
-                    }
-#pragma unroll
-                    for (uint32_t t = 0; t < MOE_RB; t++) {
-                        const uint32_t j = jb + t;
-                        const bool act = j < J && (j != Jm1 || last_ok);
-                        const uint64_t f = grow * a.cols + (uint64_t)j * 512 + 16 * lane;
-                        sv[t] = hv[t] = make_uint4(0, 0, 0, 0);
-                        nv[t] = make_uint2(0, 0);
-                        if (act) {
-                            if (R4) {
-                                sv[t] = ldg_stream16(a.sm + f);
-                                nv[t] = ldg_stream8(a.nib + f / 2);
-                            } else {
-                                sv[t] = ldg_stream16(a.W + f);
-                                hv[t] = ldg_stream16(a.W + f + 8);
-                            }
+    const uint64_t rb = a.rbound[blockIdx.x], nrows = a.rbound[blockIdx.x + 1] - rb;
+    (void)P;
+    const uint32_t J = a.J, K = (uint32_t)a.cols;
+    // the experts of rows [rb, rb + nrows) and their first pairs
+    if (nrows) {
+        const uint64_t ai0 = rb / a.ne, ai1 = (rb + nrows - 1) / a.ne;
+        const uint32_t n = (uint32_t)min(ai1 - ai0 + 1, (uint64_t)XT_MAX);
+        if (tid == 0) {
+            T.ai0 = ai0;
+            T.n = n;
+        }
+        for (uint32_t li = tid; li < n; li += blockDim.x) {
+            const uint32_t e = a.active[ai0 + li] % a.n_experts;
+            const uint32_t l0 = min(a.eoff[e], P), l1 = min(max(a.eoff[e + 1], l0), P);
+            T.e[li] = e;
+            T.l0[li] = l0;
+            T.nt[li] = l1 - l0;
+        }
+        __syncthreads();
+        for (uint32_t k = tid; k < n * XT_ENT; k += blockDim.x) {
+            const uint32_t li = k / XT_ENT, kk = k % XT_ENT;
+            if (kk < T.nt[li]) T.ent[li][kk] = a.elist[T.l0[li] + kk];
+        }
+    } else if (tid == 0) {
+        T.ai0 = 0;
+        T.n = 0;
+    }
+    // x of the tokens routed to those experts, in shared memory (as many as fit)
+    const bool xstage = a.tokens <= XS_TOKENS && a.xs_slots > 0;
+    uint16_t *xsm = reinterpret_cast<uint16_t *>(dsm + (size_t)MNW * MoeStage<R4>::NS * MoeStage<R4>::BYTES);
+    if (xstage) {
+        for (uint32_t i = tid; i < XS_TOKENS / 32; i += blockDim.x) tok_bits[i] = 0;
+        __syncthreads();
+        for (uint32_t k = tid; k < T.n * XT_ENT; k += blockDim.x) {
+            const uint32_t li = k / XT_ENT, kk = k % XT_ENT;
+            if (kk < T.nt[li]) {
+                const uint32_t tk = (T.ent[li][kk] >> 8) % a.tokens;
+                atomicOr(&tok_bits[tk >> 5], 1u << (tk & 31));
+            }
+        }
+        __syncthreads();
+        if (w == 0) {
+            // slots in token order, up to xs_slots
+            uint32_t base = 0;
+            for (uint32_t c = 0; c < XS_TOKENS / 32; c += 32) {
+                const uint32_t bits = c + lane < XS_TOKENS / 32 ? tok_bits[c + lane] : 0u;
+                uint32_t tot;
+                const uint32_t pre = warp_excl_scan(__popc(bits), &tot);
+                uint32_t b = bits, o = base + pre;
+                while (b) {
+                    const uint32_t i = __ffs(b) - 1;
+                    b &= b - 1;
+                    xslot[32 * (c + lane) + i] = o < a.xs_slots ? (uint16_t)o : (uint16_t)0xFFFFu;
+                    o++;
+                }
+                for (uint32_t i = 0; i < 32; i++)
+                    if (!((bits >> i) & 1u) && 32 * (c + lane) + i < XS_TOKENS) xslot[32 * (c + lane) + i] = 0xFFFFu;
+                base += tot;
+            }
+        }
+        __syncthreads();
+        const uint32_t kv = K / 8;   // uint4 per token row
+        for (uint32_t i = tid; i < a.tokens * kv; i += blockDim.x) {
+            const uint32_t tk = i / kv, c = i - tk * kv;
+            const uint32_t slot = xslot[tk];
+            if (slot != 0xFFFFu)
+                reinterpret_cast<uint4 *>(xsm + (size_t)slot * K)[c] =
+                    reinterpret_cast<const uint4 *>(a.x + (size_t)tk * K)[c];
+        }
+    }
+    const uint16_t *xslot_p = xstage ? xslot : nullptr;
+
+    if (tid < MNW * MNS_MAX) {
+        mbar_init(smem_u32(&full[0][0]) + 8 * tid, 1);
+        mbar_init(smem_u32(&empty[0][0]) + 8 * tid, 1);
+    }
+    if (tid == 0) abort_flag = 0;
+    if (R4 && tid < 256) table_s[tid] = a.table[tid];
+    fence_mbarrier_init();
+    __syncthreads();
+
+    if (w == MNW) {
+        // ---- producer warp: lane c keeps consumer c's ring full
+        if (lane < MNW && a.bulk) {
+            const uint32_t ring_a = smem_u32(dsm + (size_t)lane * MNS * STAGE);
+            const uint32_t full_a = smem_u32(&full[lane][0]), empty_a = smem_u32(&empty[lane][0]);
+            MoeCursor cur;
+            cur.i = lane;
+            cur.pos = row_pos(a, rb + lane);
+            moe_cursor_load(a, T, cur, nrows);
+            uint32_t q = 0, idle = 0;
+            while (cur.i < nrows && !*(volatile int *)&abort_flag) {
+                const uint32_t st = q % MNS;
+                if (q < MNS || mbar_test_wait(empty_a + 8 * st, ((q / MNS) - 1) & 1u)) {
+                    moe_issue<R4>(a, cur.grow, cur.j, ring_a + st * STAGE, full_a + 8 * st);
+                    q++;
+                    idle = 0;
+                    cur.j += MC;
+                    if (cur.j >= J) {
+                        cur.j = 0;
+                        if (++cur.pass >= cur.npass) {
+                            cur.i += MNW;
+                            row_step(a, cur.pos, MNW);
+                            moe_cursor_load(a, T, cur, nrows);
                         }
                     }
-#pragma unroll
-                    for (uint32_t t = 0; t < MOE_RB; t++) {
-                        const uint32_t j = jb + t;
-                        if (j >= J) break;
-                        const bool act = j != Jm1 || last_ok;
-                        const uint32_t c = R4 ? __shfl_sync(DGT_FULL, sgc, t) : 0u;
-                        const uint32_t b = R4 ? __shfl_sync(DGT_FULL, sgb, t) : 0u;
-                        uint32_t p[8];
-                        moe_round<R4>(a, sv[t], nv[t], hv[t], c, b, act, escb[w], table_s, p);
-                        if (act) {
-#pragma unroll
-                            for (int i = 0; i < (int)MOE_TPASS; i++)
-                                if ((uint32_t)i < ntg) acc[i] = fma_chunk16(p, xs + (size_t)tk[i] * J * 64, j, lane, acc[i]);
-                        }
-                        if (j + 1 == send) {
-                            // end of slice s: reduce and store, start the next slice from +0
-#pragma unroll
-                            for (int i = 0; i < (int)MOE_TPASS; i++) {
-                                if ((uint32_t)i < ntg) {
-                                    float v = acc[i];
-#pragma unroll
-                                    for (int d = 16; d >= 1; d >>= 1) v += __shfl_xor_sync(DGT_FULL, v, d);
-                                    const uint32_t en = __shfl_sync(DGT_FULL, ent, i);
-                                    const uint64_t q = (uint64_t)(en >> 8) * a.topk + (en & 0xFF);
-                                    if (lane == 0) a.partial[(q * a.ne + r) * S + s] = v;
-                                    acc[i] = 0.0f;
-                                }
-                            }
-                            s++;
-                            send = ((s + 1) * J) >> log2S;
-                        }
-                    }
+                } else if (++idle >= MBAR_SPIN_LIMIT) {
+                    set_status(a.status, DGT_ERR_TIMEOUT);
+                    atomicExch(&abort_flag, 1);
+                    break;
                 }
             }
         }
+        return;
     }
+
+    // ---- consumer warps
+    R4Lut L;
+    L.h0 = opaque(a.L.h0);
+    L.h1 = opaque(a.L.h1);
+    L.h2 = opaque(a.L.h2);
+    L.h3 = opaque(a.L.h3);
+    L.l0 = opaque(a.L.l0);
+    L.l1 = opaque(a.L.l1);
+    const uint8_t *ring = dsm + (size_t)w * MNS * STAGE;
+    const uint32_t full_a = smem_u32(&full[w][0]), empty_a = smem_u32(&empty[w][0]);
+    const uint32_t Jm1 = J - 1;
+    const bool act_last = 16 * lane < K - 512 * Jm1;
+    const uint32_t S = a.S, log2S = __ffs(S) - 1;
+    uint32_t st = 0, phases = 0, waited = 0;
+    bool ok = true;
+    SegPre pre = {0, 0, 0, 0};
+    if (R4 && (uint64_t)w < nrows) {
+        const MoeRow m = moe_row(a, T, row_pos(a, rb + w));
+        seg_issue(a, m.grow, 0, J, lane, pre);
+        seg_issue_esc(a, pre);
+    }
+    RowPos pos = row_pos(a, rb + w);
+    for (uint64_t i = w; i < nrows; i += MNW, row_step(a, pos, MNW)) {
+        const MoeRow m = moe_row(a, T, pos);
+        SegInfo g = {0, 0, 0, 0, 0};
+        RoundLut rl = {0, 0, 0};
+        SegPre nxt = {0, 0, 0, 0};
+        bool nxt_esc = false;
+        const bool has_next = i + MNW < nrows;
+        if (R4) {
+            g = seg_finish(pre, table_s);
+            rl = round_luts(g, L);
+            if (has_next) {
+                RowPos pn = pos;
+                row_step(a, pn, MNW);
+                const MoeRow mn = moe_row(a, T, pn);
+                seg_issue(a, mn.grow, 0, J, lane, nxt);
+            }
+        }
+        for (uint32_t tg = 0; tg < m.nt; tg += MAXT) {
+            const uint32_t ntp = min(MAXT, m.nt - tg);
+            const uint32_t ent = lane < ntp ? moe_pair(a, T, m, tg + lane) : 0u;
+            MoeRing rg{ring, full_a, empty_a, st, phases, waited, ok, &abort_flag};
+            if (ntp == 1)
+                moe_row_pass<R4, 1>(a, rg, m, ent, ntp, L, g, rl, table_s, escb[R4 ? w : 0], lane, act_last, S, log2S,
+                                     xslot_p, xsm);
+            else if (ntp == 2)
+                moe_row_pass<R4, 2>(a, rg, m, ent, ntp, L, g, rl, table_s, escb[R4 ? w : 0], lane, act_last, S, log2S,
+                                     xslot_p, xsm);
+            else
+                moe_row_pass<R4, 4>(a, rg, m, ent, ntp, L, g, rl, table_s, escb[R4 ? w : 0], lane, act_last, S, log2S,
+                                     xslot_p, xsm);
+            st = rg.st;
+            phases = rg.phases;
+            waited = rg.waited;
+            ok = rg.ok;
+            if (R4 && has_next && !nxt_esc) {
+                seg_issue_esc(a, nxt);
+                nxt_esc = true;
+            }
+        }
+        if (R4) {
+            if (has_next && !nxt_esc) seg_issue_esc(a, nxt);
+            pre = nxt;
+        }
+    }
+    // after a timeout: copies that may still be in flight land before exit
+    if (!ok && a.bulk)
+        for (uint32_t q = waited; q < waited + MNS; q++) mbar_wait(full_a + 8 * (q % MNS), (q / MNS) & 1u);
 }
 
 __global__ void __launch_bounds__(256) k_moe_combine(MoeArgs a) {
+    const float *__restrict__ part = a.partial;
+    const float *__restrict__ pw = a.p;
+    float *__restrict__ y32 = a.y32;
     const uint64_t n_out = (uint64_t)a.tokens * a.ne;
     for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n_out;
          i += (uint64_t)gridDim.x * blockDim.x) {
@@ -253,13 +713,13 @@ __global__ void __launch_bounds__(256) k_moe_combine(MoeArgs a) {
         float acc = 0.0f;
         for (uint32_t j = 0; j < a.topk; j++) {
             const uint64_t q = (uint64_t)t * a.topk + j;
-            const float *pp = a.partial + (q * a.ne + n) * a.S;
+            const float *pp = part + (q * a.ne + n) * a.S;
             float y = pp[0];
             for (uint32_t s = 1; s < a.S; s++) y = y + pp[s];
-            if (a.y32) a.y32[q * a.ne + n] = y;
-            if (a.p) acc = fmaf(a.p[q], y, acc);
+            if (y32) y32[q * a.ne + n] = y;
+            if (pw) acc = fmaf(pw[q], y, acc);
         }
-        if (a.p) {
+        if (pw) {
             if (a.out32) a.out32[i] = acc;
             if (a.out) a.out[i] = f32_to_bf16_rne(acc);
         }
@@ -274,19 +734,17 @@ int launch_moe(MoeArgs &a, void *d_ws, size_t ws_bytes, cudaStream_t st) {
     a.eoff = reinterpret_cast<uint32_t *>(ws + l.eoff);
     a.elist = reinterpret_cast<uint32_t *>(ws + l.elist);
     a.active = reinterpret_cast<uint32_t *>(ws + l.active);
+    a.rbound = reinterpret_cast<uint32_t *>(ws + l.rbound);
     a.partial = reinterpret_cast<float *>(ws + l.partial);
     DeviceInfo di;
     if (device_info(&di) != DGT_OK) return DGT_ERR_CUDA;
+    a.grid = (uint32_t)min(di.sms, (int)MOE_MAX_CTAS);
     k_moe_route<<<1, 1024, 0, st>>>(a);
-    const size_t smem = (size_t)a.tokens * a.J * 1024;
+    a.xs_slots = a.tokens <= XS_TOKENS ? (uint32_t)min((uint64_t)a.tokens, (uint64_t)(XS_BYTES / (2 * a.cols))) : 0u;
+    const size_t smem = (size_t)MNW * MoeStage<R4>::NS * MoeStage<R4>::BYTES + (size_t)a.xs_slots * a.cols * 2;
     int bps = 0;
-    if (prepare_kernel((const void *)k_moe<R4>, smem, MW * 32, &bps) != DGT_OK) return DGT_ERR_CUDA;
-    const uint64_t pairs = (uint64_t)a.tokens * a.topk;
-    const uint64_t max_units = (pairs < a.n_experts ? pairs : (uint64_t)a.n_experts) * ((a.ne + 1) / 2);
-    uint64_t grid = (max_units + MW - 1) / MW;
-    if (grid > (uint64_t)di.sms * bps) grid = (uint64_t)di.sms * bps;
-    if (grid < 1) grid = 1;
-    k_moe<R4><<<(unsigned)grid, MW * 32, smem, st>>>(a);
+    if (prepare_kernel((const void *)k_moe<R4>, smem, (MNW + 1) * 32, &bps) != DGT_OK) return DGT_ERR_CUDA;
+    k_moe<R4><<<a.grid, (MNW + 1) * 32, smem, st>>>(a);
     const uint64_t n_out = (uint64_t)a.tokens * a.ne;
     uint64_t cgrid = (n_out + 255) / 256;
     if (cgrid > (uint64_t)di.sms * 8) cgrid = (uint64_t)di.sms * 8;
@@ -303,6 +761,7 @@ static int moe_common(MoeArgs &a, uint64_t rows, uint64_t cols, uint32_t n_exper
         return DGT_ERR_SHAPE;
     if (cols == 0 || cols % 16 || cols >= (1ull << 31)) return DGT_ERR_SHAPE;
     if (!d_ids || !d_x || !w_ptr || !aligned16(d_x) || !aligned16(w_ptr)) return DGT_ERR_ARG;
+    if (rows == 0) return DGT_ERR_SHAPE;
     a.cols = cols;
     a.ne = rows / n_experts;
     a.n_experts = n_experts;
@@ -310,7 +769,6 @@ static int moe_common(MoeArgs &a, uint64_t rows, uint64_t cols, uint32_t n_exper
     a.topk = topk;
     a.J = (uint32_t)((cols + 511) / 512);
     a.S = (uint32_t)dgt_plan_slices(a.ne, cols);
-    if ((uint64_t)tokens * a.J * 1024 > MOE_XS_LIMIT) return DGT_ERR_SHAPE;
     a.ids = d_ids;
     a.x = d_x;
     a.status = d_status;
@@ -345,6 +803,7 @@ extern "C" int dgt_moe_gemv(const dgt_r4 *W, uint32_t n_experts, const int32_t *
     a.n_esc = W->n_esc;
     a.L = make_r4lut(W->table, W->n_table);
     for (int i = 0; i < 256; i++) a.table[i] = W->table[i];
+    a.bulk = W->cols % 32 == 0 && aligned16(W->sm) && aligned16(W->nib);
     a.p = d_p;
     a.y32 = d_y32;
     a.out = d_out;
@@ -362,6 +821,7 @@ extern "C" int dgt_moe_gemv_bf16(const uint16_t *d_W, uint64_t rows, uint64_t co
     int rc = moe_common(a, rows, cols, n_experts, tokens, topk, d_ids, d_x, d_W, d_status, st);
     if (rc != DGT_OK) return rc;
     a.W = d_W;
+    a.bulk = 1;
     a.p = d_p;
     a.y32 = d_y32;
     a.out = d_out;

@@ -280,8 +280,7 @@ int dgt_gemv_bf16(const uint16_t *d_W, uint64_t rows, uint64_t cols, const uint1
  * d_ws: device workspace of dgt_moe_workspace_bytes() bytes, 256-byte
  * aligned, caller-owned, contents need not be initialised.  d_status: device
  * int32, set to 0 then to an error code.  Limits: K % 16 == 0, topk <= 255,
- * tokens * topk <= 65536, tokens * ceil(K/512) KB of x <= 160 KB,
- * n_experts <= 4096.  Asynchronous.
+ * tokens * topk <= 65536, n_experts <= 4096.  Asynchronous.
  */
 size_t dgt_moe_workspace_bytes(uint32_t n_experts, uint64_t expert_rows, uint64_t cols, uint32_t tokens,
                                uint32_t topk);
