@@ -64,21 +64,30 @@ def hbm_peak():
 
 
 def src_sha(name):
-    with open(os.path.join(ROOT, "decode_gemv_tensor_gb300", "csrc", name), "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    """Hash of a kernel's source file and the device headers it includes."""
+    csrc = os.path.join(ROOT, "decode_gemv_tensor_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in [name] + sorted(x for x in os.listdir(csrc) if x.endswith(".cuh")):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
 
 
 def ncu_traffic(kernel):
-    """Per-launch DRAM bytes from the committed ncu summary, if it was taken on
-    the current kernel source; else None."""
+    """Per-launch DRAM bytes (read + write) of one op from the committed table
+    profiles/dram_traffic.md, if it was taken on the current kernel source;
+    else None.  Table rows: | op | kernel | source sha | read B | write B |."""
     try:
-        with open(os.path.join(ROOT, "profiles", "ncu_traffic.json")) as f:
-            t = json.load(f)[kernel]
-        if t["src_sha"] != src_sha(KERNEL_SRC[kernel]):
-            return None
-        return float(t["dram_bytes_per_launch"]) * t.get("scale", 1.0)
+        with open(os.path.join(ROOT, "profiles", "dram_traffic.md")) as f:
+            for line in f:
+                cells = [c.strip() for c in line.strip().strip("|").split("|")]
+                if len(cells) >= 5 and cells[0] == kernel:
+                    if cells[2] != src_sha(KERNEL_SRC[kernel]):
+                        return None
+                    return float(cells[3]) + float(cells[4])
     except Exception:
         return None
+    return None
 
 
 # ---------------------------------------------------------------------------

@@ -11,15 +11,15 @@
 // are bit-identical; against exact arithmetic the fp32 result is checked
 // normwise.
 //
-// Design (cta_group::1, one CTA of 8 warps per tile):
+// Design (cta_group::1, one CTA of 20 warps per tile):
 //  - Swap-AB: the 128-row W tile is operand A (M = 128), the X tile is operand
 //    B (N = mt in 16..256), the fp32 accumulator D = W x X^T lives in tensor
 //    memory: lane = W row, column = X row.
 //  - Operands are K-major SWIZZLE_128B tiles of 64 bf16 along K.  X (and W
 //    for the twin) arrive by 2-D TMA.  For R4, 2-D TMA stages the raw
-//    sign/mantissa and nibble tiles and warps 4..7 (one thread per W row)
-//    decode them into the same swizzled layout the TMA would write, with a
-//    running per-row escape index.
+//    sign/mantissa and nibble tiles and warps 4..19 (four threads per W row,
+//    16 columns each, sharing the row's running escape index through
+//    shuffles) decode them into the same swizzled layout the TMA would write.
 //  - Warp 0 lane 0 issues TMA, warp 1 lane 0 issues tcgen05.mma (four K=16
 //    steps per 64-wide stage) and commits each stage back to the producer;
 //    warps 4..7 read the accumulator with tcgen05.ld and write Y (or the

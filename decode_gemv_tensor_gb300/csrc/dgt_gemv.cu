@@ -499,9 +499,9 @@ __global__ void __launch_bounds__((TNW + 1) * 32, 1) k_gemv_tma(GemvArgs a) {
                 // rounds with two or more escapes: per-lane rank-15 entries, worked
                 // out before the multiply-adds; anything else takes the slow loop
                 uint32_t mh3[C], ml1[C];
-#pragma unroll
-                for (uint32_t r = 0; r < C; r++) mh3[r] = ml1[r] = 0;
                 if (R4 && ok && pm && !slow) {
+#pragma unroll
+                    for (uint32_t r = 0; r < C; r++) mh3[r] = ml1[r] = 0;
 #pragma unroll
                     for (uint32_t r = 0; r < C; r++) {
                         if ((pm >> r) & 1u) {
@@ -517,7 +517,28 @@ __global__ void __launch_bounds__((TNW + 1) * 32, 1) k_gemv_tma(GemvArgs a) {
                         }
                     }
                 }
-                if (ok && !slow) {
+                if (ok && !slow && pm == 0) {
+                    // the common piece: every round decodes with its shuffled table words
+#pragma unroll
+                    for (uint32_t r = 0; r < C; r++) {
+                        const uint32_t j = jp + r;
+                        uint32_t p[8];
+                        if (R4) {
+                            const uint4 sv = *reinterpret_cast<const uint4 *>(stg + r * 512 + 16 * lane);
+                            const uint2 nv = *reinterpret_cast<const uint2 *>(stg + C * 512 + r * 256 + 8 * lane);
+                            R4Lut Lr = L;
+                            Lr.h3 = __shfl_sync(DGT_FULL, rl.h3, b0 + r);
+                            Lr.l1 = __shfl_sync(DGT_FULL, rl.l1, b0 + r);
+                            r4_dec16(nv, sv, Lr, p);
+                        } else {
+                            const uint4 lo = *reinterpret_cast<const uint4 *>(stg + r * 1024 + 32 * lane);
+                            const uint4 hi = *reinterpret_cast<const uint4 *>(stg + r * 1024 + 32 * lane + 16);
+                            p[0] = lo.x; p[1] = lo.y; p[2] = lo.z; p[3] = lo.w;
+                            p[4] = hi.x; p[5] = hi.y; p[6] = hi.z; p[7] = hi.w;
+                        }
+                        acc = fma_chunk16(p, xs, j, lane, acc);
+                    }
+                } else if (ok && !slow) {
 #pragma unroll
                     for (uint32_t r = 0; r < C; r++) {
                         const uint32_t j = jp + r;
