@@ -134,18 +134,35 @@ __host__ __device__ inline uint32_t gemm_stage_bytes(bool r4, uint32_t mt) {
     return GT_N * 128 + mt * 128 + (r4 ? GT_N * 64 + GT_N * 32 : 0);
 }
 
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
+}
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+    return v;
+}
+__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
 // Decoder thread (row t, chunk q): the 16 weights [16q, 16q + 16) of W row t
-// of a stage, from the raw tiles into the row's swizzled bf16 chunks 2q and
-// 2q+1.  The four chunk threads of a row are lanes 4j..4j+3 of one warp; they
-// place their escapes by a prefix sum over the four and advance the row's
-// running escape index eidx by the row's total.
-__device__ __forceinline__ void decode_chunk16(const GemmArgs &a, const uint8_t *raw_sm, const uint8_t *raw_nib,
-                                               uint8_t *arow, uint32_t t, uint32_t q, uint64_t &eidx,
+// of a stage, from the raw tiles (shared addresses raw_sm, raw_nib of the
+// row) into the row's swizzled bf16 chunks 2q and 2q+1 (arow).  The four
+// chunk threads of a row are lanes 4j..4j+3 of one warp; they place their
+// escapes by a prefix sum over the four and advance the row's running escape
+// index eidx.  r0, r1: the ranks of the row's next two escapes (esc[eidx],
+// esc[eidx + 1]), loaded ahead.  A chunk with one escape that is among those
+// two decodes with the exponent table's rank-15 entry replaced by its
+// exponent; any other escape is patched weight by weight.
+__device__ __forceinline__ void decode_chunk16(const GemmArgs &a, const R4Lut &L, uint32_t raw_sm,
+                                               uint32_t raw_nib, uint32_t arow, uint32_t t, uint32_t q,
+                                               uint64_t &eidx, uint32_t &r0, uint32_t &r1,
                                                const uint8_t *table_s, bool &bad) {
-    const uint4 sv = *reinterpret_cast<const uint4 *>(raw_sm + q * 16);
-    const uint2 nv = *reinterpret_cast<const uint2 *>(raw_nib + q * 8);
-    uint32_t p[8];
-    r4_dec16(nv, sv, a.L, p);
+    const uint4 sv = lds128(raw_sm + q * 16);
+    const uint2 nv = lds64(raw_nib + q * 8);
     const uint32_t m0 = nib15_mask(nv.x), m1 = nib15_mask(nv.y);
     const uint32_t c = __popc(m0) + __popc(m1);
     uint32_t incl = c;
@@ -154,8 +171,18 @@ __device__ __forceinline__ void decode_chunk16(const GemmArgs &a, const uint8_t 
     y = __shfl_up_sync(DGT_FULL, incl, 2, 4);
     if (q >= 2) incl += y;
     const uint32_t total = __shfl_sync(DGT_FULL, incl, 3, 4);
-    if (c) {
-        uint64_t e = eidx + incl - c;
+    const uint32_t before = incl - c;
+    const bool one = c == 1 && before < 2;
+    R4Lut Lr = L;
+    if (one) {
+        const uint32_t rk = before == 0 ? r0 : r1;
+        Lr.h3 = prmt(L.h3, table_s[rk] >> 1, 0x4210u);
+        Lr.l1 = (L.l1 & 0x7FFFFFFFu) | ((table_s[rk] & 1u) << 31);
+    }
+    uint32_t p[8];
+    r4_dec16(nv, sv, Lr, p);
+    if (c && !one) {
+        uint64_t e = eidx + before;
 #pragma unroll
         for (int i = 0; i < 16; i++) {
             const uint32_t m = i < 8 ? m0 : m1;
@@ -168,11 +195,17 @@ __device__ __forceinline__ void decode_chunk16(const GemmArgs &a, const uint8_t 
                 p[i >> 1] = (p[i >> 1] & ~(0x7F80u << sh)) | (ex << (7 + sh));
             }
         }
+    } else if (one && eidx + before >= a.n_esc) {
+        bad = true;
     }
-    eidx += total;
+    if (total) {
+        eidx += total;
+        r0 = eidx < a.n_esc ? a.esc[eidx] : 0u;
+        r1 = eidx + 1 < a.n_esc ? a.esc[eidx + 1] : 0u;
+    }
     const uint32_t c0 = (2 * q) ^ (t & 7), c1 = (2 * q + 1) ^ (t & 7);
-    *reinterpret_cast<uint4 *>(arow + c0 * 16) = make_uint4(p[0], p[1], p[2], p[3]);
-    *reinterpret_cast<uint4 *>(arow + c1 * 16) = make_uint4(p[4], p[5], p[6], p[7]);
+    sts128(arow + c0 * 16, p[0], p[1], p[2], p[3]);
+    sts128(arow + c1 * 16, p[4], p[5], p[6], p[7]);
 }
 
 constexpr uint32_t GT_THREADS = 640;   // 4 control/epilogue warps + 16 decoder warps
@@ -299,17 +332,33 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
                 eidx += cnt;
             }
             bool bad = false;
+            R4Lut L;
+            L.h0 = a.L.h0;
+            L.h1 = a.L.h1;
+            L.h2 = a.L.h2;
+            L.h3 = a.L.h3;
+            L.l0 = a.L.l0;
+            L.l1 = a.L.l1;
+            uint32_t r0 = eidx < a.n_esc ? a.esc[eidx] : 0u;
+            uint32_t r1 = eidx + 1 < a.n_esc ? a.esc[eidx + 1] : 0u;
+            const uint32_t base_a = smem_u32(base);
+            uint32_t s = 0, par = 0;
             for (uint32_t i = 0; i < nkb; i++) {
-                const uint32_t s = i % P, par = (i / P) & 1u;
                 if (!wait_or_abort(smem_u32(&bar_raw[s]), par, abortp)) {
                     if (lane == 0) set_status(a.status, DGT_ERR_TIMEOUT);
                     *abortp = 1;
                     break;
                 }
-                decode_chunk16(a, RS(s) + t * 64, RN(s) + t * 32, A(s) + t * 128, t, q, eidx, table_s, bad);
+                const uint32_t st0 = base_a + s * SB;
+                decode_chunk16(a, L, st0 + GT_N * 128 + mt * 128 + t * 64, st0 + GT_N * 128 + mt * 128 + GT_N * 64 + t * 32,
+                               st0 + t * 128, t, q, eidx, r0, r1, table_s, bad);
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&bar_w[s]));
+                if (++s == P) {
+                    s = 0;
+                    par ^= 1u;
+                }
             }
             if (bad) set_status(a.status, DGT_ERR_CORRUPT);
         }
