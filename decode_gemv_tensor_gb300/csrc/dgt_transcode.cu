@@ -83,9 +83,9 @@ struct F2Args {
 };
 
 #ifndef DGT_RICE_REP
-#define DGT_RICE_REP 8
+#define DGT_RICE_REP 4
 #endif
-constexpr int RW = 32;          // warps per CTA
+constexpr int RW = 24;          // warps per CTA
 constexpr int RWIN = 12;        // table window bits
 constexpr int REP = DGT_RICE_REP;  // table copies (lane l uses copy l mod REP)
 constexpr int RCAP = 192;       // staged stream words per group (about 170 at 2.7 bits/rank)
@@ -293,11 +293,32 @@ __device__ __forceinline__ void cp_async4(uint32_t *dst, const uint32_t *src, ui
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 
-// Copy group g's stream words (up to RBUF; zeros after its end) into dst.
-__device__ __forceinline__ void rice_stage(const F2Args &a, uint64_t g, uint32_t *dst, uint32_t lane) {
+// A group's index entries and this lane's block-length byte, loaded one or
+// two groups ahead of use.
+struct RiceMeta {
+    uint32_t w0, base;     // first stream word, escapes before the group
+    uint32_t nextw, nexte; // the same for the following group (or the totals)
+    uint32_t q;            // this lane's block index byte
+};
+
+__device__ __forceinline__ RiceMeta rice_meta(const F2Args &a, uint64_t g, uint32_t lane) {
+    RiceMeta m = {0, 0, 0, 0, 0};
     if (g < a.ngrp) {
-        const uint64_t w0 = a.grp[2 * g];
-        const uint64_t w1 = g + 1 < a.ngrp ? (uint64_t)a.grp[2 * g + 2] : a.n_words;
+        m.w0 = a.grp[2 * g];
+        m.base = a.grp[2 * g + 1];
+        m.nextw = g + 1 < a.ngrp ? a.grp[2 * g + 2] : (uint32_t)a.n_words;
+        m.nexte = g + 1 < a.ngrp ? a.grp[2 * g + 3] : (uint32_t)a.n_esc;
+        const uint64_t blk = g * DGT_GROUP + lane;
+        m.q = blk < a.nblk ? a.blkq[blk] : 0u;
+    }
+    return m;
+}
+
+// Copy group g's stream words (up to RBUF; zeros after its end) into dst.
+__device__ __forceinline__ void rice_stage(const F2Args &a, uint64_t g, const RiceMeta &m, uint32_t *dst,
+                                           uint32_t lane) {
+    if (g < a.ngrp) {
+        const uint64_t w0 = m.w0, w1 = m.nextw;
         const uint64_t nw = (w1 > w0 && w1 <= a.n_words && w0 < a.n_words) ? w1 - w0 : 0;
         for (uint32_t i = lane; i < RBUF; i += 32) {
             const bool in = i < nw;
@@ -328,22 +349,28 @@ __global__ void __launch_bounds__(RW * 32, 1) k_rice_to_r4(F2Args a) {
     const uint64_t GS = (uint64_t)DGT_GROUP * DGT_BLOCK;
     uint64_t r0 = (g0 * GS) / a.cols, c0 = (g0 * GS) % a.cols;
     const uint64_t step_r = (G * GS) / a.cols, step_c = (G * GS) % a.cols;
-    rice_stage(a, g0, S.buf[0][w], lane);
+    // index entries: group g in m0, g + G in m1 (its stream is copied while g
+    // decodes), g + 2G loaded during g
+    RiceMeta m0 = rice_meta(a, g0, lane);
+    RiceMeta m1 = rice_meta(a, g0 + G, lane);
+    rice_stage(a, g0, m0, S.buf[0][w], lane);
     uint32_t cur = 0;
     for (uint64_t g = g0; g < a.ngrp; g += G, cur ^= 1) {
         uint32_t *buf = S.buf[cur][w];
-        rice_stage(a, g + G, S.buf[cur ^ 1][w], lane);
+        rice_stage(a, g + G, m1, S.buf[cur ^ 1][w], lane);
+        const RiceMeta m2 = rice_meta(a, g + 2 * G, lane);
         const uint64_t blk = g * DGT_GROUP + lane;
         const uint64_t B0 = blk * DGT_BLOCK;
         const uint32_t cnt = blk < a.nblk ? (uint32_t)min((uint64_t)DGT_BLOCK, a.n - B0) : 0u;
-        const uint32_t q = cnt ? a.blkq[blk] : 0u;
+        const uint32_t q = cnt ? m0.q : 0u;
         const uint32_t len = cnt == 0 ? 0u : (q != 255 ? cnt * (uint32_t)(k + 1) + q : 8u * cnt);
         uint32_t gbits;
         const uint32_t off = warp_excl_scan(len, &gbits);
         const uint32_t nw = (gbits + 31) / 32;
-        const uint64_t gw0 = a.grp[2 * g], gbase = a.grp[2 * g + 1];
-        const uint64_t next_w = g + 1 < a.ngrp ? (uint64_t)a.grp[2 * g + 2] : a.n_words;
-        const uint64_t next_e = g + 1 < a.ngrp ? (uint64_t)a.grp[2 * g + 3] : a.n_esc;
+        const uint64_t gw0 = m0.w0, gbase = m0.base;
+        const uint64_t next_w = m0.nextw, next_e = m0.nexte;
+        m0 = m1;
+        m1 = m2;
         // this lane's block: row and column of its first rank
         uint64_t br = r0, bc = c0 + (uint64_t)DGT_BLOCK * lane;
         if (bc >= a.cols) {
@@ -571,6 +598,35 @@ __device__ __forceinline__ void f1_tile(const uint8_t *tp, uint32_t *orow, const
     }
 }
 
+// A group's index entries (and the next group's) and this lane's tile width
+// and escape count, loaded one group ahead of use.  next_p16 = ~0 marks the
+// last group (the totals stand in for the next entries).
+struct F1Meta {
+    uint32_t p16, e1, e15;
+    uint32_t next_p16, next_e1, next_e15;
+    uint32_t wd, te;
+};
+
+__device__ __forceinline__ F1Meta f1_meta(const F1Args &a, uint64_t g, uint32_t lane) {
+    F1Meta m = {0, 0, 0, 0xFFFFFFFFu, 0, 0, 0, 0};
+    if (g < a.ngrp) {
+        m.p16 = a.grp1[3 * g];
+        m.e1 = a.grp1[3 * g + 1];
+        m.e15 = a.grp1[3 * g + 2];
+        if (g + 1 < a.ngrp) {
+            m.next_p16 = a.grp1[3 * g + 3];
+            m.next_e1 = a.grp1[3 * g + 4];
+            m.next_e15 = a.grp1[3 * g + 5];
+        }
+        const uint64_t t = g * DGT_GROUP + lane;
+        if (t < a.ntile) {
+            m.wd = a.tw[t];
+            m.te = a.tesc[t];
+        }
+    }
+    return m;
+}
+
 // Any width 0..8 and length: code by code from global memory.
 __device__ __noinline__ F1Lane f1_tile_any(const uint8_t *tp, uint32_t wd, uint32_t cnt, uint32_t *orow,
                                            const uint8_t *e1, uint32_t ge1, uint16_t *list, F1Lane L,
@@ -622,20 +678,24 @@ __global__ void __launch_bounds__(FW * 32) k_f1_to_r4(F1Args a) {
     const uint64_t GS = (uint64_t)DGT_GROUP * DGT_TILE;
     uint64_t r0 = (g0 * GS) / a.cols, c0 = (g0 * GS) % a.cols;
     const uint64_t step_r = (G * GS) / a.cols, step_c = (G * GS) % a.cols;
+    F1Meta mnext = f1_meta(a, g0, lane);
     for (uint64_t g = g0; g < a.ngrp; g += G) {
+        // this group's index entries (loaded one group ahead) and the next group's
+        const F1Meta m = mnext;
+        mnext = f1_meta(a, g + G, lane);
         const uint64_t t = g * DGT_GROUP + lane;
         const uint64_t B0 = t * DGT_TILE;
         const uint32_t cnt = t < a.ntile ? (uint32_t)min((uint64_t)DGT_TILE, a.n - B0) : 0u;
-        const uint32_t wd = cnt ? a.tw[t] : 0u;
-        const uint32_t te = cnt ? a.tesc[t] : 0u;
+        const uint32_t wd = cnt ? m.wd : 0u;
+        const uint32_t te = cnt ? m.te : 0u;
         uint32_t gsum;
         const uint32_t pre = warp_excl_scan((16 * min(wd, 9u)) | (te << 16), &gsum);
         const uint32_t toff = pre & 0xFFFFu, e1off = pre >> 16;
         const uint32_t gpay = gsum & 0xFFFFu, ge1 = gsum >> 16;
-        const uint64_t p0 = (uint64_t)a.grp1[3 * g] * 16, e10 = a.grp1[3 * g + 1], gbase = a.grp1[3 * g + 2];
-        const uint64_t next_p = g + 1 < a.ngrp ? (uint64_t)a.grp1[3 * g + 3] * 16 : a.payload_bytes;
-        const uint64_t next_e1 = g + 1 < a.ngrp ? (uint64_t)a.grp1[3 * g + 4] : a.n_esc1;
-        const uint64_t next_e = g + 1 < a.ngrp ? (uint64_t)a.grp1[3 * g + 5] : a.n_esc;
+        const uint64_t p0 = (uint64_t)m.p16 * 16, e10 = m.e1, gbase = m.e15;
+        const uint64_t next_p = m.next_p16 == 0xFFFFFFFFu ? a.payload_bytes : (uint64_t)m.next_p16 * 16;
+        const uint64_t next_e1 = m.next_p16 == 0xFFFFFFFFu ? a.n_esc1 : (uint64_t)m.next_e1;
+        const uint64_t next_e = m.next_p16 == 0xFFFFFFFFu ? a.n_esc : (uint64_t)m.next_e15;
         uint64_t br = r0, bc = c0 + (uint64_t)DGT_TILE * lane;
         if (bc >= a.cols) {
             if (a.cols >= GS) {
