@@ -118,8 +118,9 @@ struct RiceSmem {
 __device__ __forceinline__ uint32_t rice_pair_entry(uint32_t v, int k) {
     uint32_t pos = 0, byte = 0, escf = 0, escr = 0;
     for (int s = 0; s < 2; s++) {
-        uint32_t q = 0;
-        while (pos + q < RWIN && !((v >> (pos + q)) & 1u)) q++;
+        const uint32_t rest = v >> pos;   // the window's bits from pos (v < 2^RWIN)
+        if (rest == 0) return RARE;       // no terminating one inside the window
+        const uint32_t q = __ffs(rest) - 1;
         if (pos + q + 1 + (uint32_t)k > RWIN) return RARE;
         const uint32_t r = (q << k) | ((v >> (pos + q + 1)) & ((1u << k) - 1u));
         if (r >= 15) {
@@ -328,6 +329,33 @@ __device__ __forceinline__ void rice_stage(const F2Args &a, uint64_t g, const Ri
     cp_async_commit();
 }
 
+__device__ __forceinline__ void cp_async16(uint32_t *dst, const uint32_t *src, uint32_t bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(bytes)
+                 : "memory");
+}
+
+// Group g's stream in 16-byte pieces from the 16-byte boundary at or below
+// its first word (the stream then starts 32 * (w0 % 4) bits into dst); bytes
+// past the stream array's end, and past the buffer's need, are zero-filled.
+__device__ __forceinline__ void rice_stage16(const F2Args &a, uint64_t g, const RiceMeta &m, uint32_t *dst,
+                                             uint32_t lane) {
+    if (g < a.ngrp) {
+        const uint32_t a0 = m.w0 & ~3u;
+        const uint32_t need = m.nextw > a0 ? min(m.nextw - a0, (uint32_t)RBUF) : 0u;
+        for (uint32_t i = lane; i < RBUF / 4; i += 32) {
+            const uint32_t wi = a0 + 4 * i;
+            uint32_t bytes = 0;
+            if (4 * i < need && wi < a.n_words) bytes = min(16u, (uint32_t)(a.n_words - wi) * 4u);
+            cp_async16(dst + 4 * i, bytes ? a.words + wi : a.words, bytes);
+        }
+    }
+    cp_async_commit();
+}
+
+// FAST: 32-bit block indices (n < 2^31), blocks that never straddle rows
+// (cols % 64 == 0, cols >= 2048), rows * nseg < 2^32 and a 16-byte aligned
+// stream: the group bookkeeping takes a shorter path.
+template <bool FAST>
 __global__ void __launch_bounds__(RW * 32, 1) k_rice_to_r4(F2Args a) {
     extern __shared__ uint4 smem_raw[];
     RiceSmem &S = *reinterpret_cast<RiceSmem *>(smem_raw);
@@ -353,15 +381,25 @@ __global__ void __launch_bounds__(RW * 32, 1) k_rice_to_r4(F2Args a) {
     // decodes), g + 2G loaded during g
     RiceMeta m0 = rice_meta(a, g0, lane);
     RiceMeta m1 = rice_meta(a, g0 + G, lane);
-    rice_stage(a, g0, m0, S.buf[0][w], lane);
+    if (FAST) rice_stage16(a, g0, m0, S.buf[0][w], lane);
+    else rice_stage(a, g0, m0, S.buf[0][w], lane);
+    const uint32_t nfull = (uint32_t)(a.n / DGT_BLOCK), nblk32 = (uint32_t)a.nblk;
     uint32_t cur = 0;
     for (uint64_t g = g0; g < a.ngrp; g += G, cur ^= 1) {
         uint32_t *buf = S.buf[cur][w];
-        rice_stage(a, g + G, m1, S.buf[cur ^ 1][w], lane);
+        if (FAST) rice_stage16(a, g + G, m1, S.buf[cur ^ 1][w], lane);
+        else rice_stage(a, g + G, m1, S.buf[cur ^ 1][w], lane);
         const RiceMeta m2 = rice_meta(a, g + 2 * G, lane);
         const uint64_t blk = g * DGT_GROUP + lane;
         const uint64_t B0 = blk * DGT_BLOCK;
-        const uint32_t cnt = blk < a.nblk ? (uint32_t)min((uint64_t)DGT_BLOCK, a.n - B0) : 0u;
+        uint32_t cnt;
+        if (FAST) {
+            const uint32_t b32 = (uint32_t)g * DGT_GROUP + lane;
+            cnt = b32 < nfull ? DGT_BLOCK : (b32 < nblk32 ? (uint32_t)a.n - b32 * DGT_BLOCK : 0u);
+        } else {
+            cnt = blk < a.nblk ? (uint32_t)min((uint64_t)DGT_BLOCK, a.n - B0) : 0u;
+        }
+        const uint32_t boff = FAST ? 32u * (m0.w0 & 3u) : 0u;   // stream start inside the staged buffer
         const uint32_t q = cnt ? m0.q : 0u;
         const uint32_t len = cnt == 0 ? 0u : (q != 255 ? cnt * (uint32_t)(k + 1) + q : 8u * cnt);
         uint32_t gbits;
@@ -373,7 +411,15 @@ __global__ void __launch_bounds__(RW * 32, 1) k_rice_to_r4(F2Args a) {
         m1 = m2;
         // this lane's block: row and column of its first rank
         uint64_t br = r0, bc = c0 + (uint64_t)DGT_BLOCK * lane;
-        if (bc >= a.cols) {
+        if (FAST) {
+            uint32_t bc32 = (uint32_t)c0 + DGT_BLOCK * lane, br32 = (uint32_t)r0;
+            if (bc32 >= (uint32_t)a.cols) {
+                bc32 -= (uint32_t)a.cols;
+                br32++;
+            }
+            br = br32;
+            bc = bc32;
+        } else if (bc >= a.cols) {
             if (a.cols >= GS) {
                 bc -= a.cols;
                 br++;
@@ -396,7 +442,7 @@ __global__ void __launch_bounds__(RW * 32, 1) k_rice_to_r4(F2Args a) {
             continue;
         }
         const bool staged = nw <= RCAP;
-        const uint32_t end = off + len;
+        const uint32_t end = off + len + (staged ? boff : 0u);
         le->emask = 0;
         le->ec = 0;
         le->bad = 0;
@@ -404,7 +450,7 @@ __global__ void __launch_bounds__(RW * 32, 1) k_rice_to_r4(F2Args a) {
         le->cur = cur;
         bool bad = false;
         if (staged && cnt == DGT_BLOCK && q != 255) {
-            uint32_t pos = off, win = 0, out[8];
+            uint32_t pos = off + boff, win = 0, out[8];
 #pragma unroll
             for (int it = 0; it < 8; it++) {
                 const uint32_t e0 = rice_step<true>(lutc, buf, pos, win, 0u, 4 * it + 0);
@@ -420,7 +466,7 @@ __global__ void __launch_bounds__(RW * 32, 1) k_rice_to_r4(F2Args a) {
         } else if (cnt) {
             uint32_t p;
             if (staged)
-                p = rice_block_slow(WordReader<const uint32_t *>{buf, RBUF}, off, cnt, q == 255, k,
+                p = rice_block_slow(WordReader<const uint32_t *>{buf, RBUF}, off + boff, cnt, q == 255, k,
                                     a.nib + B0 / 2, le);
             else
                 p = rice_block_slow(WordReader<const uint32_t *>{a.words + gw0, nw}, off, cnt, q == 255, k,
@@ -439,13 +485,18 @@ __global__ void __launch_bounds__(RW * 32, 1) k_rice_to_r4(F2Args a) {
             if (ec <= RLIST) {
                 for (uint32_t i = 0; i < ec; i++) dst[i] = le->list[i];
             } else if (staged) {
-                rice_block_escapes(WordReader<const uint32_t *>{buf, RBUF}, off, cnt, q == 255, k, dst);
+                rice_block_escapes(WordReader<const uint32_t *>{buf, RBUF}, off + boff, cnt, q == 255, k, dst);
             } else {
                 rice_block_escapes(WordReader<const uint32_t *>{a.words + gw0, nw}, off, cnt, q == 255, k, dst);
             }
         }
         // row-segment escape index for every segment that starts in this block
-        if (cnt && !bad) {
+        if (FAST) {
+            // the block lies in one row and starts on a multiple of 64: a segment
+            // starts in it only at its first rank
+            if (cnt && !bad && (bc & (DGT_SEG - 1)) == 0)
+                a.seg[(uint32_t)br * (uint32_t)a.nseg + ((uint32_t)bc >> 9)] = (uint32_t)(gbase + eb);
+        } else if (cnt && !bad) {
             uint32_t done = 0;
             uint64_t rr = br, cc = bc;
             while (done < cnt) {
@@ -945,10 +996,16 @@ extern "C" int dgt_load_r4(const dgt_packed_view *dev, dgt_r4 *r4, int32_t *d_st
         a.seg_last = seg_last;
         a.status = d_status;
         const size_t smem = sizeof(RiceSmem);
+        const bool fast = n < (1ull << 31) && dev->cols % 64 == 0 && dev->cols >= 2048 &&
+                          dev->rows * nseg < (1ull << 32) && aligned16(dev->words) && dev->n_words < (1ull << 32);
+        const void *fn = fast ? (const void *)k_rice_to_r4<true> : (const void *)k_rice_to_r4<false>;
         int bps = 0;
-        if (prepare_kernel((const void *)k_rice_to_r4, smem, RW * 32, &bps) != DGT_OK) return DGT_ERR_CUDA;
+        if (prepare_kernel(fn, smem, RW * 32, &bps) != DGT_OK) return DGT_ERR_CUDA;
         uint64_t grid = min((uint64_t)di.sms * bps, (a.ngrp + RW - 1) / RW);
-        k_rice_to_r4<<<(unsigned)grid, RW * 32, smem, st>>>(a);
+        if (fast)
+            k_rice_to_r4<true><<<(unsigned)grid, RW * 32, smem, st>>>(a);
+        else
+            k_rice_to_r4<false><<<(unsigned)grid, RW * 32, smem, st>>>(a);
     } else {
         if (!dev->tw || !dev->tesc || !dev->grp1 || (dev->payload_bytes && !dev->payload) ||
             (dev->n_esc1 && !dev->esc1) || (dev->payload && !aligned16(dev->payload)))

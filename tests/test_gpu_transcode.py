@@ -37,7 +37,7 @@ def _check_r4(r4, ref, n):
 
 
 SHAPES = [(1, 1), (1, 5), (1, 64), (3, 65), (2, 2047), (1, 2049), (7, 512), (5, 1000), (17, 513),
-          (33, 1537), (64, 520), (11, 4096), (100, 48), (1024, 1024)]
+          (33, 1537), (64, 520), (11, 4096), (100, 48), (1024, 1024), (3, 2112), (9, 3008)]
 
 
 @pytest.mark.parametrize("fmt", [2, 1])
