@@ -270,13 +270,18 @@ __global__ void __launch_bounds__(PW * 32, 1) k_gemv(GemvArgs a) {
 }
 
 // ---------------------------------------------------------------------------
-// Bulk-copy streaming kernel (the default when cols % 32 == 0).  One CTA of
-// 16 warps per SM; CTA b owns rows [b*N/G, (b+1)*N/G) and warp w takes the
-// (row, slice) units w, w+16, ...  Each warp owns a ring of NS shared-memory
-// stages and keeps it full itself: after it has read a stage, lane 0 issues
-// the 1-D bulk copies (cp.async.bulk) of the piece NS ahead into it, the
-// arrival counted on the stage's mbarrier.  No warp waits on another warp's
-// progress.  A full piece is C rounds, decoded from shared memory without
+// Bulk-copy streaming kernel (the default when cols % 32 == 0).  One CTA per
+// SM of TNW = 16 consumer warps and TPW = 2 producer warps; CTA b owns rows
+// [b*N/G, (b+1)*N/G) and consumer warp w takes the (row, slice) units w,
+// w+16, ...  Each consumer owns a ring of NS shared-memory stages; one lane of
+// a producer warp keeps it full, issuing the 1-D bulk copies (cp.async.bulk)
+// of the next piece as soon as the consumer has released a stage (its "empty"
+// mbarrier, polled without blocking), the arrival counted on the stage's
+// "full" mbarrier.  No consumer waits on another consumer.  A bulk copy takes
+// warp-uniform operands, so a producer warp issues its lanes' copies one
+// after another: two producer warps halve that queue (BF16 streams about 7%
+// faster; R4, bound by its decode, is unchanged).  A full piece is C rounds,
+// decoded from shared memory without
 // per-round tests except the warp-uniform escape bit.  An R4 round whose
 // segment holds one escape decodes with the rank-15 entry of the exponent
 // table replaced by that escape's exponent (only the escaped weight has
@@ -289,22 +294,42 @@ __global__ void __launch_bounds__(PW * 32, 1) k_gemv(GemvArgs a) {
 #ifndef DGT_GEMV_INTERLEAVE
 #define DGT_GEMV_INTERLEAVE 0
 #endif
-constexpr int TNW = 16;    // warps per CTA
-constexpr uint32_t TNS_MAX = 5;
-constexpr uint32_t TCHUNK = 1024;  // (row, slice) units per combine chunk
+#ifndef DGT_GEMV_TNW
+#define DGT_GEMV_TNW 16
+#endif
+#ifndef DGT_GEMV_NS_R4
+#define DGT_GEMV_NS_R4 3
+#endif
+#ifndef DGT_GEMV_NS_BF16
+#define DGT_GEMV_NS_BF16 5
+#endif
+#ifndef DGT_GEMV_TCHUNK
+#define DGT_GEMV_TCHUNK 1024
+#endif
+#ifndef DGT_GEMV_TPW
+#define DGT_GEMV_TPW 2
+#endif
+constexpr int TNW = DGT_GEMV_TNW;    // consumer warps per CTA
+constexpr int TPW = DGT_GEMV_TPW;    // producer warps (producer warp p serves consumers p, p + TPW, ...)
+constexpr uint32_t TNS_MAX = DGT_GEMV_NS_R4 > DGT_GEMV_NS_BF16 ? DGT_GEMV_NS_R4 : DGT_GEMV_NS_BF16;
+constexpr uint32_t TCHUNK = DGT_GEMV_TCHUNK;  // (row, slice) units per combine chunk
+// the producer requests a warp's pieces in the order uu = w, w + TNW, ...
+// across chunks, and a chunk holds whole rows for every slice count (S <= 8)
+static_assert(TCHUNK % TNW == 0 && TCHUNK % 8 == 0, "chunk size");
+static_assert(TNW <= 32 * TPW, "one producer lane per consumer warp");
 
 template <bool R4>
 struct TmaCfg;
 template <>
 struct TmaCfg<true> {
     static constexpr uint32_t C = 4;               // rounds per piece
-    static constexpr uint32_t NS = 3;              // stages per warp
+    static constexpr uint32_t NS = DGT_GEMV_NS_R4; // stages per warp
     static constexpr uint32_t STAGE = 4 * 768;     // sm bytes then nibbles
 };
 template <>
 struct TmaCfg<false> {
     static constexpr uint32_t C = 2;
-    static constexpr uint32_t NS = 5;
+    static constexpr uint32_t NS = DGT_GEMV_NS_BF16;
     static constexpr uint32_t STAGE = 2 * 1024;
 };
 
@@ -359,7 +384,7 @@ __device__ __forceinline__ void cursor_set(PieceCursor &c, uint64_t uu, uint64_t
 }
 
 template <bool R4>
-__global__ void __launch_bounds__((TNW + 1) * 32, 1) k_gemv_tma(GemvArgs a) {
+__global__ void __launch_bounds__((TNW + TPW) * 32, 1) k_gemv_tma(GemvArgs a) {
     constexpr uint32_t C = TmaCfg<R4>::C, TNS = TmaCfg<R4>::NS, STAGE = TmaCfg<R4>::STAGE;
     extern __shared__ __align__(128) uint8_t dsm[];
     __shared__ __align__(8) uint64_t full[TNW][TNS_MAX];
@@ -385,23 +410,24 @@ __global__ void __launch_bounds__((TNW + 1) * 32, 1) k_gemv_tma(GemvArgs a) {
     const uint32_t J = a.J;
     const uint32_t K = (uint32_t)a.cols;
 
-    if (tid < TNW * TNS_MAX) {
-        mbar_init(smem_u32(&full[0][0]) + 8 * tid, 1);
-        mbar_init(smem_u32(&empty[0][0]) + 8 * tid, 1);
+    for (uint32_t i = tid; i < TNW * TNS_MAX; i += blockDim.x) {
+        mbar_init(smem_u32(&full[0][0]) + 8 * i, 1);
+        mbar_init(smem_u32(&empty[0][0]) + 8 * i, 1);
     }
     if (tid == 0) abort_flag = 0;
     fence_mbarrier_init();
     __syncthreads();
 
-    if (w == TNW) {
-        // ---- producer warp: lane c keeps consumer warp c's ring full.  It
-        // polls the ring's "empty" barriers without blocking, so no consumer
-        // waits for another.
-        if (lane < TNW) {
-            const uint32_t ring_a = smem_u32(dsm + (size_t)lane * TNS * STAGE);
-            const uint32_t full_a = smem_u32(&full[lane][0]), empty_a = smem_u32(&empty[lane][0]);
+    if (w >= TNW) {
+        // ---- producer warps: lane l of producer warp p keeps consumer warp
+        // c = p + TPW l's ring full.  It polls the ring's "empty" barriers
+        // without blocking, so no consumer waits for another.
+        const uint32_t c = (w - TNW) + TPW * lane;
+        if (c < TNW) {
+            const uint32_t ring_a = smem_u32(dsm + (size_t)c * TNS * STAGE);
+            const uint32_t full_a = smem_u32(&full[c][0]), empty_a = smem_u32(&empty[c][0]);
             PieceCursor cur;
-            cursor_set(cur, lane, units, r0, rs, log2S, J, a.cols);
+            cursor_set(cur, c, units, r0, rs, log2S, J, a.cols);
             uint32_t q = 0, idle = 0;
             while (cur.uu < units && !*(volatile int *)&abort_flag) {
                 const uint32_t st = q % TNS;
@@ -695,9 +721,9 @@ int launch_gemv(GemvArgs &a, int path, cudaStream_t st) {
     int bps = 0;
     if (path == 2) {
         const size_t smem = (size_t)TNW * TmaCfg<R4>::NS * TmaCfg<R4>::STAGE + (size_t)a.J * 1024;
-        if (prepare_kernel((const void *)k_gemv_tma<R4>, smem, (TNW + 1) * 32, &bps) != DGT_OK) return DGT_ERR_CUDA;
+        if (prepare_kernel((const void *)k_gemv_tma<R4>, smem, (TNW + TPW) * 32, &bps) != DGT_OK) return DGT_ERR_CUDA;
         const unsigned grid = (unsigned)min((uint64_t)di.sms, a.rows);
-        k_gemv_tma<R4><<<grid, (TNW + 1) * 32, smem, st>>>(a);
+        k_gemv_tma<R4><<<grid, (TNW + TPW) * 32, smem, st>>>(a);
     } else if (path == 1) {
         const size_t smem = (size_t)a.J * 1024;
         if (prepare_kernel((const void *)k_gemv<R4, 16, 4>, smem, 16 * 32, &bps) != DGT_OK) return DGT_ERR_CUDA;

@@ -232,7 +232,14 @@ __global__ void __launch_bounds__(1024) k_moe_route(MoeArgs a) {
 // row again), x read through L1.  At every slice end the chains are
 // butterfly-reduced into the workspace.
 // ---------------------------------------------------------------------------
-constexpr int MNW = 15;          // consumer warps (+ the producer: 4 warps per scheduler)
+#ifndef DGT_MOE_MNW
+#define DGT_MOE_MNW 15
+#endif
+#ifndef DGT_MOE_MPW
+#define DGT_MOE_MPW 1
+#endif
+constexpr int MNW = DGT_MOE_MNW;  // consumer warps
+constexpr int MPW = DGT_MOE_MPW;  // producer warps (producer warp p serves consumers p, p + MPW, ...)
 constexpr uint32_t MC = 4;       // rounds per piece
 constexpr uint32_t MNS_MAX = 3;  // stages per consumer (R4: 3, BF16: 2)
 constexpr uint32_t XS_BYTES = 64 * 1024;   // x of the CTA's tokens staged in shared memory
@@ -501,7 +508,7 @@ __device__ __forceinline__ void moe_row_pass(const MoeArgs &a, MoeRing &rg, cons
 }
 
 template <bool R4>
-__global__ void __launch_bounds__((MNW + 1) * 32, 1) k_moe(MoeArgs a) {
+__global__ void __launch_bounds__((MNW + MPW) * 32, 1) k_moe(MoeArgs a) {
     constexpr uint32_t STAGE = MoeStage<R4>::BYTES, MNS = MoeStage<R4>::NS;
     extern __shared__ __align__(128) uint8_t dsm[];
     __shared__ __align__(8) uint64_t full[MNW][MNS_MAX];
@@ -586,23 +593,25 @@ __global__ void __launch_bounds__((MNW + 1) * 32, 1) k_moe(MoeArgs a) {
     }
     const uint16_t *xslot_p = xstage ? xslot : nullptr;
 
-    if (tid < MNW * MNS_MAX) {
-        mbar_init(smem_u32(&full[0][0]) + 8 * tid, 1);
-        mbar_init(smem_u32(&empty[0][0]) + 8 * tid, 1);
+    for (uint32_t i = tid; i < MNW * MNS_MAX; i += blockDim.x) {
+        mbar_init(smem_u32(&full[0][0]) + 8 * i, 1);
+        mbar_init(smem_u32(&empty[0][0]) + 8 * i, 1);
     }
     if (tid == 0) abort_flag = 0;
     if (R4 && tid < 256) table_s[tid] = a.table[tid];
     fence_mbarrier_init();
     __syncthreads();
 
-    if (w == MNW) {
-        // ---- producer warp: lane c keeps consumer c's ring full
-        if (lane < MNW && a.bulk) {
-            const uint32_t ring_a = smem_u32(dsm + (size_t)lane * MNS * STAGE);
-            const uint32_t full_a = smem_u32(&full[lane][0]), empty_a = smem_u32(&empty[lane][0]);
+    if (w >= MNW) {
+        // ---- producer warps: lane l of producer warp p keeps consumer
+        // c = p + MPW l's ring full
+        const uint32_t c = (w - MNW) + MPW * lane;
+        if (c < MNW && a.bulk) {
+            const uint32_t ring_a = smem_u32(dsm + (size_t)c * MNS * STAGE);
+            const uint32_t full_a = smem_u32(&full[c][0]), empty_a = smem_u32(&empty[c][0]);
             MoeCursor cur;
-            cur.i = lane;
-            cur.pos = row_pos(a, rb + lane);
+            cur.i = c;
+            cur.pos = row_pos(a, rb + c);
             moe_cursor_load(a, T, cur, nrows);
             uint32_t q = 0, idle = 0;
             while (cur.i < nrows && !*(volatile int *)&abort_flag) {
@@ -743,8 +752,8 @@ int launch_moe(MoeArgs &a, void *d_ws, size_t ws_bytes, cudaStream_t st) {
     a.xs_slots = a.tokens <= XS_TOKENS ? (uint32_t)min((uint64_t)a.tokens, (uint64_t)(XS_BYTES / (2 * a.cols))) : 0u;
     const size_t smem = (size_t)MNW * MoeStage<R4>::NS * MoeStage<R4>::BYTES + (size_t)a.xs_slots * a.cols * 2;
     int bps = 0;
-    if (prepare_kernel((const void *)k_moe<R4>, smem, (MNW + 1) * 32, &bps) != DGT_OK) return DGT_ERR_CUDA;
-    k_moe<R4><<<a.grid, (MNW + 1) * 32, smem, st>>>(a);
+    if (prepare_kernel((const void *)k_moe<R4>, smem, (MNW + MPW) * 32, &bps) != DGT_OK) return DGT_ERR_CUDA;
+    k_moe<R4><<<a.grid, (MNW + MPW) * 32, smem, st>>>(a);
     const uint64_t n_out = (uint64_t)a.tokens * a.ne;
     uint64_t cgrid = (n_out + 255) / 256;
     if (cgrid > (uint64_t)di.sms * 8) cgrid = (uint64_t)di.sms * 8;
