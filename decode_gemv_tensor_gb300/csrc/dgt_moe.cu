@@ -654,28 +654,34 @@ __global__ void __launch_bounds__((MNW + MPW) * 32, 1) k_moe(MoeArgs a) {
     const uint32_t S = a.S, log2S = __ffs(S) - 1;
     uint32_t st = 0, phases = 0, waited = 0;
     bool ok = true;
-    SegPre pre = {0, 0, 0, 0};
-    if (R4 && (uint64_t)w < nrows) {
-        const MoeRow m = moe_row(a, T, row_pos(a, rb + w));
-        seg_issue(a, m.grow, 0, J, lane, pre);
-        seg_issue_esc(a, pre);
-    }
+    // escape metadata runs two rows ahead: the segment counts of the row
+    // after next, and the first escape ranks of the next row, are requested
+    // while this row streams, so no load is waited for at a row start
+    SegPre pre = {0, 0, 0, 0}, nxt = {0, 0, 0, 0};
     RowPos pos = row_pos(a, rb + w);
+    if (R4 && (uint64_t)w < nrows) {
+        seg_issue(a, moe_row(a, T, pos).grow, 0, J, lane, pre);
+        seg_issue_esc(a, pre);
+        if ((uint64_t)w + MNW < nrows) {
+            RowPos pn = pos;
+            row_step(a, pn, MNW);
+            seg_issue(a, moe_row(a, T, pn).grow, 0, J, lane, nxt);
+        }
+    }
     for (uint64_t i = w; i < nrows; i += MNW, row_step(a, pos, MNW)) {
         const MoeRow m = moe_row(a, T, pos);
         SegInfo g = {0, 0, 0, 0, 0};
         RoundLut rl = {0, 0, 0};
-        SegPre nxt = {0, 0, 0, 0};
-        bool nxt_esc = false;
-        const bool has_next = i + MNW < nrows;
         if (R4) {
             g = seg_finish(pre, table_s);
             rl = round_luts(g, L);
-            if (has_next) {
+            pre = nxt;
+            if (i + MNW < nrows) seg_issue_esc(a, pre);
+            nxt = SegPre{0, 0, 0, 0};
+            if (i + 2 * MNW < nrows) {
                 RowPos pn = pos;
-                row_step(a, pn, MNW);
-                const MoeRow mn = moe_row(a, T, pn);
-                seg_issue(a, mn.grow, 0, J, lane, nxt);
+                row_step(a, pn, 2 * MNW);
+                seg_issue(a, moe_row(a, T, pn).grow, 0, J, lane, nxt);
             }
         }
         for (uint32_t tg = 0; tg < m.nt; tg += MAXT) {
@@ -695,14 +701,6 @@ __global__ void __launch_bounds__((MNW + MPW) * 32, 1) k_moe(MoeArgs a) {
             phases = rg.phases;
             waited = rg.waited;
             ok = rg.ok;
-            if (R4 && has_next && !nxt_esc) {
-                seg_issue_esc(a, nxt);
-                nxt_esc = true;
-            }
-        }
-        if (R4) {
-            if (has_next && !nxt_esc) seg_issue_esc(a, nxt);
-            pre = nxt;
         }
     }
     // after a timeout: copies that may still be in flight land before exit
