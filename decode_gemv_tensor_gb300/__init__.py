@@ -99,6 +99,9 @@ def lib():
                                         vp, vp, C.c_size_t, vp, vp]),
             "dgt_moe_gemv_noalloc": (i32, [C.POINTER(R4Struct), C.c_uint32, vp, vp, C.c_uint32, C.c_uint32, vp,
                                            vp, vp, vp, vp, vp]),
+            "dgt_add_rmsnorm": (i32, [vp, vp, vp, u64, C.c_float, vp, vp]),
+            "dgt_silu_mul": (i32, [vp, vp, u64, vp, vp]),
+            "dgt_repeat": (i32, [vp, u64, u64, vp, vp]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -438,3 +441,134 @@ def gemm_bf16(W, X, plan=None, Y32=None, Y=None, ws=None, status=None, stream=No
     _check(lib().dgt_gemm_bf16(_ptr(W), N, K, _ptr(X), M, _ptr(Y32), _ptr(Y), C.byref(plan), _ptr(ws),
                                0 if ws is None else ws.numel(), _ptr(status), _stream(stream)), "dgt_gemm_bf16")
     return Y32, Y
+
+
+# ---------------------------------------------------------------------------
+# decoder-layer decode step (batch 1)
+# ---------------------------------------------------------------------------
+def add_rmsnorm(x32, gamma, eps, h=None, y32=None, stream=None):
+    """dgt_add_rmsnorm: x32 += y32 (if given, in place), then h = bf16 RMS norm
+    of x32 scaled by gamma (bf16).  Returns h."""
+    import torch
+    n = x32.numel()
+    if h is None:
+        h = torch.empty(n, dtype=torch.bfloat16, device=x32.device)
+    _check(lib().dgt_add_rmsnorm(_ptr(x32), _ptr(y32), _ptr(gamma), n, C.c_float(eps), _ptr(h), _stream(stream)),
+           "dgt_add_rmsnorm")
+    return h
+
+
+def silu_mul(g32, u32, out=None, stream=None):
+    """dgt_silu_mul: bf16(silu(g) * u) from two float32 vectors."""
+    import torch
+    n = g32.numel()
+    if out is None:
+        out = torch.empty(n, dtype=torch.bfloat16, device=g32.device)
+    _check(lib().dgt_silu_mul(_ptr(g32), _ptr(u32), n, _ptr(out), _stream(stream)), "dgt_silu_mul")
+    return out
+
+
+def repeat(v, n_out, out=None, stream=None):
+    """dgt_repeat: out[i] = v[i mod len(v)] (bf16)."""
+    import torch
+    if out is None:
+        out = torch.empty(n_out, dtype=torch.bfloat16, device=v.device)
+    _check(lib().dgt_repeat(_ptr(v), v.numel(), n_out, _ptr(out), _stream(stream)), "dgt_repeat")
+    return out
+
+
+DENSE_PROJ = ("q", "k", "v", "o", "gate", "up", "down")
+
+
+class DecodeStep:
+    """One batch-1 decode step through a stack of dense decoder layers, every
+    op a kernel of this library.  Per layer, with the fp32 residual stream x:
+
+        h = rmsnorm(x, g1);  q = Wq h;  k = Wk h;  v = Wv h
+        a = repeat(v, rows of Wq);  x += Wo a
+        h = rmsnorm(x, g2);  m = silu(Wgate h) * (Wup h);  x += Wdown m
+
+    and a final h = rmsnorm(x, g_final).  Attention itself is not part of the
+    step: the output projection reads the value vector repeated over the query
+    heads.  layers: list of dicts proj -> R4 (or bf16 tensors [rows, cols] for
+    the twin); gammas: list of 2 * len(layers) + 1 bf16 vectors.  Layer l of
+    the step uses layers[l % len(layers)] and gammas for its index, so a few
+    distinct layers can stand in for a deeper model.  The R4 step and the BF16
+    step over the same weights give bit-identical outputs."""
+
+    def __init__(self, layers, gammas, depth=None, eps=1e-5, device=None):
+        import torch
+        self.layers, self.gammas, self.eps = layers, gammas, eps
+        self.depth = depth or len(layers)
+        w0 = layers[0]
+        self.r4 = isinstance(w0["q"], R4)
+        shape = (lambda w: (w.rows, w.cols)) if self.r4 else (lambda w: tuple(w.shape))
+        hidden = shape(w0["q"])[1]
+        dims = {p: shape(w0[p])[0] for p in DENSE_PROJ}
+        dev = device or (w0["q"].sm.device if self.r4 else w0["q"].device)
+        self.hidden = hidden
+        f32 = lambda n: torch.empty(n, dtype=torch.float32, device=dev)
+        b16 = lambda n: torch.empty(n, dtype=torch.bfloat16, device=dev)
+        self.x = f32(hidden)
+        self.h = b16(hidden)
+        self.y = {p: (b16(dims[p]), f32(dims[p])) for p in DENSE_PROJ}
+        self.a = b16(dims["q"])
+        self.m = b16(dims["gate"])
+        self.out = b16(hidden)
+        self._graph = None
+
+    def _gemv(self, W, x, p, stream):
+        y, y32 = self.y[p]
+        if self.r4:
+            gemv(W, x, y, y32, stream=stream)
+        else:
+            gemv_bf16(W, x, y, y32, stream=stream)
+        return y, y32
+
+    def launch(self, stream=None):
+        """Queue the step on `stream` (self.x holds the input, then the output
+        residual stream; self.out the final normed vector)."""
+        gi = 0
+        for l in range(self.depth):
+            W = self.layers[l % len(self.layers)]
+            add_rmsnorm(self.x, self.gammas[gi % (len(self.gammas) - 1)], self.eps, self.h,
+                        None if l == 0 else self.y["down"][1], stream)
+            gi += 1
+            for p in ("q", "k", "v"):
+                self._gemv(W[p], self.h, p, stream)
+            repeat(self.y["v"][0], self.a.numel(), self.a, stream)
+            self._gemv(W["o"], self.a, "o", stream)
+            add_rmsnorm(self.x, self.gammas[gi % (len(self.gammas) - 1)], self.eps, self.h, self.y["o"][1], stream)
+            gi += 1
+            self._gemv(W["gate"], self.h, "gate", stream)
+            self._gemv(W["up"], self.h, "up", stream)
+            silu_mul(self.y["gate"][1], self.y["up"][1], self.m, stream)
+            self._gemv(W["down"], self.m, "down", stream)
+        add_rmsnorm(self.x, self.gammas[-1], self.eps, self.out, self.y["down"][1], stream)
+
+    def __call__(self, x0, stream=None):
+        """Eager step from the fp32 input x0: returns (x, out)."""
+        self.x.copy_(x0)
+        self.launch(stream)
+        return self.x, self.out
+
+    def capture(self):
+        """Capture launch() in a CUDA graph (run the step once eagerly first);
+        replay() then runs the step on the current contents of self.x."""
+        import torch
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(g, stream=s):
+                self.launch(s)
+        torch.cuda.current_stream().wait_stream(s)
+        self._graph = g
+        return g
+
+    def replay(self, x0=None):
+        if x0 is not None:
+            self.x.copy_(x0)
+        self._graph.replay()
+        return self.x, self.out
+

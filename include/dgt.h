@@ -352,6 +352,39 @@ int dgt_moe_gemv_noalloc(const dgt_r4 *W, uint32_t n_experts, const int32_t *d_i
                          uint32_t tokens, uint32_t topk, const uint16_t *d_x, float *d_y32, uint16_t *d_out,
                          float *d_out32, int32_t *d_status, void *stream);
 
+/* ------------------------------------------------------------------------ */
+/* Decoder-layer glue (batch-1 decode step)                                 */
+/* ------------------------------------------------------------------------ */
+/*
+ * The steps between the products of one decoder layer at batch 1 (Binade
+ * README, "Results": decode speed, a model's per-token time with R4 weights
+ * against BF16; "How it works": the format changes only the products).  Each
+ * has one fixed order, so a step run with R4 weights and the same step with
+ * the BF16 weights produce bit-identical outputs.  All asynchronous on
+ * `stream`; device pointers; caller-owned buffers.
+ *
+ * dgt_add_rmsnorm: residual add and RMS norm in one kernel (one CTA of 1024
+ * threads).  If d_y is not NULL, x[i] = x[i] + y[i] (fp32, in place).  Then
+ * ss = sum of x[i]^2, where thread t accumulates i = t, t + 1024, ... in
+ * increasing order with fmaf from +0, each warp adds its 32 lanes by the
+ * butterfly 16, 8, 4, 2, 1, and warp 0 does the same over the 32 warp sums;
+ * r = 1 / sqrt(ss / n + eps) (correctly rounded fp32 operations);
+ * h[i] = bf16_rne((x[i] * r) * gamma[i]).  d_x: float[n] (in/out); d_y:
+ * float[n] or NULL; d_gamma, d_h: bf16 bits [n].  n in 1..65536 (else
+ * DGT_ERR_SHAPE); eps >= 0 (else DGT_ERR_ARG).
+ *
+ * dgt_silu_mul: out[i] = bf16_rne((g[i] / (1 + exp(-g[i]))) * u[i]) in fp32
+ * (exp: CUDA's expf).  d_g, d_u: float[n]; d_out: bf16 bits [n].
+ *
+ * dgt_repeat: out[i] = v[i mod n_in] for i < n_out (bf16 bits): the grouped
+ * query heads' copy of a key/value-sized vector.  n_in == 0 with n_out > 0 is
+ * DGT_ERR_SHAPE.
+ */
+int dgt_add_rmsnorm(float *d_x, const float *d_y, const uint16_t *d_gamma, uint64_t n, float eps, uint16_t *d_h,
+                    void *stream);
+int dgt_silu_mul(const float *d_g, const float *d_u, uint64_t n, uint16_t *d_out, void *stream);
+int dgt_repeat(const uint16_t *d_v, uint64_t n_in, uint64_t n_out, uint16_t *d_out, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -77,6 +77,9 @@ def _L():
             "or_moe_gemv": (C.c_int, [u16p, u64, u64, u64, i32p, f32p, u64, u64, u16p,
                                       f32p, f32p, u16p]),
             "or_gemm_f64": (None, [u16p, u16p, u64, u64, u64, u64p, u64, f64p]),
+            "or_f64_to_bf16": (C.c_uint16, [C.c_double]),
+            "or_rmsnorm_f64": (None, [f64p, u16p, u64, C.c_double, f64p]),
+            "or_silu_mul_f64": (None, [f64p, f64p, u64, f64p]),
         }
         for name, (res, args) in sig.items():
             f = getattr(lib, name)
@@ -376,3 +379,66 @@ def gemm_f64(X, W, cols=None):
     _L().or_gemm_f64(_p(X, C.c_uint16), _p(W, C.c_uint16), M, N, K, _p(sel, C.c_uint64), nsel,
                      _p(Y, C.c_double))
     return Y[:M * nsel].reshape(M, nsel)
+
+
+# --------------------------------------------------------------------------
+# decoder-layer glue and the batch-1 decode step (fp64)
+# --------------------------------------------------------------------------
+def f64_to_bf16(v) -> np.ndarray:
+    """Nearest bf16 (ties to even) of each double, as bits."""
+    v = np.atleast_1d(np.asarray(v, np.float64))
+    return np.array([_L().or_f64_to_bf16(float(t)) for t in v.ravel()], np.uint16).reshape(v.shape)
+
+
+def bf16_to_f64(b) -> np.ndarray:
+    b = np.asarray(b, np.uint16)
+    return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def rmsnorm_f64(x, gamma):
+    """x * r * gamma with r = 1 / sqrt(mean(x^2) + eps), eps = 1e-5 unless given."""
+    return rmsnorm_eps_f64(x, gamma, 1e-5)
+
+
+def rmsnorm_eps_f64(x, gamma, eps: float):
+    x = _c(x, np.float64).ravel()
+    g = _c(gamma, np.uint16).ravel()
+    out = np.zeros(max(x.size, 1), np.float64)
+    _L().or_rmsnorm_f64(_p(x, C.c_double), _p(g, C.c_uint16), x.size, eps, _p(out, C.c_double))
+    return out[:x.size]
+
+
+def silu_mul_f64(g, u):
+    g = _c(g, np.float64).ravel()
+    u = _c(u, np.float64).ravel()
+    out = np.zeros(max(g.size, 1), np.float64)
+    _L().or_silu_mul_f64(_p(g, C.c_double), _p(u, C.c_double), g.size, _p(out, C.c_double))
+    return out[:g.size]
+
+
+def decode_step_f64(layers, gammas, x0, depth=None, eps: float = 1e-5):
+    """The batch-1 decode step of dense decoder layers in fp64 (products by
+    matmul), rounding to bf16 where the products take bf16 inputs:
+
+        h = bf16(rmsnorm(x, g1)); v = Wv h; a = bf16(v) repeated to Wq's rows;
+        x = x + Wo a; h = bf16(rmsnorm(x, g2));
+        m = bf16(silu(Wgate h) * (Wup h)); x = x + Wdown m
+
+    then out = bf16(rmsnorm(x, g_final)).  Layer l uses layers[l % len] and
+    gammas[2l mod 2len], [2l+1 mod 2len].  Returns (x, out bits)."""
+    depth = depth or len(layers)
+    x = np.asarray(x0, np.float64).copy()
+    nl = len(layers)
+    W = [{p: bf16_to_f64(np.asarray(L[p], np.uint16)) for p in L} for L in layers]
+    for l in range(depth):
+        Wl = W[l % nl]
+        h = bf16_to_f64(f64_to_bf16(rmsnorm_eps_f64(x, gammas[(2 * l) % (2 * nl)], eps)))
+        v = Wl["v"] @ h
+        q_rows = Wl["q"].shape[0]
+        a = bf16_to_f64(f64_to_bf16(v))[np.arange(q_rows) % v.size]
+        x = x + Wl["o"] @ a
+        h = bf16_to_f64(f64_to_bf16(rmsnorm_eps_f64(x, gammas[(2 * l + 1) % (2 * nl)], eps)))
+        m = bf16_to_f64(f64_to_bf16(silu_mul_f64(Wl["gate"] @ h, Wl["up"] @ h)))
+        x = x + Wl["down"] @ m
+    return x, f64_to_bf16(rmsnorm_eps_f64(x, gammas[-1], eps))
+

@@ -556,3 +556,37 @@ void or_gemm_f64(const uint16_t *X, const uint16_t *W, uint64_t M, uint64_t N,
     }
     (void)N;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Decoder-layer glue at batch 1, [B] "Results" (decode speed: a model's    */
+/* per-token time) -- the steps between the products, in fp64.              */
+/* ------------------------------------------------------------------------ */
+
+/* Round a double to the nearest bf16 (ties to even), returning its bits:
+   scale the significand to 8 bits, round half-even, scale back. */
+uint16_t or_f64_to_bf16(double v) {
+    if (v != v) return 0x7FC0;
+    if (v == 0.0) return signbit(v) ? 0x8000 : 0;
+    int e;
+    double m = frexp(fabs(v), &e);            /* |v| = m 2^e, m in [0.5, 1) */
+    double q = nearbyint(ldexp(m, 8));        /* 8 significant bits, half-even */
+    float f = (float)ldexp(q, e - 8);         /* exact: 8 bits, bf16 range */
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    uint16_t b = (uint16_t)(u >> 16);
+    return v < 0 ? (uint16_t)(b | 0x8000) : b;
+}
+
+/* RMS norm: r = 1 / sqrt(mean(x^2) + eps); out[i] = x[i] r gamma[i]. */
+void or_rmsnorm_f64(const double *x, const uint16_t *gamma, uint64_t n, double eps, double *out) {
+    double ss = 0.0;
+    for (uint64_t i = 0; i < n; i++) ss += x[i] * x[i];
+    double r = 1.0 / sqrt(ss / (double)n + eps);
+    for (uint64_t i = 0; i < n; i++) out[i] = x[i] * r * (double)or_bf16_to_f32(gamma[i]);
+}
+
+/* SiLU(g) * u = g / (1 + exp(-g)) * u. */
+void or_silu_mul_f64(const double *g, const double *u, uint64_t n, double *out) {
+    for (uint64_t i = 0; i < n; i++) out[i] = g[i] / (1.0 + exp(-g[i])) * u[i];
+}
+

@@ -177,3 +177,93 @@ def test_gemm_f64_integer_exact():
     Wi = g.integers(-20, 21, size=(9, 129))
     Y = oracle.gemm_f64(_bf16(Xi), _bf16(Wi))
     assert np.array_equal(Y, (Xi @ Wi.T).astype(np.float64))
+
+
+# ---------------------------------------------------------------------------
+# decoder-layer glue (fp64) and the batch-1 decode step
+# ---------------------------------------------------------------------------
+def test_f64_to_bf16_exact_values_and_ties():
+    # every finite bf16 value maps to itself
+    b = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    fin = (b & 0x7F80) != 0x7F80
+    v = oracle.bf16_to_f64(b[fin])
+    got = oracle.f64_to_bf16(v)
+    same = (got == b[fin]) | ((b[fin] & 0x7FFF) == 0)     # -0 / +0 keep their sign bit
+    assert same.all()
+    # halfway between neighbours goes to the even one; just above goes up
+    g = np.random.default_rng(3)
+    lo = g.integers(0x0080, 0x7F00, size=400).astype(np.uint16)
+    a, c = oracle.bf16_to_f64(lo), oracle.bf16_to_f64(lo + 1)
+    half = oracle.f64_to_bf16((a + c) / 2)
+    assert np.array_equal(half, np.where(lo % 2 == 0, lo, lo + 1))
+    up = oracle.f64_to_bf16((a + c) / 2 + (c - a) * 1e-6)
+    assert np.array_equal(up, lo + 1)
+    assert np.array_equal(oracle.f64_to_bf16(-(a + c) / 2), np.where(lo % 2 == 0, lo, lo + 1) | 0x8000)
+
+
+def test_rmsnorm_closed_forms():
+    one = np.full(7, 0x3F80, np.uint16)
+    # constant vector: c / sqrt(c^2 + eps)
+    for c in (3.0, -0.5, 1e-3):
+        out = oracle.rmsnorm_eps_f64(np.full(7, c), one, 1e-5)
+        assert np.allclose(out, c / np.sqrt(c * c + 1e-5), rtol=1e-14)
+    # one-hot of length n, eps = 0: sqrt(n) at the hot place, 0 elsewhere
+    x = np.zeros(16)
+    x[5] = -2.5
+    out = oracle.rmsnorm_eps_f64(x, one[:1].repeat(16), 0.0)
+    assert np.isclose(out[5], -4.0, rtol=1e-15) and np.count_nonzero(out) == 1
+    # scale invariance at eps = 0, and gamma multiplies elementwise
+    g = np.random.default_rng(4)
+    x = g.normal(size=33)
+    gam = _bf16(g.normal(size=33))
+    a = oracle.rmsnorm_eps_f64(x, gam, 0.0)
+    assert np.allclose(oracle.rmsnorm_eps_f64(8 * x, gam, 0.0), a, rtol=1e-13)
+    assert np.allclose(a, oracle.rmsnorm_eps_f64(x, one[:1].repeat(33), 0.0) * S.bf16_bits_to_f32(gam), rtol=1e-13)
+
+
+def test_silu_mul_closed_forms():
+    g = np.array([0.0, np.log(3.0), 60.0, -60.0, 1.0])
+    u = np.array([5.0, 2.0, 1.0, 1.0, -3.0])
+    out = oracle.silu_mul_f64(g, u)
+    assert out[0] == 0.0
+    assert np.isclose(out[1], 2.0 * 0.75 * np.log(3.0), rtol=1e-15)
+    assert np.isclose(out[2], 60.0, rtol=1e-15) and abs(out[3]) < 1e-20
+    assert np.isclose(out[4], -3.0 / (1.0 + np.exp(-1.0)), rtol=1e-15)
+
+
+def _tiny_layer(hid, kv, ffn, seed, zero_out=False):
+    g = np.random.default_rng(seed)
+    L = {p: _bf16(g.normal(scale=0.2, size=shp)) for p, shp in
+         (("q", (hid, hid)), ("k", (kv, hid)), ("v", (kv, hid)), ("o", (hid, hid)), ("gate", (ffn, hid)),
+          ("up", (ffn, hid)), ("down", (hid, ffn)))}
+    if zero_out:
+        L["o"][:] = 0
+        L["down"][:] = 0
+    return L
+
+
+def test_decode_step_f64_zero_outputs_keep_residual():
+    # Wo = Wdown = 0: the residual stream is untouched and out = bf16(rmsnorm(x0, g_final))
+    layers = [_tiny_layer(8, 4, 12, 1, zero_out=True), _tiny_layer(8, 4, 12, 2, zero_out=True)]
+    g = np.random.default_rng(9)
+    gam = [_bf16(1 + 0.1 * g.normal(size=8)) for _ in range(5)]
+    x0 = g.normal(size=8)
+    x, out = oracle.decode_step_f64(layers, gam, x0, depth=3)
+    assert np.array_equal(x, x0)
+    assert np.array_equal(out, oracle.f64_to_bf16(oracle.rmsnorm_eps_f64(x0, gam[-1], 1e-5)))
+
+
+def test_decode_step_f64_identity_attention_path():
+    # Wv = Wq-shaped identity pieces and Wo = I, with the MLP switched off:
+    # one layer adds bf16(rmsnorm(x0, g1)) repeated from the kv head to x0
+    hid, kv = 8, 4
+    L = _tiny_layer(hid, kv, 6, 3)
+    L["v"] = _bf16(np.eye(kv, hid))
+    L["o"] = _bf16(np.eye(hid))
+    L["down"][:] = 0
+    g = np.random.default_rng(10)
+    gam = [_bf16(1 + 0.1 * g.normal(size=hid)) for _ in range(3)]
+    x0 = g.normal(size=hid)
+    x, _ = oracle.decode_step_f64([L], gam, x0)
+    h = oracle.bf16_to_f64(oracle.f64_to_bf16(oracle.rmsnorm_eps_f64(x0, gam[0], 1e-5)))
+    assert np.allclose(x, x0 + h[np.arange(hid) % kv], rtol=0, atol=1e-15)
