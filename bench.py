@@ -11,7 +11,9 @@ every device row of the path:
   the R4 and BF16 tcgen05 GEMMs at 16 prompt rows;
   the MoE expert gather (R4 and BF16 twin) at 1 and 16 tokens, top-8.
 The GEMM at 128 and 2048 rows is tensor-bound and is reported separately
-("gemm_tensor", TFLOP/s against the measured bf16 peak).
+("gemm_tensor", TFLOP/s against the measured bf16 peak), and so is a whole
+batch-1 decode step through the dense-3B layer stack in a CUDA graph
+("decode_step": per-token time with R4 weights against BF16).
 Between a kernel's reuses of one tensor's data the other tensors and kernels
 move far more than the 129 MB L2, so no explicit flush is needed.
 
@@ -409,6 +411,7 @@ def run_ours(args, rank, world, dist):
 
     # ---- prompt GEMM at 128 and 2048 rows (tensor-bound), outside the timed step
     extras = gemm_extras(dgt, torch, dev) if rank == 0 else None
+    dstep = decode_step_extras(dgt, torch, dev) if rank == 0 and not args.no_decode_step else None
 
     # ---- end to end through the C ABI from pinned host buffers
     e2e = None
@@ -477,7 +480,7 @@ def run_ours(args, rank, world, dist):
                              "rice_to_r4_gsym_s": kern["rice_to_r4"]["gsym_s"],
                              "rice_to_r4_frac": kern["rice_to_r4"]["frac"],
                              "r4_vs_bf16_gemv_speedup": kern["gemv_bf16"]["ms_avg"] / kern["gemv_r4"]["ms_avg"]},
-                "kernels": kern, "roofline": roof, "gemm_tensor": extras, "cpu_baseline": cpu, "e2e": e2e,
+                "kernels": kern, "roofline": roof, "gemm_tensor": extras, "decode_step": dstep, "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": launches_per_step * args.steps, "clocks": clk,
                 "gpu": torch.cuda.get_device_name(dev)}
         print(json.dumps(line), flush=True)
@@ -523,6 +526,70 @@ def gemm_extras(dgt, torch, dev):
             res[name] = {"ms": t, "tflops": tf, "frac": tf / tpk}
         out[f"M{M}"] = {"shape": [M, N, K], "plan": [plan.m_tile, plan.split_k], "bound": "tensor",
                         "peak_tflops": tpk, "peak_kind": tkind, **res}
+    return out
+
+
+def decode_step_extras(dgt, torch, dev):
+    """Per-token time of a batch-1 decode step through the dense-3B layer stack
+    (28 layers; every layer its own weights in HBM), R4 against BF16, each step
+    one CUDA graph of the library's kernels (DecodeStep).  Attention is not
+    part of the step (the output projection reads the value vector repeated
+    over the query heads).  Weights: one N(0, 0.02) draw of the largest shape,
+    sliced per projection and uploaded once per layer (separate allocations,
+    so each layer streams its own bytes; 4.2 GB R4 / 5.6 GB BF16 per token,
+    far above L2).  CUDA events around 20 replays after 3 warm-ups, median."""
+    m = S.DENSE_3B
+    L, hid = m["layers"], m["hidden"]
+    big = S.weights(8192, 3072, (6, 0, 0, 0))
+    flat = big.reshape(-1)
+    host = {p: flat[:r * c].reshape(r, c) for p, r, c in m["proj"]}
+    packed = {p: dgt.pack(w, 2) for p, w in host.items()}
+    r4_layers, bf_layers, r4_bytes = [], [], 0
+    for _ in range(L):
+        lr = {p: dgt.load_r4(dgt.upload(packed[p], dev)) for p in host}
+        r4_layers.append(lr)
+        bf_layers.append({p: dgt.r4_to_bf16(lr[p]) for p in host})
+        r4_bytes += sum(r.sm.numel() + r.nib.numel() + r.n_esc + r.seg.numel() * 4 for r in lr.values())
+    bf_bytes = L * sum(r * c * 2 for _, r, c in m["proj"])
+    g = np.random.default_rng(7)
+    gam = [torch.from_numpy(S.f32_to_bf16_bits((1 + 0.1 * g.normal(size=hid)).astype(np.float32)).view(np.int16))
+           .to(dev).view(torch.bfloat16) for _ in range(2 * L + 1)]
+    x0 = torch.from_numpy(S.bf16_bits_to_f32(S.activations(hid, (6, 999, 0)))).to(dev)
+    out = {"model": m["name"], "layers": L, "hidden": hid, "batch": 1, "graph": True,
+           "attention": "not in the step (value vector repeated over the query heads)"}
+    res = {}
+    for name, layers, nbytes in (("r4", r4_layers, r4_bytes), ("bf16", bf_layers, bf_bytes)):
+        st = dgt.DecodeStep(layers, gam, depth=L)
+        st(x0)
+        torch.cuda.synchronize()
+        ref = (st.x.clone(), st.out.clone())
+        st.capture()
+        for _ in range(3):
+            st.replay(x0)
+        evs = []
+        cur = torch.cuda.current_stream(dev)
+        for _ in range(20):
+            st.x.copy_(x0)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(cur)
+            st._graph.replay()
+            e1.record(cur)
+            evs.append((e0, e1))
+        torch.cuda.synchronize()
+        t = sorted(a.elapsed_time(b) for a, b in evs)[10]
+        assert torch.equal(st.x.view(torch.int32), ref[0].view(torch.int32))
+        res[name] = {"us_per_token": t * 1e3, "tokens_per_s": 1e3 / t, "weight_bytes_per_token": nbytes,
+                     "weight_gb_s": nbytes / (t / 1e3) / 1e9, "x": ref[0], "out": ref[1]}
+        del st
+    same = torch.equal(res["r4"]["x"].view(torch.int32), res["bf16"]["x"].view(torch.int32)) and \
+        torch.equal(res["r4"]["out"].view(torch.int16), res["bf16"]["out"].view(torch.int16))
+    for k in ("r4", "bf16"):
+        res[k].pop("x")
+        res[k].pop("out")
+    out.update(res)
+    out["r4_over_bf16_speed"] = res["bf16"]["us_per_token"] / res["r4"]["us_per_token"]
+    out["r4_equals_bf16"] = bool(same)
+    out["kernels_per_token"] = L * 11 + 1
     return out
 
 
@@ -596,6 +663,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-decode-step", action="store_true")
     args = ap.parse_args()
     if args.case:
         run_case(args)

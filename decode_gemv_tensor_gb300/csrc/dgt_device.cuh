@@ -218,6 +218,13 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
                  : "memory");
 }
 
+// Programmatic dependent launch: let the next kernel of the stream (launched
+// with programmatic serialization) start its CTAs as this one's free their
+// SMs, and, in that next kernel, wait until this grid has completed and its
+// memory is visible (a no-op when nothing precedes programmatically).
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }

@@ -417,6 +417,10 @@ __global__ void __launch_bounds__((TNW + TPW) * 32, 1) k_gemv_tma(GemvArgs a) {
     if (tid == 0) abort_flag = 0;
     fence_mbarrier_init();
     __syncthreads();
+    // the next kernel may start as SMs free up; the weights stream from here
+    // on, while everything produced by the previous kernel (x) is read only
+    // after pdl_wait() below, and nothing is written before it
+    pdl_trigger();
 
     if (w >= TNW) {
         // ---- producer warps: lane l of producer warp p keeps consumer warp
@@ -448,6 +452,7 @@ __global__ void __launch_bounds__((TNW + TPW) * 32, 1) k_gemv_tma(GemvArgs a) {
     }
 
     // ---- consumer warps
+    pdl_wait();
     for (uint32_t i = tid; i < J * 64; i += TNW * 32) {
         const uint32_t k = 8 * i, j = k >> 9, u = (k >> 4) & 31, h = (k >> 3) & 1;
         xs[(2 * j + h) * 32 + u] = k < K ? *reinterpret_cast<const uint4 *>(a.x + k) : make_uint4(0, 0, 0, 0);
@@ -521,7 +526,10 @@ __global__ void __launch_bounds__((TNW + TPW) * 32, 1) k_gemv_tma(GemvArgs a) {
                 const uint32_t rp = (cut && Jm1 - jp < n) ? Jm1 - jp : 0xFFFFFFFFu;
                 const uint32_t pm = R4 ? (rl.multi >> b0) & ((1u << n) - 1u) : 0u;
                 const uint8_t *stg = ring + st * STAGE;
-                bool slow = n != C || rp != 0xFFFFFFFFu;
+                // an R4 piece of fewer than C rounds (a short unit's last piece)
+                // stays on the fast loops; the row's last round cut by K, and short
+                // BF16 pieces, go to the slow loop
+                bool slow = rp != 0xFFFFFFFFu || (!R4 && n != C);
                 // rounds with two or more escapes: per-lane rank-15 entries, worked
                 // out before the multiply-adds; anything else takes the slow loop
                 uint32_t mh3[C], ml1[C];
@@ -543,30 +551,38 @@ __global__ void __launch_bounds__((TNW + TPW) * 32, 1) k_gemv_tma(GemvArgs a) {
                         }
                     }
                 }
-                if (ok && !slow && pm == 0) {
-                    // the common piece: every round decodes with its shuffled table words
+                // one round of the common piece: decode with its shuffled table words
+                auto fast_round = [&](uint32_t r) {
+                    const uint32_t j = jp + r;
+                    uint32_t p[8];
+                    if (R4) {
+                        const uint4 sv = *reinterpret_cast<const uint4 *>(stg + r * 512 + 16 * lane);
+                        const uint2 nv = *reinterpret_cast<const uint2 *>(stg + C * 512 + r * 256 + 8 * lane);
+                        R4Lut Lr = L;
+                        Lr.h3 = __shfl_sync(DGT_FULL, rl.h3, b0 + r);
+                        Lr.l1 = __shfl_sync(DGT_FULL, rl.l1, b0 + r);
+                        r4_dec16(nv, sv, Lr, p);
+                    } else {
+                        const uint4 lo = *reinterpret_cast<const uint4 *>(stg + r * 1024 + 32 * lane);
+                        const uint4 hi = *reinterpret_cast<const uint4 *>(stg + r * 1024 + 32 * lane + 16);
+                        p[0] = lo.x; p[1] = lo.y; p[2] = lo.z; p[3] = lo.w;
+                        p[4] = hi.x; p[5] = hi.y; p[6] = hi.z; p[7] = hi.w;
+                    }
+                    acc = fma_chunk16(p, xs, j, lane, acc);
+                };
+                if (ok && !slow && pm == 0 && n == C) {
+#pragma unroll
+                    for (uint32_t r = 0; r < C; r++) fast_round(r);
+                } else if (ok && !slow && pm == 0) {
 #pragma unroll
                     for (uint32_t r = 0; r < C; r++) {
-                        const uint32_t j = jp + r;
-                        uint32_t p[8];
-                        if (R4) {
-                            const uint4 sv = *reinterpret_cast<const uint4 *>(stg + r * 512 + 16 * lane);
-                            const uint2 nv = *reinterpret_cast<const uint2 *>(stg + C * 512 + r * 256 + 8 * lane);
-                            R4Lut Lr = L;
-                            Lr.h3 = __shfl_sync(DGT_FULL, rl.h3, b0 + r);
-                            Lr.l1 = __shfl_sync(DGT_FULL, rl.l1, b0 + r);
-                            r4_dec16(nv, sv, Lr, p);
-                        } else {
-                            const uint4 lo = *reinterpret_cast<const uint4 *>(stg + r * 1024 + 32 * lane);
-                            const uint4 hi = *reinterpret_cast<const uint4 *>(stg + r * 1024 + 32 * lane + 16);
-                            p[0] = lo.x; p[1] = lo.y; p[2] = lo.z; p[3] = lo.w;
-                            p[4] = hi.x; p[5] = hi.y; p[6] = hi.z; p[7] = hi.w;
-                        }
-                        acc = fma_chunk16(p, xs, j, lane, acc);
+                        if (r >= n) break;
+                        fast_round(r);
                     }
                 } else if (ok && !slow) {
 #pragma unroll
                     for (uint32_t r = 0; r < C; r++) {
+                        if (r >= n) break;
                         const uint32_t j = jp + r;
                         uint32_t p[8];
                         if (R4) {
@@ -723,7 +739,8 @@ int launch_gemv(GemvArgs &a, int path, cudaStream_t st) {
         const size_t smem = (size_t)TNW * TmaCfg<R4>::NS * TmaCfg<R4>::STAGE + (size_t)a.J * 1024;
         if (prepare_kernel((const void *)k_gemv_tma<R4>, smem, (TNW + TPW) * 32, &bps) != DGT_OK) return DGT_ERR_CUDA;
         const unsigned grid = (unsigned)min((uint64_t)di.sms, a.rows);
-        k_gemv_tma<R4><<<grid, (TNW + TPW) * 32, smem, st>>>(a);
+        if (launch_pdl(k_gemv_tma<R4>, dim3(grid), dim3((TNW + TPW) * 32), smem, st, a) != cudaSuccess)
+            return DGT_ERR_CUDA;
     } else if (path == 1) {
         const size_t smem = (size_t)a.J * 1024;
         if (prepare_kernel((const void *)k_gemv<R4, 16, 4>, smem, 16 * 32, &bps) != DGT_OK) return DGT_ERR_CUDA;

@@ -27,6 +27,8 @@ __global__ void __launch_bounds__(NORM_THREADS) k_add_rmsnorm(float *__restrict_
                                                              float eps, uint16_t *__restrict__ h) {
     __shared__ float part[32];
     __shared__ float rs;
+    pdl_trigger();
+    pdl_wait();
     const uint32_t t = threadIdx.x, lane = t & 31, w = t >> 5;
     float acc = 0.0f;
     for (uint32_t i = t; i < n; i += NORM_THREADS) {
@@ -58,6 +60,8 @@ __global__ void __launch_bounds__(NORM_THREADS) k_add_rmsnorm(float *__restrict_
 // out = bf16((g / (1 + exp(-g))) * u), elementwise.
 __global__ void __launch_bounds__(256) k_silu_mul(const float *__restrict__ g, const float *__restrict__ u,
                                                  uint64_t n, uint16_t *__restrict__ out) {
+    pdl_trigger();
+    pdl_wait();
     for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (uint64_t)gridDim.x * blockDim.x) {
         const float a = g[i];
         const float s = a / (1.0f + expf(-a));
@@ -68,6 +72,8 @@ __global__ void __launch_bounds__(256) k_silu_mul(const float *__restrict__ g, c
 // out[i] = v[i mod n_in].
 __global__ void __launch_bounds__(256) k_repeat(const uint16_t *__restrict__ v, uint64_t n_in, uint64_t n_out,
                                                uint16_t *__restrict__ out) {
+    pdl_trigger();
+    pdl_wait();
     for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n_out;
          i += (uint64_t)gridDim.x * blockDim.x)
         out[i] = v[i % n_in];
@@ -90,21 +96,27 @@ extern "C" int dgt_add_rmsnorm(float *d_x, const float *d_y, const uint16_t *d_g
     if (!d_x || !d_gamma || !d_h) return DGT_ERR_ARG;
     if (n == 0 || n > NORM_MAX) return DGT_ERR_SHAPE;
     if (!(eps >= 0.0f)) return DGT_ERR_ARG;
-    k_add_rmsnorm<<<1, NORM_THREADS, 0, (cudaStream_t)stream>>>(d_x, d_y, d_gamma, (uint32_t)n, eps, d_h);
-    return cudaPeekAtLastError() == cudaSuccess ? DGT_OK : DGT_ERR_CUDA;
+    return launch_pdl(k_add_rmsnorm, dim3(1), dim3(NORM_THREADS), 0, (cudaStream_t)stream, d_x, d_y, d_gamma,
+                      (uint32_t)n, eps, d_h) == cudaSuccess
+               ? DGT_OK
+               : DGT_ERR_CUDA;
 }
 
 extern "C" int dgt_silu_mul(const float *d_g, const float *d_u, uint64_t n, uint16_t *d_out, void *stream) {
     if (!d_g || !d_u || !d_out) return DGT_ERR_ARG;
     if (n == 0) return DGT_OK;
-    k_silu_mul<<<elem_grid(n), 256, 0, (cudaStream_t)stream>>>(d_g, d_u, n, d_out);
-    return cudaPeekAtLastError() == cudaSuccess ? DGT_OK : DGT_ERR_CUDA;
+    return launch_pdl(k_silu_mul, dim3(elem_grid(n)), dim3(256), 0, (cudaStream_t)stream, d_g, d_u, n, d_out) ==
+                   cudaSuccess
+               ? DGT_OK
+               : DGT_ERR_CUDA;
 }
 
 extern "C" int dgt_repeat(const uint16_t *d_v, uint64_t n_in, uint64_t n_out, uint16_t *d_out, void *stream) {
     if (!d_v || !d_out) return DGT_ERR_ARG;
     if (n_out == 0) return DGT_OK;
     if (n_in == 0) return DGT_ERR_SHAPE;
-    k_repeat<<<elem_grid(n_out), 256, 0, (cudaStream_t)stream>>>(d_v, n_in, n_out, d_out);
-    return cudaPeekAtLastError() == cudaSuccess ? DGT_OK : DGT_ERR_CUDA;
+    return launch_pdl(k_repeat, dim3(elem_grid(n_out)), dim3(256), 0, (cudaStream_t)stream, d_v, n_in, n_out,
+                      d_out) == cudaSuccess
+               ? DGT_OK
+               : DGT_ERR_CUDA;
 }
