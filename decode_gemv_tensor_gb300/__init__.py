@@ -88,6 +88,8 @@ def lib():
             "dgt_gemv_slices": (i32, [u64, u64]),
             "dgt_gemv": (i32, [C.POINTER(R4Struct), vp, vp, vp, vp, vp]),
             "dgt_gemv_bf16": (i32, [vp, u64, u64, vp, vp, vp, vp, vp]),
+            "dgt_gemv_ex": (i32, [C.POINTER(R4Struct), vp, vp, vp, vp, C.c_uint, vp]),
+            "dgt_gemv_bf16_ex": (i32, [vp, u64, u64, vp, vp, vp, vp, C.c_uint, vp]),
             "dgt_gemm_default_plan": (i32, [u64, u64, u64, C.POINTER(GemmPlan)]),
             "dgt_gemm_workspace_bytes": (C.c_size_t, [u64, u64, C.POINTER(GemmPlan)]),
             "dgt_gemm": (i32, [C.POINTER(R4Struct), vp, u64, vp, vp, C.POINTER(GemmPlan), vp, C.c_size_t, vp, vp]),
@@ -322,8 +324,13 @@ def read_status(status, stream=None) -> int:
     return v.value
 
 
-def gemv(W: R4, x, y=None, y32=None, status=None, stream=None):
-    """dgt_gemv: y = W x with W in R4; x bf16 [cols] on the device.
+STATIC_WEIGHTS = 1
+
+
+def gemv(W: R4, x, y=None, y32=None, status=None, stream=None, static_weights=False):
+    """dgt_gemv_ex: y = W x with W in R4; x bf16 [cols] on the device.
+    static_weights: no kernel still running writes W (DGT_GEMV_STATIC_WEIGHTS),
+    so W may stream before the previous kernel ends.
     Returns (y bf16 [rows], y32 float32 [rows])."""
     import torch
     dev = W.sm.device
@@ -331,20 +338,21 @@ def gemv(W: R4, x, y=None, y32=None, status=None, stream=None):
         y = torch.empty(W.rows, dtype=torch.bfloat16, device=dev)
     if y32 is None:
         y32 = torch.empty(W.rows, dtype=torch.float32, device=dev)
-    _check(lib().dgt_gemv(C.byref(W.s), _ptr(x), _ptr(y), _ptr(y32), _ptr(status), _stream(stream)), "dgt_gemv")
+    _check(lib().dgt_gemv_ex(C.byref(W.s), _ptr(x), _ptr(y), _ptr(y32), _ptr(status),
+                             STATIC_WEIGHTS if static_weights else 0, _stream(stream)), "dgt_gemv")
     return y, y32
 
 
-def gemv_bf16(W, x, y=None, y32=None, status=None, stream=None):
-    """dgt_gemv_bf16: the same product and order with bf16 weights [rows, cols]."""
+def gemv_bf16(W, x, y=None, y32=None, status=None, stream=None, static_weights=False):
+    """dgt_gemv_bf16_ex: the same product and order with bf16 weights [rows, cols]."""
     import torch
     rows, cols = W.shape
     if y is None:
         y = torch.empty(rows, dtype=torch.bfloat16, device=W.device)
     if y32 is None:
         y32 = torch.empty(rows, dtype=torch.float32, device=W.device)
-    _check(lib().dgt_gemv_bf16(_ptr(W), rows, cols, _ptr(x), _ptr(y), _ptr(y32), _ptr(status), _stream(stream)),
-           "dgt_gemv_bf16")
+    _check(lib().dgt_gemv_bf16_ex(_ptr(W), rows, cols, _ptr(x), _ptr(y), _ptr(y32), _ptr(status),
+                                  STATIC_WEIGHTS if static_weights else 0, _stream(stream)), "dgt_gemv_bf16")
     return y, y32
 
 
@@ -518,11 +526,12 @@ class DecodeStep:
         self._graph = None
 
     def _gemv(self, W, x, p, stream):
+        # the step's weights are only read: they stream while the previous kernel ends
         y, y32 = self.y[p]
         if self.r4:
-            gemv(W, x, y, y32, stream=stream)
+            gemv(W, x, y, y32, stream=stream, static_weights=True)
         else:
-            gemv_bf16(W, x, y, y32, stream=stream)
+            gemv_bf16(W, x, y, y32, stream=stream, static_weights=True)
         return y, y32
 
     def launch(self, stream=None):

@@ -253,6 +253,10 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // barriers and tensor memory are set up while the previous kernel of the
+    // stream may still run; nothing it writes or reads is touched before this
+    pdl_trigger();
+    pdl_wait();
     const uint32_t taddr = tmem_slot;
     volatile int *abortp = &abort_flag;
 
@@ -400,6 +404,8 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
 }
 
 __global__ void __launch_bounds__(256) k_gemm_reduce(GemmArgs a) {
+    pdl_trigger();
+    pdl_wait();
     const uint64_t total = a.M * a.N;
     for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (uint64_t)gridDim.x * blockDim.x) {
         float y = a.partial[i];
@@ -468,14 +474,15 @@ static int launch_gemm(GemmArgs &a, const void *w_or_sm, const uint16_t *d_X, vo
     int bps = 0;
     if (prepare_kernel((const void *)k_gemm<R4>, smem, GT_THREADS, &bps) != DGT_OK) return DGT_ERR_CUDA;
     dim3 grid((unsigned)(a.N / GT_N), (unsigned)((a.M + a.mt - 1) / a.mt), a.split);
-    k_gemm<R4><<<grid, GT_THREADS, smem, st>>>(tm_x, tm_w, tm_nib, a);
+    if (launch_pdl(k_gemm<R4>, grid, dim3(GT_THREADS), smem, st, tm_x, tm_w, tm_nib, a) != cudaSuccess)
+        return DGT_ERR_CUDA;
     if (a.split > 1) {
         DeviceInfo di;
         if (device_info(&di) != DGT_OK) return DGT_ERR_CUDA;
         const uint64_t total = a.M * a.N;
         uint64_t g = (total + 255) / 256;
         if (g > (uint64_t)di.sms * 8) g = (uint64_t)di.sms * 8;
-        k_gemm_reduce<<<(unsigned)g, 256, 0, st>>>(a);
+        if (launch_pdl(k_gemm_reduce, dim3((unsigned)g), dim3(256), 0, st, a) != cudaSuccess) return DGT_ERR_CUDA;
     }
     return cudaPeekAtLastError() == cudaSuccess ? DGT_OK : DGT_ERR_CUDA;
 }

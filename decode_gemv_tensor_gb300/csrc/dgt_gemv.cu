@@ -52,6 +52,7 @@ struct GemvArgs {
     uint64_t rows, cols, nseg, n_esc;
     uint32_t J;
     int S;
+    uint32_t early;   // DGT_GEMV_STATIC_WEIGHTS: stream W before the grid dependency wait
     R4Lut L;
     uint8_t table[256];
     int32_t *status;
@@ -417,12 +418,13 @@ __global__ void __launch_bounds__((TNW + TPW) * 32, 1) k_gemv_tma(GemvArgs a) {
     if (tid == 0) abort_flag = 0;
     fence_mbarrier_init();
     __syncthreads();
-    // the next kernel may start as SMs free up; the weights stream from here
-    // on, while everything produced by the previous kernel (x) is read only
-    // after pdl_wait() below, and nothing is written before it
+    // the next kernel may start as SMs free up.  With static weights they
+    // stream from here on; otherwise, and for everything else the previous
+    // kernel may write (x, y), only after the grid dependency wait
     pdl_trigger();
 
     if (w >= TNW) {
+        if (!a.early) pdl_wait();
         // ---- producer warps: lane l of producer warp p keeps consumer warp
         // c = p + TPW l's ring full.  It polls the ring's "empty" barriers
         // without blocking, so no consumer waits for another.
@@ -768,9 +770,9 @@ int choose_path(uint64_t K, uint32_t J, bool aligned) {
 
 using namespace dgt;
 
-extern "C" int dgt_gemv(const dgt_r4 *W, const uint16_t *d_x, uint16_t *d_y, float *d_y32, int32_t *d_status,
-                        void *stream) {
-    if (!W) return DGT_ERR_ARG;
+extern "C" int dgt_gemv_ex(const dgt_r4 *W, const uint16_t *d_x, uint16_t *d_y, float *d_y32, int32_t *d_status,
+                           unsigned flags, void *stream) {
+    if (!W || (flags & ~(unsigned)DGT_GEMV_STATIC_WEIGHTS)) return DGT_ERR_ARG;
     const uint64_t N = W->rows, K = W->cols;
     if (K >= (1ull << 31) || (N && (N * K) / N != K)) return DGT_ERR_SHAPE;
     if (N == 0) return DGT_OK;
@@ -792,12 +794,19 @@ extern "C" int dgt_gemv(const dgt_r4 *W, const uint16_t *d_x, uint16_t *d_y, flo
     a.L = make_r4lut(W->table, W->n_table);
     for (int i = 0; i < 256; i++) a.table[i] = W->table[i];
     a.status = d_status;
+    a.early = flags & DGT_GEMV_STATIC_WEIGHTS;
     const int path = choose_path<true>(K, a.J, aligned16(W->sm) && aligned16(W->nib) && aligned16(d_x));
     return launch_gemv<true>(a, path, (cudaStream_t)stream);
 }
 
-extern "C" int dgt_gemv_bf16(const uint16_t *d_W, uint64_t rows, uint64_t cols, const uint16_t *d_x,
-                             uint16_t *d_y, float *d_y32, int32_t *d_status, void *stream) {
+extern "C" int dgt_gemv(const dgt_r4 *W, const uint16_t *d_x, uint16_t *d_y, float *d_y32, int32_t *d_status,
+                        void *stream) {
+    return dgt_gemv_ex(W, d_x, d_y, d_y32, d_status, 0u, stream);
+}
+
+extern "C" int dgt_gemv_bf16_ex(const uint16_t *d_W, uint64_t rows, uint64_t cols, const uint16_t *d_x,
+                                uint16_t *d_y, float *d_y32, int32_t *d_status, unsigned flags, void *stream) {
+    if (flags & ~(unsigned)DGT_GEMV_STATIC_WEIGHTS) return DGT_ERR_ARG;
     const uint64_t N = rows, K = cols;
     if (K >= (1ull << 31) || (N && (N * K) / N != K)) return DGT_ERR_SHAPE;
     if (N == 0) return DGT_OK;
@@ -812,6 +821,12 @@ extern "C" int dgt_gemv_bf16(const uint16_t *d_W, uint64_t rows, uint64_t cols, 
     a.rows = N;
     a.cols = K;
     a.J = (uint32_t)((K + 511) / 512);
+    a.early = flags & DGT_GEMV_STATIC_WEIGHTS;
     const int path = choose_path<false>(K, a.J, aligned16(d_W) && aligned16(d_x));
     return launch_gemv<false>(a, path, (cudaStream_t)stream);
+}
+
+extern "C" int dgt_gemv_bf16(const uint16_t *d_W, uint64_t rows, uint64_t cols, const uint16_t *d_x,
+                             uint16_t *d_y, float *d_y32, int32_t *d_status, void *stream) {
+    return dgt_gemv_bf16_ex(d_W, rows, cols, d_x, d_y, d_y32, d_status, 0u, stream);
 }

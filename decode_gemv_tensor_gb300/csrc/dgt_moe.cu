@@ -128,6 +128,8 @@ __global__ void __launch_bounds__(1024) k_moe_route(MoeArgs a) {
     // (per active expert) share one array
     __shared__ uint64_t cost[MOE_MAX_EXPERTS + 1];
     __shared__ uint64_t sw[32];
+    pdl_trigger();
+    pdl_wait();
     uint32_t *cnt = reinterpret_cast<uint32_t *>(cost);
     const uint32_t P = a.tokens * a.topk, tid = threadIdx.x;
     for (uint32_t e = tid; e < a.n_experts; e += blockDim.x) cnt[e] = 0;
@@ -519,6 +521,8 @@ __global__ void __launch_bounds__((MNW + MPW) * 32, 1) k_moe(MoeArgs a) {
     __shared__ uint8_t escb[R4 ? MNW : 1][R4 ? DGT_SEG : 1];
     __shared__ int abort_flag;
     __shared__ MoeTable T;
+    pdl_trigger();
+    pdl_wait();
     const uint32_t tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
     const uint32_t P = a.tokens * a.topk;
     const uint64_t rb = a.rbound[blockIdx.x], nrows = a.rbound[blockIdx.x + 1] - rb;
@@ -709,6 +713,8 @@ __global__ void __launch_bounds__((MNW + MPW) * 32, 1) k_moe(MoeArgs a) {
 }
 
 __global__ void __launch_bounds__(256) k_moe_combine(MoeArgs a) {
+    pdl_trigger();
+    pdl_wait();
     const float *__restrict__ part = a.partial;
     const float *__restrict__ pw = a.p;
     float *__restrict__ y32 = a.y32;
@@ -746,17 +752,19 @@ int launch_moe(MoeArgs &a, void *d_ws, size_t ws_bytes, cudaStream_t st) {
     DeviceInfo di;
     if (device_info(&di) != DGT_OK) return DGT_ERR_CUDA;
     a.grid = (uint32_t)min(di.sms, (int)MOE_MAX_CTAS);
-    k_moe_route<<<1, 1024, 0, st>>>(a);
+    if (launch_pdl(k_moe_route, dim3(1), dim3(1024), 0, st, a) != cudaSuccess) return DGT_ERR_CUDA;
     a.xs_slots = a.tokens <= XS_TOKENS ? (uint32_t)min((uint64_t)a.tokens, (uint64_t)(XS_BYTES / (2 * a.cols))) : 0u;
     const size_t smem = (size_t)MNW * MoeStage<R4>::NS * MoeStage<R4>::BYTES + (size_t)a.xs_slots * a.cols * 2;
     int bps = 0;
     if (prepare_kernel((const void *)k_moe<R4>, smem, (MNW + MPW) * 32, &bps) != DGT_OK) return DGT_ERR_CUDA;
-    k_moe<R4><<<a.grid, (MNW + MPW) * 32, smem, st>>>(a);
+    if (launch_pdl(k_moe<R4>, dim3(a.grid), dim3((MNW + MPW) * 32), smem, st, a) != cudaSuccess)
+        return DGT_ERR_CUDA;
     const uint64_t n_out = (uint64_t)a.tokens * a.ne;
     uint64_t cgrid = (n_out + 255) / 256;
     if (cgrid > (uint64_t)di.sms * 8) cgrid = (uint64_t)di.sms * 8;
     if (cgrid < 1) cgrid = 1;
-    k_moe_combine<<<(unsigned)cgrid, 256, 0, st>>>(a);
+    if (launch_pdl(k_moe_combine, dim3((unsigned)cgrid), dim3(256), 0, st, a) != cudaSuccess)
+        return DGT_ERR_CUDA;
     return cudaPeekAtLastError() == cudaSuccess ? DGT_OK : DGT_ERR_CUDA;
 }
 

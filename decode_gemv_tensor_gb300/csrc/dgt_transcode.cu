@@ -366,6 +366,10 @@ __global__ void __launch_bounds__(RW * 32, 1) k_rice_to_r4(F2Args a) {
         for (int c = 0; c < REP / 4; c++) reinterpret_cast<uint4 *>(S.lut)[v * (REP / 4) + c] = make_uint4(e, e, e, e);
     }
     if (threadIdx.x == 0) S.k = a.k;
+    // the table is built while the previous kernel of the stream may still
+    // run; its outputs (and anything it reads) are touched only after this
+    pdl_trigger();
+    pdl_wait();
     if (blockIdx.x == 0 && threadIdx.x == 0) a.seg[a.seg_last] = (uint32_t)a.n_esc;
     __syncthreads();
     const uint32_t w = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -720,6 +724,8 @@ struct E1Src {
 __global__ void __launch_bounds__(FW * 32) k_f1_to_r4(F1Args a) {
     extern __shared__ uint4 smem_raw[];
     F1Smem &S = *reinterpret_cast<F1Smem *>(smem_raw);
+    pdl_trigger();
+    pdl_wait();
     if (blockIdx.x == 0 && threadIdx.x == 0) a.seg[a.seg_last] = (uint32_t)a.n_esc;
     const uint32_t w = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint64_t nbytes = (a.n + 1) / 2;
@@ -879,6 +885,8 @@ struct R2BArgs {
 // Fast path: cols % 16 == 0, 16-byte aligned arrays.  One warp per
 // row-segment of 512 columns; lane u owns columns [512j + 16u, +16).
 __global__ void __launch_bounds__(256) k_r4_to_bf16(R2BArgs a) {
+    pdl_trigger();
+    pdl_wait();
     __shared__ uint8_t table_s[256];
     __shared__ uint8_t escb[8][DGT_SEG];
     table_s[threadIdx.x] = a.table[threadIdx.x];
@@ -922,6 +930,8 @@ __global__ void __launch_bounds__(256) k_r4_to_bf16(R2BArgs a) {
 // Any shape and alignment: one warp per row-segment, one element at a time per
 // lane chunk, escapes located by a warp prefix sum of 15-nibbles.
 __global__ void __launch_bounds__(256) k_r4_to_bf16_any(R2BArgs a) {
+    pdl_trigger();
+    pdl_wait();
     const uint32_t w = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint64_t units = a.rows * a.nseg;
     for (uint64_t u = (uint64_t)blockIdx.x * 8 + w; u < units; u += (uint64_t)gridDim.x * 8) {
@@ -1002,10 +1012,9 @@ extern "C" int dgt_load_r4(const dgt_packed_view *dev, dgt_r4 *r4, int32_t *d_st
         int bps = 0;
         if (prepare_kernel(fn, smem, RW * 32, &bps) != DGT_OK) return DGT_ERR_CUDA;
         uint64_t grid = min((uint64_t)di.sms * bps, (a.ngrp + RW - 1) / RW);
-        if (fast)
-            k_rice_to_r4<true><<<(unsigned)grid, RW * 32, smem, st>>>(a);
-        else
-            k_rice_to_r4<false><<<(unsigned)grid, RW * 32, smem, st>>>(a);
+        const cudaError_t e = fast ? launch_pdl(k_rice_to_r4<true>, dim3((unsigned)grid), dim3(RW * 32), smem, st, a)
+                                   : launch_pdl(k_rice_to_r4<false>, dim3((unsigned)grid), dim3(RW * 32), smem, st, a);
+        if (e != cudaSuccess) return DGT_ERR_CUDA;
     } else {
         if (!dev->tw || !dev->tesc || !dev->grp1 || (dev->payload_bytes && !dev->payload) ||
             (dev->n_esc1 && !dev->esc1) || (dev->payload && !aligned16(dev->payload)))
@@ -1034,7 +1043,8 @@ extern "C" int dgt_load_r4(const dgt_packed_view *dev, dgt_r4 *r4, int32_t *d_st
         int bps = 0;
         if (prepare_kernel((const void *)k_f1_to_r4, smem, FW * 32, &bps) != DGT_OK) return DGT_ERR_CUDA;
         uint64_t grid = min((uint64_t)di.sms * bps, (a.ngrp + FW - 1) / FW);
-        k_f1_to_r4<<<(unsigned)grid, FW * 32, smem, st>>>(a);
+        if (launch_pdl(k_f1_to_r4, dim3((unsigned)grid), dim3(FW * 32), smem, st, a) != cudaSuccess)
+            return DGT_ERR_CUDA;
     }
     return cudaPeekAtLastError() == cudaSuccess ? DGT_OK : DGT_ERR_CUDA;
 }
@@ -1068,10 +1078,9 @@ extern "C" int dgt_r4_to_bf16(const dgt_r4 *r4, uint16_t *d_out, int32_t *d_stat
     const void *fn = fast ? (const void *)k_r4_to_bf16 : (const void *)k_r4_to_bf16_any;
     if (prepare_kernel(fn, 0, 256, &bps) != DGT_OK) return DGT_ERR_CUDA;
     uint64_t grid = min((uint64_t)di.sms * bps, (units + 7) / 8);
-    if (fast)
-        k_r4_to_bf16<<<(unsigned)grid, 256, 0, st>>>(a);
-    else
-        k_r4_to_bf16_any<<<(unsigned)grid, 256, 0, st>>>(a);
+    if (launch_pdl(fast ? k_r4_to_bf16 : k_r4_to_bf16_any, dim3((unsigned)grid), dim3(256), 0, st, a) !=
+        cudaSuccess)
+        return DGT_ERR_CUDA;
     return cudaPeekAtLastError() == cudaSuccess ? DGT_OK : DGT_ERR_CUDA;
 }
 

@@ -261,6 +261,24 @@ int dgt_gemv(const dgt_r4 *W, const uint16_t *d_x, uint16_t *d_y, float *d_y32, 
 int dgt_gemv_bf16(const uint16_t *d_W, uint64_t rows, uint64_t cols, const uint16_t *d_x,
                   uint16_t *d_y, float *d_y32, int32_t *d_status, void *stream);
 
+/*
+ * Launch behaviour.  The streaming kernel (cols % 32 == 0, 16-byte aligned
+ * arrays) is launched with programmatic stream serialization: it may start
+ * while the previous kernel of the stream finishes, and reads x, writes y and
+ * the status word only after that kernel has completed (its writes visible).
+ * By default it also reads W only after then.  DGT_GEMV_STATIC_WEIGHTS
+ * promises that no kernel still running when this one is launched writes W
+ * (true for weights loaded earlier and only read since, as in a decode loop):
+ * the weights then start streaming into shared memory at once, overlapping
+ * the previous kernel's tail.  Results are the same either way.  Other
+ * flags: DGT_ERR_ARG.
+ */
+#define DGT_GEMV_STATIC_WEIGHTS 1u
+int dgt_gemv_ex(const dgt_r4 *W, const uint16_t *d_x, uint16_t *d_y, float *d_y32, int32_t *d_status,
+                unsigned flags, void *stream);
+int dgt_gemv_bf16_ex(const uint16_t *d_W, uint64_t rows, uint64_t cols, const uint16_t *d_x, uint16_t *d_y,
+                     float *d_y32, int32_t *d_status, unsigned flags, void *stream);
+
 /* ------------------------------------------------------------------------ */
 /* Mixture-of-experts expert gather                                         */
 /* ------------------------------------------------------------------------ */
