@@ -478,11 +478,18 @@ __global__ void __launch_bounds__((TNW + TPW) * 32, 1) k_gemv_tma(GemvArgs a) {
     const bool cut = (K & 511) != 0;
     uint32_t st = 0, phases = 0, waited = 0;
     bool ok = true;
-    SegPre pre = {0, 0, 0, 0};
+    // escape metadata runs ahead: the segment counts of the unit after next
+    // and the first escape ranks of the next unit are requested while this unit
+    // streams, so a unit start never waits on a load (units can be one piece)
+    SegPre pre = {0, 0, 0, 0}, nxt = {0, 0, 0, 0};
     if (R4 && (uint64_t)w < units) {
         const UnitRange u = unit_range(w, r0, rs, log2S, J);
         seg_issue(a, u.row, u.j0, u.j1, lane, pre);
         seg_issue_esc(a, pre);
+        if ((uint64_t)w + TNW < units) {
+            const UnitRange un = unit_range(w + TNW, r0, rs, log2S, J);
+            seg_issue(a, un.row, un.j0, un.j1, lane, nxt);
+        }
     }
     for (uint64_t ch = 0; ch < nchunks; ch++) {
         const uint64_t c0 = ch * TCHUNK, cend = min(c0 + TCHUNK, units);
@@ -491,14 +498,14 @@ __global__ void __launch_bounds__((TNW + TPW) * 32, 1) k_gemv_tma(GemvArgs a) {
             SegInfo g = {0, 0, 0, 0, 0};
             RoundLut rl = {0, 0, 0};
             uint32_t jbase = u.j0;
-            SegPre nxt = {0, 0, 0, 0};
-            bool nxt_esc = false;
-            const bool has_next = uu + TNW < units;
             if (R4) {
                 g = seg_finish(pre, table_s);
                 rl = round_luts(g, L);
-                if (has_next) {
-                    const UnitRange un = unit_range(uu + TNW, r0, rs, log2S, J);
+                pre = nxt;
+                if (uu + TNW < units) seg_issue_esc(a, pre);
+                nxt = SegPre{0, 0, 0, 0};
+                if (uu + 2 * TNW < units) {
+                    const UnitRange un = unit_range(uu + 2 * TNW, r0, rs, log2S, J);
                     seg_issue(a, un.row, un.j0, un.j1, lane, nxt);
                 }
             }
@@ -643,12 +650,7 @@ __global__ void __launch_bounds__((TNW + TPW) * 32, 1) k_gemv_tma(GemvArgs a) {
                 // producer stops, and the copies in flight are waited for below
                 if (ok && lane == 0) mbar_arrive(empty_a + 8 * st);
                 st = st + 1 == TNS ? 0 : st + 1;
-                if (R4 && has_next && !nxt_esc) {
-                    seg_issue_esc(a, nxt);
-                    nxt_esc = true;
-                }
             }
-            if (R4) pre = nxt;
 #pragma unroll
             for (int d = 16; d >= 1; d >>= 1) acc += __shfl_xor_sync(DGT_FULL, acc, d);
             if (lane == 0) part[uu - c0] = acc;

@@ -4,14 +4,15 @@
 
 // GEMV plan S(N, K): the number of K slices whose partial sums are added left
 // to right (part of the documented summation order; see dgt.h).  Slices are
-// added until the product has 16384 (row, slice) units -- about 7 for each of
-// the 16 streaming warps on each of GB300's 152 SMs, so that every SM's warps
-// get even work -- and never more than 8 or more than the 512-column rounds
-// allow (largest power of two <= J).
+// added until the product has 8192 (row, slice) units -- about 3.4 for each of
+// the 16 streaming warps on each of GB300's 152 SMs: enough for even work,
+// while each unit stays long enough that its per-unit work (escape index,
+// reduction) is small next to its rounds -- and never more than 8 or more
+// than the 512-column rounds allow (largest power of two <= J).
 static inline int dgt_plan_slices(uint64_t N, uint64_t K) {
     uint64_t J = (K + 511) / 512;
     if (N == 0 || J <= 1) return 1;
-    uint64_t want = (16384 + N - 1) / N;
+    uint64_t want = (8192 + N - 1) / N;
     int S = 1;
     while ((uint64_t)S < want && S * 2 <= 8 && (uint64_t)(S * 2) <= J) S *= 2;
     return S;

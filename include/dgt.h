@@ -240,7 +240,7 @@ int dgt_read_status(const int32_t *d_status, void *stream, int32_t *status);
  * [floor(s*J/S), floor((s+1)*J/S)), J = ceil(K/512), and
  * y = ((P_0 + P_1) + ...) + P_(S-1).  y_bf16 is y rounded to nearest-even
  * (NaN -> 0x7FC0).  dgt_gemv_slices() is the plan S(N, K): the smallest power
- * of two >= ceil(16384/N), capped at 8 and at the largest power of two <= J.
+ * of two >= ceil(8192/N), capped at 8 and at the largest power of two <= J.
  */
 int dgt_gemv_slices(uint64_t rows, uint64_t cols);
 

@@ -448,13 +448,13 @@ int or_r4_decode(const uint8_t *nib, const uint8_t *esc, const uint32_t *seg,
 /*   slice result is lane 0's value.  With S slices, slice s owns rounds     */
 /*   [floor(sJ/S), floor((s+1)J/S)), J = ceil(K/512), and y = P_0 + P_1 +   */
 /*   ... added left to right.                                                */
-/* The plan S(N, K): the smallest power of two >= ceil(16384/N), capped at 8 */
+/* The plan S(N, K): the smallest power of two >= ceil(8192/N), capped at 8 */
 /* and at the largest power of two <= J (S = 1 when J <= 1).                 */
 /* ------------------------------------------------------------------------ */
 int or_gemv_slices(uint64_t N, uint64_t K) {
     uint64_t J = (K + OR_ROUND - 1) / OR_ROUND;
     if (N == 0 || J <= 1) return 1;
-    uint64_t want = (16384 + N - 1) / N;
+    uint64_t want = (8192 + N - 1) / N;
     int S = 1;
     while ((uint64_t)S < want && S * 2 <= 8 && (uint64_t)(S * 2) <= J) S *= 2;
     return S;

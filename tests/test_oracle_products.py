@@ -52,8 +52,8 @@ def test_gemv_brute_force_tree(N, K):
     x = _bf16(g.standard_normal(K))
     wf, xf = S.bf16_bits_to_f32(w[0]), S.bf16_bits_to_f32(x)
     J = -(-K // 512)
-    # plan: smallest power of two >= ceil(16384/N), capped at 8 and at J
-    want = -(-16384 // N)
+    # plan: smallest power of two >= ceil(8192/N), capped at 8 and at J
+    want = -(-8192 // N)
     Sl = 1
     while Sl < want and Sl * 2 <= 8 and Sl * 2 <= J:
         Sl *= 2
