@@ -332,7 +332,8 @@ def run_ours(args, rank, world, dist):
         timed("rice_to_r4", [lambda it=it: dgt.load_r4_into(it["d2"], it["r4a"], stream=stream) for it in items])
         timed("f1_to_r4", [lambda it=it: dgt.load_r4_into(it["d1"], it["r4b"], stream=stream) for it in items])
         timed("r4_to_bf16", [lambda it=it: dgt.r4_to_bf16(it["r4a"], out=it["wbf"], stream=stream) for it in items])
-        # the weights were written by earlier ops and are only read here
+        # the weights were written by earlier ops, separated from these
+        # launches by the events between op groups, and are only read here
         timed("gemv_r4", [lambda it=it: dgt.gemv(it["r4a"], it["x"], it["y16"], it["y32"], stream=stream,
                                                 static_weights=True) for it in items])
         timed("gemv_bf16", [lambda it=it: dgt.gemv_bf16(it["wbf"], it["x"], it["b16"], it["b32"], stream=stream,

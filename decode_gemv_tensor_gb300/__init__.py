@@ -524,6 +524,9 @@ class DecodeStep:
         self.m = b16(dims["gate"])
         self.out = b16(hidden)
         self._graph = None
+        # the step streams its weights before each product's dependency wait
+        # (DGT_GEMV_STATIC_WEIGHTS): everything that wrote them must be done
+        torch.cuda.synchronize(dev)
 
     def _gemv(self, W, x, p, stream):
         # the step's weights are only read: they stream while the previous kernel ends

@@ -267,11 +267,14 @@ int dgt_gemv_bf16(const uint16_t *d_W, uint64_t rows, uint64_t cols, const uint1
  * while the previous kernel of the stream finishes, and reads x, writes y and
  * the status word only after that kernel has completed (its writes visible).
  * By default it also reads W only after then.  DGT_GEMV_STATIC_WEIGHTS
- * promises that no kernel still running when this one is launched writes W
- * (true for weights loaded earlier and only read since, as in a decode loop):
- * the weights then start streaming into shared memory at once, overlapping
- * the previous kernel's tail.  Results are the same either way.  Other
- * flags: DGT_ERR_ARG.
+ * promises that no work queued before this call that may still be running
+ * writes W: W was written before the stream last synchronised with the host
+ * or waited on an event recorded after the writes (true for weights loaded
+ * once and only read since, as in a decode loop).  Kernels of this library
+ * start their setup while earlier kernels finish, so without that promise a
+ * chain of them could overlap a write to W.  With it, the weights start
+ * streaming into shared memory at once, overlapping the previous kernel's
+ * tail.  Results are the same either way.  Other flags: DGT_ERR_ARG.
  */
 #define DGT_GEMV_STATIC_WEIGHTS 1u
 int dgt_gemv_ex(const dgt_r4 *W, const uint16_t *d_x, uint16_t *d_y, float *d_y32, int32_t *d_status,

@@ -125,3 +125,33 @@ def test_gemv_model_projections_sampled(dgt, model):
         rows = np.unique(np.concatenate([[0, N - 1], g.choice(N, 62, replace=False)]))
         r32, r16 = oracle.gemv(w, x, rows=rows)
         assert _eq32(y32[rows], r32) and np.array_equal(y16[rows], r16), name
+
+
+def test_gemv_static_weights_flag_and_chained_launches(dgt):
+    # back-to-back products on the stream (each may start while the previous
+    # one finishes), chained through their outputs (the next x is the
+    # previous y), with and without DGT_GEMV_STATIC_WEIGHTS (the weights are
+    # loaded and synchronised first): every result equals the oracle's; an
+    # unknown flag is rejected
+    N = K = 1024
+    ws = [S.weights(N, K, (205, i, 0, 0), outliers=True) for i in range(3)]
+    r4s = [dgt.load_r4(dgt.upload(dgt.pack(w, 2))) for w in ws]
+    torch.cuda.synchronize()
+    x0 = S.activations(K, (205, 999, 0))
+    for static in (False, True):
+        x = _dev_bf16(x0)
+        outs = []
+        for i in range(6):
+            y16, _ = dgt.gemv(r4s[i % 3], x, static_weights=static)
+            outs.append(y16)
+            x = y16
+        torch.cuda.synchronize()
+        xh = x0
+        for i in range(6):
+            r32, r16 = oracle.gemv(ws[i % 3], xh)
+            assert np.array_equal(_host(outs[i]), r16), (static, i)
+            xh = r16
+    y = torch.empty(N, dtype=torch.bfloat16, device="cuda")
+    assert dgt.lib().dgt_gemv_ex(dgt.C.byref(r4s[0].s), x.data_ptr(), y.data_ptr(), None, None, 2, None) == -1
+    assert dgt.lib().dgt_gemv_bf16_ex(_dev_bf16(ws[0]).data_ptr(), N, K, x.data_ptr(), y.data_ptr(), None, None,
+                                      4, None) == -1
