@@ -104,6 +104,7 @@ def lib():
             "dgt_add_rmsnorm": (i32, [vp, vp, vp, u64, C.c_float, vp, vp]),
             "dgt_silu_mul": (i32, [vp, vp, u64, vp, vp]),
             "dgt_repeat": (i32, [vp, u64, u64, vp, vp]),
+            "dgt_weighted_sum": (i32, [vp, vp, C.c_uint32, u64, vp, vp]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -288,6 +289,16 @@ class R4:
                                            C.byref(self.s)), "dgt_r4_init_from_view")
         self.rows, self.cols = v.rows, v.cols
         self.n_esc = v.n_esc15
+
+    def clone(self) -> "R4":
+        """A copy in new device buffers (device-to-device copies)."""
+        c = R4.__new__(R4)
+        c.sm, c.nib, c.esc, c.seg = self.sm.clone(), self.nib.clone(), self.esc.clone(), self.seg.clone()
+        c.dev = None
+        c.s = R4Struct.from_buffer_copy(self.s)
+        c.s.sm, c.s.nib, c.s.esc, c.s.seg = c.sm.data_ptr(), c.nib.data_ptr(), c.esc.data_ptr(), c.seg.data_ptr()
+        c.rows, c.cols, c.n_esc = self.rows, self.cols, self.n_esc
+        return c
 
 
 def load_r4(dev: DevicePacked, status=None, stream=None) -> R4:
@@ -567,6 +578,121 @@ class DecodeStep:
     def capture(self):
         """Capture launch() in a CUDA graph (run the step once eagerly first);
         replay() then runs the step on the current contents of self.x."""
+        import torch
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(g, stream=s):
+                self.launch(s)
+        torch.cuda.current_stream().wait_stream(s)
+        self._graph = g
+        return g
+
+    def replay(self, x0=None):
+        if x0 is not None:
+            self.x.copy_(x0)
+        self._graph.replay()
+        return self.x, self.out
+
+
+def weighted_sum(y32, p, out=None, stream=None):
+    """dgt_weighted_sum: out = sum over slots j of p[j] * y32[j] (fmaf chain in
+    slot order from +0); y32 float32 [slots, n], p float32 [slots]."""
+    import torch
+    slots = p.numel()
+    n = y32.numel() // slots
+    if out is None:
+        out = torch.empty(n, dtype=torch.float32, device=y32.device)
+    _check(lib().dgt_weighted_sum(_ptr(y32), _ptr(p), slots, n, _ptr(out), _stream(stream)), "dgt_weighted_sum")
+    return out
+
+
+class MoeDecodeStep:
+    """A batch-1 decode step through a stack of mixture-of-experts decoder
+    layers, every op a kernel of this library.  Per layer, with the fp32
+    residual stream x and the layer's routing (expert ids[j], weights p[j],
+    j < topk):
+
+        h = rmsnorm(x, g1);  q, k, v = W h;  a = repeat(v, rows of Wq);  x += Wo a
+        h = rmsnorm(x, g2);  for every slot j (one gather each):
+            m_j = silu(Wgate[ids[j]] h) * (Wup[ids[j]] h);  d_j = Wdown[ids[j]] m_j
+        x += sum_j p[j] d_j   (slot order)
+
+    and a final rmsnorm.  Wgate, Wup ([E * ffn, hidden]) and Wdown
+    ([E * hidden, ffn]) stack the experts; the gate and up gathers take the
+    token's h once for all its slots, the down gather takes slot j's m_j as
+    its own input.  Routing is an input (the router is not part of the
+    format).  layers: dicts with q, k, v, o, gate, up, down (R4, or bf16
+    tensors for the twin); routes: per layer (ids int32 [topk], p float32
+    [topk]) on the device; layer l uses layers[l % len] and routes[l % len].
+    The R4 step and the BF16 step give bit-identical outputs."""
+
+    def __init__(self, layers, gammas, routes, n_experts, depth=None, eps=1e-5):
+        import torch
+        self.layers, self.gammas, self.routes, self.E, self.eps = layers, gammas, routes, n_experts, eps
+        self.depth = depth or len(layers)
+        w0 = layers[0]
+        self.r4 = isinstance(w0["q"], R4)
+        shape = (lambda w: (w.rows, w.cols)) if self.r4 else (lambda w: tuple(w.shape))
+        hidden = shape(w0["q"])[1]
+        ffn = shape(w0["gate"])[0] // n_experts
+        topk = routes[0][0].numel()
+        dev = w0["q"].sm.device if self.r4 else w0["q"].device
+        self.hidden, self.ffn, self.topk = hidden, ffn, topk
+        f32 = lambda *s: torch.empty(s, dtype=torch.float32, device=dev)
+        b16 = lambda *s: torch.empty(s, dtype=torch.bfloat16, device=dev)
+        self.x, self.h, self.out = f32(hidden), b16(hidden), b16(hidden)
+        self.y = {p: (b16(shape(w0[p])[0]), f32(shape(w0[p])[0])) for p in ("q", "k", "v", "o")}
+        self.a = b16(shape(w0["q"])[0])
+        self.yg, self.yu = f32(1, topk, ffn), f32(1, topk, ffn)
+        self.m = b16(topk, ffn)
+        self.yd = f32(topk, 1, hidden)
+        self.comb = f32(hidden)
+        nb_up = moe_workspace_bytes(n_experts, ffn, hidden, 1, topk)
+        nb_dn = moe_workspace_bytes(n_experts, hidden, ffn, topk, 1)
+        self.ws_g = torch.empty(max(nb_up, 256), dtype=torch.uint8, device=dev)
+        self.ws_u = torch.empty(max(nb_up, 256), dtype=torch.uint8, device=dev)
+        self.ws_d = torch.empty(max(nb_dn, 256), dtype=torch.uint8, device=dev)
+        self._graph = None
+        torch.cuda.synchronize(dev)     # the products stream weights before their dependency wait
+
+    def _gemv(self, W, x, p, stream):
+        y, y32 = self.y[p]
+        if self.r4:
+            gemv(W, x, y, y32, stream=stream, static_weights=True)
+        else:
+            gemv_bf16(W, x, y, y32, stream=stream, static_weights=True)
+
+    def _moe(self, W, ids, x, ws, y32, stream):
+        f = moe_gemv if self.r4 else moe_gemv_bf16
+        f(W, self.E, ids, None, x, ws=ws, y32=y32, stream=stream)
+
+    def launch(self, stream=None):
+        ng = len(self.gammas) - 1
+        for l in range(self.depth):
+            W = self.layers[l % len(self.layers)]
+            ids, p = self.routes[l % len(self.routes)]
+            add_rmsnorm(self.x, self.gammas[(2 * l) % ng], self.eps, self.h, None if l == 0 else self.comb, stream)
+            for pr in ("q", "k", "v"):
+                self._gemv(W[pr], self.h, pr, stream)
+            repeat(self.y["v"][0], self.a.numel(), self.a, stream)
+            self._gemv(W["o"], self.a, "o", stream)
+            add_rmsnorm(self.x, self.gammas[(2 * l + 1) % ng], self.eps, self.h, self.y["o"][1], stream)
+            ids1 = ids.view(1, self.topk)
+            self._moe(W["gate"], ids1, self.h.view(1, -1), self.ws_g, self.yg, stream)
+            self._moe(W["up"], ids1, self.h.view(1, -1), self.ws_u, self.yu, stream)
+            silu_mul(self.yg, self.yu, self.m.view(-1), stream)
+            self._moe(W["down"], ids.view(self.topk, 1), self.m, self.ws_d, self.yd, stream)
+            weighted_sum(self.yd, p, self.comb, stream)
+        add_rmsnorm(self.x, self.gammas[-1], self.eps, self.out, self.comb, stream)
+
+    def __call__(self, x0, stream=None):
+        self.x.copy_(x0)
+        self.launch(stream)
+        return self.x, self.out
+
+    def capture(self):
         import torch
         g = torch.cuda.CUDAGraph()
         s = torch.cuda.Stream()

@@ -79,6 +79,19 @@ __global__ void __launch_bounds__(256) k_repeat(const uint16_t *__restrict__ v, 
         out[i] = v[i % n_in];
 }
 
+// out[i] = fmaf(p[S-1], y[S-1][i], ... fmaf(p[0], y[0][i], +0)): the routed
+// experts' outputs combined in slot order.
+__global__ void __launch_bounds__(256) k_weighted_sum(const float *__restrict__ y, const float *__restrict__ p,
+                                                     uint32_t slots, uint64_t n, float *__restrict__ out) {
+    pdl_trigger();
+    pdl_wait();
+    for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (uint64_t)gridDim.x * blockDim.x) {
+        float acc = 0.0f;
+        for (uint32_t j = 0; j < slots; j++) acc = fmaf(p[j], y[(uint64_t)j * n + i], acc);
+        out[i] = acc;
+    }
+}
+
 static unsigned elem_grid(uint64_t n) {
     DeviceInfo di;
     const int sms = device_info(&di) == DGT_OK ? di.sms : 132;
@@ -116,6 +129,17 @@ extern "C" int dgt_repeat(const uint16_t *d_v, uint64_t n_in, uint64_t n_out, ui
     if (n_out == 0) return DGT_OK;
     if (n_in == 0) return DGT_ERR_SHAPE;
     return launch_pdl(k_repeat, dim3(elem_grid(n_out)), dim3(256), 0, (cudaStream_t)stream, d_v, n_in, n_out,
+                      d_out) == cudaSuccess
+               ? DGT_OK
+               : DGT_ERR_CUDA;
+}
+
+extern "C" int dgt_weighted_sum(const float *d_y, const float *d_p, uint32_t slots, uint64_t n, float *d_out,
+                                void *stream) {
+    if (!d_y || !d_p || !d_out) return DGT_ERR_ARG;
+    if (n == 0) return DGT_OK;
+    if (slots == 0) return DGT_ERR_SHAPE;
+    return launch_pdl(k_weighted_sum, dim3(elem_grid(n)), dim3(256), 0, (cudaStream_t)stream, d_y, d_p, slots, n,
                       d_out) == cudaSuccess
                ? DGT_OK
                : DGT_ERR_CUDA;

@@ -400,11 +400,18 @@ int dgt_moe_gemv_noalloc(const dgt_r4 *W, uint32_t n_experts, const int32_t *d_i
  * dgt_repeat: out[i] = v[i mod n_in] for i < n_out (bf16 bits): the grouped
  * query heads' copy of a key/value-sized vector.  n_in == 0 with n_out > 0 is
  * DGT_ERR_SHAPE.
+ *
+ * dgt_weighted_sum: out[i] = fmaf(p[S-1], y[S-1][i], ... fmaf(p[0], y[0][i],
+ * +0)) with S = slots: the routed experts' outputs of one token combined in
+ * slot order (the combine of dgt_moe_gemv, for outputs computed per slot).
+ * d_y: float [slots, n]; d_p: float [slots]; d_out: float [n].  slots == 0
+ * with n > 0 is DGT_ERR_SHAPE.
  */
 int dgt_add_rmsnorm(float *d_x, const float *d_y, const uint16_t *d_gamma, uint64_t n, float eps, uint16_t *d_h,
                     void *stream);
 int dgt_silu_mul(const float *d_g, const float *d_u, uint64_t n, uint16_t *d_out, void *stream);
 int dgt_repeat(const uint16_t *d_v, uint64_t n_in, uint64_t n_out, uint16_t *d_out, void *stream);
+int dgt_weighted_sum(const float *d_y, const float *d_p, uint32_t slots, uint64_t n, float *d_out, void *stream);
 
 #ifdef __cplusplus
 }

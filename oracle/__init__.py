@@ -442,3 +442,41 @@ def decode_step_f64(layers, gammas, x0, depth=None, eps: float = 1e-5):
         x = x + Wl["down"] @ m
     return x, f64_to_bf16(rmsnorm_eps_f64(x, gammas[-1], eps))
 
+
+
+def decode_step_moe_f64(layers, gammas, routes, n_experts: int, x0, depth=None, eps: float = 1e-5):
+    """The batch-1 decode step of mixture-of-experts layers in fp64 (products
+    by matmul), rounding to bf16 where the products take bf16 inputs:
+
+        h = bf16(rmsnorm(x, g1)); v = Wv h; a = bf16(v) repeated to Wq's rows;
+        x = x + Wo a; h = bf16(rmsnorm(x, g2));
+        for each slot j with expert e = ids[j]:
+            m_j = bf16(silu(Wgate[e] h) * (Wup[e] h)); d_j = Wdown[e] m_j
+        x = x + sum_j p[j] d_j
+
+    then out = bf16(rmsnorm(x, g_final)).  Wgate/Wup stack the experts as
+    [E * ffn, hidden], Wdown as [E * hidden, ffn]; routes[l] = (ids, p).
+    Layer l uses layers[l % len], routes[l % len] and gammas 2l, 2l + 1 (mod
+    2 len).  Returns (x, out bits)."""
+    depth = depth or len(layers)
+    x = np.asarray(x0, np.float64).copy()
+    nl = len(layers)
+    W = [{p: bf16_to_f64(np.asarray(L[p], np.uint16)) for p in L} for L in layers]
+    for l in range(depth):
+        Wl = W[l % nl]
+        ids, pw = routes[l % len(routes)]
+        ffn = Wl["gate"].shape[0] // n_experts
+        hid = Wl["down"].shape[0] // n_experts
+        h = bf16_to_f64(f64_to_bf16(rmsnorm_eps_f64(x, gammas[(2 * l) % (2 * nl)], eps)))
+        v = Wl["v"] @ h
+        a = bf16_to_f64(f64_to_bf16(v))[np.arange(Wl["q"].shape[0]) % v.size]
+        x = x + Wl["o"] @ a
+        h = bf16_to_f64(f64_to_bf16(rmsnorm_eps_f64(x, gammas[(2 * l + 1) % (2 * nl)], eps)))
+        comb = np.zeros_like(x)
+        for e, pj in zip(np.asarray(ids).ravel(), np.asarray(pw, np.float64).ravel()):
+            g = Wl["gate"][e * ffn:(e + 1) * ffn] @ h
+            u = Wl["up"][e * ffn:(e + 1) * ffn] @ h
+            m = bf16_to_f64(f64_to_bf16(silu_mul_f64(g, u)))
+            comb = comb + pj * (Wl["down"][e * hid:(e + 1) * hid] @ m)
+        x = x + comb
+    return x, f64_to_bf16(rmsnorm_eps_f64(x, gammas[-1], eps))

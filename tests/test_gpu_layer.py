@@ -1,7 +1,8 @@
 """GPU parity for the decoder-layer glue (residual add + RMS norm, SiLU * up,
-grouped-query repeat) against the fp64 oracle, and for the batch-1 decode
-step: R4 and BF16 weights give bit-identical steps, eager and graph replay
-agree, and the step is within a normwise bound of the fp64 oracle."""
+grouped-query repeat, slot-order weighted sum) against the fp64 oracle, and
+for the batch-1 decode steps (dense and mixture-of-experts layers): R4 and
+BF16 weights give bit-identical steps, eager and graph replay agree, and the
+step is within a normwise bound of the fp64 oracle."""
 import numpy as np
 import pytest
 
@@ -144,3 +145,66 @@ def test_decode_step_3b_layer_shapes(dgt):
     sb.capture()
     xg, hg = sb.replay(x0d)
     assert torch.equal(xg.view(torch.int32), xr.view(torch.int32))
+
+
+def test_weighted_sum_matches_oracle(dgt):
+    g = np.random.default_rng(607)
+    for slots, n in ((1, 5), (8, 2816), (3, 10001)):
+        y = g.normal(size=(slots, n)).astype(np.float32)
+        p = np.abs(g.normal(size=slots)).astype(np.float32)
+        out = dgt.weighted_sum(torch.from_numpy(y).cuda(), torch.from_numpy(p).cuda()).cpu().numpy()
+        ref = (p.astype(np.float64)[:, None] * y.astype(np.float64)).sum(0)
+        scale = (np.abs(p.astype(np.float64)[:, None] * y)).sum(0)
+        assert np.all(np.abs(out - ref) <= 1e-6 * scale + 1e-30)
+    # one slot of weight 1 copies its row exactly
+    y = torch.from_numpy(g.normal(size=(1, 777)).astype(np.float32)).cuda()
+    out = dgt.weighted_sum(y, torch.ones(1, device="cuda"))
+    assert torch.equal(out.view(torch.int32), y[0].view(torch.int32))
+
+
+def _moe_layers(hid, kv, ffn, E, count, seed):
+    shapes = {"q": (hid, hid), "k": (kv, hid), "v": (kv, hid), "o": (hid, hid), "gate": (E * ffn, hid),
+              "up": (E * ffn, hid), "down": (E * hid, ffn)}
+    return [{p: S.weights(*shp, (seed, l, i, 0), outliers=True) for i, (p, shp) in enumerate(shapes.items())}
+            for l in range(count)]
+
+
+@pytest.mark.parametrize("hid,kv,ffn,E,topk,nl,depth", [(512, 128, 256, 8, 4, 2, 3), (1024, 256, 704, 16, 8, 1, 2)])
+def test_moe_decode_step_twins_graph_and_oracle(dgt, hid, kv, ffn, E, topk, nl, depth):
+    host = _moe_layers(hid, kv, ffn, E, nl, 608)
+    gam = _gammas(hid, nl, 609)
+    r4, bf, gd = _build(dgt, host, gam)
+    routes_h = []
+    for l in range(nl):
+        ids, p = S.routing(1, E, topk, (610, 777, l, 0))
+        routes_h.append((ids.reshape(-1), p.reshape(-1)))
+    routes = [(torch.from_numpy(i.astype(np.int32)).cuda(), torch.from_numpy(p.astype(np.float32)).cuda())
+              for i, p in routes_h]
+    x0 = np.random.default_rng(611).normal(size=hid).astype(np.float32)
+    x0d = torch.from_numpy(x0).cuda()
+    sr = dgt.MoeDecodeStep(r4, gd, routes, E, depth=depth)
+    sb = dgt.MoeDecodeStep(bf, gd, routes, E, depth=depth)
+    xr, hr = (t.clone() for t in sr(x0d))
+    xb, hb = (t.clone() for t in sb(x0d))
+    assert torch.equal(xr.view(torch.int32), xb.view(torch.int32))     # R4 step == BF16 step, bit for bit
+    assert torch.equal(hr.view(torch.int16), hb.view(torch.int16))
+    sr.capture()
+    xg, hg = sr.replay(x0d)
+    assert torch.equal(xg.view(torch.int32), xr.view(torch.int32))     # graph == eager
+    assert torch.equal(hg.view(torch.int16), hr.view(torch.int16))
+    xo, ho = oracle.decode_step_moe_f64(host, gam, routes_h, E, x0, depth=depth)
+    xr = xr.cpu().numpy()
+    assert np.linalg.norm(xr - xo) / np.linalg.norm(xo) <= 1e-2
+    ref = oracle.bf16_to_f64(ho)
+    assert np.linalg.norm(oracle.bf16_to_f64(_bits(hr)) - ref) / np.linalg.norm(ref) <= 2e-2
+
+
+def test_r4_clone_is_independent(dgt):
+    w = S.weights(64, 1024, (612, 0, 0, 0), outliers=True)
+    r4 = dgt.load_r4(dgt.upload(dgt.pack(w, 2)))
+    c = r4.clone()
+    x = _dev_bf16(S.activations(1024, (612, 999, 0)))
+    y0, _ = dgt.gemv(r4, x)
+    r4.nib.zero_()
+    y1, _ = dgt.gemv(c, x)
+    assert torch.equal(y0.view(torch.int16), y1.view(torch.int16))

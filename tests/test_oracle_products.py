@@ -267,3 +267,25 @@ def test_decode_step_f64_identity_attention_path():
     x, _ = oracle.decode_step_f64([L], gam, x0)
     h = oracle.bf16_to_f64(oracle.f64_to_bf16(oracle.rmsnorm_eps_f64(x0, gam[0], 1e-5)))
     assert np.allclose(x, x0 + h[np.arange(hid) % kv], rtol=0, atol=1e-15)
+
+
+def test_decode_step_moe_f64_one_expert_equals_dense_step():
+    # one expert routed with weight 1 at every slot position is the dense
+    # step with that expert's MLP; with weights summing to 1 over copies of
+    # the same expert the result is the same
+    hid, kv, ffn, E = 8, 4, 6, 3
+    L = _tiny_layer(hid, kv, ffn, 11)
+    g = np.random.default_rng(12)
+    others = {p: _bf16(g.normal(scale=0.2, size=shp)) for p, shp in (("gate", (ffn, hid)), ("up", (ffn, hid)),
+                                                                     ("down", (hid, ffn)))}
+    M = dict(L)
+    M["gate"] = np.concatenate([others["gate"], L["gate"], others["gate"]])
+    M["up"] = np.concatenate([others["up"], L["up"], others["up"]])
+    M["down"] = np.concatenate([others["down"], L["down"], others["down"]])
+    gam = [_bf16(1 + 0.1 * g.normal(size=hid)) for _ in range(3)]
+    x0 = g.normal(size=hid)
+    xd, od = oracle.decode_step_f64([L], gam, x0)
+    xm, om = oracle.decode_step_moe_f64([M], gam, [(np.array([1]), np.array([1.0]))], E, x0)
+    assert np.allclose(xm, xd, rtol=0, atol=1e-14) and np.array_equal(om, od)
+    xh, _ = oracle.decode_step_moe_f64([M], gam, [(np.array([1, 1]), np.array([0.25, 0.75]))], E, x0)
+    assert np.allclose(xh, xd, rtol=0, atol=1e-14)
