@@ -13,7 +13,8 @@ every device row of the path:
 The GEMM at 128 and 2048 rows is tensor-bound and is reported separately
 ("gemm_tensor", TFLOP/s against the measured bf16 peak), and so is a whole
 batch-1 decode step through the dense-3B layer stack in a CUDA graph
-("decode_step": per-token time with R4 weights against BF16).
+("decode_step": per-token time with R4 weights against BF16) and through the
+moe-30L-128E stack ("decode_step_moe").
 Between a kernel's reuses of one tensor's data the other tensors and kernels
 move far more than the 129 MB L2, so no explicit flush is needed.
 
@@ -417,6 +418,7 @@ def run_ours(args, rank, world, dist):
     # ---- prompt GEMM at 128 and 2048 rows (tensor-bound), outside the timed step
     extras = gemm_extras(dgt, torch, dev) if rank == 0 else None
     dstep = decode_step_extras(dgt, torch, dev) if rank == 0 and not args.no_decode_step else None
+    mstep = moe_decode_step_extras(dgt, torch, dev) if rank == 0 and not args.no_decode_step else None
 
     # ---- end to end through the C ABI from pinned host buffers
     e2e = None
@@ -485,7 +487,7 @@ def run_ours(args, rank, world, dist):
                              "rice_to_r4_gsym_s": kern["rice_to_r4"]["gsym_s"],
                              "rice_to_r4_frac": kern["rice_to_r4"]["frac"],
                              "r4_vs_bf16_gemv_speedup": kern["gemv_bf16"]["ms_avg"] / kern["gemv_r4"]["ms_avg"]},
-                "kernels": kern, "roofline": roof, "gemm_tensor": extras, "decode_step": dstep, "cpu_baseline": cpu, "e2e": e2e,
+                "kernels": kern, "roofline": roof, "gemm_tensor": extras, "decode_step": dstep, "decode_step_moe": mstep, "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": launches_per_step * args.steps, "clocks": clk,
                 "gpu": torch.cuda.get_device_name(dev)}
         print(json.dumps(line), flush=True)
@@ -595,6 +597,80 @@ def decode_step_extras(dgt, torch, dev):
     out["r4_over_bf16_speed"] = res["bf16"]["us_per_token"] / res["r4"]["us_per_token"]
     out["r4_equals_bf16"] = bool(same)
     out["kernels_per_token"] = L * 11 + 1
+    return out
+
+
+def moe_decode_step_extras(dgt, torch, dev):
+    """Per-token time of a batch-1 decode step through the moe-30L-128E stack
+    (30 layers, top-8 of 128 experts; every layer its own weights in HBM), R4
+    against BF16, each step one CUDA graph (MoeDecodeStep).  Routing is drawn
+    per layer (distinct experts, softmax weights) and fixed for the timed
+    replays.  Weights: one N(0, 0.02) draw tiled to the stacked expert shapes,
+    packed once per projection and copied on the device for every layer
+    (separate allocations).  CUDA events around 10 replays after 3 warm-ups,
+    median."""
+    m = S.MOE
+    L, hid, E, topk = m["layers"], m["hidden"], m["experts"], m["topk"]
+    base = S.weights(8192, 3072, (7, 0, 0, 0)).reshape(-1)
+    shapes = {p: (r, c) for p, r, c in m["attn_proj"]}
+    (_, ne, ke), (_, _, _), (_, nd, kd) = m["expert_proj"]
+    shapes.update({"gate": (E * ne, ke), "up": (E * ne, ke), "down": (E * nd, kd)})
+    host = {p: np.resize(base, r * c).reshape(r, c) for p, (r, c) in shapes.items()}
+    first = {p: dgt.load_r4(dgt.upload(dgt.pack(w, 2), dev)) for p, w in host.items()}
+    del host, base
+    r4_layers = [first] + [{p: t.clone() for p, t in first.items()} for _ in range(L - 1)]
+    bf_layers = [{p: dgt.r4_to_bf16(t) for p, t in lr.items()} for lr in r4_layers]
+    routes_h = [S.routing(1, E, topk, (7, 777, l, 0)) for l in range(L)]
+    routes = [(torch.from_numpy(i.reshape(-1).astype(np.int32)).to(dev),
+               torch.from_numpy(p.reshape(-1).astype(np.float32)).to(dev)) for i, p in routes_h]
+    g = np.random.default_rng(8)
+    gam = [torch.from_numpy(S.f32_to_bf16_bits((1 + 0.1 * g.normal(size=hid)).astype(np.float32)).view(np.int16))
+           .to(dev).view(torch.bfloat16) for _ in range(2 * L + 1)]
+    x0 = torch.from_numpy(S.bf16_bits_to_f32(S.activations(hid, (7, 999, 0)))).to(dev)
+
+    def bytes_r4(t):
+        return t.sm.numel() + t.nib.numel() + t.n_esc + t.seg.numel() * 4
+    per_layer_w = {p: (t.rows * t.cols, bytes_r4(t)) for p, t in first.items()}
+    tok_w = tok_r4 = 0.0
+    for p, (nw, nb) in per_layer_w.items():
+        f = topk / E if p in ("gate", "up", "down") else 1.0
+        tok_w += f * nw
+        tok_r4 += f * nb
+    out = {"model": m["name"], "layers": L, "hidden": hid, "experts": E, "topk": topk, "batch": 1, "graph": True,
+           "attention": "not in the step (value vector repeated over the query heads)",
+           "routing": "drawn per layer, fixed over the replays", "weights_per_token": L * tok_w}
+    res = {}
+    for name, layers, nbytes in (("r4", r4_layers, L * tok_r4), ("bf16", bf_layers, L * tok_w * 2)):
+        st = dgt.MoeDecodeStep(layers, gam, routes, E, depth=L)
+        st(x0)
+        torch.cuda.synchronize()
+        ref = (st.x.clone(), st.out.clone())
+        st.capture()
+        for _ in range(3):
+            st.replay(x0)
+        evs = []
+        cur = torch.cuda.current_stream(dev)
+        for _ in range(10):
+            st.x.copy_(x0)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(cur)
+            st._graph.replay()
+            e1.record(cur)
+            evs.append((e0, e1))
+        torch.cuda.synchronize()
+        t = sorted(a.elapsed_time(b) for a, b in evs)[5]
+        assert torch.equal(st.x.view(torch.int32), ref[0].view(torch.int32))
+        res[name] = {"us_per_token": t * 1e3, "tokens_per_s": 1e3 / t, "weight_bytes_per_token": nbytes,
+                     "weight_gb_s": nbytes / (t / 1e3) / 1e9, "x": ref[0], "out": ref[1]}
+        del st
+    same = torch.equal(res["r4"]["x"].view(torch.int32), res["bf16"]["x"].view(torch.int32)) and \
+        torch.equal(res["r4"]["out"].view(torch.int16), res["bf16"]["out"].view(torch.int16))
+    for k in ("r4", "bf16"):
+        res[k].pop("x")
+        res[k].pop("out")
+    out.update(res)
+    out["r4_over_bf16_speed"] = res["bf16"]["us_per_token"] / res["r4"]["us_per_token"]
+    out["r4_equals_bf16"] = bool(same)
     return out
 
 
