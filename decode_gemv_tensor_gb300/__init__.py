@@ -105,6 +105,7 @@ def lib():
             "dgt_silu_mul": (i32, [vp, vp, u64, vp, vp]),
             "dgt_repeat": (i32, [vp, u64, u64, vp, vp]),
             "dgt_weighted_sum": (i32, [vp, vp, C.c_uint32, u64, vp, vp]),
+            "dgt_exponent_stats": (i32, [vp, u64, C.c_uint32, vp, vp, vp, vp]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -709,4 +710,24 @@ class MoeDecodeStep:
             self.x.copy_(x0)
         self._graph.replay()
         return self.x, self.out
+
+
+# ---------------------------------------------------------------------------
+# exponent statistics
+# ---------------------------------------------------------------------------
+def exponent_stats(w, tile=128, stream=None):
+    """dgt_exponent_stats on a device bf16 tensor (any shape, flat order):
+    returns (hist int64 [256], tile_bits float64 [tiles] (both on the device),
+    total tile bits, tensor exponent entropy in bits per weight)."""
+    import torch
+    n = w.numel()
+    dev = w.device
+    hist = torch.empty(256, dtype=torch.int64, device=dev)
+    # an invalid tile gets a 1-element buffer; the C call rejects it
+    tb = torch.empty(max((n + tile - 1) // tile, 1) if tile > 0 else 1, dtype=torch.float64, device=dev)
+    tot = torch.empty(2, dtype=torch.float64, device=dev)
+    _check(lib().dgt_exponent_stats(_ptr(w), n, tile, _ptr(hist), _ptr(tb), _ptr(tot), _stream(stream)),
+           "dgt_exponent_stats")
+    t = tot.cpu()
+    return hist, tb, float(t[0]), float(t[1])
 

@@ -413,6 +413,31 @@ int dgt_silu_mul(const float *d_g, const float *d_u, uint64_t n, uint16_t *d_out
 int dgt_repeat(const uint16_t *d_v, uint64_t n_in, uint64_t n_out, uint16_t *d_out, void *stream);
 int dgt_weighted_sum(const float *d_y, const float *d_p, uint32_t slots, uint64_t n, float *d_out, void *stream);
 
+/* ------------------------------------------------------------------------ */
+/* Exponent statistics                                                      */
+/* ------------------------------------------------------------------------ */
+/*
+ * Binade README, "How it works" ("No exponent locality": per-tile palettes
+ * gain only 0.011 to 0.027 bits per weight over a shuffled tensor) and its
+ * exponent-statistics scripts.  For a BF16 tensor of n weights (bits d_w,
+ * device, flat order) and a tile size T (1..65536; the last tile may be
+ * shorter):
+ *   d_hist[e] = number of weights with exponent e ((b >> 7) & 0xFF), e < 256
+ *     (device uint64 [256]; zeroed by the call);
+ *   d_tile_bits[t] = c_t * H_t with H_t = -sum_e (c_te / c_t) log2(c_te / c_t)
+ *     over tile t's own counts (c_t weights): the bits of coding the tile's
+ *     exponents with its own ideal table, side information not counted
+ *     (device double [ceil(n / T)]);
+ *   d_total_bits[0] = the sum of d_tile_bits in one fixed order, and
+ *   d_total_bits[1] = the tensor's exponent entropy -sum_e (h_e/n) log2(h_e/n)
+ *     in bits per weight (device double [2]).
+ * d_total_bits[0] / n against the same for a shuffled copy is the per-tile
+ * palette gain.  Asynchronous.  Errors:
+ * DGT_ERR_ARG (null), DGT_ERR_SHAPE (n == 0, T out of range), DGT_ERR_CUDA.
+ */
+int dgt_exponent_stats(const uint16_t *d_w, uint64_t n, uint32_t tile, uint64_t *d_hist, double *d_tile_bits,
+                       double *d_total_bits, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -5,8 +5,9 @@ bench's CPU-baseline leg may import this package.  It shares no code with the
 CUDA library (``decode_gemv_tensor_gb300``) and neither imports the other.
 
 The arithmetic lives in ``oracle.c`` (plain C, sequential, fp32 ``fmaf`` for the
-fixed-order products and fp64 for the prompt product); this module only
-marshals numpy arrays.  Pins that tie it to the pages and to mathematics are in
+fixed-order products and fp64 for the prompt product, the decoder-layer glue
+and the exponent statistics); this module marshals numpy arrays, and the
+decode-step references compose those functions with numpy matrix products.  Pins that tie it to the pages and to mathematics are in
 ``tests/test_oracle_*.py``.  Every function here is pinned; the one part whose
 bytes the pages do not fix (the on-disk bit layout) is pinned by hand-derived
 golden streams instead of by the pages.
@@ -80,6 +81,7 @@ def _L():
             "or_f64_to_bf16": (C.c_uint16, [C.c_double]),
             "or_rmsnorm_f64": (None, [f64p, u16p, u64, C.c_double, f64p]),
             "or_silu_mul_f64": (None, [f64p, f64p, u64, f64p]),
+            "or_exp_tile_bits": (None, [u16p, u64, C.c_uint32, f64p]),
         }
         for name, (res, args) in sig.items():
             f = getattr(lib, name)
@@ -480,3 +482,14 @@ def decode_step_moe_f64(layers, gammas, routes, n_experts: int, x0, depth=None, 
             comb = comb + pj * (Wl["down"][e * hid:(e + 1) * hid] @ m)
         x = x + comb
     return x, f64_to_bf16(rmsnorm_eps_f64(x, gammas[-1], eps))
+
+
+def exponent_tile_bits(b, tile: int):
+    """Per tile: (weights in the tile) x (entropy of the tile's own exponent
+    counts), in bits, flat order, the last tile possibly shorter."""
+    b = _c(b, np.uint16).ravel()
+    nt = -(-b.size // tile)
+    out = np.zeros(max(nt, 1), np.float64)
+    _L().or_exp_tile_bits(_p(b, C.c_uint16), b.size, tile, _p(out, C.c_double))
+    return out[:nt]
+

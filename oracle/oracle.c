@@ -590,3 +590,24 @@ void or_silu_mul_f64(const double *g, const double *u, uint64_t n, double *out) 
     for (uint64_t i = 0; i < n; i++) out[i] = g[i] / (1.0 + exp(-g[i])) * u[i];
 }
 
+
+/* ------------------------------------------------------------------------ */
+/* Exponent statistics, [B] "How it works" ("No exponent locality": per-tile */
+/* palettes against a shuffled tensor).  Tile t (c weights, the last one     */
+/* may be shorter) costs c * H_t bits, H_t the entropy of its own exponent   */
+/* counts: the ideal code with the tile's own table, side information not    */
+/* counted.                                                                  */
+/* ------------------------------------------------------------------------ */
+void or_exp_tile_bits(const uint16_t *b, uint64_t n, uint32_t tile, double *tile_bits) {
+    uint64_t ntiles = (n + tile - 1) / tile;
+    for (uint64_t t = 0; t < ntiles; t++) {
+        uint64_t cnt[256];
+        memset(cnt, 0, sizeof(cnt));
+        uint64_t lo = t * (uint64_t)tile, hi = lo + tile < n ? lo + tile : n;
+        for (uint64_t i = lo; i < hi; i++) cnt[(b[i] >> 7) & 0xFF]++;
+        double c = (double)(hi - lo), bits = 0.0;
+        for (int e = 0; e < 256; e++)
+            if (cnt[e]) bits -= (double)cnt[e] * log2((double)cnt[e] / c);
+        tile_bits[t] = bits;
+    }
+}

@@ -332,3 +332,47 @@ def test_corrupt_streams_are_rejected():
     seg[-1] += 1
     with pytest.raises(ValueError):
         oracle.r4_decode(r4["nib"], r4["esc"], seg, 8, 512)
+
+
+# ---------------------------------------------------------------------------
+# exponent statistics: per-tile entropy
+# ---------------------------------------------------------------------------
+def _with_exponents(es):
+    # bf16 bits with the given exponents (sign and mantissa arbitrary but fixed)
+    es = np.asarray(es, np.uint16)
+    return ((es << 7) | 0x15).astype(np.uint16)
+
+
+def test_exponent_tile_bits_closed_forms():
+    one = _with_exponents([120] * 128)
+    assert np.array_equal(oracle.exponent_tile_bits(one, 128), [0.0])
+    # 2^k exponents, equally often: k bits per weight
+    for k in (1, 2, 3, 7):
+        tile = 1 << 8
+        b = _with_exponents(np.tile(np.arange(100, 100 + (1 << k)), tile >> k))
+        assert np.isclose(oracle.exponent_tile_bits(b, tile)[0], tile * k, rtol=1e-14)
+    # a short last tile uses its own count; the sign and mantissa do not matter
+    b = np.concatenate([_with_exponents([1, 2] * 64), _with_exponents([5, 6, 7])])
+    b2 = b ^ 0x807F
+    t = oracle.exponent_tile_bits(b, 128)
+    assert np.allclose(t, [128.0, 3 * np.log2(3)], rtol=1e-14)
+    assert np.array_equal(t, oracle.exponent_tile_bits(b2, 128))
+
+
+def test_exponent_tile_bits_locality_and_shuffle():
+    # tiles that each hold one exponent cost nothing; shuffled they cost the
+    # tensor's entropy (approximately); an iid tensor gains nothing from tiles
+    # beyond sampling error
+    g = np.random.default_rng(21)
+    es = np.repeat(g.integers(110, 126, size=512), 128)
+    b = _with_exponents(es)
+    assert oracle.exponent_tile_bits(b, 128).sum() == 0.0
+    sh = b[g.permutation(b.size)]
+    counts = np.bincount(es, minlength=256)
+    H = oracle.entropy(counts)
+    per = oracle.exponent_tile_bits(sh, 128).sum() / b.size
+    assert H - 0.45 < per < H                          # per-tile estimates are biased low by a few tenths
+    w = S.weights(256, 1024, (22, 0, 0, 0))
+    a = oracle.exponent_tile_bits(w, 128).sum() / w.size
+    s2 = oracle.exponent_tile_bits(w.ravel()[g.permutation(w.size)], 128).sum() / w.size
+    assert abs(a - s2) < 0.01
