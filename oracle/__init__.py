@@ -72,6 +72,7 @@ def _L():
             "or_r4_nseg": (u64, [u64]),
             "or_r4_encode": (u64, [u8p, u64, u64, u8p, u8p, u32p]),
             "or_r4_decode": (C.c_int, [u8p, u8p, u32p, u64, u64, u64, u8p]),
+            "or_r4_round_summary": (C.c_int, [u8p, u8p, u32p, u8p, u64, u64, u64, u32p]),
             "or_gemv_slices": (C.c_int, [u64, u64]),
             "or_gemv": (None, [u16p, u64, u64, u16p, u64p, u64, f32p, u16p]),
             "or_gemv_one": (C.c_float, [u16p, u64, u64, u16p]),
@@ -261,6 +262,26 @@ def r4_decode(nib, esc, seg, rows: int, cols: int):
     if rc != 0:
         raise ValueError("corrupt R4 tensor")
     return out[:n]
+
+
+def r4_round_summary(nib, esc, seg, table, rows: int, cols: int):
+    """Per (row, 512-column round): escapes in the round (counted in the
+    nibbles, capped at 255) | exponents of its first three escapes << 8, 16, 24."""
+    nib = _c(nib, np.uint8)
+    esc = _c(esc, np.uint8)
+    ne = esc.size
+    if nib.size == 0:
+        nib = np.zeros(1, np.uint8)
+    if esc.size == 0:
+        esc = np.zeros(1, np.uint8)
+    seg = _c(seg, np.uint32)
+    table = np.zeros(256, np.uint8) if table is None else np.resize(_c(table, np.uint8), 256)
+    out = np.zeros(max(rows * r4_nseg(cols), 1), np.uint32)
+    rc = _L().or_r4_round_summary(_p(nib, C.c_uint8), _p(esc, C.c_uint8), _p(seg, C.c_uint32),
+                                  _p(table, C.c_uint8), rows, cols, ne, _p(out, C.c_uint32))
+    if rc != 0:
+        raise ValueError("corrupt R4 tensor")
+    return out[:rows * r4_nseg(cols)]
 
 
 # --------------------------------------------------------------------------

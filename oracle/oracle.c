@@ -436,6 +436,37 @@ int or_r4_decode(const uint8_t *nib, const uint8_t *esc, const uint32_t *seg,
     return 0;
 }
 
+/* Per-round escape summary of the R4 layout (the row-segment index, as the   */
+/* product kernels read it): for row r and 512-column round j, the number of */
+/* escaped elements c (15-nibbles among the round's columns, counted in the   */
+/* nibbles themselves) and the exponents table[rank] of its first three      */
+/* escapes in column order.  Word = min(c, 255) | x0 << 8 | x1 << 16 |       */
+/* x2 << 24, absent escapes 0.  The ranks are taken from esc starting at     */
+/* seg[r*nseg + j].  out: rows*nseg words.  Returns 0 or -1 (index out of    */
+/* range).                                                                    */
+int or_r4_round_summary(const uint8_t *nib, const uint8_t *esc, const uint32_t *seg,
+                        const uint8_t *table, uint64_t rows, uint64_t cols, uint64_t n_esc,
+                        uint32_t *out) {
+    uint64_t nseg = or_r4_nseg(cols);
+    for (uint64_t r = 0; r < rows; r++) {
+        for (uint64_t j = 0; j < nseg; j++) {
+            uint64_t e = seg[r * nseg + j];
+            uint32_t c = 0, x[3] = {0, 0, 0};
+            for (uint64_t col = j * OR_SEG; col < cols && col < (j + 1) * OR_SEG; col++) {
+                uint64_t i = r * cols + col;
+                if (((nib[i >> 1] >> (4 * (i & 1))) & 0xF) != 15) continue;
+                if (c < 3) {
+                    if (e + c >= n_esc) return -1;
+                    x[c] = table[esc[e + c]];
+                }
+                c++;
+            }
+            out[r * nseg + j] = (c < 255 ? c : 255) | x[0] << 8 | x[1] << 16 | x[2] << 24;
+        }
+    }
+    return 0;
+}
+
 /* ------------------------------------------------------------------------ */
 /* Fixed summation order of the batch-1 product y = W x.                     */
 /* [B] "Exactness": the compressed and the BF16 kernels add the products in  */

@@ -275,6 +275,56 @@ def test_r4_layout_independent_restatement(rows, cols):
     assert np.array_equal(oracle.r4_decode(nib, r4["esc"], r4["seg"], rows, cols), rk)
 
 
+def _summary_from_weights(w, rank_of):
+    # straight from the weights: an element is escaped when the rank of its
+    # exponent is 15 or more; the summary lists the exponents themselves
+    rows, cols = w.shape
+    ex = ((w >> 7) & 0xFF).astype(np.int64)
+    esc = rank_of[ex] >= 15
+    out = []
+    for r in range(rows):
+        for j in range(-(-cols // 512)):
+            xs = ex[r, j * 512:(j + 1) * 512][esc[r, j * 512:(j + 1) * 512]]
+            word = min(xs.size, 255)
+            for q in range(min(xs.size, 3)):
+                word |= int(xs[q]) << (8 + 8 * q)
+            out.append(word)
+    return np.array(out, np.uint32)
+
+
+@pytest.mark.parametrize("rows,cols", [(1, 1), (3, 5), (2, 511), (4, 513), (7, 1024), (33, 1537)])
+def test_r4_round_summary_matches_the_weights(rows, cols):
+    w = S.weights(rows, cols, (32, rows, cols, 0), outliers=True)
+    w.ravel()[::7] = np.arange(w.ravel()[::7].size, dtype=np.uint16) * 0x0080 + 0x0101
+    rt = oracle.rank_table(w)
+    rk = oracle.ranks(w, rt["rank_of"])
+    r4 = oracle.r4_encode(rk, rows, cols)
+    got = oracle.r4_round_summary(r4["nib"], r4["esc"], r4["seg"], rt["table"], rows, cols)
+    want = _summary_from_weights(w, rt["rank_of"])
+    assert np.array_equal(got, want)
+    assert (got & 0xFF).max() >= 3 if rows * cols >= 512 else True
+
+
+def test_r4_round_summary_count_saturates():
+    # round 0 holds 300 weights of 100 rare exponents (three each): more than
+    # 255 escapes, so the count saturates; round 1 holds none
+    g = np.random.default_rng(33)
+    common = np.arange(100, 115)      # ranks 0..14: no escapes
+    w = np.zeros((1, 1024), np.uint16)
+    rare = np.repeat(np.arange(1, 101), 3)
+    ex0 = np.concatenate([rare, np.resize(common, 212)])
+    g.shuffle(ex0)
+    ex1 = np.resize(common, 512)
+    ex = np.concatenate([ex0, ex1]).astype(np.uint16)
+    w[0] = (ex << 7) | g.integers(0, 256, 1024).astype(np.uint16) & 0x807F
+    rt = oracle.rank_table(w)
+    rk = oracle.ranks(w, rt["rank_of"])
+    r4 = oracle.r4_encode(rk, 1, 1024)
+    got = oracle.r4_round_summary(r4["nib"], r4["esc"], r4["seg"], rt["table"], 1, 1024)
+    assert got[0] & 0xFF == 255 and got[1] == 0
+    assert np.array_equal(got, _summary_from_weights(w, rt["rank_of"]))
+
+
 def test_r4_bits_per_weight_near_pages():
     w = S.weights(1024, 1024, (1, 0, 0, 0), outliers=True)
     d = oracle.pack(w, 2)
