@@ -80,6 +80,7 @@ def lib():
                                C.POINTER(i32)]),
             "dgt_read_free": (None, [C.POINTER(vp), C.POINTER(C.c_char_p), i32]),
             "dgt_r4_nseg": (u64, [u64]),
+            "dgt_r4_rsum_offset": (u64, [u64, u64]),
             "dgt_r4_sizes": (i32, [u64, u64, u64, C.POINTER(u64), C.POINTER(u64), C.POINTER(u64)]),
             "dgt_r4_init_from_view": (i32, [C.POINTER(PackedView), vp, vp, vp, C.POINTER(R4Struct)]),
             "dgt_load_r4": (i32, [C.POINTER(PackedView), C.POINTER(R4Struct), vp, vp]),
@@ -300,6 +301,12 @@ class R4:
         c.s.sm, c.s.nib, c.s.esc, c.s.seg = c.sm.data_ptr(), c.nib.data_ptr(), c.esc.data_ptr(), c.seg.data_ptr()
         c.rows, c.cols, c.n_esc = self.rows, self.cols, self.n_esc
         return c
+
+    @property
+    def rsum(self):
+        """The per-round escape summaries inside seg (a view, rows*nseg words)."""
+        off = lib().dgt_r4_rsum_offset(self.rows, self.cols)
+        return self.seg[off:off + self.rows * lib().dgt_r4_nseg(self.cols)]
 
 
 def load_r4(dev: DevicePacked, status=None, stream=None) -> R4:

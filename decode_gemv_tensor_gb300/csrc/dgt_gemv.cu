@@ -45,6 +45,7 @@ struct GemvArgs {
     const uint8_t *nib;
     const uint8_t *esc;
     const uint32_t *seg;
+    const uint32_t *rsum;   // per-round escape summaries (second part of seg)
     const uint16_t *W;
     const uint16_t *x;
     uint16_t *y;
@@ -325,7 +326,7 @@ template <>
 struct TmaCfg<true> {
     static constexpr uint32_t C = 4;               // rounds per piece
     static constexpr uint32_t NS = DGT_GEMV_NS_R4; // stages per warp
-    static constexpr uint32_t STAGE = 4 * 768;     // sm bytes then nibbles
+    static constexpr uint32_t STAGE = 4 * 768 + 64; // sm bytes, nibbles, then round summaries
 };
 template <>
 struct TmaCfg<false> {
@@ -348,8 +349,11 @@ __device__ __forceinline__ UnitRange unit_range(uint64_t uu, uint64_t r0, uint64
     return u;
 }
 
+// R4: the piece's round summaries (words x .. x + n of rsum, x = row * nseg
+// + j) travel with it, as the aligned run of 16-byte chunks that covers them
+// (at most 32 bytes); word x lands at offset 4 * (x & 3) of the summary slot.
 template <bool R4>
-__device__ __forceinline__ void issue_piece(const GemvArgs &a, uint64_t rowf, uint32_t j, uint32_t j1,
+__device__ __forceinline__ void issue_piece(const GemvArgs &a, uint64_t rowf, uint64_t x, uint32_t j, uint32_t j1,
                                             uint32_t stage, uint32_t bar) {
     const uint32_t n = min(TmaCfg<R4>::C, j1 - j);
     const uint32_t k0 = j * 512;
@@ -357,9 +361,12 @@ __device__ __forceinline__ void issue_piece(const GemvArgs &a, uint64_t rowf, ui
     const uint64_t f = rowf + k0;
     fence_proxy_async_smem();
     if (R4) {
-        mbar_arrive_expect_tx(bar, cols + cols / 2);
+        const uint64_t s0 = x & ~3ull, s1 = (x + n + 3) & ~3ull;
+        const uint32_t rb = (uint32_t)(s1 - s0) * 4;
+        mbar_arrive_expect_tx(bar, cols + cols / 2 + rb);
         bulk_g2s(stage, a.sm + f, cols, bar);
         bulk_g2s(stage + TmaCfg<R4>::C * 512, a.nib + f / 2, cols / 2, bar);
+        bulk_g2s(stage + TmaCfg<R4>::C * 768, a.rsum + s0, rb, bar);
     } else {
         mbar_arrive_expect_tx(bar, cols * 2);
         bulk_g2s(stage, a.W + f, cols * 2, bar);
@@ -369,16 +376,17 @@ __device__ __forceinline__ void issue_piece(const GemvArgs &a, uint64_t rowf, ui
 // The next piece a warp copies: unit uu (of this CTA), rounds [j, j1) of
 // the row whose first weight is at flat index rowf.
 struct PieceCursor {
-    uint64_t uu, rowf;
+    uint64_t uu, rowf, rowx;
     uint32_t j, j1;
 };
 
 __device__ __forceinline__ void cursor_set(PieceCursor &c, uint64_t uu, uint64_t units, uint64_t r0, uint64_t rs,
-                                           uint32_t log2S, uint32_t J, uint64_t K) {
+                                           uint32_t log2S, uint32_t J, uint64_t K, uint64_t nseg) {
     c.uu = uu;
     if (uu < units) {
         const UnitRange u = unit_range(uu, r0, rs, log2S, J);
         c.rowf = u.row * K;
+        c.rowx = u.row * nseg;
         c.j = u.j0;
         c.j1 = u.j1;
     }
@@ -433,16 +441,16 @@ __global__ void __launch_bounds__((TNW + TPW) * 32, 1) k_gemv_tma(GemvArgs a) {
             const uint32_t ring_a = smem_u32(dsm + (size_t)c * TNS * STAGE);
             const uint32_t full_a = smem_u32(&full[c][0]), empty_a = smem_u32(&empty[c][0]);
             PieceCursor cur;
-            cursor_set(cur, c, units, r0, rs, log2S, J, a.cols);
+            cursor_set(cur, c, units, r0, rs, log2S, J, a.cols, a.nseg);
             uint32_t q = 0, idle = 0;
             while (cur.uu < units && !*(volatile int *)&abort_flag) {
                 const uint32_t st = q % TNS;
                 if (q < TNS || mbar_test_wait(empty_a + 8 * st, ((q / TNS) - 1) & 1u)) {
-                    issue_piece<R4>(a, cur.rowf, cur.j, cur.j1, ring_a + st * STAGE, full_a + 8 * st);
+                    issue_piece<R4>(a, cur.rowf, cur.rowx + cur.j, cur.j, cur.j1, ring_a + st * STAGE, full_a + 8 * st);
                     q++;
                     idle = 0;
                     cur.j += C;
-                    if (cur.j >= cur.j1) cursor_set(cur, cur.uu + TNW, units, r0, rs, log2S, J, a.cols);
+                    if (cur.j >= cur.j1) cursor_set(cur, cur.uu + TNW, units, r0, rs, log2S, J, a.cols, a.nseg);
                 } else if (++idle >= MBAR_SPIN_LIMIT) {
                     set_status(a.status, DGT_ERR_TIMEOUT);
                     atomicExch(&abort_flag, 1);
@@ -478,37 +486,10 @@ __global__ void __launch_bounds__((TNW + TPW) * 32, 1) k_gemv_tma(GemvArgs a) {
     const bool cut = (K & 511) != 0;
     uint32_t st = 0, phases = 0, waited = 0;
     bool ok = true;
-    // escape metadata runs ahead: the segment counts of the unit after next
-    // and the first escape ranks of the next unit are requested while this unit
-    // streams, so a unit start never waits on a load (units can be one piece)
-    SegPre pre = {0, 0, 0, 0}, nxt = {0, 0, 0, 0};
-    if (R4 && (uint64_t)w < units) {
-        const UnitRange u = unit_range(w, r0, rs, log2S, J);
-        seg_issue(a, u.row, u.j0, u.j1, lane, pre);
-        seg_issue_esc(a, pre);
-        if ((uint64_t)w + TNW < units) {
-            const UnitRange un = unit_range(w + TNW, r0, rs, log2S, J);
-            seg_issue(a, un.row, un.j0, un.j1, lane, nxt);
-        }
-    }
     for (uint64_t ch = 0; ch < nchunks; ch++) {
         const uint64_t c0 = ch * TCHUNK, cend = min(c0 + TCHUNK, units);
         for (uint64_t uu = c0 + w; uu < cend; uu += TNW) {
             const UnitRange u = unit_range(uu, r0, rs, log2S, J);
-            SegInfo g = {0, 0, 0, 0, 0};
-            RoundLut rl = {0, 0, 0};
-            uint32_t jbase = u.j0;
-            if (R4) {
-                g = seg_finish(pre, table_s);
-                rl = round_luts(g, L);
-                pre = nxt;
-                if (uu + TNW < units) seg_issue_esc(a, pre);
-                nxt = SegPre{0, 0, 0, 0};
-                if (uu + 2 * TNW < units) {
-                    const UnitRange un = unit_range(uu + 2 * TNW, r0, rs, log2S, J);
-                    seg_issue(a, un.row, un.j0, un.j1, lane, nxt);
-                }
-            }
             float acc = 0.0f;
             for (uint32_t jp = u.j0; jp < u.j1; jp += C) {
                 if (ok) {
@@ -526,15 +507,19 @@ __global__ void __launch_bounds__((TNW + TPW) * 32, 1) k_gemv_tma(GemvArgs a) {
                 ok = __all_sync(DGT_FULL, ok);
                 phases ^= 1u << st;
                 const uint32_t n = min(C, u.j1 - jp);
-                if (R4 && jp - jbase >= 32) {
-                    jbase = jp;
-                    g = load_seginfo(a, table_s, u.row, jbase, u.j1, lane);
-                    rl = round_luts(g, L);
-                }
-                const uint32_t b0 = jp - jbase;
                 const uint32_t rp = (cut && Jm1 - jp < n) ? Jm1 - jp : 0xFFFFFFFFu;
-                const uint32_t pm = R4 ? (rl.multi >> b0) & ((1u << n) - 1u) : 0u;
                 const uint8_t *stg = ring + st * STAGE;
+                // the piece's round summaries arrived with it: lane r < n holds
+                // round jp + r's word, and its two table words for the decode
+                uint32_t rec = 0;
+                RoundLut rl = {0, 0, 0};
+                if (R4) {
+                    const uint32_t *recs =
+                        reinterpret_cast<const uint32_t *>(stg + C * 768) + ((u.row * a.nseg + jp) & 3u);
+                    rec = lane < n ? recs[lane] : 0u;
+                    rl = round_luts_rec(rec, L);
+                }
+                const uint32_t pm = rl.multi;
                 // an R4 piece of fewer than C rounds (a short unit's last piece)
                 // stays on the fast loops; the row's last round cut by K, and short
                 // BF16 pieces, go to the slow loop
@@ -550,7 +535,7 @@ __global__ void __launch_bounds__((TNW + TPW) * 32, 1) k_gemv_tma(GemvArgs a) {
                         if ((pm >> r) & 1u) {
                             const uint2 nv = *reinterpret_cast<const uint2 *>(stg + C * 512 + r * 256 + 8 * lane);
                             uint32_t e;
-                            if (multi_exponent(a, g, b0 + r, nv, table_s, lane, e)) {
+                            if (rec_exponent(__shfl_sync(DGT_FULL, rec, r), nv, lane, e)) {
                                 const R4Lut t = lut15(L, e);
                                 mh3[r] = t.h3;
                                 ml1[r] = t.l1;
@@ -568,8 +553,8 @@ __global__ void __launch_bounds__((TNW + TPW) * 32, 1) k_gemv_tma(GemvArgs a) {
                         const uint4 sv = *reinterpret_cast<const uint4 *>(stg + r * 512 + 16 * lane);
                         const uint2 nv = *reinterpret_cast<const uint2 *>(stg + C * 512 + r * 256 + 8 * lane);
                         R4Lut Lr = L;
-                        Lr.h3 = __shfl_sync(DGT_FULL, rl.h3, b0 + r);
-                        Lr.l1 = __shfl_sync(DGT_FULL, rl.l1, b0 + r);
+                        Lr.h3 = __shfl_sync(DGT_FULL, rl.h3, r);
+                        Lr.l1 = __shfl_sync(DGT_FULL, rl.l1, r);
                         r4_dec16(nv, sv, Lr, p);
                     } else {
                         const uint4 lo = *reinterpret_cast<const uint4 *>(stg + r * 1024 + 32 * lane);
@@ -598,8 +583,8 @@ __global__ void __launch_bounds__((TNW + TPW) * 32, 1) k_gemv_tma(GemvArgs a) {
                             const uint4 sv = *reinterpret_cast<const uint4 *>(stg + r * 512 + 16 * lane);
                             const uint2 nv = *reinterpret_cast<const uint2 *>(stg + C * 512 + r * 256 + 8 * lane);
                             R4Lut Lr = L;
-                            const uint32_t h3 = __shfl_sync(DGT_FULL, rl.h3, b0 + r);
-                            const uint32_t l1 = __shfl_sync(DGT_FULL, rl.l1, b0 + r);
+                            const uint32_t h3 = __shfl_sync(DGT_FULL, rl.h3, r);
+                            const uint32_t l1 = __shfl_sync(DGT_FULL, rl.l1, r);
                             Lr.h3 = ((pm >> r) & 1u) ? mh3[r] : h3;
                             Lr.l1 = ((pm >> r) & 1u) ? ml1[r] : l1;
                             r4_dec16(nv, sv, Lr, p);
@@ -620,10 +605,13 @@ __global__ void __launch_bounds__((TNW + TPW) * 32, 1) k_gemv_tma(GemvArgs a) {
                         if (R4) {
                             const uint4 sv = *reinterpret_cast<const uint4 *>(stg + r * 512 + 16 * lane);
                             const uint2 nv = *reinterpret_cast<const uint2 *>(stg + C * 512 + r * 256 + 8 * lane);
-                            const uint32_t h3 = __shfl_sync(DGT_FULL, rl.h3, b0 + r);
-                            const uint32_t l1 = __shfl_sync(DGT_FULL, rl.l1, b0 + r);
+                            const uint32_t h3 = __shfl_sync(DGT_FULL, rl.h3, r);
+                            const uint32_t l1 = __shfl_sync(DGT_FULL, rl.l1, r);
                             if ((pm >> r) & 1u) {
-                                r4_round_general(a, L, nv, sv, g, b0 + r, escb[R4 ? w : 0], table_s, lane, ract, p);
+                                // a rare round: its escape index straight from seg
+                                const uint64_t sx = u.row * a.nseg + jp + r;
+                                const uint32_t b = a.seg[sx], c = a.seg[sx + 1] - b;
+                                r4_round_general_cb(a, L, nv, sv, c, b, escb[R4 ? w : 0], table_s, lane, ract, p);
                             } else {
                                 R4Lut Lr = L;
                                 Lr.h3 = h3;
@@ -785,6 +773,7 @@ extern "C" int dgt_gemv_ex(const dgt_r4 *W, const uint16_t *d_x, uint16_t *d_y, 
     a.nib = W->nib;
     a.esc = W->esc;
     a.seg = W->seg;
+    a.rsum = W->seg + dgt_rsum_offset(N, dgt_r4_nseg(K));
     a.x = d_x;
     a.y = d_y;
     a.y32 = d_y32;

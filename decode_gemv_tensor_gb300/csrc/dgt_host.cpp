@@ -443,9 +443,11 @@ int dgt_r4_sizes(uint64_t rows, uint64_t cols, uint64_t n_esc, uint64_t *nib_byt
     if (rows && n / rows != cols) return DGT_ERR_SHAPE;
     if (nib_bytes) *nib_bytes = (n + 1) / 2;
     if (esc_bytes) *esc_bytes = n_esc;
-    if (seg_bytes) *seg_bytes = (rows * dgt_r4_nseg(cols) + 1) * 4;
+    if (seg_bytes) *seg_bytes = dgt_seg_words(rows, dgt_r4_nseg(cols)) * 4;
     return DGT_OK;
 }
+
+uint64_t dgt_r4_rsum_offset(uint64_t rows, uint64_t cols) { return dgt_rsum_offset(rows, dgt_r4_nseg(cols)); }
 
 int dgt_r4_init_from_view(const dgt_packed_view *v, uint8_t *d_nib, uint8_t *d_esc,
                           uint32_t *d_seg, dgt_r4 *r4) {

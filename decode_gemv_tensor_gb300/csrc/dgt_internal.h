@@ -17,3 +17,12 @@ static inline int dgt_plan_slices(uint64_t N, uint64_t K) {
     while ((uint64_t)S < want && S * 2 <= 8 && (uint64_t)(S * 2) <= J) S *= 2;
     return S;
 }
+
+// R4 row-segment index, in one array of 32-bit words: rows*nseg + 1 prefix
+// counts, padded to a multiple of 4 words, then rows*nseg per-round escape
+// summaries, padded to a multiple of 4 words (so that 16-byte bulk copies of
+// any run of summaries stay inside the array).
+static inline uint64_t dgt_rsum_offset(uint64_t rows, uint64_t nseg) { return (rows * nseg + 1 + 3) & ~3ull; }
+static inline uint64_t dgt_seg_words(uint64_t rows, uint64_t nseg) {
+    return dgt_rsum_offset(rows, nseg) + ((rows * nseg + 3) & ~3ull);
+}

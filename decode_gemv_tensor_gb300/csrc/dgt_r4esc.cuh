@@ -104,6 +104,32 @@ __device__ __forceinline__ RoundLut round_luts(const SegInfo &g, const R4Lut &L)
     return o;
 }
 
+// The same per piece from the round summaries (lane r: round r's word,
+// min(c, 255) | x0 << 8 | x1 << 16 | x2 << 24): rank 15 -> x0 where c >= 1.
+__device__ __forceinline__ RoundLut round_luts_rec(uint32_t rec, const R4Lut &L) {
+    RoundLut o;
+    const uint32_t c = rec & 0xFFu;
+    const R4Lut m = lut15(L, (rec >> 8) & 0xFFu);
+    o.h3 = c ? m.h3 : L.h3;
+    o.l1 = c ? m.l1 : L.l1;
+    o.multi = __ballot_sync(DGT_FULL, c >= 2);
+    return o;
+}
+
+// A round with two or three escapes, each in a different lane: this lane's
+// escape exponent from the round's summary word (its place among the escaped
+// lanes picks x0, x1 or x2).  Returns false (the general patch is needed)
+// for more escapes, a lane with two, or counts that disagree.
+__device__ __forceinline__ bool rec_exponent(uint32_t rec, uint2 nv, uint32_t lane, uint32_t &e) {
+    const uint32_t c = rec & 0xFFu;
+    const uint32_t k = __popc(nib15_mask(nv.x)) + __popc(nib15_mask(nv.y));
+    const uint32_t bal = __ballot_sync(DGT_FULL, k != 0);
+    if (c > 3 || __any_sync(DGT_FULL, k > 1) || (uint32_t)__popc(bal) != c) return false;
+    const uint32_t q = __popc(bal & ((1u << lane) - 1u));
+    e = k ? (rec >> (8 + 8 * q)) & 0xFFu : 0u;
+    return true;
+}
+
 // A round whose segment holds two or more escapes, when every lane holds at
 // most one of them: the exponent of this lane's escape (its place among the
 // round's escaped lanes; the first two come prefetched).  Returns false when
@@ -125,13 +151,12 @@ __device__ __forceinline__ bool multi_exponent(const A &a, const SegInfo &g, uin
 }
 
 // Any R4 round with escapes, in line: decode, then patch every escaped weight
-// from the segment's escape ranks (staged in shared memory).
+// from the segment's escape ranks (staged in shared memory); c escapes from
+// index b on.
 template <class A>
-__device__ __forceinline__ void r4_round_general(const A &a, const R4Lut &L, uint2 nv, uint4 sv,
-                                                 const SegInfo &g, uint32_t bit, uint8_t *escb,
-                                                 const uint8_t *table_s, uint32_t lane, bool act, uint32_t p[8]) {
-    const uint32_t c = __shfl_sync(DGT_FULL, g.cnt, bit);
-    const uint32_t b = __shfl_sync(DGT_FULL, g.base, bit);
+__device__ __forceinline__ void r4_round_general_cb(const A &a, const R4Lut &L, uint2 nv, uint4 sv, uint32_t c,
+                                                    uint32_t b, uint8_t *escb, const uint8_t *table_s,
+                                                    uint32_t lane, bool act, uint32_t p[8]) {
     r4_dec16(nv, sv, L, p);
     const uint32_t m0 = act ? nib15_mask(nv.x) : 0u;
     const uint32_t m1 = act ? nib15_mask(nv.y) : 0u;
@@ -140,6 +165,15 @@ __device__ __forceinline__ void r4_round_general(const A &a, const R4Lut &L, uin
     __syncwarp();
     patch_escapes(p, m0, m1, cc, escb, table_s);
     __syncwarp();
+}
+
+template <class A>
+__device__ __forceinline__ void r4_round_general(const A &a, const R4Lut &L, uint2 nv, uint4 sv,
+                                                 const SegInfo &g, uint32_t bit, uint8_t *escb,
+                                                 const uint8_t *table_s, uint32_t lane, bool act, uint32_t p[8]) {
+    const uint32_t c = __shfl_sync(DGT_FULL, g.cnt, bit);
+    const uint32_t b = __shfl_sync(DGT_FULL, g.base, bit);
+    r4_round_general_cb(a, L, nv, sv, c, b, escb, table_s, lane, act, p);
 }
 
 }  // namespace dgt

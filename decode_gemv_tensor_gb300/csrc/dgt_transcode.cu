@@ -21,6 +21,7 @@
 
 #include "../../include/dgt.h"
 #include "dgt_device.cuh"
+#include "dgt_internal.h"
 #include "dgt_launch.h"
 
 namespace dgt {
@@ -870,6 +871,34 @@ __global__ void __launch_bounds__(FW * 32) k_f1_to_r4(F1Args a) {
 // ---------------------------------------------------------------------------
 // R4 -> BF16
 // ---------------------------------------------------------------------------
+// Per-round escape summaries (the second part of the seg array): thread i
+// reads the prefix counts of round i and i + 1 and the ranks of the round's
+// first three escapes, and writes min(c, 255) | x0 << 8 | x1 << 16 | x2 << 24
+// with x = table[rank].  Runs after the transcode that wrote seg and esc.
+struct RsumArgs {
+    const uint32_t *seg;
+    const uint8_t *esc;
+    uint64_t n_esc, nrounds;
+    uint32_t *rsum;
+    uint8_t table[256];
+};
+
+__global__ void __launch_bounds__(256) k_r4_rsum(RsumArgs a) {
+    __shared__ uint8_t tb[256];
+    pdl_trigger();
+    tb[threadIdx.x] = a.table[threadIdx.x];
+    pdl_wait();
+    __syncthreads();
+    for (uint64_t i = (uint64_t)blockIdx.x * 256 + threadIdx.x; i < a.nrounds; i += (uint64_t)gridDim.x * 256) {
+        const uint32_t b = a.seg[i], c = a.seg[i + 1] - b;
+        uint32_t w = c < 255u ? c : 255u;
+#pragma unroll
+        for (uint32_t q = 0; q < 3; q++)
+            if (q < c && (uint64_t)b + q < a.n_esc) w |= (uint32_t)tb[a.esc[b + q]] << (8 + 8 * q);
+        a.rsum[i] = w;
+    }
+}
+
 struct R2BArgs {
     const uint8_t *sm;
     const uint8_t *nib;
@@ -1046,6 +1075,15 @@ extern "C" int dgt_load_r4(const dgt_packed_view *dev, dgt_r4 *r4, int32_t *d_st
         if (launch_pdl(k_f1_to_r4, dim3((unsigned)grid), dim3(FW * 32), smem, st, a) != cudaSuccess)
             return DGT_ERR_CUDA;
     }
+    RsumArgs ra;
+    ra.seg = r4->seg;
+    ra.esc = r4->esc;
+    ra.n_esc = dev->n_esc15;
+    ra.nrounds = seg_last;
+    ra.rsum = r4->seg + dgt_rsum_offset(dev->rows, nseg);
+    for (int i = 0; i < 256; i++) ra.table[i] = r4->table[i];
+    const uint64_t rgrid = min((uint64_t)di.sms * 8, (seg_last + 255) / 256);
+    if (launch_pdl(k_r4_rsum, dim3((unsigned)rgrid), dim3(256), 0, st, ra) != cudaSuccess) return DGT_ERR_CUDA;
     return cudaPeekAtLastError() == cudaSuccess ? DGT_OK : DGT_ERR_CUDA;
 }
 

@@ -176,8 +176,18 @@ void dgt_read_free(dgt_packed **tensors, char **names, int count);
  * nib: ceil(n/2) bytes, element i in byte i/2, low nibble when i is even,
  *      value min(rank, 15).
  * esc: n_esc bytes, the rank of every element whose nibble is 15, flat order.
- * seg: rows*nseg + 1 words, nseg = ceil(cols/512); seg[r*nseg + j] counts the
- *      escapes at flat positions < r*cols + 512*j; the last word is n_esc.
+ * seg: the row-segment escape index, nseg = ceil(cols/512), in two parts:
+ *      - words [0, rows*nseg]: seg[r*nseg + j] counts the escapes at flat
+ *        positions < r*cols + 512*j; word rows*nseg is n_esc;
+ *      - from word dgt_r4_rsum_offset(rows, cols) (rows*nseg + 1 rounded up
+ *        to a multiple of 4): rows*nseg per-round summaries, word r*nseg + j =
+ *        min(c, 255) | x0 << 8 | x1 << 16 | x2 << 24, where c is the number
+ *        of escapes in round j of row r (its 512 columns) and x0..x2 are the
+ *        exponents table[rank] of the first three, in column order (0 when
+ *        absent).  The product kernels read these with the weights, so a
+ *        round's escape exponents need no dependent lookup.
+ *      Both parts are written by dgt_load_r4; the array is
+ *      dgt_r4_sizes(...seg_bytes) long (the summaries padded to 4 words).
  * sm:  n bytes, sign << 7 | mantissa (the packed array itself, not a copy).
  * All four device arrays must start on 16-byte boundaries.
  */
@@ -195,6 +205,10 @@ typedef struct dgt_r4 {
 
 /* nseg = ceil(cols / 512). */
 uint64_t dgt_r4_nseg(uint64_t cols);
+
+/* Word offset of the per-round escape summaries inside seg:
+   rows*nseg + 1 rounded up to a multiple of 4. */
+uint64_t dgt_r4_rsum_offset(uint64_t rows, uint64_t cols);
 
 /* Byte sizes of the R4 arrays for a rows x cols tensor with n_esc escapes. */
 int dgt_r4_sizes(uint64_t rows, uint64_t cols, uint64_t n_esc, uint64_t *nib_bytes,

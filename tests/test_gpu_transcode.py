@@ -24,7 +24,9 @@ def _oracle_r4(w):
     rows, cols = w.shape
     rt = oracle.rank_table(w)
     rk = oracle.ranks(w, rt["rank_of"])
-    return oracle.r4_encode(rk, rows, cols)
+    ref = oracle.r4_encode(rk, rows, cols)
+    ref["rsum"] = oracle.r4_round_summary(ref["nib"], ref["esc"], ref["seg"], rt["table"], rows, cols)
+    return ref
 
 
 def _check_r4(r4, ref, n):
@@ -34,6 +36,7 @@ def _check_r4(r4, ref, n):
     assert r4.n_esc == ne
     assert np.array_equal(r4.esc[:ne].cpu().numpy(), ref["esc"]), "esc"
     assert np.array_equal(r4.seg[:ref["seg"].size].cpu().numpy().view(np.uint32), ref["seg"]), "seg"
+    assert np.array_equal(r4.rsum.cpu().numpy().view(np.uint32), ref["rsum"]), "round summaries"
 
 
 SHAPES = [(1, 1), (1, 5), (1, 64), (3, 65), (2, 2047), (1, 2049), (7, 512), (5, 1000), (17, 513),
