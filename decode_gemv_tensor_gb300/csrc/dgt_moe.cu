@@ -37,6 +37,7 @@ constexpr uint32_t MOE_MAX_PAIRS = 1u << 16;
 struct MoeArgs {
     const uint8_t *sm, *nib, *esc;
     const uint32_t *seg;
+    const uint32_t *rsum;   // per-round escape summaries (second part of seg)
     const uint16_t *W;
     const int32_t *ids;
     const float *p;
@@ -249,7 +250,7 @@ constexpr uint32_t XS_TOKENS = 1024;       // token bitmap / slot map size
 
 template <bool R4>
 struct MoeStage {
-    static constexpr uint32_t BYTES = R4 ? MC * 768 : MC * 1024;
+    static constexpr uint32_t BYTES = R4 ? MC * 768 + 64 : MC * 1024;   // R4: sm, nibbles, round summaries
     static constexpr uint32_t NS = R4 ? 3 : 2;
 };
 
@@ -347,9 +348,14 @@ __device__ __forceinline__ void moe_issue(const MoeArgs &a, uint64_t grow, uint3
     const uint64_t f = grow * a.cols + k0;
     fence_proxy_async_smem();
     if (R4) {
-        mbar_arrive_expect_tx(bar, cols + cols / 2);
+        // the piece's round summaries (words x .. x + n), as the aligned run of
+        // 16-byte chunks that covers them; word x lands at slot offset 4 (x & 3)
+        const uint64_t x = grow * a.nseg + j, s0 = x & ~3ull, s1 = (x + n + 3) & ~3ull;
+        const uint32_t rb = (uint32_t)(s1 - s0) * 4;
+        mbar_arrive_expect_tx(bar, cols + cols / 2 + rb);
         bulk_g2s(stage, a.sm + f, cols, bar);
         bulk_g2s(stage + MC * 512, a.nib + f / 2, cols / 2, bar);
+        bulk_g2s(stage + MC * 768, a.rsum + s0, rb, bar);
     } else {
         mbar_arrive_expect_tx(bar, cols * 2);
         bulk_g2s(stage, a.W + f, cols * 2, bar);
@@ -394,7 +400,7 @@ struct MoeRing {
 // the others repeat token 0 and store nothing): pieces from the ring, each
 // 16-weight lane chunk decoded once, one fmaf chain per token, slice partials
 // butterfly-reduced into the workspace.
-template <bool R4, int NT>
+template <bool R4, bool BK, int NT>
 __device__ __forceinline__ void moe_row_pass(const MoeArgs &a, MoeRing &rg, const MoeRow &m, uint32_t ent,
                                              uint32_t ntp, const R4Lut &L, SegInfo &g, RoundLut &rl,
                                              const uint8_t *table_s, uint8_t *escb, uint32_t lane, bool act_last,
@@ -416,7 +422,7 @@ __device__ __forceinline__ void moe_row_pass(const MoeArgs &a, MoeRing &rg, cons
     for (int t = 0; t < NT; t++) acc[t] = 0.0f;
     uint32_t s = 0, send = J >> log2S, jbase = 0;
     for (uint32_t jp = 0; jp < J; jp += MC) {
-        if (rg.ok && a.bulk) {
+        if (rg.ok && BK) {
             if (mbar_wait(rg.full_a + 8 * rg.st, (rg.phases >> rg.st) & 1u)) {
                 rg.waited++;
             } else {
@@ -431,12 +437,28 @@ __device__ __forceinline__ void moe_row_pass(const MoeArgs &a, MoeRing &rg, cons
         rg.ok = __all_sync(DGT_FULL, rg.ok);
         rg.phases ^= 1u << rg.st;
         const uint32_t n = min(MC, J - jp);
-        if (R4 && jp - jbase >= 32) {
-            jbase = jp;
-            g = load_seginfo(a, table_s, m.grow, jbase, J, lane);
-            rl = round_luts(g, L);
-        }
         const uint8_t *stg = rg.ring + rg.st * STAGE;
+        // escape tables of the piece's rounds: from the round summaries that
+        // came with the piece (bulk), else from the row's seg window
+        uint32_t rec = 0, wb = 0;
+        RoundLut prl = rl;
+        if (R4) {
+            if (BK) {
+                const uint32_t *recs =
+                    reinterpret_cast<const uint32_t *>(stg + MC * 768) + ((m.grow * a.nseg + jp) & 3u);
+                rec = lane < n ? recs[lane] : 0u;
+                prl = round_luts_rec(rec, L);
+                wb = jp;
+            } else {
+                if (jp - jbase >= 32) {
+                    jbase = jp;
+                    g = load_seginfo(a, table_s, m.grow, jbase, J, lane);
+                    rl = round_luts(g, L);
+                }
+                prl = rl;
+                wb = jbase;
+            }
+        }
         const uint4 *xp[NT];
 #pragma unroll
         for (int t = 0; t < NT; t++) xp[t] = xr[t] + 64 * jp;
@@ -449,7 +471,7 @@ __device__ __forceinline__ void moe_row_pass(const MoeArgs &a, MoeRing &rg, cons
             if (R4) {
                 uint4 sv;
                 uint2 nv;
-                if (a.bulk) {
+                if (BK) {
                     sv = *reinterpret_cast<const uint4 *>(stg + r * 512 + 16 * lane);
                     nv = *reinterpret_cast<const uint2 *>(stg + MC * 512 + r * 256 + 8 * lane);
                 } else {
@@ -458,15 +480,22 @@ __device__ __forceinline__ void moe_row_pass(const MoeArgs &a, MoeRing &rg, cons
                     sv = act ? ldg_stream16(a.sm + f) : make_uint4(0, 0, 0, 0);
                     nv = act ? ldg_stream8(a.nib + f / 2) : make_uint2(0, 0);
                 }
-                const uint32_t bit = j - jbase;
+                const uint32_t bit = j - wb;
                 R4Lut Lr = L;
-                Lr.h3 = __shfl_sync(DGT_FULL, rl.h3, bit);
-                Lr.l1 = __shfl_sync(DGT_FULL, rl.l1, bit);
-                if ((rl.multi >> bit) & 1u) {
+                Lr.h3 = __shfl_sync(DGT_FULL, prl.h3, bit);
+                Lr.l1 = __shfl_sync(DGT_FULL, prl.l1, bit);
+                if ((prl.multi >> bit) & 1u) {
                     uint32_t e;
                     const uint2 nva = act ? nv : make_uint2(0, 0);
-                    if (multi_exponent(a, g, bit, nva, table_s, lane, e)) {
+                    const bool one_each = BK ? rec_exponent(__shfl_sync(DGT_FULL, rec, bit), nva, lane, e)
+                                                 : multi_exponent(a, g, bit, nva, table_s, lane, e);
+                    if (one_each) {
                         r4_dec16(nv, sv, lut15(L, e), p);
+                    } else if (BK) {
+                        // a rare round: its escape index straight from seg
+                        const uint64_t sx = m.grow * a.nseg + j;
+                        const uint32_t b = a.seg[sx], c = a.seg[sx + 1] - b;
+                        r4_round_general_cb(a, L, nv, sv, c, b, escb, table_s, lane, act, p);
                     } else {
                         r4_round_general(a, L, nv, sv, g, bit, escb, table_s, lane, act, p);
                     }
@@ -502,14 +531,14 @@ __device__ __forceinline__ void moe_row_pass(const MoeArgs &a, MoeRing &rg, cons
             }
         }
         __syncwarp();
-        if (a.bulk) {
+        if (BK) {
             if (rg.ok && lane == 0) mbar_arrive(rg.empty_a + 8 * rg.st);
             rg.st = rg.st + 1 == MoeStage<R4>::NS ? 0 : rg.st + 1;
         }
     }
 }
 
-template <bool R4>
+template <bool R4, bool BK>
 __global__ void __launch_bounds__((MNW + MPW) * 32, 1) k_moe(MoeArgs a) {
     constexpr uint32_t STAGE = MoeStage<R4>::BYTES, MNS = MoeStage<R4>::NS;
     extern __shared__ __align__(128) uint8_t dsm[];
@@ -610,7 +639,7 @@ __global__ void __launch_bounds__((MNW + MPW) * 32, 1) k_moe(MoeArgs a) {
         // ---- producer warps: lane l of producer warp p keeps consumer
         // c = p + MPW l's ring full
         const uint32_t c = (w - MNW) + MPW * lane;
-        if (c < MNW && a.bulk) {
+        if (c < MNW && BK) {
             const uint32_t ring_a = smem_u32(dsm + (size_t)c * MNS * STAGE);
             const uint32_t full_a = smem_u32(&full[c][0]), empty_a = smem_u32(&empty[c][0]);
             MoeCursor cur;
@@ -663,7 +692,9 @@ __global__ void __launch_bounds__((MNW + MPW) * 32, 1) k_moe(MoeArgs a) {
     // while this row streams, so no load is waited for at a row start
     SegPre pre = {0, 0, 0, 0}, nxt = {0, 0, 0, 0};
     RowPos pos = row_pos(a, rb + w);
-    if (R4 && (uint64_t)w < nrows) {
+    // (bulk rows take their escape tables from the round summaries instead)
+    const bool segpre = R4 && !BK;
+    if (segpre && (uint64_t)w < nrows) {
         seg_issue(a, moe_row(a, T, pos).grow, 0, J, lane, pre);
         seg_issue_esc(a, pre);
         if ((uint64_t)w + MNW < nrows) {
@@ -676,7 +707,7 @@ __global__ void __launch_bounds__((MNW + MPW) * 32, 1) k_moe(MoeArgs a) {
         const MoeRow m = moe_row(a, T, pos);
         SegInfo g = {0, 0, 0, 0, 0};
         RoundLut rl = {0, 0, 0};
-        if (R4) {
+        if (segpre) {
             g = seg_finish(pre, table_s);
             rl = round_luts(g, L);
             pre = nxt;
@@ -693,13 +724,13 @@ __global__ void __launch_bounds__((MNW + MPW) * 32, 1) k_moe(MoeArgs a) {
             const uint32_t ent = lane < ntp ? moe_pair(a, T, m, tg + lane) : 0u;
             MoeRing rg{ring, full_a, empty_a, st, phases, waited, ok, &abort_flag};
             if (ntp == 1)
-                moe_row_pass<R4, 1>(a, rg, m, ent, ntp, L, g, rl, table_s, escb[R4 ? w : 0], lane, act_last, S, log2S,
+                moe_row_pass<R4, BK, 1>(a, rg, m, ent, ntp, L, g, rl, table_s, escb[R4 ? w : 0], lane, act_last, S, log2S,
                                      xslot_p, xsm);
             else if (ntp == 2)
-                moe_row_pass<R4, 2>(a, rg, m, ent, ntp, L, g, rl, table_s, escb[R4 ? w : 0], lane, act_last, S, log2S,
+                moe_row_pass<R4, BK, 2>(a, rg, m, ent, ntp, L, g, rl, table_s, escb[R4 ? w : 0], lane, act_last, S, log2S,
                                      xslot_p, xsm);
             else
-                moe_row_pass<R4, 4>(a, rg, m, ent, ntp, L, g, rl, table_s, escb[R4 ? w : 0], lane, act_last, S, log2S,
+                moe_row_pass<R4, BK, 4>(a, rg, m, ent, ntp, L, g, rl, table_s, escb[R4 ? w : 0], lane, act_last, S, log2S,
                                      xslot_p, xsm);
             st = rg.st;
             phases = rg.phases;
@@ -708,7 +739,7 @@ __global__ void __launch_bounds__((MNW + MPW) * 32, 1) k_moe(MoeArgs a) {
         }
     }
     // after a timeout: copies that may still be in flight land before exit
-    if (!ok && a.bulk)
+    if (!ok && BK)
         for (uint32_t q = waited; q < waited + MNS; q++) mbar_wait(full_a + 8 * (q % MNS), (q / MNS) & 1u);
 }
 
@@ -756,9 +787,11 @@ int launch_moe(MoeArgs &a, void *d_ws, size_t ws_bytes, cudaStream_t st) {
     a.xs_slots = a.tokens <= XS_TOKENS ? (uint32_t)min((uint64_t)a.tokens, (uint64_t)(XS_BYTES / (2 * a.cols))) : 0u;
     const size_t smem = (size_t)MNW * MoeStage<R4>::NS * MoeStage<R4>::BYTES + (size_t)a.xs_slots * a.cols * 2;
     int bps = 0;
-    if (prepare_kernel((const void *)k_moe<R4>, smem, (MNW + MPW) * 32, &bps) != DGT_OK) return DGT_ERR_CUDA;
-    if (launch_pdl(k_moe<R4>, dim3(a.grid), dim3((MNW + MPW) * 32), smem, st, a) != cudaSuccess)
-        return DGT_ERR_CUDA;
+    const void *fn = a.bulk ? (const void *)k_moe<R4, true> : (const void *)k_moe<R4, false>;
+    if (prepare_kernel(fn, smem, (MNW + MPW) * 32, &bps) != DGT_OK) return DGT_ERR_CUDA;
+    const cudaError_t e = a.bulk ? launch_pdl(k_moe<R4, true>, dim3(a.grid), dim3((MNW + MPW) * 32), smem, st, a)
+                                 : launch_pdl(k_moe<R4, false>, dim3(a.grid), dim3((MNW + MPW) * 32), smem, st, a);
+    if (e != cudaSuccess) return DGT_ERR_CUDA;
     const uint64_t n_out = (uint64_t)a.tokens * a.ne;
     uint64_t cgrid = (n_out + 255) / 256;
     if (cgrid > (uint64_t)di.sms * 8) cgrid = (uint64_t)di.sms * 8;
@@ -818,7 +851,8 @@ extern "C" int dgt_moe_gemv(const dgt_r4 *W, uint32_t n_experts, const int32_t *
     a.n_esc = W->n_esc;
     a.L = make_r4lut(W->table, W->n_table);
     for (int i = 0; i < 256; i++) a.table[i] = W->table[i];
-    a.bulk = W->cols % 32 == 0 && aligned16(W->sm) && aligned16(W->nib);
+    a.bulk = W->cols % 32 == 0 && aligned16(W->sm) && aligned16(W->nib) && aligned16(W->seg);
+    a.rsum = W->seg + dgt_rsum_offset(W->rows, a.nseg);
     a.p = d_p;
     a.y32 = d_y32;
     a.out = d_out;
