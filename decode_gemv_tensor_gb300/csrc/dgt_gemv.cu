@@ -297,19 +297,22 @@ __global__ void __launch_bounds__(PW * 32, 1) k_gemv(GemvArgs a) {
 #define DGT_GEMV_INTERLEAVE 0
 #endif
 #ifndef DGT_GEMV_TNW
-#define DGT_GEMV_TNW 16
+#define DGT_GEMV_TNW 14
 #endif
 #ifndef DGT_GEMV_NS_R4
-#define DGT_GEMV_NS_R4 3
+#define DGT_GEMV_NS_R4 4
 #endif
 #ifndef DGT_GEMV_NS_BF16
 #define DGT_GEMV_NS_BF16 5
 #endif
 #ifndef DGT_GEMV_TCHUNK
-#define DGT_GEMV_TCHUNK 1024
+#define DGT_GEMV_TCHUNK 896
 #endif
 #ifndef DGT_GEMV_TPW
 #define DGT_GEMV_TPW 2
+#endif
+#ifndef DGT_GEMV_SMEM_KB
+#define DGT_GEMV_SMEM_KB 212   // dynamic shared memory of the bulk-copy kernel (rings + x), at most
 #endif
 constexpr int TNW = DGT_GEMV_TNW;    // consumer warps per CTA
 constexpr int TPW = DGT_GEMV_TPW;    // producer warps (producer warp p serves consumers p, p + TPW, ...)
@@ -521,9 +524,10 @@ __global__ void __launch_bounds__((TNW + TPW) * 32, 1) k_gemv_tma(GemvArgs a) {
                 }
                 const uint32_t pm = rl.multi;
                 // an R4 piece of fewer than C rounds (a short unit's last piece)
-                // stays on the fast loops; the row's last round cut by K, and short
-                // BF16 pieces, go to the slow loop
-                bool slow = rp != 0xFFFFFFFFu || (!R4 && n != C);
+                // and the row's last round cut by K (round rp: its lanes past K
+                // add +0) stay on the fast loops; short BF16 pieces go to the
+                // slow loop
+                bool slow = !R4 && n != C;
                 // rounds with two or more escapes: per-lane rank-15 entries, worked
                 // out before the multiply-adds; anything else takes the slow loop
                 uint32_t mh3[C], ml1[C];
@@ -533,7 +537,8 @@ __global__ void __launch_bounds__((TNW + TPW) * 32, 1) k_gemv_tma(GemvArgs a) {
 #pragma unroll
                     for (uint32_t r = 0; r < C; r++) {
                         if ((pm >> r) & 1u) {
-                            const uint2 nv = *reinterpret_cast<const uint2 *>(stg + C * 512 + r * 256 + 8 * lane);
+                            uint2 nv = *reinterpret_cast<const uint2 *>(stg + C * 512 + r * 256 + 8 * lane);
+                            if (r == rp && !act) nv = make_uint2(0, 0);   // bytes past K are not this row's
                             uint32_t e;
                             if (rec_exponent(__shfl_sync(DGT_FULL, rec, r), nv, lane, e)) {
                                 const R4Lut t = lut15(L, e);
@@ -546,6 +551,14 @@ __global__ void __launch_bounds__((TNW + TPW) * 32, 1) k_gemv_tma(GemvArgs a) {
                     }
                 }
                 // one round of the common piece: decode with its shuffled table words
+                // the cut round: lanes past K multiply +0 weights (x there is 0 too)
+                auto cut_mask = [&](uint32_t r, uint32_t p[8]) {
+                    if (r == rp) {
+                        const uint32_t m = act ? 0xFFFFFFFFu : 0u;
+#pragma unroll
+                        for (int i = 0; i < 8; i++) p[i] &= m;
+                    }
+                };
                 auto fast_round = [&](uint32_t r) {
                     const uint32_t j = jp + r;
                     uint32_t p[8];
@@ -562,6 +575,7 @@ __global__ void __launch_bounds__((TNW + TPW) * 32, 1) k_gemv_tma(GemvArgs a) {
                         p[0] = lo.x; p[1] = lo.y; p[2] = lo.z; p[3] = lo.w;
                         p[4] = hi.x; p[5] = hi.y; p[6] = hi.z; p[7] = hi.w;
                     }
+                    cut_mask(r, p);
                     acc = fma_chunk16(p, xs, j, lane, acc);
                 };
                 if (ok && !slow && pm == 0 && n == C) {
@@ -594,6 +608,7 @@ __global__ void __launch_bounds__((TNW + TPW) * 32, 1) k_gemv_tma(GemvArgs a) {
                             p[0] = lo.x; p[1] = lo.y; p[2] = lo.z; p[3] = lo.w;
                             p[4] = hi.x; p[5] = hi.y; p[6] = hi.z; p[7] = hi.w;
                         }
+                        cut_mask(r, p);
                         acc = fma_chunk16(p, xs, j, lane, acc);
                     }
                 } else if (ok) {
@@ -752,7 +767,7 @@ template <bool R4>
 int choose_path(uint64_t K, uint32_t J, bool aligned) {
     if (K == 0 || K % 16 != 0 || !aligned) return 0;
     const size_t tma_smem = (size_t)TNW * TmaCfg<R4>::NS * TmaCfg<R4>::STAGE + (size_t)J * 1024;
-    if (K % 32 == 0 && tma_smem <= 200 * 1024) return 2;
+    if (K % 32 == 0 && tma_smem <= (size_t)DGT_GEMV_SMEM_KB * 1024) return 2;
     return J <= MAX_FAST_ROUNDS ? 1 : 0;
 }
 
