@@ -79,6 +79,8 @@ def _L():
             "or_moe_gemv": (C.c_int, [u16p, u64, u64, u64, i32p, f32p, u64, u64, u16p,
                                       f32p, f32p, u16p]),
             "or_gemm_f64": (None, [u16p, u16p, u64, u64, u64, u64p, u64, f64p]),
+            "or_moe_gemm_f64": (C.c_int, [u16p, u64, u64, u64, i32p, f32p, u64, u64, u16p, u64p, u64,
+                                          u64p, u64, f64p, f64p]),
             "or_f64_to_bf16": (C.c_uint16, [C.c_double]),
             "or_rmsnorm_f64": (None, [f64p, u16p, u64, C.c_double, f64p]),
             "or_silu_mul_f64": (None, [f64p, f64p, u64, f64p]),
@@ -385,6 +387,32 @@ def moe_gemv(W, n_experts: int, ids, p, X):
     if p is None:
         return y, None, None
     return y, out32[:T * Ne].reshape(T, Ne), out16[:T * Ne].reshape(T, Ne)
+
+
+def moe_gemm_f64(W, n_experts: int, ids, p, X, tokens=None, cols=None):
+    """Expert products of every (token, slot) pair in fp64: y [ntok, topk, ncol]
+    and, with routing weights p, out [ntok, ncol] = sum_j p[t, j] y[t, j]; over
+    the selected tokens and output columns (all if None)."""
+    W = _c(W, np.uint16)
+    Ne = W.shape[0] // n_experts
+    K = W.shape[1]
+    ids = _c(ids, np.int32)
+    T, topk = ids.shape
+    X = _c(X, np.uint16).reshape(T, K)
+    ts = None if tokens is None else _c(tokens, np.uint64)
+    ns = None if cols is None else _c(cols, np.uint64)
+    ntok = T if ts is None else ts.size
+    ncol = Ne if ns is None else ns.size
+    y = np.zeros(max(ntok * topk * ncol, 1), np.float64)
+    out = np.zeros(max(ntok * ncol, 1), np.float64)
+    pp = None if p is None else _c(p, np.float32)
+    rc = _L().or_moe_gemm_f64(_p(W, C.c_uint16), n_experts, Ne, K, _p(ids, C.c_int32), _p(pp, C.c_float), T,
+                              topk, _p(X, C.c_uint16), _p(ts, C.c_uint64), ntok, _p(ns, C.c_uint64), ncol,
+                              _p(y, C.c_double), _p(out, C.c_double))
+    if rc != 0:
+        raise ValueError("expert id, token or column out of range")
+    y = y[:ntok * topk * ncol].reshape(ntok, topk, ncol)
+    return y, (None if p is None else out[:ntok * ncol].reshape(ntok, ncol))
 
 
 def gemm_f64(X, W, cols=None):

@@ -588,6 +588,39 @@ void or_gemm_f64(const uint16_t *X, const uint16_t *W, uint64_t M, uint64_t N,
     (void)N;
 }
 
+/* Expert products at prompt length, [B] "Results" (the fused prompt kernels */
+/* cover every expert product): for token t and slot j with expert e =       */
+/* ids[t, j], y[t, j, n] = sum_k x[t, k] W[e*Ne + n, k] (exact products, fp64, */
+/* k increasing) and out[t, n] = sum_j p[t, j] y[t, j, n] (fp64, slot order). */
+/* tsel/nsel: the tokens and output columns computed (all when NULL);       */
+/* y: ntok x topk x ncol, out: ntok x ncol (may be NULL).  -1 on a bad id.  */
+/* ------------------------------------------------------------------------ */
+int or_moe_gemm_f64(const uint16_t *W, uint64_t n_experts, uint64_t Ne, uint64_t K,
+                    const int32_t *ids, const float *p, uint64_t T, uint64_t topk,
+                    const uint16_t *X, const uint64_t *tsel, uint64_t ntok,
+                    const uint64_t *nsel, uint64_t ncol, double *y, double *out) {
+    for (uint64_t a = 0; a < ntok; a++) {
+        uint64_t t = tsel ? tsel[a] : a;
+        if (t >= T) return -1;
+        for (uint64_t c = 0; c < ncol; c++) {
+            uint64_t n = nsel ? nsel[c] : c;
+            double o = 0.0;
+            for (uint64_t j = 0; j < topk; j++) {
+                int32_t e = ids[t * topk + j];
+                if (e < 0 || (uint64_t)e >= n_experts || n >= Ne) return -1;
+                const uint16_t *wrow = W + ((uint64_t)e * Ne + n) * K;
+                double acc = 0.0;
+                for (uint64_t k = 0; k < K; k++)
+                    acc += (double)or_bf16_to_f32(X[t * K + k]) * (double)or_bf16_to_f32(wrow[k]);
+                y[(a * topk + j) * ncol + c] = acc;
+                if (p) o += (double)p[t * topk + j] * acc;
+            }
+            if (out) out[a * ncol + c] = o;
+        }
+    }
+    return 0;
+}
+
 /* ------------------------------------------------------------------------ */
 /* Decoder-layer glue at batch 1, [B] "Results" (decode speed: a model's    */
 /* per-token time) -- the steps between the products, in fp64.              */

@@ -180,6 +180,59 @@ def test_gemm_f64_integer_exact():
 
 
 # ---------------------------------------------------------------------------
+# expert products at prompt length (fp64)
+# ---------------------------------------------------------------------------
+def test_moe_gemm_f64_one_expert_is_a_library_matmul():
+    X = S.activations(256, (82, 999, 0), count=6)
+    W = S.weights(40, 256, (82, 0, 0, 0), outliers=True)
+    ids = np.zeros((6, 1), np.int32)
+    y, out = oracle.moe_gemm_f64(W, 1, ids, np.ones((6, 1), np.float32), X)
+    ref = S.bf16_bits_to_f32(X).astype(np.float64) @ S.bf16_bits_to_f32(W).astype(np.float64).T
+    assert np.allclose(y[:, 0], ref, rtol=1e-12, atol=1e-15)
+    assert np.array_equal(out, y[:, 0])
+
+
+def test_moe_gemm_f64_integer_brute_force():
+    # small integers: every product and sum is exact; computed here by plain loops
+    g = np.random.default_rng(83)
+    E, Ne, K, T, topk = 3, 4, 33, 5, 2
+    Wi = g.integers(-9, 10, size=(E * Ne, K))
+    Xi = g.integers(-9, 10, size=(T, K))
+    ids = g.integers(0, E, size=(T, topk)).astype(np.int32)
+    pw = np.array([[0.5, 0.25], [1.0, 2.0], [0.75, 0.125], [4.0, 0.5], [1.5, 1.0]], np.float32)
+    y, out = oracle.moe_gemm_f64(_bf16(Wi), E, ids, pw, _bf16(Xi))
+    for t in range(T):
+        for n in range(Ne):
+            o = 0.0
+            for j in range(topk):
+                e = int(ids[t, j])
+                v = sum(int(Xi[t, k]) * int(Wi[e * Ne + n, k]) for k in range(K))
+                assert y[t, j, n] == v
+                o += float(pw[t, j]) * v
+            assert out[t, n] == o
+
+
+def test_moe_gemm_f64_expert_relabelling_and_selection():
+    # permuting the expert blocks and relabelling the ids changes nothing; a
+    # token/column selection returns the same entries
+    E, Ne, K, T, topk = 5, 6, 64, 7, 3
+    W = S.weights(E * Ne, K, (84, 0, 0, 0), outliers=True)
+    X = S.activations(K, (84, 999, 0), count=T).reshape(T, K)
+    ids, p = S.routing(T, E, topk, (84, 1, 0, 0))
+    y, out = oracle.moe_gemm_f64(W, E, ids, p, X)
+    perm = np.random.default_rng(85).permutation(E)
+    W2 = np.empty_like(W)
+    for e in range(E):
+        W2[perm[e] * Ne:(perm[e] + 1) * Ne] = W[e * Ne:(e + 1) * Ne]
+    y2, out2 = oracle.moe_gemm_f64(W2, E, perm[ids].astype(np.int32), p, X)
+    assert np.array_equal(y, y2) and np.array_equal(out, out2)
+    ys, outs = oracle.moe_gemm_f64(W, E, ids, p, X, tokens=[6, 0], cols=[5, 1])
+    assert np.array_equal(ys, y[[6, 0]][:, :, [5, 1]]) and np.array_equal(outs, out[[6, 0]][:, [5, 1]])
+    with pytest.raises(ValueError):
+        oracle.moe_gemm_f64(W, E, np.full((T, topk), E, np.int32), p, X)
+
+
+# ---------------------------------------------------------------------------
 # decoder-layer glue (fp64) and the batch-1 decode step
 # ---------------------------------------------------------------------------
 def test_f64_to_bf16_exact_values_and_ties():
