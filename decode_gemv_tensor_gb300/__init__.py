@@ -102,6 +102,11 @@ def lib():
                                         vp, vp, C.c_size_t, vp, vp]),
             "dgt_moe_gemv_noalloc": (i32, [C.POINTER(R4Struct), C.c_uint32, vp, vp, C.c_uint32, C.c_uint32, vp,
                                            vp, vp, vp, vp, vp]),
+            "dgt_moe_gemm_workspace_bytes": (C.c_size_t, [C.c_uint32, u64, u64, C.c_uint32, C.c_uint32]),
+            "dgt_moe_gemm": (i32, [C.POINTER(R4Struct), C.c_uint32, vp, vp, vp, C.c_uint32, C.c_uint32, vp, vp, vp,
+                                   vp, C.c_size_t, vp, vp]),
+            "dgt_moe_gemm_bf16": (i32, [vp, u64, u64, C.c_uint32, vp, vp, vp, C.c_uint32, C.c_uint32, vp, vp, vp,
+                                        vp, C.c_size_t, vp, vp]),
             "dgt_add_rmsnorm": (i32, [vp, vp, vp, u64, C.c_float, vp, vp]),
             "dgt_silu_mul": (i32, [vp, vp, u64, vp, vp]),
             "dgt_repeat": (i32, [vp, u64, u64, vp, vp]),
@@ -422,6 +427,47 @@ def moe_gemv_bf16(W, n_experts: int, ids, p, x, ws=None, y32=None, out=None, out
     _check(lib().dgt_moe_gemv_bf16(_ptr(W), rows, cols, n_experts, _ptr(ids), _ptr(p), tokens, topk, _ptr(x),
                                    _ptr(y32), _ptr(out), _ptr(out32), _ptr(ws), ws.numel(), _ptr(status),
                                    _stream(stream)), "dgt_moe_gemv_bf16")
+    return y32, out, out32
+
+
+def moe_gemm_workspace_bytes(n_experts: int, expert_rows: int, cols: int, tokens: int, topk: int) -> int:
+    return int(lib().dgt_moe_gemm_workspace_bytes(n_experts, expert_rows, cols, tokens, topk))
+
+
+def moe_gemm(W: R4, n_experts: int, ids, p, X, ws=None, y32=None, out=None, out32=None, status=None,
+             stream=None):
+    """dgt_moe_gemm: the expert products of every (token, slot) pair on the
+    tensor cores, experts stacked in one R4 tensor.  ids int32 [T, topk], p
+    float32 [T, topk] or None, X bf16 [T, K].  Returns (y32 [T, topk, Ne],
+    out bf16 [T, Ne], out32 [T, Ne]) (out and out32 None without p)."""
+    import torch
+    tokens, topk = ids.shape
+    ne = W.rows // n_experts
+    dev = W.sm.device
+    y32, out, out32 = _moe_outputs(tokens, topk, ne, dev, True, p is not None, y32, out, out32)
+    nb = moe_gemm_workspace_bytes(n_experts, ne, W.cols, tokens, topk)
+    if ws is None:
+        ws = torch.empty(max(nb, 256), dtype=torch.uint8, device=dev)
+    _check(lib().dgt_moe_gemm(C.byref(W.s), n_experts, _ptr(ids), _ptr(p), _ptr(X), tokens, topk, _ptr(y32),
+                              _ptr(out), _ptr(out32), _ptr(ws), ws.numel(), _ptr(status), _stream(stream)),
+           "dgt_moe_gemm")
+    return y32, out, out32
+
+
+def moe_gemm_bf16(W, n_experts: int, ids, p, X, ws=None, y32=None, out=None, out32=None, status=None,
+                  stream=None):
+    """dgt_moe_gemm_bf16: the same products with stacked bf16 experts W [E*Ne, K]."""
+    import torch
+    tokens, topk = ids.shape
+    rows, cols = W.shape
+    ne = rows // n_experts
+    y32, out, out32 = _moe_outputs(tokens, topk, ne, W.device, True, p is not None, y32, out, out32)
+    nb = moe_gemm_workspace_bytes(n_experts, ne, cols, tokens, topk)
+    if ws is None:
+        ws = torch.empty(max(nb, 256), dtype=torch.uint8, device=W.device)
+    _check(lib().dgt_moe_gemm_bf16(_ptr(W), rows, cols, n_experts, _ptr(ids), _ptr(p), _ptr(X), tokens, topk,
+                                   _ptr(y32), _ptr(out), _ptr(out32), _ptr(ws), ws.numel(), _ptr(status),
+                                   _stream(stream)), "dgt_moe_gemm_bf16")
     return y32, out, out32
 
 

@@ -55,6 +55,12 @@ struct GemmArgs {
     int32_t *status;
     R4Lut L;
     uint8_t table[256];
+    // grouped expert products: CTA (x, y) takes n-tile x of the expert and
+    // m-tile of job gjob[y] (e << 16 | m-tile, or ~0 for no work); the X rows
+    // are the expert's pairs, gathered in glist order starting at geoff[e]
+    const uint32_t *gjob, *geoff, *glist;
+    uint64_t ne;
+    uint32_t grouped, topk;
 };
 
 // ---- tcgen05 / TMA wrappers -------------------------------------------------
@@ -224,7 +230,8 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
     const uint32_t tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t mt = a.mt, P = a.stages;
     const uint32_t SB = gemm_stage_bytes(R4, mt);
-    const uint32_t n0 = blockIdx.x * GT_N, m0 = blockIdx.y * mt, sl = blockIdx.z;
+    uint32_t n0 = blockIdx.x * GT_N, m0 = blockIdx.y * mt;
+    const uint32_t sl = blockIdx.z;
     const uint32_t kb0 = (uint32_t)((uint64_t)sl * a.kb_total / a.split);
     const uint32_t kb1 = (uint32_t)((uint64_t)(sl + 1) * a.kb_total / a.split);
     const uint32_t nkb = kb1 - kb0;
@@ -259,6 +266,26 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
     pdl_wait();
     const uint32_t taddr = tmem_slot;
     volatile int *abortp = &abort_flag;
+    // grouped: this CTA's expert, its first gathered X row, and how many of
+    // the tile's rows (W) and columns (X) are real
+    uint32_t nvalid = GT_N, mvalid = mt;
+    if (a.grouped) {
+        const uint32_t job = a.gjob[blockIdx.y];
+        if (job == 0xFFFFFFFFu) {
+            tc_fence_before();
+            __syncthreads();
+            tc_fence_after();
+            if (warp == 1) tmem_dealloc(taddr, ncols);
+            return;
+        }
+        const uint32_t e = job >> 16, mtile = job & 0xFFFFu;
+        const uint32_t p0 = a.geoff[e] + mtile * mt;
+        mvalid = min(mt, a.geoff[e + 1] - p0);
+        m0 = p0;
+        const uint64_t nt0 = (uint64_t)blockIdx.x * GT_N;
+        nvalid = (uint32_t)min((uint64_t)GT_N, a.ne - nt0);
+        n0 = (uint32_t)((uint64_t)e * a.ne + nt0);
+    }
 
     if (warp == 0) {
         if (lane == 0) {
@@ -315,11 +342,12 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
         if (R4) {
             // ---- decoders: thread (t, q) owns chunk q of W row n0 + t
             const uint32_t d = tid - 128, t = d >> 2, q = d & 3;
-            const uint64_t row = n0 + t;
+            const uint64_t row = (uint64_t)n0 + t;
+            const bool rin = row < a.N;   // rows past the tensor (grouped tail tiles) read zeros
             const uint64_t kstart = (uint64_t)kb0 * GT_K;
             const uint64_t j = kstart / DGT_SEG;
-            uint64_t eidx = a.seg[row * a.nseg + j];
-            {
+            uint64_t eidx = rin ? a.seg[row * a.nseg + j] : a.n_esc;
+            if (rin) {
                 // escapes of this row's segment before kstart: at most 448 nibbles,
                 // read as up to 14 independent 16-byte loads
                 const uint4 *np = reinterpret_cast<const uint4 *>(a.nib + (row * a.K + j * DGT_SEG) / 2);
@@ -380,6 +408,18 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
                 uint32_t r[16];
                 tmem_ld16(taddr + lane_base + c, r);
                 tmem_wait_ld();
+                if (a.grouped) {
+                    // row t of the expert's n-tile for each of its pairs
+#pragma unroll
+                    for (int i = 0; i < 16; i++) {
+                        if (c + i < mvalid && t < nvalid) {
+                            const uint32_t pr = a.glist[m0 + c + i];
+                            const uint64_t q = (uint64_t)(pr >> 8) * a.topk + (pr & 0xFFu);
+                            a.y32[q * a.ne + (uint64_t)blockIdx.x * GT_N + t] = __uint_as_float(r[i]);
+                        }
+                    }
+                    continue;
+                }
 #pragma unroll
                 for (int i = 0; i < 16; i++) {
                     const uint64_t m = (uint64_t)m0 + c + i;
@@ -510,9 +550,341 @@ static int fill_common(GemmArgs &a, uint64_t M, uint64_t N, uint64_t K, const dg
     return DGT_OK;
 }
 
+// ---- grouped expert products ---------------------------------------------------
+// Pairs (t, j) of tokens and their routed slots are placed expert by expert
+// in (t, j) order by a three-kernel counting sort (per-block expert counts,
+// one scan, placement), which also gathers each pair's x row; the tcgen05
+// kernel then runs one CTA per (n-tile, expert m-tile) job, and a last kernel
+// adds out[t] = sum_j p[t, j] y[t, j] in slot order.
+constexpr uint32_t MG_MAX_EXPERTS = 4096;
+constexpr uint32_t MG_MAX_PAIRS = 1u << 16;
+constexpr uint32_t MG_BLOCK = 256;   // pairs per counting block
+
+struct MgArgs {
+    const int32_t *ids;
+    const float *p;
+    const uint16_t *x;
+    uint16_t *xg;        // gathered x rows, pairs x K
+    uint32_t *hist;      // n_experts x nb: counts, then exclusive prefixes over blocks
+    uint32_t *geoff;     // n_experts + 1
+    uint32_t *gjob;      // jobs (grid y of the product kernel)
+    uint32_t *glist;     // pairs in expert order: t << 8 | j
+    const float *y32;    // pairs x ne
+    float *out32;
+    uint16_t *out;
+    uint64_t K, ne;
+    uint32_t n_experts, tokens, topk, pairs, nb, mt, njobs_max;
+    int32_t *status;
+};
+
+static inline uint32_t mg_mtile(uint32_t pairs, uint32_t n_experts) {
+    const uint32_t used = pairs < n_experts ? pairs : n_experts;
+    uint32_t mean = (pairs + used - 1) / used;
+    uint32_t mt = (mean + 15) / 16 * 16;
+    return mt < 16 ? 16u : (mt > 128 ? 128u : mt);
+}
+
+__global__ void __launch_bounds__(MG_BLOCK) k_mg_count(MgArgs a) {
+    __shared__ uint32_t cnt[MG_MAX_EXPERTS];
+    pdl_trigger();
+    pdl_wait();
+    for (uint32_t e = threadIdx.x; e < a.n_experts; e += MG_BLOCK) cnt[e] = 0;
+    __syncthreads();
+    const uint32_t q = blockIdx.x * MG_BLOCK + threadIdx.x;
+    if (q < a.pairs) {
+        const int32_t e = a.ids[q];
+        if (e >= 0 && (uint32_t)e < a.n_experts) atomicAdd(&cnt[e], 1u);
+        else set_status(a.status, DGT_ERR_ARG);
+    }
+    __syncthreads();
+    for (uint32_t e = threadIdx.x; e < a.n_experts; e += MG_BLOCK) a.hist[(uint64_t)e * a.nb + blockIdx.x] = cnt[e];
+}
+
+// One CTA: per expert, exclusive prefixes of its block counts (in place) and
+// its total; geoff = exclusive prefix of the totals; the job list (every
+// m-tile of every expert in use, expert order), padded with ~0.
+__global__ void __launch_bounds__(1024) k_mg_scan(MgArgs a) {
+    __shared__ uint32_t tot[MG_MAX_EXPERTS];
+    __shared__ uint32_t wsum[32];
+    pdl_trigger();
+    pdl_wait();
+    const uint32_t tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    for (uint32_t e = tid; e < a.n_experts; e += 1024) {
+        uint32_t sacc = 0;
+        for (uint32_t b = 0; b < a.nb; b++) {
+            const uint32_t v = a.hist[(uint64_t)e * a.nb + b];
+            a.hist[(uint64_t)e * a.nb + b] = sacc;
+            sacc += v;
+        }
+        tot[e] = sacc;
+    }
+    __syncthreads();
+    // two exclusive scans over the experts (pairs, then m-tiles), four per thread
+    constexpr uint32_t PER = MG_MAX_EXPERTS / 1024;
+    for (int pass = 0; pass < 2; pass++) {
+        uint32_t v[PER], sum = 0;
+#pragma unroll
+        for (uint32_t i = 0; i < PER; i++) {
+            const uint32_t e = tid * PER + i;
+            const uint32_t c = e < a.n_experts ? tot[e] : 0u;
+            v[i] = pass == 0 ? c : (c + a.mt - 1) / a.mt;
+            sum += v[i];
+        }
+        uint32_t x = sum;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const uint32_t y = __shfl_up_sync(DGT_FULL, x, d);
+            if (lane >= (uint32_t)d) x += y;
+        }
+        if (lane == 31) wsum[w] = x;
+        __syncthreads();
+        if (w == 0) {
+            uint32_t t = wsum[lane];
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const uint32_t y = __shfl_up_sync(DGT_FULL, t, d);
+                if (lane >= (uint32_t)d) t += y;
+            }
+            wsum[lane] = t;
+        }
+        __syncthreads();
+        uint32_t run = (w ? wsum[w - 1] : 0u) + x - sum;
+        const uint32_t all = wsum[31];
+#pragma unroll
+        for (uint32_t i = 0; i < PER; i++) {
+            const uint32_t e = tid * PER + i;
+            if (e < a.n_experts) {
+                if (pass == 0) {
+                    a.geoff[e] = run;
+                } else {
+                    for (uint32_t m = 0; m < v[i] && run + m < a.njobs_max; m++) a.gjob[run + m] = e << 16 | m;
+                }
+            }
+            run += v[i];
+        }
+        if (tid == 0) {
+            if (pass == 0) a.geoff[a.n_experts] = all;
+        }
+        if (pass == 1)
+            for (uint32_t j = all + tid; j < a.njobs_max; j += 1024) a.gjob[j] = 0xFFFFFFFFu;
+        __syncthreads();
+    }
+}
+
+// Block b places its pairs (rank among the block's earlier pairs of the same
+// expert) and copies their x rows to the gathered matrix.
+__global__ void __launch_bounds__(MG_BLOCK) k_mg_place(MgArgs a) {
+    __shared__ int32_t sid[MG_BLOCK];
+    __shared__ uint32_t spos[MG_BLOCK];
+    pdl_trigger();
+    pdl_wait();
+    const uint32_t tid = threadIdx.x, q = blockIdx.x * MG_BLOCK + tid;
+    const int32_t e = q < a.pairs ? a.ids[q] : -1;
+    sid[tid] = e;
+    __syncthreads();
+    uint32_t pos = 0xFFFFFFFFu;
+    if (e >= 0 && (uint32_t)e < a.n_experts) {
+        uint32_t r = 0;
+        for (uint32_t i = 0; i < tid; i++) r += sid[i] == e;
+        pos = a.geoff[e] + a.hist[(uint64_t)e * a.nb + blockIdx.x] + r;
+        a.glist[pos] = ((q / a.topk) << 8) | (q % a.topk);
+    }
+    spos[tid] = pos;
+    __syncthreads();
+    const uint32_t kv = (uint32_t)(a.K / 8);   // uint4 per row
+    const uint32_t nloc = min(MG_BLOCK, a.pairs - blockIdx.x * MG_BLOCK);
+    for (uint32_t i = tid; i < nloc * kv; i += MG_BLOCK) {
+        const uint32_t r = i / kv, c = i - r * kv;
+        const uint32_t ps = spos[r];
+        if (ps == 0xFFFFFFFFu) continue;
+        const uint32_t tk = (blockIdx.x * MG_BLOCK + r) / a.topk;
+        reinterpret_cast<uint4 *>(a.xg + (uint64_t)ps * a.K)[c] =
+            reinterpret_cast<const uint4 *>(a.x + (uint64_t)tk * a.K)[c];
+    }
+}
+
+// out[t, n] = fmaf(p[t, topk-1], y[t, topk-1, n], ... fmaf(p[t, 0], y[t, 0, n], +0)).
+__global__ void __launch_bounds__(256) k_mg_combine(MgArgs a) {
+    pdl_trigger();
+    pdl_wait();
+    const uint64_t total = (uint64_t)a.tokens * a.ne;
+    for (uint64_t i = (uint64_t)blockIdx.x * 256 + threadIdx.x; i < total; i += (uint64_t)gridDim.x * 256) {
+        const uint64_t t = i / a.ne, n = i - t * a.ne;
+        float acc = 0.0f;
+        for (uint32_t j = 0; j < a.topk; j++) {
+            const uint64_t q = t * a.topk + j;
+            const int32_t e = a.ids[q];
+            if (e < 0 || (uint32_t)e >= a.n_experts) continue;
+            acc = fmaf(a.p[q], a.y32[q * a.ne + n], acc);
+        }
+        if (a.out32) a.out32[i] = acc;
+        if (a.out) a.out[i] = f32_to_bf16_rne(acc);
+    }
+}
+
+struct MgLayout {
+    size_t hist, geoff, gjob, glist, xg, y, total;
+    uint32_t nb, mt, njobs;
+};
+
+static inline size_t al256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+static MgLayout mg_layout(uint32_t n_experts, uint64_t ne, uint64_t K, uint32_t tokens, uint32_t topk) {
+    MgLayout l;
+    const uint32_t P = tokens * topk;
+    l.nb = (P + MG_BLOCK - 1) / MG_BLOCK;
+    l.mt = mg_mtile(P, n_experts);
+    l.njobs = (P + l.mt - 1) / l.mt + (P < n_experts ? P : n_experts);
+    l.hist = 0;
+    l.geoff = al256(l.hist + 4ull * n_experts * l.nb);
+    l.gjob = al256(l.geoff + 4ull * (n_experts + 1));
+    l.glist = al256(l.gjob + 4ull * l.njobs);
+    l.xg = al256(l.glist + 4ull * P);
+    l.y = al256(l.xg + 2ull * P * K);
+    l.total = al256(l.y + 4ull * P * ne);
+    return l;
+}
+
+// The grouped product: route and gather, the tcgen05 kernel over the jobs,
+// then the weighted sum (when p is given).
+template <bool R4>
+static int launch_moe_gemm(GemmArgs &g, MgArgs &m, const void *w_or_sm, void *d_ws, size_t ws_bytes, float *d_y32,
+                           cudaStream_t st) {
+    const MgLayout l = mg_layout(m.n_experts, m.ne, m.K, m.tokens, m.topk);
+    if (!d_ws || ws_bytes < l.total || ((uintptr_t)d_ws & 255)) return DGT_ERR_ARG;
+    uint8_t *ws = static_cast<uint8_t *>(d_ws);
+    m.hist = reinterpret_cast<uint32_t *>(ws + l.hist);
+    m.geoff = reinterpret_cast<uint32_t *>(ws + l.geoff);
+    m.gjob = reinterpret_cast<uint32_t *>(ws + l.gjob);
+    m.glist = reinterpret_cast<uint32_t *>(ws + l.glist);
+    m.xg = reinterpret_cast<uint16_t *>(ws + l.xg);
+    float *y = d_y32 ? d_y32 : reinterpret_cast<float *>(ws + l.y);
+    m.y32 = y;
+    m.nb = l.nb;
+    m.mt = l.mt;
+    m.njobs_max = l.njobs;
+    if (launch_pdl(k_mg_count, dim3(l.nb), dim3(MG_BLOCK), 0, st, m) != cudaSuccess) return DGT_ERR_CUDA;
+    if (launch_pdl(k_mg_scan, dim3(1), dim3(1024), 0, st, m) != cudaSuccess) return DGT_ERR_CUDA;
+    if (launch_pdl(k_mg_place, dim3(l.nb), dim3(MG_BLOCK), 0, st, m) != cudaSuccess) return DGT_ERR_CUDA;
+    g.M = m.pairs;
+    g.K = m.K;
+    g.mt = l.mt;
+    g.kb_total = (uint32_t)(m.K / GT_K);
+    g.split = 1;
+    g.y32 = y;
+    g.y = nullptr;
+    g.status = m.status;
+    g.grouped = 1;
+    g.gjob = m.gjob;
+    g.geoff = m.geoff;
+    g.glist = m.glist;
+    g.ne = m.ne;
+    g.topk = m.topk;
+    g.stages = gemm_stages(true, g.mt);
+    CUtensorMap tm_x, tm_w, tm_nib;
+    if (!make_map(&tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, m.xg, g.K, g.M, g.K * 2, GT_K, g.mt,
+                  CU_TENSOR_MAP_SWIZZLE_128B))
+        return DGT_ERR_CUDA;
+    if (R4) {
+        if (!make_map(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, w_or_sm, g.K, g.N, g.K, GT_K, GT_N,
+                      CU_TENSOR_MAP_SWIZZLE_NONE) ||
+            !make_map(&tm_nib, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.nib, g.K / 2, g.N, g.K / 2, GT_K / 2, GT_N,
+                      CU_TENSOR_MAP_SWIZZLE_NONE))
+            return DGT_ERR_CUDA;
+    } else {
+        if (!make_map(&tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, w_or_sm, g.K, g.N, g.K * 2, GT_K, GT_N,
+                      CU_TENSOR_MAP_SWIZZLE_128B))
+            return DGT_ERR_CUDA;
+        tm_nib = tm_w;
+    }
+    const size_t smem = (size_t)g.stages * gemm_stage_bytes(R4, g.mt) + 1024;
+    int bps = 0;
+    if (prepare_kernel((const void *)k_gemm<R4>, smem, GT_THREADS, &bps) != DGT_OK) return DGT_ERR_CUDA;
+    dim3 grid((unsigned)((m.ne + GT_N - 1) / GT_N), l.njobs, 1);
+    if (launch_pdl(k_gemm<R4>, grid, dim3(GT_THREADS), smem, st, tm_x, tm_w, tm_nib, g) != cudaSuccess)
+        return DGT_ERR_CUDA;
+    if (m.p && (m.out || m.out32)) {
+        DeviceInfo di;
+        if (device_info(&di) != DGT_OK) return DGT_ERR_CUDA;
+        const uint64_t total = (uint64_t)m.tokens * m.ne;
+        uint64_t cg = (total + 255) / 256;
+        if (cg > (uint64_t)di.sms * 8) cg = (uint64_t)di.sms * 8;
+        if (launch_pdl(k_mg_combine, dim3((unsigned)cg), dim3(256), 0, st, m) != cudaSuccess) return DGT_ERR_CUDA;
+    }
+    return cudaPeekAtLastError() == cudaSuccess ? DGT_OK : DGT_ERR_CUDA;
+}
+
+static int mg_common(MgArgs &m, GemmArgs &g, uint64_t rows, uint64_t cols, uint32_t n_experts, uint32_t tokens,
+                     uint32_t topk, const int32_t *d_ids, const float *d_p, const uint16_t *d_X, uint16_t *d_out,
+                     float *d_out32, int32_t *d_status, cudaStream_t st) {
+    if (n_experts == 0 || n_experts > MG_MAX_EXPERTS || rows % n_experts) return DGT_ERR_SHAPE;
+    if (topk == 0 || topk > 255 || (uint64_t)tokens * topk > MG_MAX_PAIRS || tokens >= (1u << 24))
+        return DGT_ERR_SHAPE;
+    if (cols == 0 || cols % GT_K || cols >= (1ull << 31) || rows >= (1ull << 31)) return DGT_ERR_SHAPE;
+    if (!d_ids || !d_X || !aligned16(d_X) || ((d_out || d_out32) && !d_p)) return DGT_ERR_ARG;
+    m.ids = d_ids;
+    m.p = d_p;
+    m.x = d_X;
+    m.out = d_out;
+    m.out32 = d_out32;
+    m.K = cols;
+    m.ne = rows / n_experts;
+    m.n_experts = n_experts;
+    m.tokens = tokens;
+    m.topk = topk;
+    m.pairs = tokens * topk;
+    m.status = d_status;
+    g.N = rows;
+    if (d_status && cudaMemsetAsync(d_status, 0, 4, st) != cudaSuccess) return DGT_ERR_CUDA;
+    return DGT_OK;
+}
+
 }  // namespace dgt
 
 using namespace dgt;
+
+extern "C" size_t dgt_moe_gemm_workspace_bytes(uint32_t n_experts, uint64_t expert_rows, uint64_t cols,
+                                               uint32_t tokens, uint32_t topk) {
+    if (n_experts == 0 || tokens == 0 || topk == 0) return 0;
+    return mg_layout(n_experts, expert_rows, cols, tokens, topk).total;
+}
+
+extern "C" int dgt_moe_gemm(const dgt_r4 *W, uint32_t n_experts, const int32_t *d_ids, const float *d_p,
+                            const uint16_t *d_X, uint32_t tokens, uint32_t topk, float *d_y32, uint16_t *d_out,
+                            float *d_out32, void *d_ws, size_t ws_bytes, int32_t *d_status, void *stream) {
+    if (!W) return DGT_ERR_ARG;
+    if (tokens == 0) return DGT_OK;
+    cudaStream_t st = (cudaStream_t)stream;
+    MgArgs m = {};
+    GemmArgs g = {};
+    int rc = mg_common(m, g, W->rows, W->cols, n_experts, tokens, topk, d_ids, d_p, d_X, d_out, d_out32, d_status, st);
+    if (rc != DGT_OK) return rc;
+    if (!W->sm || !W->nib || !W->seg || (W->n_esc && !W->esc) || !aligned16(W->sm) || !aligned16(W->nib))
+        return DGT_ERR_ARG;
+    g.nib = W->nib;
+    g.esc = W->esc;
+    g.seg = W->seg;
+    g.n_esc = W->n_esc;
+    g.nseg = dgt_r4_nseg(W->cols);
+    g.L = make_r4lut(W->table, W->n_table);
+    for (int i = 0; i < 256; i++) g.table[i] = W->table[i];
+    return launch_moe_gemm<true>(g, m, W->sm, d_ws, ws_bytes, d_y32, st);
+}
+
+extern "C" int dgt_moe_gemm_bf16(const uint16_t *d_W, uint64_t rows, uint64_t cols, uint32_t n_experts,
+                                 const int32_t *d_ids, const float *d_p, const uint16_t *d_X, uint32_t tokens,
+                                 uint32_t topk, float *d_y32, uint16_t *d_out, float *d_out32, void *d_ws,
+                                 size_t ws_bytes, int32_t *d_status, void *stream) {
+    if (!d_W) return DGT_ERR_ARG;
+    if (tokens == 0) return DGT_OK;
+    cudaStream_t st = (cudaStream_t)stream;
+    MgArgs m = {};
+    GemmArgs g = {};
+    int rc = mg_common(m, g, rows, cols, n_experts, tokens, topk, d_ids, d_p, d_X, d_out, d_out32, d_status, st);
+    if (rc != DGT_OK) return rc;
+    if (!aligned16(d_W)) return DGT_ERR_ARG;
+    return launch_moe_gemm<false>(g, m, d_W, d_ws, ws_bytes, d_y32, st);
+}
 
 extern "C" int dgt_gemm_default_plan(uint64_t M, uint64_t N, uint64_t K, dgt_gemm_plan *plan) {
     if (!plan || M == 0 || N == 0 || K == 0) return DGT_ERR_ARG;

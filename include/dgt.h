@@ -366,6 +366,40 @@ int dgt_gemm_bf16(const uint16_t *d_W, uint64_t N, uint64_t K, const uint16_t *d
                   void *stream);
 
 /*
+ * Expert products at prompt length on the tensor cores (Binade README,
+ * "Results": the fused prompt kernels cover every expert product).  W holds
+ * n_experts stacked experts (rows = n_experts * Ne, expert e = rows
+ * [e*Ne, (e+1)*Ne)); d_ids int32 [tokens, topk], d_p float32 [tokens, topk]
+ * (or NULL), d_X bf16 [tokens, K], all device, row-major.
+ *   y[t, j, n] = sum_k X[t, k] W[ids[t, j]*Ne + n, k]
+ *   out[t, n]  = fmaf chain over j = 0..topk-1 of p[t, j] * y[t, j, n]
+ * The pairs (t, j) are placed expert by expert in (t, j) order with their x
+ * rows gathered; one CTA computes a 128-row tile of one expert against up to
+ * m_tile of its pairs (m_tile = the mean pairs per expert in use rounded up
+ * to 16, 16..128) with K in 64-wide steps of four K=16 tcgen05.mma, fp32
+ * accumulation in tensor memory; no split-K.  The R4 and the bf16 calls
+ * issue the same MMAs on byte-identical tiles, so y, out and out32 are
+ * bit-identical.
+ * d_y32: [tokens*topk, Ne] float32 or NULL (then it stays in the workspace);
+ * d_out (bf16) and d_out32: [tokens, Ne], need d_p.  d_ws: device, 256-byte
+ * aligned, dgt_moe_gemm_workspace_bytes(...) bytes (pair lists, job list,
+ * gathered X, y when d_y32 is NULL).
+ * Limits: K % 64 == 0, n_experts <= 4096, topk <= 255,
+ * tokens * topk <= 65536.  Errors: DGT_ERR_SHAPE, DGT_ERR_ARG (also, on the
+ * device status, an expert id out of range: that pair contributes nothing),
+ * DGT_ERR_CUDA, DGT_ERR_TIMEOUT (status).  Asynchronous on stream.
+ */
+size_t dgt_moe_gemm_workspace_bytes(uint32_t n_experts, uint64_t expert_rows, uint64_t cols, uint32_t tokens,
+                                    uint32_t topk);
+int dgt_moe_gemm(const dgt_r4 *W, uint32_t n_experts, const int32_t *d_ids, const float *d_p, const uint16_t *d_X,
+                 uint32_t tokens, uint32_t topk, float *d_y32, uint16_t *d_out, float *d_out32, void *d_ws,
+                 size_t ws_bytes, int32_t *d_status, void *stream);
+int dgt_moe_gemm_bf16(const uint16_t *d_W, uint64_t rows, uint64_t cols, uint32_t n_experts, const int32_t *d_ids,
+                      const float *d_p, const uint16_t *d_X, uint32_t tokens, uint32_t topk, float *d_y32,
+                      uint16_t *d_out, float *d_out32, void *d_ws, size_t ws_bytes, int32_t *d_status,
+                      void *stream);
+
+/*
  * Allocation-free expert gather.  The paper has no counterpart: this entry
  * point exists for callers that cannot allocate device memory when they call
  * -- a plugin inside a host framework that owns the whole device memory pool,
