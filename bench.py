@@ -11,7 +11,9 @@ every device row of the path:
   the R4 and BF16 tcgen05 GEMMs at 16 prompt rows;
   the MoE expert gather (R4 and BF16 twin) at 1 and 16 tokens, top-8.
 The GEMM at 128 and 2048 rows is tensor-bound and is reported separately
-("gemm_tensor", TFLOP/s against the measured bf16 peak), and so is a whole
+("gemm_tensor", TFLOP/s against the measured bf16 peak), as are the grouped
+expert products of the 128-expert projection at 16, 128 and 2048 tokens
+("moe_gemm"), and so is a whole
 batch-1 decode step through the dense-3B layer stack in a CUDA graph
 ("decode_step": per-token time with R4 weights against BF16) and through the
 moe-30L-128E stack ("decode_step_moe").
@@ -101,16 +103,18 @@ def ncu_traffic(kernel):
 # ---------------------------------------------------------------------------
 def algo_bytes(p2_arrays, p1_arrays, n, n_esc, rows, cols):
     nib = (n + 1) // 2
-    seg = (rows * ((cols + 511) // 512) + 1) * 4
-    r4_out = nib + n_esc + seg
+    rounds = rows * ((cols + 511) // 512)
+    seg = (rounds + 1) * 4          # escape prefix counts
+    rsum = rounds * 4               # per-round escape summaries
+    r4_out = nib + n_esc + seg + rsum
     f2_in = sum(p2_arrays[k].nbytes for k in ("words", "blkq", "grp"))
     f1_in = sum(p1_arrays[k].nbytes for k in ("payload", "tw", "tesc", "esc1", "grp1"))
-    r4_in = n + nib + n_esc + seg
     return {
         "rice_to_r4": f2_in + r4_out,
         "f1_to_r4": f1_in + r4_out,
-        "r4_to_bf16": r4_in + 2 * n,
-        "gemv_r4": r4_in + 2 * cols + 6 * rows,
+        "r4_to_bf16": n + nib + n_esc + seg + 2 * n,
+        # the GEMV reads the summaries with the weights (prefix counts only for rare rounds)
+        "gemv_r4": n + nib + n_esc + rsum + 2 * cols + 6 * rows,
         "gemv_bf16": 2 * n + 2 * cols + 6 * rows,
     }
 
@@ -309,7 +313,8 @@ def run_ours(args, rank, world, dist):
         r["o16b"] = torch.empty((T, NE), dtype=torch.bfloat16, device=dev)
         distinct = len(np.unique(ids))
         io = T * KE * 2 + T * TOPK * NE * 4 + T * NE * 6
-        r["bytes_r4"] = distinct * NE * KE * 1.5 + io
+        # sign/mantissa bytes, nibbles and the per-round escape summaries of the experts in use
+        r["bytes_r4"] = distinct * NE * (KE * 1.5 + ((KE + 511) // 512) * 4) + io
         r["bytes_bf16"] = distinct * NE * KE * 2 + io
         moe_runs.append(r)
     del wm
@@ -417,6 +422,7 @@ def run_ours(args, rank, world, dist):
 
     # ---- prompt GEMM at 128 and 2048 rows (tensor-bound), outside the timed step
     extras = gemm_extras(dgt, torch, dev) if rank == 0 else None
+    mgemm = moe_gemm_extras(dgt, torch, dev) if rank == 0 else None
     dstep = decode_step_extras(dgt, torch, dev) if rank == 0 and not args.no_decode_step else None
     mstep = moe_decode_step_extras(dgt, torch, dev) if rank == 0 and not args.no_decode_step else None
 
@@ -487,7 +493,7 @@ def run_ours(args, rank, world, dist):
                              "rice_to_r4_gsym_s": kern["rice_to_r4"]["gsym_s"],
                              "rice_to_r4_frac": kern["rice_to_r4"]["frac"],
                              "r4_vs_bf16_gemv_speedup": kern["gemv_bf16"]["ms_avg"] / kern["gemv_r4"]["ms_avg"]},
-                "kernels": kern, "roofline": roof, "gemm_tensor": extras, "decode_step": dstep, "decode_step_moe": mstep, "cpu_baseline": cpu, "e2e": e2e,
+                "kernels": kern, "roofline": roof, "gemm_tensor": extras, "moe_gemm": mgemm, "decode_step": dstep, "decode_step_moe": mstep, "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": launches_per_step * args.steps, "clocks": clk,
                 "gpu": torch.cuda.get_device_name(dev)}
         print(json.dumps(line), flush=True)
@@ -533,6 +539,54 @@ def gemm_extras(dgt, torch, dev):
             res[name] = {"ms": t, "tflops": tf, "frac": tf / tpk}
         out[f"M{M}"] = {"shape": [M, N, K], "plan": [plan.m_tile, plan.split_k], "bound": "tensor",
                         "peak_tflops": tpk, "peak_kind": tkind, **res}
+    return out
+
+
+def moe_gemm_extras(dgt, torch, dev):
+    """Grouped expert products of the 128-expert gate projection (704 x 2816
+    per expert, top-8) at 16, 128 and 2048 tokens on the tensor cores: R4 and
+    bf16 times (CUDA events, median of 10), TFLOP/s of the pairs' products
+    against the measured bf16 peak, and whether the two are bit-identical."""
+    E, topk = S.MOE["experts"], S.MOE["topk"]
+    _, Ne, K = S.MOE["expert_proj"][0]
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            tpk, tkind = float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        tpk, tkind = 1900.0, "fallback"
+    w = S.weights(E * Ne, K, (6, 0, 0, 0))
+    r4 = dgt.load_r4(dgt.upload(dgt.pack(w, 2), dev))
+    wb = torch.from_numpy(w.view(np.int16)).to(dev).view(torch.bfloat16)
+    del w
+    st = torch.cuda.current_stream(dev)
+    out = {"shape": [E, Ne, K], "topk": topk, "bound": "tensor", "peak_tflops": tpk, "peak_kind": tkind}
+    for T in (16, 128, 2048):
+        ids, p = S.routing(T, E, topk, (6, 1, T, 0))
+        idd = torch.from_numpy(ids).to(dev)
+        pd = torch.from_numpy(p).to(dev)
+        X = torch.from_numpy(S.activations(K, (6, 999, T), count=T).reshape(T, K).view(np.int16)).to(dev)
+        X = X.view(torch.bfloat16)
+        ws = torch.empty(dgt.moe_gemm_workspace_bytes(E, Ne, K, T, topk), dtype=torch.uint8, device=dev)
+        res = {}
+        outs = {}
+        for name, fn in (("r4", lambda: dgt.moe_gemm(r4, E, idd, pd, X, ws=ws, stream=st)),
+                         ("bf16", lambda: dgt.moe_gemm_bf16(wb, E, idd, pd, X, ws=ws, stream=st))):
+            for _ in range(3):
+                outs[name] = fn()
+            evs = []
+            for _ in range(10):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(st)
+                fn()
+                e1.record(st)
+                evs.append((e0, e1))
+            torch.cuda.synchronize()
+            t = sorted(a.elapsed_time(b) for a, b in evs)[5]
+            tf = 2.0 * T * topk * Ne * K / (t / 1e3) / 1e12
+            res[name] = {"ms": t, "tflops": tf, "frac": tf / tpk}
+        same = bool(torch.equal(outs["r4"][2].view(torch.int32), outs["bf16"][2].view(torch.int32)))
+        out[f"T{T}"] = {"pairs": T * topk, "experts_used": int(len(np.unique(ids))), **res,
+                        "r4_over_bf16_speed": res["bf16"]["ms"] / res["r4"]["ms"], "r4_equals_bf16": same}
     return out
 
 
