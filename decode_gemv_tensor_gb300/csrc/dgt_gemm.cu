@@ -40,7 +40,7 @@ namespace dgt {
 
 constexpr uint32_t GT_N = 128;      // W rows per tile (MMA M)
 constexpr uint32_t GT_K = 64;       // bf16 columns per stage (one 128-byte swizzle row)
-constexpr uint32_t GT_MAXP = 8;     // pipeline stages, upper bound
+constexpr uint32_t GT_MAXP = 12;    // pipeline stages, upper bound
 constexpr uint32_t GT_SMEM_LIMIT = 200 * 1024;
 
 struct GemmArgs {
@@ -780,7 +780,7 @@ static int launch_moe_gemm(GemmArgs &g, MgArgs &m, const void *w_or_sm, void *d_
     g.glist = m.glist;
     g.ne = m.ne;
     g.topk = m.topk;
-    g.stages = gemm_stages(true, g.mt);
+    g.stages = gemm_stages(R4, g.mt);
     CUtensorMap tm_x, tm_w, tm_nib;
     if (!make_map(&tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, m.xg, g.K, g.M, g.K * 2, GT_K, g.mt,
                   CU_TENSOR_MAP_SWIZZLE_128B))
@@ -937,6 +937,6 @@ extern "C" int dgt_gemm_bf16(const uint16_t *d_W, uint64_t N, uint64_t K, const 
     int rc = fill_common(a, M, N, K, plan, d_Y32, d_Y, d_status, st);
     if (rc != DGT_OK) return rc;
     if (!aligned16(d_W) || !aligned16(d_X)) return DGT_ERR_ARG;
-    a.stages = gemm_stages(true, a.mt);   // same pipeline depth as the R4 GEMM
+    a.stages = gemm_stages(false, a.mt);
     return launch_gemm<false>(a, d_W, d_X, d_ws, ws_bytes, st);
 }
