@@ -60,7 +60,7 @@ KERNELS = ["rice_to_r4", "f1_to_r4", "r4_to_bf16", "gemv_r4", "gemv_bf16", "moe_
 KERNEL_SRC = {"rice_to_r4": "dgt_transcode.cu", "f1_to_r4": "dgt_transcode.cu",
               "r4_to_bf16": "dgt_transcode.cu", "gemv_r4": "dgt_gemv.cu", "gemv_bf16": "dgt_gemv.cu",
               "moe_r4": "dgt_moe.cu", "moe_bf16": "dgt_moe.cu", "gemm_r4": "dgt_gemm.cu",
-              "gemm_bf16": "dgt_gemm.cu"}
+              "gemm_bf16": "dgt_gemm.cu", "mgemm_r4": "dgt_gemm.cu", "mgemm_bf16": "dgt_gemm.cu"}
 
 
 def hbm_peak():
@@ -741,7 +741,23 @@ def run_case(args):
         return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
 
     c = args.case
-    if c.startswith("moe"):
+    if c.startswith("mgemm"):
+        # grouped expert products of the 128-expert gate projection at 2048 tokens, top-8
+        E, TOPK = S.MOE["experts"], S.MOE["topk"]
+        _, NE, KE = S.MOE["expert_proj"][0]
+        T = 2048
+        w = S.weights(E * NE, KE, (6, 0, 0, 0))
+        r4 = dgt.load_r4(dgt.upload(dgt.pack(w, 2), dev))
+        wb = bf(w)
+        ids, p = S.routing(T, E, TOPK, (6, 1, T, 0))
+        idd, pd = torch.from_numpy(ids).to(dev), torch.from_numpy(p).to(dev)
+        xm = bf(S.activations(KE, (6, 999, T), count=T).reshape(T, KE))
+        for _ in range(args.reps):
+            if c == "mgemm_r4":
+                dgt.moe_gemm(r4, E, idd, pd, xm)
+            else:
+                dgt.moe_gemm_bf16(wb, E, idd, pd, xm)
+    elif c.startswith("moe"):
         # the bench's MoE runs: one gather at 1 token, then one at 16, per rep
         E, TOPK = S.MOE["experts"], S.MOE["topk"]
         _, NE, KE = S.MOE["expert_proj"][0]

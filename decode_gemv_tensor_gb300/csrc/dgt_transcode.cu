@@ -86,7 +86,10 @@ struct F2Args {
 #ifndef DGT_RICE_REP
 #define DGT_RICE_REP 4
 #endif
-constexpr int RW = 24;          // warps per CTA
+#ifndef DGT_RICE_RW
+#define DGT_RICE_RW 24
+#endif
+constexpr int RW = DGT_RICE_RW;  // warps per CTA
 constexpr int RWIN = 12;        // table window bits
 constexpr int REP = DGT_RICE_REP;  // table copies (lane l uses copy l mod REP)
 constexpr int RCAP = 192;       // staged stream words per group (about 170 at 2.7 bits/rank)
