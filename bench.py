@@ -421,10 +421,11 @@ def run_ours(args, rank, world, dist):
             "algorithmic_bytes_per_launch": op_bytes[dom] / op_count[dom], "traffic": ncu_traffic(dom)}
 
     # ---- prompt GEMM at 128 and 2048 rows (tensor-bound), outside the timed step
-    extras = gemm_extras(dgt, torch, dev) if rank == 0 else None
-    mgemm = moe_gemm_extras(dgt, torch, dev) if rank == 0 else None
-    dstep = decode_step_extras(dgt, torch, dev) if rank == 0 and not args.no_decode_step else None
-    mstep = moe_decode_step_extras(dgt, torch, dev) if rank == 0 and not args.no_decode_step else None
+    more = rank == 0 and not args.no_extras
+    extras = gemm_extras(dgt, torch, dev) if more else None
+    mgemm = moe_gemm_extras(dgt, torch, dev) if more else None
+    dstep = decode_step_extras(dgt, torch, dev) if more and not args.no_decode_step else None
+    mstep = moe_decode_step_extras(dgt, torch, dev) if more and not args.no_decode_step else None
 
     # ---- end to end through the C ABI from pinned host buffers
     e2e = None
@@ -815,6 +816,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode-step", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="only the timed step (no GEMM/grouped-product/decode-step extras): for launch lists")
     args = ap.parse_args()
     if args.case:
         run_case(args)

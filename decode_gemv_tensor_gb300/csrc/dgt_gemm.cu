@@ -671,35 +671,37 @@ __global__ void __launch_bounds__(1024) k_mg_scan(MgArgs a) {
     }
 }
 
-// Block b places its pairs (rank among the block's earlier pairs of the same
-// expert) and copies their x rows to the gathered matrix.
+// Block b places its pairs: rank among the block's earlier pairs of the
+// same expert.
 __global__ void __launch_bounds__(MG_BLOCK) k_mg_place(MgArgs a) {
     __shared__ int32_t sid[MG_BLOCK];
-    __shared__ uint32_t spos[MG_BLOCK];
     pdl_trigger();
     pdl_wait();
     const uint32_t tid = threadIdx.x, q = blockIdx.x * MG_BLOCK + tid;
     const int32_t e = q < a.pairs ? a.ids[q] : -1;
     sid[tid] = e;
     __syncthreads();
-    uint32_t pos = 0xFFFFFFFFu;
     if (e >= 0 && (uint32_t)e < a.n_experts) {
         uint32_t r = 0;
         for (uint32_t i = 0; i < tid; i++) r += sid[i] == e;
-        pos = a.geoff[e] + a.hist[(uint64_t)e * a.nb + blockIdx.x] + r;
+        const uint32_t pos = a.geoff[e] + a.hist[(uint64_t)e * a.nb + blockIdx.x] + r;
         a.glist[pos] = ((q / a.topk) << 8) | (q % a.topk);
     }
-    spos[tid] = pos;
-    __syncthreads();
+}
+
+// The gathered matrix: row i = x of pair glist[i]'s token (16-byte pieces,
+// grid-stride over every SM).  Rows of pairs with a bad id stay unwritten;
+// no job reads them.
+__global__ void __launch_bounds__(256) k_mg_gather(MgArgs a) {
+    pdl_trigger();
+    pdl_wait();
     const uint32_t kv = (uint32_t)(a.K / 8);   // uint4 per row
-    const uint32_t nloc = min(MG_BLOCK, a.pairs - blockIdx.x * MG_BLOCK);
-    for (uint32_t i = tid; i < nloc * kv; i += MG_BLOCK) {
-        const uint32_t r = i / kv, c = i - r * kv;
-        const uint32_t ps = spos[r];
-        if (ps == 0xFFFFFFFFu) continue;
-        const uint32_t tk = (blockIdx.x * MG_BLOCK + r) / a.topk;
-        reinterpret_cast<uint4 *>(a.xg + (uint64_t)ps * a.K)[c] =
-            reinterpret_cast<const uint4 *>(a.x + (uint64_t)tk * a.K)[c];
+    const uint32_t placed = a.geoff[a.n_experts];
+    const uint64_t total = (uint64_t)placed * kv;
+    for (uint64_t i = (uint64_t)blockIdx.x * 256 + threadIdx.x; i < total; i += (uint64_t)gridDim.x * 256) {
+        const uint32_t r = (uint32_t)(i / kv), c = (uint32_t)(i - (uint64_t)r * kv);
+        const uint32_t tk = a.glist[r] >> 8;
+        reinterpret_cast<uint4 *>(a.xg + (uint64_t)r * a.K)[c] = reinterpret_cast<const uint4 *>(a.x + (uint64_t)tk * a.K)[c];
     }
 }
 
@@ -766,6 +768,13 @@ static int launch_moe_gemm(GemmArgs &g, MgArgs &m, const void *w_or_sm, void *d_
     if (launch_pdl(k_mg_count, dim3(l.nb), dim3(MG_BLOCK), 0, st, m) != cudaSuccess) return DGT_ERR_CUDA;
     if (launch_pdl(k_mg_scan, dim3(1), dim3(1024), 0, st, m) != cudaSuccess) return DGT_ERR_CUDA;
     if (launch_pdl(k_mg_place, dim3(l.nb), dim3(MG_BLOCK), 0, st, m) != cudaSuccess) return DGT_ERR_CUDA;
+    {
+        DeviceInfo di;
+        if (device_info(&di) != DGT_OK) return DGT_ERR_CUDA;
+        const uint64_t need = ((uint64_t)m.pairs * (m.K / 8) + 255) / 256;
+        const uint64_t gg = need < (uint64_t)di.sms * 4 ? (need ? need : 1) : (uint64_t)di.sms * 4;
+        if (launch_pdl(k_mg_gather, dim3((unsigned)gg), dim3(256), 0, st, m) != cudaSuccess) return DGT_ERR_CUDA;
+    }
     g.M = m.pairs;
     g.K = m.K;
     g.mt = l.mt;
