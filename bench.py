@@ -606,15 +606,21 @@ def decode_step_extras(dgt, torch, dev):
     (28 layers; every layer its own weights in HBM), R4 against BF16, each step
     one CUDA graph of the library's kernels (DecodeStep).  Attention is not
     part of the step (the output projection reads the value vector repeated
-    over the query heads).  Weights: one N(0, 0.02) draw of the largest shape,
-    sliced per projection and uploaded once per layer (separate allocations,
-    so each layer streams its own bytes; 4.2 GB R4 / 5.6 GB BF16 per token,
-    far above L2).  CUDA events around 20 replays after 3 warm-ups, median."""
+    over the query heads).  The layer's weights are stacked as a serving stack
+    would hold them: q, k, v as one 5120 x 3072 tensor and gate, up as one
+    16384 x 3072 tensor (one product each), o and down alone.  Weights: one
+    N(0, 0.02) draw of the largest shape, sliced per tensor and uploaded once
+    per layer (separate allocations, so each layer streams its own bytes;
+    4.2 GB R4 / 5.6 GB BF16 per token, far above L2).  CUDA events around 20
+    replays after 3 warm-ups, median."""
     m = S.DENSE_3B
     L, hid = m["layers"], m["hidden"]
-    big = S.weights(8192, 3072, (6, 0, 0, 0))
+    dims = {p: (r, c) for p, r, c in m["proj"]}
+    stacked = {"qkv": (dims["q"][0] + dims["k"][0] + dims["v"][0], hid), "o": dims["o"],
+               "gate_up": (dims["gate"][0] + dims["up"][0], hid), "down": dims["down"]}
+    big = S.weights(max(r for r, _ in stacked.values()), hid, (6, 0, 0, 0))
     flat = big.reshape(-1)
-    host = {p: flat[:r * c].reshape(r, c) for p, r, c in m["proj"]}
+    host = {p: flat[:r * c].reshape(r, c) for p, (r, c) in stacked.items()}
     packed = {p: dgt.pack(w, 2) for p, w in host.items()}
     r4_layers, bf_layers, r4_bytes = [], [], 0
     for _ in range(L):
@@ -622,13 +628,14 @@ def decode_step_extras(dgt, torch, dev):
         r4_layers.append(lr)
         bf_layers.append({p: dgt.r4_to_bf16(lr[p]) for p in host})
         r4_bytes += sum(r.sm.numel() + r.nib.numel() + r.n_esc + r.seg.numel() * 4 for r in lr.values())
-    bf_bytes = L * sum(r * c * 2 for _, r, c in m["proj"])
+    bf_bytes = L * sum(r * c * 2 for r, c in stacked.values())
     g = np.random.default_rng(7)
     gam = [torch.from_numpy(S.f32_to_bf16_bits((1 + 0.1 * g.normal(size=hid)).astype(np.float32)).view(np.int16))
            .to(dev).view(torch.bfloat16) for _ in range(2 * L + 1)]
     x0 = torch.from_numpy(S.bf16_bits_to_f32(S.activations(hid, (6, 999, 0)))).to(dev)
     out = {"model": m["name"], "layers": L, "hidden": hid, "batch": 1, "graph": True,
-           "attention": "not in the step (value vector repeated over the query heads)"}
+           "attention": "not in the step (value vector repeated over the query heads)",
+           "stacked": "q|k|v and gate|up, one product each"}
     res = {}
     for name, layers, nbytes in (("r4", r4_layers, r4_bytes), ("bf16", bf_layers, bf_bytes)):
         st = dgt.DecodeStep(layers, gam, depth=L)
@@ -661,7 +668,7 @@ def decode_step_extras(dgt, torch, dev):
     out.update(res)
     out["r4_over_bf16_speed"] = res["bf16"]["us_per_token"] / res["r4"]["us_per_token"]
     out["r4_equals_bf16"] = bool(same)
-    out["kernels_per_token"] = L * 11 + 1
+    out["kernels_per_token"] = L * 8 + 1
     return out
 
 
@@ -670,16 +677,18 @@ def moe_decode_step_extras(dgt, torch, dev):
     (30 layers, top-8 of 128 experts; every layer its own weights in HBM), R4
     against BF16, each step one CUDA graph (MoeDecodeStep).  Routing is drawn
     per layer (distinct experts, softmax weights) and fixed for the timed
-    replays.  Weights: one N(0, 0.02) draw tiled to the stacked expert shapes,
-    packed once per projection and copied on the device for every layer
-    (separate allocations).  CUDA events around 10 replays after 3 warm-ups,
-    median."""
+    replays.  q, k, v are stacked as one tensor (one product) and each
+    expert's gate and up rows as one block of one stacked tensor (one gather).
+    Weights: one N(0, 0.02) draw tiled to the stacked shapes, packed once per
+    tensor and copied on the device for every layer (separate allocations).
+    CUDA events around 10 replays after 3 warm-ups, median."""
     m = S.MOE
     L, hid, E, topk = m["layers"], m["hidden"], m["experts"], m["topk"]
     base = S.weights(8192, 3072, (7, 0, 0, 0)).reshape(-1)
-    shapes = {p: (r, c) for p, r, c in m["attn_proj"]}
+    attn = {p: (r, c) for p, r, c in m["attn_proj"]}
     (_, ne, ke), (_, _, _), (_, nd, kd) = m["expert_proj"]
-    shapes.update({"gate": (E * ne, ke), "up": (E * ne, ke), "down": (E * nd, kd)})
+    shapes = {"qkv": (attn["q"][0] + attn["k"][0] + attn["v"][0], hid), "o": attn["o"],
+              "gate_up": (E * 2 * ne, ke), "down": (E * nd, kd)}
     host = {p: np.resize(base, r * c).reshape(r, c) for p, (r, c) in shapes.items()}
     first = {p: dgt.load_r4(dgt.upload(dgt.pack(w, 2), dev)) for p, w in host.items()}
     del host, base
@@ -698,12 +707,13 @@ def moe_decode_step_extras(dgt, torch, dev):
     per_layer_w = {p: (t.rows * t.cols, bytes_r4(t)) for p, t in first.items()}
     tok_w = tok_r4 = 0.0
     for p, (nw, nb) in per_layer_w.items():
-        f = topk / E if p in ("gate", "up", "down") else 1.0
+        f = topk / E if p in ("gate_up", "down") else 1.0
         tok_w += f * nw
         tok_r4 += f * nb
     out = {"model": m["name"], "layers": L, "hidden": hid, "experts": E, "topk": topk, "batch": 1, "graph": True,
            "attention": "not in the step (value vector repeated over the query heads)",
-           "routing": "drawn per layer, fixed over the replays", "weights_per_token": L * tok_w}
+           "routing": "drawn per layer, fixed over the replays", "weights_per_token": L * tok_w,
+           "stacked": "q|k|v one product; each expert's gate|up one block, one gather"}
     res = {}
     for name, layers, nbytes in (("r4", r4_layers, L * tok_r4), ("bf16", bf_layers, L * tok_w * 2)):
         st = dgt.MoeDecodeStep(layers, gam, routes, E, depth=L)

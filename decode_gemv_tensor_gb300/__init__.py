@@ -109,6 +109,7 @@ def lib():
                                         vp, C.c_size_t, vp, vp]),
             "dgt_add_rmsnorm": (i32, [vp, vp, vp, u64, C.c_float, vp, vp]),
             "dgt_silu_mul": (i32, [vp, vp, u64, vp, vp]),
+            "dgt_silu_mul_rows": (i32, [vp, C.c_uint32, u64, vp, vp]),
             "dgt_repeat": (i32, [vp, u64, u64, vp, vp]),
             "dgt_weighted_sum": (i32, [vp, vp, C.c_uint32, u64, vp, vp]),
             "dgt_exponent_stats": (i32, [vp, u64, C.c_uint32, vp, vp, vp, vp]),
@@ -541,6 +542,18 @@ def silu_mul(g32, u32, out=None, stream=None):
     return out
 
 
+def silu_mul_rows(gu32, out=None, stream=None):
+    """dgt_silu_mul_rows: gu32 float32 [rows, 2n] = [gate | up] per row ->
+    bf16 [rows, n]."""
+    import torch
+    rows, n2 = gu32.shape
+    n = n2 // 2
+    if out is None:
+        out = torch.empty((rows, n), dtype=torch.bfloat16, device=gu32.device)
+    _check(lib().dgt_silu_mul_rows(_ptr(gu32), rows, n, _ptr(out), _stream(stream)), "dgt_silu_mul_rows")
+    return out
+
+
 def repeat(v, n_out, out=None, stream=None):
     """dgt_repeat: out[i] = v[i mod len(v)] (bf16)."""
     import torch
@@ -564,29 +577,44 @@ class DecodeStep:
     and a final h = rmsnorm(x, g_final).  Attention itself is not part of the
     step: the output projection reads the value vector repeated over the query
     heads.  layers: list of dicts proj -> R4 (or bf16 tensors [rows, cols] for
-    the twin); gammas: list of 2 * len(layers) + 1 bf16 vectors.  Layer l of
-    the step uses layers[l % len(layers)] and gammas for its index, so a few
-    distinct layers can stand in for a deeper model.  The R4 step and the BF16
-    step over the same weights give bit-identical outputs."""
+    the twin), either q, k, v, o, gate, up, down, or the stacked form qkv
+    (rows of q, then k, then v; k and v of equal size), o, gate_up (rows of
+    gate, then up) and down, which computes the same step with one product
+    for q, k, v and one for gate and up; gammas: list of 2 * len(layers) + 1
+    bf16 vectors.  Layer l of the step uses layers[l % len(layers)] and gammas
+    for its index, so a few distinct layers can stand in for a deeper model.
+    The R4 step and the BF16 step over the same weights give bit-identical
+    outputs."""
 
     def __init__(self, layers, gammas, depth=None, eps=1e-5, device=None):
         import torch
         self.layers, self.gammas, self.eps = layers, gammas, eps
         self.depth = depth or len(layers)
         w0 = layers[0]
-        self.r4 = isinstance(w0["q"], R4)
+        self.fused = "qkv" in w0
+        self.r4 = isinstance(w0["o"], R4)
         shape = (lambda w: (w.rows, w.cols)) if self.r4 else (lambda w: tuple(w.shape))
-        hidden = shape(w0["q"])[1]
-        dims = {p: shape(w0[p])[0] for p in DENSE_PROJ}
-        dev = device or (w0["q"].sm.device if self.r4 else w0["q"].device)
+        hidden = shape(w0["o"])[0]
+        dims = {p: shape(w0[p])[0] for p in w0}
+        dev = device or (w0["o"].sm.device if self.r4 else w0["o"].device)
         self.hidden = hidden
         f32 = lambda n: torch.empty(n, dtype=torch.float32, device=dev)
         b16 = lambda n: torch.empty(n, dtype=torch.bfloat16, device=dev)
         self.x = f32(hidden)
         self.h = b16(hidden)
-        self.y = {p: (b16(dims[p]), f32(dims[p])) for p in DENSE_PROJ}
-        self.a = b16(dims["q"])
-        self.m = b16(dims["gate"])
+        self.y = {p: (b16(dims[p]), f32(dims[p])) for p in w0}
+        nq = shape(w0["o"])[1]                       # query width: the output projection's input
+        self.ffn = shape(w0["down"])[1]
+        if self.fused:
+            nkv = (dims["qkv"] - nq) // 2
+            self.v16 = self.y["qkv"][0][nq + nkv:nq + 2 * nkv]
+            self.g32 = self.y["gate_up"][1][:self.ffn]
+            self.u32 = self.y["gate_up"][1][self.ffn:]
+        else:
+            self.v16 = self.y["v"][0]
+            self.g32, self.u32 = self.y["gate"][1], self.y["up"][1]
+        self.a = b16(nq)
+        self.m = b16(self.ffn)
         self.out = b16(hidden)
         self._graph = None
         # the step streams its weights before each product's dependency wait
@@ -611,15 +639,15 @@ class DecodeStep:
             add_rmsnorm(self.x, self.gammas[gi % (len(self.gammas) - 1)], self.eps, self.h,
                         None if l == 0 else self.y["down"][1], stream)
             gi += 1
-            for p in ("q", "k", "v"):
+            for p in (("qkv",) if self.fused else ("q", "k", "v")):
                 self._gemv(W[p], self.h, p, stream)
-            repeat(self.y["v"][0], self.a.numel(), self.a, stream)
+            repeat(self.v16, self.a.numel(), self.a, stream)
             self._gemv(W["o"], self.a, "o", stream)
             add_rmsnorm(self.x, self.gammas[gi % (len(self.gammas) - 1)], self.eps, self.h, self.y["o"][1], stream)
             gi += 1
-            self._gemv(W["gate"], self.h, "gate", stream)
-            self._gemv(W["up"], self.h, "up", stream)
-            silu_mul(self.y["gate"][1], self.y["up"][1], self.m, stream)
+            for p in (("gate_up",) if self.fused else ("gate", "up")):
+                self._gemv(W[p], self.h, p, stream)
+            silu_mul(self.g32, self.u32, self.m, stream)
             self._gemv(W["down"], self.m, "down", stream)
         add_rmsnorm(self.x, self.gammas[-1], self.eps, self.out, self.y["down"][1], stream)
 
@@ -678,32 +706,44 @@ class MoeDecodeStep:
     token's h once for all its slots, the down gather takes slot j's m_j as
     its own input.  Routing is an input (the router is not part of the
     format).  layers: dicts with q, k, v, o, gate, up, down (R4, or bf16
-    tensors for the twin); routes: per layer (ids int32 [topk], p float32
-    [topk]) on the device; layer l uses layers[l % len] and routes[l % len].
-    The R4 step and the BF16 step give bit-identical outputs."""
+    tensors for the twin), or the stacked form qkv, o, gate_up, down, where
+    gate_up stacks expert e's gate rows and then its up rows as expert e's
+    block ([E * 2 ffn, hidden]): one product for q, k, v and one gather for
+    gate and up.  routes: per layer (ids int32 [topk], p float32 [topk]) on
+    the device; layer l uses layers[l % len] and routes[l % len].  The R4 step
+    and the BF16 step give bit-identical outputs."""
 
     def __init__(self, layers, gammas, routes, n_experts, depth=None, eps=1e-5):
         import torch
         self.layers, self.gammas, self.routes, self.E, self.eps = layers, gammas, routes, n_experts, eps
         self.depth = depth or len(layers)
         w0 = layers[0]
-        self.r4 = isinstance(w0["q"], R4)
+        self.fused = "qkv" in w0
+        self.r4 = isinstance(w0["o"], R4)
         shape = (lambda w: (w.rows, w.cols)) if self.r4 else (lambda w: tuple(w.shape))
-        hidden = shape(w0["q"])[1]
-        ffn = shape(w0["gate"])[0] // n_experts
+        hidden = shape(w0["o"])[0]
+        ffn = shape(w0["down"])[1]
         topk = routes[0][0].numel()
-        dev = w0["q"].sm.device if self.r4 else w0["q"].device
+        dev = w0["o"].sm.device if self.r4 else w0["o"].device
         self.hidden, self.ffn, self.topk = hidden, ffn, topk
         f32 = lambda *s: torch.empty(s, dtype=torch.float32, device=dev)
         b16 = lambda *s: torch.empty(s, dtype=torch.bfloat16, device=dev)
         self.x, self.h, self.out = f32(hidden), b16(hidden), b16(hidden)
-        self.y = {p: (b16(shape(w0[p])[0]), f32(shape(w0[p])[0])) for p in ("q", "k", "v", "o")}
-        self.a = b16(shape(w0["q"])[0])
-        self.yg, self.yu = f32(1, topk, ffn), f32(1, topk, ffn)
+        attn = ("qkv", "o") if self.fused else ("q", "k", "v", "o")
+        self.y = {p: (b16(shape(w0[p])[0]), f32(shape(w0[p])[0])) for p in attn}
+        nq = shape(w0["o"])[1]
+        if self.fused:
+            nkv = (shape(w0["qkv"])[0] - nq) // 2
+            self.v16 = self.y["qkv"][0][nq + nkv:nq + 2 * nkv]
+            self.ygu = f32(1, topk, 2 * ffn)
+        else:
+            self.v16 = self.y["v"][0]
+            self.yg, self.yu = f32(1, topk, ffn), f32(1, topk, ffn)
+        self.a = b16(nq)
         self.m = b16(topk, ffn)
         self.yd = f32(topk, 1, hidden)
         self.comb = f32(hidden)
-        nb_up = moe_workspace_bytes(n_experts, ffn, hidden, 1, topk)
+        nb_up = moe_workspace_bytes(n_experts, 2 * ffn if self.fused else ffn, hidden, 1, topk)
         nb_dn = moe_workspace_bytes(n_experts, hidden, ffn, topk, 1)
         self.ws_g = torch.empty(max(nb_up, 256), dtype=torch.uint8, device=dev)
         self.ws_u = torch.empty(max(nb_up, 256), dtype=torch.uint8, device=dev)
@@ -728,15 +768,19 @@ class MoeDecodeStep:
             W = self.layers[l % len(self.layers)]
             ids, p = self.routes[l % len(self.routes)]
             add_rmsnorm(self.x, self.gammas[(2 * l) % ng], self.eps, self.h, None if l == 0 else self.comb, stream)
-            for pr in ("q", "k", "v"):
+            for pr in (("qkv",) if self.fused else ("q", "k", "v")):
                 self._gemv(W[pr], self.h, pr, stream)
-            repeat(self.y["v"][0], self.a.numel(), self.a, stream)
+            repeat(self.v16, self.a.numel(), self.a, stream)
             self._gemv(W["o"], self.a, "o", stream)
             add_rmsnorm(self.x, self.gammas[(2 * l + 1) % ng], self.eps, self.h, self.y["o"][1], stream)
             ids1 = ids.view(1, self.topk)
-            self._moe(W["gate"], ids1, self.h.view(1, -1), self.ws_g, self.yg, stream)
-            self._moe(W["up"], ids1, self.h.view(1, -1), self.ws_u, self.yu, stream)
-            silu_mul(self.yg, self.yu, self.m.view(-1), stream)
+            if self.fused:
+                self._moe(W["gate_up"], ids1, self.h.view(1, -1), self.ws_g, self.ygu, stream)
+                silu_mul_rows(self.ygu.view(self.topk, 2 * self.ffn), self.m, stream)
+            else:
+                self._moe(W["gate"], ids1, self.h.view(1, -1), self.ws_g, self.yg, stream)
+                self._moe(W["up"], ids1, self.h.view(1, -1), self.ws_u, self.yu, stream)
+                silu_mul(self.yg, self.yu, self.m.view(-1), stream)
             self._moe(W["down"], ids.view(self.topk, 1), self.m, self.ws_d, self.yd, stream)
             weighted_sum(self.yd, p, self.comb, stream)
         add_rmsnorm(self.x, self.gammas[-1], self.eps, self.out, self.comb, stream)

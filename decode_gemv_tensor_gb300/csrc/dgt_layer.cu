@@ -69,6 +69,22 @@ __global__ void __launch_bounds__(256) k_silu_mul(const float *__restrict__ g, c
     }
 }
 
+// Row r of gu holds [gate (n) | up (n)]: out[r, i] = bf16(silu(gate) * up),
+// the same per-element arithmetic as k_silu_mul.
+__global__ void __launch_bounds__(256) k_silu_mul_rows(const float *__restrict__ gu, uint32_t rows, uint64_t n,
+                                                      uint16_t *__restrict__ out) {
+    pdl_trigger();
+    pdl_wait();
+    const uint64_t total = (uint64_t)rows * n;
+    for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (uint64_t)gridDim.x * blockDim.x) {
+        const uint64_t r = i / n, c = i - r * n;
+        const float a = gu[r * 2 * n + c];
+        const float s = a / (1.0f + expf(-a));
+        out[i] = f32_to_bf16_rne(s * gu[r * 2 * n + n + c]);
+    }
+}
+
 // out[i] = v[i mod n_in].
 __global__ void __launch_bounds__(256) k_repeat(const uint16_t *__restrict__ v, uint64_t n_in, uint64_t n_out,
                                                uint16_t *__restrict__ out) {
@@ -120,6 +136,17 @@ extern "C" int dgt_silu_mul(const float *d_g, const float *d_u, uint64_t n, uint
     if (n == 0) return DGT_OK;
     return launch_pdl(k_silu_mul, dim3(elem_grid(n)), dim3(256), 0, (cudaStream_t)stream, d_g, d_u, n, d_out) ==
                    cudaSuccess
+               ? DGT_OK
+               : DGT_ERR_CUDA;
+}
+
+extern "C" int dgt_silu_mul_rows(const float *d_gu, uint32_t rows, uint64_t n, uint16_t *d_out, void *stream) {
+    if (!d_gu || !d_out) return DGT_ERR_ARG;
+    if (n == 0 || rows == 0) return DGT_OK;
+    const uint64_t total = (uint64_t)rows * n;
+    if (total / rows != n) return DGT_ERR_SHAPE;
+    return launch_pdl(k_silu_mul_rows, dim3(elem_grid(total)), dim3(256), 0, (cudaStream_t)stream, d_gu, rows, n,
+                      d_out) == cudaSuccess
                ? DGT_OK
                : DGT_ERR_CUDA;
 }

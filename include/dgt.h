@@ -458,6 +458,12 @@ int dgt_moe_gemv_noalloc(const dgt_r4 *W, uint32_t n_experts, const int32_t *d_i
 int dgt_add_rmsnorm(float *d_x, const float *d_y, const uint16_t *d_gamma, uint64_t n, float eps, uint16_t *d_h,
                     void *stream);
 int dgt_silu_mul(const float *d_g, const float *d_u, uint64_t n, uint16_t *d_out, void *stream);
+
+/* The same for stacked pairs: row r of d_gu (float32 [rows, 2n]) holds
+   [gate | up]; d_out (bf16 [rows, n]) row r = bf16(silu(gate) * up), the
+   per-element arithmetic of dgt_silu_mul.  Used after a product whose rows
+   stack each gate row block with its up block (one launch for both). */
+int dgt_silu_mul_rows(const float *d_gu, uint32_t rows, uint64_t n, uint16_t *d_out, void *stream);
 int dgt_repeat(const uint16_t *d_v, uint64_t n_in, uint64_t n_out, uint16_t *d_out, void *stream);
 int dgt_weighted_sum(const float *d_y, const float *d_p, uint32_t slots, uint64_t n, float *d_out, void *stream);
 

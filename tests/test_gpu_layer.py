@@ -208,3 +208,76 @@ def test_r4_clone_is_independent(dgt):
     r4.nib.zero_()
     y1, _ = dgt.gemv(c, x)
     assert torch.equal(y0.view(torch.int16), y1.view(torch.int16))
+
+
+@pytest.mark.parametrize("rows,n", [(1, 5), (8, 704), (3, 8192)])
+def test_silu_mul_rows_matches_oracle_and_flat_kernel(dgt, rows, n):
+    g = np.random.default_rng(rows * 1000 + n)
+    gu = (2 * g.normal(size=(rows, 2 * n))).astype(np.float32)
+    gd = torch.from_numpy(gu).cuda()
+    out = dgt.silu_mul_rows(gd)
+    ref = oracle.f64_to_bf16(oracle.silu_mul_f64(gu[:, :n].astype(np.float64), gu[:, n:].astype(np.float64)))
+    assert _ulp_diff(_bits(out).reshape(rows, n), ref.reshape(rows, n)).max() <= 1
+    for r in range(rows):     # the same arithmetic as the flat kernel, row by row
+        flat = dgt.silu_mul(gd[r, :n].contiguous(), gd[r, n:].contiguous())
+        assert torch.equal(flat.view(torch.int16), out[r].view(torch.int16))
+
+
+def _stack_dense(L):
+    return {"qkv": np.concatenate([L["q"], L["k"], L["v"]]), "o": L["o"],
+            "gate_up": np.concatenate([L["gate"], L["up"]]), "down": L["down"]}
+
+
+@pytest.mark.parametrize("hid,kv,ffn,nl,depth", [(512, 128, 1024, 2, 3), (1024, 256, 2816, 1, 2)])
+def test_decode_step_stacked_twins_graph_and_oracle(dgt, hid, kv, ffn, nl, depth):
+    host = _layers(hid, kv, ffn, nl, 621)
+    gam = _gammas(hid, nl, 622)
+    r4, bf, gd = _build(dgt, [_stack_dense(L) for L in host], gam)
+    x0 = np.random.default_rng(623).normal(size=hid).astype(np.float32)
+    x0d = torch.from_numpy(x0).cuda()
+    sr, sb = dgt.DecodeStep(r4, gd, depth=depth), dgt.DecodeStep(bf, gd, depth=depth)
+    assert sr.fused and sb.fused
+    xr, hr = (t.clone() for t in sr(x0d))
+    xb, hb = (t.clone() for t in sb(x0d))
+    assert torch.equal(xr.view(torch.int32), xb.view(torch.int32))
+    assert torch.equal(hr.view(torch.int16), hb.view(torch.int16))
+    sr.capture()
+    xg, hg = sr.replay(x0d)
+    assert torch.equal(xg.view(torch.int32), xr.view(torch.int32))
+    xo, ho = oracle.decode_step_f64(host, gam, x0, depth=depth)
+    assert np.linalg.norm(xr.cpu().numpy() - xo) / np.linalg.norm(xo) <= 1e-2
+    ref = oracle.bf16_to_f64(ho)
+    assert np.linalg.norm(oracle.bf16_to_f64(_bits(hr)) - ref) / np.linalg.norm(ref) <= 2e-2
+
+
+def _stack_moe(L, E, ffn):
+    gu = np.concatenate([np.concatenate([L["gate"][e * ffn:(e + 1) * ffn], L["up"][e * ffn:(e + 1) * ffn]])
+                         for e in range(E)])
+    return {"qkv": np.concatenate([L["q"], L["k"], L["v"]]), "o": L["o"], "gate_up": gu, "down": L["down"]}
+
+
+def test_moe_decode_step_stacked_twins_graph_and_oracle(dgt):
+    hid, kv, ffn, E, topk, nl, depth = 512, 128, 256, 8, 4, 2, 3
+    host = _moe_layers(hid, kv, ffn, E, nl, 624)
+    gam = _gammas(hid, nl, 625)
+    r4, bf, gd = _build(dgt, [_stack_moe(L, E, ffn) for L in host], gam)
+    routes_h = []
+    for l in range(nl):
+        ids, p = S.routing(1, E, topk, (626, 777, l, 0))
+        routes_h.append((ids.reshape(-1), p.reshape(-1)))
+    routes = [(torch.from_numpy(i.astype(np.int32)).cuda(), torch.from_numpy(p.astype(np.float32)).cuda())
+              for i, p in routes_h]
+    x0 = np.random.default_rng(627).normal(size=hid).astype(np.float32)
+    x0d = torch.from_numpy(x0).cuda()
+    sr = dgt.MoeDecodeStep(r4, gd, routes, E, depth=depth)
+    sb = dgt.MoeDecodeStep(bf, gd, routes, E, depth=depth)
+    assert sr.fused and sb.fused
+    xr, hr = (t.clone() for t in sr(x0d))
+    xb, hb = (t.clone() for t in sb(x0d))
+    assert torch.equal(xr.view(torch.int32), xb.view(torch.int32))
+    assert torch.equal(hr.view(torch.int16), hb.view(torch.int16))
+    sr.capture()
+    xg, hg = sr.replay(x0d)
+    assert torch.equal(xg.view(torch.int32), xr.view(torch.int32))
+    xo, ho = oracle.decode_step_moe_f64(host, gam, routes_h, E, x0, depth=depth)
+    assert np.linalg.norm(xr.cpu().numpy() - xo) / np.linalg.norm(xo) <= 1e-2
