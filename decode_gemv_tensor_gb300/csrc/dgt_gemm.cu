@@ -34,9 +34,7 @@
 
 #include "../../include/dgt.h"
 #include "dgt_device.cuh"
-#include "dgt_internal.h"
 #include "dgt_launch.h"
-#include "dgt_r4esc.cuh"
 
 namespace dgt {
 
@@ -48,7 +46,6 @@ constexpr uint32_t GT_SMEM_LIMIT = 200 * 1024;
 struct GemmArgs {
     const uint8_t *nib, *esc;
     const uint32_t *seg;
-    const uint32_t *rsum;   // per-round escape summaries (second part of seg)
     uint64_t n_esc, nseg;
     uint64_t M, N, K;
     uint32_t mt, kb_total, split, stages;
@@ -159,59 +156,58 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, ui
 
 // Decoder thread (row t, chunk q): the 16 weights [16q, 16q + 16) of W row t
 // of a stage, from the raw tiles (shared addresses raw_sm, raw_nib of the
-// row) into the row's swizzled bf16 chunks 2q and 2q+1 (arow).  rw is the
-// summary of the row's current 512-column round (escape count c, exponents
-// of its first three escapes):
-//  - c = 0: the plain decode;
-//  - c = 1: the round's one 15-nibble is its escape: the decode with the
-//    table's rank-15 entry replaced by the escape's exponent;
-//  - c >= 2: the four chunk threads of the row (lanes 4j..4j+3) number their
-//    15-nibbles by a prefix sum from rc (the round's escapes before this
-//    stage) and patch each from the summary (first three) or from esc
-//    (index seg[row, round] + number; rare).
+// row) into the row's swizzled bf16 chunks 2q and 2q+1 (arow).  The four
+// chunk threads of a row are lanes 4j..4j+3 of one warp; they place their
+// escapes by a prefix sum over the four and advance the row's running escape
+// index eidx.  r0, r1: the ranks of the row's next two escapes (esc[eidx],
+// esc[eidx + 1]), loaded ahead.  A chunk with one escape that is among those
+// two decodes with the exponent table's rank-15 entry replaced by its
+// exponent; any other escape is patched weight by weight.
 __device__ __forceinline__ void decode_chunk16(const GemmArgs &a, const R4Lut &L, uint32_t raw_sm,
                                                uint32_t raw_nib, uint32_t arow, uint32_t t, uint32_t q,
-                                               uint32_t lane, uint32_t rw, uint32_t &rc, uint64_t sx,
+                                               uint64_t &eidx, uint32_t &r0, uint32_t &r1,
                                                const uint8_t *table_s, bool &bad) {
     const uint4 sv = lds128(raw_sm + q * 16);
     const uint2 nv = lds64(raw_nib + q * 8);
-    const uint32_t cnt = rw & 0xFFu;
+    const uint32_t m0 = nib15_mask(nv.x), m1 = nib15_mask(nv.y);
+    const uint32_t c = __popc(m0) + __popc(m1);
+    uint32_t incl = c;
+    uint32_t y = __shfl_up_sync(DGT_FULL, incl, 1, 4);
+    if (q >= 1) incl += y;
+    y = __shfl_up_sync(DGT_FULL, incl, 2, 4);
+    if (q >= 2) incl += y;
+    const uint32_t total = __shfl_sync(DGT_FULL, incl, 3, 4);
+    const uint32_t before = incl - c;
+    const bool one = c == 1 && before < 2;
+    R4Lut Lr = L;
+    if (one) {
+        const uint32_t rk = before == 0 ? r0 : r1;
+        Lr.h3 = prmt(L.h3, table_s[rk] >> 1, 0x4210u);
+        Lr.l1 = (L.l1 & 0x7FFFFFFFu) | ((table_s[rk] & 1u) << 31);
+    }
     uint32_t p[8];
-    if (cnt <= 1) {
-        r4_dec16(nv, sv, cnt ? lut15(L, (rw >> 8) & 0xFFu) : L, p);
-    } else {
-        const uint32_t gm = 0xFu << (lane & 28u);
-        const uint32_t m0 = nib15_mask(nv.x), m1 = nib15_mask(nv.y);
-        const uint32_t c = __popc(m0) + __popc(m1);
-        uint32_t incl = c;
-        uint32_t y = __shfl_up_sync(gm, incl, 1, 4);
-        if (q >= 1) incl += y;
-        y = __shfl_up_sync(gm, incl, 2, 4);
-        if (q >= 2) incl += y;
-        const uint32_t total = __shfl_sync(gm, incl, 3, 4);
-        uint32_t e = rc + incl - c;   // this chunk's first escape, numbered within the round
-        r4_dec16(nv, sv, L, p);
-        if (c) {
-            const uint64_t b0 = cnt > 3 ? a.seg[sx] : 0;
+    r4_dec16(nv, sv, Lr, p);
+    if (c && !one) {
+        uint64_t e = eidx + before;
 #pragma unroll
-            for (int i = 0; i < 16; i++) {
-                const uint32_t m = i < 8 ? m0 : m1;
-                if ((m >> (4 * (i & 7))) & 1u) {
-                    uint32_t ex = 0;
-                    if (cnt <= 3) {
-                        if (e < cnt) ex = (rw >> (8 + 8 * e)) & 0xFFu;
-                        else bad = true;
-                    } else {
-                        if (b0 + e < a.n_esc) ex = table_s[a.esc[b0 + e]];
-                        else bad = true;
-                    }
-                    e++;
-                    const uint32_t sh = 16 * (i & 1);
-                    p[i >> 1] = (p[i >> 1] & ~(0x7F80u << sh)) | (ex << (7 + sh));
-                }
+        for (int i = 0; i < 16; i++) {
+            const uint32_t m = i < 8 ? m0 : m1;
+            if ((m >> (4 * (i & 7))) & 1u) {
+                uint32_t ex = 0;
+                if (e < a.n_esc) ex = table_s[a.esc[e]];
+                else bad = true;
+                e++;
+                const uint32_t sh = 16 * (i & 1);
+                p[i >> 1] = (p[i >> 1] & ~(0x7F80u << sh)) | (ex << (7 + sh));
             }
         }
-        rc += total;
+    } else if (one && eidx + before >= a.n_esc) {
+        bad = true;
+    }
+    if (total) {
+        eidx += total;
+        r0 = eidx < a.n_esc ? a.esc[eidx] : 0u;
+        r1 = eidx + 1 < a.n_esc ? a.esc[eidx + 1] : 0u;
     }
     const uint32_t c0 = (2 * q) ^ (t & 7), c1 = (2 * q + 1) ^ (t & 7);
     sts128(arow + c0 * 16, p[0], p[1], p[2], p[3]);
@@ -350,13 +346,8 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
             const bool rin = row < a.N;   // rows past the tensor (grouped tail tiles) read zeros
             const uint64_t kstart = (uint64_t)kb0 * GT_K;
             const uint64_t j = kstart / DGT_SEG;
-            // the current round's summary and the next one's (loaded a round
-            // ahead); rc: the round's escapes before the current stage
-            uint64_t sx = row * a.nseg + j;
-            uint32_t rw = rin ? a.rsum[sx] : 0u;
-            uint32_t rwn = (rin && j + 1 < a.nseg) ? a.rsum[sx + 1] : 0u;
-            uint32_t rc = 0;
-            if (rin && kstart % DGT_SEG) {
+            uint64_t eidx = rin ? a.seg[row * a.nseg + j] : a.n_esc;
+            if (rin) {
                 // escapes of this row's segment before kstart: at most 448 nibbles,
                 // read as up to 14 independent 16-byte loads
                 const uint4 *np = reinterpret_cast<const uint4 *>(a.nib + (row * a.K + j * DGT_SEG) / 2);
@@ -370,7 +361,7 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
                                __popc(nib15_mask(qv.w));
                     }
                 }
-                rc = cnt;
+                eidx += cnt;
             }
             bool bad = false;
             R4Lut L;
@@ -380,6 +371,8 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
             L.h3 = a.L.h3;
             L.l0 = a.L.l0;
             L.l1 = a.L.l1;
+            uint32_t r0 = eidx < a.n_esc ? a.esc[eidx] : 0u;
+            uint32_t r1 = eidx + 1 < a.n_esc ? a.esc[eidx + 1] : 0u;
             const uint32_t base_a = smem_u32(base);
             uint32_t s = 0, par = 0;
             for (uint32_t i = 0; i < nkb; i++) {
@@ -389,16 +382,8 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
                     break;
                 }
                 const uint32_t st0 = base_a + s * SB;
-                const uint64_t k = kstart + (uint64_t)i * GT_K;
-                if (i > 0 && k % DGT_SEG == 0) {
-                    // a new round
-                    sx++;
-                    rw = rwn;
-                    rwn = (rin && (k / DGT_SEG) + 1 < a.nseg) ? a.rsum[sx + 1] : 0u;
-                    rc = 0;
-                }
                 decode_chunk16(a, L, st0 + GT_N * 128 + mt * 128 + t * 64, st0 + GT_N * 128 + mt * 128 + GT_N * 64 + t * 32,
-                               st0 + t * 128, t, q, lane, rw, rc, sx, table_s, bad);
+                               st0 + t * 128, t, q, eidx, r0, r1, table_s, bad);
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&bar_w[s]));
@@ -888,7 +873,6 @@ extern "C" int dgt_moe_gemm(const dgt_r4 *W, uint32_t n_experts, const int32_t *
     g.nib = W->nib;
     g.esc = W->esc;
     g.seg = W->seg;
-    g.rsum = W->seg + dgt_rsum_offset(W->rows, dgt_r4_nseg(W->cols));
     g.n_esc = W->n_esc;
     g.nseg = dgt_r4_nseg(W->cols);
     g.L = make_r4lut(W->table, W->n_table);
@@ -945,7 +929,6 @@ extern "C" int dgt_gemm(const dgt_r4 *W, const uint16_t *d_X, uint64_t M, float 
     a.nib = W->nib;
     a.esc = W->esc;
     a.seg = W->seg;
-    a.rsum = W->seg + dgt_rsum_offset(W->rows, dgt_r4_nseg(W->cols));
     a.n_esc = W->n_esc;
     a.nseg = dgt_r4_nseg(W->cols);
     a.L = make_r4lut(W->table, W->n_table);
