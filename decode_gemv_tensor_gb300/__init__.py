@@ -7,7 +7,11 @@ This module only marshals arguments: numpy arrays for host data, torch tensors
 for device memory and streams.  It fails loudly when libdgt.so is missing.
 
 Names follow the C ABI: pack, unpack, write, read, upload, load_r4,
-r4_to_bf16, gemv, gemv_bf16, gemv_slices, read_status.
+load_r4_into, r4_to_bf16, gemv, gemv_bf16, gemv_slices, moe_gemv,
+moe_gemv_bf16, gemm, gemm_bf16, gemm_plan, moe_gemm, moe_gemm_bf16,
+add_rmsnorm, silu_mul, silu_mul_rows, repeat, weighted_sum, exponent_stats,
+read_status; DecodeStep and MoeDecodeStep compose a batch-1 decode step from
+them and capture it in a CUDA graph.
 """
 from __future__ import annotations
 
