@@ -8,7 +8,7 @@ for device memory and streams.  It fails loudly when libdgt.so is missing.
 
 Names follow the C ABI: pack, unpack, write, read, upload, load_r4,
 load_r4_into, r4_to_bf16, gemv, gemv_bf16, gemv_slices, moe_gemv,
-moe_gemv_bf16, gemm, gemm_bf16, gemm_plan, moe_gemm, moe_gemm_bf16,
+moe_gemv_bf16, gemm, gemm_bf16, gemm_rebuild, gemm_plan, moe_gemm, moe_gemm_bf16,
 add_rmsnorm, silu_mul, silu_mul_rows, repeat, weighted_sum, exponent_stats,
 read_status; DecodeStep and MoeDecodeStep compose a batch-1 decode step from
 them and capture it in a CUDA graph.
@@ -99,6 +99,8 @@ def lib():
             "dgt_gemm_workspace_bytes": (C.c_size_t, [u64, u64, C.POINTER(GemmPlan)]),
             "dgt_gemm": (i32, [C.POINTER(R4Struct), vp, u64, vp, vp, C.POINTER(GemmPlan), vp, C.c_size_t, vp, vp]),
             "dgt_gemm_bf16": (i32, [vp, u64, u64, vp, u64, vp, vp, C.POINTER(GemmPlan), vp, C.c_size_t, vp, vp]),
+            "dgt_gemm_rebuild": (i32, [C.POINTER(R4Struct), vp, u64, vp, vp, C.POINTER(GemmPlan), vp, vp, C.c_size_t,
+                                       vp, vp]),
             "dgt_moe_workspace_bytes": (C.c_size_t, [C.c_uint32, u64, u64, C.c_uint32, C.c_uint32]),
             "dgt_moe_gemv": (i32, [C.POINTER(R4Struct), C.c_uint32, vp, vp, C.c_uint32, C.c_uint32, vp, vp, vp,
                                    vp, vp, C.c_size_t, vp, vp]),
@@ -518,6 +520,22 @@ def gemm_bf16(W, X, plan=None, Y32=None, Y=None, ws=None, status=None, stream=No
     Y32, Y, ws = _gemm_out(M, N, W.device, Y32, Y, plan, ws)
     _check(lib().dgt_gemm_bf16(_ptr(W), N, K, _ptr(X), M, _ptr(Y32), _ptr(Y), C.byref(plan), _ptr(ws),
                                0 if ws is None else ws.numel(), _ptr(status), _stream(stream)), "dgt_gemm_bf16")
+    return Y32, Y
+
+
+def gemm_rebuild(W: R4, X, scratch=None, plan=None, Y32=None, Y=None, ws=None, status=None, stream=None):
+    """dgt_gemm_rebuild: the R4 weights rebuilt to bf16 in `scratch` (allocated
+    when None), then the bf16 GEMM (for long prompts).  Returns (Y32, Y)."""
+    import torch
+    M, K = X.shape
+    N = W.rows
+    plan = plan or gemm_plan(M, N, K)
+    if scratch is None:
+        scratch = torch.empty((N, K), dtype=torch.bfloat16, device=W.sm.device)
+    Y32, Y, ws = _gemm_out(M, N, W.sm.device, Y32, Y, plan, ws)
+    _check(lib().dgt_gemm_rebuild(C.byref(W.s), _ptr(X), M, _ptr(Y32), _ptr(Y), C.byref(plan), _ptr(scratch),
+                                  _ptr(ws), 0 if ws is None else ws.numel(), _ptr(status), _stream(stream)),
+           "dgt_gemm_rebuild")
     return Y32, Y
 
 

@@ -528,7 +528,7 @@ static int launch_gemm(GemmArgs &a, const void *w_or_sm, const uint16_t *d_X, vo
 }
 
 static int fill_common(GemmArgs &a, uint64_t M, uint64_t N, uint64_t K, const dgt_gemm_plan *plan, float *d_Y32,
-                       uint16_t *d_Y, int32_t *d_status, cudaStream_t st) {
+                       uint16_t *d_Y, int32_t *d_status, cudaStream_t st, bool reset = true) {
     if (M == 0 || N == 0 || K == 0) return DGT_ERR_SHAPE;
     if (N % GT_N || K % GT_K || M >= (1ull << 31) || N >= (1ull << 31) || K >= (1ull << 31)) return DGT_ERR_SHAPE;
     if (!d_Y32 && !d_Y) return DGT_ERR_ARG;
@@ -546,8 +546,22 @@ static int fill_common(GemmArgs &a, uint64_t M, uint64_t N, uint64_t K, const dg
     a.y32 = d_Y32;
     a.y = d_Y;
     a.status = d_status;
-    if (d_status && cudaMemsetAsync(d_status, 0, 4, st) != cudaSuccess) return DGT_ERR_CUDA;
+    if (reset && d_status && cudaMemsetAsync(d_status, 0, 4, st) != cudaSuccess) return DGT_ERR_CUDA;
     return DGT_OK;
+}
+
+// The bf16 GEMM; reset = false keeps the status word as an earlier call of
+// the same stream left it.
+static int gemm_bf16_impl(const uint16_t *d_W, uint64_t N, uint64_t K, const uint16_t *d_X, uint64_t M,
+                          float *d_Y32, uint16_t *d_Y, const dgt_gemm_plan *plan, void *d_ws, size_t ws_bytes,
+                          int32_t *d_status, cudaStream_t st, bool reset) {
+    if (!d_W || !d_X) return DGT_ERR_ARG;
+    GemmArgs a = {};
+    int rc = fill_common(a, M, N, K, plan, d_Y32, d_Y, d_status, st, reset);
+    if (rc != DGT_OK) return rc;
+    if (!aligned16(d_W) || !aligned16(d_X)) return DGT_ERR_ARG;
+    a.stages = gemm_stages(false, a.mt);
+    return launch_gemm<false>(a, d_W, d_X, d_ws, ws_bytes, st);
 }
 
 // ---- grouped expert products ---------------------------------------------------
@@ -937,15 +951,18 @@ extern "C" int dgt_gemm(const dgt_r4 *W, const uint16_t *d_X, uint64_t M, float 
     return launch_gemm<true>(a, W->sm, d_X, d_ws, ws_bytes, st);
 }
 
+extern "C" int dgt_gemm_rebuild(const dgt_r4 *W, const uint16_t *d_X, uint64_t M, float *d_Y32, uint16_t *d_Y,
+                                const dgt_gemm_plan *plan, uint16_t *d_scratch, void *d_ws, size_t ws_bytes,
+                                int32_t *d_status, void *stream) {
+    if (!W || !d_scratch) return DGT_ERR_ARG;
+    int rc = dgt_r4_to_bf16(W, d_scratch, d_status, stream);   // resets d_status, then may set it
+    if (rc != DGT_OK) return rc;
+    return gemm_bf16_impl(d_scratch, W->rows, W->cols, d_X, M, d_Y32, d_Y, plan, d_ws, ws_bytes, d_status,
+                          (cudaStream_t)stream, false);
+}
+
 extern "C" int dgt_gemm_bf16(const uint16_t *d_W, uint64_t N, uint64_t K, const uint16_t *d_X, uint64_t M,
                              float *d_Y32, uint16_t *d_Y, const dgt_gemm_plan *plan, void *d_ws, size_t ws_bytes,
                              int32_t *d_status, void *stream) {
-    if (!d_W || !d_X) return DGT_ERR_ARG;
-    cudaStream_t st = (cudaStream_t)stream;
-    GemmArgs a = {};
-    int rc = fill_common(a, M, N, K, plan, d_Y32, d_Y, d_status, st);
-    if (rc != DGT_OK) return rc;
-    if (!aligned16(d_W) || !aligned16(d_X)) return DGT_ERR_ARG;
-    a.stages = gemm_stages(false, a.mt);
-    return launch_gemm<false>(a, d_W, d_X, d_ws, ws_bytes, st);
+    return gemm_bf16_impl(d_W, N, K, d_X, M, d_Y32, d_Y, plan, d_ws, ws_bytes, d_status, (cudaStream_t)stream, true);
 }

@@ -366,6 +366,21 @@ int dgt_gemm_bf16(const uint16_t *d_W, uint64_t N, uint64_t K, const uint16_t *d
                   void *stream);
 
 /*
+ * Long prompts from R4 weights by the rebuilt-weight path (Binade README,
+ * "NVIDIA GPUs": the runtime rebuilds the BF16 weight where no fused kernel
+ * applies): dgt_r4_to_bf16 of W into d_scratch (device, W->rows * W->cols
+ * bf16, 16-byte aligned, caller-owned), then dgt_gemm_bf16 on it with the
+ * same plan and workspace rules.  Its outputs are the bf16 GEMM's, and so
+ * bit-identical to dgt_gemm's.  At 2048 rows of a 4096 x 3840 tensor it runs
+ * at 0.88x the bf16 GEMM's speed where the fused dgt_gemm runs at 0.68x; at
+ * 128 rows the fused product is faster.  d_status: reset once, then the
+ * rebuild's and the product's errors.  Errors: as the two calls.
+ */
+int dgt_gemm_rebuild(const dgt_r4 *W, const uint16_t *d_X, uint64_t M, float *d_Y32, uint16_t *d_Y,
+                     const dgt_gemm_plan *plan, uint16_t *d_scratch, void *d_ws, size_t ws_bytes, int32_t *d_status,
+                     void *stream);
+
+/*
  * Expert products at prompt length on the tensor cores (Binade README,
  * "Results": the fused prompt kernels cover every expert product).  W holds
  * n_experts stacked experts (rows = n_experts * Ne, expert e = rows

@@ -83,3 +83,18 @@ def test_gemm_12b_shapes(dgt, M):
         ref = oracle.gemm_f64(X[rows], W, cols=cols)
         got = y32.cpu().numpy()[np.ix_(rows, cols)]
         assert _normwise(got, ref) <= 1e-3, (name, M)
+
+
+@pytest.mark.parametrize("M,N,K,split", [(16, 256, 512, 1), (300, 384, 1024, 3), (2048, 128, 640, 1)])
+def test_gemm_rebuild_is_the_bf16_gemm(dgt, M, N, K, split):
+    # rebuild-then-bf16 gives the fused R4 GEMM's bits (and the bf16 GEMM's)
+    W = S.weights(N, K, (502, N, K), outliers=True)
+    X = S.activations(K, (502, 999, M), count=M).reshape(M, K)
+    plan = dgt.gemm_plan(M, N, K, split_k=split)
+    y32, y16, b32, b16 = _both(dgt, W, X, plan=plan)
+    r4 = dgt.load_r4(dgt.upload(dgt.pack(W, 2)))
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    r32, r16 = dgt.gemm_rebuild(r4, _dev_bf16(X), plan=plan, status=st)
+    assert dgt.read_status(st) == 0
+    assert torch.equal(r32.view(torch.int32), y32.view(torch.int32))
+    assert torch.equal(r16.view(torch.int16), b16.view(torch.int16))
