@@ -373,7 +373,10 @@ def run_ours(args, rank, world, dist):
                                                         Y=it["h16"], ws=it["gws"], stream=stream) for it in items])
 
     split_launches = sum(2 if it["plan"].split_k > 1 else 1 for it in items)
-    launches_per_step = 5 * BATCH + 2 * 3 * len(moe_runs) + 2 * split_launches
+    # per tensor: two transcodes of two kernels each (decode, round summaries),
+    # the rebuild and the two GEMVs; per MoE run three kernels per format;
+    # the GEMMs (with their split-K reductions)
+    launches_per_step = 7 * BATCH + 2 * 3 * len(moe_runs) + 2 * split_launches
     moe_bytes = {"moe_r4": sum(r["bytes_r4"] for r in moe_runs), "moe_bf16": sum(r["bytes_bf16"] for r in moe_runs)}
     op_bytes = {k: sum(it["bytes"][k] for it in items) for k in KERNELS if not k.startswith("moe")}
     op_bytes.update(moe_bytes)
