@@ -441,6 +441,7 @@ def run_ours(args, rank, world, dist):
     more = rank == 0 and not args.no_extras
     extras = gemm_extras(dgt, torch, dev) if more else None
     mgemm = moe_gemm_extras(dgt, torch, dev) if more else None
+    projs = projection_extras(dgt, torch, dev) if more else None
     dstep = decode_step_extras(dgt, torch, dev) if more and not args.no_decode_step else None
     mstep = moe_decode_step_extras(dgt, torch, dev) if more and not args.no_decode_step else None
 
@@ -507,7 +508,7 @@ def run_ours(args, rank, world, dist):
                              "rice_to_r4_gsym_s": kern["rice_to_r4"]["gsym_s"],
                              "rice_to_r4_frac": kern["rice_to_r4"]["frac"],
                              "r4_vs_bf16_gemv_speedup": kern["gemv_bf16"]["ms_avg"] / kern["gemv_r4"]["ms_avg"]},
-                "kernels": kern, "roofline": roof, "gemm_tensor": extras, "moe_gemm": mgemm, "decode_step": dstep, "decode_step_moe": mstep, "cpu_baseline": cpu, "e2e": e2e,
+                "kernels": kern, "roofline": roof, "gemm_tensor": extras, "moe_gemm": mgemm, "projections": projs, "decode_step": dstep, "decode_step_moe": mstep, "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": launches_per_step * args.steps, "clocks": clk,
                 "gpu": torch.cuda.get_device_name(dev)}
         print(json.dumps(line), flush=True)
@@ -561,6 +562,54 @@ def gemm_extras(dgt, torch, dev):
             res[name] = {"ms": t, "tflops": tf, "frac": tf / tpk}
         out[f"M{M}"] = {"shape": [M, N, K], "plan": [plan.m_tile, plan.split_k], "bound": "tensor",
                         "peak_tflops": tpk, "peak_kind": tkind, **res}
+    return out
+
+
+def projection_extras(dgt, torch, dev):
+    """Batch-1 products on every distinct projection shape of the dense-3B and
+    dense-12B stacks: R4 GEMV, the BF16 twin and cuBLAS (torch linear, context
+    only), each the mean of 20 back-to-back launches (median of 5 batches)
+    over enough weight copies to exceed L2, and whether R4 equals the twin."""
+    out = {}
+    for m in (S.DENSE_3B, S.DENSE_12B):
+        for name, N, K in m["proj"]:
+            key = f"{N}x{K}"
+            if key in out:
+                out[key]["proj"].append(f'{m["name"]}:{name}')
+                continue
+            nc = max(2, int(np.ceil(400e6 / (N * K * 1.5))))
+            w = S.weights(N, K, (9, N, K, 0))
+            p = dgt.pack(w, 2)
+            r4s = [dgt.load_r4(dgt.upload(p, dev)) for _ in range(nc)]
+            wbs = [dgt.r4_to_bf16(r) for r in r4s]
+            x = torch.from_numpy(S.activations(K, (9, 999, 0)).view(np.int16)).to(dev).view(torch.bfloat16)
+            y, y32 = dgt.gemv(r4s[0], x)
+            b, b32 = dgt.gemv_bf16(wbs[0], x)
+            same = bool(torch.equal(y32.view(torch.int32), b32.view(torch.int32)))
+            st = torch.cuda.current_stream(dev)
+
+            def tm(fn):
+                for i in range(nc):
+                    fn(i)
+                res = []
+                for _ in range(5):
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record(st)
+                    for i in range(20):
+                        fn(i % nc)
+                    e1.record(st)
+                    torch.cuda.synchronize()
+                    res.append(e0.elapsed_time(e1) / 20 * 1e3)
+                return sorted(res)[2]
+            t4 = tm(lambda i: dgt.gemv(r4s[i], x, y, y32, stream=st, static_weights=True))
+            tb = tm(lambda i: dgt.gemv_bf16(wbs[i], x, b, b32, stream=st, static_weights=True))
+            tc = tm(lambda i: torch.nn.functional.linear(x, wbs[i]))
+            b4 = N * K * 1.5 + N * ((K + 511) // 512) * 4 + 2 * K + 6 * N
+            bb = N * K * 2 + 2 * K + 6 * N
+            out[key] = {"proj": [f'{m["name"]}:{name}'], "r4_us": t4, "bf16_us": tb, "cublas_us": tc,
+                        "r4_gb_s": b4 / t4 / 1e3, "bf16_gb_s": bb / tb / 1e3,
+                        "r4_over_bf16_speed": tb / t4, "r4_equals_bf16": same}
+            del r4s, wbs
     return out
 
 
