@@ -119,52 +119,6 @@ __device__ __noinline__ float round_with_escapes(const uint8_t *esc, uint64_t n_
     return acc;
 }
 
-// Decode a 16-weight lane chunk of a round that holds escapes (out of line:
-// keeps the common path small).  Called by all 32 lanes; c = escapes in the
-// round, b = index of the first, e = its exponent.
-struct Pairs8 {
-    uint32_t v[8];
-};
-
-__device__ __noinline__ Pairs8 decode_with_escapes_impl(const uint8_t *esc, uint64_t n_esc, R4Lut L, uint2 n,
-                                                      uint4 s, uint8_t *escb, const uint8_t *table_s,
-                                                      uint32_t lane, bool act, uint32_t c, uint32_t b,
-                                                      uint32_t e) {
-    Pairs8 out;
-    uint32_t *p = out.v;
-    r4_dec16(n, s, L, p);
-    const uint32_t m0 = act ? nib15_mask(n.x) : 0u;
-    const uint32_t m1 = act ? nib15_mask(n.y) : 0u;
-    if (c == 1) {
-        if (m0 | m1) {
-            const uint32_t pos = m0 ? (__ffs(m0) - 1) >> 2 : 8 + ((__ffs(m1) - 1) >> 2);
-#pragma unroll
-            for (int i = 0; i < 8; i++) {
-                if ((pos >> 1) == (uint32_t)i) {
-                    const uint32_t sh = (pos & 1) * 16;
-                    p[i] = (p[i] & ~(0x7F80u << sh)) | (e << (7 + sh));
-                }
-            }
-        }
-    } else {
-        const uint32_t cc = c > DGT_SEG ? DGT_SEG : c;
-        for (uint32_t i = lane; i < cc; i += 32) escb[i] = (uint64_t)b + i < n_esc ? esc[b + i] : 0;
-        __syncwarp();
-        patch_escapes(p, m0, m1, cc, escb, table_s);
-        __syncwarp();
-    }
-    return out;
-}
-
-__device__ __forceinline__ void decode_with_escapes(const uint8_t *esc, uint64_t n_esc, const R4Lut &L, uint2 n,
-                                                    uint4 s, uint8_t *escb, const uint8_t *table_s,
-                                                    uint32_t lane, bool act, uint32_t c, uint32_t b, uint32_t e,
-                                                    uint32_t p[8]) {
-    const Pairs8 r = decode_with_escapes_impl(esc, n_esc, L, n, s, escb, table_s, lane, act, c, b, e);
-#pragma unroll
-    for (int i = 0; i < 8; i++) p[i] = r.v[i];
-}
-
 template <bool R4, int U>
 __device__ __forceinline__ float compute_batch(const GemvArgs &a, const Batch<R4, U> &B, const uint4 *xs,
                                                uint8_t *escb, const uint8_t *table_s, const SegInfo &g,
