@@ -3,6 +3,9 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+#include <mutex>
+
 #include "../../include/dgt.h"
 
 namespace dgt {
@@ -14,12 +17,15 @@ struct DeviceInfo {
 };
 
 // The current device's SM count and compute capability, cached per device.
+// Safe to call from several host threads at once: a cache entry is published
+// (release) only after it is filled, and read only after that flag (acquire).
 static inline int device_info(DeviceInfo *out) {
     static DeviceInfo cache[64];
-    static bool have[64];
+    static std::atomic<bool> have[64];
+    static std::mutex fill;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return DGT_ERR_CUDA;
-    if (dev < 64 && have[dev]) {
+    if (dev < 64 && have[dev].load(std::memory_order_acquire)) {
         *out = cache[dev];
         return DGT_OK;
     }
@@ -30,8 +36,11 @@ static inline int device_info(DeviceInfo *out) {
         cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
         return DGT_ERR_CUDA;
     if (dev < 64) {
-        cache[dev] = d;
-        have[dev] = true;
+        std::lock_guard<std::mutex> lock(fill);
+        if (!have[dev].load(std::memory_order_relaxed)) {
+            cache[dev] = d;
+            have[dev].store(true, std::memory_order_release);
+        }
     }
     *out = d;
     return DGT_OK;

@@ -902,15 +902,16 @@ extern "C" int dgt_moe_gemv_bf16(const uint16_t *d_W, uint64_t rows, uint64_t co
 static __device__ __align__(256) uint8_t g_moe_scratch[DGT_MOE_NOALLOC_SCRATCH_BYTES];
 
 static int moe_scratch_address(void **out) {
-    static void *cached[64];
+    static std::atomic<void *> cached[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return DGT_ERR_CUDA;
-    if (!cached[dev]) {
-        void *p = nullptr;
+    void *p = cached[dev].load(std::memory_order_acquire);
+    if (!p) {
+        // Two threads may both look the address up; they store the same value.
         if (cudaGetSymbolAddress(&p, g_moe_scratch) != cudaSuccess || !p) return DGT_ERR_CUDA;
-        cached[dev] = p;
+        cached[dev].store(p, std::memory_order_release);
     }
-    *out = cached[dev];
+    *out = p;
     return DGT_OK;
 }
 
