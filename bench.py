@@ -444,6 +444,7 @@ def run_ours(args, rank, world, dist):
     projs = projection_extras(dgt, torch, dev) if more else None
     dstep = decode_step_extras(dgt, torch, dev) if more and not args.no_decode_step else None
     mstep = moe_decode_step_extras(dgt, torch, dev) if more and not args.no_decode_step else None
+    hpack = host_pack_extras(dgt) if more else None
 
     # ---- end to end through the C ABI from pinned host buffers
     e2e = None
@@ -508,10 +509,52 @@ def run_ours(args, rank, world, dist):
                              "rice_to_r4_gsym_s": kern["rice_to_r4"]["gsym_s"],
                              "rice_to_r4_frac": kern["rice_to_r4"]["frac"],
                              "r4_vs_bf16_gemv_speedup": kern["gemv_bf16"]["ms_avg"] / kern["gemv_r4"]["ms_avg"]},
-                "kernels": kern, "roofline": roof, "gemm_tensor": extras, "moe_gemm": mgemm, "projections": projs, "decode_step": dstep, "decode_step_moe": mstep, "cpu_baseline": cpu, "e2e": e2e,
+                "kernels": kern, "roofline": roof, "gemm_tensor": extras, "moe_gemm": mgemm, "projections": projs, "decode_step": dstep, "decode_step_moe": mstep, "host_pack": hpack, "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": launches_per_step * args.steps, "clocks": clk,
                 "gpu": torch.cuda.get_device_name(dev)}
         print(json.dumps(line), flush=True)
+
+
+def host_pack_extras(dgt, rows=ROWS, cols=COLS, reps=2):
+    """The host rows of the path on one bulk tensor: split + rank table + Rice
+    encode (format 2), format 1 encode, host unpack of each, and the container
+    write and read (a temporary file), each timed as the best of `reps` runs
+    on every host thread (the library's default).  GB/s counts the bf16 bytes
+    of the tensor; every result is checked to round-trip bit for bit."""
+    import tempfile
+    w = S.weights(rows, cols, (2, 0, 0, 0), outliers=True)
+    nbytes = w.nbytes
+
+    def best(fn):
+        out, dt = None, float("inf")
+        for _ in range(reps):
+            t = time.perf_counter()
+            out = fn()
+            dt = min(dt, time.perf_counter() - t)
+        return out, dt
+
+    res = {"workload": f"{rows}x{cols} bf16, N(0,0.02) + 0.1% outliers", "threads": os.cpu_count(),
+           "bytes_bf16": nbytes}
+    packed = {}
+    for fmt in (2, 1):
+        p, dt = best(lambda: dgt.pack(w, fmt))
+        packed[fmt] = p
+        res[f"pack_f{fmt}_ms"] = dt * 1e3
+        res[f"pack_f{fmt}_gb_s"] = nbytes / dt / 1e9
+        res[f"bits_per_weight_f{fmt}"] = p.bits_per_weight()
+        u, dt = best(lambda: dgt.unpack(p))
+        assert np.array_equal(u.reshape(w.shape), w), f"format {fmt} round trip"
+        res[f"unpack_f{fmt}_ms"] = dt * 1e3
+        res[f"unpack_f{fmt}_gb_s"] = nbytes / dt / 1e9
+    with tempfile.TemporaryDirectory() as d:
+        path = os.path.join(d, "bulk.dgt")
+        _, dt = best(lambda: dgt.write(path, {"f2": packed[2], "f1": packed[1]}))
+        size = os.path.getsize(path)
+        res["write_ms"], res["file_bytes"] = dt * 1e3, size
+        back, dt = best(lambda: dgt.read(path))
+        res["read_ms"] = dt * 1e3
+        assert np.array_equal(dgt.unpack(back["f2"]).reshape(w.shape), w), "container round trip"
+    return res
 
 
 def gemm_extras(dgt, torch, dev):

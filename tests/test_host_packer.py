@@ -145,3 +145,17 @@ def test_library_exports_every_declared_symbol(dgt):
         assert getattr(lib, name) is not None
     assert lib.dgt_version() == 100
     assert lib.dgt_status_string(-3) == b"corrupt packed data"
+
+
+def test_bench_host_pack_measurement_round_trips(dgt):
+    # the bench's host rows (pack, unpack, container write and read) on a
+    # small tensor: every timing is positive and every result round-trips
+    import sys
+    sys.path.insert(0, ROOT)
+    import bench
+    r = bench.host_pack_extras(dgt, rows=8, cols=4096, reps=1)
+    for key in ("pack_f2_ms", "pack_f1_ms", "unpack_f2_ms", "unpack_f1_ms", "write_ms", "read_ms"):
+        assert r[key] > 0, key
+    assert r["bytes_bf16"] == 8 * 4096 * 2
+    assert 9.0 < r["bits_per_weight_f2"] < 13.0 and 9.0 < r["bits_per_weight_f1"] < 13.0
+    assert r["file_bytes"] > 0
