@@ -444,7 +444,12 @@ def run_ours(args, rank, world, dist):
     projs = projection_extras(dgt, torch, dev) if more else None
     dstep = decode_step_extras(dgt, torch, dev) if more and not args.no_decode_step else None
     mstep = moe_decode_step_extras(dgt, torch, dev) if more and not args.no_decode_step else None
-    hpack = host_pack_extras(dgt) if more else None
+    hpack = None
+    if more:
+        try:
+            hpack = host_pack_extras(dgt)
+        except Exception as e:       # a host-side extra never takes the bench line down
+            hpack = {"error": f"{type(e).__name__}: {e}"}
 
     # ---- end to end through the C ABI from pinned host buffers
     e2e = None
