@@ -250,43 +250,57 @@ int dgt_read(const char *path, dgt_packed ***tensors, char ***names, int *count)
     uint64_t hl = 0;
     for (int i = 0; i < 8; i++) hl |= (uint64_t)le[i] << (8 * i);
     if (hl > (64u << 20)) return DGT_ERR_CORRUPT;
-    if (std::fseek(f, 0, SEEK_END) != 0) return DGT_ERR_IO;
-    long fsz = std::ftell(f);
+    if (fseeko(f, 0, SEEK_END) != 0) return DGT_ERR_IO;
+    const off_t fsz = ftello(f);
     if (fsz < 0 || (uint64_t)fsz < 8 + hl) return DGT_ERR_CORRUPT;
-    uint64_t dsz = (uint64_t)fsz - 8 - hl;
-    std::fseek(f, 8, SEEK_SET);
+    const uint64_t dsz = (uint64_t)fsz - 8 - hl;
+    if (fseeko(f, 8, SEEK_SET) != 0) return DGT_ERR_IO;
     std::string hdr(hl, '\0');
-    std::vector<uint8_t> data;
-    try {
-        data.resize(dsz);
-    } catch (const std::bad_alloc &) {
-        return DGT_ERR_OOM;
-    }
-    if (std::fread(&hdr[0], 1, hl, f) != hl) return DGT_ERR_CORRUPT;
-    if (dsz && std::fread(data.data(), 1, dsz, f) != dsz) return DGT_ERR_CORRUPT;
+    if (hl && std::fread(&hdr[0], 1, hl, f) != hl) return DGT_ERR_CORRUPT;
     JParser jp{hdr.data(), hdr.data() + hdr.size()};
     JVal root;
     if (!jp.val(root) || root.kind != JVal::OBJ) return DGT_ERR_CORRUPT;
     auto mit = root.obj.find("__metadata__");
     if (mit == root.obj.end() || mit->second.kind != JVal::OBJ) return DGT_ERR_CORRUPT;
-    auto get = [&](const std::string &nm, std::vector<uint8_t> &dst) -> bool {
+    // Each array is read from the file straight into its destination (no
+    // whole-file buffer): its byte range [a, b) of the data section.
+    bool oom = false;
+    auto span = [&](const std::string &nm, uint64_t *a, uint64_t *b) -> bool {
         auto it = root.obj.find(nm);
         if (it == root.obj.end() || it->second.kind != JVal::OBJ) return false;
         auto &o = it->second.obj;
-        if (!o.count("data_offsets") || o["data_offsets"].kind != JVal::ARR ||
-            o["data_offsets"].arr.size() != 2)
+        auto d = o.find("data_offsets");
+        if (d == o.end() || d->second.kind != JVal::ARR || d->second.arr.size() != 2) return false;
+        *a = d->second.arr[0].num;
+        *b = d->second.arr[1].num;
+        return *a <= *b && *b <= dsz;
+    };
+    auto fill = [&](uint64_t a, void *dst, uint64_t bytes) -> bool {
+        if (bytes == 0) return true;
+        if (fseeko(f, (off_t)(8 + hl + a), SEEK_SET) != 0) return false;
+        return std::fread(dst, 1, bytes, f) == bytes;
+    };
+    auto get = [&](const std::string &nm, std::vector<uint8_t> &dst) -> bool {
+        uint64_t a, b;
+        if (!span(nm, &a, &b)) return false;
+        try {
+            dst.resize(b - a);
+        } catch (const std::bad_alloc &) {
+            oom = true;
             return false;
-        uint64_t a = o["data_offsets"].arr[0].num, b = o["data_offsets"].arr[1].num;
-        if (a > b || b > dsz) return false;
-        dst.assign(data.begin() + (long)a, data.begin() + (long)b);
-        return true;
+        }
+        return fill(a, dst.data(), b - a);
     };
     auto get32 = [&](const std::string &nm, std::vector<uint32_t> &dst) -> bool {
-        std::vector<uint8_t> tmp;
-        if (!get(nm, tmp) || tmp.size() % 4) return false;
-        dst.resize(tmp.size() / 4);
-        if (!tmp.empty()) std::memcpy(dst.data(), tmp.data(), tmp.size());
-        return true;
+        uint64_t a, b;
+        if (!span(nm, &a, &b) || (b - a) % 4) return false;
+        try {
+            dst.resize((b - a) / 4);
+        } catch (const std::bad_alloc &) {
+            oom = true;
+            return false;
+        }
+        return fill(a, dst.data(), b - a);
     };
     std::vector<dgt_packed *> out;
     std::vector<std::string> nms;
@@ -313,7 +327,7 @@ int dgt_read(const char *path, dgt_packed ***tensors, char ***names, int *count)
         }
         if (!ok) {
             delete t;
-            rc = DGT_ERR_CORRUPT;
+            rc = oom ? DGT_ERR_OOM : DGT_ERR_CORRUPT;
             break;
         }
         t->refresh();
@@ -334,9 +348,16 @@ int dgt_read(const char *path, dgt_packed ***tensors, char ***names, int *count)
         return DGT_ERR_OOM;
     }
     for (int i = 0; i < c; i++) {
-        ta[i] = out[i];
         na[i] = (char *)std::malloc(nms[i].size() + 1);
-        if (na[i]) std::memcpy(na[i], nms[i].c_str(), nms[i].size() + 1);
+        if (!na[i]) {
+            for (int j = 0; j < i; j++) std::free(na[j]);
+            std::free(ta);
+            std::free(na);
+            for (auto *t : out) delete t;
+            return DGT_ERR_OOM;
+        }
+        std::memcpy(na[i], nms[i].c_str(), nms[i].size() + 1);
+        ta[i] = out[i];
     }
     *tensors = ta;
     *names = na;

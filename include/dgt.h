@@ -159,7 +159,9 @@ int dgt_unpack(const dgt_packed_view *view, uint16_t *out_bf16, int nthreads);
  * "X.grp1" (format 1), and the metadata entry "X" = "format=..;rows=..;...".
  * dgt_write: tensors/names are host arrays of count entries.
  * dgt_read: *tensors and *names are library-allocated arrays of *count
- * entries; release them with dgt_read_free().
+ * entries; release them with dgt_read_free().  Each array is read from the
+ * file straight into its tensor (host memory: the packed size, no second
+ * copy of the file).
  * Errors: DGT_ERR_ARG, DGT_ERR_IO, DGT_ERR_CORRUPT (malformed header or
  * arrays whose sizes disagree with the metadata), DGT_ERR_OOM.
  */
