@@ -15,6 +15,8 @@
 #include <string>
 #include <vector>
 
+#include <unistd.h>
+
 #include "../../include/dgt.h"
 #include "dgt_packed.h"
 
@@ -225,7 +227,11 @@ int dgt_write(const char *path, const dgt_packed *const *tensors, const char *co
     }
     hdr += "}";
     while (hdr.size() % 8) hdr += ' ';
-    FILE *f = std::fopen(path, "wb");
+    // Written to a temporary file beside the target and renamed over it once
+    // complete, so a failed or interrupted write never leaves a partial
+    // container under `path`.
+    const std::string tmp = std::string(path) + ".tmp" + std::to_string((long long)getpid());
+    FILE *f = std::fopen(tmp.c_str(), "wb");
     if (!f) return DGT_ERR_IO;
     uint64_t hl = hdr.size();
     uint8_t le[8];
@@ -234,6 +240,8 @@ int dgt_write(const char *path, const dgt_packed *const *tensors, const char *co
     for (const Arr &a : arrs)
         if (ok && a.bytes) ok = std::fwrite(a.data, 1, a.bytes, f) == a.bytes;
     ok = (std::fclose(f) == 0) && ok;
+    ok = ok && std::rename(tmp.c_str(), path) == 0;
+    if (!ok) std::remove(tmp.c_str());
     return ok ? DGT_OK : DGT_ERR_IO;
 }
 

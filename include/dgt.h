@@ -157,7 +157,9 @@ int dgt_unpack(const dgt_packed_view *view, uint16_t *out_bf16, int nthreads);
  * header, then the data -- with, per tensor name X, arrays "X.sm", "X.rice",
  * "X.blkq", "X.grp" (format 2) or "X.f1", "X.tw", "X.tesc", "X.esc1",
  * "X.grp1" (format 1), and the metadata entry "X" = "format=..;rows=..;...".
- * dgt_write: tensors/names are host arrays of count entries.
+ * dgt_write: tensors/names are host arrays of count entries.  The file is
+ * written under a temporary name beside `path` and renamed to `path` when
+ * complete; on an error nothing is left under either name.
  * dgt_read: *tensors and *names are library-allocated arrays of *count
  * entries; release them with dgt_read_free().  Each array is read from the
  * file straight into its tensor (host memory: the packed size, no second

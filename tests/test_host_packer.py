@@ -159,3 +159,18 @@ def test_bench_host_pack_measurement_round_trips(dgt):
     assert r["bytes_bf16"] == 8 * 4096 * 2
     assert 9.0 < r["bits_per_weight_f2"] < 13.0 and 9.0 < r["bits_per_weight_f1"] < 13.0
     assert r["file_bytes"] > 0
+
+
+def test_container_write_is_atomic(dgt, tmp_path):
+    # a write that cannot complete leaves neither a partial file nor a
+    # temporary one; a rewrite replaces the old container whole
+    p = dgt.pack(S.weights(4, 256, (96, 0, 0, 0)), 2)
+    with pytest.raises(dgt.DgtError) as e:
+        dgt.write(str(tmp_path / "no_such_dir" / "m.dgt"), {"w": p})
+    assert e.value.code == -7
+    path = str(tmp_path / "m.dgt")
+    dgt.write(path, {"w": p})
+    q = dgt.pack(S.weights(2, 128, (96, 1, 0, 0)), 1)
+    dgt.write(path, {"v": q})
+    assert set(dgt.read(path)) == {"v"}
+    assert sorted(os.listdir(tmp_path)) == ["m.dgt"]
