@@ -85,6 +85,20 @@ def test_gemm_12b_shapes(dgt, M):
         assert _normwise(got, ref) <= 1e-3, (name, M)
 
 
+def test_gemm_bulk_tensor_bench_configuration(dgt):
+    # the timed prompt product: the 4096 x 16384 bulk tensor (0.1% outliers at
+    # 100x) at 16 rows with the default plan; twins bit-identical, sampled
+    # columns within the normwise bound of the fp64 oracle
+    W = S.weights(4096, 16384, (2, 0, 0, 0), outliers=True)
+    X = S.activations(16384, (2, 998, 0), count=16).reshape(16, 16384)
+    y32, y16, b32, b16 = _both(dgt, W, X)
+    assert torch.equal(y32.view(torch.int32), b32.view(torch.int32))
+    assert torch.equal(y16.view(torch.int16), b16.view(torch.int16))
+    cols = np.sort(np.random.default_rng(16384).choice(4096, 128, replace=False))
+    ref = oracle.gemm_f64(X, W, cols=cols)
+    assert _normwise(y32.cpu().numpy()[:, cols], ref) <= 1e-3
+
+
 @pytest.mark.parametrize("M,N,K,split", [(16, 256, 512, 1), (300, 384, 1024, 3), (2048, 128, 640, 1)])
 def test_gemm_rebuild_is_the_bf16_gemm(dgt, M, N, K, split):
     # rebuild-then-bf16 gives the fused R4 GEMM's bits (and the bf16 GEMM's)
