@@ -92,11 +92,19 @@ struct BitReader {
 
 inline uint8_t sm_of(uint16_t b) { return (uint8_t)(((b >> 8) & 0x80) | (b & 0x7F)); }
 inline uint8_t exp_of(uint16_t b) { return (uint8_t)((b >> 7) & 0xFF); }
+// The ranks of a tensor, read from its bf16 bits through the rank table
+// (not stored as an array of their own).
+struct Ranks {
+    const uint16_t *b;
+    uint8_t rank_of[256];
+    uint8_t operator[](uint64_t i) const { return rank_of[exp_of(b[i])]; }
+};
+
 inline uint16_t bf16_of(uint8_t sm, uint8_t e) {
     return (uint16_t)(((uint16_t)(sm & 0x80) << 8) | ((uint16_t)e << 7) | (sm & 0x7F));
 }
 
-int pack_format2(dgt_packed *p, const std::vector<uint8_t> &rk, int nt) {
+int pack_format2(dgt_packed *p, const Ranks &rk, int nt) {
     const uint64_t n = p->v.rows * p->v.cols;
     const uint64_t nblk = (n + DGT_BLOCK - 1) / DGT_BLOCK;
     const uint64_t ngrp = (nblk + DGT_GROUP - 1) / DGT_GROUP;
@@ -171,11 +179,15 @@ int pack_format2(dgt_packed *p, const std::vector<uint8_t> &rk, int nt) {
     return DGT_OK;
 }
 
-inline int tile_width(const uint8_t *r, uint64_t cnt) {
+inline int tile_width(const Ranks &rk, uint64_t i0, uint64_t cnt) {
     uint32_t hist[256];
     std::memset(hist, 0, sizeof(hist));
     bool nz = false;
-    for (uint64_t i = 0; i < cnt; i++) { hist[r[i]]++; nz |= r[i] != 0; }
+    for (uint64_t i = 0; i < cnt; i++) {
+        const uint8_t r = rk[i0 + i];
+        hist[r]++;
+        nz |= r != 0;
+    }
     if (!nz) return 0;
     // ranks >= t for every threshold t, from the histogram
     uint32_t ge[257];
@@ -190,7 +202,7 @@ inline int tile_width(const uint8_t *r, uint64_t cnt) {
     return best;
 }
 
-int pack_format1(dgt_packed *p, const std::vector<uint8_t> &rk, int nt) {
+int pack_format1(dgt_packed *p, const Ranks &rk, int nt) {
     const uint64_t n = p->v.rows * p->v.cols;
     const uint64_t ntile = (n + DGT_TILE - 1) / DGT_TILE;
     const uint64_t ngrp = (ntile + DGT_GROUP - 1) / DGT_GROUP;
@@ -200,7 +212,7 @@ int pack_format1(dgt_packed *p, const std::vector<uint8_t> &rk, int nt) {
     parallel_for(nt, ntile, [&](uint64_t t0, uint64_t t1) {
         for (uint64_t t = t0; t < t1; t++) {
             uint64_t i0 = t * DGT_TILE, cnt = std::min<uint64_t>(DGT_TILE, n - i0);
-            int w = tile_width(&rk[i0], cnt);
+            int w = tile_width(rk, i0, cnt);
             uint32_t top = w ? (1u << w) - 1u : 0u;
             uint32_t e = 0, e15 = 0;
             for (uint64_t i = 0; i < cnt; i++) {
@@ -289,13 +301,36 @@ int dgt_pack(const uint16_t *bf16, uint64_t rows, uint64_t cols, int format, int
         p->v.rows = rows;
         p->v.cols = cols;
         p->v.format = format;
-        // exponent histogram
+        // exponent histogram and the sign/mantissa bytes, in one pass (sm is
+        // first touched here, by the threads that fill it)
+        p->sm.resize(n);
         const uint64_t chunks = std::min<uint64_t>((uint64_t)nt * 4, std::max<uint64_t>(1, n / 65536));
         std::vector<uint64_t> part(chunks * 256, 0);
         parallel_for(nt, chunks, [&](uint64_t c0, uint64_t c1) {
+            // four sub-histograms, so that equal exponents in a row do not
+            // wait on one another's counter
+            std::vector<uint64_t> h4(4 * 256);
             for (uint64_t c = c0; c < c1; c++) {
+                std::fill(h4.begin(), h4.end(), 0);
+                const uint64_t lo = n * c / chunks, hi = n * (c + 1) / chunks;
+                uint64_t i = lo;
+                for (; i + 4 <= hi; i += 4) {
+                    const uint16_t b0 = bf16[i], b1 = bf16[i + 1], b2 = bf16[i + 2], b3 = bf16[i + 3];
+                    h4[exp_of(b0)]++;
+                    h4[256 + exp_of(b1)]++;
+                    h4[512 + exp_of(b2)]++;
+                    h4[768 + exp_of(b3)]++;
+                    p->sm[i] = sm_of(b0);
+                    p->sm[i + 1] = sm_of(b1);
+                    p->sm[i + 2] = sm_of(b2);
+                    p->sm[i + 3] = sm_of(b3);
+                }
+                for (; i < hi; i++) {
+                    h4[exp_of(bf16[i])]++;
+                    p->sm[i] = sm_of(bf16[i]);
+                }
                 uint64_t *h = &part[c * 256];
-                for (uint64_t i = n * c / chunks; i < n * (c + 1) / chunks; i++) h[exp_of(bf16[i])]++;
+                for (int e = 0; e < 256; e++) h[e] = h4[e] + h4[256 + e] + h4[512 + e] + h4[768 + e];
             }
         });
         uint64_t counts[256] = {0};
@@ -306,26 +341,17 @@ int dgt_pack(const uint16_t *bf16, uint64_t rows, uint64_t cols, int format, int
         for (int e = 0; e < 256; e++)
             if (counts[e]) order[T++] = e;
         std::stable_sort(order, order + T, [&](int a, int b) { return counts[a] > counts[b]; });
-        uint8_t rank_of[256];
-        std::memset(rank_of, 0, sizeof(rank_of));
+        Ranks rk;
+        rk.b = bf16;
+        std::memset(rk.rank_of, 0, sizeof(rk.rank_of));
         for (int r = 0; r < T; r++) {
             p->v.table[r] = (uint8_t)order[r];
-            rank_of[order[r]] = (uint8_t)r;
+            rk.rank_of[order[r]] = (uint8_t)r;
         }
         p->v.n_table = T;
         uint64_t e15 = 0;
         for (int r = 15; r < T; r++) e15 += counts[order[r]];
         p->v.n_esc15 = e15;
-        // sign/mantissa bytes and ranks
-        p->sm.resize(n);
-        std::vector<uint8_t> rk(n);
-        parallel_for(nt, (n + 4095) / 4096, [&](uint64_t b0, uint64_t b1) {
-            for (uint64_t i = b0 * 4096; i < std::min(n, b1 * 4096); i++) {
-                uint16_t b = bf16[i];
-                p->sm[i] = sm_of(b);
-                rk[i] = rank_of[exp_of(b)];
-            }
-        });
         int rc = format == 2 ? pack_format2(p, rk, nt) : pack_format1(p, rk, nt);
         if (rc != DGT_OK) {
             delete p;

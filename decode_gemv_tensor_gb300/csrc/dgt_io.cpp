@@ -288,7 +288,7 @@ int dgt_read(const char *path, dgt_packed ***tensors, char ***names, int *count)
         if (fseeko(f, (off_t)(8 + hl + a), SEEK_SET) != 0) return false;
         return std::fread(dst, 1, bytes, f) == bytes;
     };
-    auto get = [&](const std::string &nm, std::vector<uint8_t> &dst) -> bool {
+    auto get = [&](const std::string &nm, auto &dst) -> bool {
         uint64_t a, b;
         if (!span(nm, &a, &b)) return false;
         try {
