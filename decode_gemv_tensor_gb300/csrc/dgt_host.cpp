@@ -73,20 +73,49 @@ struct BitWriter {
     }
 };
 
-struct BitReader {
+// One Rice code at bit pos of an LSB-first word stream of limit bits, read
+// through a 64-bit window (words past the end read as zero).  Returns the
+// rank; a unary run that reaches the end of the stream, or runs past 255
+// zeros, or a code that ends past the end, sets bad.
+struct RiceReader {
     const uint32_t *w;
-    uint64_t pos, limit;
+    uint64_t nw, pos, limit;
     bool bad = false;
-    int bit() {
-        if (pos >= limit) { bad = true; return 1; }
-        int b = (int)((w[pos >> 5] >> (pos & 31)) & 1u);
-        pos++;
-        return b;
+    uint64_t word(uint64_t i) const { return i < nw ? w[i] : 0u; }
+    uint64_t window() const {
+        const uint64_t i = pos >> 5;
+        const unsigned sh = (unsigned)(pos & 31);
+        const uint64_t v = (word(i) | (word(i + 1) << 32)) >> sh;
+        return sh ? v | (word(i + 2) << (64 - sh)) : v;
     }
-    uint32_t bits(int len) {
-        uint32_t v = 0;
-        for (int i = 0; i < len; i++) v |= (uint32_t)bit() << i;
-        return v;
+    uint32_t code(int k, uint32_t *quo) {
+        const uint64_t v = window();
+        uint32_t q, r;
+        if (v != 0 && (unsigned)__builtin_ctzll(v) + 1 + k <= 64) {
+            q = (uint32_t)__builtin_ctzll(v);
+            r = (q << k) | (uint32_t)((v >> (q + 1)) & ((1u << k) - 1u));
+            pos += q + 1 + k;
+        } else {
+            // a unary run of 64 or more zeros: only valid data up to 255
+            q = 0;
+            while (pos < limit && !((word(pos >> 5) >> (pos & 31)) & 1u) && q <= 255) {
+                q++;
+                pos++;
+            }
+            pos++;
+            const uint64_t rem = window() & ((1u << k) - 1u);
+            r = (q << k) | (uint32_t)rem;
+            pos += k;
+        }
+        if (pos > limit || q > 255) bad = true;
+        *quo = q;
+        return r;
+    }
+    uint32_t raw8() {
+        const uint32_t r = (uint32_t)(window() & 0xFFu);
+        pos += 8;
+        if (pos > limit) bad = true;
+        return r;
     }
 };
 
@@ -400,7 +429,7 @@ int dgt_unpack(const dgt_packed_view *v, uint16_t *out, int nthreads) {
         const int k = v->rice_k;
         parallel_for(nt, ngrp, [&](uint64_t g0, uint64_t g1) {
             for (uint64_t g = g0; g < g1 && !bad.load(std::memory_order_relaxed); g++) {
-                BitReader br{v->words, (uint64_t)v->grp[2 * g] * 32, v->n_words * 32};
+                RiceReader br{v->words, v->n_words, (uint64_t)v->grp[2 * g] * 32, v->n_words * 32};
                 uint64_t b_end = std::min(nblk, (g + 1) * DGT_GROUP);
                 for (uint64_t b = g * DGT_GROUP; b < b_end; b++) {
                     uint64_t i0 = b * DGT_BLOCK, cnt = std::min<uint64_t>(DGT_BLOCK, n - i0);
@@ -410,8 +439,7 @@ int dgt_unpack(const dgt_packed_view *v, uint16_t *out, int nthreads) {
                         uint32_t qs = 0;
                         for (uint64_t i = 0; i < cnt; i++) {
                             uint32_t quo = 0;
-                            while (!br.bit() && quo <= 255) quo++;
-                            uint32_t r = (quo << k) | br.bits(k);
+                            const uint32_t r = br.code(k, &quo);
                             if (r > 255) br.bad = true;
                             qs += quo;
                             out[i0 + i] = bf16_of(v->sm[i0 + i], v->table[r & 255]);
@@ -419,7 +447,7 @@ int dgt_unpack(const dgt_packed_view *v, uint16_t *out, int nthreads) {
                         if (qs != q || br.pos - start != cnt * (uint64_t)(k + 1) + q) br.bad = true;
                     } else {
                         for (uint64_t i = 0; i < cnt; i++)
-                            out[i0 + i] = bf16_of(v->sm[i0 + i], v->table[br.bits(8)]);
+                            out[i0 + i] = bf16_of(v->sm[i0 + i], v->table[br.raw8()]);
                     }
                     if (br.bad) { bad.store(1); break; }
                 }
@@ -439,10 +467,14 @@ int dgt_unpack(const dgt_packed_view *v, uint16_t *out, int nthreads) {
                     if (w > 8 || off + 16ull * w > v->payload_bytes) { bad.store(1); break; }
                     uint32_t top = w ? (1u << w) - 1u : 0u, seen = 0;
                     for (uint64_t i = 0; i < cnt; i++) {
+                        // w <= 8 bits from bit position off*8 + i*w: two bytes
+                        // at most, the second only inside the payload
                         uint32_t c = 0;
-                        for (int b = 0; b < w; b++) {
-                            uint64_t bit = off * 8 + i * (uint64_t)w + b;
-                            c |= (uint32_t)((v->payload[bit >> 3] >> (bit & 7)) & 1u) << b;
+                        if (w) {
+                            const uint64_t bit = off * 8 + i * (uint64_t)w, by = bit >> 3;
+                            uint32_t two = v->payload[by];
+                            if (by + 1 < v->payload_bytes) two |= (uint32_t)v->payload[by + 1] << 8;
+                            c = (two >> (bit & 7)) & top;
                         }
                         uint32_t r = c;
                         if (w && c == top) {
