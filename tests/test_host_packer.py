@@ -174,3 +174,31 @@ def test_container_write_is_atomic(dgt, tmp_path):
     dgt.write(path, {"v": q})
     assert set(dgt.read(path)) == {"v"}
     assert sorted(os.listdir(tmp_path)) == ["m.dgt"]
+
+
+DEVICE_ENTRY_POINTS = ["dgt_load_r4", "dgt_r4_to_bf16", "dgt_r4_init_from_view", "dgt_read_status", "dgt_gemv",
+                       "dgt_gemv_bf16", "dgt_gemv_ex", "dgt_gemv_bf16_ex", "dgt_gemm", "dgt_gemm_bf16",
+                       "dgt_gemm_rebuild", "dgt_moe_gemv", "dgt_moe_gemv_bf16", "dgt_moe_gemv_noalloc",
+                       "dgt_moe_gemm", "dgt_moe_gemm_bf16", "dgt_add_rmsnorm", "dgt_silu_mul", "dgt_silu_mul_rows",
+                       "dgt_repeat", "dgt_weighted_sum", "dgt_exponent_stats"]
+
+
+@pytest.mark.parametrize("name", DEVICE_ENTRY_POINTS)
+def test_device_entry_points_reject_null_arguments_before_any_device_call(dgt, name):
+    # every pointer NULL, every size non-zero: DGT_ERR_ARG, returned before
+    # the entry point touches a device (this machine may have none)
+    import ctypes as C
+    f = getattr(dgt.lib(), name)
+    args = []
+    for t in f.argtypes:
+        if t in (C.c_uint64, C.c_size_t):
+            args.append(1024)
+        elif t in (C.c_uint32, C.c_uint, C.c_int):
+            args.append(8)
+        elif t is C.c_float:
+            args.append(1e-5)
+        else:
+            args.append(None)
+    if name.endswith("_ex"):
+        args[-2] = 0                  # launch flags
+    assert f(*args) == -1
