@@ -56,7 +56,7 @@ class R4Struct(C.Structure):
 
 
 class GemmPlan(C.Structure):
-    _fields_ = [("m_tile", C.c_int32), ("split_k", C.c_int32), ("reserved0", C.c_int32), ("reserved1", C.c_int32)]
+    _fields_ = [("m_tile", C.c_int32), ("split_k", C.c_int32), ("test_flags", C.c_uint32), ("reserved1", C.c_int32)]
 
 
 _lib = None
@@ -104,6 +104,8 @@ def lib():
             "dgt_moe_workspace_bytes": (C.c_size_t, [C.c_uint32, u64, u64, C.c_uint32, C.c_uint32]),
             "dgt_moe_gemv": (i32, [C.POINTER(R4Struct), C.c_uint32, vp, vp, C.c_uint32, C.c_uint32, vp, vp, vp,
                                    vp, vp, C.c_size_t, vp, vp]),
+            "dgt_moe_gemv_ex": (i32, [C.POINTER(R4Struct), C.c_uint32, vp, vp, C.c_uint32, C.c_uint32, vp, vp, vp,
+                                      vp, vp, C.c_size_t, vp, C.c_uint, vp]),
             "dgt_moe_gemv_bf16": (i32, [vp, u64, u64, C.c_uint32, vp, vp, C.c_uint32, C.c_uint32, vp, vp, vp,
                                         vp, vp, C.c_size_t, vp, vp]),
             "dgt_moe_gemv_noalloc": (i32, [C.POINTER(R4Struct), C.c_uint32, vp, vp, C.c_uint32, C.c_uint32, vp,
@@ -356,12 +358,25 @@ def read_status(status, stream=None) -> int:
 
 
 STATIC_WEIGHTS = 1
+TEST_SHORT_WAITS = 2
 
 
-def gemv(W: R4, x, y=None, y32=None, status=None, stream=None, static_weights=False):
+def test_wait_flags(polls=None) -> int:
+    """Launch flags of the failure-path test hook (DGT_TEST_SHORT_WAITS with
+    DGT_TEST_WAIT_POLLS(polls)): waits for streamed data give up after
+    `polls` polls.  None: 0 (no hook)."""
+    if polls is None:
+        return 0
+    if not 0 <= int(polls) <= 0xFFFF:
+        raise ValueError("polls must be in 0..65535")
+    return TEST_SHORT_WAITS | (int(polls) << 16)
+
+
+def gemv(W: R4, x, y=None, y32=None, status=None, stream=None, static_weights=False, test_wait_polls=None):
     """dgt_gemv_ex: y = W x with W in R4; x bf16 [cols] on the device.
     static_weights: no kernel still running writes W (DGT_GEMV_STATIC_WEIGHTS),
-    so W may stream before the previous kernel ends.
+    so W may stream before the previous kernel ends.  test_wait_polls: the
+    failure-path test hook (see test_wait_flags).
     Returns (y bf16 [rows], y32 float32 [rows])."""
     import torch
     dev = W.sm.device
@@ -369,12 +384,13 @@ def gemv(W: R4, x, y=None, y32=None, status=None, stream=None, static_weights=Fa
         y = torch.empty(W.rows, dtype=torch.bfloat16, device=dev)
     if y32 is None:
         y32 = torch.empty(W.rows, dtype=torch.float32, device=dev)
-    _check(lib().dgt_gemv_ex(C.byref(W.s), _ptr(x), _ptr(y), _ptr(y32), _ptr(status),
-                             STATIC_WEIGHTS if static_weights else 0, _stream(stream)), "dgt_gemv")
+    flags = (STATIC_WEIGHTS if static_weights else 0) | test_wait_flags(test_wait_polls)
+    _check(lib().dgt_gemv_ex(C.byref(W.s), _ptr(x), _ptr(y), _ptr(y32), _ptr(status), flags, _stream(stream)),
+           "dgt_gemv")
     return y, y32
 
 
-def gemv_bf16(W, x, y=None, y32=None, status=None, stream=None, static_weights=False):
+def gemv_bf16(W, x, y=None, y32=None, status=None, stream=None, static_weights=False, test_wait_polls=None):
     """dgt_gemv_bf16_ex: the same product and order with bf16 weights [rows, cols]."""
     import torch
     rows, cols = W.shape
@@ -382,8 +398,9 @@ def gemv_bf16(W, x, y=None, y32=None, status=None, stream=None, static_weights=F
         y = torch.empty(rows, dtype=torch.bfloat16, device=W.device)
     if y32 is None:
         y32 = torch.empty(rows, dtype=torch.float32, device=W.device)
-    _check(lib().dgt_gemv_bf16_ex(_ptr(W), rows, cols, _ptr(x), _ptr(y), _ptr(y32), _ptr(status),
-                                  STATIC_WEIGHTS if static_weights else 0, _stream(stream)), "dgt_gemv_bf16")
+    flags = (STATIC_WEIGHTS if static_weights else 0) | test_wait_flags(test_wait_polls)
+    _check(lib().dgt_gemv_bf16_ex(_ptr(W), rows, cols, _ptr(x), _ptr(y), _ptr(y32), _ptr(status), flags,
+                                  _stream(stream)), "dgt_gemv_bf16")
     return y, y32
 
 
@@ -403,9 +420,10 @@ def _moe_outputs(tokens, topk, ne, dev, want_y, want_out, y32, out, out32):
 
 
 def moe_gemv(W: R4, n_experts: int, ids, p, x, ws=None, y32=None, out=None, out32=None, status=None,
-             stream=None, want_y=True):
-    """dgt_moe_gemv: expert gather with stacked R4 experts.  ids int32 [T, topk],
-    p float32 [T, topk] or None, x bf16 [T, K].  Returns (y32, out, out32)."""
+             stream=None, want_y=True, test_wait_polls=None):
+    """dgt_moe_gemv_ex: expert gather with stacked R4 experts.  ids int32 [T, topk],
+    p float32 [T, topk] or None, x bf16 [T, K].  test_wait_polls: the
+    failure-path test hook (see test_wait_flags).  Returns (y32, out, out32)."""
     import torch
     tokens, topk = ids.shape
     ne = W.rows // n_experts
@@ -414,9 +432,9 @@ def moe_gemv(W: R4, n_experts: int, ids, p, x, ws=None, y32=None, out=None, out3
     nb = moe_workspace_bytes(n_experts, ne, W.cols, tokens, topk)
     if ws is None:
         ws = torch.empty(max(nb, 256), dtype=torch.uint8, device=dev)
-    _check(lib().dgt_moe_gemv(C.byref(W.s), n_experts, _ptr(ids), _ptr(p), tokens, topk, _ptr(x), _ptr(y32),
-                              _ptr(out), _ptr(out32), _ptr(ws), ws.numel(), _ptr(status), _stream(stream)),
-           "dgt_moe_gemv")
+    _check(lib().dgt_moe_gemv_ex(C.byref(W.s), n_experts, _ptr(ids), _ptr(p), tokens, topk, _ptr(x), _ptr(y32),
+                                 _ptr(out), _ptr(out32), _ptr(ws), ws.numel(), _ptr(status),
+                                 test_wait_flags(test_wait_polls), _stream(stream)), "dgt_moe_gemv")
     return y32, out, out32
 
 
@@ -478,14 +496,16 @@ def moe_gemm_bf16(W, n_experts: int, ids, p, X, ws=None, y32=None, out=None, out
     return y32, out, out32
 
 
-def gemm_plan(M: int, N: int, K: int, m_tile=None, split_k=None) -> GemmPlan:
-    """dgt_gemm_default_plan, optionally overridden."""
+def gemm_plan(M: int, N: int, K: int, m_tile=None, split_k=None, test_wait_polls=None) -> GemmPlan:
+    """dgt_gemm_default_plan, optionally overridden (test_wait_polls: the
+    failure-path test hook, see test_wait_flags)."""
     p = GemmPlan()
     _check(lib().dgt_gemm_default_plan(M, N, K, C.byref(p)), "dgt_gemm_default_plan")
     if m_tile is not None:
         p.m_tile = m_tile
     if split_k is not None:
         p.split_k = split_k
+    p.test_flags = test_wait_flags(test_wait_polls)
     return p
 
 

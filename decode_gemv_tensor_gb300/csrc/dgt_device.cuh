@@ -18,6 +18,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "../../include/dgt.h"
+
 #define DGT_FULL 0xFFFFFFFFu
 
 namespace dgt {
@@ -261,6 +263,44 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
     for (uint32_t i = 0; i < MBAR_SPIN_LIMIT; i++)
         if (mbar_try_wait(bar, parity)) return true;
     return false;
+}
+
+// The same with a caller-chosen limit (0: give up at once).
+__device__ __forceinline__ bool mbar_wait_n(uint32_t bar, uint32_t parity, uint32_t limit) {
+    for (uint32_t i = 0; i < limit; i++)
+        if (mbar_try_wait(bar, parity)) return true;
+    return false;
+}
+
+// Launch-time wait limit for waits on work in flight: the library default, or
+// the short limit a caller asked for through DGT_TEST_SHORT_WAITS.
+static inline uint32_t wait_limit_from_flags(unsigned flags) {
+    return (flags & DGT_TEST_SHORT_WAITS) ? (flags >> 16) : MBAR_SPIN_LIMIT;
+}
+
+// Producer/consumer rings with one producer lane per consumer warp: when the
+// producer lane stops (its work done, or told to abort) it publishes how many
+// pieces it issued, with bit 31 set, in the ring's stop word.
+__device__ __forceinline__ void ring_publish_stop(uint32_t *stop_word, uint32_t issued) {
+    *(volatile uint32_t *)stop_word = issued | 0x80000000u;
+}
+
+// After a consumer gave up (a wait ran out, or the CTA aborted): wait, bounded,
+// for its producer to stop, then for every piece that producer issued and the
+// consumer did not take (pieces consumed..issued-1 of a ring of ns stages), so
+// that no bulk copy is still writing shared memory when the CTA exits.  All
+// lanes of the warp call it.
+__device__ __forceinline__ void ring_drain(const uint32_t *stop_word, uint32_t full_a, uint32_t consumed,
+                                           uint32_t ns) {
+    uint32_t v = 0;
+    for (uint32_t i = 0; i < MBAR_SPIN_LIMIT; i++) {
+        v = *(const volatile uint32_t *)stop_word;
+        if (v >> 31) break;
+        __nanosleep(64);
+    }
+    if (!(v >> 31)) return;
+    const uint32_t issued = v & 0x7FFFFFFFu;
+    for (uint32_t q = consumed; q < issued; q++) mbar_wait(full_a + 8 * (q % ns), (q / ns) & 1u);
 }
 
 }  // namespace dgt

@@ -61,6 +61,7 @@ struct GemmArgs {
     const uint32_t *gjob, *geoff, *glist;
     uint64_t ne;
     uint32_t grouped, topk;
+    uint32_t spin;   // polls a wait for work in flight takes before it gives up
 };
 
 // ---- tcgen05 / TMA wrappers -------------------------------------------------
@@ -128,8 +129,11 @@ __host__ __device__ constexpr uint32_t idesc_bf16(uint32_t n) {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((n >> 3) << 17) | ((128u >> 4) << 24);
 }
 
-__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int *abort_flag) {
-    for (uint32_t i = 0; i < MBAR_SPIN_LIMIT; i++) {
+// A wait for work in flight: true when the phase completed; false when the
+// CTA aborted or `limit` polls ran out.
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                              uint32_t limit) {
+    for (uint32_t i = 0; i < limit; i++) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((i & 63) == 63 && *abort_flag) return false;
     }
@@ -293,7 +297,7 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
             uint32_t issued = 0;
             for (uint32_t i = 0; i < nkb; i++) {
                 const uint32_t s = i % P, use = i / P;
-                if (use > 0 && !wait_or_abort(smem_u32(&bar_empty[s]), (use - 1) & 1u, abortp)) {
+                if (use > 0 && !wait_or_abort(smem_u32(&bar_empty[s]), (use - 1) & 1u, abortp, a.spin)) {
                     set_status(a.status, DGT_ERR_TIMEOUT);
                     *abortp = 1;
                     break;
@@ -313,8 +317,8 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
             // let every copy issued land before the CTA can exit
             for (uint32_t i = issued > P ? issued - P : 0; i < issued; i++) {
                 const uint32_t s = i % P, par = (i / P) & 1u;
-                wait_or_abort(smem_u32(&bar_full[s]), par, abortp) || mbar_wait(smem_u32(&bar_full[s]), par);
-                if (R4) wait_or_abort(smem_u32(&bar_raw[s]), par, abortp) || mbar_wait(smem_u32(&bar_raw[s]), par);
+                wait_or_abort(smem_u32(&bar_full[s]), par, abortp, a.spin) || mbar_wait(smem_u32(&bar_full[s]), par);
+                if (R4) wait_or_abort(smem_u32(&bar_raw[s]), par, abortp, a.spin) || mbar_wait(smem_u32(&bar_raw[s]), par);
             }
         }
     } else if (warp == 1) {
@@ -323,8 +327,8 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
             const uint32_t idesc = idesc_bf16(mt);
             for (uint32_t i = 0; i < nkb; i++) {
                 const uint32_t s = i % P, par = (i / P) & 1u;
-                if (!wait_or_abort(smem_u32(&bar_full[s]), par, abortp) ||
-                    (R4 && !wait_or_abort(smem_u32(&bar_w[s]), par, abortp))) {
+                if (!wait_or_abort(smem_u32(&bar_full[s]), par, abortp, a.spin) ||
+                    (R4 && !wait_or_abort(smem_u32(&bar_w[s]), par, abortp, a.spin))) {
                     set_status(a.status, DGT_ERR_TIMEOUT);
                     *abortp = 1;
                     break;
@@ -376,7 +380,7 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
             const uint32_t base_a = smem_u32(base);
             uint32_t s = 0, par = 0;
             for (uint32_t i = 0; i < nkb; i++) {
-                if (!wait_or_abort(smem_u32(&bar_raw[s]), par, abortp)) {
+                if (!wait_or_abort(smem_u32(&bar_raw[s]), par, abortp, a.spin)) {
                     if (lane == 0) set_status(a.status, DGT_ERR_TIMEOUT);
                     *abortp = 1;
                     break;
@@ -399,7 +403,7 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
         } else {
         const uint32_t t = tid - 128;  // accumulator row, TMEM lane
         // ---- epilogue: thread t holds accumulator row t (W row n0 + t)
-        const bool ok = wait_or_abort(smem_u32(&bar_done), 0, abortp) || mbar_wait(smem_u32(&bar_done), 0);
+        const bool ok = wait_or_abort(smem_u32(&bar_done), 0, abortp, a.spin) || mbar_wait(smem_u32(&bar_done), 0);
         tc_fence_after();
         if (ok && !*abortp) {
             const uint32_t lane_base = ((warp - 4) * 32) << 16;
@@ -537,6 +541,10 @@ static int fill_common(GemmArgs &a, uint64_t M, uint64_t N, uint64_t K, const dg
     else dgt_gemm_default_plan(M, N, K, &p);
     if (p.m_tile < 16 || p.m_tile > 256 || p.m_tile % 16 || p.split_k < 1 || (uint64_t)p.split_k > K / GT_K)
         return DGT_ERR_ARG;
+    if ((p.test_flags & ~(DGT_TEST_SHORT_WAITS | 0xFFFF0000u)) ||
+        (!(p.test_flags & DGT_TEST_SHORT_WAITS) && (p.test_flags >> 16)))
+        return DGT_ERR_ARG;
+    a.spin = wait_limit_from_flags(p.test_flags);
     a.M = M;
     a.N = N;
     a.K = K;
@@ -798,6 +806,7 @@ static int launch_moe_gemm(GemmArgs &g, MgArgs &m, const void *w_or_sm, void *d_
     g.y = nullptr;
     g.status = m.status;
     g.grouped = 1;
+    g.spin = MBAR_SPIN_LIMIT;
     g.gjob = m.gjob;
     g.geoff = m.geoff;
     g.glist = m.glist;
@@ -920,7 +929,7 @@ extern "C" int dgt_gemm_default_plan(uint64_t M, uint64_t N, uint64_t K, dgt_gem
     if (split < 1) split = 1;
     plan->m_tile = (int32_t)mt;
     plan->split_k = (int32_t)split;
-    plan->reserved0 = 0;
+    plan->test_flags = 0;
     plan->reserved1 = 0;
     return DGT_OK;
 }

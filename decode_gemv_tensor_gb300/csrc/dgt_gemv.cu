@@ -54,6 +54,7 @@ struct GemvArgs {
     uint32_t J;
     int S;
     uint32_t early;   // DGT_GEMV_STATIC_WEIGHTS: stream W before the grid dependency wait
+    uint32_t spin;    // polls a consumer waits for a piece before it gives up
     R4Lut L;
     uint8_t table[256];
     int32_t *status;
@@ -359,6 +360,7 @@ __global__ void __launch_bounds__((TNW + TPW) * 32, 1) k_gemv_tma(GemvArgs a) {
     __shared__ uint8_t escb[R4 ? TNW : 1][R4 ? DGT_SEG : 1];
     __shared__ float part[TCHUNK];
     __shared__ int abort_flag;
+    __shared__ uint32_t stop_word[TNW];   // producer lane of ring w: pieces issued, bit 31 once stopped
     const uint32_t tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
     uint4 *xs = reinterpret_cast<uint4 *>(dsm + (size_t)TNW * TNS * STAGE);
     const uint64_t G = gridDim.x;
@@ -381,6 +383,7 @@ __global__ void __launch_bounds__((TNW + TPW) * 32, 1) k_gemv_tma(GemvArgs a) {
         mbar_init(smem_u32(&empty[0][0]) + 8 * i, 1);
     }
     if (tid == 0) abort_flag = 0;
+    if (tid < TNW) stop_word[tid] = 0;
     fence_mbarrier_init();
     __syncthreads();
     // the next kernel may start as SMs free up.  With static weights they
@@ -414,6 +417,7 @@ __global__ void __launch_bounds__((TNW + TPW) * 32, 1) k_gemv_tma(GemvArgs a) {
                     break;
                 }
             }
+            ring_publish_stop(&stop_word[c], q);
         }
         return;
     }
@@ -450,7 +454,7 @@ __global__ void __launch_bounds__((TNW + TPW) * 32, 1) k_gemv_tma(GemvArgs a) {
             float acc = 0.0f;
             for (uint32_t jp = u.j0; jp < u.j1; jp += C) {
                 if (ok) {
-                    if (mbar_wait(full_a + 8 * st, (phases >> st) & 1u)) {
+                    if (mbar_wait_n(full_a + 8 * st, (phases >> st) & 1u, a.spin)) {
                         waited++;
                     } else {
                         ok = false;
@@ -623,9 +627,9 @@ __global__ void __launch_bounds__((TNW + TPW) * 32, 1) k_gemv_tma(GemvArgs a) {
         }
         asm volatile("bar.sync 1, %0;" ::"r"(TNW * 32) : "memory");
     }
-    // after a timeout: copies that may still be in flight land before exit
-    if (!ok)
-        for (uint32_t q = waited; q < waited + TNS; q++) mbar_wait(full_a + 8 * (q % TNS), (q / TNS) & 1u);
+    // after a timeout: the ring's producer stops, and the copies it issued
+    // that this warp did not take land before exit
+    if (!ok) ring_drain(&stop_word[w], full_a, waited, TNS);
 }
 
 // Any shape / alignment: one warp per (row, slice), element loads, x read
@@ -729,9 +733,17 @@ int choose_path(uint64_t K, uint32_t J, bool aligned) {
 
 using namespace dgt;
 
+// Flags the batch-1 products accept: the static-weights promise, and the
+// failure-path test hook with its poll count in bits 16..31.
+static inline bool gemv_flags_ok(unsigned flags) {
+    const unsigned known = DGT_GEMV_STATIC_WEIGHTS | DGT_TEST_SHORT_WAITS;
+    if (flags & ~(known | 0xFFFF0000u)) return false;
+    return (flags & DGT_TEST_SHORT_WAITS) || !(flags >> 16);
+}
+
 extern "C" int dgt_gemv_ex(const dgt_r4 *W, const uint16_t *d_x, uint16_t *d_y, float *d_y32, int32_t *d_status,
                            unsigned flags, void *stream) {
-    if (!W || (flags & ~(unsigned)DGT_GEMV_STATIC_WEIGHTS)) return DGT_ERR_ARG;
+    if (!W || !gemv_flags_ok(flags)) return DGT_ERR_ARG;
     const uint64_t N = W->rows, K = W->cols;
     if (K >= (1ull << 31) || (N && (N * K) / N != K)) return DGT_ERR_SHAPE;
     if (N == 0) return DGT_OK;
@@ -755,6 +767,7 @@ extern "C" int dgt_gemv_ex(const dgt_r4 *W, const uint16_t *d_x, uint16_t *d_y, 
     for (int i = 0; i < 256; i++) a.table[i] = W->table[i];
     a.status = d_status;
     a.early = flags & DGT_GEMV_STATIC_WEIGHTS;
+    a.spin = wait_limit_from_flags(flags);
     const int path = choose_path<true>(K, a.J, aligned16(W->sm) && aligned16(W->nib) && aligned16(d_x));
     return launch_gemv<true>(a, path, (cudaStream_t)stream);
 }
@@ -766,7 +779,7 @@ extern "C" int dgt_gemv(const dgt_r4 *W, const uint16_t *d_x, uint16_t *d_y, flo
 
 extern "C" int dgt_gemv_bf16_ex(const uint16_t *d_W, uint64_t rows, uint64_t cols, const uint16_t *d_x,
                                 uint16_t *d_y, float *d_y32, int32_t *d_status, unsigned flags, void *stream) {
-    if (flags & ~(unsigned)DGT_GEMV_STATIC_WEIGHTS) return DGT_ERR_ARG;
+    if (!gemv_flags_ok(flags)) return DGT_ERR_ARG;
     const uint64_t N = rows, K = cols;
     if (K >= (1ull << 31) || (N && (N * K) / N != K)) return DGT_ERR_SHAPE;
     if (N == 0) return DGT_OK;
@@ -782,6 +795,7 @@ extern "C" int dgt_gemv_bf16_ex(const uint16_t *d_W, uint64_t rows, uint64_t col
     a.cols = K;
     a.J = (uint32_t)((K + 511) / 512);
     a.early = flags & DGT_GEMV_STATIC_WEIGHTS;
+    a.spin = wait_limit_from_flags(flags);
     const int path = choose_path<false>(K, a.J, aligned16(d_W) && aligned16(d_x));
     return launch_gemv<false>(a, path, (cudaStream_t)stream);
 }

@@ -59,6 +59,7 @@ struct MoeArgs {
     uint32_t grid;     // CTAs of the gather kernel
     float *partial;    // pairs * ne * S
     int32_t *status;
+    uint32_t spin;     // polls a consumer waits for a piece before it gives up
 };
 
 static inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -423,7 +424,7 @@ __device__ __forceinline__ void moe_row_pass(const MoeArgs &a, MoeRing &rg, cons
     uint32_t s = 0, send = J >> log2S, jbase = 0;
     for (uint32_t jp = 0; jp < J; jp += MC) {
         if (rg.ok && BK) {
-            if (mbar_wait(rg.full_a + 8 * rg.st, (rg.phases >> rg.st) & 1u)) {
+            if (mbar_wait_n(rg.full_a + 8 * rg.st, (rg.phases >> rg.st) & 1u, a.spin)) {
                 rg.waited++;
             } else {
                 rg.ok = false;
@@ -549,6 +550,7 @@ __global__ void __launch_bounds__((MNW + MPW) * 32, 1) k_moe(MoeArgs a) {
     __shared__ uint8_t table_s[256];
     __shared__ uint8_t escb[R4 ? MNW : 1][R4 ? DGT_SEG : 1];
     __shared__ int abort_flag;
+    __shared__ uint32_t stop_word[MNW];   // producer lane of ring w: pieces issued, bit 31 once stopped
     __shared__ MoeTable T;
     pdl_trigger();
     pdl_wait();
@@ -631,6 +633,7 @@ __global__ void __launch_bounds__((MNW + MPW) * 32, 1) k_moe(MoeArgs a) {
         mbar_init(smem_u32(&empty[0][0]) + 8 * i, 1);
     }
     if (tid == 0) abort_flag = 0;
+    if (tid < MNW) stop_word[tid] = 0;
     if (R4 && tid < 256) table_s[tid] = a.table[tid];
     fence_mbarrier_init();
     __syncthreads();
@@ -668,6 +671,7 @@ __global__ void __launch_bounds__((MNW + MPW) * 32, 1) k_moe(MoeArgs a) {
                     break;
                 }
             }
+            ring_publish_stop(&stop_word[c], q);
         }
         return;
     }
@@ -738,9 +742,9 @@ __global__ void __launch_bounds__((MNW + MPW) * 32, 1) k_moe(MoeArgs a) {
             ok = rg.ok;
         }
     }
-    // after a timeout: copies that may still be in flight land before exit
-    if (!ok && BK)
-        for (uint32_t q = waited; q < waited + MNS; q++) mbar_wait(full_a + 8 * (q % MNS), (q / MNS) & 1u);
+    // after a timeout: the ring's producer stops, and the copies it issued
+    // that this warp did not take land before exit
+    if (!ok && BK) ring_drain(&stop_word[w], full_a, waited, MNS);
 }
 
 __global__ void __launch_bounds__(256) k_moe_combine(MoeArgs a) {
@@ -820,6 +824,7 @@ static int moe_common(MoeArgs &a, uint64_t rows, uint64_t cols, uint32_t n_exper
     a.ids = d_ids;
     a.x = d_x;
     a.status = d_status;
+    a.spin = MBAR_SPIN_LIMIT;
     if (d_status && cudaMemsetAsync(d_status, 0, 4, st) != cudaSuccess) return DGT_ERR_CUDA;
     return DGT_OK;
 }
@@ -833,15 +838,19 @@ extern "C" size_t dgt_moe_workspace_bytes(uint32_t n_experts, uint64_t expert_ro
     return moe_ws_layout(n_experts, expert_rows, cols, tokens, topk).total;
 }
 
-extern "C" int dgt_moe_gemv(const dgt_r4 *W, uint32_t n_experts, const int32_t *d_ids, const float *d_p,
-                            uint32_t tokens, uint32_t topk, const uint16_t *d_x, float *d_y32, uint16_t *d_out,
-                            float *d_out32, void *d_ws, size_t ws_bytes, int32_t *d_status, void *stream) {
+extern "C" int dgt_moe_gemv_ex(const dgt_r4 *W, uint32_t n_experts, const int32_t *d_ids, const float *d_p,
+                               uint32_t tokens, uint32_t topk, const uint16_t *d_x, float *d_y32, uint16_t *d_out,
+                               float *d_out32, void *d_ws, size_t ws_bytes, int32_t *d_status, unsigned flags,
+                               void *stream) {
     if (!W) return DGT_ERR_ARG;
+    if ((flags & ~(DGT_TEST_SHORT_WAITS | 0xFFFF0000u)) || (!(flags & DGT_TEST_SHORT_WAITS) && (flags >> 16)))
+        return DGT_ERR_ARG;
     if (tokens == 0) return DGT_OK;
     cudaStream_t st = (cudaStream_t)stream;
     MoeArgs a = {};
     int rc = moe_common(a, W->rows, W->cols, n_experts, tokens, topk, d_ids, d_x, W->sm, d_status, st);
     if (rc != DGT_OK) return rc;
+    a.spin = wait_limit_from_flags(flags);
     if (!W->nib || !W->seg || (W->n_esc && !W->esc) || !aligned16(W->nib)) return DGT_ERR_ARG;
     a.sm = W->sm;
     a.nib = W->nib;
@@ -858,6 +867,13 @@ extern "C" int dgt_moe_gemv(const dgt_r4 *W, uint32_t n_experts, const int32_t *
     a.out = d_out;
     a.out32 = d_out32;
     return launch_moe<true>(a, d_ws, ws_bytes, st);
+}
+
+extern "C" int dgt_moe_gemv(const dgt_r4 *W, uint32_t n_experts, const int32_t *d_ids, const float *d_p,
+                            uint32_t tokens, uint32_t topk, const uint16_t *d_x, float *d_y32, uint16_t *d_out,
+                            float *d_out32, void *d_ws, size_t ws_bytes, int32_t *d_status, void *stream) {
+    return dgt_moe_gemv_ex(W, n_experts, d_ids, d_p, tokens, topk, d_x, d_y32, d_out, d_out32, d_ws, ws_bytes,
+                           d_status, 0u, stream);
 }
 
 extern "C" int dgt_moe_gemv_bf16(const uint16_t *d_W, uint64_t rows, uint64_t cols, uint32_t n_experts,

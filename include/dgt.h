@@ -295,6 +295,24 @@ int dgt_gemv_bf16(const uint16_t *d_W, uint64_t rows, uint64_t cols, const uint1
  * tail.  Results are the same either way.  Other flags: DGT_ERR_ARG.
  */
 #define DGT_GEMV_STATIC_WEIGHTS 1u
+
+/*
+ * Test hook for the failure path (accepted in the flags of dgt_gemv_ex,
+ * dgt_gemv_bf16_ex and dgt_moe_gemv_ex, and in dgt_gemm_plan.test_flags).
+ * Every wait of the streaming kernels is bounded: a wait for data that does
+ * not arrive within the limit writes DGT_ERR_TIMEOUT to the status word, and
+ * the kernel stops its producers, lets every bulk copy it issued land, frees
+ * its tensor memory and returns, so the context stays usable.  With
+ * DGT_TEST_SHORT_WAITS set, the waits for weights and operands give up after
+ * DGT_TEST_WAIT_POLLS(n) polls (n = 0..65535; 0 gives up at once) instead of
+ * the library's limit of 2^24 polls, so a test can drive that path without a
+ * fault or a hang.  Outputs of such a call are unspecified; the status word
+ * is the result.  The waits that drain copies already issued keep the full
+ * limit.
+ */
+#define DGT_TEST_SHORT_WAITS (1u << 1)
+#define DGT_TEST_WAIT_POLLS(n) (((uint32_t)(n) & 0xFFFFu) << 16)
+
 int dgt_gemv_ex(const dgt_r4 *W, const uint16_t *d_x, uint16_t *d_y, float *d_y32, int32_t *d_status,
                 unsigned flags, void *stream);
 int dgt_gemv_bf16_ex(const uint16_t *d_W, uint64_t rows, uint64_t cols, const uint16_t *d_x, uint16_t *d_y,
@@ -327,6 +345,12 @@ int dgt_moe_gemv(const dgt_r4 *W, uint32_t n_experts, const int32_t *d_ids, cons
                  uint32_t topk, const uint16_t *d_x, float *d_y32, uint16_t *d_out, float *d_out32, void *d_ws,
                  size_t ws_bytes, int32_t *d_status, void *stream);
 
+/* dgt_moe_gemv with launch flags: 0, or the failure-path test hook
+   DGT_TEST_SHORT_WAITS | DGT_TEST_WAIT_POLLS(n); other bits: DGT_ERR_ARG. */
+int dgt_moe_gemv_ex(const dgt_r4 *W, uint32_t n_experts, const int32_t *d_ids, const float *d_p, uint32_t tokens,
+                    uint32_t topk, const uint16_t *d_x, float *d_y32, uint16_t *d_out, float *d_out32, void *d_ws,
+                    size_t ws_bytes, int32_t *d_status, unsigned flags, void *stream);
+
 /* The same gather and order with plain BF16 stacked weights d_W [rows, cols]. */
 int dgt_moe_gemv_bf16(const uint16_t *d_W, uint64_t rows, uint64_t cols, uint32_t n_experts,
                       const int32_t *d_ids, const float *d_p, uint32_t tokens, uint32_t topk,
@@ -358,7 +382,8 @@ int dgt_moe_gemv_bf16(const uint16_t *d_W, uint64_t rows, uint64_t cols, uint32_
 typedef struct dgt_gemm_plan {
     int32_t m_tile;
     int32_t split_k;
-    int32_t reserved0, reserved1;
+    uint32_t test_flags;   /* 0, or DGT_TEST_SHORT_WAITS | DGT_TEST_WAIT_POLLS(n) */
+    int32_t reserved1;
 } dgt_gemm_plan;
 
 int dgt_gemm_default_plan(uint64_t M, uint64_t N, uint64_t K, dgt_gemm_plan *plan);

@@ -100,3 +100,33 @@ MOE = dict(name="moe-30L-128E", layers=30, hidden=2816, experts=128, topk=8,
                       ("o", 2816, 2816)])
 
 GEMM_ROWS = (16, 128, 2048)
+
+
+# Special-value inputs (the exactness claim covers every bf16 pattern, not
+# only the model-like draws above).
+def bf16_patterns(count: int, key, finite_only: bool = False) -> np.ndarray:
+    """`count` bf16 bit patterns: every pattern of the set (all 65,536, or the
+    finite ones) once in a seeded random order, repeated in fresh orders
+    until `count` are drawn."""
+    g = rng(*key)
+    allp = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    if finite_only:
+        allp = allp[np.isfinite(bf16_bits_to_f32(allp))]
+    reps = -(-count // allp.size)
+    return np.concatenate([g.permutation(allp) for _ in range(reps)])[:count]
+
+
+def tiny_weights(rows: int, cols: int, key, log2_scale: int = -128) -> np.ndarray:
+    """bf16 bit patterns of N(0, 1) * 2^log2_scale: at the default scale most
+    are bf16 subnormals (below 2^-126) and the rest the smallest normals."""
+    g = rng(*key)
+    w = np.ldexp(g.standard_normal(rows * cols, dtype=np.float32), log2_scale).astype(np.float32)
+    return f32_to_bf16_bits(w).reshape(rows, cols)
+
+
+def scaled_activations(k: int, key, log2_scale: int, count: int = 1) -> np.ndarray:
+    """bf16 bit patterns [count, k] (or [k]) of N(0, 1) * 2^log2_scale."""
+    g = rng(*key)
+    x = np.ldexp(g.standard_normal(count * k, dtype=np.float32), log2_scale).astype(np.float32)
+    b = f32_to_bf16_bits(x)
+    return b if count == 1 else b.reshape(count, k)

@@ -71,8 +71,10 @@ def test_gemm_matches_twin_and_oracle(dgt, M, N, K, split):
 
 @pytest.mark.parametrize("M", [16, 128, 2048])
 def test_gemm_12b_shapes(dgt, M):
+    # every dense-12B projection, the 3840 x 15360 down projection (longest K,
+    # most split-K) included
     g = np.random.default_rng(M)
-    for pi, (name, N, K) in enumerate(S.DENSE_12B["proj"][:5]):
+    for pi, (name, N, K) in enumerate(S.DENSE_12B["proj"]):
         W = S.weights(N, K, (4, 0, pi, 0))
         X = S.activations(K, (4, 999, M), count=M).reshape(M, K)
         y32, y16, b32, b16 = _both(dgt, W, X)

@@ -152,6 +152,9 @@ def test_gemv_static_weights_flag_and_chained_launches(dgt):
             assert np.array_equal(_host(outs[i]), r16), (static, i)
             xh = r16
     y = torch.empty(N, dtype=torch.bfloat16, device="cuda")
-    assert dgt.lib().dgt_gemv_ex(dgt.C.byref(r4s[0].s), x.data_ptr(), y.data_ptr(), None, None, 2, None) == -1
+    assert dgt.lib().dgt_gemv_ex(dgt.C.byref(r4s[0].s), x.data_ptr(), y.data_ptr(), None, None, 4, None) == -1
     assert dgt.lib().dgt_gemv_bf16_ex(_dev_bf16(ws[0]).data_ptr(), N, K, x.data_ptr(), y.data_ptr(), None, None,
-                                      4, None) == -1
+                                      8, None) == -1
+    # a poll count without the test hook's flag is rejected too
+    assert dgt.lib().dgt_gemv_ex(dgt.C.byref(r4s[0].s), x.data_ptr(), y.data_ptr(), None, None, 1 << 16,
+                                 None) == -1

@@ -68,12 +68,13 @@ def test_moe_without_weights_and_repeated_experts(dgt):
     assert np.array_equal(_u32(yb), ry.view(np.uint32))
 
 
-@pytest.mark.parametrize("proj", S.MOE["expert_proj"], ids=lambda p: p[0])
-def test_moe_layer_shapes_t1_and_t16(dgt, proj):
-    # one layer's stacked experts at full size (128 experts, top-8)
-    name, Ne, K = proj
+@pytest.mark.parametrize("pi", range(len(S.MOE["expert_proj"])), ids=lambda i: S.MOE["expert_proj"][i][0])
+def test_moe_layer_shapes_t1_and_t16(dgt, pi):
+    # one layer's stacked experts at full size (128 experts, top-8), seeded
+    # by the projection's index
+    name, Ne, K = S.MOE["expert_proj"][pi]
     E, topk = S.MOE["experts"], S.MOE["topk"]
-    W = S.weights(E * Ne, K, (5, 0, hash(name) % 97, 0))
+    W = S.weights(E * Ne, K, (5, 0, pi, 0))
     r4 = dgt.load_r4(dgt.upload(dgt.pack(W, 2)))
     Wd = _dev_bf16(W)
     for T in (1, 16):

@@ -342,3 +342,73 @@ def test_decode_step_moe_f64_one_expert_equals_dense_step():
     assert np.allclose(xm, xd, rtol=0, atol=1e-14) and np.array_equal(om, od)
     xh, _ = oracle.decode_step_moe_f64([M], gam, [(np.array([1, 1]), np.array([0.25, 0.75]))], E, x0)
     assert np.allclose(xh, xd, rtol=0, atol=1e-14)
+
+
+# ---------------------------------------------------------------------------
+# special values: IEEE single-precision arithmetic with subnormals kept
+# (no flush to zero), infinities and NaN, which the products must share
+# ---------------------------------------------------------------------------
+def test_gemv_subnormal_weights_are_exact_integers_times_2_pow_minus_133():
+    # a bf16 subnormal with mantissa m is m * 2^-133; with small integer x the
+    # products and partial sums are integers times 2^-133, exact in float32
+    # (a flush to zero would give 0)
+    g = np.random.default_rng(91)
+    N, K = 16, 1500
+    for mmax, xmax in ((127, 3), (3, 1)):          # normal-range sums, then subnormal sums
+        m = g.integers(-mmax, mmax + 1, size=(N, K))
+        xi = g.integers(-xmax, xmax + 1, size=K)
+        w = np.where(m < 0, 0x8000, 0).astype(np.uint16) | np.abs(m).astype(np.uint16)
+        y32, _ = oracle.gemv(w, _bf16(xi))
+        want = (m @ xi).astype(np.float64) * 2.0 ** -133
+        assert np.array_equal(y32.astype(np.float64), want)
+    assert np.any((np.abs(want) < 2.0 ** -126) & (want != 0))
+
+
+def test_gemv_subnormal_products_round_once():
+    # w = 2^-126 (smallest normal), x = 3 * 2^-24: the exact product
+    # 3 * 2^-150 lies between subnormals and one fmaf from +0 rounds it to
+    # nearest even (2^-148, i.e. 2 * 2^-149); a second product adds exactly
+    w = np.array([[0x0080, 0x0080]], np.uint16)
+    x = _bf16([3 * 2.0 ** -24, 3 * 2.0 ** -24])
+    y32, _ = oracle.gemv(w, x)
+    assert y32[0] == np.float32(2.0 ** -147)
+
+
+def test_gemv_infinities_and_nan():
+    K = 600
+    base = np.zeros(K, np.float32)
+    base[:40] = 1.0
+    x = _bf16(np.ones(K))
+    rows = []
+    r = base.copy(); r[7] = np.inf; rows.append((r, "+inf"))
+    r = base.copy(); r[7] = -np.inf; rows.append((r, "-inf"))
+    r = base.copy(); r[7] = np.inf; r[560] = -np.inf; rows.append((r, "nan"))
+    r = base.copy(); r[300] = np.nan; rows.append((r, "nan"))
+    r = base.copy(); r[3] = 2.0 ** 127; r[4] = 2.0 ** 127; rows.append((r, "+inf"))   # overflow
+    w = _bf16(np.stack([r for r, _ in rows]))
+    y32, y16 = oracle.gemv(w, x)
+    for (_, want), v, b in zip(rows, y32, y16):
+        if want == "nan":
+            assert np.isnan(v) and b == 0x7FC0
+        else:
+            assert v == (np.inf if want == "+inf" else -np.inf)
+            assert b == (0x7F80 if want == "+inf" else 0xFF80)
+    # inf * 0 is NaN
+    x0 = np.ones(K, np.float32); x0[7] = 0.0
+    y32, _ = oracle.gemv(_bf16(np.stack([rows[0][0]])), _bf16(x0))
+    assert np.isnan(y32[0])
+
+
+def test_gemv_signed_zeros_give_positive_zero():
+    # every lane starts at +0 and (-0) + (+0) = +0 under round to nearest, so
+    # rows of -0 weights, and products that cancel exactly, give +0 bits
+    K = 1024
+    w = np.zeros((3, K), np.uint16)
+    w[0] = 0x8000
+    w[1, ::2] = 0x8000
+    w[2, 0], w[2, 1] = 0x3F80, 0xBF80           # 1, -1 in one lane chunk
+    x = _bf16(np.ones(K))
+    x[5] = 0x8000
+    y32, y16 = oracle.gemv(w, x)
+    assert np.array_equal(y32.view(np.uint32), np.zeros(3, np.uint32))
+    assert np.array_equal(y16, np.zeros(3, np.uint16))
