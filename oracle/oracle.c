@@ -144,12 +144,29 @@ static int get_bit(const uint32_t *w, uint64_t pos) {
 /* ------------------------------------------------------------------------ */
 /* Format 2, [B] "Two file formats": Rice codes of the ranks.                 */
 /* Block = 64 ranks ([W] BLOCK=64), group = 32 blocks.                       */
-/* A block with Q = sum(r >> k) <= 254 is Rice coded: per rank, q = r >> k   */
-/* zero bits, one 1 bit, then the k low bits of r, least significant first; */
-/* its index byte is Q, so its length is count*(k+1) + Q bits.  A block with */
-/* Q >= 255 stores 8-bit raw ranks and index byte 255.                        */
+/* A block with Q = sum(r >> k) <= 254 is Rice coded; its index byte is Q,   */
+/* so its length is count*(k+1) + Q bits.  Reading (the pages fix no bit     */
+/* layout): the block first holds every rank's k low bits (the remainder     */
+/* field, count*k bits), then every rank's unary part, q = r >> k zero bits  */
+/* and one 1 bit, in rank order.  Remainders are stored least significant   */
+/* bit first, in rank order, except in a full block with k = 1 or 2: there   */
+/* bit i of the remainder of rank 8m + j sits at field bit                   */
+/* 32*floor(m*k/4) + 4j + k*(m mod 4/k) + i ("nibble-slot order": one       */
+/* 32-bit field word, shifted right by k*(m mod 4/k), puts the remainders   */
+/* of ranks 8m..8m+7 under their 4-bit output slots).                        */
+/* A block with Q >= 255 stores 8-bit raw ranks and index byte 255.          */
 /* Every group starts on a 32-bit word boundary.                              */
 /* ------------------------------------------------------------------------ */
+/* Position, inside a block's remainder field, of bit t of the remainder of
+   the block's rank i (cnt ranks in the block). */
+static uint64_t rem_bit_pos(int k, uint64_t cnt, uint64_t i, int t) {
+    if (cnt == OR_BLOCK && (k == 1 || k == 2)) {
+        uint64_t m = i / 8, j = i % 8, per = (uint64_t)(4 / k);   /* output words per field word */
+        return 32 * (m / per) + 4 * j + (uint64_t)k * (m % per) + (uint64_t)t;
+    }
+    return (uint64_t)k * i + (uint64_t)t;
+}
+
 static uint64_t rice_block_q(const uint8_t *r, uint64_t cnt, int k) {
     uint64_t q = 0;
     for (uint64_t i = 0; i < cnt; i++) q += (uint64_t)(r[i] >> k);
@@ -208,12 +225,17 @@ uint64_t or_f2_encode(const uint8_t *ranks, uint64_t n, int k, uint32_t *words,
             uint64_t b = b0 / OR_BLOCK;
             if (q <= 254) {
                 blkq[b] = (uint8_t)q;
+                /* remainder field, then the unary parts */
                 for (uint64_t i = 0; i < cnt; i++) {
                     uint32_t r = ranks[b0 + i];
-                    uint32_t quo = r >> k;
+                    for (int t = 0; t < k; t++)
+                        put_bit(words, pos + rem_bit_pos(k, cnt, i, t), (int)((r >> t) & 1u));
+                }
+                pos += cnt * (uint64_t)k;
+                for (uint64_t i = 0; i < cnt; i++) {
+                    uint32_t quo = (uint32_t)ranks[b0 + i] >> k;
                     for (uint32_t z = 0; z < quo; z++) put_bit(words, pos++, 0);
                     put_bit(words, pos++, 1);
-                    for (int t = 0; t < k; t++) put_bit(words, pos++, (int)((r >> t) & 1u));
                 }
             } else {
                 blkq[b] = 255;
@@ -244,6 +266,8 @@ int or_f2_decode(const uint32_t *words, uint64_t n_words, const uint8_t *blkq,
             uint64_t start = pos;
             if (q != 255) {
                 uint64_t qsum = 0;
+                uint64_t rem0 = pos;            /* remainder field */
+                pos += cnt * (uint64_t)k;       /* unary parts */
                 for (uint64_t i = 0; i < cnt; i++) {
                     uint32_t quo = 0;
                     for (;;) {
@@ -254,8 +278,9 @@ int or_f2_decode(const uint32_t *words, uint64_t n_words, const uint8_t *blkq,
                     }
                     uint32_t rem = 0;
                     for (int t = 0; t < k; t++) {
-                        if (pos >= limit) return -1;
-                        rem |= (uint32_t)get_bit(words, pos++) << t;
+                        uint64_t bp = rem0 + rem_bit_pos(k, cnt, i, t);
+                        if (bp >= limit) return -1;
+                        rem |= (uint32_t)get_bit(words, bp) << t;
                     }
                     uint32_t r = (quo << k) | rem;
                     if (r > 255) return -1;

@@ -131,18 +131,55 @@ def test_f2_golden_tiny_k0():
     assert d["grp"].tolist() == g["grp"]
 
 
+def _golden_block_bits(g):
+    """A golden block's stream bits: the remainder field words (LSB first),
+    then the unary codes repeated."""
+    bits = [(w >> b) & 1 for w in g["rem_words"] for b in range(32)]
+    bits += [int(c) for _ in range(g["repeat"]) for code in g["unary_codes"] for c in code]
+    return bits
+
+
 def test_f2_golden_period_k1():
     g = golden("f2_period_k1.json")
     ex = np.array(g["exponents_pattern"] * g["repeat"], np.int64)
     vals = np.ldexp(1.0, ex - 127).astype(np.float32)
     d = oracle.pack(_bf16(vals).reshape(1, -1), 2)
     assert d["k"] == g["k"]
-    bits = [int(c) for _ in range(g["repeat"]) for code in g["codes"] for c in code]
+    bits = _golden_block_bits(g)
     assert len(bits) == 224
     assert d["words"].tolist() == _pack_bits(bits)
     assert d["words"].size == g["n_words"]
     assert d["blkq"].tolist() == g["blkq"]
     assert d["grp"].tolist() == g["grp"]
+    assert np.array_equal(oracle.unpack(d), _bf16(vals).reshape(1, -1))
+
+
+def test_f2_golden_period_k2():
+    g = golden("f2_period_k2.json")
+    i = np.arange(64)
+    vals = np.ldexp(1.0, 112 + (i % 16) - 127).astype(np.float32)
+    w = _bf16(vals).reshape(1, -1)
+    d = oracle.pack(w, 2)
+    assert d["k"] == g["k"]
+    assert d["table"].tolist() == g["table"]
+    bits = _golden_block_bits(g)
+    assert len(bits) == 288
+    assert d["words"].tolist() == _pack_bits(bits)
+    assert d["words"].size == g["n_words"]
+    assert d["blkq"].tolist() == g["blkq"]
+    assert d["grp"].tolist() == g["grp"]
+    r4 = oracle.r4_encode(d["ranks"], 1, 64)
+    assert r4["esc"].tolist() == g["r4_esc"]
+    assert np.array_equal(oracle.unpack(d), w)
+
+
+def test_f2_partial_block_keeps_rank_order():
+    # a block shorter than 64 ranks stores its remainders in rank order:
+    # 3 ranks [1, 2, 3] with k = 1 -> field bits 1,0,1 then unary '1','01','01'
+    enc = oracle.f2_encode(np.array([1, 2, 3], np.uint8), 1)
+    bits = [1, 0, 1] + [1] + [0, 1] + [0, 1]
+    assert enc["words"].tolist() == _pack_bits(bits)
+    assert enc["blkq"].tolist() == [2]
 
 
 def test_f2_golden_raw_block_and_r4():
