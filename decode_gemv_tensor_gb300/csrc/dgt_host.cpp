@@ -119,6 +119,20 @@ struct RiceReader {
     }
 };
 
+// Format 2 block layout: a Rice block stores its remainder field (the k low
+// bits of every rank) and then the unary parts.  Bit position, inside the
+// remainder field, of the remainder of rank i of a block of cnt ranks: in a
+// full block with k = 1 or 2 the field is in nibble-slot order (one 32-bit
+// field word shifted right by k * (m mod 4/k) lines the remainders of ranks
+// 8m..8m+7 up with their 4-bit R4 slots); otherwise k bits per rank in order.
+inline uint32_t rem_field_pos(int k, uint64_t cnt, uint32_t i) {
+    if (cnt == DGT_BLOCK && (k == 1 || k == 2)) {
+        const uint32_t m = i >> 3, j = i & 7, per = 4u / (uint32_t)k;
+        return 32u * (m / per) + 4u * j + (uint32_t)k * (m % per);
+    }
+    return (uint32_t)k * i;
+}
+
 inline uint8_t sm_of(uint16_t b) { return (uint8_t)(((b >> 8) & 0x80) | (b & 0x7F)); }
 inline uint8_t exp_of(uint16_t b) { return (uint8_t)((b >> 7) & 0xFF); }
 // The ranks of a tensor, read from its bf16 bits through the rank table
@@ -191,11 +205,21 @@ int pack_format2(dgt_packed *p, const Ranks &rk, int nt) {
                 for (uint64_t i = 0; i < cnt; i++) q += (uint32_t)rk[i0 + i] >> k;
                 if (q <= 254) {
                     p->blkq[b] = (uint8_t)q;
+                    // remainder field (at most 64 * 7 bits), then the unary parts
+                    uint32_t fld[DGT_BLOCK * 7 / 32] = {0};
+                    if (k) {
+                        for (uint32_t i = 0; i < (uint32_t)cnt; i++) {
+                            const uint32_t rem = (uint32_t)rk[i0 + i] & ((1u << k) - 1u);
+                            const uint32_t at = rem_field_pos(k, cnt, i);
+                            for (int t = 0; t < k; t++)
+                                fld[(at + t) >> 5] |= ((rem >> t) & 1u) << ((at + t) & 31);
+                        }
+                        const uint32_t fbits = (uint32_t)cnt * (uint32_t)k;
+                        for (uint32_t o = 0; o < fbits; o += 32) bw.put(fld[o >> 5], (int)std::min(32u, fbits - o));
+                    }
                     for (uint64_t i = 0; i < cnt; i++) {
-                        uint32_t r = rk[i0 + i];
-                        uint32_t quo = r >> k;
-                        bw.zeros((int)quo);
-                        bw.put(1u | ((uint64_t)(r & ((1u << k) - 1u)) << 1), k + 1);
+                        bw.zeros((int)((uint32_t)rk[i0 + i] >> k));
+                        bw.put(1u, 1);
                     }
                 } else {
                     p->blkq[b] = 255;
@@ -435,16 +459,29 @@ int dgt_unpack(const dgt_packed_view *v, uint16_t *out, int nthreads) {
                     uint64_t i0 = b * DGT_BLOCK, cnt = std::min<uint64_t>(DGT_BLOCK, n - i0);
                     uint8_t q = v->blkq[b];
                     if (q != 255) {
-                        uint64_t start = br.pos;
+                        const uint64_t start = br.pos;
+                        // the remainder field, read whole (at most 64 * 7 bits)
+                        uint32_t fld[DGT_BLOCK * 7 / 32 + 1] = {0};
+                        const uint32_t fbits = (uint32_t)cnt * (uint32_t)k;
+                        for (uint32_t o = 0; o < fbits; o += 32) {
+                            fld[o >> 5] = (uint32_t)br.window();
+                            br.pos += std::min(32u, fbits - o);
+                        }
+                        if (fbits & 31) fld[fbits >> 5] &= (1u << (fbits & 31)) - 1u;
                         uint32_t qs = 0;
                         for (uint64_t i = 0; i < cnt; i++) {
                             uint32_t quo = 0;
-                            const uint32_t r = br.code(k, &quo);
+                            br.code(0, &quo);
+                            const uint32_t at = rem_field_pos(k, cnt, (uint32_t)i);
+                            const uint64_t two = fld[at >> 5] | ((uint64_t)fld[(at >> 5) + 1] << 32);
+                            const uint32_t rem = k ? (uint32_t)(two >> (at & 31)) & ((1u << k) - 1u) : 0u;
+                            const uint32_t r = (quo << k) | rem;
                             if (r > 255) br.bad = true;
                             qs += quo;
                             out[i0 + i] = bf16_of(v->sm[i0 + i], v->table[r & 255]);
                         }
-                        if (qs != q || br.pos - start != cnt * (uint64_t)(k + 1) + q) br.bad = true;
+                        if (qs != q || br.pos - start != cnt * (uint64_t)(k + 1) + q || br.pos > br.limit)
+                            br.bad = true;
                     } else {
                         for (uint64_t i = 0; i < cnt; i++)
                             out[i0 + i] = bf16_of(v->sm[i0 + i], v->table[br.raw8()]);

@@ -56,18 +56,28 @@ __device__ __forceinline__ void next_seg_start(SegWalk &s, uint64_t cols) {
 // ---------------------------------------------------------------------------
 // format 2 (Rice) -> R4
 //
-// One warp per group, one lane per 64-rank block.  A full Rice block is
-// decoded in exactly 32 steps of two codes each: the next 12 stream bits index
-// a table whose entry holds both codes' ranks as one output byte and the bits
-// they use, so a step is a few integer instructions, its output byte lands at
-// a fixed place and no lane waits on another.  The table is replicated REP
-// times, copy c in the banks = c (mod REP), so that only the lanes sharing a
-// copy can conflict.  An entry also carries the rank of one escape
-// (rank >= 15) when both codes fit; windows the table cannot finish (codes
-// longer than the window, two escapes) take an out-of-line step that decodes
-// the two codes one by one.  The next group's stream is copied to shared
-// memory (cp.async) while this one decodes.  Partial and raw blocks, and
-// groups too long to stage, take a per-code path.
+// Block layout (dgt.h): a Rice block holds its remainder field (the k low
+// bits of every rank; in a full block with k = 1, 2 in nibble-slot order)
+// and then every rank's unary part (q = r >> k zeros, a one).  One warp per
+// group of 32 blocks, one lane per 64-rank block, a persistent grid.
+//
+// A full block with k <= 2 is decoded in exactly 16 steps of four ranks.  The
+// next 14 bits of its unary parts index a table whose entry holds the four
+// quotients as 4-bit fields min(q << k, 15), the bits they use and a flag for
+// a field that may belong to an escape (rank >= 15).  A step is a window
+// extract, one table load and a position update.  Two steps give the
+// quotient fields of eight ranks; one shift and one mask of a remainder field
+// word put the remainders under them, giving one 32-bit word of eight R4
+// nibbles (nibble = min(rank, 15) since (q << k) | rem saturates exactly when
+// the rank is 15 or more).  A window with fewer than four complete codes
+// finishes its step code by code with find-first-set, in line.  The table is
+// built at compile time (one per k) and bulk-copied into shared memory while
+// the previous kernel of the stream finishes.  An output word whose fields
+// may hold an escape records where its codes start; after the loop those
+// words are decoded again code by code to get the escapes' exact ranks.  Raw
+// and partial blocks, k >= 3 and groups too long to stage take a per-code
+// path.  The next group's stream is copied to shared memory (cp.async) while
+// this one decodes.
 // ---------------------------------------------------------------------------
 struct F2Args {
     const uint32_t *words;
@@ -83,60 +93,49 @@ struct F2Args {
     int32_t *status;
 };
 
-#ifndef DGT_RICE_REP
-#define DGT_RICE_REP 4
-#endif
 #ifndef DGT_RICE_RW
-#define DGT_RICE_RW 24
+#define DGT_RICE_RW 32
 #endif
 constexpr int RW = DGT_RICE_RW;  // warps per CTA
-constexpr int RWIN = 12;        // table window bits
-constexpr int REP = DGT_RICE_REP;  // table copies (lane l uses copy l mod REP)
-constexpr int RCAP = 192;       // staged stream words per group (about 170 at 2.7 bits/rank)
-constexpr int RPAD = 16;        // zero words after the staged stream
+constexpr int RWIN = 14;         // table window bits
+constexpr int RCAP = 192;        // staged stream words per group (about 170 at 2.7 bits/rank)
+constexpr int RPAD = 16;         // zero words after the staged stream
 constexpr int RBUF = RCAP + RPAD;
-constexpr int RLIST = 16;       // escapes kept per lane; more re-walk the block
-constexpr uint32_t RARE = 1u << 26;
+constexpr int RESC = 16;         // escape ranks kept per lane; more re-walk the block
+constexpr uint32_t R4_ESCF = 1u << 16;   // table entry: a field may belong to an escape
 
-// Per-lane escape record of the block being decoded.
-struct LaneEsc {
-    unsigned long long emask;   // bit s: rank s of the block is an escape
-    uint32_t ec;                // escapes seen
-    uint32_t bad;
-    uint32_t end;               // bit position after the block
-    uint32_t cur;               // which stream buffer holds the group
-    uint8_t list[RLIST];        // escape ranks, in order
-};
-
-struct RiceSmem {
-    uint32_t lut[(1 << RWIN) * REP];
-    uint32_t buf[2][RW][RBUF];
-    LaneEsc le[RW][32];
-    int k;
-};
-
-// Table entry for window v (bit 0 = next stream bit).  Both codes fit:
-// bits 0..4 and 27..31 = their bit count, 8..15 = output byte (min(rank,15)
-// nibbles); with one escape also bit 24/25 (first/second code), 16..23 = its
-// rank, and RARE.  Otherwise RARE alone.
-__device__ __forceinline__ uint32_t rice_pair_entry(uint32_t v, int k) {
-    uint32_t pos = 0, byte = 0, escf = 0, escr = 0;
-    for (int s = 0; s < 2; s++) {
-        const uint32_t rest = v >> pos;   // the window's bits from pos (v < 2^RWIN)
-        if (rest == 0) return RARE;       // no terminating one inside the window
-        const uint32_t q = __ffs(rest) - 1;
-        if (pos + q + 1 + (uint32_t)k > RWIN) return RARE;
-        const uint32_t r = (q << k) | ((v >> (pos + q + 1)) & ((1u << k) - 1u));
-        if (r >= 15) {
-            if (escf) return RARE;
-            escf = 1u << (24 + s);
-            escr = r;
-        }
-        byte |= min(r, 15u) << (4 * s);
-        pos += q + 1 + k;
+// Table entry for window v (bit 0 = next bit of the unary parts): bits 0..15
+// the fields min(q << k, 15) of the first four codes, R4_ESCF if one of them
+// is at least 16 - 2^k (the rank may be 15 or more), bits 28..31 the bits the
+// four use.  A window with fewer than four complete codes has 0 in bits
+// 28..31, the fields of its c complete codes, c in bits 17..19 and the bits
+// they use in bits 20..23.
+constexpr uint32_t rice4_entry(uint32_t v, int k) {
+    uint32_t pos = 0, f = 0, fl = 0;
+    for (uint32_t c = 0; c < 4; c++) {
+        uint32_t q = 0;
+        while (pos + q < (uint32_t)RWIN && !((v >> (pos + q)) & 1u)) q++;
+        if (pos + q >= (uint32_t)RWIN) return f | fl | (c << 17) | (pos << 20);
+        const uint32_t fq = (q << k) < 15u ? (q << k) : 15u;
+        f |= fq << (4 * c);
+        if (fq >= 16u - (1u << k)) fl = R4_ESCF;
+        pos += q + 1;
     }
-    return pos | (byte << 8) | (escr << 16) | escf | (escf ? RARE : 0u) | (pos << 27);
+    return f | fl | (pos << 28);
 }
+
+struct RiceLut {
+    uint32_t t[3][1 << RWIN];
+};
+constexpr RiceLut make_rice_lut() {
+    RiceLut r{};
+    for (int k = 0; k < 3; k++)
+        for (uint32_t v = 0; v < (1u << RWIN); v++) r.t[k][v] = rice4_entry(v, k);
+    return r;
+}
+// The three tables (k = 0, 1, 2) in the library's device image: 192 KB,
+// built by the compiler.
+__device__ __align__(16) const RiceLut g_rice_lut = make_rice_lut();
 
 template <class Src>
 struct WordReader {
@@ -145,45 +144,63 @@ struct WordReader {
     __device__ __forceinline__ uint32_t operator()(uint32_t i) const { return i < nw ? src[i] : 0u; }
 };
 
-// One code at bit pos (Rice parameter k, or 8 raw bits when raw): returns its
-// rank and advances pos.  Unary runs longer than 255 or ranks above 255 set
-// bad.
+// Zeros before the next one at bit pos (at most 255 counted; more set bad);
+// pos moves past the one.
 template <class Rd>
-__device__ __forceinline__ uint32_t rice_code(const Rd &rd, uint32_t &pos, int k, bool raw, bool &bad) {
-    const uint32_t wi = pos >> 5;
-    const uint32_t win = __funnelshift_r(rd(wi), rd(wi + 1), pos);
-    if (raw) {
-        pos += 8;
-        return win & 0xFFu;
+__device__ __forceinline__ uint32_t unary_at(const Rd &rd, uint32_t &pos, bool &bad) {
+    const uint32_t win = __funnelshift_r(rd(pos >> 5), rd((pos >> 5) + 1), pos);
+    if (win) {
+        const uint32_t q = __ffs(win) - 1;
+        pos += q + 1;
+        return q;
     }
-    const uint32_t kmask = (1u << k) - 1u;
-    uint32_t r;
-    uint32_t z;
-    if (win != 0 && (z = __ffs(win) - 1) + 1 + (uint32_t)k <= 32) {
-        r = (z << k) | (k ? (win >> (z + 1)) & kmask : 0u);
-        pos += z + 1 + k;
-    } else {
-        // the unary part runs past this window: walk word by word
-        uint32_t p = pos, zz = 0;
-        for (;;) {
-            const uint32_t wv = rd(p >> 5) >> (p & 31);
-            const uint32_t avail = 32 - (p & 31);
-            if (wv) {
-                const uint32_t f = __ffs(wv) - 1;
-                zz += f;
-                p += f;
-                break;
-            }
-            zz += avail;
-            p += avail;
-            if (zz > 255) break;
+    uint32_t p = pos, q = 0;
+    for (;;) {
+        const uint32_t wv = rd(p >> 5) >> (p & 31);
+        const uint32_t avail = 32 - (p & 31);
+        if (wv) {
+            const uint32_t f = __ffs(wv) - 1;
+            q += f;
+            p += f;
+            break;
         }
-        p += 1;
-        const uint32_t rem = __funnelshift_r(rd(p >> 5), rd((p >> 5) + 1), p) & kmask;
-        r = (zz << k) | rem;
-        pos = p + k;
-        if (zz > 255) bad = true;
+        q += avail;
+        p += avail;
+        if (q > 255) {
+            bad = true;
+            break;
+        }
     }
+    pos = p + 1;
+    return q;
+}
+
+// k bits at bit pos (k <= 8).
+template <class Rd>
+__device__ __forceinline__ uint32_t bits_at(const Rd &rd, uint32_t pos, int k) {
+    return __funnelshift_r(rd(pos >> 5), rd((pos >> 5) + 1), pos) & ((1u << k) - 1u);
+}
+
+// Position, inside a block's remainder field, of the remainder of rank i
+// (cnt ranks): nibble-slot order for a full block with k = 1, 2, else k bits
+// per rank in order.
+__device__ __forceinline__ uint32_t rem_field_pos(int k, uint32_t cnt, uint32_t i) {
+    if (cnt == DGT_BLOCK && (k == 1 || k == 2)) {
+        const uint32_t m = i >> 3, j = i & 7, per = 4u / (uint32_t)k;
+        return 32u * (m / per) + 4u * j + (uint32_t)k * (m % per);
+    }
+    return (uint32_t)k * i;
+}
+
+// Rank i of a block starting at bit b0 (the per-code path); *up = the next
+// unary part (advanced).
+template <class Rd>
+__device__ __forceinline__ uint32_t rice_rank_slow(const Rd &rd, uint32_t b0, uint32_t *up, uint32_t i, uint32_t cnt,
+                                                   int k, bool raw, bool &bad) {
+    if (raw) return bits_at(rd, b0 + 8 * i, 8);
+    const uint32_t q = unary_at(rd, *up, bad);
+    const uint32_t rem = k ? bits_at(rd, b0 + rem_field_pos(k, cnt, i), k) : 0u;
+    uint32_t r = (q << k) | rem;
     if (r > 255) {
         bad = true;
         r = 255;
@@ -191,114 +208,72 @@ __device__ __forceinline__ uint32_t rice_code(const Rd &rd, uint32_t &pos, int k
     return r;
 }
 
-__device__ __forceinline__ void note_escape(LaneEsc *le, uint32_t r, uint32_t s) {
-    const uint32_t c = le->ec;
-    if (c < RLIST) le->list[c] = (uint8_t)r;
-    le->ec = c + 1;
-    le->emask |= 1ull << s;
-}
-
-struct RareOut {
-    uint32_t e, pos, win;
+// Per-code path for one block: nibbles straight to nib (bytes).
+struct SlowBlock {
+    uint32_t ec, end, bad;
+    uint64_t emask;   // bit s: rank s of the block is an escape
 };
-
-// Out-of-line part of step j: record the table entry's escape, or decode the
-// two codes at pos one by one (returning an entry with the output byte and a
-// zero bit count, pos after the codes, clamped to the block end, and the
-// window there).  The lane's state is read from shared memory so that the
-// call passes four words.
-__device__ __noinline__ RareOut rice_rare(uint32_t e, uint32_t pos, uint32_t win, uint32_t j) {
-    extern __shared__ uint4 smem_raw[];
-    RiceSmem &S = *reinterpret_cast<RiceSmem *>(smem_raw);
-    const uint32_t w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    LaneEsc *le = &S.le[w][lane];
-    RareOut o;
-    if (e & (3u << 24)) {
-        note_escape(le, (e >> 16) & 0xFFu, 2 * j + ((e >> 25) & 1u));
-        o.e = e;
-        o.pos = pos;
-        o.win = win;
-        return o;
-    }
-    const uint32_t *buf = S.buf[le->cur][w];
-    const int k = S.k;
-    const uint32_t end = le->end;
-    WordReader<const uint32_t *> rd{buf, RBUF};
-    bool bad = false;
-    const uint32_t r0 = rice_code(rd, pos, k, false, bad);
-    const uint32_t r1 = rice_code(rd, pos, k, false, bad);
-    if (pos > end) {
-        bad = true;
-        pos = end;
-    }
-    if (r0 >= 15) note_escape(le, r0, 2 * j);
-    if (r1 >= 15) note_escape(le, r1, 2 * j + 1);
-    if (bad) le->bad = 1;
-    o.e = (min(r0, 15u) | (min(r1, 15u) << 4)) << 8;
-    o.pos = pos;
-    o.win = __funnelshift_r(buf[pos >> 5], buf[(pos >> 5) + 1], pos);
-    return o;
-}
-
-// Step j of a full block: returns the table entry (output byte at bits 8..15).
-template <bool REFILL>
-__device__ __forceinline__ uint32_t rice_step(const uint32_t *lutc, const uint32_t *buf, uint32_t &pos,
-                                              uint32_t &win, uint32_t prev, uint32_t j) {
-    if (REFILL) {
-        const uint32_t wi = pos >> 5;
-        win = __funnelshift_r(buf[wi], buf[wi + 1], pos);
-    } else {
-        win = __funnelshift_r(win, 0u, prev);
-    }
-    uint32_t e = lutc[(win & ((1u << RWIN) - 1u)) * REP];
-    if (e & RARE) {
-        const RareOut o = rice_rare(e, pos, win, j);
-        e = o.e;
-        pos = o.pos;
-        win = o.win;
-    }
-    pos += e >> 27;
-    return e;
-}
-
-// Per-code path for one block: nibbles go straight to nib (bytes), escapes to
-// the lane's record.  Returns the bit position after the block.
 template <class Rd>
-__device__ __noinline__ uint32_t rice_block_slow(Rd rd, uint32_t pos, uint32_t cnt, bool raw, int k,
-                                                 uint8_t *nib, LaneEsc *le) {
+__device__ __noinline__ SlowBlock rice_block_slow(Rd rd, uint32_t b0, uint32_t cnt, bool raw, int k, uint8_t *nib) {
     bool bad = false;
-    uint32_t byte = 0;
+    uint32_t up = b0 + cnt * (uint32_t)k, byte = 0, ec = 0;
+    uint64_t em = 0;
     for (uint32_t s = 0; s < cnt; s++) {
-        const uint32_t r = rice_code(rd, pos, k, raw, bad);
-        if (r >= 15) note_escape(le, r, s);
+        const uint32_t r = rice_rank_slow(rd, b0, &up, s, cnt, k, raw, bad);
+        if (r >= 15) {
+            ec++;
+            em |= 1ull << s;
+        }
         byte |= min(r, 15u) << (4 * (s & 1));
         if ((s & 1) || s + 1 == cnt) {
             nib[s >> 1] = (uint8_t)byte;
             byte = 0;
         }
     }
-    if (bad) le->bad = 1;
-    return pos;
+    SlowBlock o;
+    o.ec = ec;
+    o.end = raw ? b0 + 8 * cnt : up;
+    o.bad = bad;
+    o.emask = em;
+    return o;
 }
 
-// Escapes of one block written straight to esc (more than RLIST of them).
+// The escapes of one block (per-code path) written to dst in order.
 template <class Rd>
-__device__ __noinline__ void rice_block_escapes(Rd rd, uint32_t pos, uint32_t cnt, bool raw, int k, uint8_t *dst) {
+__device__ __noinline__ void rice_block_slow_escapes(Rd rd, uint32_t b0, uint32_t cnt, bool raw, int k, uint8_t *dst) {
     bool bad = false;
+    uint32_t up = b0 + cnt * (uint32_t)k;
     for (uint32_t s = 0; s < cnt; s++) {
-        const uint32_t r = rice_code(rd, pos, k, raw, bad);
+        const uint32_t r = rice_rank_slow(rd, b0, &up, s, cnt, k, raw, bad);
         if (r >= 15) *dst++ = (uint8_t)r;
     }
 }
 
+// A unary run of 32 or more zeros at bit p of the staged buffer.
+struct LongRun {
+    uint32_t q, p, bad;
+};
+__device__ __noinline__ LongRun rice_long_run(const uint32_t *buf, uint32_t p) {
+    bool bad = false;
+    LongRun o;
+    o.q = unary_at(WordReader<const uint32_t *>{buf, RBUF}, p, bad);
+    o.p = p;
+    o.bad = bad;
+    return o;
+}
+
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+__device__ __forceinline__ void cp_async16(uint32_t *dst, const uint32_t *src, uint32_t bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(bytes)
+                 : "memory");
+}
 __device__ __forceinline__ void cp_async4(uint32_t *dst, const uint32_t *src, uint32_t bytes) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(bytes)
                  : "memory");
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 
-// A group's index entries and this lane's block-length byte, loaded one or
+// A group's index entries and this lane's block index byte, loaded one or
 // two groups ahead of use.
 struct RiceMeta {
     uint32_t w0, base;     // first stream word, escapes before the group
@@ -319,28 +294,10 @@ __device__ __forceinline__ RiceMeta rice_meta(const F2Args &a, uint64_t g, uint3
     return m;
 }
 
-// Copy group g's stream words (up to RBUF; zeros after its end) into dst.
-__device__ __forceinline__ void rice_stage(const F2Args &a, uint64_t g, const RiceMeta &m, uint32_t *dst,
-                                           uint32_t lane) {
-    if (g < a.ngrp) {
-        const uint64_t w0 = m.w0, w1 = m.nextw;
-        const uint64_t nw = (w1 > w0 && w1 <= a.n_words && w0 < a.n_words) ? w1 - w0 : 0;
-        for (uint32_t i = lane; i < RBUF; i += 32) {
-            const bool in = i < nw;
-            cp_async4(dst + i, in ? a.words + w0 + i : a.words, in ? 4u : 0u);
-        }
-    }
-    cp_async_commit();
-}
-
-__device__ __forceinline__ void cp_async16(uint32_t *dst, const uint32_t *src, uint32_t bytes) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(bytes)
-                 : "memory");
-}
-
 // Group g's stream in 16-byte pieces from the 16-byte boundary at or below
 // its first word (the stream then starts 32 * (w0 % 4) bits into dst); bytes
 // past the stream array's end, and past the buffer's need, are zero-filled.
+// The stream array must start on a 16-byte boundary.
 __device__ __forceinline__ void rice_stage16(const F2Args &a, uint64_t g, const RiceMeta &m, uint32_t *dst,
                                              uint32_t lane) {
     if (g < a.ngrp) {
@@ -356,30 +313,63 @@ __device__ __forceinline__ void rice_stage16(const F2Args &a, uint64_t g, const 
     cp_async_commit();
 }
 
+// Word by word copy for a stream array that is not 16-byte aligned (the
+// stream starts at dst[0]).
+__device__ __forceinline__ void rice_stage4(const F2Args &a, uint64_t g, const RiceMeta &m, uint32_t *dst,
+                                            uint32_t lane) {
+    if (g < a.ngrp) {
+        const uint64_t w0 = m.w0, w1 = m.nextw;
+        const uint64_t nw = (w1 > w0 && w1 <= a.n_words && w0 < a.n_words) ? w1 - w0 : 0;
+        for (uint32_t i = lane; i < RBUF; i += 32) {
+            const bool in = i < nw;
+            cp_async4(dst + i, in ? a.words + w0 + i : a.words, in ? 4u : 0u);
+        }
+    }
+    cp_async_commit();
+}
+
+struct RiceSmem {
+    uint32_t lut[1 << RWIN];
+    uint32_t buf[2][RW][RBUF];
+    uint32_t rec[RW][8][32];      // per lane: where each flagged output word's codes start
+    uint32_t recf[RW][8][32];     // and its quotient fields
+    uint8_t escl[RW][RESC][32];   // per lane: escape ranks of the block, in order
+    uint64_t lut_bar;
+};
+
 // FAST: 32-bit block indices (n < 2^31), blocks that never straddle rows
 // (cols % 64 == 0, cols >= 2048), rows * nseg < 2^32 and a 16-byte aligned
-// stream: the group bookkeeping takes a shorter path.
-template <bool FAST>
+// stream: the group bookkeeping takes a shorter path.  K = the tensor's Rice
+// parameter for 0, 1, 2 (the table path); 3 for any larger k (per-code path).
+template <bool FAST, int K>
 __global__ void __launch_bounds__(RW * 32, 1) k_rice_to_r4(F2Args a) {
-    extern __shared__ uint4 smem_raw[];
-    RiceSmem &S = *reinterpret_cast<RiceSmem *>(smem_raw);
-    static_assert(REP % 4 == 0, "table rows are written as uint4");
-    for (uint32_t v = threadIdx.x; v < (1u << RWIN); v += blockDim.x) {
-        const uint32_t e = rice_pair_entry(v, a.k);
-#pragma unroll
-        for (int c = 0; c < REP / 4; c++) reinterpret_cast<uint4 *>(S.lut)[v * (REP / 4) + c] = make_uint4(e, e, e, e);
+    extern __shared__ __align__(16) uint8_t rice_smem[];
+    RiceSmem &S = *reinterpret_cast<RiceSmem *>(rice_smem);
+    const uint32_t w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    constexpr bool TAB = K <= 2;
+    const int k = TAB ? K : a.k;
+    const uint32_t bar = smem_u32(&S.lut_bar);
+    if (TAB && threadIdx.x == 0) {
+        // the table does not depend on the previous kernel: it is copied while
+        // that kernel may still run
+        mbar_init(bar, 1);
+        fence_mbarrier_init();
+        mbar_arrive_expect_tx(bar, sizeof(S.lut));
+        bulk_g2s(smem_u32(S.lut), g_rice_lut.t[TAB ? K : 0], sizeof(S.lut), bar);
     }
-    if (threadIdx.x == 0) S.k = a.k;
-    // the table is built while the previous kernel of the stream may still
-    // run; its outputs (and anything it reads) are touched only after this
     pdl_trigger();
     pdl_wait();
     if (blockIdx.x == 0 && threadIdx.x == 0) a.seg[a.seg_last] = (uint32_t)a.n_esc;
     __syncthreads();
-    const uint32_t w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint32_t *lutc = S.lut + (lane & (REP - 1));
-    LaneEsc *le = &S.le[w][lane];
-    const int k = a.k;
+    bool lut_ok = true;
+    if (TAB) {
+        lut_ok = mbar_wait(bar, 0);
+        if (!lut_ok) {
+            if (threadIdx.x == 0) set_status(a.status, DGT_ERR_TIMEOUT);
+            mbar_wait(bar, 0);   // the copy lands before the CTA can exit
+            return;
+        }
+    }
     // row / column of the group's first rank, stepped with the grid stride
     const uint64_t g0 = (uint64_t)blockIdx.x * RW + w, G = (uint64_t)gridDim.x * RW;
     const uint64_t GS = (uint64_t)DGT_GROUP * DGT_BLOCK;
@@ -390,13 +380,13 @@ __global__ void __launch_bounds__(RW * 32, 1) k_rice_to_r4(F2Args a) {
     RiceMeta m0 = rice_meta(a, g0, lane);
     RiceMeta m1 = rice_meta(a, g0 + G, lane);
     if (FAST) rice_stage16(a, g0, m0, S.buf[0][w], lane);
-    else rice_stage(a, g0, m0, S.buf[0][w], lane);
+    else rice_stage4(a, g0, m0, S.buf[0][w], lane);
     const uint32_t nfull = (uint32_t)(a.n / DGT_BLOCK), nblk32 = (uint32_t)a.nblk;
     uint32_t cur = 0;
     for (uint64_t g = g0; g < a.ngrp; g += G, cur ^= 1) {
-        uint32_t *buf = S.buf[cur][w];
+        const uint32_t *buf = S.buf[cur][w];
         if (FAST) rice_stage16(a, g + G, m1, S.buf[cur ^ 1][w], lane);
-        else rice_stage(a, g + G, m1, S.buf[cur ^ 1][w], lane);
+        else rice_stage4(a, g + G, m1, S.buf[cur ^ 1][w], lane);
         const RiceMeta m2 = rice_meta(a, g + 2 * G, lane);
         const uint64_t blk = g * DGT_GROUP + lane;
         const uint64_t B0 = blk * DGT_BLOCK;
@@ -409,7 +399,8 @@ __global__ void __launch_bounds__(RW * 32, 1) k_rice_to_r4(F2Args a) {
         }
         const uint32_t boff = FAST ? 32u * (m0.w0 & 3u) : 0u;   // stream start inside the staged buffer
         const uint32_t q = cnt ? m0.q : 0u;
-        const uint32_t len = cnt == 0 ? 0u : (q != 255 ? cnt * (uint32_t)(k + 1) + q : 8u * cnt);
+        const bool raw = q == 255;
+        const uint32_t len = cnt == 0 ? 0u : (!raw ? cnt * (uint32_t)(k + 1) + q : 8u * cnt);
         uint32_t gbits;
         const uint32_t off = warp_excl_scan(len, &gbits);
         const uint32_t nw = (gbits + 31) / 32;
@@ -449,53 +440,180 @@ __global__ void __launch_bounds__(RW * 32, 1) k_rice_to_r4(F2Args a) {
             __syncwarp();
             continue;
         }
-        const bool staged = nw <= RCAP;
-        const uint32_t end = off + len + (staged ? boff : 0u);
-        le->emask = 0;
-        le->ec = 0;
-        le->bad = 0;
-        le->end = end;
-        le->cur = cur;
+        const bool staged = nw + (boff >> 5) <= RCAP;
+        const uint32_t b0 = off + (staged ? boff : 0u);   // block start (bits) in the staged buffer or the stream
+        const uint32_t end = b0 + len;
         bool bad = false;
-        if (staged && cnt == DGT_BLOCK && q != 255) {
-            uint32_t pos = off + boff, win = 0, out[8];
+        uint32_t ec = 0;
+        uint64_t emask = 0;
+        const bool fast = TAB && staged && cnt == DGT_BLOCK && !raw;
+        if (TAB && fast) {
+            constexpr uint32_t KK = TAB ? K : 0;
+            constexpr uint32_t THR = 16u - (1u << KK);   // a field at least this may hold an escape
+            uint32_t fw[4] = {0, 0, 0, 0};               // remainder field words
 #pragma unroll
-            for (int it = 0; it < 8; it++) {
-                const uint32_t e0 = rice_step<true>(lutc, buf, pos, win, 0u, 4 * it + 0);
-                const uint32_t e1 = rice_step<false>(lutc, buf, pos, win, e0, 4 * it + 1);
-                const uint32_t e2 = rice_step<true>(lutc, buf, pos, win, 0u, 4 * it + 2);
-                const uint32_t e3 = rice_step<false>(lutc, buf, pos, win, e2, 4 * it + 3);
-                out[it] = __byte_perm(__byte_perm(e0, e1, 0x51u), __byte_perm(e2, e3, 0x51u), 0x5410u);
+            for (int h = 0; h < 2 * (int)KK; h++) {
+                const uint32_t p = b0 + 32 * h;
+                fw[h] = __funnelshift_r(buf[p >> 5], buf[(p >> 5) + 1], p);
             }
-            if (pos != end) bad = true;
+            uint32_t p = b0 + 64 * KK;   // the unary parts
+            uint32_t wi = p >> 5, lo = buf[wi], hi = buf[wi + 1];
+            uint32_t out[8], nrec = 0, badw = 0;
+#pragma unroll
+            for (uint32_t m = 0; m < 8; m++) {
+                const uint32_t pws = p;
+                // two steps from one 32-bit window: a step uses at most 14 bits,
+                // so the window shifted past the first step still covers the second
+                uint32_t win = __funnelshift_r(lo, hi, p);
+                uint32_t e2[2];
+                bool inc = false;
+#pragma unroll
+                for (uint32_t h = 0; h < 2; h++) {
+                    const uint32_t e = S.lut[win & ((1u << RWIN) - 1u)];
+                    inc |= e < (1u << 28);
+                    e2[h] = e;
+                    win >>= e >> 28;
+                }
+                if (inc) {
+                    // a window with fewer than four complete codes: each step again
+                    // from its true start, the table's complete codes first, then
+                    // the others one by one (find-first-set; long runs word by word)
+#pragma unroll 1
+                    for (uint32_t h = 0; h < 2; h++) {
+                        uint32_t e = e2[0];
+                        if (h) {
+                            const uint32_t xi = p >> 5;
+                            e = S.lut[__funnelshift_r(buf[xi], buf[xi + 1], p) & ((1u << RWIN) - 1u)];
+                        }
+                        if (e >= (1u << 28)) {
+                            p += e >> 28;
+                        } else {
+                            uint32_t f = e & (0xFFFFu | R4_ESCF);
+                            p += (e >> 20) & 15u;
+                            for (uint32_t c = (e >> 17) & 7u; c < 4; c++) {
+                                uint32_t qq = 0;
+                                for (;;) {
+                                    const uint32_t xi = p >> 5;
+                                    const uint32_t x = __funnelshift_r(buf[xi], buf[xi + 1], p);
+                                    if (x) {
+                                        const uint32_t z = __ffs(x) - 1;
+                                        qq += z;
+                                        p += z + 1;
+                                        break;
+                                    }
+                                    qq += 32;
+                                    p += 32;
+                                    if (qq > 255 || p > 32u * RCAP) break;
+                                }
+                                if (qq > 255 || p > 32u * RCAP) {
+                                    badw = 1;
+                                    p = 32u * RCAP;   // keeps every later buffer index in range
+                                }
+                                const uint32_t fq = min(qq << KK, 15u);
+                                f |= fq << (4 * c);
+                                if (fq >= THR) f |= R4_ESCF;
+                            }
+                            e = f;
+                        }
+                        e2[h] = e;
+                    }
+                    wi = p >> 5;
+                    lo = buf[wi];
+                    hi = buf[wi + 1];
+                } else {
+                    p += (e2[0] >> 28) + (e2[1] >> 28);
+                    if ((p >> 5) != wi) {
+                        lo = hi;
+                        wi++;
+                        hi = buf[wi + 1];
+                    }
+                }
+                uint32_t x = __byte_perm(e2[0], e2[1], 0x5410u);
+                if (KK == 1) x |= (fw[m >> 2] >> (m & 3)) & 0x11111111u;
+                if (KK == 2) x |= (fw[m >> 1] >> (2 * (m & 1))) & 0x33333333u;
+                out[m] = x;
+                if ((e2[0] | e2[1]) & R4_ESCF) {
+                    S.rec[w][nrec][lane] = pws << 3 | m;
+                    S.recf[w][nrec][lane] = __byte_perm(e2[0], e2[1], 0x5410u);
+                    nrec++;
+                }
+            }
+            if (p != end || badw) bad = true;
             uint4 *dst = reinterpret_cast<uint4 *>(a.nib + B0 / 2);
             dst[0] = make_uint4(out[0], out[1], out[2], out[3]);
             dst[1] = make_uint4(out[4], out[5], out[6], out[7]);
+            // flagged words: the exact rank of every field that may be an escape.
+            // Code j of a word starts j + (sum of the earlier codes' quotients)
+            // bits after the word's start; a field below the threshold is its
+            // quotient << k exactly, a candidate's quotient is read from the stream.
+            if (nrec) {
+                const WordReader<const uint32_t *> rd{buf, RBUF};
+                for (uint32_t i = 0; i < nrec; i++) {
+                    const uint32_t rv = S.rec[w][i][lane];
+                    const uint32_t ws = rv >> 3, mm = rv & 7u;
+                    const uint32_t xw = mm < 4 ? (mm < 2 ? (mm == 0 ? out[0] : out[1]) : (mm == 2 ? out[2] : out[3]))
+                                               : (mm < 6 ? (mm == 4 ? out[4] : out[5]) : (mm == 6 ? out[6] : out[7]));
+                    // remainders from the field words (a saturated field reads 15 in
+                    // the nibble whatever its remainder)
+                    const uint32_t remw = KK == 1 ? ((mm >= 4 ? fw[1] : fw[0]) >> (mm & 3)) & 0x11111111u
+                                        : KK == 2 ? ((mm >= 4 ? (mm >= 6 ? fw[3] : fw[2]) : (mm >= 2 ? fw[1] : fw[0])) >>
+                                                     (2 * (mm & 1))) & 0x33333333u
+                                                  : 0u;
+                    // escapes are the nibbles 15.  One whose field is below 15 is
+                    // exactly rank 15; a saturated field (15) is always an escape,
+                    // and its quotient is read from the stream: its code starts j +
+                    // (sum of the earlier quotients) bits after the word's start,
+                    // where a field below 15 is its quotient << k exactly
+                    const uint32_t F = S.recf[w][i][lane];
+                    const uint32_t sat = nib15_mask(F);
+                    uint32_t cand = nib15_mask(xw);
+                    uint32_t fix = 0;   // saturated fields so far: exact quotient minus 15 >> k
+                    while (cand) {
+                        const uint32_t j = (__ffs(cand) - 1) >> 2;
+                        cand &= cand - 1;
+                        uint32_t r = 15;
+                        if ((sat >> (4 * j)) & 1u) {
+                            const uint32_t y = (F >> KK) & ((0xFu >> KK) * 0x11111111u) & ((1u << (4 * j)) - 1u);
+                            const uint32_t before = __popc(y & 0x11111111u) + 2u * __popc(y & 0x22222222u) +
+                                                    4u * __popc(y & 0x44444444u) + 8u * __popc(y & 0x88888888u);
+                            uint32_t pp = ws + j + before + fix;
+                            const uint32_t qq = unary_at(rd, pp, bad);
+                            r = (qq << KK) | ((remw >> (4 * j)) & ((1u << KK) - 1u));
+                            fix += qq - (15u >> KK);
+                        }
+                        if (ec < RESC) S.escl[w][ec][lane] = (uint8_t)min(r, 255u);
+                        if (r > 255 || r < 15) bad = true;
+                        ec++;
+                    }
+                }
+            }
+            if (!FAST && ec) {
+                for (int mm = 0; mm < 8; mm++) {
+                    const uint32_t msk = nib15_mask(out[mm]);
+                    for (int j = 0; j < 8; j++)
+                        if ((msk >> (4 * j)) & 1u) emask |= 1ull << (8 * mm + j);
+                }
+            }
         } else if (cnt) {
-            uint32_t p;
-            if (staged)
-                p = rice_block_slow(WordReader<const uint32_t *>{buf, RBUF}, off + boff, cnt, q == 255, k,
-                                    a.nib + B0 / 2, le);
-            else
-                p = rice_block_slow(WordReader<const uint32_t *>{a.words + gw0, nw}, off, cnt, q == 255, k,
-                                    a.nib + B0 / 2, le);
-            if (p != end) bad = true;
+            const SlowBlock o = staged
+                ? rice_block_slow(WordReader<const uint32_t *>{buf, RBUF}, b0, cnt, raw, k, a.nib + B0 / 2)
+                : rice_block_slow(WordReader<const uint32_t *>{a.words + gw0, nw}, b0, cnt, raw, k, a.nib + B0 / 2);
+            ec = o.ec;
+            emask = o.emask;
+            if (o.bad || o.end != end) bad = true;
         }
-        const uint32_t ec = le->ec;
-        const uint64_t emask = le->emask;
-        if (le->bad) bad = true;
         // escapes, placed by a warp prefix sum from the group's escape base
         uint32_t etot;
         const uint32_t eb = warp_excl_scan(ec, &etot);
         if (gbase + etot != next_e || next_e > a.n_esc) bad = true;
         if (ec && !bad) {
             uint8_t *dst = a.esc + gbase + eb;
-            if (ec <= RLIST) {
-                for (uint32_t i = 0; i < ec; i++) dst[i] = le->list[i];
+            if (fast && ec <= RESC) {
+                for (uint32_t i = 0; i < ec; i++) dst[i] = S.escl[w][i][lane];
             } else if (staged) {
-                rice_block_escapes(WordReader<const uint32_t *>{buf, RBUF}, off + boff, cnt, q == 255, k, dst);
+                rice_block_slow_escapes(WordReader<const uint32_t *>{buf, RBUF}, b0, cnt, raw, k, dst);
             } else {
-                rice_block_escapes(WordReader<const uint32_t *>{a.words + gw0, nw}, off, cnt, q == 255, k, dst);
+                rice_block_slow_escapes(WordReader<const uint32_t *>{a.words + gw0, nw}, b0, cnt, raw, k, dst);
             }
         }
         // row-segment escape index for every segment that starts in this block
@@ -1040,13 +1158,21 @@ extern "C" int dgt_load_r4(const dgt_packed_view *dev, dgt_r4 *r4, int32_t *d_st
         const size_t smem = sizeof(RiceSmem);
         const bool fast = n < (1ull << 31) && dev->cols % 64 == 0 && dev->cols >= 2048 &&
                           dev->rows * nseg < (1ull << 32) && aligned16(dev->words) && dev->n_words < (1ull << 32);
-        const void *fn = fast ? (const void *)k_rice_to_r4<true> : (const void *)k_rice_to_r4<false>;
+        void (*fn)(F2Args) = nullptr;
+        switch ((fast ? 4 : 0) + (a.k < 3 ? a.k : 3)) {
+            case 0: fn = k_rice_to_r4<false, 0>; break;
+            case 1: fn = k_rice_to_r4<false, 1>; break;
+            case 2: fn = k_rice_to_r4<false, 2>; break;
+            case 3: fn = k_rice_to_r4<false, 3>; break;
+            case 4: fn = k_rice_to_r4<true, 0>; break;
+            case 5: fn = k_rice_to_r4<true, 1>; break;
+            case 6: fn = k_rice_to_r4<true, 2>; break;
+            default: fn = k_rice_to_r4<true, 3>; break;
+        }
         int bps = 0;
-        if (prepare_kernel(fn, smem, RW * 32, &bps) != DGT_OK) return DGT_ERR_CUDA;
+        if (prepare_kernel((const void *)fn, smem, RW * 32, &bps) != DGT_OK) return DGT_ERR_CUDA;
         uint64_t grid = min((uint64_t)di.sms * bps, (a.ngrp + RW - 1) / RW);
-        const cudaError_t e = fast ? launch_pdl(k_rice_to_r4<true>, dim3((unsigned)grid), dim3(RW * 32), smem, st, a)
-                                   : launch_pdl(k_rice_to_r4<false>, dim3((unsigned)grid), dim3(RW * 32), smem, st, a);
-        if (e != cudaSuccess) return DGT_ERR_CUDA;
+        if (launch_pdl(fn, dim3((unsigned)grid), dim3(RW * 32), smem, st, a) != cudaSuccess) return DGT_ERR_CUDA;
     } else {
         if (!dev->tw || !dev->tesc || !dev->grp1 || (dev->payload_bytes && !dev->payload) ||
             (dev->n_esc1 && !dev->esc1) || (dev->payload && !aligned16(dev->payload)))
