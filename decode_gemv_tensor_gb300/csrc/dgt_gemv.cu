@@ -257,6 +257,9 @@ __global__ void __launch_bounds__(PW * 32, 1) k_gemv(GemvArgs a) {
 #ifndef DGT_GEMV_NS_R4
 #define DGT_GEMV_NS_R4 4
 #endif
+#ifndef DGT_GEMV_C_R4
+#define DGT_GEMV_C_R4 4   // rounds per R4 piece (at most 13: the summary slot holds C + 6 words)
+#endif
 #ifndef DGT_GEMV_NS_BF16
 #define DGT_GEMV_NS_BF16 5
 #endif
@@ -277,14 +280,15 @@ constexpr uint32_t TCHUNK = DGT_GEMV_TCHUNK;  // (row, slice) units per combine 
 // across chunks, and a chunk holds whole rows for every slice count (S <= 8)
 static_assert(TCHUNK % TNW == 0 && TCHUNK % 8 == 0, "chunk size");
 static_assert(TNW <= 32 * TPW, "one producer lane per consumer warp");
+static_assert(DGT_GEMV_C_R4 >= 1 && DGT_GEMV_C_R4 <= 13, "R4 piece rounds");
 
 template <bool R4>
 struct TmaCfg;
 template <>
 struct TmaCfg<true> {
-    static constexpr uint32_t C = 4;               // rounds per piece
+    static constexpr uint32_t C = DGT_GEMV_C_R4;   // rounds per piece
     static constexpr uint32_t NS = DGT_GEMV_NS_R4; // stages per warp
-    static constexpr uint32_t STAGE = 4 * 768 + 64; // sm bytes, nibbles, then round summaries
+    static constexpr uint32_t STAGE = C * 768 + 64; // sm bytes, nibbles, then round summaries
 };
 template <>
 struct TmaCfg<false> {
