@@ -56,7 +56,7 @@ class R4Struct(C.Structure):
 
 
 class GemmPlan(C.Structure):
-    _fields_ = [("m_tile", C.c_int32), ("split_k", C.c_int32), ("test_flags", C.c_uint32), ("reserved1", C.c_int32)]
+    _fields_ = [("m_tile", C.c_int32), ("split_k", C.c_int32), ("test_flags", C.c_uint32), ("schedule", C.c_int32)]
 
 
 _lib = None
@@ -496,15 +496,18 @@ def moe_gemm_bf16(W, n_experts: int, ids, p, X, ws=None, y32=None, out=None, out
     return y32, out, out32
 
 
-def gemm_plan(M: int, N: int, K: int, m_tile=None, split_k=None, test_wait_polls=None) -> GemmPlan:
-    """dgt_gemm_default_plan, optionally overridden (test_wait_polls: the
-    failure-path test hook, see test_wait_flags)."""
+def gemm_plan(M: int, N: int, K: int, m_tile=None, split_k=None, test_wait_polls=None, schedule=None) -> GemmPlan:
+    """dgt_gemm_default_plan, optionally overridden (schedule: 0 auto, 1 one
+    CTA per tile, 2 persistent; test_wait_polls: the failure-path test hook,
+    see test_wait_flags)."""
     p = GemmPlan()
     _check(lib().dgt_gemm_default_plan(M, N, K, C.byref(p)), "dgt_gemm_default_plan")
     if m_tile is not None:
         p.m_tile = m_tile
     if split_k is not None:
         p.split_k = split_k
+    if schedule is not None:
+        p.schedule = schedule
     p.test_flags = test_wait_flags(test_wait_polls)
     return p
 

@@ -62,6 +62,7 @@ struct GemmArgs {
     uint64_t ne;
     uint32_t grouped, topk;
     uint32_t spin;   // polls a wait for work in flight takes before it gives up
+    uint32_t schedule;   // 0 auto, 1 one CTA per tile, 2 persistent (split_k = 1)
 };
 
 // ---- tcgen05 / TMA wrappers -------------------------------------------------
@@ -447,6 +448,231 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
     if (warp == 1) tmem_dealloc(taddr, ncols);
 }
 
+// ---- persistent schedule: one CTA per SM --------------------------------------
+// One CTA per SM walks the output tiles b, b + G, b + 2G, ... (G = grid size)
+// with two accumulators in tensor memory: the MMA warp fills accumulator
+// i & 1 for the CTA's i-th tile while the epilogue warps drain the other, so
+// a tile's epilogue runs under the next tile's loads and MMAs.  The TMA
+// producer, the MMA warp and (R4) the decoder warps walk one continuous
+// sequence of pipeline stages across the tiles.  Each tile issues the same
+// MMA sequence as k_gemm with split_k = 1, so the outputs are bit-identical
+// to it.  Warps: 0 TMA, 1 MMA (and the tensor-memory allocation), 4..7 the
+// epilogue (warp 4 + w reads accumulator lanes 32w..32w + 31), 8..23 the R4
+// decoders (four threads per W row, as in k_gemm).
+constexpr uint32_t PT_WARPS_R4 = 24, PT_WARPS_BF16 = 8;
+
+template <bool R4>
+__global__ void __launch_bounds__((R4 ? PT_WARPS_R4 : PT_WARPS_BF16) * 32, 1)
+    k_gemm_pt(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
+              const __grid_constant__ CUtensorMap tm_nib, GemmArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t bar_full[GT_MAXP], bar_raw[GT_MAXP], bar_w[GT_MAXP], bar_empty[GT_MAXP];
+    __shared__ __align__(8) uint64_t acc_full[2], acc_empty[2], bar_done;
+    __shared__ uint32_t tmem_slot;
+    __shared__ uint8_t table_s[256];
+    __shared__ int abort_flag;
+    uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    const uint32_t tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t mt = a.mt, P = a.stages;
+    const uint32_t SB = gemm_stage_bytes(R4, mt);
+    const uint32_t ncols = mt <= 32 ? 32 : (mt <= 64 ? 64 : (mt <= 128 ? 128 : 256));   // per accumulator
+    const uint32_t NT = (uint32_t)(a.N / GT_N), MTL = (uint32_t)((a.M + mt - 1) / mt), tiles = NT * MTL;
+    const uint32_t nkb = a.kb_total;
+    const uint32_t my_tiles = blockIdx.x < tiles ? (tiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+    auto A = [&](uint32_t s) { return base + (size_t)s * SB; };
+    auto B = [&](uint32_t s) { return base + (size_t)s * SB + GT_N * 128; };
+    auto RS = [&](uint32_t s) { return base + (size_t)s * SB + GT_N * 128 + mt * 128; };
+    auto RN = [&](uint32_t s) { return base + (size_t)s * SB + GT_N * 128 + mt * 128 + GT_N * 64; };
+    auto tile_of = [&](uint32_t i, uint32_t &n0, uint32_t &m0) {
+        const uint32_t t = blockIdx.x + i * gridDim.x;
+        n0 = (t % NT) * GT_N;
+        m0 = (t / NT) * mt;
+    };
+
+    if (tid == 0) {
+        for (uint32_t i = 0; i < P; i++) {
+            mbar_init(smem_u32(&bar_full[i]), 1);
+            mbar_init(smem_u32(&bar_raw[i]), 1);
+            mbar_init(smem_u32(&bar_w[i]), 16);
+            mbar_init(smem_u32(&bar_empty[i]), 1);
+        }
+        for (int i = 0; i < 2; i++) {
+            mbar_init(smem_u32(&acc_full[i]), 1);
+            mbar_init(smem_u32(&acc_empty[i]), 4);
+        }
+        mbar_init(smem_u32(&bar_done), 1);
+        abort_flag = 0;
+        fence_mbarrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&tmem_slot), 2 * ncols);
+        tmem_relinquish();
+    }
+    if (tid < 256) table_s[tid] = a.table[tid];
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    pdl_trigger();
+    pdl_wait();
+    const uint32_t taddr = tmem_slot;
+    volatile int *abortp = &abort_flag;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---- TMA producer
+            uint32_t g = 0;
+            bool stop = false;
+            for (uint32_t i = 0; i < my_tiles && !stop; i++) {
+                uint32_t n0, m0;
+                tile_of(i, n0, m0);
+                for (uint32_t kb = 0; kb < nkb; kb++) {
+                    const uint32_t s = g % P, use = g / P;
+                    if (use > 0 && !wait_or_abort(smem_u32(&bar_empty[s]), (use - 1) & 1u, abortp, a.spin)) {
+                        set_status(a.status, DGT_ERR_TIMEOUT);
+                        *abortp = 1;
+                        stop = true;
+                        break;
+                    }
+                    const int32_t k = (int32_t)(kb * GT_K);
+                    mbar_arrive_expect_tx(smem_u32(&bar_full[s]), mt * 128 + (R4 ? 0 : GT_N * 128));
+                    tma_load_2d(smem_u32(B(s)), &tm_x, smem_u32(&bar_full[s]), k, (int32_t)m0);
+                    if (!R4) {
+                        tma_load_2d(smem_u32(A(s)), &tm_w, smem_u32(&bar_full[s]), k, (int32_t)n0);
+                    } else {
+                        mbar_arrive_expect_tx(smem_u32(&bar_raw[s]), GT_N * 64 + GT_N * 32);
+                        tma_load_2d(smem_u32(RS(s)), &tm_w, smem_u32(&bar_raw[s]), k, (int32_t)n0);
+                        tma_load_2d(smem_u32(RN(s)), &tm_nib, smem_u32(&bar_raw[s]), k / 2, (int32_t)n0);
+                    }
+                    g++;
+                }
+            }
+            // let every copy issued land before the CTA can exit
+            for (uint32_t j = g > P ? g - P : 0; j < g; j++) {
+                const uint32_t s = j % P, par = (j / P) & 1u;
+                wait_or_abort(smem_u32(&bar_full[s]), par, abortp, a.spin) || mbar_wait(smem_u32(&bar_full[s]), par);
+                if (R4) wait_or_abort(smem_u32(&bar_raw[s]), par, abortp, a.spin) || mbar_wait(smem_u32(&bar_raw[s]), par);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---- MMA issuer
+            const uint32_t idesc = idesc_bf16(mt);
+            uint32_t g = 0;
+            bool stop = false;
+            for (uint32_t i = 0; i < my_tiles && !stop; i++) {
+                const uint32_t ab = i & 1u;
+                // the epilogue has drained this accumulator (its tile i - 2)
+                if (i >= 2 && !wait_or_abort(smem_u32(&acc_empty[ab]), ((i >> 1) - 1) & 1u, abortp, a.spin)) {
+                    set_status(a.status, DGT_ERR_TIMEOUT);
+                    *abortp = 1;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d = taddr + ab * ncols;
+                for (uint32_t kb = 0; kb < nkb; kb++, g++) {
+                    const uint32_t s = g % P, par = (g / P) & 1u;
+                    if (!wait_or_abort(smem_u32(&bar_full[s]), par, abortp, a.spin) ||
+                        (R4 && !wait_or_abort(smem_u32(&bar_w[s]), par, abortp, a.spin))) {
+                        set_status(a.status, DGT_ERR_TIMEOUT);
+                        *abortp = 1;
+                        stop = true;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t ad = sw128_desc(smem_u32(A(s))), bd = sw128_desc(smem_u32(B(s)));
+#pragma unroll
+                    for (uint32_t kk = 0; kk < GT_K / 16; kk++)
+                        mma_bf16(d, ad + 2 * kk, bd + 2 * kk, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+                    mma_commit(smem_u32(&bar_empty[s]));
+                }
+                if (!stop) mma_commit(smem_u32(&acc_full[ab]));
+            }
+            mma_commit(smem_u32(&bar_done));
+        }
+    } else if (warp >= 4 && warp < 8) {
+        // ---- epilogue: thread t holds accumulator row t (W row n0 + t)
+        const uint32_t t = tid - 128;
+        const uint32_t lane_base = ((warp - 4) * 32) << 16;
+        for (uint32_t i = 0; i < my_tiles; i++) {
+            const uint32_t ab = i & 1u;
+            const bool ok = wait_or_abort(smem_u32(&acc_full[ab]), (i >> 1) & 1u, abortp, a.spin);
+            tc_fence_after();
+            if (!ok) {
+                if (lane == 0) set_status(a.status, DGT_ERR_TIMEOUT);
+                *abortp = 1;
+                break;
+            }
+            uint32_t n0, m0;
+            tile_of(i, n0, m0);
+            const uint64_t n = n0 + t;
+            for (uint32_t c = 0; c < mt; c += 16) {
+                uint32_t r[16];
+                tmem_ld16(taddr + lane_base + ab * ncols + c, r);
+                tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 16; j++) {
+                    const uint64_t m = (uint64_t)m0 + c + j;
+                    if (m < a.M) {
+                        const float v = __uint_as_float(r[j]);
+                        if (a.y32) a.y32[m * a.N + n] = v;
+                        if (a.y) a.y[m * a.N + n] = f32_to_bf16_rne(v);
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&acc_empty[ab]));
+        }
+    } else if (R4 && warp >= 8) {
+        // ---- decoders: thread (t, q) owns chunk q of W row n0 + t of every tile
+        const uint32_t dd = tid - 256, t = dd >> 2, q = dd & 3;
+        R4Lut L;
+        L.h0 = a.L.h0;
+        L.h1 = a.L.h1;
+        L.h2 = a.L.h2;
+        L.h3 = a.L.h3;
+        L.l0 = a.L.l0;
+        L.l1 = a.L.l1;
+        const uint32_t base_a = smem_u32(base);
+        uint32_t g = 0;
+        bool bad = false, stop = false;
+        for (uint32_t i = 0; i < my_tiles && !stop; i++) {
+            uint32_t n0, m0;
+            tile_of(i, n0, m0);
+            const uint64_t row = (uint64_t)n0 + t;
+            uint64_t eidx = a.seg[row * a.nseg];
+            uint32_t r0 = eidx < a.n_esc ? a.esc[eidx] : 0u;
+            uint32_t r1 = eidx + 1 < a.n_esc ? a.esc[eidx + 1] : 0u;
+            for (uint32_t kb = 0; kb < nkb; kb++, g++) {
+                const uint32_t s = g % P, par = (g / P) & 1u;
+                if (!wait_or_abort(smem_u32(&bar_raw[s]), par, abortp, a.spin)) {
+                    if (lane == 0) set_status(a.status, DGT_ERR_TIMEOUT);
+                    *abortp = 1;
+                    stop = true;
+                    break;
+                }
+                const uint32_t st0 = base_a + s * SB;
+                decode_chunk16(a, L, st0 + GT_N * 128 + mt * 128 + t * 64,
+                               st0 + GT_N * 128 + mt * 128 + GT_N * 64 + t * 32, st0 + t * 128, t, q, eidx, r0, r1,
+                               table_s, bad);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&bar_w[s]));
+            }
+        }
+        if (bad) set_status(a.status, DGT_ERR_CORRUPT);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) {
+        // every MMA this CTA issued has completed before its tensor memory goes
+        wait_or_abort(smem_u32(&bar_done), 0, abortp, a.spin) || mbar_wait(smem_u32(&bar_done), 0);
+        tc_fence_after();
+        tmem_dealloc(taddr, 2 * ncols);
+    }
+}
+
 __global__ void __launch_bounds__(256) k_gemm_reduce(GemmArgs a) {
     pdl_trigger();
     pdl_wait();
@@ -516,13 +742,23 @@ static int launch_gemm(GemmArgs &a, const void *w_or_sm, const uint16_t *d_X, vo
     }
     const size_t smem = (size_t)a.stages * gemm_stage_bytes(R4, a.mt) + 1024;
     int bps = 0;
+    DeviceInfo di;
+    if (device_info(&di) != DGT_OK) return DGT_ERR_CUDA;
+    const uint64_t tiles = (a.N / GT_N) * ((a.M + a.mt - 1) / a.mt);
+    const bool persistent = a.split == 1 && (a.schedule == 2 || (a.schedule == 0 && tiles > (uint64_t)di.sms));
+    if (persistent) {
+        const uint32_t threads = (R4 ? PT_WARPS_R4 : PT_WARPS_BF16) * 32;
+        if (prepare_kernel((const void *)k_gemm_pt<R4>, smem, threads, &bps) != DGT_OK) return DGT_ERR_CUDA;
+        const unsigned grid = (unsigned)min(tiles, (uint64_t)di.sms);
+        if (launch_pdl(k_gemm_pt<R4>, dim3(grid), dim3(threads), smem, st, tm_x, tm_w, tm_nib, a) != cudaSuccess)
+            return DGT_ERR_CUDA;
+        return cudaPeekAtLastError() == cudaSuccess ? DGT_OK : DGT_ERR_CUDA;
+    }
     if (prepare_kernel((const void *)k_gemm<R4>, smem, GT_THREADS, &bps) != DGT_OK) return DGT_ERR_CUDA;
     dim3 grid((unsigned)(a.N / GT_N), (unsigned)((a.M + a.mt - 1) / a.mt), a.split);
     if (launch_pdl(k_gemm<R4>, grid, dim3(GT_THREADS), smem, st, tm_x, tm_w, tm_nib, a) != cudaSuccess)
         return DGT_ERR_CUDA;
     if (a.split > 1) {
-        DeviceInfo di;
-        if (device_info(&di) != DGT_OK) return DGT_ERR_CUDA;
         const uint64_t total = a.M * a.N;
         uint64_t g = (total + 255) / 256;
         if (g > (uint64_t)di.sms * 8) g = (uint64_t)di.sms * 8;
@@ -545,6 +781,8 @@ static int fill_common(GemmArgs &a, uint64_t M, uint64_t N, uint64_t K, const dg
         (!(p.test_flags & DGT_TEST_SHORT_WAITS) && (p.test_flags >> 16)))
         return DGT_ERR_ARG;
     a.spin = wait_limit_from_flags(p.test_flags);
+    if (p.schedule < 0 || p.schedule > 2 || (p.schedule == 2 && p.split_k != 1)) return DGT_ERR_ARG;
+    a.schedule = (uint32_t)p.schedule;
     a.M = M;
     a.N = N;
     a.K = K;
@@ -930,7 +1168,7 @@ extern "C" int dgt_gemm_default_plan(uint64_t M, uint64_t N, uint64_t K, dgt_gem
     plan->m_tile = (int32_t)mt;
     plan->split_k = (int32_t)split;
     plan->test_flags = 0;
-    plan->reserved1 = 0;
+    plan->schedule = 0;
     return DGT_OK;
 }
 

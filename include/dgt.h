@@ -371,7 +371,7 @@ int dgt_moe_gemv_bf16(const uint16_t *d_W, uint64_t rows, uint64_t cols, uint32_
  * byte-identical tiles, so their outputs are bit-identical.
  * dgt_gemm_default_plan: m_tile = round_up(M, 16) up to 256; split_k =
  * floor(152 / tiles) (one wave of one CTA per SM; 1 when tiles >= 152), at
- * most K/256 and 16.
+ * most K/256 and 16; schedule 0 (auto).
  * d_X: device bf16 [M, K].  d_Y32 / d_Y: device float / bf16 [M, N] (either
  * may be NULL).  d_ws: device workspace of dgt_gemm_workspace_bytes() bytes
  * (split partials; NULL when split_k == 1).  Limits: N % 128 == 0,
@@ -383,8 +383,19 @@ typedef struct dgt_gemm_plan {
     int32_t m_tile;
     int32_t split_k;
     uint32_t test_flags;   /* 0, or DGT_TEST_SHORT_WAITS | DGT_TEST_WAIT_POLLS(n) */
-    int32_t reserved1;
+    int32_t schedule;      /* 0 auto, 1 one CTA per output tile, 2 persistent (see below) */
 } dgt_gemm_plan;
+
+/*
+ * Schedules (the plan's arithmetic is the same under each, so the outputs are
+ * bit-identical whichever runs).  One CTA per output tile (x split_k) is the
+ * first.  The persistent schedule (split_k = 1 only) runs one CTA per SM that
+ * walks the tiles b, b + G, ... with two accumulators in tensor memory: the
+ * MMAs of a tile fill one while the epilogue drains the other, so a tile's
+ * stores run under the next tile's loads and MMAs.  Auto (0) takes the
+ * persistent schedule when split_k = 1 and there are more tiles than SMs.
+ * schedule = 2 with split_k > 1, or a value outside 0..2: DGT_ERR_ARG.
+ */
 
 int dgt_gemm_default_plan(uint64_t M, uint64_t N, uint64_t K, dgt_gemm_plan *plan);
 size_t dgt_gemm_workspace_bytes(uint64_t M, uint64_t N, const dgt_gemm_plan *plan);

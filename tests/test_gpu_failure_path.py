@@ -86,16 +86,19 @@ def test_moe_wait_runs_out_then_recovers(dgt):
     assert np.array_equal(_u32(out32), rout.view(np.uint32))
 
 
-@pytest.mark.parametrize("M,split", [(16, 1), (16, 4), (128, 2)])
-def test_gemm_wait_runs_out_then_recovers(dgt, M, split):
+@pytest.mark.parametrize("M,split,sched", [(16, 1, 1), (16, 4, 1), (128, 2, 1), (128, 1, 2), (1024, 1, 2)])
+def test_gemm_wait_runs_out_then_recovers(dgt, M, split, sched):
+    # one CTA per tile with and without split-K, and the persistent schedule
+    # (two accumulators in tensor memory, several tiles per CTA at 1024 rows)
     N = K = 1024
     W = S.weights(N, K, (703, 0, 0, 0), outliers=True)
     X = S.activations(K, (703, 999, M), count=M)
     r4 = dgt.load_r4(dgt.upload(dgt.pack(W, 2)))
     wd, xd = _dev_bf16(W), _dev_bf16(X)
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
-    short = dgt.gemm_plan(M, N, K, split_k=split, test_wait_polls=0)
-    plan = dgt.gemm_plan(M, N, K, split_k=split)
+    mt = 64 if M == 1024 else None
+    short = dgt.gemm_plan(M, N, K, m_tile=mt, split_k=split, test_wait_polls=0, schedule=sched)
+    plan = dgt.gemm_plan(M, N, K, m_tile=mt, split_k=split, schedule=sched)
     dgt.gemm(r4, xd, plan=short, status=st)
     torch.cuda.synchronize()
     assert dgt.read_status(st) == TIMEOUT

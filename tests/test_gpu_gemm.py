@@ -114,3 +114,36 @@ def test_gemm_rebuild_is_the_bf16_gemm(dgt, M, N, K, split):
     assert dgt.read_status(st) == 0
     assert torch.equal(r32.view(torch.int32), y32.view(torch.int32))
     assert torch.equal(r16.view(torch.int16), b16.view(torch.int16))
+
+
+@pytest.mark.parametrize("M,N,K,mt", [(300, 256, 1024, 256), (2048, 4096, 3840, 256), (1000, 2048, 512, 64),
+                                      (512, 15360, 256, 128), (64, 19200, 128, 16)])
+def test_gemm_persistent_schedule_equals_one_cta_per_tile(dgt, M, N, K, mt):
+    # the persistent schedule (one CTA per SM walking the tiles, two
+    # accumulators in tensor memory) issues each tile's MMAs in the same
+    # order: R4 and BF16 under both schedules give the same bits; from 4 tiles
+    # to about 4 tiles per CTA, ragged M, the smallest tile width
+    W = S.weights(N, K, (503, N, K), outliers=True)
+    X = S.activations(K, (503, 999, M), count=M).reshape(M, K)
+    one = dgt.gemm_plan(M, N, K, m_tile=mt, split_k=1, schedule=1)
+    per = dgt.gemm_plan(M, N, K, m_tile=mt, split_k=1, schedule=2)
+    y1, h1, b1, c1 = _both(dgt, W, X, plan=one)
+    y2, h2, b2, c2 = _both(dgt, W, X, plan=per)
+    for t in (b1, y2, b2):
+        assert torch.equal(t.view(torch.int32), y1.view(torch.int32))
+    for t in (c1, h2, c2):
+        assert torch.equal(t.view(torch.int16), h1.view(torch.int16))
+    cols = np.sort(np.random.default_rng(M + N).choice(N, min(N, 96), replace=False))
+    rows = np.sort(np.random.default_rng(M).choice(M, min(M, 64), replace=False))
+    ref = oracle.gemm_f64(X[rows], W, cols=cols)
+    assert _normwise(y2.cpu().numpy()[np.ix_(rows, cols)], ref) <= 1e-3
+
+
+def test_gemm_schedule_arguments(dgt):
+    N = K = 256
+    r4 = dgt.load_r4(dgt.upload(dgt.pack(S.weights(N, K, (504, 0, 0, 0)), 2)))
+    X = _dev_bf16(S.activations(K, (504, 999, 0), count=16).reshape(16, K))
+    for bad in (dgt.gemm_plan(16, N, K, split_k=2, schedule=2), dgt.gemm_plan(16, N, K, schedule=3),
+                dgt.gemm_plan(16, N, K, schedule=-1)):
+        with pytest.raises(dgt.DgtError):
+            dgt.gemm(r4, X, plan=bad)
