@@ -242,10 +242,9 @@ __global__ void __launch_bounds__(PW * 32, 1) k_gemv(GemvArgs a) {
 // per-round tests except the warp-uniform escape bit.  An R4 round whose
 // segment holds one escape decodes with the rank-15 entry of the exponent
 // table replaced by that escape's exponent (only the escaped weight has
-// nibble 15); two escapes in different lanes do the same per lane; other
-// cases go out of line.  The row-segment escape counts of the next unit and
-// the exponents of their first two escapes are fetched while the current unit
-// runs.  Every wait is bounded: one that runs out sets the status word, and
+// nibble 15); two or three escapes do the same per lane, a lane holding two
+// of them rewriting its second escaped weight's exponent; other cases take a
+// general patch from the escape list.  Every wait is bounded: one that runs out sets the status word, and
 // the warp stops, lets its copies in flight land and exits.
 // ---------------------------------------------------------------------------
 #ifndef DGT_GEMV_INTERLEAVE
@@ -485,51 +484,46 @@ __global__ void __launch_bounds__((TNW + TPW) * 32, 1) k_gemv_tma(GemvArgs a) {
                     rl = round_luts_rec(rec, L);
                 }
                 const uint32_t pm = rl.multi;
-                // an R4 piece of fewer than C rounds (a short unit's last piece)
-                // and the row's last round cut by K (round rp: its lanes past K
-                // add +0) stay on the fast loops; short BF16 pieces go to the
-                // slow loop
+                // BF16 pieces of fewer than C rounds take the general loop
                 bool slow = !R4 && n != C;
-                // rounds with two or more escapes: per-lane rank-15 entries, worked
-                // out before the multiply-adds; anything else takes the slow loop
-                uint32_t mh3[C], ml1[C];
-                if (R4 && ok && pm && !slow) {
+                // rounds with two or three escapes: per-lane rank-15 entries (and,
+                // for a lane holding two, its second escaped weight), worked out
+                // before the multiply-adds; a round where that fails takes the
+                // general patch from the escape list
+                uint32_t mh3[C], ml1[C], mi2[C], me2[C];
+                uint32_t pm2 = 0, pmok = 0;   // rounds with a second patch; rounds worked out
+                if (R4 && ok && pm) {
 #pragma unroll
-                    for (uint32_t r = 0; r < C; r++) mh3[r] = ml1[r] = 0;
+                    for (uint32_t r = 0; r < C; r++) mh3[r] = ml1[r] = 0, mi2[r] = 16, me2[r] = 0;
 #pragma unroll
                     for (uint32_t r = 0; r < C; r++) {
                         if ((pm >> r) & 1u) {
                             uint2 nv = *reinterpret_cast<const uint2 *>(stg + C * 512 + r * 256 + 8 * lane);
                             if (r == rp && !act) nv = make_uint2(0, 0);   // bytes past K are not this row's
-                            uint32_t e;
-                            if (rec_exponent(__shfl_sync(DGT_FULL, rec, r), nv, lane, e)) {
+                            uint32_t e, e2, i2;
+                            if (rec_exponent2(__shfl_sync(DGT_FULL, rec, r), nv, lane, e, e2, i2)) {
                                 const R4Lut t = lut15(L, e);
                                 mh3[r] = t.h3;
                                 ml1[r] = t.l1;
+                                mi2[r] = i2;
+                                me2[r] = e2;
+                                pmok |= 1u << r;
+                                if (__any_sync(DGT_FULL, i2 < 16)) pm2 |= 1u << r;
                             } else {
                                 slow = true;
                             }
                         }
                     }
                 }
-                // one round of the common piece: decode with its shuffled table words
-                // the cut round: lanes past K multiply +0 weights (x there is 0 too)
-                auto cut_mask = [&](uint32_t r, uint32_t p[8]) {
-                    if (r == rp) {
-                        const uint32_t m = act ? 0xFFFFFFFFu : 0u;
-#pragma unroll
-                        for (int i = 0; i < 8; i++) p[i] &= m;
-                    }
-                };
-                auto fast_round = [&](uint32_t r) {
-                    const uint32_t j = jp + r;
-                    uint32_t p[8];
+                // round r's weights into bf16 pairs: R4 decoded with the table
+                // words h3, l1 (rank 15 -> an escape's exponent), or the BF16 words
+                auto weights = [&](uint32_t r, uint32_t h3, uint32_t l1, uint32_t p[8]) {
                     if (R4) {
                         const uint4 sv = *reinterpret_cast<const uint4 *>(stg + r * 512 + 16 * lane);
                         const uint2 nv = *reinterpret_cast<const uint2 *>(stg + C * 512 + r * 256 + 8 * lane);
                         R4Lut Lr = L;
-                        Lr.h3 = __shfl_sync(DGT_FULL, rl.h3, r);
-                        Lr.l1 = __shfl_sync(DGT_FULL, rl.l1, r);
+                        Lr.h3 = h3;
+                        Lr.l1 = l1;
                         r4_dec16(nv, sv, Lr, p);
                     } else {
                         const uint4 lo = *reinterpret_cast<const uint4 *>(stg + r * 1024 + 32 * lane);
@@ -537,77 +531,77 @@ __global__ void __launch_bounds__((TNW + TPW) * 32, 1) k_gemv_tma(GemvArgs a) {
                         p[0] = lo.x; p[1] = lo.y; p[2] = lo.z; p[3] = lo.w;
                         p[4] = hi.x; p[5] = hi.y; p[6] = hi.z; p[7] = hi.w;
                     }
-                    cut_mask(r, p);
-                    acc = fma_chunk16(p, xs, j, lane, acc);
                 };
-                if (ok && !slow && pm == 0 && n == C) {
+                // the multiply-adds of round r; in the row's last round cut by K
+                // (r == rp) a lane past K adds fma(+0, +0) = +0 instead, its
+                // weights there being the next row's
+                auto fma_round = [&](uint32_t r, const uint32_t p[8]) {
+                    const float t = fma_chunk16(p, xs, jp + r, lane, acc);
+                    acc = (r == rp && !act) ? __fadd_rn(acc, 0.0f) : t;
+                };
+                // a lane holding two of the round's escapes: its second escaped
+                // weight (index mi2[r]) gets exponent me2[r], without an indexed store
+                auto second_escape = [&](uint32_t r, uint32_t p[8]) {
+                    const uint32_t fm = 0x7F80u << (16 * (mi2[r] & 1u));
+                    const uint32_t fv = me2[r] * 0x00800080u;
 #pragma unroll
-                    for (uint32_t r = 0; r < C; r++) fast_round(r);
-                } else if (ok && !slow && pm == 0) {
-#pragma unroll
-                    for (uint32_t r = 0; r < C; r++) {
-                        if (r >= n) break;
-                        fast_round(r);
+                    for (uint32_t t = 0; t < 8; t++) {
+                        const uint32_t hit = (mi2[r] >> 1) == t ? fm : 0u;
+                        p[t] = (p[t] & ~hit) | (fv & hit);
                     }
-                } else if (ok && !slow) {
+                };
+                // the piece's rounds, each decoded with its own table words
+                // (multi-escape rounds with the lane's own); no branch between
+                // the rounds of a full piece, so that one round's decode overlaps
+                // the previous round's multiply-adds
+                auto table_round = [&](uint32_t r) {
+                    uint32_t p[8];
+                    const uint32_t h3 = __shfl_sync(DGT_FULL, rl.h3, r);
+                    const uint32_t l1 = __shfl_sync(DGT_FULL, rl.l1, r);
+                    const bool own = (pm >> r) & 1u;
+                    weights(r, own ? mh3[r] : h3, own ? ml1[r] : l1, p);
+                    fma_round(r, p);
+                };
+                if (ok && !slow && pm == 0 && n == C && rp >= C) {
+                    // the common piece: full, one escape at most per round, no cut
+#pragma unroll
+                    for (uint32_t r = 0; r < C; r++) {
+                        uint32_t p[8];
+                        weights(r, __shfl_sync(DGT_FULL, rl.h3, r), __shfl_sync(DGT_FULL, rl.l1, r), p);
+                        acc = fma_chunk16(p, xs, jp + r, lane, acc);
+                    }
+                } else if (ok && !slow && pm2 == 0 && n == C) {
+#pragma unroll
+                    for (uint32_t r = 0; r < C; r++) table_round(r);
+                } else if (ok && !slow && pm2 == 0) {
 #pragma unroll
                     for (uint32_t r = 0; r < C; r++) {
                         if (r >= n) break;
-                        const uint32_t j = jp + r;
-                        uint32_t p[8];
-                        if (R4) {
-                            const uint4 sv = *reinterpret_cast<const uint4 *>(stg + r * 512 + 16 * lane);
-                            const uint2 nv = *reinterpret_cast<const uint2 *>(stg + C * 512 + r * 256 + 8 * lane);
-                            R4Lut Lr = L;
-                            const uint32_t h3 = __shfl_sync(DGT_FULL, rl.h3, r);
-                            const uint32_t l1 = __shfl_sync(DGT_FULL, rl.l1, r);
-                            Lr.h3 = ((pm >> r) & 1u) ? mh3[r] : h3;
-                            Lr.l1 = ((pm >> r) & 1u) ? ml1[r] : l1;
-                            r4_dec16(nv, sv, Lr, p);
-                        } else {
-                            const uint4 lo = *reinterpret_cast<const uint4 *>(stg + r * 1024 + 32 * lane);
-                            const uint4 hi = *reinterpret_cast<const uint4 *>(stg + r * 1024 + 32 * lane + 16);
-                            p[0] = lo.x; p[1] = lo.y; p[2] = lo.z; p[3] = lo.w;
-                            p[4] = hi.x; p[5] = hi.y; p[6] = hi.z; p[7] = hi.w;
-                        }
-                        cut_mask(r, p);
-                        acc = fma_chunk16(p, xs, j, lane, acc);
+                        table_round(r);
                     }
                 } else if (ok) {
-                    // partial or cut piece, or a round whose escapes need the general patch
-                    for (uint32_t r = 0; r < n; r++) {
-                        const uint32_t j = jp + r;
-                        const bool ract = r != rp || act;
+                    // a round whose escapes need the general patch, a lane with two
+                    // escapes, or a short BF16 piece
+#pragma unroll
+                    for (uint32_t r = 0; r < C; r++) {
+                        if (r >= n) break;
                         uint32_t p[8];
-                        if (R4) {
+                        const uint32_t h3 = __shfl_sync(DGT_FULL, rl.h3, r);
+                        const uint32_t l1 = __shfl_sync(DGT_FULL, rl.l1, r);
+                        if (R4 && ((pm >> r) & 1u) && !((pmok >> r) & 1u)) {
+                            // its escape index and ranks straight from memory
+                            const uint64_t sx = u.row * a.nseg + jp + r;
+                            const uint32_t b = a.seg[sx], c = a.seg[sx + 1] - b;
                             const uint4 sv = *reinterpret_cast<const uint4 *>(stg + r * 512 + 16 * lane);
                             const uint2 nv = *reinterpret_cast<const uint2 *>(stg + C * 512 + r * 256 + 8 * lane);
-                            const uint32_t h3 = __shfl_sync(DGT_FULL, rl.h3, r);
-                            const uint32_t l1 = __shfl_sync(DGT_FULL, rl.l1, r);
-                            if ((pm >> r) & 1u) {
-                                // a rare round: its escape index straight from seg
-                                const uint64_t sx = u.row * a.nseg + jp + r;
-                                const uint32_t b = a.seg[sx], c = a.seg[sx + 1] - b;
-                                r4_round_general_cb(a, L, nv, sv, c, b, escb[R4 ? w : 0], table_s, lane, ract, p);
-                            } else {
-                                R4Lut Lr = L;
-                                Lr.h3 = h3;
-                                Lr.l1 = l1;
-                                r4_dec16(nv, sv, Lr, p);
-                            }
+                            r4_round_general_cb(a, L, nv, sv, c, b, escb[R4 ? w : 0], table_s, lane,
+                                                r != rp || act, p);
                         } else {
-                            const uint4 lo = *reinterpret_cast<const uint4 *>(stg + r * 1024 + 32 * lane);
-                            const uint4 hi = *reinterpret_cast<const uint4 *>(stg + r * 1024 + 32 * lane + 16);
-                            p[0] = lo.x; p[1] = lo.y; p[2] = lo.z; p[3] = lo.w;
-                            p[4] = hi.x; p[5] = hi.y; p[6] = hi.z; p[7] = hi.w;
+                            const bool own = (pm >> r) & 1u;
+                            weights(r, own ? mh3[r] : h3, own ? ml1[r] : l1, p);
+                            if ((pm2 >> r) & 1u) second_escape(r, p);
                         }
-                        if (r == rp) {
-                            // the row's last round, cut by K: lanes past K add +0 (x there is 0 too)
-                            const uint32_t m = act ? 0xFFFFFFFFu : 0u;
-#pragma unroll
-                            for (int i = 0; i < 8; i++) p[i] &= m;
-                        }
-                        acc = fma_chunk16(p, xs, j, lane, acc);
+                        fma_round(r, p);
                     }
                 }
                 __syncwarp();

@@ -130,6 +130,33 @@ __device__ __forceinline__ bool rec_exponent(uint32_t rec, uint2 nv, uint32_t la
     return true;
 }
 
+// The same when a lane may hold two of the round's (at most three) escapes:
+// e1 = this lane's first escape exponent, and for a lane with two, e2 = the
+// second's and i2 = its weight index (0..15) in the lane's 16-weight chunk
+// (i2 = 16 otherwise).  The lane decodes with the rank-15 entry set to e1 and
+// then rewrites weight i2's exponent to e2.  Returns false for more than
+// three escapes, three in one lane, or counts that disagree.
+__device__ __forceinline__ bool rec_exponent2(uint32_t rec, uint2 nv, uint32_t lane, uint32_t &e1, uint32_t &e2,
+                                              uint32_t &i2) {
+    const uint32_t c = rec & 0xFFu;
+    const uint32_t m0 = nib15_mask(nv.x), m1 = nib15_mask(nv.y);
+    const uint32_t k = __popc(m0) + __popc(m1);
+    const uint32_t b1 = __ballot_sync(DGT_FULL, k == 1), b2 = __ballot_sync(DGT_FULL, k == 2);
+    if (c > 3 || __any_sync(DGT_FULL, k > 2) || (uint32_t)(__popc(b1) + 2 * __popc(b2)) != c) return false;
+    const uint32_t lt = (1u << lane) - 1u;
+    const uint32_t q = __popc(b1 & lt) + 2u * __popc(b2 & lt);   // escapes in the lanes before this one
+    e1 = k ? (rec >> (8 + 8 * q)) & 0xFFu : 0u;
+    e2 = 0;
+    i2 = 16;
+    if (k == 2) {
+        e2 = (rec >> (16 + 8 * q)) & 0xFFu;   // q <= 1: the two fit in x0..x2
+        const uint32_t lo_rest = m0 & (m0 - 1u);   // m0 without its first escape
+        i2 = m0 == 0 ? 8 + ((__ffs(m1 & (m1 - 1u)) - 1) >> 2)
+                     : (lo_rest ? (__ffs(lo_rest) - 1) >> 2 : 8 + ((__ffs(m1) - 1) >> 2));
+    }
+    return true;
+}
+
 // A round whose segment holds two or more escapes, when every lane holds at
 // most one of them: the exponent of this lane's escape (its place among the
 // round's escaped lanes; the first two come prefetched).  Returns false when

@@ -113,6 +113,48 @@ def test_gemv_bulk_4096x16384_full(dgt):
     assert _eq32(b32, r32) and np.array_equal(b16, r16)
 
 
+def _plant_escapes(w, key, n_rounds):
+    # rounds holding many escapes (4 to 40, some past 32) and rounds of 2 or 3
+    # escapes with two in one lane's 16 columns; the planted weights take
+    # exponents 1..24 (rare in N(0, 0.02) data, so their ranks are >= 15)
+    g = np.random.default_rng(key)
+    N, K = w.shape
+    J = K // 512
+    rows = set()
+    for i in range(n_rounds):
+        r, j = int(g.integers(N)), int(g.integers(J))
+        if i % 3 == 2:
+            lane = int(g.integers(32))
+            cols = 512 * j + 16 * lane + g.choice(16, 2, replace=False)
+            if i % 2:
+                cols = np.append(cols, 512 * j + 16 * ((lane + 1 + int(g.integers(31))) % 32) + int(g.integers(16)))
+        else:
+            c = int(g.integers(4, 41))
+            cols = 512 * j + g.choice(512, c, replace=False)
+        e = g.integers(1, 25, size=len(cols)).astype(np.uint16)
+        w[r, cols] = (g.integers(0, 2, size=len(cols)).astype(np.uint16) << 15) | (e << 7) | \
+            g.integers(0, 128, size=len(cols)).astype(np.uint16)
+        rows.add(r)
+    return sorted(rows)
+
+
+@pytest.mark.parametrize("N,K", [(2048, 16384), (8192, 16384)])
+def test_gemv_escape_heavy_rounds(dgt, N, K):
+    # long units (8 and 32 rounds, slice plans 4 and 1), so that the escape
+    # lists of rounds with four or more escapes are fetched a unit ahead, and
+    # the 32nd round of a unit takes them from memory; R4 == BF16 on every
+    # row, the oracle on the planted rows and a sample
+    w = S.weights(N, K, (207, N, K, 0))
+    planted = _plant_escapes(w, N, 600)
+    x = S.activations(K, (207, 999, N))
+    y16, y32, b16, b32 = _run_both(dgt, w, x)
+    assert _eq32(y32, b32) and np.array_equal(y16, b16)
+    g = np.random.default_rng(N + 1)
+    rows = np.unique(np.concatenate([planted, [0, N - 1], g.choice(N, 64, replace=False)]))
+    r32, r16 = oracle.gemv(w, x, rows=rows)
+    assert _eq32(y32[rows], r32) and np.array_equal(y16[rows], r16)
+
+
 @pytest.mark.parametrize("model", [S.DENSE_3B, S.DENSE_12B], ids=lambda m: m["name"])
 def test_gemv_model_projections_sampled(dgt, model):
     # one layer's projections at full size: R4 == BF16 on every row, oracle on sampled rows
