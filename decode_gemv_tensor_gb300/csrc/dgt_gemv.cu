@@ -228,9 +228,9 @@ __global__ void __launch_bounds__(PW * 32, 1) k_gemv(GemvArgs a) {
 
 // ---------------------------------------------------------------------------
 // Bulk-copy streaming kernel (the default when cols % 32 == 0).  One CTA per
-// SM of TNW = 16 consumer warps and TPW = 2 producer warps; CTA b owns rows
+// SM of TNW = 18 consumer warps and TPW = 2 producer warps; CTA b owns rows
 // [b*N/G, (b+1)*N/G) and consumer warp w takes the (row, slice) units w,
-// w+16, ...  Each consumer owns a ring of NS shared-memory stages; one lane of
+// w+18, ...  Each consumer owns a ring of NS shared-memory stages; one lane of
 // a producer warp keeps it full, issuing the 1-D bulk copies (cp.async.bulk)
 // of the next piece as soon as the consumer has released a stage (its "empty"
 // mbarrier, polled without blocking), the arrival counted on the stage's
@@ -251,19 +251,19 @@ __global__ void __launch_bounds__(PW * 32, 1) k_gemv(GemvArgs a) {
 #define DGT_GEMV_INTERLEAVE 0
 #endif
 #ifndef DGT_GEMV_TNW
-#define DGT_GEMV_TNW 14
+#define DGT_GEMV_TNW 18
 #endif
 #ifndef DGT_GEMV_NS_R4
-#define DGT_GEMV_NS_R4 4
+#define DGT_GEMV_NS_R4 3
 #endif
 #ifndef DGT_GEMV_C_R4
 #define DGT_GEMV_C_R4 4   // rounds per R4 piece (at most 13: the summary slot holds C + 6 words)
 #endif
 #ifndef DGT_GEMV_NS_BF16
-#define DGT_GEMV_NS_BF16 5
+#define DGT_GEMV_NS_BF16 4
 #endif
 #ifndef DGT_GEMV_TCHUNK
-#define DGT_GEMV_TCHUNK 896
+#define DGT_GEMV_TCHUNK 864
 #endif
 #ifndef DGT_GEMV_TPW
 #define DGT_GEMV_TPW 2
