@@ -159,18 +159,48 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, ui
     asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
+// Escape ranks a decoder row keeps in shared memory: the row's next GT_EW
+// escapes from where its pass over the tile starts, so that the decode of a
+// stage reads no escape from global memory; escapes past them (rows with
+// more than GT_EW in the tile's K range) are read from the list itself.
+constexpr uint32_t GT_EW = 32;
+
+// The window of row t: esc[wbase, wbase + GT_EW), the row's four chunk
+// threads loading 8 bytes each (q: the thread's chunk).
+__device__ __forceinline__ void load_esc_window(const GemmArgs &a, uint8_t *win, uint64_t wbase, uint32_t q) {
+    uint32_t lo = 0, hi = 0;
+#pragma unroll
+    for (uint32_t b = 0; b < 8; b++) {
+        const uint64_t e = wbase + 8 * q + b;
+        const uint32_t v = e < a.n_esc ? a.esc[e] : 0u;
+        if (b < 4) lo |= v << (8 * b);
+        else hi |= v << (8 * (b - 4));
+    }
+    *reinterpret_cast<uint2 *>(win + 8 * q) = make_uint2(lo, hi);
+}
+
+// The rank of escape e of the row (its window starting at escape wbase).
+__device__ __forceinline__ uint32_t esc_rank(const GemmArgs &a, const uint8_t *win, uint64_t wbase, uint64_t e,
+                                             bool &bad) {
+    if (e >= a.n_esc) {
+        bad = true;
+        return 0u;
+    }
+    const uint64_t rel = e - wbase;
+    return rel < GT_EW ? win[rel] : a.esc[e];
+}
+
 // Decoder thread (row t, chunk q): the 16 weights [16q, 16q + 16) of W row t
 // of a stage, from the raw tiles (shared addresses raw_sm, raw_nib of the
 // row) into the row's swizzled bf16 chunks 2q and 2q+1 (arow).  The four
 // chunk threads of a row are lanes 4j..4j+3 of one warp; they place their
 // escapes by a prefix sum over the four and advance the row's running escape
-// index eidx.  r0, r1: the ranks of the row's next two escapes (esc[eidx],
-// esc[eidx + 1]), loaded ahead.  A chunk with one escape that is among those
-// two decodes with the exponent table's rank-15 entry replaced by its
-// exponent; any other escape is patched weight by weight.
+// index eidx, the ranks coming from the row's window (win, from escape wbase
+// on).  A chunk with one escape decodes with the exponent table's rank-15
+// entry replaced by its exponent; more are patched weight by weight.
 __device__ __forceinline__ void decode_chunk16(const GemmArgs &a, const R4Lut &L, uint32_t raw_sm,
                                                uint32_t raw_nib, uint32_t arow, uint32_t t, uint32_t q,
-                                               uint64_t &eidx, uint32_t &r0, uint32_t &r1,
+                                               uint64_t &eidx, const uint8_t *win, uint64_t wbase,
                                                const uint8_t *table_s, bool &bad) {
     const uint4 sv = lds128(raw_sm + q * 16);
     const uint2 nv = lds64(raw_nib + q * 8);
@@ -183,37 +213,28 @@ __device__ __forceinline__ void decode_chunk16(const GemmArgs &a, const R4Lut &L
     if (q >= 2) incl += y;
     const uint32_t total = __shfl_sync(DGT_FULL, incl, 3, 4);
     const uint32_t before = incl - c;
-    const bool one = c == 1 && before < 2;
     R4Lut Lr = L;
-    if (one) {
-        const uint32_t rk = before == 0 ? r0 : r1;
-        Lr.h3 = prmt(L.h3, table_s[rk] >> 1, 0x4210u);
-        Lr.l1 = (L.l1 & 0x7FFFFFFFu) | ((table_s[rk] & 1u) << 31);
+    if (c == 1) {
+        const uint32_t ex = table_s[esc_rank(a, win, wbase, eidx + before, bad)];
+        Lr.h3 = prmt(L.h3, ex >> 1, 0x4210u);
+        Lr.l1 = (L.l1 & 0x7FFFFFFFu) | ((ex & 1u) << 31);
     }
     uint32_t p[8];
     r4_dec16(nv, sv, Lr, p);
-    if (c && !one) {
+    if (c > 1) {
         uint64_t e = eidx + before;
 #pragma unroll
         for (int i = 0; i < 16; i++) {
             const uint32_t m = i < 8 ? m0 : m1;
             if ((m >> (4 * (i & 7))) & 1u) {
-                uint32_t ex = 0;
-                if (e < a.n_esc) ex = table_s[a.esc[e]];
-                else bad = true;
+                const uint32_t ex = table_s[esc_rank(a, win, wbase, e, bad)];
                 e++;
                 const uint32_t sh = 16 * (i & 1);
                 p[i >> 1] = (p[i >> 1] & ~(0x7F80u << sh)) | (ex << (7 + sh));
             }
         }
-    } else if (one && eidx + before >= a.n_esc) {
-        bad = true;
     }
-    if (total) {
-        eidx += total;
-        r0 = eidx < a.n_esc ? a.esc[eidx] : 0u;
-        r1 = eidx + 1 < a.n_esc ? a.esc[eidx + 1] : 0u;
-    }
+    eidx += total;
     const uint32_t c0 = (2 * q) ^ (t & 7), c1 = (2 * q + 1) ^ (t & 7);
     sts128(arow + c0 * 16, p[0], p[1], p[2], p[3]);
     sts128(arow + c1 * 16, p[4], p[5], p[6], p[7]);
@@ -230,6 +251,7 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
     __shared__ __align__(8) uint64_t bar_done;
     __shared__ uint32_t tmem_slot;
     __shared__ uint8_t table_s[256];
+    __shared__ __align__(8) uint8_t escw[R4 ? GT_N : 1][GT_EW];
     __shared__ int abort_flag;
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     const uint32_t tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -376,8 +398,9 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
             L.h3 = a.L.h3;
             L.l0 = a.L.l0;
             L.l1 = a.L.l1;
-            uint32_t r0 = eidx < a.n_esc ? a.esc[eidx] : 0u;
-            uint32_t r1 = eidx + 1 < a.n_esc ? a.esc[eidx + 1] : 0u;
+            const uint64_t wbase = eidx;
+            if (rin) load_esc_window(a, escw[t], wbase, q);
+            __syncwarp();
             const uint32_t base_a = smem_u32(base);
             uint32_t s = 0, par = 0;
             for (uint32_t i = 0; i < nkb; i++) {
@@ -388,7 +411,7 @@ __global__ void __launch_bounds__(GT_THREADS, 1)
                 }
                 const uint32_t st0 = base_a + s * SB;
                 decode_chunk16(a, L, st0 + GT_N * 128 + mt * 128 + t * 64, st0 + GT_N * 128 + mt * 128 + GT_N * 64 + t * 32,
-                               st0 + t * 128, t, q, eidx, r0, r1, table_s, bad);
+                               st0 + t * 128, t, q, eidx, escw[t], wbase, table_s, bad);
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&bar_w[s]));
@@ -470,6 +493,7 @@ __global__ void __launch_bounds__((R4 ? PT_WARPS_R4 : PT_WARPS_BF16) * 32, 1)
     __shared__ __align__(8) uint64_t acc_full[2], acc_empty[2], bar_done;
     __shared__ uint32_t tmem_slot;
     __shared__ uint8_t table_s[256];
+    __shared__ __align__(8) uint8_t escw[R4 ? GT_N : 1][GT_EW];
     __shared__ int abort_flag;
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     const uint32_t tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -640,9 +664,12 @@ __global__ void __launch_bounds__((R4 ? PT_WARPS_R4 : PT_WARPS_BF16) * 32, 1)
             uint32_t n0, m0;
             tile_of(i, n0, m0);
             const uint64_t row = (uint64_t)n0 + t;
-            uint64_t eidx = a.seg[row * a.nseg];
-            uint32_t r0 = eidx < a.n_esc ? a.esc[eidx] : 0u;
-            uint32_t r1 = eidx + 1 < a.n_esc ? a.esc[eidx + 1] : 0u;
+            const bool rin = row < a.N;   // rows past the tensor read zeros
+            uint64_t eidx = rin ? a.seg[row * a.nseg] : a.n_esc;
+            const uint64_t wbase = eidx;
+            __syncwarp();   // the previous tile's reads of the window are done
+            if (rin) load_esc_window(a, escw[t], wbase, q);
+            __syncwarp();
             for (uint32_t kb = 0; kb < nkb; kb++, g++) {
                 const uint32_t s = g % P, par = (g / P) & 1u;
                 if (!wait_or_abort(smem_u32(&bar_raw[s]), par, abortp, a.spin)) {
@@ -653,7 +680,7 @@ __global__ void __launch_bounds__((R4 ? PT_WARPS_R4 : PT_WARPS_BF16) * 32, 1)
                 }
                 const uint32_t st0 = base_a + s * SB;
                 decode_chunk16(a, L, st0 + GT_N * 128 + mt * 128 + t * 64,
-                               st0 + GT_N * 128 + mt * 128 + GT_N * 64 + t * 32, st0 + t * 128, t, q, eidx, r0, r1,
+                               st0 + GT_N * 128 + mt * 128 + GT_N * 64 + t * 32, st0 + t * 128, t, q, eidx, escw[t], wbase,
                                table_s, bad);
                 fence_proxy_async_smem();
                 __syncwarp();
