@@ -197,7 +197,9 @@ __device__ __forceinline__ uint32_t esc_rank(const GemmArgs &a, const uint8_t *w
 // escapes by a prefix sum over the four and advance the row's running escape
 // index eidx, the ranks coming from the row's window (win, from escape wbase
 // on).  A chunk with one escape decodes with the exponent table's rank-15
-// entry replaced by its exponent; more are patched weight by weight.
+// entry replaced by its exponent; more are patched weight by weight.  A
+// stage where no lane of the warp holds an escape (most of them) skips all
+// of that.
 __device__ __forceinline__ void decode_chunk16(const GemmArgs &a, const R4Lut &L, uint32_t raw_sm,
                                                uint32_t raw_nib, uint32_t arow, uint32_t t, uint32_t q,
                                                uint64_t &eidx, const uint8_t *win, uint64_t wbase,
@@ -205,36 +207,40 @@ __device__ __forceinline__ void decode_chunk16(const GemmArgs &a, const R4Lut &L
     const uint4 sv = lds128(raw_sm + q * 16);
     const uint2 nv = lds64(raw_nib + q * 8);
     const uint32_t m0 = nib15_mask(nv.x), m1 = nib15_mask(nv.y);
-    const uint32_t c = __popc(m0) + __popc(m1);
-    uint32_t incl = c;
-    uint32_t y = __shfl_up_sync(DGT_FULL, incl, 1, 4);
-    if (q >= 1) incl += y;
-    y = __shfl_up_sync(DGT_FULL, incl, 2, 4);
-    if (q >= 2) incl += y;
-    const uint32_t total = __shfl_sync(DGT_FULL, incl, 3, 4);
-    const uint32_t before = incl - c;
-    R4Lut Lr = L;
-    if (c == 1) {
-        const uint32_t ex = table_s[esc_rank(a, win, wbase, eidx + before, bad)];
-        Lr.h3 = prmt(L.h3, ex >> 1, 0x4210u);
-        Lr.l1 = (L.l1 & 0x7FFFFFFFu) | ((ex & 1u) << 31);
-    }
     uint32_t p[8];
-    r4_dec16(nv, sv, Lr, p);
-    if (c > 1) {
-        uint64_t e = eidx + before;
+    if (!__any_sync(DGT_FULL, (m0 | m1) != 0)) {
+        r4_dec16(nv, sv, L, p);
+    } else {
+        const uint32_t c = __popc(m0) + __popc(m1);
+        uint32_t incl = c;
+        uint32_t y = __shfl_up_sync(DGT_FULL, incl, 1, 4);
+        if (q >= 1) incl += y;
+        y = __shfl_up_sync(DGT_FULL, incl, 2, 4);
+        if (q >= 2) incl += y;
+        const uint32_t total = __shfl_sync(DGT_FULL, incl, 3, 4);
+        const uint32_t before = incl - c;
+        R4Lut Lr = L;
+        if (c == 1) {
+            const uint32_t ex = table_s[esc_rank(a, win, wbase, eidx + before, bad)];
+            Lr.h3 = prmt(L.h3, ex >> 1, 0x4210u);
+            Lr.l1 = (L.l1 & 0x7FFFFFFFu) | ((ex & 1u) << 31);
+        }
+        r4_dec16(nv, sv, Lr, p);
+        if (c > 1) {
+            uint64_t e = eidx + before;
 #pragma unroll
-        for (int i = 0; i < 16; i++) {
-            const uint32_t m = i < 8 ? m0 : m1;
-            if ((m >> (4 * (i & 7))) & 1u) {
-                const uint32_t ex = table_s[esc_rank(a, win, wbase, e, bad)];
-                e++;
-                const uint32_t sh = 16 * (i & 1);
-                p[i >> 1] = (p[i >> 1] & ~(0x7F80u << sh)) | (ex << (7 + sh));
+            for (int i = 0; i < 16; i++) {
+                const uint32_t m = i < 8 ? m0 : m1;
+                if ((m >> (4 * (i & 7))) & 1u) {
+                    const uint32_t ex = table_s[esc_rank(a, win, wbase, e, bad)];
+                    e++;
+                    const uint32_t sh = 16 * (i & 1);
+                    p[i >> 1] = (p[i >> 1] & ~(0x7F80u << sh)) | (ex << (7 + sh));
+                }
             }
         }
+        eidx += total;
     }
-    eidx += total;
     const uint32_t c0 = (2 * q) ^ (t & 7), c1 = (2 * q + 1) ^ (t & 7);
     sts128(arow + c0 * 16, p[0], p[1], p[2], p[3]);
     sts128(arow + c1 * 16, p[4], p[5], p[6], p[7]);
