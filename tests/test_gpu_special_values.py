@@ -251,6 +251,22 @@ def test_gemm_every_pattern(dgt, M, N, K, split, finite):
         assert err <= 1e-3
 
 
+@pytest.mark.parametrize("finite", [True, False], ids=["finite", "all"])
+def test_gemm_every_pattern_persistent(dgt, finite):
+    # the persistent schedule (two accumulators in tensor memory) over 160
+    # tiles of 128 x 64, so that some CTAs walk two: the same checks
+    M, N, K = 640, 2048, 512
+    W = S.bf16_patterns(N * K, (612, N, K, int(finite)), finite_only=finite).reshape(N, K)
+    X = S.scaled_activations(K, (612, 999, M), -100, count=M)
+    y = _gemm_both(dgt, W, X, dgt.gemm_plan(M, N, K, m_tile=64, split_k=1, schedule=2))
+    ref = oracle.gemm_f64(X, W)
+    assert np.array_equal(_classes(y), _classes(ref))
+    fin = np.isfinite(ref)
+    if fin.any():
+        err = np.linalg.norm(y[fin].astype(np.float64) - ref[fin]) / np.linalg.norm(ref[fin])
+        assert err <= 1e-3
+
+
 def test_gemm_subnormal_weights_exact(dgt):
     # subnormal weights m * 2^-133 and integer X: exact integer multiples of
     # 2^-133 (a flush of subnormal operands would give zeros)
@@ -261,9 +277,9 @@ def test_gemm_subnormal_weights_exact(dgt):
     xi = g.integers(-2, 3, size=(M, K))
     W = np.where(m < 0, 0x8000, 0).astype(np.uint16) | np.abs(m).astype(np.uint16)
     X = S.f32_to_bf16_bits(xi.astype(np.float32))
-    for split in (1, 4):
-        y = _gemm_both(dgt, W, X, dgt.gemm_plan(M, N, K, split_k=split))
-        assert np.array_equal(y.astype(np.float64), (xi @ m.T).astype(np.float64) * 2.0 ** -133), split
+    for split, sched in ((1, 1), (4, 1), (1, 2)):
+        y = _gemm_both(dgt, W, X, dgt.gemm_plan(M, N, K, split_k=split, schedule=sched))
+        assert np.array_equal(y.astype(np.float64), (xi @ m.T).astype(np.float64) * 2.0 ** -133), (split, sched)
 
 
 def test_gemm_planted_infinities_and_zeros(dgt):
