@@ -12,20 +12,20 @@
 // d = 16, 8, 4, 2, 1; with S slices (dgt_plan_slices) slice s owns rounds
 // [sJ/S, (s+1)J/S) and the slice results are added left to right.
 //
-// GB300 design: a persistent grid of one 16-warp CTA per SM.  CTA b owns a
-// contiguous, even share of the rows and walks its (row, slice) units warp by
-// warp, so no SM waits on a second wave.  x is copied once per CTA into shared
-// memory as bf16 pairs in a [round][half][lane] uint4 layout (two
-// conflict-free LDS.128 per lane and round), and the products use the
-// mixed-precision fma.rn.f32.bf16, which takes the bf16 halves directly.
-// R4 weights stream with one 16-byte load of
-// sign/mantissa bytes and one 8-byte load of nibbles per lane and round
-// (L1 no-allocate), double-buffered so that eight rounds are in flight per
-// lane; the exponent comes from register byte-permutes.  Escapes are known
-// per round from the row-segment index: a ballot gives a warp-uniform mask of
-// rounds with escapes, which go to one out-of-line function (one escape is
-// patched from a prefetched exponent, more are staged through shared
-// memory); rounds without escapes pay one test and stay in a small loop.
+// GB300 design: a persistent grid of one CTA per SM; CTA b owns a contiguous,
+// even share of the rows and walks its (row, slice) units warp by warp, so no
+// SM waits on a second wave.  x is copied once per CTA into shared memory as
+// bf16 pairs in a [round][half][lane] uint4 layout (two conflict-free LDS.128
+// per lane and round), and the products use the mixed-precision
+// fma.rn.f32.bf16, which takes the bf16 halves directly; the exponent comes
+// from register byte-permutes.  Three kernels: the bulk-copy kernel
+// (k_gemv_tma, the default, described below); a register-streaming kernel
+// (k_gemv) when a row's length is a multiple of 16 but not of 32, or the
+// bulk-copy kernel's rings and x do not fit shared memory (16-byte
+// sign/mantissa and 8-byte nibble loads per lane and round, double-buffered;
+// a ballot gives a warp-uniform mask of the rounds with escapes, which go out
+// of line); and an any-shape kernel (k_gemv_any) for unaligned arrays, other
+// lengths and rows longer than 160 rounds.
 #include <cuda_runtime.h>
 
 #include "../../include/dgt.h"
@@ -237,15 +237,16 @@ __global__ void __launch_bounds__(PW * 32, 1) k_gemv(GemvArgs a) {
 // "full" mbarrier.  No consumer waits on another consumer.  A bulk copy takes
 // warp-uniform operands, so a producer warp issues its lanes' copies one
 // after another: two producer warps halve that queue (BF16 streams about 7%
-// faster; R4, bound by its decode, is unchanged).  A full piece is C rounds,
-// decoded from shared memory without
-// per-round tests except the warp-uniform escape bit.  An R4 round whose
-// segment holds one escape decodes with the rank-15 entry of the exponent
-// table replaced by that escape's exponent (only the escaped weight has
-// nibble 15); two or three escapes do the same per lane, a lane holding two
-// of them rewriting its second escaped weight's exponent; other cases take a
-// general patch from the escape list.  Every wait is bounded: one that runs out sets the status word, and
-// the warp stops, lets its copies in flight land and exits.
+// faster; R4, bound by its decode, is unchanged).  A piece is C rounds (fewer
+// at a unit's end), decoded from shared memory with no branch between its
+// rounds, so that one round's decode overlaps the previous round's
+// multiply-adds.  An R4 round whose segment holds one escape decodes with the
+// rank-15 entry of the exponent table replaced by that escape's exponent
+// (only the escaped weight has nibble 15); two or three escapes do the same
+// per lane, a lane holding two of them rewriting its second escaped weight's
+// exponent; other cases take a general patch from the escape list.  Every
+// wait is bounded: one that runs out sets the status word, and the warp
+// stops, lets its copies in flight land and exits.
 // ---------------------------------------------------------------------------
 #ifndef DGT_GEMV_INTERLEAVE
 #define DGT_GEMV_INTERLEAVE 0
