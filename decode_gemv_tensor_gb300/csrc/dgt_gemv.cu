@@ -58,6 +58,12 @@ struct GemvArgs {
     R4Lut L;
     uint8_t table[256];
     int32_t *status;
+    // expert blocks (the expert gather with few (token, slot) pairs): pair i
+    // takes a contiguous group of CTAs, which compute y32[i * ne + n] =
+    // W[ids[i] * ne + n] . x[i / topk] for n < ne; ids == nullptr otherwise
+    const int32_t *ids;
+    uint32_t pairs, topk, n_experts;
+    uint64_t ne;
 };
 
 template <bool R4, int U>
@@ -370,12 +376,35 @@ __global__ void __launch_bounds__((TNW + TPW) * 32, 1) k_gemv_tma(GemvArgs a) {
     const uint64_t G = gridDim.x;
 #if DGT_GEMV_INTERLEAVE
     // CTA b owns rows b, b + G, b + 2G, ...: the whole grid sweeps one window
-    const uint64_t r0 = blockIdx.x, rs = G;
-    const uint64_t nrows = a.rows > r0 ? (a.rows - r0 + G - 1) / G : 0;
+    uint64_t r0 = blockIdx.x, nrows = a.rows > r0 ? (a.rows - r0 + G - 1) / G : 0;
+    const uint64_t rs = G;
 #else
-    const uint64_t r0 = (uint64_t)blockIdx.x * a.rows / G, rs = 1;
-    const uint64_t nrows = (uint64_t)(blockIdx.x + 1) * a.rows / G - r0;
+    uint64_t r0 = (uint64_t)blockIdx.x * a.rows / G, nrows = (uint64_t)(blockIdx.x + 1) * a.rows / G - r0;
+    const uint64_t rs = 1;
 #endif
+    uint64_t o0 = r0;           // output index of row r0
+    const uint16_t *xv = a.x;   // this CTA's x
+    if (a.ids) {
+        // expert blocks: CTAs [ceil(iG/P), ceil((i+1)G/P)) take pair i, each an
+        // even share of the expert's rows.  The pair's expert id may come from
+        // the previous kernel, so everything here waits for it first.
+        pdl_wait();
+        const uint32_t P = a.pairs;
+        const uint32_t i = (uint32_t)(((uint64_t)blockIdx.x * P) / G);
+        const uint64_t g0 = ((uint64_t)i * G + P - 1) / P, g1 = ((uint64_t)(i + 1) * G + P - 1) / P;
+        const uint64_t c = blockIdx.x - g0, ng = g1 - g0;
+        const int32_t e = a.ids[i];
+        const uint64_t lr0 = c * a.ne / ng, lr1 = (c + 1) * a.ne / ng;
+        if (e < 0 || (uint32_t)e >= a.n_experts) {
+            if (threadIdx.x == 0) set_status(a.status, DGT_ERR_ARG);
+            nrows = 0;
+        } else {
+            r0 = (uint64_t)e * a.ne + lr0;
+            nrows = lr1 - lr0;
+        }
+        o0 = (uint64_t)i * a.ne + lr0;
+        xv = a.x + (uint64_t)(i / a.topk) * a.cols;
+    }
     const uint32_t log2S = __ffs(a.S) - 1;
     const uint64_t units = nrows << log2S;
     const uint64_t nchunks = (units + TCHUNK - 1) / TCHUNK;
@@ -430,7 +459,7 @@ __global__ void __launch_bounds__((TNW + TPW) * 32, 1) k_gemv_tma(GemvArgs a) {
     pdl_wait();
     for (uint32_t i = tid; i < J * 64; i += TNW * 32) {
         const uint32_t k = 8 * i, j = k >> 9, u = (k >> 4) & 31, h = (k >> 3) & 1;
-        xs[(2 * j + h) * 32 + u] = k < K ? *reinterpret_cast<const uint4 *>(a.x + k) : make_uint4(0, 0, 0, 0);
+        xs[(2 * j + h) * 32 + u] = k < K ? *reinterpret_cast<const uint4 *>(xv + k) : make_uint4(0, 0, 0, 0);
     }
     if (R4 && tid < 256) table_s[tid] = a.table[tid];
     asm volatile("bar.sync 1, %0;" ::"r"(TNW * 32) : "memory");
@@ -620,9 +649,9 @@ __global__ void __launch_bounds__((TNW + TPW) * 32, 1) k_gemv_tma(GemvArgs a) {
         for (uint32_t t = tid; t < (cend - c0) / S; t += TNW * 32) {
             float y = part[t * S];
             for (uint32_t s = 1; s < S; s++) y = y + part[t * S + s];
-            const uint64_t row = r0 + (c0 / S + t) * rs;
-            if (a.y32) a.y32[row] = y;
-            if (a.y) a.y[row] = f32_to_bf16_rne(y);
+            const uint64_t orow = o0 + (c0 / S + t) * rs;
+            if (a.y32) a.y32[orow] = y;
+            if (a.y) a.y[orow] = f32_to_bf16_rne(y);
         }
         asm volatile("bar.sync 1, %0;" ::"r"(TNW * 32) : "memory");
     }
@@ -802,4 +831,86 @@ extern "C" int dgt_gemv_bf16_ex(const uint16_t *d_W, uint64_t rows, uint64_t col
 extern "C" int dgt_gemv_bf16(const uint16_t *d_W, uint64_t rows, uint64_t cols, const uint16_t *d_x,
                              uint16_t *d_y, float *d_y32, int32_t *d_status, void *stream) {
     return dgt_gemv_bf16_ex(d_W, rows, cols, d_x, d_y, d_y32, d_status, 0u, stream);
+}
+
+// ---------------------------------------------------------------------------
+// Expert blocks: the expert gather with few (token, slot) pairs runs as the
+// bulk-copy kernel over the pairs' expert rows (GemvArgs.ids), each pair with
+// its own group of CTAs and its token's x; no routing lists, no slice
+// workspace.  Same order as the gather (the batch-1 order, plan S(ne, K)).
+// ---------------------------------------------------------------------------
+namespace dgt {
+
+template <bool R4>
+static int launch_expert_blocks(GemvArgs &a, cudaStream_t st) {
+    const uint64_t pairs = a.pairs;
+    if (pairs == 0) return DGT_OK;
+    DeviceInfo di;
+    if (device_info(&di) != DGT_OK) return DGT_ERR_CUDA;
+    const size_t smem = (size_t)TNW * TmaCfg<R4>::NS * TmaCfg<R4>::STAGE + (size_t)a.J * 1024;
+    if (a.cols % 32 || smem > (size_t)DGT_GEMV_SMEM_KB * 1024 || pairs > (uint64_t)di.sms)
+        return DGT_ERR_UNSUPPORTED;
+    a.S = dgt_plan_slices(a.ne, a.cols);
+    int bps = 0;
+    if (prepare_kernel((const void *)k_gemv_tma<R4>, smem, (TNW + TPW) * 32, &bps) != DGT_OK) return DGT_ERR_CUDA;
+    const unsigned grid = (unsigned)min((uint64_t)di.sms, pairs * a.ne);
+    if (launch_pdl(k_gemv_tma<R4>, dim3(grid), dim3((TNW + TPW) * 32), smem, st, a) != cudaSuccess)
+        return DGT_ERR_CUDA;
+    return cudaPeekAtLastError() == cudaSuccess ? DGT_OK : DGT_ERR_CUDA;
+}
+
+}  // namespace dgt
+
+int dgt_gemv_expert_blocks(const dgt_r4 *W, uint32_t n_experts, const int32_t *d_ids, uint32_t tokens,
+                           uint32_t topk, const uint16_t *d_x, float *d_y32, int32_t *d_status, uint32_t spin,
+                           void *stream) {
+    if (!W || !n_experts || W->rows % n_experts || !d_ids || !d_x || !d_y32) return DGT_ERR_ARG;
+    if (!aligned16(W->sm) || !aligned16(W->nib) || !aligned16(W->seg) || !aligned16(d_x))
+        return DGT_ERR_UNSUPPORTED;
+    const uint64_t K = W->cols;
+    GemvArgs a = {};
+    a.sm = W->sm;
+    a.nib = W->nib;
+    a.esc = W->esc;
+    a.seg = W->seg;
+    a.rsum = W->seg + dgt_rsum_offset(W->rows, dgt_r4_nseg(K));
+    a.x = d_x;
+    a.y32 = d_y32;
+    a.rows = W->rows;
+    a.cols = K;
+    a.nseg = dgt_r4_nseg(K);
+    a.n_esc = W->n_esc;
+    a.J = (uint32_t)((K + 511) / 512);
+    a.L = make_r4lut(W->table, W->n_table);
+    for (int i = 0; i < 256; i++) a.table[i] = W->table[i];
+    a.status = d_status;
+    a.spin = spin;
+    a.ids = d_ids;
+    a.pairs = tokens * topk;
+    a.topk = topk;
+    a.n_experts = n_experts;
+    a.ne = W->rows / n_experts;
+    return launch_expert_blocks<true>(a, (cudaStream_t)stream);
+}
+
+int dgt_gemv_expert_blocks_bf16(const uint16_t *d_W, uint64_t rows, uint64_t cols, uint32_t n_experts,
+                                const int32_t *d_ids, uint32_t tokens, uint32_t topk, const uint16_t *d_x,
+                                float *d_y32, int32_t *d_status, uint32_t spin, void *stream) {
+    if (!d_W || !n_experts || rows % n_experts || !d_ids || !d_x || !d_y32) return DGT_ERR_ARG;
+    if (!aligned16(d_W) || !aligned16(d_x)) return DGT_ERR_UNSUPPORTED;
+    GemvArgs a = {};
+    a.W = d_W;
+    a.x = d_x;
+    a.y32 = d_y32;
+    a.rows = rows;
+    a.cols = cols;
+    a.J = (uint32_t)((cols + 511) / 512);
+    a.status = d_status;
+    a.spin = spin;
+    a.ids = d_ids;
+    a.pairs = tokens * topk;
+    a.topk = topk;
+    a.n_experts = n_experts;
+    a.ne = rows / n_experts;
+    return launch_expert_blocks<false>(a, (cudaStream_t)stream);
 }

@@ -26,3 +26,19 @@ static inline uint64_t dgt_rsum_offset(uint64_t rows, uint64_t nseg) { return (r
 static inline uint64_t dgt_seg_words(uint64_t rows, uint64_t nseg) {
     return dgt_rsum_offset(rows, nseg) + ((rows * nseg + 3) & ~3ull);
 }
+
+// The expert gather's path for few (token, slot) pairs (dgt_moe.cu): each pair
+// as a block of the batch-1 product's bulk-copy kernel (dgt_gemv.cu), which
+// writes y32[(t * topk + j) * ne + n] = W[ids[t, j] * ne + n] . x[t] in the
+// batch-1 order with the plan S(ne, K), and DGT_ERR_ARG into the status word
+// for an id outside [0, n_experts).  DGT_ERR_UNSUPPORTED (nothing launched)
+// when that kernel does not apply: row length not a multiple of 32, arrays
+// not 16-byte aligned, x too long for its shared memory, or more pairs than
+// the grid has CTAs.
+struct dgt_r4;
+int dgt_gemv_expert_blocks(const dgt_r4 *W, uint32_t n_experts, const int32_t *d_ids, uint32_t tokens,
+                           uint32_t topk, const uint16_t *d_x, float *d_y32, int32_t *d_status, uint32_t spin,
+                           void *stream);
+int dgt_gemv_expert_blocks_bf16(const uint16_t *d_W, uint64_t rows, uint64_t cols, uint32_t n_experts,
+                                const int32_t *d_ids, uint32_t tokens, uint32_t topk, const uint16_t *d_x,
+                                float *d_y32, int32_t *d_status, uint32_t spin, void *stream);

@@ -21,6 +21,9 @@
 //     butterfly-reduced into the workspace.
 //  3. k_moe_combine: adds each pair's slices left to right (y) and applies
 //     the routing weights in slot order (out).
+// With few (token, slot) pairs (a decode step: one token, or one slot per
+// token) each pair instead runs as a block of the batch-1 product's bulk-copy
+// kernel, then the combine over its results if routing weights are given.
 #include <cuda_runtime.h>
 
 #include "../../include/dgt.h"
@@ -805,6 +808,42 @@ int launch_moe(MoeArgs &a, void *d_ws, size_t ws_bytes, cudaStream_t st) {
     return cudaPeekAtLastError() == cudaSuccess ? DGT_OK : DGT_ERR_CUDA;
 }
 
+// Few (token, slot) pairs -- a decode step's gather: every pair as a block of
+// the batch-1 product's bulk-copy kernel (dgt_gemv.cu), its own group of CTAs
+// streaming its expert's rows with its token's x, in the same order and slice
+// plan; no routing lists and no slice workspace.  Reading the experts' rows
+// once per pair instead of once per expert costs nothing when every pair has
+// its own expert (one token, or one slot per token).  The routing weights, if
+// given, are applied by the combine kernel over those results (one slice
+// each).  DGT_ERR_UNSUPPORTED (nothing launched) hands the call to the
+// gather kernels.
+constexpr uint64_t MOE_FEW_PAIRS = 32;
+
+template <bool R4>
+static int moe_few_pairs(MoeArgs &a, const dgt_r4 *W, const uint16_t *d_W, void *d_ws, size_t ws_bytes,
+                         cudaStream_t st) {
+    if ((uint64_t)a.tokens * a.topk > MOE_FEW_PAIRS) return DGT_ERR_UNSUPPORTED;
+    const WsLayout l = moe_ws_layout(a.n_experts, a.ne, a.cols, a.tokens, a.topk);
+    if (!d_ws || ws_bytes < l.total || ((uintptr_t)d_ws & 255)) return DGT_ERR_ARG;
+    float *y = a.y32 ? a.y32 : reinterpret_cast<float *>(static_cast<uint8_t *>(d_ws) + l.partial);
+    const int rc = R4 ? dgt_gemv_expert_blocks(W, a.n_experts, a.ids, a.tokens, a.topk, a.x, y, a.status, a.spin, st)
+                      : dgt_gemv_expert_blocks_bf16(d_W, a.ne * a.n_experts, a.cols, a.n_experts, a.ids, a.tokens,
+                                                    a.topk, a.x, y, a.status, a.spin, st);
+    if (rc != DGT_OK || !a.p) return rc;
+    MoeArgs c = a;
+    c.partial = y;
+    c.S = 1;
+    c.y32 = nullptr;
+    DeviceInfo di;
+    if (device_info(&di) != DGT_OK) return DGT_ERR_CUDA;
+    const uint64_t n_out = (uint64_t)a.tokens * a.ne;
+    uint64_t cgrid = (n_out + 255) / 256;
+    if (cgrid > (uint64_t)di.sms * 8) cgrid = (uint64_t)di.sms * 8;
+    if (cgrid < 1) cgrid = 1;
+    if (launch_pdl(k_moe_combine, dim3((unsigned)cgrid), dim3(256), 0, st, c) != cudaSuccess) return DGT_ERR_CUDA;
+    return cudaPeekAtLastError() == cudaSuccess ? DGT_OK : DGT_ERR_CUDA;
+}
+
 static int moe_common(MoeArgs &a, uint64_t rows, uint64_t cols, uint32_t n_experts, uint32_t tokens, uint32_t topk,
                       const int32_t *d_ids, const uint16_t *d_x, const void *w_ptr, int32_t *d_status,
                       cudaStream_t st) {
@@ -866,6 +905,8 @@ extern "C" int dgt_moe_gemv_ex(const dgt_r4 *W, uint32_t n_experts, const int32_
     a.y32 = d_y32;
     a.out = d_out;
     a.out32 = d_out32;
+    const int frc = moe_few_pairs<true>(a, W, nullptr, d_ws, ws_bytes, st);
+    if (frc != DGT_ERR_UNSUPPORTED) return frc;
     return launch_moe<true>(a, d_ws, ws_bytes, st);
 }
 
@@ -891,6 +932,8 @@ extern "C" int dgt_moe_gemv_bf16(const uint16_t *d_W, uint64_t rows, uint64_t co
     a.y32 = d_y32;
     a.out = d_out;
     a.out32 = d_out32;
+    const int frc = moe_few_pairs<false>(a, nullptr, d_W, d_ws, ws_bytes, st);
+    if (frc != DGT_ERR_UNSUPPORTED) return frc;
     return launch_moe<false>(a, d_ws, ws_bytes, st);
 }
 
