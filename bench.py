@@ -59,7 +59,8 @@ KERNELS = ["rice_to_r4", "f1_to_r4", "r4_to_bf16", "gemv_r4", "gemv_bf16", "moe_
            "gemm_bf16"]
 KERNEL_SRC = {"rice_to_r4": "dgt_transcode.cu", "f1_to_r4": "dgt_transcode.cu",
               "r4_to_bf16": "dgt_transcode.cu", "gemv_r4": "dgt_gemv.cu", "gemv_bf16": "dgt_gemv.cu",
-              "moe_r4": "dgt_moe.cu", "moe_bf16": "dgt_moe.cu", "gemm_r4": "dgt_gemm.cu",
+              "moe_r4": ("dgt_moe.cu", "dgt_gemv.cu"), "moe_bf16": ("dgt_moe.cu", "dgt_gemv.cu"),
+              "gemm_r4": "dgt_gemm.cu",
               "gemm_bf16": "dgt_gemm.cu", "mgemm_r4": "dgt_gemm.cu", "mgemm_bf16": "dgt_gemm.cu"}
 
 
@@ -72,10 +73,12 @@ def hbm_peak():
 
 
 def src_sha(name):
-    """Hash of a kernel's source file and the device headers it includes."""
+    """Hash of a kernel's source file(s) and the device headers they include
+    (the expert gather runs its few-pair case on the batch-1 product's kernel)."""
     csrc = os.path.join(ROOT, "decode_gemv_tensor_gb300", "csrc")
     h = hashlib.sha256()
-    for f in [name] + sorted(x for x in os.listdir(csrc) if x.endswith(".cuh")):
+    names = list(name) if isinstance(name, tuple) else [name]
+    for f in names + sorted(x for x in os.listdir(csrc) if x.endswith(".cuh")):
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
