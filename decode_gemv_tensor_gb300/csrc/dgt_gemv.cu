@@ -246,7 +246,10 @@ __global__ void __launch_bounds__(PW * 32, 1) k_gemv(GemvArgs a) {
 // faster; R4, bound by its decode, is unchanged).  A piece is C rounds (fewer
 // at a unit's end), decoded from shared memory with no branch between its
 // rounds, so that one round's decode overlaps the previous round's
-// multiply-adds.  An R4 round whose segment holds one escape decodes with the
+// multiply-adds.  R4 pieces are 4 rounds in three stages, or 6 rounds in two
+// stages when a unit's round count is a multiple of 6 (a 3072-column row,
+// say): a short last piece costs nearly as much as a full one, so 6-round
+// units as 4 + 2 rounds ran about 15% slower.  An R4 round whose segment holds one escape decodes with the
 // rank-15 entry of the exponent table replaced by that escape's exponent
 // (only the escaped weight has nibble 15); two or three escapes do the same
 // per lane, a lane holding two of them rewriting its second escaped weight's
@@ -288,20 +291,23 @@ static_assert(TCHUNK % TNW == 0 && TCHUNK % 8 == 0, "chunk size");
 static_assert(TNW <= 32 * TPW, "one producer lane per consumer warp");
 static_assert(DGT_GEMV_C_R4 >= 1 && DGT_GEMV_C_R4 <= 13, "R4 piece rounds");
 
-template <bool R4>
-struct TmaCfg;
-template <>
-struct TmaCfg<true> {
-    static constexpr uint32_t C = DGT_GEMV_C_R4;   // rounds per piece
-    static constexpr uint32_t NS = DGT_GEMV_NS_R4; // stages per warp
-    static constexpr uint32_t STAGE = C * 768 + 64; // sm bytes, nibbles, then round summaries
+// R4 rings: pieces of DGT_GEMV_C_R4 rounds in NS_R4 stages, or (CR = 6, for
+// units whose round count is a multiple of 6: 6-round rows, and longer rows
+// split into such slices) pieces of 6 rounds in two stages of the same total
+// size, so that such a unit is whole pieces.
+template <bool R4, uint32_t CR = DGT_GEMV_C_R4>
+struct TmaCfg {
+    static constexpr uint32_t C = CR;                                   // rounds per piece
+    static constexpr uint32_t NS = CR == DGT_GEMV_C_R4 ? DGT_GEMV_NS_R4 : 2;   // stages per warp
+    static constexpr uint32_t STAGE = C * 768 + 64;   // sm bytes, nibbles, then round summaries
 };
-template <>
-struct TmaCfg<false> {
+template <uint32_t CR>
+struct TmaCfg<false, CR> {
     static constexpr uint32_t C = 2;
     static constexpr uint32_t NS = DGT_GEMV_NS_BF16;
     static constexpr uint32_t STAGE = 2 * 1024;
 };
+constexpr uint32_t GEMV_C6 = 6;   // the second R4 piece length
 
 struct UnitRange {
     uint64_t row;
@@ -320,10 +326,11 @@ __device__ __forceinline__ UnitRange unit_range(uint64_t uu, uint64_t r0, uint64
 // R4: the piece's round summaries (words x .. x + n of rsum, x = row * nseg
 // + j) travel with it, as the aligned run of 16-byte chunks that covers them
 // (at most 32 bytes); word x lands at offset 4 * (x & 3) of the summary slot.
-template <bool R4>
+template <bool R4, uint32_t CR>
 __device__ __forceinline__ void issue_piece(const GemvArgs &a, uint64_t rowf, uint64_t x, uint32_t j, uint32_t j1,
                                             uint32_t stage, uint32_t bar) {
-    const uint32_t n = min(TmaCfg<R4>::C, j1 - j);
+    constexpr uint32_t C = TmaCfg<R4, CR>::C;
+    const uint32_t n = min(C, j1 - j);
     const uint32_t k0 = j * 512;
     const uint32_t cols = min((j + n) * 512, (uint32_t)a.cols) - k0;
     const uint64_t f = rowf + k0;
@@ -333,8 +340,8 @@ __device__ __forceinline__ void issue_piece(const GemvArgs &a, uint64_t rowf, ui
         const uint32_t rb = (uint32_t)(s1 - s0) * 4;
         mbar_arrive_expect_tx(bar, cols + cols / 2 + rb);
         bulk_g2s(stage, a.sm + f, cols, bar);
-        bulk_g2s(stage + TmaCfg<R4>::C * 512, a.nib + f / 2, cols / 2, bar);
-        bulk_g2s(stage + TmaCfg<R4>::C * 768, a.rsum + s0, rb, bar);
+        bulk_g2s(stage + C * 512, a.nib + f / 2, cols / 2, bar);
+        bulk_g2s(stage + C * 768, a.rsum + s0, rb, bar);
     } else {
         mbar_arrive_expect_tx(bar, cols * 2);
         bulk_g2s(stage, a.W + f, cols * 2, bar);
@@ -360,9 +367,13 @@ __device__ __forceinline__ void cursor_set(PieceCursor &c, uint64_t uu, uint64_t
     }
 }
 
-template <bool R4>
+template <bool R4, uint32_t CR = DGT_GEMV_C_R4>
 __global__ void __launch_bounds__((TNW + TPW) * 32, 1) k_gemv_tma(GemvArgs a) {
-    constexpr uint32_t C = TmaCfg<R4>::C, TNS = TmaCfg<R4>::NS, STAGE = TmaCfg<R4>::STAGE;
+    constexpr uint32_t C = TmaCfg<R4, CR>::C, TNS = TmaCfg<R4, CR>::NS, STAGE = TmaCfg<R4, CR>::STAGE;
+    // longer pieces keep their rare paths (multi-escape set-up, general
+    // patch) as rolled loops: unrolled over 6 rounds they overflow the
+    // instruction cache on escape-rich tensors
+    constexpr bool ROLL = R4 && C > DGT_GEMV_C_R4;
     extern __shared__ __align__(128) uint8_t dsm[];
     __shared__ __align__(8) uint64_t full[TNW][TNS_MAX];
     __shared__ __align__(8) uint64_t empty[TNW][TNS_MAX];
@@ -439,7 +450,7 @@ __global__ void __launch_bounds__((TNW + TPW) * 32, 1) k_gemv_tma(GemvArgs a) {
             while (cur.uu < units && !*(volatile int *)&abort_flag) {
                 const uint32_t st = q % TNS;
                 if (q < TNS || mbar_test_wait(empty_a + 8 * st, ((q / TNS) - 1) & 1u)) {
-                    issue_piece<R4>(a, cur.rowf, cur.rowx + cur.j, cur.j, cur.j1, ring_a + st * STAGE, full_a + 8 * st);
+                    issue_piece<R4, CR>(a, cur.rowf, cur.rowx + cur.j, cur.j, cur.j1, ring_a + st * STAGE, full_a + 8 * st);
                     q++;
                     idle = 0;
                     cur.j += C;
@@ -525,24 +536,41 @@ __global__ void __launch_bounds__((TNW + TPW) * 32, 1) k_gemv_tma(GemvArgs a) {
                 if (R4 && ok && pm) {
 #pragma unroll
                     for (uint32_t r = 0; r < C; r++) mh3[r] = ml1[r] = 0, mi2[r] = 16, me2[r] = 0;
+                    // round r of the set bits of pm: its lane's values, placed by
+                    // compile-time index (a select per round when rolled)
+                    auto multi_round = [&](uint32_t r) {
+                        uint2 nv = *reinterpret_cast<const uint2 *>(stg + C * 512 + r * 256 + 8 * lane);
+                        if (r == rp && !act) nv = make_uint2(0, 0);   // bytes past K are not this row's
+                        uint32_t e, e2, i2;
+                        if (rec_exponent2(__shfl_sync(DGT_FULL, rec, r), nv, lane, e, e2, i2)) {
+                            const R4Lut t = lut15(L, e);
 #pragma unroll
-                    for (uint32_t r = 0; r < C; r++) {
-                        if ((pm >> r) & 1u) {
-                            uint2 nv = *reinterpret_cast<const uint2 *>(stg + C * 512 + r * 256 + 8 * lane);
-                            if (r == rp && !act) nv = make_uint2(0, 0);   // bytes past K are not this row's
-                            uint32_t e, e2, i2;
-                            if (rec_exponent2(__shfl_sync(DGT_FULL, rec, r), nv, lane, e, e2, i2)) {
-                                const R4Lut t = lut15(L, e);
-                                mh3[r] = t.h3;
-                                ml1[r] = t.l1;
-                                mi2[r] = i2;
-                                me2[r] = e2;
-                                pmok |= 1u << r;
-                                if (__any_sync(DGT_FULL, i2 < 16)) pm2 |= 1u << r;
-                            } else {
-                                slow = true;
+                            for (uint32_t i = 0; i < C; i++) {
+                                if (i == r) {
+                                    mh3[i] = t.h3;
+                                    ml1[i] = t.l1;
+                                    mi2[i] = i2;
+                                    me2[i] = e2;
+                                }
                             }
+                            pmok |= 1u << r;
+                            if (__any_sync(DGT_FULL, i2 < 16)) pm2 |= 1u << r;
+                        } else {
+                            slow = true;
                         }
+                    };
+                    if constexpr (ROLL) {
+                        uint32_t bits = pm;
+#pragma unroll 1
+                        while (bits) {
+                            const uint32_t r = __ffs(bits) - 1;
+                            bits &= bits - 1u;
+                            multi_round(r);
+                        }
+                    } else {
+#pragma unroll
+                        for (uint32_t r = 0; r < C; r++)
+                            if ((pm >> r) & 1u) multi_round(r);
                     }
                 }
                 // round r's weights into bf16 pairs: R4 decoded with the table
@@ -571,12 +599,13 @@ __global__ void __launch_bounds__((TNW + TPW) * 32, 1) k_gemv_tma(GemvArgs a) {
                 };
                 // a lane holding two of the round's escapes: its second escaped
                 // weight (index mi2[r]) gets exponent me2[r], without an indexed store
-                auto second_escape = [&](uint32_t r, uint32_t p[8]) {
-                    const uint32_t fm = 0x7F80u << (16 * (mi2[r] & 1u));
-                    const uint32_t fv = me2[r] * 0x00800080u;
+                // (index i2, exponent e2: mi2[r] and me2[r] of the round)
+                auto second_escape = [&](uint32_t i2, uint32_t e2, uint32_t p[8]) {
+                    const uint32_t fm = 0x7F80u << (16 * (i2 & 1u));
+                    const uint32_t fv = e2 * 0x00800080u;
 #pragma unroll
                     for (uint32_t t = 0; t < 8; t++) {
-                        const uint32_t hit = (mi2[r] >> 1) == t ? fm : 0u;
+                        const uint32_t hit = (i2 >> 1) == t ? fm : 0u;
                         p[t] = (p[t] & ~hit) | (fv & hit);
                     }
                 };
@@ -612,9 +641,7 @@ __global__ void __launch_bounds__((TNW + TPW) * 32, 1) k_gemv_tma(GemvArgs a) {
                 } else if (ok) {
                     // a round whose escapes need the general patch, a lane with two
                     // escapes, or a short BF16 piece
-#pragma unroll
-                    for (uint32_t r = 0; r < C; r++) {
-                        if (r >= n) break;
+                    auto general_round = [&](uint32_t r) {
                         uint32_t p[8];
                         const uint32_t h3 = __shfl_sync(DGT_FULL, rl.h3, r);
                         const uint32_t l1 = __shfl_sync(DGT_FULL, rl.l1, r);
@@ -628,10 +655,30 @@ __global__ void __launch_bounds__((TNW + TPW) * 32, 1) k_gemv_tma(GemvArgs a) {
                                                 r != rp || act, p);
                         } else {
                             const bool own = (pm >> r) & 1u;
-                            weights(r, own ? mh3[r] : h3, own ? ml1[r] : l1, p);
-                            if ((pm2 >> r) & 1u) second_escape(r, p);
+                            uint32_t oh3 = h3, ol1 = l1, oi2 = 16, oe2 = 0;
+#pragma unroll
+                            for (uint32_t i = 0; i < C; i++) {
+                                if (i == r && own) {
+                                    oh3 = mh3[i];
+                                    ol1 = ml1[i];
+                                    oi2 = mi2[i];
+                                    oe2 = me2[i];
+                                }
+                            }
+                            weights(r, oh3, ol1, p);
+                            if ((pm2 >> r) & 1u) second_escape(oi2, oe2, p);
                         }
                         fma_round(r, p);
+                    };
+                    if constexpr (ROLL) {
+#pragma unroll 1
+                        for (uint32_t r = 0; r < n; r++) general_round(r);
+                    } else {
+#pragma unroll
+                        for (uint32_t r = 0; r < C; r++) {
+                            if (r >= n) break;
+                            general_round(r);
+                        }
                     }
                 }
                 __syncwarp();
@@ -729,10 +776,17 @@ int launch_gemv(GemvArgs &a, int path, cudaStream_t st) {
     a.S = dgt_plan_slices(a.rows, a.cols);
     int bps = 0;
     if (path == 2) {
-        const size_t smem = (size_t)TNW * TmaCfg<R4>::NS * TmaCfg<R4>::STAGE + (size_t)a.J * 1024;
-        if (prepare_kernel((const void *)k_gemv_tma<R4>, smem, (TNW + TPW) * 32, &bps) != DGT_OK) return DGT_ERR_CUDA;
+        // R4 units whose round count is a multiple of 6 stream as 6-round pieces
+        constexpr uint32_t C6 = R4 ? GEMV_C6 : DGT_GEMV_C_R4;   // BF16 has one piece length
+        using D = TmaCfg<R4>;
+        using E = TmaCfg<R4, C6>;
+        const bool c6 = R4 && a.J % a.S == 0 && (a.J / a.S) % GEMV_C6 == 0 &&
+                        (size_t)TNW * E::NS * E::STAGE + (size_t)a.J * 1024 <= (size_t)DGT_GEMV_SMEM_KB * 1024;
+        void (*fn)(GemvArgs) = c6 ? k_gemv_tma<R4, C6> : k_gemv_tma<R4>;
+        const size_t smem = (size_t)TNW * (c6 ? E::NS * E::STAGE : D::NS * D::STAGE) + (size_t)a.J * 1024;
+        if (prepare_kernel((const void *)fn, smem, (TNW + TPW) * 32, &bps) != DGT_OK) return DGT_ERR_CUDA;
         const unsigned grid = (unsigned)min((uint64_t)di.sms, a.rows);
-        if (launch_pdl(k_gemv_tma<R4>, dim3(grid), dim3((TNW + TPW) * 32), smem, st, a) != cudaSuccess)
+        if (launch_pdl(fn, dim3(grid), dim3((TNW + TPW) * 32), smem, st, a) != cudaSuccess)
             return DGT_ERR_CUDA;
     } else if (path == 1) {
         const size_t smem = (size_t)a.J * 1024;

@@ -155,6 +155,24 @@ def test_gemv_escape_heavy_rounds(dgt, N, K):
     assert _eq32(y32[rows], r32) and np.array_equal(y16[rows], r16)
 
 
+@pytest.mark.parametrize("N,K,outl", [(8192, 3072, True), (4096, 6144, False), (8192, 2816, True)])
+def test_gemv_six_round_units(dgt, N, K, outl):
+    # units of six rounds (a 3072-column row; 6144 columns in two slices; 2816
+    # columns, the last round cut) stream as six-round pieces, whose rare
+    # paths (rounds with two or more escapes, the general patch) run as rolled
+    # loops; planted escape-heavy rounds take them.  R4 == BF16 on every row,
+    # the oracle on the planted rows and a sample
+    w = S.weights(N, K, (208, N, K, 0), outliers=outl)
+    planted = _plant_escapes(w, N + K, 300)
+    x = S.activations(K, (208, 999, N))
+    y16, y32, b16, b32 = _run_both(dgt, w, x)
+    assert _eq32(y32, b32) and np.array_equal(y16, b16)
+    g = np.random.default_rng(N + K)
+    rows = np.unique(np.concatenate([planted, [0, N - 1], g.choice(N, 64, replace=False)]))
+    r32, r16 = oracle.gemv(w, x, rows=rows)
+    assert _eq32(y32[rows], r32) and np.array_equal(y16[rows], r16)
+
+
 @pytest.mark.parametrize("model", [S.DENSE_3B, S.DENSE_12B], ids=lambda m: m["name"])
 def test_gemv_model_projections_sampled(dgt, model):
     # one layer's projections at full size: R4 == BF16 on every row, oracle on sampled rows
