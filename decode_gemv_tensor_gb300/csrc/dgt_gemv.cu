@@ -233,33 +233,34 @@ __global__ void __launch_bounds__(PW * 32, 1) k_gemv(GemvArgs a) {
 }
 
 // ---------------------------------------------------------------------------
-// Bulk-copy streaming kernel (the default when cols % 32 == 0).  One CTA per
-// SM of TNW = 18 consumer warps and TPW = 2 producer warps; CTA b owns rows
-// [b*N/G, (b+1)*N/G) and consumer warp w takes the (row, slice) units w,
-// w+18, ...  Each consumer owns a ring of NS shared-memory stages; one lane of
-// a producer warp keeps it full, issuing the 1-D bulk copies (cp.async.bulk)
-// of the next piece as soon as the consumer has released a stage (its "empty"
-// mbarrier, polled without blocking), the arrival counted on the stage's
-// "full" mbarrier.  No consumer waits on another consumer.  A bulk copy takes
-// warp-uniform operands, so a producer warp issues its lanes' copies one
-// after another: two producer warps halve that queue (BF16 streams about 7%
-// faster; R4, bound by its decode, is unchanged).  A piece is C rounds (fewer
-// at a unit's end), decoded from shared memory with no branch between its
-// rounds, so that one round's decode overlaps the previous round's
-// multiply-adds.  R4 pieces are 4 rounds in three stages, or 6 rounds in two
-// stages when a unit's round count is a multiple of 6 (a 3072-column row,
-// say): a short last piece costs nearly as much as a full one, so 6-round
-// units as 4 + 2 rounds ran about 15% slower.  An R4 round whose segment holds one escape decodes with the
-// rank-15 entry of the exponent table replaced by that escape's exponent
-// (only the escaped weight has nibble 15); two or three escapes do the same
-// per lane, a lane holding two of them rewriting its second escaped weight's
-// exponent; other cases take a general patch from the escape list.  Every
-// wait is bounded: one that runs out sets the status word, and the warp
-// stops, lets its copies in flight land and exits.
+// Bulk-copy streaming kernel (the default when cols % 32 == 0). One CTA per SM
+// of TNW = 18 consumer warps and TPW = 2 producer warps; CTA b owns rows
+// [b*N/G, (b+1)*N/G) and consumer warp w takes the (row, slice) units w, w+18,
+// ...; or (CONTIG, R4 units of one or two rounds) the w-th of 18 even
+// contiguous stretches of them, streamed as pieces that run across unit ends
+// (and across row ends when a row is whole rounds): a unit that ends inside a
+// piece leaves its sum there (fin) and the next unit's sum starts at 0, in the
+// same order as unit by unit. Each consumer owns a ring of NS shared-memory
+// stages; one lane of a producer warp keeps it full, issuing the 1-D bulk
+// copies (cp.async.bulk) of the next piece as soon as the consumer has released
+// a stage (its "empty" mbarrier, polled without blocking), the arrival counted
+// on the stage's "full" mbarrier. No consumer waits on another consumer. A bulk
+// copy takes warp-uniform operands, so a producer warp issues its lanes' copies
+// one after another: two producer warps halve that queue (BF16 streams about 7%
+// faster; R4, bound by its decode, is unchanged). A piece is C rounds (fewer at
+// a unit's end), decoded from shared memory with no branch between its rounds,
+// so that one round's decode overlaps the previous round's multiply-adds. R4
+// pieces are 4 rounds in three stages, or 6 rounds in two stages when a unit's
+// round count is a multiple of 6 (a 3072-column row, say): a short last piece
+// costs nearly as much as a full one, so 6-round units as 4 + 2 rounds ran
+// about 15% slower. An R4 round whose segment holds one escape decodes with the
+// rank-15 entry of the exponent table replaced by that escape's exponent (only
+// the escaped weight has nibble 15); two or three escapes do the same per lane,
+// a lane holding two of them rewriting its second escaped weight's exponent;
+// other cases take a general patch from the escape list. Every wait is bounded:
+// one that runs out sets the status word, and the warp stops, lets its copies
+// in flight land and exits.
 // ---------------------------------------------------------------------------
-#ifndef DGT_GEMV_INTERLEAVE
-#define DGT_GEMV_INTERLEAVE 0
-#endif
 #ifndef DGT_GEMV_TNW
 #define DGT_GEMV_TNW 18
 #endif
@@ -285,8 +286,8 @@ constexpr int TNW = DGT_GEMV_TNW;    // consumer warps per CTA
 constexpr int TPW = DGT_GEMV_TPW;    // producer warps (producer warp p serves consumers p, p + TPW, ...)
 constexpr uint32_t TNS_MAX = DGT_GEMV_NS_R4 > DGT_GEMV_NS_BF16 ? DGT_GEMV_NS_R4 : DGT_GEMV_NS_BF16;
 constexpr uint32_t TCHUNK = DGT_GEMV_TCHUNK;  // (row, slice) units per combine chunk
-// the producer requests a warp's pieces in the order uu = w, w + TNW, ...
-// across chunks, and a chunk holds whole rows for every slice count (S <= 8)
+// a chunk holds whole rows for every slice count (S <= 8); consumer warp w
+// takes the w-th of TNW even, contiguous stretches of each chunk's units
 static_assert(TCHUNK % TNW == 0 && TCHUNK % 8 == 0, "chunk size");
 static_assert(TNW <= 32 * TPW, "one producer lane per consumer warp");
 static_assert(DGT_GEMV_C_R4 >= 1 && DGT_GEMV_C_R4 <= 13, "R4 piece rounds");
@@ -309,31 +310,15 @@ struct TmaCfg<false, CR> {
 };
 constexpr uint32_t GEMV_C6 = 6;   // the second R4 piece length
 
-struct UnitRange {
-    uint64_t row;
-    uint32_t j0, j1;
-};
-
-__device__ __forceinline__ UnitRange unit_range(uint64_t uu, uint64_t r0, uint64_t rs, uint32_t log2S, uint32_t J) {
-    UnitRange u;
-    u.row = r0 + (uu >> log2S) * rs;
-    const uint32_t s = (uint32_t)uu & ((1u << log2S) - 1u);
-    u.j0 = (s * J) >> log2S;
-    u.j1 = ((s + 1) * J) >> log2S;
-    return u;
-}
-
-// R4: the piece's round summaries (words x .. x + n of rsum, x = row * nseg
-// + j) travel with it, as the aligned run of 16-byte chunks that covers them
-// (at most 32 bytes); word x lands at offset 4 * (x & 3) of the summary slot.
+// A piece: n rounds from round j of row `row` (flat weight index f = row * K
+// + 512 j), cols weights.  R4: the piece's round summaries (words x .. x + n
+// of rsum, x = row * nseg + j) travel with it, as the aligned run of 16-byte
+// chunks that covers them (at most 48 bytes); word x lands at offset
+// 4 * (x & 3) of the summary slot.
 template <bool R4, uint32_t CR>
-__device__ __forceinline__ void issue_piece(const GemvArgs &a, uint64_t rowf, uint64_t x, uint32_t j, uint32_t j1,
+__device__ __forceinline__ void issue_piece(const GemvArgs &a, uint64_t f, uint64_t x, uint32_t n, uint32_t cols,
                                             uint32_t stage, uint32_t bar) {
     constexpr uint32_t C = TmaCfg<R4, CR>::C;
-    const uint32_t n = min(C, j1 - j);
-    const uint32_t k0 = j * 512;
-    const uint32_t cols = min((j + n) * 512, (uint32_t)a.cols) - k0;
-    const uint64_t f = rowf + k0;
     fence_proxy_async_smem();
     if (R4) {
         const uint64_t s0 = x & ~3ull, s1 = (x + n + 3) & ~3ull;
@@ -348,26 +333,79 @@ __device__ __forceinline__ void issue_piece(const GemvArgs &a, uint64_t rowf, ui
     }
 }
 
-// The next piece a warp copies: unit uu (of this CTA), rounds [j, j1) of
-// the row whose first weight is at flat index rowf.
-struct PieceCursor {
-    uint64_t uu, rowf, rowx;
-    uint32_t j, j1;
-};
-
-__device__ __forceinline__ void cursor_set(PieceCursor &c, uint64_t uu, uint64_t units, uint64_t r0, uint64_t rs,
-                                           uint32_t log2S, uint32_t J, uint64_t K, uint64_t nseg) {
-    c.uu = uu;
-    if (uu < units) {
-        const UnitRange u = unit_range(uu, r0, rs, log2S, J);
-        c.rowf = u.row * K;
-        c.rowx = u.row * nseg;
-        c.j = u.j0;
-        c.j1 = u.j1;
-    }
+// First round of unit uu in its row, and its round count.
+__device__ __forceinline__ uint32_t unit_j0(uint32_t uu, uint32_t log2S, uint32_t J) {
+    return ((uu & ((1u << log2S) - 1u)) * J) >> log2S;
+}
+__device__ __forceinline__ uint32_t unit_len(uint32_t uu, uint32_t log2S, uint32_t J) {
+    const uint32_t s = uu & ((1u << log2S) - 1u);
+    return (((s + 1) * J) >> log2S) - ((s * J) >> log2S);
 }
 
-template <bool R4, uint32_t CR = DGT_GEMV_C_R4>
+// A stretch: units [ua, ub) of the CTA (row-major: a row's slices in order,
+// then the next row's), whose rounds follow one another in memory.  The
+// cursor is at round j of its row, x = row * nseg + j (the round's index in
+// the round summaries; nseg = J), f = row * K + 512 j (its first weight),
+// with left rounds to go.  x0 = r0 * J and f0 = r0 * K for the CTA's first
+// row r0.
+struct Stretch {
+    uint64_t x, f;
+    uint32_t j, left;
+};
+
+__device__ __forceinline__ Stretch stretch_start(uint32_t ua, uint32_t ub, uint64_t x0, uint64_t f0, uint32_t log2S,
+                                                 uint32_t J, uint32_t K) {
+    Stretch c;
+    const uint32_t rowl = ua >> log2S;
+    c.j = unit_j0(ua, log2S, J);
+    c.x = x0 + (rowl * J + c.j);
+    c.f = f0 + (uint64_t)rowl * K + c.j * 512;
+    c.left = ((ub >> log2S) - rowl) * J + unit_j0(ub, log2S, J) - c.j;
+    return c;
+}
+
+// The next piece's round count: C at most, and within the row unless rows
+// are whole rounds and at least C of them (then a piece may run on into the
+// next row).
+template <uint32_t C>
+__device__ __forceinline__ uint32_t piece_len(const Stretch &c, uint32_t J, bool span) {
+    return min(min(C, c.left), span ? C : J - c.j);
+}
+
+__device__ __forceinline__ void stretch_advance(Stretch &c, uint32_t n, uint32_t J) {
+    c.x += n;
+    c.j += n;
+    c.left -= n;
+    if (c.j >= J) c.j -= J;
+}
+
+// Warp w's stretches of chunk ch: with contig, the w-th of TNW even
+// contiguous shares of the chunk's units, [ua, ub) as one stretch (step =
+// ub - ua); otherwise the single units ua = c0 + w, ua + TNW, ... < ub
+// (step = TNW), each its own stretch.
+// (A CTA's units number below 2^31: its rows are at most 2^35 / G.)
+struct ChunkWalk {
+    uint32_t ua, ub, step;
+};
+__device__ __forceinline__ ChunkWalk chunk_walk(uint32_t ch, uint32_t units, uint32_t w, bool contig) {
+    const uint32_t c0 = ch * TCHUNK, nu = min(c0 + TCHUNK, units) - c0;
+    ChunkWalk k;
+    if (contig) {
+        k.ua = c0 + (w * nu) / TNW;
+        k.ub = c0 + ((w + 1) * nu) / TNW;
+        k.step = k.ub - k.ua;
+    } else {
+        k.ua = c0 + w;
+        k.ub = c0 + nu;
+        k.step = TNW;
+    }
+    return k;
+}
+__device__ __forceinline__ uint32_t stretch_end(const ChunkWalk &k, uint32_t sa, bool contig) {
+    return contig ? k.ub : sa + 1;
+}
+
+template <bool R4, uint32_t CR = DGT_GEMV_C_R4, bool CONTIG = false>
 __global__ void __launch_bounds__((TNW + TPW) * 32, 1) k_gemv_tma(GemvArgs a) {
     constexpr uint32_t C = TmaCfg<R4, CR>::C, TNS = TmaCfg<R4, CR>::NS, STAGE = TmaCfg<R4, CR>::STAGE;
     // longer pieces keep their rare paths (multi-escape set-up, general
@@ -385,14 +423,7 @@ __global__ void __launch_bounds__((TNW + TPW) * 32, 1) k_gemv_tma(GemvArgs a) {
     const uint32_t tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
     uint4 *xs = reinterpret_cast<uint4 *>(dsm + (size_t)TNW * TNS * STAGE);
     const uint64_t G = gridDim.x;
-#if DGT_GEMV_INTERLEAVE
-    // CTA b owns rows b, b + G, b + 2G, ...: the whole grid sweeps one window
-    uint64_t r0 = blockIdx.x, nrows = a.rows > r0 ? (a.rows - r0 + G - 1) / G : 0;
-    const uint64_t rs = G;
-#else
     uint64_t r0 = (uint64_t)blockIdx.x * a.rows / G, nrows = (uint64_t)(blockIdx.x + 1) * a.rows / G - r0;
-    const uint64_t rs = 1;
-#endif
     uint64_t o0 = r0;           // output index of row r0
     const uint16_t *xv = a.x;   // this CTA's x
     if (a.ids) {
@@ -421,6 +452,9 @@ __global__ void __launch_bounds__((TNW + TPW) * 32, 1) k_gemv_tma(GemvArgs a) {
     const uint64_t nchunks = (units + TCHUNK - 1) / TCHUNK;
     const uint32_t J = a.J;
     const uint32_t K = (uint32_t)a.cols;
+    // pieces may run on from one row into the next when rows are whole rounds
+    const bool span = (K & 511u) == 0 && J >= C;
+    const uint64_t x0 = r0 * J, f0 = r0 * K;   // the CTA's first row: its first round and weight
 
     for (uint32_t i = tid; i < TNW * TNS_MAX; i += blockDim.x) {
         mbar_init(smem_u32(&full[0][0]) + 8 * i, 1);
@@ -444,17 +478,60 @@ __global__ void __launch_bounds__((TNW + TPW) * 32, 1) k_gemv_tma(GemvArgs a) {
         if (c < TNW) {
             const uint32_t ring_a = smem_u32(dsm + (size_t)c * TNS * STAGE);
             const uint32_t full_a = smem_u32(&full[c][0]), empty_a = smem_u32(&empty[c][0]);
-            PieceCursor cur;
-            cursor_set(cur, c, units, r0, rs, log2S, J, a.cols, a.nseg);
+            // ring c's pieces in consumer c's order
             uint32_t q = 0, idle = 0;
-            while (cur.uu < units && !*(volatile int *)&abort_flag) {
+            uint64_t ch = 0, uu = c, rowf = 0, rowx = 0;   // CONTIG: chunk; else unit, its row's first weight and round
+            uint32_t j = 0, j1 = 0;
+            Stretch cs = {0, 0, 0, 0};
+            bool more;
+            auto next_stretch = [&]() {
+                for (; ch < nchunks; ch++) {
+                    const ChunkWalk k = chunk_walk((uint32_t)ch, (uint32_t)units, c, true);
+                    if (k.ua < k.ub) {
+                        cs = stretch_start(k.ua, k.ub, x0, f0, log2S, J, K);
+                        return true;
+                    }
+                }
+                return false;
+            };
+            auto unit_start = [&]() {
+                if (uu >= units) return false;
+                rowf = f0 + (uu >> log2S) * K;
+                rowx = x0 + (uu >> log2S) * J;
+                j = unit_j0((uint32_t)uu, log2S, J);
+                j1 = j + unit_len((uint32_t)uu, log2S, J);
+                return true;
+            };
+            if constexpr (CONTIG) more = next_stretch();
+            else more = unit_start();
+            while (more && !*(volatile int *)&abort_flag) {
                 const uint32_t st = q % TNS;
                 if (q < TNS || mbar_test_wait(empty_a + 8 * st, ((q / TNS) - 1) & 1u)) {
-                    issue_piece<R4, CR>(a, cur.rowf, cur.rowx + cur.j, cur.j, cur.j1, ring_a + st * STAGE, full_a + 8 * st);
+                    if constexpr (CONTIG) {
+                        const uint32_t n = piece_len<C>(cs, J, span);
+                        // a piece within the row stops at K (the row's last piece
+                        // ends where the next row starts); one running on into the
+                        // next row only exists when K is whole rounds
+                        const uint32_t cols = span ? n * 512 : min(n * 512, K - cs.j * 512);
+                        issue_piece<R4, CR>(a, cs.f, cs.x, n, cols, ring_a + st * STAGE, full_a + 8 * st);
+                        cs.f += cols;
+                        stretch_advance(cs, n, J);
+                        if (cs.left == 0) {
+                            ch++;
+                            more = next_stretch();
+                        }
+                    } else {
+                        const uint32_t n = min(C, j1 - j);
+                        const uint32_t cols = min(n * 512, K - j * 512);
+                        issue_piece<R4, CR>(a, rowf + j * 512, rowx + j, n, cols, ring_a + st * STAGE, full_a + 8 * st);
+                        j += n;
+                        if (j >= j1) {
+                            uu += TNW;
+                            more = unit_start();
+                        }
+                    }
                     q++;
                     idle = 0;
-                    cur.j += C;
-                    if (cur.j >= cur.j1) cursor_set(cur, cur.uu + TNW, units, r0, rs, log2S, J, a.cols, a.nseg);
                 } else if (++idle >= MBAR_SPIN_LIMIT) {
                     set_status(a.status, DGT_ERR_TIMEOUT);
                     atomicExch(&abort_flag, 1);
@@ -491,212 +568,279 @@ __global__ void __launch_bounds__((TNW + TPW) * 32, 1) k_gemv_tma(GemvArgs a) {
     const bool cut = (K & 511) != 0;
     uint32_t st = 0, phases = 0, waited = 0;
     bool ok = true;
-    for (uint64_t ch = 0; ch < nchunks; ch++) {
-        const uint64_t c0 = ch * TCHUNK, cend = min(c0 + TCHUNK, units);
-        for (uint64_t uu = c0 + w; uu < cend; uu += TNW) {
-            const UnitRange u = unit_range(uu, r0, rs, log2S, J);
-            float acc = 0.0f;
-            for (uint32_t jp = u.j0; jp < u.j1; jp += C) {
-                if (ok) {
-                    if (mbar_wait_n(full_a + 8 * st, (phases >> st) & 1u, a.spin)) {
-                        waited++;
-                    } else {
-                        ok = false;
-                        if (lane == 0) {
-                            set_status(a.status, DGT_ERR_TIMEOUT);
-                            atomicExch(&abort_flag, 1);
-                        }
-                    }
-                    if (*(volatile int *)&abort_flag) ok = false;
+    // one piece: n rounds from round jp of its row (px = row * nseg + jp in
+    // the round summaries); inner: its rounds before the last that end a unit
+    // (their sums leave through fin); rounds r >= jw belong to the next row
+    uint64_t c0 = 0;
+    uint32_t udone = 0;   // next unit to finish
+    float acc = 0.0f;
+    auto piece = [&](const uint32_t n, const uint32_t jp, const uint64_t px, const uint32_t inner, const uint32_t jw) {
+        if (ok) {
+            if (mbar_wait_n(full_a + 8 * st, (phases >> st) & 1u, a.spin)) {
+                waited++;
+            } else {
+                ok = false;
+                if (lane == 0) {
+                    set_status(a.status, DGT_ERR_TIMEOUT);
+                    atomicExch(&abort_flag, 1);
                 }
-                ok = __all_sync(DGT_FULL, ok);
-                phases ^= 1u << st;
-                const uint32_t n = min(C, u.j1 - jp);
-                const uint32_t rp = (cut && Jm1 - jp < n) ? Jm1 - jp : 0xFFFFFFFFu;
-                const uint8_t *stg = ring + st * STAGE;
-                // the piece's round summaries arrived with it: lane r < n holds
-                // round jp + r's word, and its two table words for the decode
-                uint32_t rec = 0;
-                RoundLut rl = {0, 0, 0};
-                if (R4) {
-                    const uint32_t *recs =
-                        reinterpret_cast<const uint32_t *>(stg + C * 768) + ((u.row * a.nseg + jp) & 3u);
-                    rec = lane < n ? recs[lane] : 0u;
-                    rl = round_luts_rec(rec, L);
-                }
-                const uint32_t pm = rl.multi;
-                // BF16 pieces of fewer than C rounds take the general loop
-                bool slow = !R4 && n != C;
-                // rounds with two or three escapes: per-lane rank-15 entries (and,
-                // for a lane holding two, its second escaped weight), worked out
-                // before the multiply-adds; a round where that fails takes the
-                // general patch from the escape list
-                uint32_t mh3[C], ml1[C], mi2[C], me2[C];
-                uint32_t pm2 = 0, pmok = 0;   // rounds with a second patch; rounds worked out
-                if (R4 && ok && pm) {
-#pragma unroll
-                    for (uint32_t r = 0; r < C; r++) mh3[r] = ml1[r] = 0, mi2[r] = 16, me2[r] = 0;
-                    // round r of the set bits of pm: its lane's values, placed by
-                    // compile-time index (a select per round when rolled)
-                    auto multi_round = [&](uint32_t r) {
-                        uint2 nv = *reinterpret_cast<const uint2 *>(stg + C * 512 + r * 256 + 8 * lane);
-                        if (r == rp && !act) nv = make_uint2(0, 0);   // bytes past K are not this row's
-                        uint32_t e, e2, i2;
-                        if (rec_exponent2(__shfl_sync(DGT_FULL, rec, r), nv, lane, e, e2, i2)) {
-                            const R4Lut t = lut15(L, e);
-#pragma unroll
-                            for (uint32_t i = 0; i < C; i++) {
-                                if (i == r) {
-                                    mh3[i] = t.h3;
-                                    ml1[i] = t.l1;
-                                    mi2[i] = i2;
-                                    me2[i] = e2;
-                                }
-                            }
-                            pmok |= 1u << r;
-                            if (__any_sync(DGT_FULL, i2 < 16)) pm2 |= 1u << r;
-                        } else {
-                            slow = true;
-                        }
-                    };
-                    if constexpr (ROLL) {
-                        uint32_t bits = pm;
-#pragma unroll 1
-                        while (bits) {
-                            const uint32_t r = __ffs(bits) - 1;
-                            bits &= bits - 1u;
-                            multi_round(r);
-                        }
-                    } else {
-#pragma unroll
-                        for (uint32_t r = 0; r < C; r++)
-                            if ((pm >> r) & 1u) multi_round(r);
-                    }
-                }
-                // round r's weights into bf16 pairs: R4 decoded with the table
-                // words h3, l1 (rank 15 -> an escape's exponent), or the BF16 words
-                auto weights = [&](uint32_t r, uint32_t h3, uint32_t l1, uint32_t p[8]) {
-                    if (R4) {
-                        const uint4 sv = *reinterpret_cast<const uint4 *>(stg + r * 512 + 16 * lane);
-                        const uint2 nv = *reinterpret_cast<const uint2 *>(stg + C * 512 + r * 256 + 8 * lane);
-                        R4Lut Lr = L;
-                        Lr.h3 = h3;
-                        Lr.l1 = l1;
-                        r4_dec16(nv, sv, Lr, p);
-                    } else {
-                        const uint4 lo = *reinterpret_cast<const uint4 *>(stg + r * 1024 + 32 * lane);
-                        const uint4 hi = *reinterpret_cast<const uint4 *>(stg + r * 1024 + 32 * lane + 16);
-                        p[0] = lo.x; p[1] = lo.y; p[2] = lo.z; p[3] = lo.w;
-                        p[4] = hi.x; p[5] = hi.y; p[6] = hi.z; p[7] = hi.w;
-                    }
-                };
-                // the multiply-adds of round r; in the row's last round cut by K
-                // (r == rp) a lane past K adds fma(+0, +0) = +0 instead, its
-                // weights there being the next row's
-                auto fma_round = [&](uint32_t r, const uint32_t p[8]) {
-                    const float t = fma_chunk16(p, xs, jp + r, lane, acc);
-                    acc = (r == rp && !act) ? __fadd_rn(acc, 0.0f) : t;
-                };
-                // a lane holding two of the round's escapes: its second escaped
-                // weight (index mi2[r]) gets exponent me2[r], without an indexed store
-                // (index i2, exponent e2: mi2[r] and me2[r] of the round)
-                auto second_escape = [&](uint32_t i2, uint32_t e2, uint32_t p[8]) {
-                    const uint32_t fm = 0x7F80u << (16 * (i2 & 1u));
-                    const uint32_t fv = e2 * 0x00800080u;
-#pragma unroll
-                    for (uint32_t t = 0; t < 8; t++) {
-                        const uint32_t hit = (i2 >> 1) == t ? fm : 0u;
-                        p[t] = (p[t] & ~hit) | (fv & hit);
-                    }
-                };
-                // the piece's rounds, each decoded with its own table words
-                // (multi-escape rounds with the lane's own); no branch between
-                // the rounds of a full piece, so that one round's decode overlaps
-                // the previous round's multiply-adds
-                auto table_round = [&](uint32_t r) {
-                    uint32_t p[8];
-                    const uint32_t h3 = __shfl_sync(DGT_FULL, rl.h3, r);
-                    const uint32_t l1 = __shfl_sync(DGT_FULL, rl.l1, r);
-                    const bool own = (pm >> r) & 1u;
-                    weights(r, own ? mh3[r] : h3, own ? ml1[r] : l1, p);
-                    fma_round(r, p);
-                };
-                if (ok && !slow && pm == 0 && n == C && rp >= C) {
-                    // the common piece: full, one escape at most per round, no cut
-#pragma unroll
-                    for (uint32_t r = 0; r < C; r++) {
-                        uint32_t p[8];
-                        weights(r, __shfl_sync(DGT_FULL, rl.h3, r), __shfl_sync(DGT_FULL, rl.l1, r), p);
-                        acc = fma_chunk16(p, xs, jp + r, lane, acc);
-                    }
-                } else if (ok && !slow && pm2 == 0 && n == C) {
-#pragma unroll
-                    for (uint32_t r = 0; r < C; r++) table_round(r);
-                } else if (ok && !slow && pm2 == 0) {
-#pragma unroll
-                    for (uint32_t r = 0; r < C; r++) {
-                        if (r >= n) break;
-                        table_round(r);
-                    }
-                } else if (ok) {
-                    // a round whose escapes need the general patch, a lane with two
-                    // escapes, or a short BF16 piece
-                    auto general_round = [&](uint32_t r) {
-                        uint32_t p[8];
-                        const uint32_t h3 = __shfl_sync(DGT_FULL, rl.h3, r);
-                        const uint32_t l1 = __shfl_sync(DGT_FULL, rl.l1, r);
-                        if (R4 && ((pm >> r) & 1u) && !((pmok >> r) & 1u)) {
-                            // its escape index and ranks straight from memory
-                            const uint64_t sx = u.row * a.nseg + jp + r;
-                            const uint32_t b = a.seg[sx], c = a.seg[sx + 1] - b;
-                            const uint4 sv = *reinterpret_cast<const uint4 *>(stg + r * 512 + 16 * lane);
-                            const uint2 nv = *reinterpret_cast<const uint2 *>(stg + C * 512 + r * 256 + 8 * lane);
-                            r4_round_general_cb(a, L, nv, sv, c, b, escb[R4 ? w : 0], table_s, lane,
-                                                r != rp || act, p);
-                        } else {
-                            const bool own = (pm >> r) & 1u;
-                            uint32_t oh3 = h3, ol1 = l1, oi2 = 16, oe2 = 0;
-#pragma unroll
-                            for (uint32_t i = 0; i < C; i++) {
-                                if (i == r && own) {
-                                    oh3 = mh3[i];
-                                    ol1 = ml1[i];
-                                    oi2 = mi2[i];
-                                    oe2 = me2[i];
-                                }
-                            }
-                            weights(r, oh3, ol1, p);
-                            if ((pm2 >> r) & 1u) second_escape(oi2, oe2, p);
-                        }
-                        fma_round(r, p);
-                    };
-                    if constexpr (ROLL) {
-#pragma unroll 1
-                        for (uint32_t r = 0; r < n; r++) general_round(r);
-                    } else {
-#pragma unroll
-                        for (uint32_t r = 0; r < C; r++) {
-                            if (r >= n) break;
-                            general_round(r);
-                        }
-                    }
-                }
-                __syncwarp();
-                // a stage is released only after a good wait: after a timeout the
-                // producer stops, and the copies in flight are waited for below
-                if (ok && lane == 0) mbar_arrive(empty_a + 8 * st);
-                st = st + 1 == TNS ? 0 : st + 1;
             }
+            if (*(volatile int *)&abort_flag) ok = false;
+        }
+        ok = __all_sync(DGT_FULL, ok);
+        phases ^= 1u << st;
+        const uint32_t rp = (cut && Jm1 - jp < n) ? Jm1 - jp : 0xFFFFFFFFu;
+        const uint8_t *stg = ring + st * STAGE;
+        // the piece's round summaries arrived with it: lane r < n holds
+        // round jp + r's word, and its two table words for the decode
+        uint32_t rec = 0;
+        RoundLut rl = {0, 0, 0};
+        if (R4) {
+            const uint32_t *recs =
+                reinterpret_cast<const uint32_t *>(stg + C * 768) + (px & 3u);
+            rec = lane < n ? recs[lane] : 0u;
+            rl = round_luts_rec(rec, L);
+        }
+        const uint32_t pm = rl.multi;
+        // BF16 pieces of fewer than C rounds take the general loop
+        bool slow = !R4 && n != C;
+        // rounds with two or three escapes: per-lane rank-15 entries (and,
+        // for a lane holding two, its second escaped weight), worked out
+        // before the multiply-adds; a round where that fails takes the
+        // general patch from the escape list
+        uint32_t mh3[C], ml1[C], mi2[C], me2[C];
+        uint32_t pm2 = 0, pmok = 0;   // rounds with a second patch; rounds worked out
+        if (R4 && ok && pm) {
 #pragma unroll
-            for (int d = 16; d >= 1; d >>= 1) acc += __shfl_xor_sync(DGT_FULL, acc, d);
-            if (lane == 0) part[uu - c0] = acc;
+            for (uint32_t r = 0; r < C; r++) mh3[r] = ml1[r] = 0, mi2[r] = 16, me2[r] = 0;
+            // round r of the set bits of pm: its lane's values, placed by
+            // compile-time index (a select per round when rolled)
+            auto multi_round = [&](uint32_t r) {
+                uint2 nv = *reinterpret_cast<const uint2 *>(stg + C * 512 + r * 256 + 8 * lane);
+                if (r == rp && !act) nv = make_uint2(0, 0);   // bytes past K are not this row's
+                uint32_t e, e2, i2;
+                if (rec_exponent2(__shfl_sync(DGT_FULL, rec, r), nv, lane, e, e2, i2)) {
+                    const R4Lut t = lut15(L, e);
+#pragma unroll
+                    for (uint32_t i = 0; i < C; i++) {
+                        if (i == r) {
+                            mh3[i] = t.h3;
+                            ml1[i] = t.l1;
+                            mi2[i] = i2;
+                            me2[i] = e2;
+                        }
+                    }
+                    pmok |= 1u << r;
+                    if (__any_sync(DGT_FULL, i2 < 16)) pm2 |= 1u << r;
+                } else {
+                    slow = true;
+                }
+            };
+            if constexpr (ROLL) {
+                uint32_t bits = pm;
+#pragma unroll 1
+                while (bits) {
+                    const uint32_t r = __ffs(bits) - 1;
+                    bits &= bits - 1u;
+                    multi_round(r);
+                }
+            } else {
+#pragma unroll
+                for (uint32_t r = 0; r < C; r++)
+                    if ((pm >> r) & 1u) multi_round(r);
+            }
+        }
+        // round r's weights into bf16 pairs: R4 decoded with the table
+        // words h3, l1 (rank 15 -> an escape's exponent), or the BF16 words
+        auto weights = [&](uint32_t r, uint32_t h3, uint32_t l1, uint32_t p[8]) {
+            if (R4) {
+                const uint4 sv = *reinterpret_cast<const uint4 *>(stg + r * 512 + 16 * lane);
+                const uint2 nv = *reinterpret_cast<const uint2 *>(stg + C * 512 + r * 256 + 8 * lane);
+                R4Lut Lr = L;
+                Lr.h3 = h3;
+                Lr.l1 = l1;
+                r4_dec16(nv, sv, Lr, p);
+            } else {
+                const uint4 lo = *reinterpret_cast<const uint4 *>(stg + r * 1024 + 32 * lane);
+                const uint4 hi = *reinterpret_cast<const uint4 *>(stg + r * 1024 + 32 * lane + 16);
+                p[0] = lo.x; p[1] = lo.y; p[2] = lo.z; p[3] = lo.w;
+                p[4] = hi.x; p[5] = hi.y; p[6] = hi.z; p[7] = hi.w;
+            }
+        };
+        // the multiply-adds of round r (x round jp + r, or jp + r - J past
+        // the row's end); in the row's last round cut by K (r == rp) a
+        // lane past K adds fma(+0, +0) = +0 instead, its weights there
+        // being the next row's.  fin[r] keeps the sum after round r; a
+        // round that ends a unit starts the next unit's sum at 0
+        float fin[C];
+        auto fma_round = [&](uint32_t r, const uint32_t p[8]) {
+            const uint32_t jx = jp + r - (r >= jw ? J : 0u);
+            float t = fma_chunk16(p, xs, jx, lane, acc);
+            t = (r == rp && !act) ? __fadd_rn(acc, 0.0f) : t;
+            if constexpr (CONTIG) {
+#pragma unroll
+                for (uint32_t i = 0; i < C; i++)
+                    if (i == r) fin[i] = t;
+            }
+            acc = ((inner >> r) & 1u) ? 0.0f : t;
+        };
+        // a lane holding two of the round's escapes: its second escaped
+        // weight (index mi2[r]) gets exponent me2[r], without an indexed store
+        // (index i2, exponent e2: mi2[r] and me2[r] of the round)
+        auto second_escape = [&](uint32_t i2, uint32_t e2, uint32_t p[8]) {
+            const uint32_t fm = 0x7F80u << (16 * (i2 & 1u));
+            const uint32_t fv = e2 * 0x00800080u;
+#pragma unroll
+            for (uint32_t t = 0; t < 8; t++) {
+                const uint32_t hit = (i2 >> 1) == t ? fm : 0u;
+                p[t] = (p[t] & ~hit) | (fv & hit);
+            }
+        };
+        // the piece's rounds, each decoded with its own table words
+        // (multi-escape rounds with the lane's own); no branch between
+        // the rounds of a full piece, so that one round's decode overlaps
+        // the previous round's multiply-adds
+        auto table_round = [&](uint32_t r) {
+            uint32_t p[8];
+            const uint32_t h3 = __shfl_sync(DGT_FULL, rl.h3, r);
+            const uint32_t l1 = __shfl_sync(DGT_FULL, rl.l1, r);
+            const bool own = (pm >> r) & 1u;
+            weights(r, own ? mh3[r] : h3, own ? ml1[r] : l1, p);
+            fma_round(r, p);
+        };
+        if (ok && !slow && pm == 0 && n == C && rp >= C && jw >= C && inner == 0) {
+            // the common piece: full, one escape at most per round, no cut,
+            // within one row and one unit (which may end at its last round)
+#pragma unroll
+            for (uint32_t r = 0; r < C; r++) {
+                uint32_t p[8];
+                weights(r, __shfl_sync(DGT_FULL, rl.h3, r), __shfl_sync(DGT_FULL, rl.l1, r), p);
+                acc = fma_chunk16(p, xs, jp + r, lane, acc);
+            }
+        } else if (ok && !slow && pm2 == 0 && n == C) {
+#pragma unroll
+            for (uint32_t r = 0; r < C; r++) table_round(r);
+        } else if (ok && !slow && pm2 == 0) {
+#pragma unroll
+            for (uint32_t r = 0; r < C; r++) {
+                if (r >= n) break;
+                table_round(r);
+            }
+        } else if (ok) {
+            // a round whose escapes need the general patch, a lane with two
+            // escapes, or a short BF16 piece
+            auto general_round = [&](uint32_t r) {
+                uint32_t p[8];
+                const uint32_t h3 = __shfl_sync(DGT_FULL, rl.h3, r);
+                const uint32_t l1 = __shfl_sync(DGT_FULL, rl.l1, r);
+                if (R4 && ((pm >> r) & 1u) && !((pmok >> r) & 1u)) {
+                    // its escape index and ranks straight from memory
+                    const uint64_t sx = px + r;
+                    const uint32_t b = a.seg[sx], c = a.seg[sx + 1] - b;
+                    const uint4 sv = *reinterpret_cast<const uint4 *>(stg + r * 512 + 16 * lane);
+                    const uint2 nv = *reinterpret_cast<const uint2 *>(stg + C * 512 + r * 256 + 8 * lane);
+                    r4_round_general_cb(a, L, nv, sv, c, b, escb[R4 ? w : 0], table_s, lane,
+                                        r != rp || act, p);
+                } else {
+                    const bool own = (pm >> r) & 1u;
+                    uint32_t oh3 = h3, ol1 = l1, oi2 = 16, oe2 = 0;
+#pragma unroll
+                    for (uint32_t i = 0; i < C; i++) {
+                        if (i == r && own) {
+                            oh3 = mh3[i];
+                            ol1 = ml1[i];
+                            oi2 = mi2[i];
+                            oe2 = me2[i];
+                        }
+                    }
+                    weights(r, oh3, ol1, p);
+                    if ((pm2 >> r) & 1u) second_escape(oi2, oe2, p);
+                }
+                fma_round(r, p);
+            };
+            if constexpr (ROLL) {
+#pragma unroll 1
+                for (uint32_t r = 0; r < n; r++) general_round(r);
+            } else {
+#pragma unroll
+                for (uint32_t r = 0; r < C; r++) {
+                    if (r >= n) break;
+                    general_round(r);
+                }
+            }
+        }
+        __syncwarp();
+        // a stage is released only after a good wait: after a timeout the
+        // producer stops, and the copies in flight are waited for below
+        if (ok && lane == 0) mbar_arrive(empty_a + 8 * st);
+        st = st + 1 == TNS ? 0 : st + 1;
+        // the units that ended in this piece, in order: before its last
+        // round (fin), then at it (acc)
+        if (inner) {
+#pragma unroll
+            for (uint32_t r = 0; r + 1 < C; r++) {
+                if ((inner >> r) & 1u) {
+                    float v = fin[r];
+#pragma unroll
+                    for (int d = 16; d >= 1; d >>= 1) v += __shfl_xor_sync(DGT_FULL, v, d);
+                    if (lane == 0) part[udone - c0] = v;
+                    udone++;
+                }
+            }
+        }
+    };
+    for (uint64_t ch = 0; ch < nchunks; ch++) {
+        c0 = ch * TCHUNK;
+        const uint64_t cend = min(c0 + TCHUNK, units);
+        if constexpr (CONTIG) {
+            // this warp's stretch of the chunk, walked piece by piece; a piece
+            // may hold the ends of several units
+            const ChunkWalk k = chunk_walk((uint32_t)ch, (uint32_t)units, w, true);
+            if (k.ua < k.ub) {
+                Stretch cs = stretch_start(k.ua, k.ub, x0, f0, log2S, J, K);
+                udone = k.ua;
+                uint32_t unext = k.ua + 1;                   // the unit after the current one
+                uint32_t uleft = unit_len(k.ua, log2S, J);   // rounds of the current unit not yet taken
+                acc = 0.0f;
+                while (cs.left) {
+                    const uint32_t n = piece_len<C>(cs, J, span);
+                    // the piece's rounds that end a unit (bit r: round r)
+                    uint32_t emask = 0, r = 0;
+                    while (uleft <= n - r) {
+                        r += uleft;
+                        emask |= 1u << (r - 1);
+                        uleft = unit_len(unext++, log2S, J);
+                    }
+                    uleft -= n - r;
+                    piece(n, cs.j, cs.x, emask & ((1u << (n - 1)) - 1u), J - cs.j);
+                    if (emask >> (n - 1)) {
+#pragma unroll
+                        for (int d = 16; d >= 1; d >>= 1) acc += __shfl_xor_sync(DGT_FULL, acc, d);
+                        if (lane == 0) part[udone - c0] = acc;
+                        udone++;
+                        acc = 0.0f;
+                    }
+                    stretch_advance(cs, n, J);
+                }
+            }
+        } else {
+            // units w, w + TNW, ...: each its own pieces
+            for (uint64_t uu = c0 + w; uu < cend; uu += TNW) {
+                const uint32_t j0 = unit_j0((uint32_t)uu, log2S, J), j1 = j0 + unit_len((uint32_t)uu, log2S, J);
+                const uint64_t xr = x0 + (uu >> log2S) * J;
+                acc = 0.0f;
+                for (uint32_t jp = j0; jp < j1; jp += C) piece(min(C, j1 - jp), jp, xr + jp, 0u, 0xFFFFFFFFu);
+#pragma unroll
+                for (int d = 16; d >= 1; d >>= 1) acc += __shfl_xor_sync(DGT_FULL, acc, d);
+                if (lane == 0) part[uu - c0] = acc;
+            }
         }
         asm volatile("bar.sync 1, %0;" ::"r"(TNW * 32) : "memory");
         const uint32_t S = 1u << log2S;
         for (uint32_t t = tid; t < (cend - c0) / S; t += TNW * 32) {
             float y = part[t * S];
             for (uint32_t s = 1; s < S; s++) y = y + part[t * S + s];
-            const uint64_t orow = o0 + (c0 / S + t) * rs;
+            const uint64_t orow = o0 + c0 / S + t;
             if (a.y32) a.y32[orow] = y;
             if (a.y) a.y[orow] = f32_to_bf16_rne(y);
         }
@@ -782,7 +926,12 @@ int launch_gemv(GemvArgs &a, int path, cudaStream_t st) {
         using E = TmaCfg<R4, C6>;
         const bool c6 = R4 && a.J % a.S == 0 && (a.J / a.S) % GEMV_C6 == 0 &&
                         (size_t)TNW * E::NS * E::STAGE + (size_t)a.J * 1024 <= (size_t)DGT_GEMV_SMEM_KB * 1024;
-        void (*fn)(GemvArgs) = c6 ? k_gemv_tma<R4, C6> : k_gemv_tma<R4>;
+        // R4 units of one or two rounds (fewer than two on average): each warp
+        // streams a contiguous stretch of them, pieces running across their
+        // ends.  (At two rounds each, 3840 x 4096, the stretches ran faster
+        // back to back but slower inside a decode step.)
+        const bool contig = R4 && a.J < 2u * (uint32_t)a.S;
+        void (*fn)(GemvArgs) = c6 ? k_gemv_tma<R4, C6> : contig ? k_gemv_tma<R4, DGT_GEMV_C_R4, R4> : k_gemv_tma<R4>;
         const size_t smem = (size_t)TNW * (c6 ? E::NS * E::STAGE : D::NS * D::STAGE) + (size_t)a.J * 1024;
         if (prepare_kernel((const void *)fn, smem, (TNW + TPW) * 32, &bps) != DGT_OK) return DGT_ERR_CUDA;
         const unsigned grid = (unsigned)min((uint64_t)di.sms, a.rows);
@@ -905,10 +1054,11 @@ static int launch_expert_blocks(GemvArgs &a, cudaStream_t st) {
     if (a.cols % 32 || smem > (size_t)DGT_GEMV_SMEM_KB * 1024 || pairs > (uint64_t)di.sms)
         return DGT_ERR_UNSUPPORTED;
     a.S = dgt_plan_slices(a.ne, a.cols);
+    void (*fn)(GemvArgs) = R4 && a.J < 2u * (uint32_t)a.S ? k_gemv_tma<R4, DGT_GEMV_C_R4, R4> : k_gemv_tma<R4>;
     int bps = 0;
-    if (prepare_kernel((const void *)k_gemv_tma<R4>, smem, (TNW + TPW) * 32, &bps) != DGT_OK) return DGT_ERR_CUDA;
+    if (prepare_kernel((const void *)fn, smem, (TNW + TPW) * 32, &bps) != DGT_OK) return DGT_ERR_CUDA;
     const unsigned grid = (unsigned)min((uint64_t)di.sms, pairs * a.ne);
-    if (launch_pdl(k_gemv_tma<R4>, dim3(grid), dim3((TNW + TPW) * 32), smem, st, a) != cudaSuccess)
+    if (launch_pdl(fn, dim3(grid), dim3((TNW + TPW) * 32), smem, st, a) != cudaSuccess)
         return DGT_ERR_CUDA;
     return cudaPeekAtLastError() == cudaSuccess ? DGT_OK : DGT_ERR_CUDA;
 }
