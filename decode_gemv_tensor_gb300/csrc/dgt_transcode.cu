@@ -18,6 +18,7 @@
 //  - every group checks its index against its neighbours and its decoded
 //    length against its index bytes; a mismatch sets the status word.
 #include <cuda_runtime.h>
+#include <type_traits>
 
 #include "../../include/dgt.h"
 #include "dgt_device.cuh"
@@ -281,15 +282,18 @@ struct RiceMeta {
     uint32_t q;            // this lane's block index byte
 };
 
-__device__ __forceinline__ RiceMeta rice_meta(const F2Args &a, uint64_t g, uint32_t lane) {
+template <class IX>
+__device__ __forceinline__ RiceMeta rice_meta(const F2Args &a, IX g, uint32_t lane) {
     RiceMeta m = {0, 0, 0, 0, 0};
-    if (g < a.ngrp) {
-        m.w0 = a.grp[2 * g];
-        m.base = a.grp[2 * g + 1];
-        m.nextw = g + 1 < a.ngrp ? a.grp[2 * g + 2] : (uint32_t)a.n_words;
-        m.nexte = g + 1 < a.ngrp ? a.grp[2 * g + 3] : (uint32_t)a.n_esc;
-        const uint64_t blk = g * DGT_GROUP + lane;
-        m.q = blk < a.nblk ? a.blkq[blk] : 0u;
+    const IX ngrp = (IX)a.ngrp;
+    if (g < ngrp) {
+        const uint32_t *gp = a.grp + 2 * (uint64_t)g;
+        m.w0 = gp[0];
+        m.base = gp[1];
+        m.nextw = g + 1 < ngrp ? gp[2] : (uint32_t)a.n_words;
+        m.nexte = g + 1 < ngrp ? gp[3] : (uint32_t)a.n_esc;
+        const IX blk = g * DGT_GROUP + lane;
+        m.q = blk < (IX)a.nblk ? a.blkq[blk] : 0u;
     }
     return m;
 }
@@ -298,15 +302,17 @@ __device__ __forceinline__ RiceMeta rice_meta(const F2Args &a, uint64_t g, uint3
 // its first word (the stream then starts 32 * (w0 % 4) bits into dst); bytes
 // past the stream array's end, and past the buffer's need, are zero-filled.
 // The stream array must start on a 16-byte boundary.
-__device__ __forceinline__ void rice_stage16(const F2Args &a, uint64_t g, const RiceMeta &m, uint32_t *dst,
+template <class IX>
+__device__ __forceinline__ void rice_stage16(const F2Args &a, IX g, const RiceMeta &m, uint32_t *dst,
                                              uint32_t lane) {
-    if (g < a.ngrp) {
+    if (g < (IX)a.ngrp) {
         const uint32_t a0 = m.w0 & ~3u;
         const uint32_t need = m.nextw > a0 ? min(m.nextw - a0, (uint32_t)RBUF) : 0u;
+        const uint32_t nw = (uint32_t)a.n_words;   // < 2^32 on this path
         for (uint32_t i = lane; i < RBUF / 4; i += 32) {
             const uint32_t wi = a0 + 4 * i;
             uint32_t bytes = 0;
-            if (4 * i < need && wi < a.n_words) bytes = min(16u, (uint32_t)(a.n_words - wi) * 4u);
+            if (4 * i < need && wi < nw) bytes = min(16u, (nw - wi) * 4u);
             cp_async16(dst + 4 * i, bytes ? a.words + wi : a.words, bytes);
         }
     }
@@ -371,10 +377,13 @@ __global__ void __launch_bounds__(RW * 32, 1) k_rice_to_r4(F2Args a) {
         }
     }
     // row / column of the group's first rank, stepped with the grid stride
-    const uint64_t g0 = (uint64_t)blockIdx.x * RW + w, G = (uint64_t)gridDim.x * RW;
-    const uint64_t GS = (uint64_t)DGT_GROUP * DGT_BLOCK;
-    uint64_t r0 = (g0 * GS) / a.cols, c0 = (g0 * GS) % a.cols;
-    const uint64_t step_r = (G * GS) / a.cols, step_c = (G * GS) % a.cols;
+    // (32-bit indices on the FAST path: n < 2^31)
+    using IX = typename std::conditional<FAST, uint32_t, uint64_t>::type;
+    const IX g0 = (IX)blockIdx.x * RW + w, G = (IX)gridDim.x * RW;
+    const IX GS = (IX)DGT_GROUP * DGT_BLOCK;
+    const IX cols = (IX)a.cols;
+    IX r0 = (IX)(((uint64_t)g0 * GS) / cols), c0 = (IX)(((uint64_t)g0 * GS) % cols);
+    const IX step_r = (IX)(((uint64_t)G * GS) / cols), step_c = (IX)(((uint64_t)G * GS) % cols);
     // index entries: group g in m0, g + G in m1 (its stream is copied while g
     // decodes), g + 2G loaded during g
     RiceMeta m0 = rice_meta(a, g0, lane);
@@ -383,13 +392,14 @@ __global__ void __launch_bounds__(RW * 32, 1) k_rice_to_r4(F2Args a) {
     else rice_stage4(a, g0, m0, S.buf[0][w], lane);
     const uint32_t nfull = (uint32_t)(a.n / DGT_BLOCK), nblk32 = (uint32_t)a.nblk;
     uint32_t cur = 0;
-    for (uint64_t g = g0; g < a.ngrp; g += G, cur ^= 1) {
+    const IX ngrp = (IX)a.ngrp;
+    for (IX g = g0; g < ngrp; g += G, cur ^= 1) {
         const uint32_t *buf = S.buf[cur][w];
         if (FAST) rice_stage16(a, g + G, m1, S.buf[cur ^ 1][w], lane);
         else rice_stage4(a, g + G, m1, S.buf[cur ^ 1][w], lane);
         const RiceMeta m2 = rice_meta(a, g + 2 * G, lane);
-        const uint64_t blk = g * DGT_GROUP + lane;
-        const uint64_t B0 = blk * DGT_BLOCK;
+        const IX blk = g * DGT_GROUP + lane;
+        const uint64_t B0 = (uint64_t)blk * DGT_BLOCK;
         uint32_t cnt;
         if (FAST) {
             const uint32_t b32 = (uint32_t)g * DGT_GROUP + lane;
@@ -409,7 +419,7 @@ __global__ void __launch_bounds__(RW * 32, 1) k_rice_to_r4(F2Args a) {
         m0 = m1;
         m1 = m2;
         // this lane's block: row and column of its first rank
-        uint64_t br = r0, bc = c0 + (uint64_t)DGT_BLOCK * lane;
+        uint64_t br = r0, bc = c0 + (IX)DGT_BLOCK * lane;
         if (FAST) {
             uint32_t bc32 = (uint32_t)c0 + DGT_BLOCK * lane, br32 = (uint32_t)r0;
             if (bc32 >= (uint32_t)a.cols) {
@@ -429,8 +439,8 @@ __global__ void __launch_bounds__(RW * 32, 1) k_rice_to_r4(F2Args a) {
         }
         c0 += step_c;
         r0 += step_r;
-        if (c0 >= a.cols) {
-            c0 -= a.cols;
+        if (c0 >= cols) {
+            c0 -= cols;
             r0++;
         }
         cp_async_wait1();
