@@ -708,14 +708,17 @@ __global__ void __launch_bounds__((TNW + TPW) * 32, 1) k_gemv_tma(GemvArgs a) {
             weights(r, own ? mh3[r] : h3, own ? ml1[r] : l1, p);
             fma_round(r, p);
         };
-        if (ok && !slow && pm == 0 && n == C && rp >= C && jw >= C && inner == 0) {
-            // the common piece: full, one escape at most per round, no cut,
-            // within one row and one unit (which may end at its last round)
+        if (ok && !slow && pm == 0 && n == C && rp >= C - 1 && jw >= C && inner == 0) {
+            // the common piece: full, one escape at most per round, within one
+            // row and one unit (which may end at its last round); a cut row's
+            // last round may be its last (rp == C - 1)
+            const bool cutl = rp == C - 1 && !act;
 #pragma unroll
             for (uint32_t r = 0; r < C; r++) {
                 uint32_t p[8];
                 weights(r, __shfl_sync(DGT_FULL, rl.h3, r), __shfl_sync(DGT_FULL, rl.l1, r), p);
-                acc = fma_chunk16(p, xs, jp + r, lane, acc);
+                const float t = fma_chunk16(p, xs, jp + r, lane, acc);
+                acc = (r == C - 1 && cutl) ? __fadd_rn(acc, 0.0f) : t;
             }
         } else if (ok && !slow && pm2 == 0 && n == C) {
 #pragma unroll
