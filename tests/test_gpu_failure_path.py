@@ -37,9 +37,10 @@ def _u32(t):
     return t.cpu().numpy().view(np.uint32)
 
 
-@pytest.mark.parametrize("N,K", [(1024, 1024), (8192, 3072)])
+@pytest.mark.parametrize("N,K", [(1024, 1024), (8192, 3072), (3072, 3072)])
 def test_gemv_wait_runs_out_then_recovers(dgt, N, K):
-    # 8192 x 3072: units of six rounds, the six-round-piece rings (two stages)
+    # 8192 x 3072: units of six rounds, the six-round-piece rings (two stages);
+    # 3072 x 3072: units of one or two rounds, walked as contiguous stretches
     w = S.weights(N, K, (701, 0, 0, 0), outliers=True)
     x = S.activations(K, (701, 999, 0))
     r32, _ = oracle.gemv(w, x)

@@ -173,6 +173,25 @@ def test_gemv_six_round_units(dgt, N, K, outl):
     assert _eq32(y32[rows], r32) and np.array_equal(y16[rows], r16)
 
 
+@pytest.mark.parametrize("N,K,outl", [(3072, 3072, True), (2816, 2816, True), (2048, 1024, False), (1024, 4096, True)])
+def test_gemv_short_unit_stretches(dgt, N, K, outl):
+    # units of one or two rounds (slice plans 2 to 8): each warp streams a
+    # contiguous stretch of them, pieces running across unit ends (3072 and
+    # 4096 columns: across row ends too; 2816: the last round cut, pieces stop
+    # at the row's end; 1024: rows of two rounds).  Planted escape-heavy
+    # rounds take the per-round paths inside such pieces.  R4 == BF16 on
+    # every row, the oracle on the planted rows and a sample
+    w = S.weights(N, K, (209, N, K, 0), outliers=outl)
+    planted = _plant_escapes(w, N * 7 + K, 200)
+    x = S.activations(K, (209, 999, N))
+    y16, y32, b16, b32 = _run_both(dgt, w, x)
+    assert _eq32(y32, b32) and np.array_equal(y16, b16)
+    g = np.random.default_rng(N * 7 + K)
+    rows = np.unique(np.concatenate([planted, [0, N - 1], g.choice(N, 64, replace=False)]))
+    r32, r16 = oracle.gemv(w, x, rows=rows)
+    assert _eq32(y32[rows], r32) and np.array_equal(y16[rows], r16)
+
+
 @pytest.mark.parametrize("model", [S.DENSE_3B, S.DENSE_12B], ids=lambda m: m["name"])
 def test_gemv_model_projections_sampled(dgt, model):
     # one layer's projections at full size: R4 == BF16 on every row, oracle on sampled rows
