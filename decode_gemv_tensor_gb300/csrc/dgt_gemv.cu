@@ -379,30 +379,18 @@ __device__ __forceinline__ void stretch_advance(Stretch &c, uint32_t n, uint32_t
     if (c.j >= J) c.j -= J;
 }
 
-// Warp w's stretches of chunk ch: with contig, the w-th of TNW even
-// contiguous shares of the chunk's units, [ua, ub) as one stretch (step =
-// ub - ua); otherwise the single units ua = c0 + w, ua + TNW, ... < ub
-// (step = TNW), each its own stretch.
-// (A CTA's units number below 2^31: its rows are at most 2^35 / G.)
+// Warp w's stretch of chunk ch (CONTIG): the w-th of TNW even contiguous
+// shares of the chunk's units, [ua, ub).  (A CTA's units number below 2^31:
+// its rows are at most 2^35 / G.)
 struct ChunkWalk {
-    uint32_t ua, ub, step;
+    uint32_t ua, ub;
 };
-__device__ __forceinline__ ChunkWalk chunk_walk(uint32_t ch, uint32_t units, uint32_t w, bool contig) {
+__device__ __forceinline__ ChunkWalk chunk_walk(uint32_t ch, uint32_t units, uint32_t w) {
     const uint32_t c0 = ch * TCHUNK, nu = min(c0 + TCHUNK, units) - c0;
     ChunkWalk k;
-    if (contig) {
-        k.ua = c0 + (w * nu) / TNW;
-        k.ub = c0 + ((w + 1) * nu) / TNW;
-        k.step = k.ub - k.ua;
-    } else {
-        k.ua = c0 + w;
-        k.ub = c0 + nu;
-        k.step = TNW;
-    }
+    k.ua = c0 + (w * nu) / TNW;
+    k.ub = c0 + ((w + 1) * nu) / TNW;
     return k;
-}
-__device__ __forceinline__ uint32_t stretch_end(const ChunkWalk &k, uint32_t sa, bool contig) {
-    return contig ? k.ub : sa + 1;
 }
 
 template <bool R4, uint32_t CR = DGT_GEMV_C_R4, bool CONTIG = false>
@@ -486,7 +474,7 @@ __global__ void __launch_bounds__((TNW + TPW) * 32, 1) k_gemv_tma(GemvArgs a) {
             bool more;
             auto next_stretch = [&]() {
                 for (; ch < nchunks; ch++) {
-                    const ChunkWalk k = chunk_walk((uint32_t)ch, (uint32_t)units, c, true);
+                    const ChunkWalk k = chunk_walk((uint32_t)ch, (uint32_t)units, c);
                     if (k.ua < k.ub) {
                         cs = stretch_start(k.ua, k.ub, x0, f0, log2S, J, K);
                         return true;
@@ -798,7 +786,7 @@ __global__ void __launch_bounds__((TNW + TPW) * 32, 1) k_gemv_tma(GemvArgs a) {
         if constexpr (CONTIG) {
             // this warp's stretch of the chunk, walked piece by piece; a piece
             // may hold the ends of several units
-            const ChunkWalk k = chunk_walk((uint32_t)ch, (uint32_t)units, w, true);
+            const ChunkWalk k = chunk_walk((uint32_t)ch, (uint32_t)units, w);
             if (k.ua < k.ub) {
                 Stretch cs = stretch_start(k.ua, k.ub, x0, f0, log2S, J, K);
                 udone = k.ua;
