@@ -126,16 +126,59 @@ def algo_bytes(p2_arrays, p1_arrays, n, n_esc, rows, cols):
 # clocks sampled during the timed region
 # ---------------------------------------------------------------------------
 class Clocks:
+    """SM clock and clock-event reasons sampled while the timed region runs.
+
+    Reads NVML (the driver's libnvidia-ml) from a background thread every
+    5 ms, so even a short timed region gets several samples; falls back to
+    `nvidia-smi -lms 200` when NVML cannot be opened.  Read-only: no setting
+    of the GPU is changed."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    # NVML clock-event reason bits (nvml.h)
+    BITS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20,
+            "hw_thermal_slowdown": 0x40, "hw_power_brake_slowdown": 0x80}
 
     def __init__(self, device_index):
         self.dev = device_index
         self.proc = None
         self.path = os.path.join("/tmp", f"dgt_clocks_{os.getpid()}.csv")
+        self.nvml = None
+        self.thread = None
+        try:
+            import ctypes as C
+            import torch
+            lib = C.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                raise OSError("nvmlInit")
+            h = C.c_void_p()
+            uuid = "GPU-" + str(torch.cuda.get_device_properties(device_index).uuid)
+            if lib.nvmlDeviceGetHandleByUUID(C.c_char_p(uuid.encode()), C.byref(h)) != 0:
+                raise OSError("no NVML handle for " + uuid)
+            reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                lib.nvmlDeviceGetCurrentClocksThrottleReasons
+            self.C, self.nvml, self.h, self.reasons_fn = C, lib, h, reasons
+        except Exception:
+            self.nvml = None
+
+    def _sample_nvml(self):
+        C = self.C
+        v, mx, r = C.c_uint(), C.c_uint(), C.c_ulonglong()
+        self.nvml.nvmlDeviceGetMaxClockInfo(self.h, 1, C.byref(mx))   # NVML_CLOCK_SM
+        self.max_mhz = float(mx.value)
+        while not self.done:
+            if self.nvml.nvmlDeviceGetClockInfo(self.h, 1, C.byref(v)) == 0 and \
+                    self.reasons_fn(self.h, C.byref(r)) == 0:
+                self.rows.append((float(v.value), int(r.value)))
+            time.sleep(0.005)
 
     def start(self):
+        if self.nvml is not None:
+            import threading
+            self.rows, self.done, self.max_mhz = [], False, 0.0
+            self.thread = threading.Thread(target=self._sample_nvml, daemon=True)
+            self.thread.start()
+            return
         try:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.Q}",
@@ -145,6 +188,14 @@ class Clocks:
             self.proc = None
 
     def stop(self):
+        if self.thread is not None:
+            self.done = True
+            self.thread.join(timeout=5)
+            if not self.rows:
+                return None
+            reasons = sorted(nm for nm, bit in self.BITS.items() if any(r & bit for _, r in self.rows))
+            return {"sm_mhz": statistics.median(c for c, _ in self.rows), "sm_max_mhz": self.max_mhz,
+                    "reasons": reasons, "samples": len(self.rows), "source": "nvml, every 5 ms"}
         if not self.proc:
             return None
         self.proc.terminate()
@@ -170,7 +221,7 @@ class Clocks:
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "source": "nvidia-smi -lms 200"}
 
 
 # ---------------------------------------------------------------------------
