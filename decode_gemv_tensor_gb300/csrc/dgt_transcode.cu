@@ -250,19 +250,6 @@ __device__ __noinline__ void rice_block_slow_escapes(Rd rd, uint32_t b0, uint32_
     }
 }
 
-// A unary run of 32 or more zeros at bit p of the staged buffer.
-struct LongRun {
-    uint32_t q, p, bad;
-};
-__device__ __noinline__ LongRun rice_long_run(const uint32_t *buf, uint32_t p) {
-    bool bad = false;
-    LongRun o;
-    o.q = unary_at(WordReader<const uint32_t *>{buf, RBUF}, p, bad);
-    o.p = p;
-    o.bad = bad;
-    return o;
-}
-
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 __device__ __forceinline__ void cp_async16(uint32_t *dst, const uint32_t *src, uint32_t bytes) {
