@@ -233,7 +233,8 @@ __global__ void __launch_bounds__(1024) k_moe_route(MoeArgs a) {
 // (active[] order, expert by expert) are split over one CTA per SM by cost;
 // consumer warp w of a CTA takes its rows w, w + MNW, ...  A producer warp
 // keeps each consumer's ring of stages full with 1-D bulk copies of pieces of
-// MC rounds (polling the rings' "empty" barriers without blocking).  For each
+// MCV rounds (R4: 6 in two stages, BF16: 4 in two stages; polling the rings'
+// "empty" barriers without blocking).  For each
 // row a warp decodes every 16-weight lane chunk once and runs one fmaf chain
 // per routed token (up to MAXT per pass over the row; more tokens stream the
 // row again), x read through L1.  At every slice end the chains are
@@ -247,15 +248,16 @@ __global__ void __launch_bounds__(1024) k_moe_route(MoeArgs a) {
 #endif
 constexpr int MNW = DGT_MOE_MNW;  // consumer warps
 constexpr int MPW = DGT_MOE_MPW;  // producer warps (producer warp p serves consumers p, p + MPW, ...)
-constexpr uint32_t MC = 4;       // rounds per piece
-constexpr uint32_t MNS_MAX = 3;  // stages per consumer (R4: 3, BF16: 2)
+template <bool R4>
+constexpr uint32_t MCV = R4 ? 6u : 4u;   // rounds per piece (R4: a 2816-column expert row in one piece)
+constexpr uint32_t MNS_MAX = 2;  // stages per consumer
 constexpr uint32_t XS_BYTES = 64 * 1024;   // x of the CTA's tokens staged in shared memory
 constexpr uint32_t XS_TOKENS = 1024;       // token bitmap / slot map size
 
 template <bool R4>
 struct MoeStage {
-    static constexpr uint32_t BYTES = R4 ? MC * 768 + 64 : MC * 1024;   // R4: sm, nibbles, round summaries
-    static constexpr uint32_t NS = R4 ? 3 : 2;
+    static constexpr uint32_t BYTES = R4 ? MCV<R4> * 768 + 64 : MCV<R4> * 1024;   // R4: sm, nibbles, round summaries
+    static constexpr uint32_t NS = 2;
 };
 
 // Row gi of the active rows: the expert's flat row and its routed pairs.
@@ -346,7 +348,7 @@ __device__ __forceinline__ void moe_cursor_load(const MoeArgs &a, const MoeTable
 
 template <bool R4>
 __device__ __forceinline__ void moe_issue(const MoeArgs &a, uint64_t grow, uint32_t j, uint32_t stage, uint32_t bar) {
-    const uint32_t n = min(MC, a.J - j);
+    const uint32_t n = min(MCV<R4>, a.J - j);
     const uint32_t k0 = j * 512;
     const uint32_t cols = min((j + n) * 512, (uint32_t)a.cols) - k0;
     const uint64_t f = grow * a.cols + k0;
@@ -358,8 +360,8 @@ __device__ __forceinline__ void moe_issue(const MoeArgs &a, uint64_t grow, uint3
         const uint32_t rb = (uint32_t)(s1 - s0) * 4;
         mbar_arrive_expect_tx(bar, cols + cols / 2 + rb);
         bulk_g2s(stage, a.sm + f, cols, bar);
-        bulk_g2s(stage + MC * 512, a.nib + f / 2, cols / 2, bar);
-        bulk_g2s(stage + MC * 768, a.rsum + s0, rb, bar);
+        bulk_g2s(stage + MCV<R4> * 512, a.nib + f / 2, cols / 2, bar);
+        bulk_g2s(stage + MCV<R4> * 768, a.rsum + s0, rb, bar);
     } else {
         mbar_arrive_expect_tx(bar, cols * 2);
         bulk_g2s(stage, a.W + f, cols * 2, bar);
@@ -425,7 +427,7 @@ __device__ __forceinline__ void moe_row_pass(const MoeArgs &a, MoeRing &rg, cons
 #pragma unroll
     for (int t = 0; t < NT; t++) acc[t] = 0.0f;
     uint32_t s = 0, send = J >> log2S, jbase = 0;
-    for (uint32_t jp = 0; jp < J; jp += MC) {
+    for (uint32_t jp = 0; jp < J; jp += MCV<R4>) {
         if (rg.ok && BK) {
             if (mbar_wait_n(rg.full_a + 8 * rg.st, (rg.phases >> rg.st) & 1u, a.spin)) {
                 rg.waited++;
@@ -440,7 +442,7 @@ __device__ __forceinline__ void moe_row_pass(const MoeArgs &a, MoeRing &rg, cons
         }
         rg.ok = __all_sync(DGT_FULL, rg.ok);
         rg.phases ^= 1u << rg.st;
-        const uint32_t n = min(MC, J - jp);
+        const uint32_t n = min(MCV<R4>, J - jp);
         const uint8_t *stg = rg.ring + rg.st * STAGE;
         // escape tables of the piece's rounds: from the round summaries that
         // came with the piece (bulk), else from the row's seg window
@@ -449,7 +451,7 @@ __device__ __forceinline__ void moe_row_pass(const MoeArgs &a, MoeRing &rg, cons
         if (R4) {
             if (BK) {
                 const uint32_t *recs =
-                    reinterpret_cast<const uint32_t *>(stg + MC * 768) + ((m.grow * a.nseg + jp) & 3u);
+                    reinterpret_cast<const uint32_t *>(stg + MCV<R4> * 768) + ((m.grow * a.nseg + jp) & 3u);
                 rec = lane < n ? recs[lane] : 0u;
                 prl = round_luts_rec(rec, L);
                 wb = jp;
@@ -467,7 +469,7 @@ __device__ __forceinline__ void moe_row_pass(const MoeArgs &a, MoeRing &rg, cons
 #pragma unroll
         for (int t = 0; t < NT; t++) xp[t] = xr[t] + 64 * jp;
 #pragma unroll
-        for (uint32_t r = 0; r < MC; r++) {
+        for (uint32_t r = 0; r < MCV<R4>; r++) {
             if (r >= n) break;
             const uint32_t j = jp + r;
             const bool act = j != Jm1 || act_last;
@@ -477,7 +479,7 @@ __device__ __forceinline__ void moe_row_pass(const MoeArgs &a, MoeRing &rg, cons
                 uint2 nv;
                 if (BK) {
                     sv = *reinterpret_cast<const uint4 *>(stg + r * 512 + 16 * lane);
-                    nv = *reinterpret_cast<const uint2 *>(stg + MC * 512 + r * 256 + 8 * lane);
+                    nv = *reinterpret_cast<const uint2 *>(stg + MCV<R4> * 512 + r * 256 + 8 * lane);
                 } else {
                     // rows whose nibbles are not 16-byte aligned: direct loads
                     const uint64_t f = m.grow * a.cols + 512 * j + 16 * lane;
@@ -659,7 +661,7 @@ __global__ void __launch_bounds__((MNW + MPW) * 32, 1) k_moe(MoeArgs a) {
                     moe_issue<R4>(a, cur.grow, cur.j, ring_a + st * STAGE, full_a + 8 * st);
                     q++;
                     idle = 0;
-                    cur.j += MC;
+                    cur.j += MCV<R4>;
                     if (cur.j >= J) {
                         cur.j = 0;
                         if (++cur.pass >= cur.npass) {
